@@ -1,0 +1,461 @@
+"""Throughput of the gated full-attention layer step on GB300.
+
+One "step" is one layer step (q/k/v dequant projections with the norm / rotary
+/ append epilogue, causal GQA attention with the gate, o_proj) over one batch
+of synthetic input.  Default workload: the 4B-class decode layer (hidden 2560,
+16/4 heads, head_dim 256, rotary 64, 8-bit group-64 weights, one sequence, one
+new row, cache length 4096).
+
+Device timing: a CUDA graph of consecutive steps cycling over enough distinct
+layer instances (weights + caches) that their bytes exceed 4x the L2 cache, so
+every step streams from HBM; CUDA events on the launching stream.  A second
+pass records per-kernel events (no programmatic overlap) for the roofline of
+the dominant kernel.  e2e: the same steps through the C ABI with the input
+copied from pinned host memory and the output read back every step.
+
+--impl reference times the float64 CPU oracle (the reference arm) on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from qwen3_gated_attention_gb300 import synth  # noqa: E402
+
+METRIC = "gated-attn layer steps/s & tokens/s; achieved HBM GB/s vs GB300 peak"
+UNIT = "layer-steps/s"
+
+
+def algorithmic_bytes(spec):
+    """Per-step and per-kernel algorithmic bytes (packed weights + bf16
+    scales/biases, KV read over every attended position, KV rows written, x,
+    out and the small intermediates each kernel must move)."""
+    H, Hk, d, Hd, B, R = (spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.hidden,
+                          spec.batch, spec.q_len)
+    M = B * R
+
+    def wbytes(N, K, bits, group):
+        return N * K * bits // 8 + N * (K // group) * 4
+
+    wq = wbytes(spec.n_q, Hd, spec.bits[0], spec.group[0])
+    wk = wbytes(spec.n_kv, Hd, spec.bits[1], spec.group[1])
+    wv = wbytes(spec.n_kv, Hd, spec.bits[2], spec.group[2])
+    wo = wbytes(Hd, H * d, spec.bits[3], spec.group[3])
+    pos = spec.positions().astype(np.int64)
+    kv_read = int(((pos + R) * Hk * d * 2 * 2).sum())
+    kv_write = M * Hk * d * 2 * 2
+    xb = M * Hd * (4 if spec.x_dtype == "f32" else 2)
+    outb = M * Hd * 2
+    x16 = M * Hd * 2
+    qn = M * H * d * 2
+    gate = M * H * d * 4
+    o16 = M * H * d * 2
+    per_kernel = {
+        "xprep": xb + x16,
+        "proj_qkv": wq + wk + wv + x16 + qn + gate + kv_write,
+        "attn": kv_read + qn + gate + o16,
+        "proj_o": wo + o16 + outb,
+    }
+    step = wq + wk + wv + wo + kv_read + kv_write + xb + outb
+    return step, per_kernel
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "qwen3_gated_attention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    src_hash, traffic = None, None
+    with open(path) as f:
+        for line in f:
+            if line.startswith("sources:"):
+                src_hash = line.split(":", 1)[1].strip()
+            if line.startswith("traffic_bytes_per_launch:"):
+                traffic = float(line.split(":", 1)[1].strip())
+    if src_hash != kernel_source_hash():
+        return None
+    return traffic
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gattn_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------- cpu baseline
+
+def oracle_sample(spec, budget_s=15.0, max_steps=64):
+    """Time the oracle as it stands on a bounded sample of the workload: whole
+    layer steps of the same shapes, one core."""
+    import oracle as orc
+    wf = synth.weights_f32(spec)
+    op = [orc.quantize_affine(w.astype(np.float64), spec.bits[i], spec.group[i])
+          for i, w in enumerate(wf)]
+    qn, kn = synth.norm_weights_bf16(spec)
+    W = orc.OracleWeights([p for p, _, _ in op], [s for _, s, _ in op], [b for _, _, b in op],
+                          qn, kn, list(spec.bits), list(spec.group))
+    cap = spec.capacity()
+    ck, cv = synth.cache(spec, cap)
+    x = synth.x_values(spec, synth.layer_input(spec))
+    pos = spec.positions()
+    steps = 0
+    t0 = time.perf_counter()
+    while steps < max_steps:
+        k2, v2 = ck.copy(), cv.copy()
+        ts = time.perf_counter()
+        orc.layer_step(spec, W, x, k2, v2, pos)
+        steps += 1
+        if time.perf_counter() - t0 + (time.perf_counter() - ts) > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return steps / el, steps, el
+
+
+def reference_arm(args, spec):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    K, W = args.steps, max(args.warmup, 0)
+    budget = min(120.0, max(10.0, 2.0 * (K + W)))
+    rate, n, el = oracle_sample(spec, budget_s=budget, max_steps=max(1, K + W))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": 1000.0 / rate,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(spec, args),
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{n} whole layer steps of {spec.name} in {el:.1f} s"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(spec, args, extra=None):
+    d = {"workload": spec.name, "hidden": spec.hidden, "num_heads": spec.num_heads,
+         "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+         "rotary_dim": int(spec.head_dim * spec.partial_rotary_factor),
+         "bits": list(spec.bits), "group": list(spec.group), "batch": spec.batch,
+         "q_len": spec.q_len, "cache_len": int(spec.positions().max()) + spec.q_len,
+         "head_chunk": not args.no_head_chunk, "parallelism": f"replicas x{args.gpus}"}
+    if extra:
+        d.update(extra)
+    return d
+
+
+# ------------------------------------------------------------------ ours
+
+def our_arm(args, spec):
+    import torch
+    import torch.distributed as dist
+
+    from qwen3_gated_attention_gb300 import build as libbuild
+    from qwen3_gated_attention_gb300 import gattn
+    from qwen3_gated_attention_gb300.device import DeviceLayer, x_to_device
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    # CPU baseline first (rank 0, N = 1): the oracle as it stands, before any GPU work
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n, el = oracle_sample(spec, budget_s=args.cpu_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} whole layer steps of {spec.name} ({el:.1f} s, one core)"}
+
+    if rank == 0:
+        libbuild.build()
+    if world > 1:
+        dist.init_process_group("nccl")
+        dist.barrier()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
+
+    step_bytes, kernel_bytes = algorithmic_bytes(spec)
+    inst_bytes = step_bytes
+    n_inst = max(2, math.ceil(4 * l2 / inst_bytes))
+    if args.instances:
+        n_inst = args.instances
+
+    # one instance's inputs on the host, replicated across instances on the device
+    wf = synth.weights_f32(spec)
+    packed = [gattn.pack_affine_host(w, spec.bits[i], spec.group[i]) for i, w in enumerate(wf)]
+    del wf
+    qn, kn = synth.norm_weights_bf16(spec)
+    cap = spec.capacity()
+    ck, cv = synth.cache(spec, cap)
+    pos = spec.positions()
+    x = synth.layer_input(spec)
+    layers = []
+    for _ in range(n_inst):
+        dl = DeviceLayer(spec, packed, qn, kn, cap, head_chunk=not args.no_head_chunk,
+                         device=dev)
+        dl._w = None          # interchange copies are no longer needed after repacking
+        dl.load_cache(ck, cv)
+        layers.append(dl)
+    del ck, cv
+    xd = x_to_device(spec, x, dev)
+    pd = torch.from_numpy(pos).to(dev)
+    outs = [torch.empty((spec.batch, spec.q_len, spec.hidden), dtype=torch.bfloat16, device=dev)
+            for _ in range(n_inst)]
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+
+    def enqueue(i):
+        dl = layers[i % n_inst]
+        gattn.layer_step(dl.h, xd.data_ptr(), dl.kv, pd.data_ptr(), spec.batch, spec.q_len,
+                         outs[i % n_inst].data_ptr(), sh)
+
+    # eager warm-up (also checks status), then graphs
+    with torch.cuda.stream(stream):
+        for i in range(n_inst):
+            enqueue(i)
+    stream.synchronize()
+    for dl in layers:
+        gattn.layer_poll_status(dl.h, sh)
+    launches = gattn.layer_launches_per_step(layers[0].h)
+
+    K = args.steps
+    W = max(args.warmup, 3)
+    gsize = min(K, args.graph_steps)
+    gsize = max(1, (gsize // n_inst) * n_inst) if gsize >= n_inst else gsize
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            g.capture_begin()
+            for i in range(n):
+                enqueue(i)
+            g.capture_end()
+        return g
+
+    graph = capture(gsize)
+    rem = K % gsize
+    graph_rem = capture(rem) if rem else None
+    reps = K // gsize
+
+    # warm-up: W steps
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(W / gsize))):
+            graph.replay()
+    stream.synchronize()
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        if graph_rem is not None:
+            graph_rem.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        dist.barrier()
+    steps_per_s = world * K / (elapsed_ms / 1e3)
+    for dl in layers:
+        gattn.layer_poll_status(dl.h, sh)
+
+    # per-kernel pass: events between the step's kernels (programmatic overlap off)
+    names = ["xprep", "proj_qkv", "attn", "proj_o"]
+    nper = min(K, max(n_inst, 4 * n_inst))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(nper)]
+    per_kernel_ms = {n: [] for n in names}
+    with torch.cuda.stream(stream):
+        for row in evs:
+            for e in row:
+                e.record(stream)          # creates the underlying cudaEvent_t
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(nper):
+            dl = layers[i % n_inst]
+            gattn.layer_set_events(dl.h, [e.cuda_event for e in evs[i]])
+            enqueue(i)
+            gattn.layer_set_events(dl.h, [])
+    stream.synchronize()
+    for i in range(nper):
+        for j, n in enumerate(names):
+            per_kernel_ms[n].append(evs[i][j].elapsed_time(evs[i][j + 1]))
+    kernel_avg_ms = {n: statistics.mean(v) for n, v in per_kernel_ms.items()}
+    dominant = max(kernel_bytes, key=lambda n: kernel_bytes[n])
+    peak, peak_kind = load_peaks()
+    achieved = kernel_bytes[dominant] / (kernel_avg_ms[dominant] / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(dominant, spec.name),
+                "kernel": dominant, "peak_source": peak_kind,
+                "kernel_avg_us": {n: 1e3 * v for n, v in kernel_avg_ms.items()},
+                "kernel_bytes": kernel_bytes}
+
+    # e2e through the C ABI with pinned host buffers, copies inside the timed region
+    xh = torch.from_numpy(np.ascontiguousarray(xd.cpu().view(torch.int16).numpy())).pin_memory() \
+        if spec.x_dtype != "f32" else xd.cpu().pin_memory()
+    ph = torch.from_numpy(pos.copy()).pin_memory()
+    oh = torch.empty(outs[0].shape, dtype=torch.bfloat16).pin_memory()
+    xdev = torch.empty_like(xd)
+    pdev = torch.empty_like(pd)
+    n_e2e = min(K, args.e2e_steps)
+    h2d = xh.numel() * xh.element_size() + ph.numel() * ph.element_size()
+    d2h = oh.numel() * oh.element_size()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n_e2e):
+            dl = layers[i % n_inst]
+            xdev.view(torch.int16 if spec.x_dtype != "f32" else torch.float32).copy_(
+                xh, non_blocking=True)
+            pdev.copy_(ph, non_blocking=True)
+            gattn.layer_step(dl.h, xdev.data_ptr(), dl.kv, pdev.data_ptr(), spec.batch, spec.q_len,
+                             outs[i % n_inst].data_ptr(), sh)
+            oh.copy_(outs[i % n_inst], non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_rate = world * n_e2e / (e2e_ms / 1e3)
+
+    tokens_per_step = spec.batch * spec.q_len
+    line = {
+        "metric": METRIC, "value": steps_per_s, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(spec, args, {
+            "l2": f"rotating {n_inst} layer instances, {n_inst * inst_bytes / 2**20:.0f} MiB "
+                  f"> 4x L2 ({l2 / 2**20:.0f} MiB)",
+            "arith": "bf16/fp16 tensor-core operands, fp32 accumulate; 8/4/6/3-bit codes"}),
+        "tokens_per_s": steps_per_s * tokens_per_step,
+        "hbm_gbs": steps_per_s / world * step_bytes / 1e9,
+        "hbm_frac_of_peak": steps_per_s / world * step_bytes / 1e9 / peak,
+        "bytes_per_step": step_bytes,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_rate, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": n_e2e},
+        "gpu_launches": launches * K,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for dl in layers:
+        dl.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60000)
+    ap.add_argument("--warmup", type=int, default=600)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_4b", choices=list(synth.WORKLOADS))
+    ap.add_argument("--instances", type=int, default=0)
+    ap.add_argument("--graph-steps", type=int, default=600)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-head-chunk", action="store_true")
+    args = ap.parse_args()
+    spec = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, spec)
+    else:
+        our_arm(args, spec)
+
+
+if __name__ == "__main__":
+    main()

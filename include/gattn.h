@@ -1,0 +1,245 @@
+/*
+ * gattn.h -- C ABI of the GB300 (sm_103a) gated full-attention layer library.
+ *
+ * One thing runs here: the Qwen3.5-family full-attention decoder layer at
+ * decode and speculative-verify time, for B sequences of R new rows each
+ * (R = q_len, 1..4 is the target range):
+ *
+ *   q_full = Wq x  (doubled q_proj: per head h the rows [h*2d, h*2d+d) are the
+ *                   query and [h*2d+d, (h+1)*2d) the output gate)
+ *   k = Wk x,  v = Wv x
+ *   q = RoPE(RMSNorm(query, q_norm)),  k = RoPE(RMSNorm(k, k_norm))
+ *   cache[cache_pos + r] = bf16(k), bf16(v)
+ *   attn = causal GQA softmax(q k^T / sqrt(d)) v over t <= cache_pos + r
+ *   out = Wo (attn * sigmoid(gate))
+ *
+ * Sources: "feat(engine): stage D6 - qwen3_5 dense full-attn deltas" (Summary:
+ * doubled q_proj -> split queries/gate -> o_proj(attn * sigmoid(gate)); Audit
+ * table: partial_rotary_factor, has_qk_norm); Atlas "spark_model/forward/
+ * qwen3_5/mod.rs" (Qwen35ForwardConfig, q_total = num_heads*head_dim*2,
+ * LayerKvCache: caller pre-allocates, KV-append at cache_pos, attention over
+ * cache_pos+1); DS4Server issue 113 "Reproduction and boundary" (the verify
+ * head-chunk plan); TensorFold issue 503 "Option C" (generic affine row decoder,
+ * 2-8 bit, groups 32/64/128).
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked (device) are CUDA device addresses, (host) host memory.
+ *   - Weights, caches, x, out and cache_pos are BORROWED: the library never
+ *     frees them.  The library OWNS its handles, its repacked weights, its
+ *     scratch and its TMA descriptors (freed by the matching destroy call).
+ *   - A status other than GATTN_OK leaves a message for gattn_last_error()
+ *     (thread-local, valid until the next call on the same thread).
+ *   - Streams are cudaStream_t values passed as gattn_stream (0 = legacy default).
+ *   - Inadmissible configurations are rejected at create time, never silently
+ *     at step time.
+ */
+#ifndef GATTN_H
+#define GATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gattn_stream; /* same type as cudaStream_t */
+
+typedef enum gattn_status {
+    GATTN_OK = 0,
+    GATTN_E_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer */
+    GATTN_E_UNSUPPORTED = 2,   /* admissible on the pages but not built here */
+    GATTN_E_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    GATTN_E_DEVICE_RANGE = 4,  /* a kernel saw cache_pos + q_len > capacity */
+    GATTN_E_STATE = 5,         /* call out of order (e.g. step before set_weights) */
+    GATTN_E_DEVICE_TIMEOUT = 6 /* a bounded device wait gave up (kernel returned early) */
+} gattn_status;
+
+enum { GATTN_DTYPE_F32 = 0, GATTN_DTYPE_BF16 = 1 };
+enum { GATTN_PROJ_Q = 0, GATTN_PROJ_K = 1, GATTN_PROJ_V = 2, GATTN_PROJ_O = 3 };
+
+/*
+ * Layer configuration (mirrors the config fields of Qwen35ForwardConfig).
+ *   hidden                 Hd, width of x and out
+ *   num_heads, num_kv_heads H, Hk (H % Hk == 0, gqa = H / Hk; query head h uses KV head h / gqa)
+ *   head_dim               d; d % 64 == 0 and d <= 256 on this build
+ *   partial_rotary_factor  prf in (0, 1]; rotary dims rd = trunc(d * prf), even and >= 2
+ *   rope_theta             base of inv_freq_i = theta^(-2i/rd)
+ *   rms_eps                QK-RMSNorm epsilon (inside the square root)
+ *   bits, group_size       default code width {2,3,4,5,6,8} and group {32,64,128}
+ *   proj_bits[4], proj_group[4]  per projection q,k,v,o; 0 = the default
+ *   x_dtype                GATTN_DTYPE_F32 or GATTN_DTYPE_BF16 (out is always bf16)
+ *   max_batch, max_q_len   upper bounds for step(); max_batch*max_q_len <= 32
+ *   head_chunk             1 = the verify head-chunk plan is on (the pages'
+ *                          default), 0 = off; both routes give the same result
+ */
+typedef struct gattn_cfg {
+    int32_t hidden;
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    float partial_rotary_factor;
+    float rope_theta;
+    float rms_eps;
+    int32_t bits;
+    int32_t group_size;
+    int32_t proj_bits[4];
+    int32_t proj_group[4];
+    int32_t x_dtype;
+    int32_t max_batch;
+    int32_t max_q_len;
+    int32_t head_chunk;
+} gattn_cfg;
+
+/*
+ * Packed affine weights of one projection in the interchange layout, all (device):
+ *   packed  uint32 [N][K*bits/32]: row n is an LSB-first bitstream, code k at
+ *           bits [k*bits, (k+1)*bits) of the row's little-endian words
+ *   scales  bf16   [N][K/group]
+ *   biases  bf16   [N][K/group]      weight = scale * code + bias
+ * N x K: q = (2*H*d) x Hd, k = v = (Hk*d) x Hd, o = Hd x (H*d).
+ */
+typedef struct gattn_proj {
+    const uint32_t *packed;
+    const uint16_t *scales;
+    const uint16_t *biases;
+} gattn_proj;
+
+typedef struct gattn_weights {
+    gattn_proj proj[4];        /* q, k, v, o */
+    const uint16_t *q_norm;    /* bf16 [d] (device) */
+    const uint16_t *k_norm;    /* bf16 [d] (device) */
+} gattn_weights;
+
+/*
+ * A caller-owned bf16 KV cache (device), element (b, kv_head, token, j) of K at
+ *   k + b*stride_batch + kv_head*stride_head + token*stride_token + j
+ * and the same for V (same strides).  Strides are in elements; each must be a
+ * multiple of 8 (16 bytes) and the base pointers 16-byte aligned.
+ * [B][Hk][cap][d] is stride_token = d, stride_head = cap*d, stride_batch = Hk*cap*d;
+ * the token-major [B][cap][Hk*d] layout is stride_token = Hk*d, stride_head = d.
+ */
+typedef struct gattn_kv_desc {
+    void *k;
+    void *v;
+    int32_t batch;       /* sequences held */
+    int32_t capacity;    /* tokens per sequence */
+    int64_t stride_token;
+    int64_t stride_head;
+    int64_t stride_batch;
+} gattn_kv_desc;
+
+/* Intermediate taps of the last step (device, fp32), each may be NULL:
+ *   y     [B*R][2*H*d + 2*Hk*d]  projection outputs q_full | k | v before the norm
+ *   attn  [B*R][H*d]             attention output before the gate */
+typedef struct gattn_taps {
+    float *y;
+    float *attn;
+} gattn_taps;
+
+typedef struct gattn_layer gattn_layer;
+typedef struct gattn_kv gattn_kv;
+
+/* Validate a configuration without touching a GPU.  Same rules as create(). */
+gattn_status gattn_cfg_validate(const gattn_cfg *cfg);
+
+/* Rotary dims the layer uses: trunc(head_dim * partial_rotary_factor), computed
+ * in double ("rope dims" of the qwen3_5 deltas page); -1 if cfg is NULL. */
+int32_t gattn_rotary_dims(const gattn_cfg *cfg);
+
+/* Create a layer on the current CUDA device: validates cfg, allocates scratch
+ * (sized by max_batch/max_q_len) and the repacked-weight buffers.  *out owned
+ * by the caller, release with gattn_layer_destroy. */
+gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out);
+
+/* Repack the interchange weights into the library's device tile layout (same
+ * bytes per step).  Runs and synchronizes on `stream`; the caller may free the
+ * interchange buffers after it returns. */
+gattn_status gattn_layer_set_weights(gattn_layer *layer, const gattn_weights *w, gattn_stream stream);
+
+/* Register a cache for this layer: checks sizes/alignment and encodes the TMA
+ * tensor maps once.  The cache memory must outlive the registration. */
+gattn_status gattn_kv_register(gattn_layer *layer, const gattn_kv_desc *desc, gattn_kv **out);
+
+/*
+ * One layer step, enqueued on `stream` with no host synchronization and no
+ * allocation (capturable into a CUDA graph).
+ *   x          (device) [batch][q_len][hidden], cfg.x_dtype
+ *   kv         registered cache holding sequences 0..batch-1
+ *   cache_pos  (device) int32 [batch]: first new position of each sequence;
+ *              the new rows go to cache_pos[b] .. cache_pos[b]+q_len-1 and
+ *              row r attends positions 0 .. cache_pos[b]+r
+ *   out        (device) bf16 [batch][q_len][hidden]
+ * A sequence with cache_pos < 0 or cache_pos + q_len > capacity is skipped on
+ * the device (its cache is untouched and its out rows are zero) and the next
+ * gattn_layer_poll_status() returns GATTN_E_DEVICE_RANGE.  One step at a time
+ * per layer handle: steps of one handle on different streams race on its scratch.
+ */
+gattn_status gattn_layer_step(gattn_layer *layer, const void *x, gattn_kv *kv,
+                              const int32_t *cache_pos, int32_t batch, int32_t q_len,
+                              void *out, gattn_stream stream);
+
+/* Synchronize `stream`, then read and clear the layer's device status word:
+ * GATTN_OK, GATTN_E_DEVICE_RANGE or GATTN_E_DEVICE_TIMEOUT. */
+gattn_status gattn_layer_poll_status(gattn_layer *layer, gattn_stream stream);
+
+/* Ask the next steps to also write the taps (NULL or all-NULL turns them off). */
+gattn_status gattn_layer_set_taps(gattn_layer *layer, const gattn_taps *taps);
+
+void gattn_layer_destroy(gattn_layer *layer);
+void gattn_kv_destroy(gattn_kv *kv);
+
+/* Thread-local message of the last failed call on this thread ("" if none). */
+const char *gattn_last_error(void);
+
+/*
+ * Host quantizer + packer for synthetic weights (host): per (row, group)
+ *   bias = bf16(min w), scale = bf16((max w - min w)/(2^bits - 1)),
+ *   code = clamp(nearest-even((w - bias)/scale), 0, 2^bits - 1), code = 0 if scale == 0,
+ * all arithmetic in double with ties-to-even bf16 rounding, written into the
+ * interchange layout above.  w float [N][K]; packed [N][K*bits/32];
+ * scales/biases [N][K/group].  Requires K % group == 0 and K*bits % 32 == 0.
+ */
+gattn_status gattn_pack_affine_host(const float *w, int64_t N, int64_t K, int32_t bits,
+                                    int32_t group, uint32_t *packed, uint16_t *scales,
+                                    uint16_t *biases);
+
+/* Decode interchange codes on the GPU (device in/out): codes uint8 [N][K]. */
+gattn_status gattn_unpack_codes_device(const uint32_t *packed, int64_t N, int64_t K, int32_t bits,
+                                       uint8_t *codes, gattn_stream stream);
+
+/* Dequantize one projection of a layer FROM ITS REPACKED DEVICE LAYOUT with the
+ * same register unpack the projection kernels use: w (device) float [N][K],
+ * w = fp32(scale*code + bias) (exact: scale*code has <= 16 significant bits). */
+gattn_status gattn_layer_dequant_device(gattn_layer *layer, int32_t proj, float *w,
+                                        gattn_stream stream);
+
+/*
+ * The verify head-chunk plan (DS4Server issue 113, "Reproduction and boundary"):
+ * when enabled and q_len*gqa > 32 and q_len <= 32, the query heads of each KV
+ * group are split into chunks of max(1, min(gqa, 32/q_len)) heads (the last
+ * chunk of a group holds the remainder), in head order; otherwise each KV
+ * group is one chunk.  Writes up to `cap` chunks (first head, head count) and
+ * returns the chunk count, or -1 for bad arguments.
+ */
+int32_t gattn_head_chunk_plan(int32_t q_len, int32_t num_heads, int32_t num_kv_heads,
+                              int32_t enabled, int32_t *chunk_first_head, int32_t *chunk_len,
+                              int32_t cap);
+
+/* Per-step launch report of the layer's last step: number of kernel launches
+ * it enqueued (all of them this library's own kernels). */
+int32_t gattn_layer_launches_per_step(const gattn_layer *layer);
+
+/* Instrumentation: with n == launches_per_step + 1 cudaEvent_t handles, each
+ * following step records events[i] on its stream right before its i-th kernel
+ * launch and events[n-1] after the last one, so per-kernel durations can be
+ * read with cudaEventElapsedTime.  n == 0 (or events == NULL) turns it off.
+ * The events are borrowed.  Recording between kernels serializes them (no
+ * programmatic overlap), so use it for per-kernel timing passes only. */
+gattn_status gattn_layer_set_events(gattn_layer *layer, void *const *events, int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GATTN_H */

@@ -1,0 +1,640 @@
+// api.cu -- host side of the C ABI declared in include/gattn.h.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "gattn.h"
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace gattn;
+
+namespace {
+
+thread_local std::string g_err;
+
+gattn_status fail(gattn_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+gattn_status fail(gattn_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+#define CUDA_TRY(expr)                                                                             \
+    do {                                                                                           \
+        cudaError_t e_ = (expr);                                                                   \
+        if (e_ != cudaSuccess)                                                                     \
+            return fail(GATTN_E_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));             \
+    } while (0)
+
+bool bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
+bool group_ok(int g) { return g == 32 || g == 64 || g == 128; }
+
+int proj_bits(const gattn_cfg &c, int p) { return c.proj_bits[p] ? c.proj_bits[p] : c.bits; }
+int proj_group(const gattn_cfg &c, int p) { return c.proj_group[p] ? c.proj_group[p] : c.group_size; }
+
+int rotary_dims(const gattn_cfg &c)
+{
+    return (int)((double)c.head_dim * (double)c.partial_rotary_factor);
+}
+
+gattn_status validate(const gattn_cfg *c)
+{
+    if (!c)
+        return fail(GATTN_E_INVALID_ARG, "cfg is NULL");
+    if (c->hidden <= 0 || c->num_heads <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0)
+        return fail(GATTN_E_INVALID_ARG, "hidden, num_heads, num_kv_heads, head_dim must be > 0");
+    if (c->num_heads % c->num_kv_heads)
+        return fail(GATTN_E_INVALID_ARG, "num_heads %% num_kv_heads != 0");
+    if (!(c->partial_rotary_factor > 0.f && c->partial_rotary_factor <= 1.f))
+        return fail(GATTN_E_INVALID_ARG, "partial_rotary_factor must be in (0, 1]");
+    const int rd = rotary_dims(*c);
+    if (rd < 2 || (rd & 1))
+        return fail(GATTN_E_INVALID_ARG, "rotary dims %d must be even and >= 2", rd);
+    if (!(c->rope_theta > 0.f) || !(c->rms_eps >= 0.f))
+        return fail(GATTN_E_INVALID_ARG, "rope_theta must be > 0 and rms_eps >= 0");
+    if (c->x_dtype != GATTN_DTYPE_F32 && c->x_dtype != GATTN_DTYPE_BF16)
+        return fail(GATTN_E_INVALID_ARG, "x_dtype must be GATTN_DTYPE_F32 or GATTN_DTYPE_BF16");
+    for (int p = 0; p < 4; ++p) {
+        if (c->proj_bits[p] < 0 || c->proj_group[p] < 0)
+            return fail(GATTN_E_INVALID_ARG, "proj_bits/proj_group must be >= 0");
+        if (!bits_ok(proj_bits(*c, p)))
+            return fail(GATTN_E_INVALID_ARG, "bits %d of projection %d not in {2,3,4,5,6,8}",
+                        proj_bits(*c, p), p);
+        if (!group_ok(proj_group(*c, p)))
+            return fail(GATTN_E_INVALID_ARG, "group %d of projection %d not in {32,64,128}",
+                        proj_group(*c, p), p);
+    }
+    if (c->max_batch <= 0 || c->max_q_len <= 0)
+        return fail(GATTN_E_INVALID_ARG, "max_batch and max_q_len must be > 0");
+    if (c->head_chunk != 0 && c->head_chunk != 1)
+        return fail(GATTN_E_INVALID_ARG, "head_chunk must be 0 or 1");
+    // shapes this build implements
+    if (c->head_dim % 64 || c->head_dim > 256)
+        return fail(GATTN_E_UNSUPPORTED, "head_dim %d: this build needs a multiple of 64 <= 256",
+                    c->head_dim);
+    if (c->hidden % 128)
+        return fail(GATTN_E_UNSUPPORTED, "hidden %d must be a multiple of 128", c->hidden);
+    if ((c->num_heads * c->head_dim) % 128)
+        return fail(GATTN_E_UNSUPPORTED, "num_heads*head_dim must be a multiple of 128");
+    if (proj_bits(*c, 0) != proj_bits(*c, 1) || proj_bits(*c, 0) != proj_bits(*c, 2) ||
+        proj_group(*c, 0) != proj_group(*c, 1) || proj_group(*c, 0) != proj_group(*c, 2))
+        return fail(GATTN_E_UNSUPPORTED, "q, k and v must share bits and group (one fused launch)");
+    if (proj_group(*c, 3) > c->head_dim)
+        return fail(GATTN_E_UNSUPPORTED, "o_proj group must not exceed head_dim");
+    if (c->max_batch * c->max_q_len > 32)
+        return fail(GATTN_E_UNSUPPORTED, "max_batch*max_q_len must be <= 32");
+    if (c->max_batch > 32)
+        return fail(GATTN_E_UNSUPPORTED, "max_batch must be <= 32");
+    const int gqa = c->num_heads / c->num_kv_heads;
+    if (gqa > 64 * kMaxRowBlocks)
+        return fail(GATTN_E_UNSUPPORTED, "gqa too large");
+    return GATTN_OK;
+}
+
+struct ProjPlan {
+    int N = 0, K = 0, bits = 0, group = 0, nrb = 0, nku = 0, ubytes = 0, step_bytes = 0;
+    int stage_bytes[3] = {0, 0, 0}, stages[3] = {0, 0, 0}, grid[3] = {0, 0, 0};  // per NT index
+    uint8_t *w = nullptr;
+};
+
+int nt_index(int NT) { return NT == 1 ? 0 : (NT == 2 ? 1 : 2); }
+
+void plan_proj(ProjPlan &p, int N, int K, int bits, int group)
+{
+    p.N = N;
+    p.K = K;
+    p.bits = bits;
+    p.group = group;
+    p.nrb = (N + kRBR - 1) / kRBR;
+    p.nku = K / kKU;
+    p.ubytes = unit_bytes(bits, group);
+    p.step_bytes = kWR * p.ubytes;
+    for (int i = 0; i < 3; ++i) {
+        const int NT = 1 << i;
+        const int xb = 2048 * NT, sb = (kKU / group) * 32 * NT;
+        int sbytes = p.step_bytes + xb + sb;
+        sbytes = (sbytes + 127) & ~127;
+        p.stage_bytes[i] = sbytes;
+        int st = (96 * 1024) / sbytes;
+        if (st < 2) st = 2;
+        if (st > 8) st = 8;
+        p.stages[i] = st;
+    }
+}
+
+int proj_smem_for(const ProjPlan &p, int i)
+{
+    return p.stages[i] * p.stage_bytes[i] + 2 * p.stages[i] * 8 + 16 + kWR * 256 * 4;
+}
+
+}  // namespace
+
+struct gattn_layer {
+    gattn_cfg cfg{};
+    int rd = 0, gqa = 0, Nq = 0, Nkv = 0, Ko = 0;
+    int device = 0, num_sms = 0;
+    ProjPlan pqkv, po;
+    int M_max = 0;
+    // scratch
+    __half *x16_a = nullptr, *x16_o = nullptr;
+    float *xsum_a = nullptr, *xsum_o = nullptr;
+    __nv_bfloat16 *qn = nullptr;
+    float *gate = nullptr;
+    float *ws_proj = nullptr, *ws_attn = nullptr;
+    int *cnt_qkv = nullptr, *cnt_o = nullptr, *cnt_attn = nullptr;
+    unsigned *status = nullptr;
+    double *inv_freq = nullptr;
+    uint16_t *q_norm = nullptr, *k_norm = nullptr;
+    size_t ws_proj_floats = 0, ws_attn_floats = 0;
+    int attn_grid = 0;
+    int max_seg = 0;
+    gattn_taps taps{};
+    bool weights_set = false;
+    int launches = 0;
+    bool pdl = true;
+    std::vector<cudaEvent_t> events;
+};
+
+struct gattn_kv {
+    gattn_layer *layer = nullptr;
+    gattn_kv_desc desc{};
+    CUtensorMap kmap;   // CUtensorMap is itself 64-byte aligned
+    CUtensorMap vmap;
+};
+
+extern "C" {
+
+const char *gattn_last_error(void) { return g_err.c_str(); }
+
+gattn_status gattn_cfg_validate(const gattn_cfg *cfg) { return validate(cfg); }
+
+int32_t gattn_rotary_dims(const gattn_cfg *cfg) { return cfg ? rotary_dims(*cfg) : -1; }
+
+int32_t gattn_head_chunk_plan(int32_t q_len, int32_t num_heads, int32_t num_kv_heads,
+                              int32_t enabled, int32_t *first, int32_t *len, int32_t cap)
+{
+    if (q_len <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || cap < 0 ||
+        (cap > 0 && (!first || !len)))
+        return -1;
+    const int gqa = num_heads / num_kv_heads;
+    // eligible: more than 32 (row, head) pairs per KV group and at most 32 rows
+    const bool eligible = enabled && q_len <= 32 && (long long)q_len * gqa > 32;
+    int per = gqa;
+    if (eligible) {
+        per = 32 / q_len;
+        per = per < gqa ? per : gqa;
+        per = per > 1 ? per : 1;
+    }
+    const int per_group = (gqa + per - 1) / per;
+    const int count = num_kv_heads * per_group;
+    int n = 0;
+    for (int g = 0; g < num_kv_heads; ++g)
+        for (int j = 0; j < per_group; ++j, ++n)
+            if (n < cap) {
+                first[n] = g * gqa + j * per;
+                len[n] = (j == per_group - 1) ? gqa - j * per : per;
+            }
+    return count;
+}
+
+gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
+{
+    if (!out)
+        return fail(GATTN_E_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    gattn_status st = validate(cfg);
+    if (st != GATTN_OK)
+        return st;
+    gattn_layer *L = new (std::nothrow) gattn_layer();
+    if (!L)
+        return fail(GATTN_E_CUDA, "out of host memory");
+    L->cfg = *cfg;
+    const gattn_cfg &c = L->cfg;
+    L->rd = rotary_dims(c);
+    L->gqa = c.num_heads / c.num_kv_heads;
+    L->Nq = 2 * c.num_heads * c.head_dim;
+    L->Nkv = c.num_kv_heads * c.head_dim;
+    L->Ko = c.num_heads * c.head_dim;
+    L->M_max = c.max_batch * c.max_q_len;
+    auto cleanup = [&](gattn_status s) {
+        gattn_layer_destroy(L);
+        return s;
+    };
+#define TRY(expr)                                                                                  \
+    do {                                                                                           \
+        cudaError_t e_ = (expr);                                                                   \
+        if (e_ != cudaSuccess)                                                                     \
+            return cleanup(fail(GATTN_E_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_)));   \
+    } while (0)
+    TRY(cudaGetDevice(&L->device));
+    TRY(cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device));
+
+    plan_proj(L->pqkv, L->Nq + 2 * L->Nkv, c.hidden, proj_bits(c, 0), proj_group(c, 0));
+    plan_proj(L->po, c.hidden, L->Ko, proj_bits(c, 3), proj_group(c, 3));
+
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        cudaError_t e = attn_set_smem_limits();
+        for (int b : {2, 3, 4, 5, 6, 8})
+            for (int NT : {1, 2, 4})
+                for (int mode : {kModeQKV, kModeO})
+                    if (e == cudaSuccess)
+                        e = proj_set_smem_limits(b, NT, mode, 200 * 1024);
+        attr_err = e;
+    });
+    TRY(attr_err);
+    for (ProjPlan *p : {&L->pqkv, &L->po}) {
+        for (int i = 0; i < 3; ++i) {
+            ProjArgs a{};
+            a.stages = p->stages[i];
+            a.stage_bytes = p->stage_bytes[i];
+            const int smem = proj_smem_bytes(a);
+            int occ = 0;
+            TRY(proj_occupancy(p->bits, 1 << i, p == &L->pqkv ? kModeQKV : kModeO, smem, &occ));
+            if (occ < 1)
+                occ = 1;
+            long long T = (long long)p->nrb * p->nku;
+            long long gsz = (long long)L->num_sms * occ;
+            p->grid[i] = (int)(T < gsz ? T : gsz);
+        }
+    }
+    L->attn_grid = L->num_sms;
+
+    const int MP = 32;  // columns of the widest (NT = 4) operand layout
+    const size_t nku_a = c.hidden / kKU, nku_o = L->Ko / kKU;
+    TRY(cudaMalloc(&L->pqkv.w, (size_t)L->pqkv.nrb * L->pqkv.nku * L->pqkv.step_bytes));
+    TRY(cudaMalloc(&L->po.w, (size_t)L->po.nrb * L->po.nku * L->po.step_bytes));
+    TRY(cudaMalloc(&L->x16_a, nku_a * 4 * 2048));
+    TRY(cudaMalloc(&L->x16_o, nku_o * 4 * 2048));
+    TRY(cudaMemset(L->x16_o, 0, nku_o * 4 * 2048));
+    TRY(cudaMalloc(&L->xsum_a, nku_a * (kKU / L->pqkv.group) * MP * sizeof(float)));
+    TRY(cudaMalloc(&L->xsum_o, nku_o * (kKU / L->po.group) * MP * sizeof(float)));
+    TRY(cudaMemset(L->xsum_o, 0, nku_o * (kKU / L->po.group) * MP * sizeof(float)));
+    TRY(cudaMalloc(&L->qn, (size_t)L->M_max * L->Ko * 2));
+    TRY(cudaMalloc(&L->gate, (size_t)L->M_max * L->Ko * sizeof(float)));
+    const int grid_max = std::max(std::max(L->pqkv.grid[2], L->po.grid[2]),
+                                  std::max(L->pqkv.grid[0], L->po.grid[0]));
+    L->ws_proj_floats = (size_t)(std::max(L->pqkv.nrb, L->po.nrb) + grid_max + 1) * kRBR * MP;
+    TRY(cudaMalloc(&L->ws_proj, L->ws_proj_floats * sizeof(float)));
+    TRY(cudaMalloc(&L->cnt_qkv, (size_t)L->pqkv.nrb * sizeof(int)));
+    TRY(cudaMalloc(&L->cnt_o, (size_t)L->po.nrb * sizeof(int)));
+    TRY(cudaMemset(L->cnt_qkv, 0, (size_t)L->pqkv.nrb * sizeof(int)));
+    TRY(cudaMemset(L->cnt_o, 0, (size_t)L->po.nrb * sizeof(int)));
+    // attention segments: batch x KV heads x row blocks (at most gqa row blocks)
+    L->max_seg = c.max_batch * c.num_kv_heads * std::min(L->gqa, kMaxRowBlocks);
+    L->ws_attn_floats = (size_t)(L->max_seg + L->attn_grid + 1) * (2 * 64 + 64 * c.head_dim);
+    TRY(cudaMalloc(&L->ws_attn, L->ws_attn_floats * sizeof(float)));
+    TRY(cudaMalloc(&L->cnt_attn, (size_t)L->max_seg * sizeof(int)));
+    TRY(cudaMemset(L->cnt_attn, 0, (size_t)L->max_seg * sizeof(int)));
+    TRY(cudaMalloc(&L->status, sizeof(unsigned)));
+    TRY(cudaMemset(L->status, 0, sizeof(unsigned)));
+    std::vector<double> inv(L->rd / 2);
+    for (int i = 0; i < L->rd / 2; ++i)
+        inv[i] = std::pow((double)c.rope_theta, -2.0 * (double)i / (double)L->rd);
+    TRY(cudaMalloc(&L->inv_freq, inv.size() * sizeof(double)));
+    TRY(cudaMemcpy(L->inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice));
+    TRY(cudaMalloc(&L->q_norm, c.head_dim * 2));
+    TRY(cudaMalloc(&L->k_norm, c.head_dim * 2));
+#undef TRY
+    *out = L;
+    return GATTN_OK;
+}
+
+void gattn_layer_destroy(gattn_layer *L)
+{
+    if (!L)
+        return;
+    void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
+                    L->qn,     L->gate,      L->ws_proj, L->ws_attn, L->cnt_qkv, L->cnt_o,
+                    L->cnt_attn, L->status,  L->inv_freq, L->q_norm, L->k_norm};
+    for (void *p : ptrs)
+        if (p)
+            cudaFree(p);
+    delete L;
+}
+
+gattn_status gattn_layer_set_weights(gattn_layer *L, const gattn_weights *w, gattn_stream stream)
+{
+    if (!L || !w)
+        return fail(GATTN_E_INVALID_ARG, "layer or weights is NULL");
+    for (int p = 0; p < 4; ++p)
+        if (!w->proj[p].packed || !w->proj[p].scales || !w->proj[p].biases)
+            return fail(GATTN_E_INVALID_ARG, "projection %d has a NULL buffer", p);
+    if (!w->q_norm || !w->k_norm)
+        return fail(GATTN_E_INVALID_ARG, "q_norm/k_norm is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    RepackSrc a{};
+    a.nsrc = 3;
+    const int rows[3] = {L->Nq, L->Nkv, L->Nkv};
+    for (int i = 0; i < 3; ++i) {
+        a.packed[i] = w->proj[i].packed;
+        a.scales[i] = w->proj[i].scales;
+        a.biases[i] = w->proj[i].biases;
+        a.rows[i] = rows[i];
+    }
+    CUDA_TRY(launch_repack(a, L->pqkv.K, L->pqkv.bits, L->pqkv.group, L->pqkv.nrb, L->pqkv.w, s));
+    RepackSrc o{};
+    o.nsrc = 1;
+    o.packed[0] = w->proj[3].packed;
+    o.scales[0] = w->proj[3].scales;
+    o.biases[0] = w->proj[3].biases;
+    o.rows[0] = L->po.N;
+    CUDA_TRY(launch_repack(o, L->po.K, L->po.bits, L->po.group, L->po.nrb, L->po.w, s));
+    CUDA_TRY(cudaMemcpyAsync(L->q_norm, w->q_norm, L->cfg.head_dim * 2, cudaMemcpyDeviceToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(L->k_norm, w->k_norm, L->cfg.head_dim * 2, cudaMemcpyDeviceToDevice, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    L->weights_set = true;
+    return GATTN_OK;
+}
+
+gattn_status gattn_kv_register(gattn_layer *L, const gattn_kv_desc *d, gattn_kv **out)
+{
+    if (!L || !d || !out)
+        return fail(GATTN_E_INVALID_ARG, "NULL argument");
+    *out = nullptr;
+    if (!d->k || !d->v)
+        return fail(GATTN_E_INVALID_ARG, "cache pointers are NULL");
+    if ((reinterpret_cast<uintptr_t>(d->k) | reinterpret_cast<uintptr_t>(d->v)) & 15)
+        return fail(GATTN_E_INVALID_ARG, "cache pointers must be 16-byte aligned");
+    if (d->batch <= 0 || d->capacity < 16)
+        return fail(GATTN_E_INVALID_ARG, "batch must be > 0 and capacity >= 16");
+    if (d->stride_token <= 0 || d->stride_head <= 0 || d->stride_batch <= 0 ||
+        (d->stride_token | d->stride_head | d->stride_batch) & 7)
+        return fail(GATTN_E_INVALID_ARG, "strides must be positive multiples of 8 elements");
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        CUDA_TRY(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                  cudaEnableDefault, &q));
+        if (q != cudaDriverEntryPointSuccess || !fn)
+            return fail(GATTN_E_CUDA, "cuTensorMapEncodeTiled is not available");
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    gattn_kv *kv = new (std::nothrow) gattn_kv();
+    if (!kv)
+        return fail(GATTN_E_CUDA, "out of host memory");
+    kv->layer = L;
+    kv->desc = *d;
+    const cuuint64_t dims[4] = {(cuuint64_t)L->cfg.head_dim, (cuuint64_t)d->capacity,
+                                (cuuint64_t)L->cfg.num_kv_heads, (cuuint64_t)d->batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)d->stride_token * 2, (cuuint64_t)d->stride_head * 2,
+                                   (cuuint64_t)d->stride_batch * 2};
+    const cuuint32_t box[4] = {64, kAttnUnit, 1, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    for (int i = 0; i < 2; ++i) {
+        CUresult r = encode(i == 0 ? &kv->kmap : &kv->vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                            i == 0 ? d->k : d->v, dims, strides, box, es,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            delete kv;
+            return fail(GATTN_E_INVALID_ARG, "cuTensorMapEncodeTiled rejected the cache (code %d)",
+                        (int)r);
+        }
+    }
+    *out = kv;
+    return GATTN_OK;
+}
+
+void gattn_kv_destroy(gattn_kv *kv) { delete kv; }
+
+gattn_status gattn_layer_set_taps(gattn_layer *L, const gattn_taps *t)
+{
+    if (!L)
+        return fail(GATTN_E_INVALID_ARG, "layer is NULL");
+    L->taps = t ? *t : gattn_taps{};
+    return GATTN_OK;
+}
+
+int32_t gattn_layer_launches_per_step(const gattn_layer *L) { return L ? L->launches : -1; }
+
+gattn_status gattn_layer_set_events(gattn_layer *L, void *const *events, int32_t n)
+{
+    if (!L || n < 0 || (n > 0 && !events))
+        return fail(GATTN_E_INVALID_ARG, "bad event arguments");
+    if (n != 0 && n != 5)
+        return fail(GATTN_E_INVALID_ARG, "need launches_per_step + 1 = 5 events");
+    L->events.assign(reinterpret_cast<cudaEvent_t const *>(events),
+                     reinterpret_cast<cudaEvent_t const *>(events) + n);
+    return GATTN_OK;
+}
+
+gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const int32_t *cache_pos,
+                              int32_t batch, int32_t q_len, void *out, gattn_stream stream)
+{
+    if (!L || !x || !kv || !cache_pos || !out)
+        return fail(GATTN_E_INVALID_ARG, "NULL argument");
+    if (!L->weights_set)
+        return fail(GATTN_E_STATE, "set_weights has not been called");
+    if (kv->layer != L)
+        return fail(GATTN_E_INVALID_ARG, "cache registered with another layer");
+    const gattn_cfg &c = L->cfg;
+    if (batch <= 0 || batch > c.max_batch || batch > kv->desc.batch)
+        return fail(GATTN_E_INVALID_ARG, "batch %d outside [1, min(max_batch %d, cache batch %d)]",
+                    batch, c.max_batch, kv->desc.batch);
+    if (q_len <= 0 || q_len > c.max_q_len)
+        return fail(GATTN_E_INVALID_ARG, "q_len %d outside [1, %d]", q_len, c.max_q_len);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int M = batch * q_len;
+    const int NT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
+    const int ni = nt_index(NT);
+    const bool timing = !L->events.empty();
+    const bool pdl = L->pdl && !timing;
+    int launches = 0;
+    auto mark = [&](int i) -> cudaError_t {
+        return timing ? cudaEventRecord(L->events[i], s) : cudaSuccess;
+    };
+
+    // 1. x -> fp16 tensor-core operand + group sums
+    CUDA_TRY(mark(0));
+    CUDA_TRY(launch_xprep(x, c.x_dtype, M, c.hidden, L->pqkv.group, NT, L->x16_a, L->xsum_a, pdl, s));
+    ++launches;
+
+    // 2. fused q|k|v projection with the norm / rotary / append epilogue
+    ProjArgs a{};
+    a.w = L->pqkv.w;
+    a.x16 = L->x16_a;
+    a.xsum = L->xsum_a;
+    a.nrb = L->pqkv.nrb;
+    a.nku = L->pqkv.nku;
+    a.N = L->pqkv.N;
+    a.M = M;
+    a.group = L->pqkv.group;
+    a.unit_bytes = L->pqkv.ubytes;
+    a.step_bytes = L->pqkv.step_bytes;
+    a.stage_bytes = L->pqkv.stage_bytes[ni];
+    a.stages = L->pqkv.stages[ni];
+    a.T = (long long)a.nrb * a.nku;
+    a.ws = L->ws_proj;
+    a.cnt = L->cnt_qkv;
+    a.eb_rows = std::max(kRBR, c.head_dim);
+    a.status = L->status;
+    EpiQKV eq{};
+    eq.R = q_len;
+    eq.H = c.num_heads;
+    eq.Hk = c.num_kv_heads;
+    eq.d = c.head_dim;
+    eq.rd = L->rd;
+    eq.Nq = L->Nq;
+    eq.Nkv = L->Nkv;
+    eq.cache_pos = cache_pos;
+    eq.cap = kv->desc.capacity;
+    eq.kc = static_cast<__nv_bfloat16 *>(kv->desc.k);
+    eq.vc = static_cast<__nv_bfloat16 *>(kv->desc.v);
+    eq.st_tok = kv->desc.stride_token;
+    eq.st_head = kv->desc.stride_head;
+    eq.st_batch = kv->desc.stride_batch;
+    eq.q_norm = L->q_norm;
+    eq.k_norm = L->k_norm;
+    eq.eps = c.rms_eps;
+    eq.inv_freq = L->inv_freq;
+    eq.qn = L->qn;
+    eq.gate = L->gate;
+    eq.tap_y = L->taps.y;
+    EpiO eo{};
+    CUDA_TRY(mark(1));
+    CUDA_TRY(launch_proj(L->pqkv.bits, NT, kModeQKV, a, eq, eo, L->pqkv.grid[ni], pdl, s));
+    ++launches;
+
+    // 3. attention + merge + gate -> o_proj operand
+    AttnArgs t{};
+    t.qn = L->qn;
+    t.gate = L->gate;
+    t.cache_pos = cache_pos;
+    t.B = batch;
+    t.R = q_len;
+    t.H = c.num_heads;
+    t.Hk = c.num_kv_heads;
+    t.d = c.head_dim;
+    t.cap = kv->desc.capacity;
+    int32_t first[kMaxRowBlocks * 64], len[kMaxRowBlocks * 64];
+    const int nchunks = gattn_head_chunk_plan(q_len, c.num_heads, c.num_kv_heads, c.head_chunk,
+                                              first, len, kMaxRowBlocks * 64);
+    const int per_group = nchunks / c.num_kv_heads;
+    int nrb = 0, max_rows = 0;
+    for (int j = 0; j < per_group; ++j) {
+        // a chunk of more than 64 rows is cut into row blocks of whole heads
+        const int hpb = std::max(1, 64 / q_len);
+        for (int h = 0; h < len[j]; h += hpb) {
+            if (nrb >= kMaxRowBlocks)
+                return fail(GATTN_E_UNSUPPORTED, "too many attention row blocks");
+            t.rb_h0[nrb] = first[j] + h;
+            t.rb_nh[nrb] = std::min(hpb, len[j] - h);
+            max_rows = std::max(max_rows, t.rb_nh[nrb] * q_len);
+            ++nrb;
+        }
+    }
+    if ((long long)batch * c.num_kv_heads * nrb > L->max_seg)
+        return fail(GATTN_E_UNSUPPORTED, "attention segments exceed the scratch sized at create");
+    t.nrb = nrb;
+    t.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+    t.ws = L->ws_attn;
+    t.cnt = L->cnt_attn;
+    t.x16 = L->x16_o;
+    t.xsum = L->xsum_o;
+    t.NT = NT;
+    t.group_o = L->po.group;
+    t.tap_attn = L->taps.attn;
+    t.status = L->status;
+    const int MT = (max_rows + 15) / 16;
+    CUDA_TRY(mark(2));
+    CUDA_TRY(launch_attn(MT, c.head_dim / 64, t, kv->kmap, kv->vmap, L->attn_grid, pdl, s));
+    ++launches;
+
+    // 4. o_proj
+    ProjArgs o = a;
+    o.w = L->po.w;
+    o.x16 = L->x16_o;
+    o.xsum = L->xsum_o;
+    o.nrb = L->po.nrb;
+    o.nku = L->po.nku;
+    o.N = L->po.N;
+    o.group = L->po.group;
+    o.unit_bytes = L->po.ubytes;
+    o.step_bytes = L->po.step_bytes;
+    o.stage_bytes = L->po.stage_bytes[ni];
+    o.stages = L->po.stages[ni];
+    o.T = (long long)o.nrb * o.nku;
+    o.cnt = L->cnt_o;
+    o.eb_rows = kRBR;
+    EpiO e2{};
+    e2.R = q_len;
+    e2.cache_pos = cache_pos;
+    e2.cap = kv->desc.capacity;
+    e2.out = static_cast<__nv_bfloat16 *>(out);
+    CUDA_TRY(mark(3));
+    CUDA_TRY(launch_proj(L->po.bits, NT, kModeO, o, eq, e2, L->po.grid[ni], pdl, s));
+    ++launches;
+    CUDA_TRY(mark(4));
+    L->launches = launches;
+    return GATTN_OK;
+}
+
+gattn_status gattn_layer_poll_status(gattn_layer *L, gattn_stream stream)
+{
+    if (!L)
+        return fail(GATTN_E_INVALID_ARG, "layer is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned v = 0;
+    CUDA_TRY(cudaStreamSynchronize(s));
+    CUDA_TRY(cudaMemcpy(&v, L->status, sizeof v, cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemset(L->status, 0, sizeof v));
+    if (v & kStatusTimeout)
+        return fail(GATTN_E_DEVICE_TIMEOUT, "a bounded device wait gave up");
+    if (v & kStatusRange)
+        return fail(GATTN_E_DEVICE_RANGE, "cache_pos + q_len exceeded the cache capacity");
+    return GATTN_OK;
+}
+
+gattn_status gattn_unpack_codes_device(const uint32_t *packed, int64_t N, int64_t K, int32_t bits,
+                                       uint8_t *codes, gattn_stream stream)
+{
+    if (!packed || !codes || N < 0 || K < 0 || bits < 1 || bits > 8 || (K * bits) % 32)
+        return fail(GATTN_E_INVALID_ARG, "bad unpack arguments");
+    CUDA_TRY(launch_unpack_codes(packed, N, K, bits, codes, reinterpret_cast<cudaStream_t>(stream)));
+    return GATTN_OK;
+}
+
+gattn_status gattn_layer_dequant_device(gattn_layer *L, int32_t proj, float *w, gattn_stream stream)
+{
+    if (!L || !w || proj < 0 || proj > 3)
+        return fail(GATTN_E_INVALID_ARG, "bad dequant arguments");
+    if (!L->weights_set)
+        return fail(GATTN_E_STATE, "set_weights has not been called");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const ProjPlan &p = proj == 3 ? L->po : L->pqkv;
+    float *tmp = nullptr;
+    CUDA_TRY(cudaMalloc(&tmp, (size_t)p.nrb * kRBR * p.K * sizeof(float)));
+    cudaError_t e = launch_dequant_tiles(p.w, p.nrb * kRBR, p.K, p.bits, p.group, p.nrb, tmp, s);
+    const int row0 = proj == 0 ? 0 : (proj == 1 ? L->Nq : (proj == 2 ? L->Nq + L->Nkv : 0));
+    const int rows = proj == 0 ? L->Nq : (proj == 3 ? L->po.N : L->Nkv);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(w, tmp + (size_t)row0 * p.K, (size_t)rows * p.K * sizeof(float),
+                            cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    cudaFree(tmp);
+    if (e != cudaSuccess)
+        return fail(GATTN_E_CUDA, "dequant failed: %s", cudaGetErrorString(e));
+    return GATTN_OK;
+}
+
+}  // extern "C"

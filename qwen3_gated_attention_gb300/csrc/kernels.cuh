@@ -1,0 +1,153 @@
+// kernels.cuh -- parameter blocks, layout constants and launchers shared by the
+// library's translation units (internal; not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gattn {
+
+// ----------------------------------------------------- projection layout
+//
+// A projection matrix W [N][K] (q|k|v concatenated for the fused launch) is
+// repacked into "units" of 32 rows x 128 k.  A row block is kWR units stacked
+// along N (one per consumer warp); the device buffer is ordered
+// [row block][k unit][warp][unit bytes], so one pipeline stage (all warps'
+// units of one k unit) is a single contiguous bulk copy.
+//
+// Unit bytes: codes 512*bits (per lane 16*bits bytes, 16-byte chunk i of lane
+// t at (i*32 + t)*16), then scale/bias pairs 128*(128/group) bytes: for group
+// gi of the unit, lane-quad g, row slot rs (rows g, g+8, g+16, g+24) one
+// uint32 (bf16 scale low half, bf16 bias high half) at ((gi*8 + g)*4 + rs)*4.
+//
+// Lane t = 4g + c holds the tensor-core A fragments of both 16-row m-tiles
+// for all 8 k16-steps: fragment value v (0..7) of MMA mi = 2*kstep + mt is
+// row mt*16 + g + 8*((v>>1)&1), k kstep*16 + 2c + 8*(v>>2) + (v&1), stored as
+// code number mi*8 + v of the lane's bitstream (4-bit codes use the nibble
+// order 0,4,1,5,2,6,3,7 inside each word so that one mask extracts a pair).
+constexpr int kWR = 4;            // consumer warps per CTA = 32-row tiles per row block
+constexpr int kRBR = 32 * kWR;    // rows per row block
+constexpr int kKU = 128;          // k per unit
+
+__host__ __device__ inline int unit_code_bytes(int bits) { return 512 * bits; }
+__host__ __device__ inline int unit_sb_bytes(int group) { return 128 * (128 / group); }
+__host__ __device__ inline int unit_bytes(int bits, int group)
+{
+    return unit_code_bytes(bits) + unit_sb_bytes(group);
+}
+
+// x operand in tensor-core B-fragment order, fp16, for MP = 8*NT columns:
+// element (m, k) at half offset (((ku*NT + m/8)*8 + kstep)*32 + lane)*4 + hi*2 + e
+// with ku = k/128, kstep = (k%128)/16, q = k%16, hi = q/8, lane = (m%8)*4 + (q%8)/2,
+// e = q%2.  Group sums of the same fp16 values: xsum[(ku*(128/group) + gi)*MP + m].
+__host__ __device__ inline long long x16_offset(int m, int k, int NT)
+{
+    int ku = k >> 7, kk = k & 127, kstep = kk >> 4, q = kk & 15;
+    int lane = ((m & 7) << 2) | ((q & 7) >> 1);
+    return ((((long long)ku * NT + (m >> 3)) * 8 + kstep) * 32 + lane) * 4 + ((q >> 3) << 1) +
+           (q & 1);
+}
+
+struct ProjArgs {
+    const uint8_t *w;     // repacked weights
+    const __half *x16;    // B-fragment-ordered x
+    const float *xsum;    // group sums of x16
+    int nrb, nku;         // row blocks, k units
+    int N;                // valid rows
+    int M;                // valid x rows (columns of the product)
+    int group;
+    int unit_bytes, step_bytes, stage_bytes, stages;
+    long long T;          // nrb * nku stream-K units
+    float *ws;            // partial sums [slot][MP][kRBR]
+    int *cnt;             // arrival counters per epilogue block
+    int eb_rows;          // rows per epilogue block (multiple of kRBR)
+    unsigned *status;
+};
+
+// qkv epilogue: per head block, RMSNorm + RoPE + bf16 append / q and gate outputs
+struct EpiQKV {
+    int R;                         // q_len; column m is sequence m / R, row m % R
+    int H, Hk, d, rd;
+    int Nq, Nkv;
+    const int *cache_pos;
+    int cap;
+    __nv_bfloat16 *kc, *vc;        // cache bases
+    long long st_tok, st_head, st_batch;
+    const uint16_t *q_norm, *k_norm;
+    float eps;
+    const double *inv_freq;        // [rd/2]
+    __nv_bfloat16 *qn;             // [B][R][H][d]
+    float *gate;                   // [M][H*d]
+    float *tap_y;                  // [M][Nq + 2 Nkv] or null
+};
+
+struct EpiO {
+    int R;
+    const int *cache_pos;
+    int cap;
+    __nv_bfloat16 *out;            // [M][N]
+};
+
+enum { kModeQKV = 0, kModeO = 1 };
+
+// launchers (return cudaGetLastError() of the launch)
+cudaError_t launch_proj(int bits, int NT, int mode, const ProjArgs &a, const EpiQKV &eq,
+                        const EpiO &eo, int grid, bool pdl, cudaStream_t s);
+int proj_smem_bytes(const ProjArgs &a);
+cudaError_t proj_set_smem_limits(int bits, int NT, int mode, int bytes);
+cudaError_t proj_occupancy(int bits, int NT, int mode, int smem, int *blocks_per_sm);
+
+cudaError_t launch_xprep(const void *x, int x_dtype, int M, int K, int group, int NT, __half *x16,
+                         float *xsum, bool pdl, cudaStream_t s);
+
+struct RepackSrc {
+    const uint32_t *packed[3];
+    const uint16_t *scales[3];
+    const uint16_t *biases[3];
+    int rows[3];                   // rows of each source, concatenated in order
+    int nsrc;
+};
+cudaError_t launch_repack(const RepackSrc &src, int K, int bits, int group, int nrb, uint8_t *dst,
+                          cudaStream_t s);
+cudaError_t launch_dequant_tiles(const uint8_t *w, int N, int K, int bits, int group, int nrb,
+                                 float *out, cudaStream_t s);
+cudaError_t launch_unpack_codes(const uint32_t *packed, long long N, long long K, int bits,
+                                uint8_t *codes, cudaStream_t s);
+
+// ------------------------------------------------------------- attention
+
+constexpr int kAttnWarps = 8;          // consumer warps
+constexpr int kAttnThreads = (kAttnWarps + 1) * 32;
+constexpr int kAttnUnit = 16;          // tokens per stream-K unit
+constexpr int kAttnTile = 64;          // tokens per pipeline stage
+constexpr int kAttnStages = 2;
+constexpr int kMaxRowBlocks = 64;
+
+struct AttnArgs {
+    const __nv_bfloat16 *qn;     // [B][R][H][d]
+    const float *gate;           // [M][H*d]
+    const int *cache_pos;
+    int B, R, H, Hk, d, cap;
+    int nrb;                     // row blocks per KV group
+    int rb_h0[kMaxRowBlocks];    // first head of each row block (relative to the group)
+    int rb_nh[kMaxRowBlocks];    // heads of each row block
+    float scale_log2;            // log2(e) / sqrt(d)
+    float *ws;                   // partials [slot][64 rows][d + 2]
+    int *cnt;                    // per segment
+    // o_proj operand
+    __half *x16;
+    float *xsum;
+    int NT, group_o;
+    float *tap_attn;             // [M][H*d] or null
+    unsigned *status;
+};
+
+cudaError_t launch_attn(int MT, int DB, const AttnArgs &a, const CUtensorMap &kmap,
+                        const CUtensorMap &vmap, int grid, bool pdl, cudaStream_t s);
+int attn_smem_bytes(int MT, int DB);
+cudaError_t attn_set_smem_limits();
+
+}  // namespace gattn

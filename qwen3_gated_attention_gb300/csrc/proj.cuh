@@ -1,0 +1,473 @@
+// proj.cuh -- affine-dequant projection kernel: y[m][n] = sum_k W[n][k] x[m][k]
+// with W = scale * code + bias per (row, group).
+//
+// Weights stream once from HBM: one producer warp issues 1-D TMA bulk copies
+// of contiguous stages (all warps' units of one 128-wide k unit, plus the x
+// fragments and group sums of that k unit) into a shared-memory ring; kWR
+// consumer warps unpack the codes in registers straight into exact fp16
+// tensor-core A fragments and run mma.sync m16n8k16 against x (B fragments).
+// Per group, D = sum code*x is folded as y += scale*D + bias*sum(x) in fp32, so
+// no per-weight dequantization multiply is spent.
+//
+// Work is split stream-K: the nrb*nku (row block, k unit) units are cut into
+// gridDim.x contiguous ranges.  A CTA writes one partial per row block it
+// touches; the last CTA to arrive on an epilogue block (counter, no waiting)
+// sums the partials in a fixed order and runs the epilogue.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace gattn {
+
+__device__ __forceinline__ uint32_t h2_sub_1024(uint32_t v)
+{
+    __half2 h = *reinterpret_cast<__half2 *>(&v);
+    h = __hsub2(h, __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// (1024 + 16 n) / 16 - 64 = n, exact in fp16
+__device__ __forceinline__ uint32_t h2_div16_sub64(uint32_t v)
+{
+    __half2 h = *reinterpret_cast<__half2 *>(&v);
+    h = __hfma2(h, __half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00)),
+                __half2(__ushort_as_half(0xD400), __ushort_as_half(0xD400)));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t code_at(const uint32_t *cw, int off)
+{
+    const int word = off >> 5, sh = off & 31;
+    const uint32_t mask = (1u << BITS) - 1u;
+    if (sh + BITS <= 32)
+        return (cw[word] >> sh) & mask;
+    return __funnelshift_r(cw[word], cw[word + 1], sh) & mask;
+}
+
+// Exact fp16 codes of the A fragment of MMA mi from the lane's code stream.
+template <int BITS>
+__device__ __forceinline__ void unpack_a(const uint32_t *cw, int mi, uint32_t (&A)[4])
+{
+    if constexpr (BITS == 8) {
+        const uint32_t w0 = cw[2 * mi], w1 = cw[2 * mi + 1];
+        A[0] = h2_sub_1024(__byte_perm(w0, 0x64646464u, 0x4140));
+        A[1] = h2_sub_1024(__byte_perm(w0, 0x64646464u, 0x4342));
+        A[2] = h2_sub_1024(__byte_perm(w1, 0x64646464u, 0x4140));
+        A[3] = h2_sub_1024(__byte_perm(w1, 0x64646464u, 0x4342));
+    } else if constexpr (BITS == 4) {
+        const uint32_t w = cw[mi], w8 = w >> 8;
+        A[0] = h2_sub_1024((w & 0x000F000Fu) | 0x64006400u);
+        A[1] = h2_div16_sub64((w & 0x00F000F0u) | 0x64006400u);
+        A[2] = h2_sub_1024((w8 & 0x000F000Fu) | 0x64006400u);
+        A[3] = h2_div16_sub64((w8 & 0x00F000F0u) | 0x64006400u);
+    } else {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int off = (mi * 8 + 2 * p) * BITS;
+            const uint32_t c0 = code_at<BITS>(cw, off), c1 = code_at<BITS>(cw, off + BITS);
+            A[p] = h2_sub_1024(c0 | (c1 << 16) | 0x64006400u);
+        }
+    }
+}
+
+// One stage: all 8 k16-steps of this warp's unit, folded into Y.
+template <int BITS, int NT>
+__device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, int ubytes, int group,
+                                           int w, int lane, float (&Y)[2][NT][4])
+{
+    const uint8_t *unit = st + w * ubytes;
+    const uint8_t *sb = unit + unit_code_bytes(BITS);
+    const uint2 *xf = reinterpret_cast<const uint2 *>(st + step_bytes);
+    const float *xs = reinterpret_cast<const float *>(st + step_bytes + 2048 * NT);
+    const int kpg = group >> 4;
+    const int g = lane >> 2, c = lane & 3;
+
+    uint32_t cw[4 * BITS];
+#pragma unroll
+    for (int i = 0; i < BITS; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(unit + (i * 32 + lane) * 16);
+        cw[4 * i] = v.x;
+        cw[4 * i + 1] = v.y;
+        cw[4 * i + 2] = v.z;
+        cw[4 * i + 3] = v.w;
+    }
+    float D[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                D[mt][nt][i] = 0.f;
+
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        uint32_t A[2][4];
+        unpack_a<BITS>(cw, 2 * ks, A[0]);
+        unpack_a<BITS>(cw, 2 * ks + 1, A[1]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint2 b = xf[(nt * 8 + ks) * 32 + lane];
+            mma_f16(D[0][nt], A[0], b.x, b.y, D[0][nt]);
+            mma_f16(D[1][nt], A[1], b.x, b.y, D[1][nt]);
+        }
+        if ((ks % kpg) == kpg - 1) {
+            const int gi = ks / kpg;
+            const uint4 e = *reinterpret_cast<const uint4 *>(sb + (gi * 8 + g) * 16);
+            const float s[4] = {bf16_lo(e.x), bf16_lo(e.y), bf16_lo(e.z), bf16_lo(e.w)};
+            const float bb[4] = {bf16_hi(e.x), bf16_hi(e.y), bf16_hi(e.z), bf16_hi(e.w)};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float2 xv = *reinterpret_cast<const float2 *>(xs + gi * 8 * NT + nt * 8 + 2 * c);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    float *y = Y[mt][nt];
+                    float *dd = D[mt][nt];
+                    y[0] = fmaf(s[2 * mt], dd[0], fmaf(bb[2 * mt], xv.x, y[0]));
+                    y[1] = fmaf(s[2 * mt], dd[1], fmaf(bb[2 * mt], xv.y, y[1]));
+                    y[2] = fmaf(s[2 * mt + 1], dd[2], fmaf(bb[2 * mt + 1], xv.x, y[2]));
+                    y[3] = fmaf(s[2 * mt + 1], dd[3], fmaf(bb[2 * mt + 1], xv.y, y[3]));
+                    dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
+                }
+            }
+        }
+    }
+}
+
+// Final value of row n (global), column m, summed over the row block's partials.
+__device__ __forceinline__ float proj_final(const ProjArgs &a, int MP, int n, int m)
+{
+    const long long G = gridDim.x;
+    const int rb = n / kRBR, rr = n % kRBR;
+    const long long s0 = (long long)rb * a.nku, s1 = s0 + a.nku - 1;
+    const long long cf = sk_owner(s0, a.T, G), cl = sk_owner(s1, a.T, G);
+    float v = 0.f;
+    for (long long j = 0; j <= cl - cf; ++j) {
+        const float *p = a.ws + ((long long)rb + cf + j) * MP * kRBR;
+        v += __ldcg(p + (long long)m * kRBR + rr);
+    }
+    return v;
+}
+
+// qkv epilogue for one epilogue block: every (head, column) pair is one warp's job.
+static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, int MP, int eb, int warp,
+                             int lane, float *wbuf)
+{
+    const int d = e.d, half = e.rd >> 1, heads = a.eb_rows / d, per = d >> 5;
+    const int Ny = e.Nq + 2 * e.Nkv;
+    for (int job = warp; job < heads * a.M; job += kWR) {
+        const int hb = job / a.M, m = job % a.M;
+        const int n0 = eb * a.eb_rows + hb * d;
+        if (n0 >= a.N)
+            continue;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < per)
+                v[i] = proj_final(a, MP, n0 + lane + 32 * i, m);
+        if (e.tap_y) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < per)
+                    e.tap_y[(long long)m * Ny + n0 + lane + 32 * i] = v[i];
+        }
+        const int b = m / e.R, r = m % e.R;
+        const int p0 = e.cache_pos[b];
+        const bool valid = p0 >= 0 && p0 + e.R <= e.cap;
+        int kind, head;    // 0 query, 1 gate, 2 k, 3 v
+        if (n0 < e.Nq) {
+            head = n0 / (2 * d);
+            kind = ((n0 % (2 * d)) >= d) ? 1 : 0;
+        } else if (n0 < e.Nq + e.Nkv) {
+            head = (n0 - e.Nq) / d;
+            kind = 2;
+        } else {
+            head = (n0 - e.Nq - e.Nkv) / d;
+            kind = 3;
+        }
+        if (kind == 1) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < per)
+                    e.gate[(long long)m * e.H * d + head * d + lane + 32 * i] = v[i];
+            continue;
+        }
+        if (kind == 0 || kind == 2) {
+            // RMSNorm over the head: x / sqrt(mean(x^2) + eps) * w
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < per)
+                    ss = fmaf(v[i], v[i], ss);
+#pragma unroll
+            for (int o = 16; o; o >>= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float inv = rsqrtf(ss / (float)d + e.eps);
+            const uint16_t *nw = kind == 0 ? e.q_norm : e.k_norm;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < per)
+                    v[i] = v[i] * inv * __uint_as_float((uint32_t)nw[lane + 32 * i] << 16);
+            // partial rotary on dims [0, rd): pairs (i, i + rd/2) at position p0 + r
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < per)
+                    wbuf[lane + 32 * i] = v[i];
+            __syncwarp();
+            const double pos = (double)(p0 + r);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = lane + 32 * i;
+                if (i < per && j < e.rd) {
+                    const int fi = j < half ? j : j - half;
+                    const double ang = pos * e.inv_freq[fi];
+                    const double turns = rint(ang * 0.15915494309189535);
+                    const float red = (float)fma(-turns, 6.283185307179586, ang);
+                    float sn, cs;
+                    sincosf(red, &sn, &cs);
+                    if (j < half)
+                        v[i] = v[i] * cs - wbuf[j + half] * sn;
+                    else
+                        v[i] = v[i] * cs + wbuf[j - half] * sn;
+                }
+            }
+            __syncwarp();
+        }
+        if (kind == 0) {
+            __nv_bfloat16 *q = e.qn + (((long long)b * e.R + r) * e.H + head) * d;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < per)
+                    q[lane + 32 * i] = __float2bfloat16_rn(v[i]);
+            continue;
+        }
+        if (!valid) {
+            if (lane == 0)
+                atomicOr(a.status, kStatusRange);
+            continue;
+        }
+        __nv_bfloat16 *dst = (kind == 2 ? e.kc : e.vc) + (long long)b * e.st_batch +
+                             (long long)head * e.st_head + (long long)(p0 + r) * e.st_tok;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < per)
+                dst[lane + 32 * i] = __float2bfloat16_rn(v[i]);
+    }
+}
+
+static __device__ void epilogue_o(const ProjArgs &a, const EpiO &e, int MP, int eb, int tid)
+{
+    const int n = eb * a.eb_rows + tid;     // eb_rows == kRBR, one row per thread
+    if (tid >= a.eb_rows || n >= a.N)
+        return;
+    for (int m = 0; m < a.M; ++m) {
+        const int b = m / e.R;
+        const int p0 = e.cache_pos[b];
+        const bool valid = p0 >= 0 && p0 + e.R <= e.cap;
+        const float v = valid ? proj_final(a, MP, n, m) : 0.f;
+        e.out[(long long)m * a.N + n] = __float2bfloat16_rn(v);
+    }
+}
+
+template <int BITS, int NT, int MODE>
+__global__ void __launch_bounds__((kWR + 1) * 32)
+    proj_kernel(const ProjArgs a, const EpiQKV eq, const EpiO eo)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int MP = 8 * NT;
+    const int S = a.stages;
+    uint8_t *stages = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * a.stage_bytes);
+    uint64_t *empty = full + S;
+    int *flags = reinterpret_cast<int *>(empty + S);      // [0] abort, [1] last arrival
+    float *wbuf = reinterpret_cast<float *>(flags + 4);    // kWR x 256 floats
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kWR);
+        }
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const long long G = gridDim.x, c = blockIdx.x;
+    const long long beg = sk_start(c, a.T, G), end = sk_start(c + 1, a.T, G);
+    const int xbytes = 2048 * NT, sbytes = (kKU / a.group) * 4 * MP;
+    volatile int *abort = flags;
+
+    if (warp == kWR) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            long long it = 0;
+            // weights do not depend on the previous kernel: start streaming them
+            // before waiting for it, then fetch x once it is visible.
+            const long long pre = (end - beg) < S ? (end - beg) : S;
+            for (; it < pre; ++it) {
+                const long long s = beg + it;
+                uint8_t *st = stages + (size_t)(it % S) * a.stage_bytes;
+                mbar_arrive_expect_tx(&full[it % S], a.step_bytes + xbytes + sbytes);
+                bulk_g2s(st, a.w + s * a.step_bytes, a.step_bytes, &full[it % S], pol);
+            }
+            pdl_wait();
+            for (long long i = 0; i < pre; ++i) {
+                const long long s = beg + i;
+                const int ku = (int)(s % a.nku);
+                uint8_t *st = stages + (size_t)(i % S) * a.stage_bytes;
+                bulk_g2s(st + a.step_bytes, a.x16 + (long long)ku * NT * 1024, xbytes,
+                         &full[i % S], pol);
+                bulk_g2s(st + a.step_bytes + xbytes, a.xsum + (long long)ku * (kKU / a.group) * MP,
+                         sbytes, &full[i % S], pol);
+            }
+            for (; beg + it < end; ++it) {
+                const long long s = beg + it;
+                const int slot = (int)(it % S);
+                const uint32_t ph = (uint32_t)((it / S) & 1);
+                if (!mbar_wait(&empty[slot], ph ^ 1u, abort, a.status))
+                    break;
+                const int ku = (int)(s % a.nku);
+                uint8_t *st = stages + (size_t)slot * a.stage_bytes;
+                mbar_arrive_expect_tx(&full[slot], a.step_bytes + xbytes + sbytes);
+                bulk_g2s(st, a.w + s * a.step_bytes, a.step_bytes, &full[slot], pol);
+                bulk_g2s(st + a.step_bytes, a.x16 + (long long)ku * NT * 1024, xbytes, &full[slot],
+                         pol);
+                bulk_g2s(st + a.step_bytes + xbytes, a.xsum + (long long)ku * (kKU / a.group) * MP,
+                         sbytes, &full[slot], pol);
+            }
+            // let every copy this CTA issued land before the CTA may exit
+            const long long first = it > S ? it - S : 0;
+            for (long long i = first; i < it; ++i) {
+                unsigned long long t0 = global_ns();
+                while (!mbar_try(&full[i % S], (uint32_t)((i / S) & 1)) &&
+                       global_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------- consumers
+    pdl_wait();
+    pdl_launch_dependents();
+    const int tid = threadIdx.x;           // 0 .. kWR*32-1
+    const int g = lane >> 2, cq = lane & 3;
+    float Y[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                Y[mt][nt][i] = 0.f;
+
+    long long it = 0;
+    for (long long s = beg; s < end; ++s, ++it) {
+        const int slot = (int)(it % S);
+        const uint32_t ph = (uint32_t)((it / S) & 1);
+        const int rb = (int)(s / a.nku), ku = (int)(s % a.nku);
+        if (mbar_wait(&full[slot], ph, abort, a.status))
+            proj_stage<BITS, NT>(stages + (size_t)slot * a.stage_bytes, a.step_bytes, a.unit_bytes,
+                                 a.group, warp, lane, Y);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[slot]);
+
+        if (ku == a.nku - 1 || s == end - 1) {
+            // partial of this row block: [MP][kRBR] floats in slot rb + first + j
+            const long long s0 = (long long)rb * a.nku;
+            const long long cf = sk_owner(s0, a.T, G);
+            float *p = a.ws + ((long long)rb + c) * MP * kRBR;    // rb + cf + (c - cf)
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int row = warp * 32 + mt * 16 + g, col = nt * 8 + 2 * cq;
+                    p[(long long)col * kRBR + row] = Y[mt][nt][0];
+                    p[(long long)(col + 1) * kRBR + row] = Y[mt][nt][1];
+                    p[(long long)col * kRBR + row + 8] = Y[mt][nt][2];
+                    p[(long long)(col + 1) * kRBR + row + 8] = Y[mt][nt][3];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        Y[mt][nt][i] = 0.f;
+                }
+            (void)cf;
+            __threadfence();
+            named_bar_sync(1, kWR * 32);
+            const int eb = rb * kRBR / a.eb_rows;
+            if (tid == 0) {
+                int total = 0;
+                const int rb0 = eb * a.eb_rows / kRBR, rb1 = rb0 + a.eb_rows / kRBR;
+                for (int q = rb0; q < rb1 && q < a.nrb; ++q) {
+                    const long long q0 = (long long)q * a.nku;
+                    total += (int)(sk_owner(q0 + a.nku - 1, a.T, G) - sk_owner(q0, a.T, G) + 1);
+                }
+                const int old = atomicAdd(&a.cnt[eb], 1);
+                flags[1] = (old == total - 1);
+            }
+            named_bar_sync(1, kWR * 32);
+            if (flags[1]) {
+                __threadfence();
+                if constexpr (MODE == kModeQKV)
+                    epilogue_qkv(a, eq, MP, eb, warp, lane, wbuf + warp * 256);
+                else
+                    epilogue_o(a, eo, MP, eb, tid);
+                named_bar_sync(1, kWR * 32);
+                if (tid == 0)
+                    a.cnt[eb] = 0;
+            }
+        }
+    }
+}
+
+template <int BITS, int NT, int MODE>
+cudaError_t launch_proj_t(const ProjArgs &a, const EpiQKV &eq, const EpiO &eo, int grid, bool pdl,
+                          cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((kWR + 1) * 32);
+    cfg.dynamicSmemBytes = proj_smem_bytes(a);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, proj_kernel<BITS, NT, MODE>, a, eq, eo);
+}
+
+template <int BITS>
+cudaError_t launch_proj_bits(int NT, int mode, const ProjArgs &a, const EpiQKV &eq, const EpiO &eo,
+                             int grid, bool pdl, cudaStream_t s)
+{
+    if (mode == kModeQKV) {
+        if (NT == 1) return launch_proj_t<BITS, 1, kModeQKV>(a, eq, eo, grid, pdl, s);
+        if (NT == 2) return launch_proj_t<BITS, 2, kModeQKV>(a, eq, eo, grid, pdl, s);
+        return launch_proj_t<BITS, 4, kModeQKV>(a, eq, eo, grid, pdl, s);
+    }
+    if (NT == 1) return launch_proj_t<BITS, 1, kModeO>(a, eq, eo, grid, pdl, s);
+    if (NT == 2) return launch_proj_t<BITS, 2, kModeO>(a, eq, eo, grid, pdl, s);
+    return launch_proj_t<BITS, 4, kModeO>(a, eq, eo, grid, pdl, s);
+}
+
+template <int BITS>
+cudaError_t set_smem_bits(int bytes)
+{
+    cudaError_t e = cudaSuccess;
+#define GATTN_SET(NT, MODE)                                                                        \
+    if (e == cudaSuccess)                                                                          \
+        e = cudaFuncSetAttribute(proj_kernel<BITS, NT, MODE>,                                      \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    GATTN_SET(1, kModeQKV) GATTN_SET(2, kModeQKV) GATTN_SET(4, kModeQKV)
+    GATTN_SET(1, kModeO) GATTN_SET(2, kModeO) GATTN_SET(4, kModeO)
+#undef GATTN_SET
+    return e;
+}
+
+}  // namespace gattn
