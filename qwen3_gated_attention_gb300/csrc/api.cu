@@ -97,8 +97,9 @@ gattn_status validate(const gattn_cfg *c)
         return fail(GATTN_E_UNSUPPORTED, "q, k and v must share bits and group (one fused launch)");
     if (proj_group(*c, 3) > c->head_dim)
         return fail(GATTN_E_UNSUPPORTED, "o_proj group must not exceed head_dim");
-    if (c->max_batch * c->max_q_len > 32)
-        return fail(GATTN_E_UNSUPPORTED, "max_batch*max_q_len must be <= 32");
+    if (c->max_batch * c->max_q_len > (c->x_dtype == GATTN_DTYPE_F32 ? 16 : 32))
+        return fail(GATTN_E_UNSUPPORTED,
+                    "max_batch*max_q_len must be <= 32 (<= 16 for fp32 x, which takes two fp16 planes)");
     if (c->max_batch > 32)
         return fail(GATTN_E_UNSUPPORTED, "max_batch must be <= 32");
     const int gqa = c->num_heads / c->num_kv_heads;
@@ -289,8 +290,9 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaMemset(L->xsum_o, 0, nku_o * (kKU / L->po.group) * MP * sizeof(float)));
     TRY(cudaMalloc(&L->qn, (size_t)L->M_max * L->Ko * 2));
     TRY(cudaMalloc(&L->gate, (size_t)L->M_max * L->Ko * sizeof(float)));
-    const int grid_max = std::max(std::max(L->pqkv.grid[2], L->po.grid[2]),
-                                  std::max(L->pqkv.grid[0], L->po.grid[0]));
+    int grid_max = 0;
+    for (int i = 0; i < 3; ++i)
+        grid_max = std::max(grid_max, std::max(L->pqkv.grid[i], L->po.grid[i]));
     L->ws_proj_floats = (size_t)(std::max(L->pqkv.nrb, L->po.nrb) + grid_max + 1) * kRBR * MP;
     TRY(cudaMalloc(&L->ws_proj, L->ws_proj_floats * sizeof(float)));
     TRY(cudaMalloc(&L->cnt_qkv, (size_t)L->pqkv.nrb * sizeof(int)));
@@ -454,8 +456,11 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
         return fail(GATTN_E_INVALID_ARG, "q_len %d outside [1, %d]", q_len, c.max_q_len);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int M = batch * q_len;
+    // the q|k|v operand has 2M columns for fp32 x (exact hi + lo fp16 planes)
+    const int Ma = c.x_dtype == GATTN_DTYPE_F32 ? 2 * M : M;
+    const int NTa = Ma <= 8 ? 1 : (Ma <= 16 ? 2 : 4);
     const int NT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
-    const int ni = nt_index(NT);
+    const int nia = nt_index(NTa), ni = nt_index(NT);
     const bool timing = !L->events.empty();
     const bool pdl = L->pdl && !timing;
     int launches = 0;
@@ -465,7 +470,7 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
 
     // 1. x -> fp16 tensor-core operand + group sums
     CUDA_TRY(mark(0));
-    CUDA_TRY(launch_xprep(x, c.x_dtype, M, c.hidden, L->pqkv.group, NT, L->x16_a, L->xsum_a, pdl, s));
+    CUDA_TRY(launch_xprep(x, c.x_dtype, M, c.hidden, L->pqkv.group, NTa, L->x16_a, L->xsum_a, pdl, s));
     ++launches;
 
     // 2. fused q|k|v projection with the norm / rotary / append epilogue
@@ -480,12 +485,13 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     a.group = L->pqkv.group;
     a.unit_bytes = L->pqkv.ubytes;
     a.step_bytes = L->pqkv.step_bytes;
-    a.stage_bytes = L->pqkv.stage_bytes[ni];
-    a.stages = L->pqkv.stages[ni];
+    a.stage_bytes = L->pqkv.stage_bytes[nia];
+    a.stages = L->pqkv.stages[nia];
     a.T = (long long)a.nrb * a.nku;
     a.ws = L->ws_proj;
     a.cnt = L->cnt_qkv;
     a.eb_rows = std::max(kRBR, c.head_dim);
+    a.xsplit = c.x_dtype == GATTN_DTYPE_F32 ? M : 0;
     a.status = L->status;
     EpiQKV eq{};
     eq.R = q_len;
@@ -511,7 +517,7 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     eq.tap_y = L->taps.y;
     EpiO eo{};
     CUDA_TRY(mark(1));
-    CUDA_TRY(launch_proj(L->pqkv.bits, NT, kModeQKV, a, eq, eo, L->pqkv.grid[ni], pdl, s));
+    CUDA_TRY(launch_proj(L->pqkv.bits, NTa, kModeQKV, a, eq, eo, L->pqkv.grid[nia], pdl, s));
     ++launches;
 
     // 3. attention + merge + gate -> o_proj operand
@@ -575,6 +581,7 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     o.T = (long long)o.nrb * o.nku;
     o.cnt = L->cnt_o;
     o.eb_rows = kRBR;
+    o.xsplit = 0;
     EpiO e2{};
     e2.R = q_len;
     e2.cache_pos = cache_pos;

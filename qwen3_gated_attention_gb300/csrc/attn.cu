@@ -118,8 +118,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     __syncthreads();
 
-    const long long T = prefix[a.B], G = gridDim.x, c = blockIdx.x;
-    const long long beg = sk_start(c, T, G), end = sk_start(c + 1, T, G);
+    // Ranges are cut over min(grid, units) CTAs so that every participating CTA
+    // owns at least one unit (the merge counts contributors by range); the
+    // remaining CTAs have nothing to do.
+    const long long T = prefix[a.B], c = blockIdx.x;
+    const long long G = T < (long long)gridDim.x ? (T > 0 ? T : 1) : (long long)gridDim.x;
+    const long long beg = c < G ? sk_start(c, T, G) : T, end = c < G ? sk_start(c + 1, T, G) : T;
     volatile int *abort = flags;
 
     if (warp == kAttnWarps) {

@@ -64,6 +64,7 @@ struct ProjArgs {
     float *ws;            // partial sums [slot][MP][kRBR]
     int *cnt;             // arrival counters per epilogue block
     int eb_rows;          // rows per epilogue block (multiple of kRBR)
+    int xsplit;           // > 0: column m + xsplit holds the low fp16 part of column m
     unsigned *status;
 };
 
@@ -100,6 +101,8 @@ int proj_smem_bytes(const ProjArgs &a);
 cudaError_t proj_set_smem_limits(int bits, int NT, int mode, int bytes);
 cudaError_t proj_occupancy(int bits, int NT, int mode, int smem, int *blocks_per_sm);
 
+// fp32 x is split exactly into hi = fp16(x) (column m) and lo = fp16(x - hi)
+// (column M + m); bf16 x converts to fp16 exactly (finite, |x| < 65504).
 cudaError_t launch_xprep(const void *x, int x_dtype, int M, int K, int group, int NT, __half *x16,
                          float *xsum, bool pdl, cudaStream_t s);
 

@@ -213,11 +213,14 @@ __global__ void __launch_bounds__(256) xprep_kernel(const void *x, int x_dtype, 
     if (m >= MP)
         return;
     const int k0 = ku * kKU + part * 16;
+    // fp32 input: columns [M, 2M) carry the exact remainder x - fp16(x)
+    const bool lo_part = x_dtype == 0 && m >= M && m < 2 * M;
+    const int src_m = lo_part ? m - M : m;
     float v[16];
-    if (m < M) {
+    if (m < M || lo_part) {
         if (x_dtype == 0) {
             const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(x) +
-                                                                 (long long)m * K + k0);
+                                                                 (long long)src_m * K + k0);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float4 f = src[i];
@@ -249,7 +252,8 @@ __global__ void __launch_bounds__(256) xprep_kernel(const void *x, int x_dtype, 
     float sum = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        h[i] = __float2half_rn(v[i]);
+        const __half hi = __float2half_rn(v[i]);
+        h[i] = lo_part ? __float2half_rn(v[i] - __half2float(hi)) : hi;
         sum += __half2float(h[i]);
     }
     // element q of this k16 step goes to lane (m%8)*4 + (q%8)/2, half slot (q/8)*2 + q%2

@@ -147,6 +147,8 @@ __device__ __forceinline__ float proj_final(const ProjArgs &a, int MP, int n, in
     for (long long j = 0; j <= cl - cf; ++j) {
         const float *p = a.ws + ((long long)rb + cf + j) * MP * kRBR;
         v += __ldcg(p + (long long)m * kRBR + rr);
+        if (a.xsplit)
+            v += __ldcg(p + (long long)(m + a.xsplit) * kRBR + rr);
     }
     return v;
 }
@@ -296,6 +298,7 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
     }
     __syncthreads();
 
+    // every CTA of the grid owns at least one unit: the host launches at most T CTAs
     const long long G = gridDim.x, c = blockIdx.x;
     const long long beg = sk_start(c, a.T, G), end = sk_start(c + 1, a.T, G);
     const int xbytes = 2048 * NT, sbytes = (kKU / a.group) * 4 * MP;
