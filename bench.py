@@ -66,7 +66,8 @@ def algorithmic_bytes(spec):
     per_kernel = {
         "xprep": xb + x16,
         "proj_qkv": wq + wk + wv + x16 + qn + gate + kv_write,
-        "attn": kv_read + qn + gate + o16,
+        "attn": kv_read + qn,
+        "merge": gate + o16,
         "proj_o": wo + o16 + outb,
     }
     step = wq + wk + wv + wo + kv_read + kv_write + xb + outb
@@ -347,7 +348,7 @@ def our_arm(args, spec):
         gattn.layer_poll_status(dl.h, sh)
 
     # per-kernel pass: events between the step's kernels (programmatic overlap off)
-    names = ["xprep", "proj_qkv", "attn", "proj_o"]
+    names = ["xprep", "proj_qkv", "attn", "merge", "proj_o"]
     nper = min(K, max(n_inst, 4 * n_inst))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(nper)]
     per_kernel_ms = {n: [] for n in names}

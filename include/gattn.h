@@ -227,7 +227,8 @@ int32_t gattn_head_chunk_plan(int32_t q_len, int32_t num_heads, int32_t num_kv_h
                               int32_t cap);
 
 /* Per-step launch report of the layer's last step: number of kernel launches
- * it enqueued (all of them this library's own kernels). */
+ * it enqueued (all of them this library's own kernels: x operand prep, fused
+ * q|k|v projection, attention, attention merge + gate, o_proj). */
 int32_t gattn_layer_launches_per_step(const gattn_layer *layer);
 
 /* Instrumentation: with n == launches_per_step + 1 cudaEvent_t handles, each

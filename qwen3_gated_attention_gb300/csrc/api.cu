@@ -116,6 +116,10 @@ struct ProjPlan {
 
 int nt_index(int NT) { return NT == 1 ? 0 : (NT == 2 ? 1 : 2); }
 
+constexpr int kLaunchesPerStep = 5;  // xprep, q|k|v projection, attention, merge, o_proj
+constexpr int kProjMinSteps = 4;     // k units per projection CTA, at least
+constexpr int kAttnMinUnits = 4;     // 16-token units per attention CTA, at least
+
 void plan_proj(ProjPlan &p, int N, int K, int bits, int group)
 {
     p.N = N;
@@ -158,7 +162,7 @@ struct gattn_layer {
     __nv_bfloat16 *qn = nullptr;
     float *gate = nullptr;
     float *ws_proj = nullptr, *ws_attn = nullptr;
-    int *cnt_qkv = nullptr, *cnt_o = nullptr, *cnt_attn = nullptr;
+    int *cnt_qkv = nullptr, *cnt_o = nullptr;
     unsigned *status = nullptr;
     double *inv_freq = nullptr;
     uint16_t *q_norm = nullptr, *k_norm = nullptr;
@@ -266,13 +270,18 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
             ProjArgs a{};
             a.stages = p->stages[i];
             a.stage_bytes = p->stage_bytes[i];
+            a.eb_rows = p == &L->pqkv ? std::max(kRBR, c.head_dim) : kRBR;
             const int smem = proj_smem_bytes(a);
             int occ = 0;
             TRY(proj_occupancy(p->bits, 1 << i, p == &L->pqkv ? kModeQKV : kModeO, smem, &occ));
             if (occ < 1)
                 occ = 1;
-            long long T = (long long)p->nrb * p->nku;
+            // at most one CTA per resident slot, and at least kProjMinSteps k units
+            // per CTA so that each row block has few partials to merge
+            const long long T = (long long)p->nrb * p->nku;
             long long gsz = (long long)L->num_sms * occ;
+            const long long by_work = std::max<long long>(1, T / kProjMinSteps);
+            gsz = std::min(gsz, by_work);
             p->grid[i] = (int)(T < gsz ? T : gsz);
         }
     }
@@ -301,10 +310,8 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaMemset(L->cnt_o, 0, (size_t)L->po.nrb * sizeof(int)));
     // attention segments: batch x KV heads x row blocks (at most gqa row blocks)
     L->max_seg = c.max_batch * c.num_kv_heads * std::min(L->gqa, kMaxRowBlocks);
-    L->ws_attn_floats = (size_t)(L->max_seg + L->attn_grid + 1) * (2 * 64 + 64 * c.head_dim);
+    L->ws_attn_floats = (size_t)(L->max_seg + L->attn_grid + 1) * attn_slot_floats(c.head_dim);
     TRY(cudaMalloc(&L->ws_attn, L->ws_attn_floats * sizeof(float)));
-    TRY(cudaMalloc(&L->cnt_attn, (size_t)L->max_seg * sizeof(int)));
-    TRY(cudaMemset(L->cnt_attn, 0, (size_t)L->max_seg * sizeof(int)));
     TRY(cudaMalloc(&L->status, sizeof(unsigned)));
     TRY(cudaMemset(L->status, 0, sizeof(unsigned)));
     std::vector<double> inv(L->rd / 2);
@@ -325,7 +332,7 @@ void gattn_layer_destroy(gattn_layer *L)
         return;
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_proj, L->ws_attn, L->cnt_qkv, L->cnt_o,
-                    L->cnt_attn, L->status,  L->inv_freq, L->q_norm, L->k_norm};
+                    L->status,  L->inv_freq, L->q_norm, L->k_norm};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -432,8 +439,9 @@ gattn_status gattn_layer_set_events(gattn_layer *L, void *const *events, int32_t
 {
     if (!L || n < 0 || (n > 0 && !events))
         return fail(GATTN_E_INVALID_ARG, "bad event arguments");
-    if (n != 0 && n != 5)
-        return fail(GATTN_E_INVALID_ARG, "need launches_per_step + 1 = 5 events");
+    if (n != 0 && n != kLaunchesPerStep + 1)
+        return fail(GATTN_E_INVALID_ARG, "need launches_per_step + 1 = %d events",
+                    kLaunchesPerStep + 1);
     L->events.assign(reinterpret_cast<cudaEvent_t const *>(events),
                      reinterpret_cast<cudaEvent_t const *>(events) + n);
     return GATTN_OK;
@@ -553,7 +561,8 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     t.nrb = nrb;
     t.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
     t.ws = L->ws_attn;
-    t.cnt = L->cnt_attn;
+    t.min_units = kAttnMinUnits;
+    t.grid = L->attn_grid;
     t.x16 = L->x16_o;
     t.xsum = L->xsum_o;
     t.NT = NT;
@@ -563,6 +572,9 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     const int MT = (max_rows + 15) / 16;
     CUDA_TRY(mark(2));
     CUDA_TRY(launch_attn(MT, c.head_dim / 64, t, kv->kmap, kv->vmap, L->attn_grid, pdl, s));
+    ++launches;
+    CUDA_TRY(mark(3));
+    CUDA_TRY(launch_attn_merge(t, max_rows, pdl, s));
     ++launches;
 
     // 4. o_proj
@@ -587,10 +599,10 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     e2.cache_pos = cache_pos;
     e2.cap = kv->desc.capacity;
     e2.out = static_cast<__nv_bfloat16 *>(out);
-    CUDA_TRY(mark(3));
+    CUDA_TRY(mark(4));
     CUDA_TRY(launch_proj(L->po.bits, NT, kModeO, o, eq, e2, L->po.grid[ni], pdl, s));
     ++launches;
-    CUDA_TRY(mark(4));
+    CUDA_TRY(mark(5));
     L->launches = launches;
     return GATTN_OK;
 }

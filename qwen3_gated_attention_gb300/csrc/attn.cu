@@ -90,7 +90,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gqa = a.H / a.Hk;
 
-    pdl_wait();
+    // Dependents (the merge) may launch at once.  Before waiting for the q|k|v
+    // projection this kernel only reads cache_pos and cache rows older than the
+    // step: the projection starts its dependents after its own wait, so every
+    // earlier kernel (which wrote those rows) has completed by then.
     pdl_launch_dependents();
 
     if (tid == 0) {
@@ -118,11 +121,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     __syncthreads();
 
-    // Ranges are cut over min(grid, units) CTAs so that every participating CTA
-    // owns at least one unit (the merge counts contributors by range); the
-    // remaining CTAs have nothing to do.
+    // Ranges are cut over attn_ranges(T) CTAs, each owning at least min_units
+    // units (the merge kernel counts contributors by range); the remaining CTAs
+    // have nothing to do.
     const long long T = prefix[a.B], c = blockIdx.x;
-    const long long G = T < (long long)gridDim.x ? (T > 0 ? T : 1) : (long long)gridDim.x;
+    const long long G = attn_ranges(T, gridDim.x, a.min_units);
     const long long beg = c < G ? sk_start(c, T, G) : T, end = c < G ? sk_start(c + 1, T, G) : T;
     volatile int *abort = flags;
 
@@ -133,11 +136,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             prefetch_tensormap(&vmap);
             const uint64_t pol = l2_evict_first_policy();
             long long it = 0;
-            bool stop = false;
+            bool stop = false, waited = false;
             for (long long pos = beg; pos < end && !stop;) {
                 const Piece p = find_piece(prefix, ub, a.B, a.Hk, a.nrb, pos, end);
+                const int p0 = a.cache_pos[p.b];
                 for (int u = p.u0; u < p.u1; u += kAttnTile / kAttnUnit, ++it) {
                     const int nun = min(kAttnTile / kAttnUnit, p.u1 - u);
+                    // tiles that hold this step's new rows load after the projection
+                    if (!waited && (it >= kAttnStages || (u + nun) * kAttnUnit > p0)) {
+                        pdl_wait();
+                        waited = true;
+                    }
                     const int slot = (int)(it % kAttnStages);
                     const uint32_t ph = (uint32_t)((it / kAttnStages) & 1);
                     if (!mbar_wait(&empty[slot], ph ^ 1u, abort, a.status)) {
@@ -160,6 +169,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 pos = p.seg_start + p.u1;
             }
+            if (!waited)
+                pdl_wait();
             const long long first = it > kAttnStages ? it - kAttnStages : 0;
             for (long long i = first; i < it; ++i) {
                 unsigned long long t0 = global_ns();
@@ -172,6 +183,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
 
     // --------------------------------------------------------------- consumers
+    pdl_wait();                 // q rows come from the q|k|v projection
     const int g = lane >> 2, cq = lane & 3;
     const int NT = a.NT, MP = 8 * NT;
     const int Ktot = a.H * D;
@@ -356,9 +368,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mbar_arrive(&empty[slot]);
         }
 
-        // ---- partial (m, l, O) of this piece into slot seg + c
-        const int HB = 64;
-        float *part = a.ws + (p.seg + c) * (long long)(2 * HB + HB * D);
+        // ---- partial (m, l, O) of this piece into slot seg + c (valid rows only);
+        //      a separate merge kernel combines the slots of each segment
+        float *part = a.ws + (p.seg + c) * (long long)attn_slot_floats(D);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -375,10 +387,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int j = 0; j < DB; ++j) {
                 const int col = (warp * DB + j) * 8 + 2 * cq;
                 const int r0 = mt * 16 + g;
-                *reinterpret_cast<float2 *>(part + 2 * HB + (long long)r0 * D + col) =
-                    make_float2(O[mt][j][0], O[mt][j][1]);
-                *reinterpret_cast<float2 *>(part + 2 * HB + (long long)(r0 + 8) * D + col) =
-                    make_float2(O[mt][j][2], O[mt][j][3]);
+                if (r0 < nrows)
+                    *reinterpret_cast<float2 *>(part + 2 * kAttnMaxRows + (long long)r0 * D + col) =
+                        make_float2(O[mt][j][0], O[mt][j][1]);
+                if (r0 + 8 < nrows)
+                    *reinterpret_cast<float2 *>(part + 2 * kAttnMaxRows + (long long)(r0 + 8) * D +
+                                                col) = make_float2(O[mt][j][2], O[mt][j][3]);
             }
         named_bar_sync(1, kAttnWarps * 32);
         if (warp == 0 && cq == 0) {
@@ -392,102 +406,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int w2 = 0; w2 < kAttnWarps; ++w2)
                         l += red_l[w2 * 64 + i];
                     part[i] = m_run[mt][hr];
-                    part[HB + i] = l;
+                    part[kAttnMaxRows + i] = l;
                 }
         }
-        __threadfence();
+        // red_l is reused by the next piece: keep warp 0's reads before new writes
         named_bar_sync(1, kAttnWarps * 32);
-        if (tid == 0) {
-            const long long cf = sk_owner(p.seg_start, T, G);
-            const long long cl = sk_owner(p.seg_end - 1, T, G);
-            const int old = atomicAdd(&a.cnt[p.seg], 1);
-            flags[1] = (old == (int)(cl - cf));
-        }
-        named_bar_sync(1, kAttnWarps * 32);
-
-        if (flags[1]) {
-            // ---- merge the partials of this segment, gate, write the o_proj operand
-            __threadfence();
-            const long long cf = sk_owner(p.seg_start, T, G);
-            const long long cl = sk_owner(p.seg_end - 1, T, G);
-            const int row = tid >> 2, qd = tid & 3;
-            const int QW = D / 4;                       // elements per thread
-            const bool live = row < nrows;
-            const int hl = live ? row / a.R : 0, r = live ? row % a.R : 0;
-            const int h = h0 + hl, m = p.b * a.R + r;
-            float M = -INFINITY;
-            for (long long j = cf; j <= cl; ++j) {
-                const float *pj = a.ws + (p.seg + j) * (long long)(2 * HB + HB * D);
-                M = fmaxf(M, __ldcg(pj + row));
-            }
-            float wsum = 0.f;
-            float acc[64];
-#pragma unroll
-            for (int e = 0; e < 64; ++e)
-                acc[e] = 0.f;
-            for (long long j = cf; j <= cl; ++j) {
-                const float *pj = a.ws + (p.seg + j) * (long long)(2 * HB + HB * D);
-                const float mj = __ldcg(pj + row);
-                const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-                wsum += wj * __ldcg(pj + HB + row);
-                const float4 *src =
-                    reinterpret_cast<const float4 *>(pj + 2 * HB + (long long)row * D + qd * QW);
-#pragma unroll
-                for (int e4 = 0; e4 < 16; ++e4) {
-                    if (e4 * 4 < QW) {
-                        const float4 v = __ldcg(src + e4);
-                        acc[4 * e4] += wj * v.x;
-                        acc[4 * e4 + 1] += wj * v.y;
-                        acc[4 * e4 + 2] += wj * v.z;
-                        acc[4 * e4 + 3] += wj * v.w;
-                    }
-                }
-            }
-            const float inv = live && wsum > 0.f ? 1.f / wsum : 0.f;
-            const int gs = a.group_o;
-            float gsum = 0.f;
-#pragma unroll
-            for (int e = 0; e < 64; ++e) {
-                if (e < QW) {
-                    const int jd = qd * QW + e;
-                    const float o = acc[e] * inv;
-                    float gated = 0.f;
-                    if (live) {
-                        const float gt = a.gate[(long long)m * Ktot + h * D + jd];
-                        gated = o * (1.f / (1.f + __expf(-gt)));
-                        if (a.tap_attn)
-                            a.tap_attn[(long long)m * Ktot + h * D + jd] = o;
-                    }
-                    const __half hv = __float2half_rn(gated);
-                    if (live)
-                        a.x16[x16_offset(m, h * D + jd, NT)] = hv;
-                    gsum += __half2float(hv);
-                    if (gs < QW && ((jd + 1) % gs) == 0) {
-                        if (live) {
-                            const int k0 = h * D + jd + 1 - gs;
-                            a.xsum[((long long)(k0 >> 7) * (kKU / gs) + ((k0 & 127) / gs)) * MP + m] =
-                                gsum;
-                        }
-                        gsum = 0.f;
-                    }
-                }
-            }
-            if (gs >= QW) {
-                // a group spans gs/QW consecutive quarters of this row
-                const int span = gs / QW;
-                if (span >= 2)
-                    gsum += __shfl_xor_sync(0xffffffffu, gsum, 1);
-                if (span >= 4)
-                    gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
-                if (live && (qd % span) == 0) {
-                    const int k0 = h * D + qd * QW;
-                    a.xsum[((long long)(k0 >> 7) * (kKU / gs) + ((k0 & 127) / gs)) * MP + m] = gsum;
-                }
-            }
-            named_bar_sync(1, kAttnWarps * 32);
-            if (tid == 0)
-                a.cnt[p.seg] = 0;
-        }
         pos = p.seg_start + p.u1;
     }
 }

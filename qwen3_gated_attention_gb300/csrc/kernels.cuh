@@ -128,6 +128,19 @@ constexpr int kAttnUnit = 16;          // tokens per stream-K unit
 constexpr int kAttnTile = 64;          // tokens per pipeline stage
 constexpr int kAttnStages = 2;
 constexpr int kMaxRowBlocks = 64;
+constexpr int kAttnMaxRows = 64;       // query rows per segment
+
+// floats per attention partial slot: m[64], l[64], O[64][d]
+__host__ __device__ inline int attn_slot_floats(int d) { return 2 * kAttnMaxRows + kAttnMaxRows * d; }
+
+// CTAs the attention units are cut over: at most the grid, at least min_units
+// units per CTA, at least one CTA.
+__host__ __device__ inline long long attn_ranges(long long T, long long grid, int min_units)
+{
+    long long g = (T + min_units - 1) / min_units;
+    g = g < grid ? g : grid;
+    return g > 0 ? g : 1;
+}
 
 struct AttnArgs {
     const __nv_bfloat16 *qn;     // [B][R][H][d]
@@ -138,8 +151,9 @@ struct AttnArgs {
     int rb_h0[kMaxRowBlocks];    // first head of each row block (relative to the group)
     int rb_nh[kMaxRowBlocks];    // heads of each row block
     float scale_log2;            // log2(e) / sqrt(d)
-    float *ws;                   // partials [slot][64 rows][d + 2]
-    int *cnt;                    // per segment
+    int min_units;               // minimum 16-token units per attention CTA
+    int grid;                    // attention grid size (the merge recomputes the ranges)
+    float *ws;                   // partials, attn_slot_floats(d) per slot
     // o_proj operand
     __half *x16;
     float *xsum;
@@ -150,6 +164,8 @@ struct AttnArgs {
 
 cudaError_t launch_attn(int MT, int DB, const AttnArgs &a, const CUtensorMap &kmap,
                         const CUtensorMap &vmap, int grid, bool pdl, cudaStream_t s);
+// merge of the attention partials + output gate -> o_proj operand
+cudaError_t launch_attn_merge(const AttnArgs &a, int max_rows, bool pdl, cudaStream_t s);
 int attn_smem_bytes(int MT, int DB);
 cudaError_t attn_set_smem_limits();
 

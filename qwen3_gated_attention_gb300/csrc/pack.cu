@@ -205,8 +205,9 @@ cudaError_t launch_unpack_codes(const uint32_t *packed, long long N, long long K
 __global__ void __launch_bounds__(256) xprep_kernel(const void *x, int x_dtype, int M, int K,
                                                     int group, int NT, __half *x16, float *xsum)
 {
-    pdl_wait();
+    // the next kernel (the q|k|v projection) may start streaming weights at once
     pdl_launch_dependents();
+    pdl_wait();
     const int ku = blockIdx.x;
     const int m = threadIdx.x >> 3, part = threadIdx.x & 7;
     const int MP = 8 * NT;

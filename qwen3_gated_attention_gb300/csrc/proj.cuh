@@ -136,141 +136,204 @@ __device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, in
     }
 }
 
-// Final value of row n (global), column m, summed over the row block's partials.
-__device__ __forceinline__ float proj_final(const ProjArgs &a, int MP, int n, int m)
+// Statics an epilogue needs, staged in shared memory before the main loop so
+// the epilogue itself has no dependent global round trips besides the partials.
+struct EpiSmem {
+    float *vals;        // [8][eb_rows] final values of up to 8 columns
+    float *nq, *nk;     // q_norm / k_norm as fp32 [d]
+    double *invf;       // inv_freq [rd/2]
+    int *cpos;          // cache_pos [B]
+};
+
+// Phase 1 of an epilogue: the final value of every row of epilogue block eb
+// for columns m0 .. m0+mc-1, i.e. the sum of the partials of every CTA whose
+// range touched the row's block, into vals[mm][row].  One row per thread.
+template <int MP>
+__device__ __forceinline__ void gather_block(const ProjArgs &a, int eb, int m0, int mc, int tid,
+                                             float *vals)
 {
     const long long G = gridDim.x;
-    const int rb = n / kRBR, rr = n % kRBR;
-    const long long s0 = (long long)rb * a.nku, s1 = s0 + a.nku - 1;
-    const long long cf = sk_owner(s0, a.T, G), cl = sk_owner(s1, a.T, G);
-    float v = 0.f;
-    for (long long j = 0; j <= cl - cf; ++j) {
-        const float *p = a.ws + ((long long)rb + cf + j) * MP * kRBR;
-        v += __ldcg(p + (long long)m * kRBR + rr);
-        if (a.xsplit)
-            v += __ldcg(p + (long long)(m + a.xsplit) * kRBR + rr);
+    const int rb0 = eb * a.eb_rows / kRBR, nrbs = a.eb_rows / kRBR;
+    for (int q = 0; q < nrbs; ++q) {
+        const int rb = rb0 + q;
+        if (rb >= a.nrb)
+            break;
+        const long long s0 = (long long)rb * a.nku;
+        const long long cf = sk_owner(s0, a.T, G), cl = sk_owner(s0 + a.nku - 1, a.T, G);
+        const float *p0 = a.ws + ((long long)rb + cf) * MP * kRBR + tid;
+        float acc[8];
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm)
+            acc[mm] = 0.f;
+        const int n = (int)(cl - cf + 1);
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+            const float *p = p0 + (long long)j * MP * kRBR;
+#pragma unroll
+            for (int mm = 0; mm < 8; ++mm) {
+                if (mm < mc) {
+                    acc[mm] += __ldcg(p + (long long)(m0 + mm) * kRBR);
+                    if (a.xsplit)
+                        acc[mm] += __ldcg(p + (long long)(m0 + mm + a.xsplit) * kRBR);
+                }
+            }
+        }
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm)
+            if (mm < mc)
+                vals[mm * a.eb_rows + q * kRBR + tid] = acc[mm];
     }
-    return v;
 }
 
-// qkv epilogue for one epilogue block: every (head, column) pair is one warp's job.
-static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, int MP, int eb, int warp,
-                             int lane, float *wbuf)
+// qkv epilogue for one epilogue block (whole heads): per (head, column) one
+// warp splits query / gate / k / v, applies RMSNorm + partial RoPE to query
+// and k, and writes q (bf16), the gate (fp32) and the new cache rows (bf16).
+template <int MP>
+static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const EpiSmem &sm, int eb,
+                                    int warp, int lane, int tid)
 {
     const int d = e.d, half = e.rd >> 1, heads = a.eb_rows / d, per = d >> 5;
     const int Ny = e.Nq + 2 * e.Nkv;
-    for (int job = warp; job < heads * a.M; job += kWR) {
-        const int hb = job / a.M, m = job % a.M;
-        const int n0 = eb * a.eb_rows + hb * d;
-        if (n0 >= a.N)
-            continue;
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (i < per)
-                v[i] = proj_final(a, MP, n0 + lane + 32 * i, m);
-        if (e.tap_y) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i < per)
-                    e.tap_y[(long long)m * Ny + n0 + lane + 32 * i] = v[i];
-        }
-        const int b = m / e.R, r = m % e.R;
-        const int p0 = e.cache_pos[b];
-        const bool valid = p0 >= 0 && p0 + e.R <= e.cap;
-        int kind, head;    // 0 query, 1 gate, 2 k, 3 v
-        if (n0 < e.Nq) {
-            head = n0 / (2 * d);
-            kind = ((n0 % (2 * d)) >= d) ? 1 : 0;
-        } else if (n0 < e.Nq + e.Nkv) {
-            head = (n0 - e.Nq) / d;
-            kind = 2;
-        } else {
-            head = (n0 - e.Nq - e.Nkv) / d;
-            kind = 3;
-        }
-        if (kind == 1) {
+    for (int m0 = 0; m0 < a.M; m0 += 8) {
+        const int mc = min(8, a.M - m0);
+        gather_block<MP>(a, eb, m0, mc, tid, sm.vals);
+        named_bar_sync(1, kWR * 32);
+        for (int job = warp; job < heads * mc; job += kWR) {
+            const int hb = job / mc, mm = job % mc, m = m0 + mm;
+            const int n0 = eb * a.eb_rows + hb * d;
+            if (n0 >= a.N)
+                continue;
+            const float *hv = sm.vals + mm * a.eb_rows + hb * d;
+            float v[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                if (i < per)
-                    e.gate[(long long)m * e.H * d + head * d + lane + 32 * i] = v[i];
-            continue;
-        }
-        if (kind == 0 || kind == 2) {
-            // RMSNorm over the head: x / sqrt(mean(x^2) + eps) * w
-            float ss = 0.f;
+                v[i] = i < per ? hv[lane + 32 * i] : 0.f;
+            if (e.tap_y) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i < per)
+                for (int i = 0; i < 8; ++i)
+                    if (i < per)
+                        e.tap_y[(long long)m * Ny + n0 + lane + 32 * i] = v[i];
+            }
+            const int b = m / e.R, r = m % e.R;
+            const int p0 = sm.cpos[b];
+            const bool valid = p0 >= 0 && p0 + e.R <= e.cap;
+            int kind, head;    // 0 query, 1 gate, 2 k, 3 v
+            if (n0 < e.Nq) {
+                head = n0 / (2 * d);
+                kind = ((n0 % (2 * d)) >= d) ? 1 : 0;
+            } else if (n0 < e.Nq + e.Nkv) {
+                head = (n0 - e.Nq) / d;
+                kind = 2;
+            } else {
+                head = (n0 - e.Nq - e.Nkv) / d;
+                kind = 3;
+            }
+            if (kind == 1) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i < per)
+                        e.gate[(long long)m * e.H * d + head * d + lane + 32 * i] = v[i];
+                continue;
+            }
+            if (kind == 0 || kind == 2) {
+                // RMSNorm over the head: x / sqrt(mean(x^2) + eps) * w
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
                     ss = fmaf(v[i], v[i], ss);
 #pragma unroll
-            for (int o = 16; o; o >>= 1)
-                ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float inv = rsqrtf(ss / (float)d + e.eps);
-            const uint16_t *nw = kind == 0 ? e.q_norm : e.k_norm;
+                for (int o = 16; o; o >>= 1)
+                    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float inv = rsqrtf(ss / (float)d + e.eps);
+                const float *nw = kind == 0 ? sm.nq : sm.nk;
+                // partial rotary on dims [0, rd): pairs (j, j + rd/2) at position p0 + r
+                const double pos = (double)(p0 + r);
+                float o[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i < per)
-                    v[i] = v[i] * inv * __uint_as_float((uint32_t)nw[lane + 32 * i] << 16);
-            // partial rotary on dims [0, rd): pairs (i, i + rd/2) at position p0 + r
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i < per)
-                    wbuf[lane + 32 * i] = v[i];
-            __syncwarp();
-            const double pos = (double)(p0 + r);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = lane + 32 * i;
-                if (i < per && j < e.rd) {
-                    const int fi = j < half ? j : j - half;
-                    const double ang = pos * e.inv_freq[fi];
-                    const double turns = rint(ang * 0.15915494309189535);
-                    const float red = (float)fma(-turns, 6.283185307179586, ang);
-                    float sn, cs;
-                    sincosf(red, &sn, &cs);
-                    if (j < half)
-                        v[i] = v[i] * cs - wbuf[j + half] * sn;
-                    else
-                        v[i] = v[i] * cs + wbuf[j - half] * sn;
+                for (int i = 0; i < 8; ++i) {
+                    const int j = lane + 32 * i;
+                    o[i] = v[i] * inv * nw[j];
+                    if (i < per && j < e.rd) {
+                        const int fi = j < half ? j : j - half;
+                        const int jp = j < half ? j + half : j - half;
+                        const float partner = hv[jp] * inv * nw[jp];
+                        const double ang = pos * sm.invf[fi];
+                        const double turns = rint(ang * 0.15915494309189535);
+                        const float red = (float)fma(-turns, 6.283185307179586, ang);
+                        float sn, cs;
+                        sincosf(red, &sn, &cs);
+                        o[i] = j < half ? o[i] * cs - partner * sn : o[i] * cs + partner * sn;
+                    }
                 }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[i] = o[i];
             }
-            __syncwarp();
-        }
-        if (kind == 0) {
-            __nv_bfloat16 *q = e.qn + (((long long)b * e.R + r) * e.H + head) * d;
+            if (kind == 0) {
+                __nv_bfloat16 *q = e.qn + (((long long)b * e.R + r) * e.H + head) * d;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i < per)
+                        q[lane + 32 * i] = __float2bfloat16_rn(v[i]);
+                continue;
+            }
+            if (!valid) {
+                if (lane == 0)
+                    atomicOr(a.status, kStatusRange);
+                continue;
+            }
+            __nv_bfloat16 *dst = (kind == 2 ? e.kc : e.vc) + (long long)b * e.st_batch +
+                                 (long long)head * e.st_head + (long long)(p0 + r) * e.st_tok;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 if (i < per)
-                    q[lane + 32 * i] = __float2bfloat16_rn(v[i]);
-            continue;
+                    dst[lane + 32 * i] = __float2bfloat16_rn(v[i]);
         }
-        if (!valid) {
-            if (lane == 0)
-                atomicOr(a.status, kStatusRange);
-            continue;
-        }
-        __nv_bfloat16 *dst = (kind == 2 ? e.kc : e.vc) + (long long)b * e.st_batch +
-                             (long long)head * e.st_head + (long long)(p0 + r) * e.st_tok;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (i < per)
-                dst[lane + 32 * i] = __float2bfloat16_rn(v[i]);
+        named_bar_sync(1, kWR * 32);
     }
 }
 
-static __device__ void epilogue_o(const ProjArgs &a, const EpiO &e, int MP, int eb, int tid)
+// o_proj epilogue: final bf16 outputs of one row block, one row per thread.
+template <int MP>
+static __device__ void epilogue_o(const ProjArgs &a, const EpiO &e, const EpiSmem &sm, int eb,
+                                  int tid)
 {
     const int n = eb * a.eb_rows + tid;     // eb_rows == kRBR, one row per thread
     if (tid >= a.eb_rows || n >= a.N)
         return;
-    for (int m = 0; m < a.M; ++m) {
-        const int b = m / e.R;
-        const int p0 = e.cache_pos[b];
-        const bool valid = p0 >= 0 && p0 + e.R <= e.cap;
-        const float v = valid ? proj_final(a, MP, n, m) : 0.f;
-        e.out[(long long)m * a.N + n] = __float2bfloat16_rn(v);
+    const long long G = gridDim.x;
+    const int rb = n / kRBR, rr = n % kRBR;
+    const long long s0 = (long long)rb * a.nku;
+    const long long cf = sk_owner(s0, a.T, G), cl = sk_owner(s0 + a.nku - 1, a.T, G);
+    const float *p0 = a.ws + ((long long)rb + cf) * MP * kRBR + rr;
+    float acc[MP];
+#pragma unroll
+    for (int m = 0; m < MP; ++m)
+        acc[m] = 0.f;
+    const int nc = (int)(cl - cf + 1);
+#pragma unroll 4
+    for (int j = 0; j < nc; ++j) {
+        const float *p = p0 + (long long)j * MP * kRBR;
+#pragma unroll
+        for (int m = 0; m < MP; ++m)
+            if (m < a.M)
+                acc[m] += __ldcg(p + (long long)m * kRBR);
     }
+#pragma unroll
+    for (int m = 0; m < MP; ++m) {
+        if (m < a.M) {
+            const int b = m / e.R;
+            const int pb = sm.cpos[b];
+            const bool valid = pb >= 0 && pb + e.R <= e.cap;
+            e.out[(long long)m * a.N + n] = __float2bfloat16_rn(valid ? acc[m] : 0.f);
+        }
+    }
+}
+
+// shared memory past the stage ring: barriers, flags, epilogue statics
+__host__ __device__ inline int proj_tail_bytes(int eb_rows)
+{
+    return 256 + 8 * eb_rows * 4 + 2 * 256 * 4 + 128 * 8 + 32 * 4;
 }
 
 template <int BITS, int NT, int MODE>
@@ -281,10 +344,16 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
     constexpr int MP = 8 * NT;
     const int S = a.stages;
     uint8_t *stages = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * a.stage_bytes);
-    uint64_t *empty = full + S;
-    int *flags = reinterpret_cast<int *>(empty + S);      // [0] abort, [1] last arrival
-    float *wbuf = reinterpret_cast<float *>(flags + 4);    // kWR x 256 floats
+    uint8_t *tail = smem + (size_t)S * a.stage_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(tail);             // [S <= 8]
+    uint64_t *empty = full + 8;                                       // [8]
+    int *flags = reinterpret_cast<int *>(tail + 128);                 // [0] abort, [1] last arrival
+    EpiSmem sm;
+    sm.vals = reinterpret_cast<float *>(tail + 256);
+    sm.nq = sm.vals + 8 * a.eb_rows;
+    sm.nk = sm.nq + 256;
+    sm.invf = reinterpret_cast<double *>(sm.nk + 256);
+    sm.cpos = reinterpret_cast<int *>(sm.invf + 128);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -295,6 +364,27 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
         flags[0] = 0;
         flags[1] = 0;
         fence_mbar_init();
+    }
+    // o_proj lets the next step's kernels launch at once: their pre-wait work
+    // (weight streaming) reads nothing this kernel writes
+    if constexpr (MODE == kModeO)
+        pdl_launch_dependents();
+    // epilogue statics: layer weights and the step's cache_pos (a step input)
+    if (threadIdx.x < kWR * 32) {
+        const int t = threadIdx.x;
+        if constexpr (MODE == kModeQKV) {
+            for (int j = t; j < eq.d; j += kWR * 32) {
+                sm.nq[j] = __uint_as_float((uint32_t)eq.q_norm[j] << 16);
+                sm.nk[j] = __uint_as_float((uint32_t)eq.k_norm[j] << 16);
+            }
+            for (int j = t; j < eq.rd / 2; j += kWR * 32)
+                sm.invf[j] = eq.inv_freq[j];
+            if (t < a.M / eq.R + (a.M % eq.R != 0))
+                sm.cpos[t] = eq.cache_pos[t];
+        } else {
+            if (t < a.M / eo.R + (a.M % eo.R != 0))
+                sm.cpos[t] = eo.cache_pos[t];
+        }
     }
     __syncthreads();
 
@@ -357,7 +447,10 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
 
     // ------------------------------------------------------------- consumers
     pdl_wait();
-    pdl_launch_dependents();
+    // q|k|v: dependents (attention) may launch only once the previous kernels
+    // have completed, so that attention can prefetch cache rows before waiting
+    if constexpr (MODE == kModeQKV)
+        pdl_launch_dependents();
     const int tid = threadIdx.x;           // 0 .. kWR*32-1
     const int g = lane >> 2, cq = lane & 3;
     float Y[2][NT][4];
@@ -382,10 +475,8 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
             mbar_arrive(&empty[slot]);
 
         if (ku == a.nku - 1 || s == end - 1) {
-            // partial of this row block: [MP][kRBR] floats in slot rb + first + j
-            const long long s0 = (long long)rb * a.nku;
-            const long long cf = sk_owner(s0, a.T, G);
-            float *p = a.ws + ((long long)rb + c) * MP * kRBR;    // rb + cf + (c - cf)
+            // partial of this row block: [MP][kRBR] floats in slot rb + c
+            float *p = a.ws + ((long long)rb + c) * MP * kRBR;
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -399,11 +490,10 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
                     for (int i = 0; i < 4; ++i)
                         Y[mt][nt][i] = 0.f;
                 }
-            (void)cf;
-            __threadfence();
             named_bar_sync(1, kWR * 32);
             const int eb = rb * kRBR / a.eb_rows;
             if (tid == 0) {
+                __threadfence();   // publishes the CTA's partial (ordered by the barrier)
                 int total = 0;
                 const int rb0 = eb * a.eb_rows / kRBR, rb1 = rb0 + a.eb_rows / kRBR;
                 for (int q = rb0; q < rb1 && q < a.nrb; ++q) {
@@ -412,14 +502,15 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
                 }
                 const int old = atomicAdd(&a.cnt[eb], 1);
                 flags[1] = (old == total - 1);
+                if (flags[1])
+                    __threadfence();
             }
             named_bar_sync(1, kWR * 32);
             if (flags[1]) {
-                __threadfence();
                 if constexpr (MODE == kModeQKV)
-                    epilogue_qkv(a, eq, MP, eb, warp, lane, wbuf + warp * 256);
+                    epilogue_qkv<MP>(a, eq, sm, eb, warp, lane, tid);
                 else
-                    epilogue_o(a, eo, MP, eb, tid);
+                    epilogue_o<MP>(a, eo, sm, eb, tid);
                 named_bar_sync(1, kWR * 32);
                 if (tid == 0)
                     a.cnt[eb] = 0;

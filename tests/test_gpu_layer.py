@@ -123,8 +123,11 @@ def test_head_chunk_route_agrees_with_unchunked(name):
     ref = oracle_run(case)
     check_parity(case, on, ref, what="chunked")
     check_parity(case, off, ref, what="unchunked")
-    # the two routes differ only in how heads are grouped per CTA
-    np.testing.assert_allclose(on["attn"], off["attn"], rtol=2e-3, atol=2e-4)
+    # the two routes differ only in how heads are grouped per CTA, hence in how
+    # the keys are cut into pieces: P is rounded to bf16 against different
+    # running maxima, so agreement is to bf16 level (~1e-3), not bitwise
+    ok, rep = refs.close(on["attn"], off["attn"], abs_tol=1e-3, rel_tol=1e-2, l2_tol=2e-3)
+    assert ok, rep
     assert np.array_equal(on["y"], off["y"])
     assert np.array_equal(on["k"], off["k"]) and np.array_equal(on["v"], off["v"])
 
@@ -199,7 +202,8 @@ def test_capacity_overflow_is_reported_and_skipped():
     assert np.all(o[1] == 0.0)
     assert np.array_equal(k[1], case.ck[1]) and np.array_equal(v[1], case.cv[1])
     for b in (0, 2):
-        assert np.array_equal(o[b], good["out"][b].astype(np.float32))
+        ok, rep = refs.close(o[b], good["out"][b])
+        assert ok, rep
         assert np.array_equal(k[b], good["k"][b])
 
 
