@@ -110,23 +110,27 @@ gattn_status validate(const gattn_cfg *c)
 
 struct ProjPlan {
     int N = 0, K = 0, bits = 0, group = 0, nrb = 0, nku = 0, ubytes = 0, step_bytes = 0;
-    int stage_bytes[3] = {0, 0, 0}, stages[3] = {0, 0, 0}, grid[3] = {0, 0, 0};  // per NT index
+    int rbc = 1;                              // row blocks per cluster (whole heads for q|k|v)
+    int stage_bytes[3] = {0, 0, 0}, stages[3] = {0, 0, 0};  // per NT index
+    int ks[3] = {1, 1, 1}, grid[3] = {0, 0, 0};
     uint8_t *w = nullptr;
 };
 
 int nt_index(int NT) { return NT == 1 ? 0 : (NT == 2 ? 1 : 2); }
 
 constexpr int kLaunchesPerStep = 5;  // xprep, q|k|v projection, attention, merge, o_proj
-constexpr int kProjMinSteps = 4;     // k units per projection CTA, at least
 constexpr int kAttnMinUnits = 4;     // 16-token units per attention CTA, at least
+constexpr int kMaxCluster = 8;       // portable cluster size
 
-void plan_proj(ProjPlan &p, int N, int K, int bits, int group)
+void plan_proj(ProjPlan &p, int N, int K, int bits, int group, int rbc)
 {
     p.N = N;
     p.K = K;
     p.bits = bits;
     p.group = group;
+    p.rbc = rbc;
     p.nrb = (N + kRBR - 1) / kRBR;
+    p.nrb = (p.nrb + rbc - 1) / rbc * rbc;    // whole clusters (padding rows are zero)
     p.nku = K / kKU;
     p.ubytes = unit_bytes(bits, group);
     p.step_bytes = kWR * p.ubytes;
@@ -136,16 +140,16 @@ void plan_proj(ProjPlan &p, int N, int K, int bits, int group)
         int sbytes = p.step_bytes + xb + sb;
         sbytes = (sbytes + 127) & ~127;
         p.stage_bytes[i] = sbytes;
-        int st = (96 * 1024) / sbytes;
+        // a small ring per CTA so that three or four CTAs (12-16 consumer warps)
+        // share an SM: the stage loop is latency bound, not bandwidth bound
+        int st = (48 * 1024) / sbytes;
         if (st < 2) st = 2;
         if (st > 8) st = 8;
+        // the drained ring holds the CTA's partial sums [8*NT][kRBR] floats
+        while (st * sbytes < 8 * NT * kRBR * 4 && st < 8)
+            ++st;
         p.stages[i] = st;
     }
-}
-
-int proj_smem_for(const ProjPlan &p, int i)
-{
-    return p.stages[i] * p.stage_bytes[i] + 2 * p.stages[i] * 8 + 16 + kWR * 256 * 4;
 }
 
 }  // namespace
@@ -161,12 +165,11 @@ struct gattn_layer {
     float *xsum_a = nullptr, *xsum_o = nullptr;
     __nv_bfloat16 *qn = nullptr;
     float *gate = nullptr;
-    float *ws_proj = nullptr, *ws_attn = nullptr;
-    int *cnt_qkv = nullptr, *cnt_o = nullptr;
+    float *ws_attn = nullptr;
     unsigned *status = nullptr;
     double *inv_freq = nullptr;
     uint16_t *q_norm = nullptr, *k_norm = nullptr;
-    size_t ws_proj_floats = 0, ws_attn_floats = 0;
+    size_t ws_attn_floats = 0;
     int attn_grid = 0;
     int max_seg = 0;
     gattn_taps taps{};
@@ -250,8 +253,10 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaGetDevice(&L->device));
     TRY(cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device));
 
-    plan_proj(L->pqkv, L->Nq + 2 * L->Nkv, c.hidden, proj_bits(c, 0), proj_group(c, 0));
-    plan_proj(L->po, c.hidden, L->Ko, proj_bits(c, 3), proj_group(c, 3));
+    // a q|k|v cluster covers whole heads (RMSNorm needs every row of a head)
+    plan_proj(L->pqkv, L->Nq + 2 * L->Nkv, c.hidden, proj_bits(c, 0), proj_group(c, 0),
+              std::max(1, c.head_dim / kRBR));
+    plan_proj(L->po, c.hidden, L->Ko, proj_bits(c, 3), proj_group(c, 3), 1);
 
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -270,19 +275,23 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
             ProjArgs a{};
             a.stages = p->stages[i];
             a.stage_bytes = p->stage_bytes[i];
-            a.eb_rows = p == &L->pqkv ? std::max(kRBR, c.head_dim) : kRBR;
+            a.eb_rows = p->rbc * kRBR;
             const int smem = proj_smem_bytes(a);
             int occ = 0;
-            TRY(proj_occupancy(p->bits, 1 << i, p == &L->pqkv ? kModeQKV : kModeO, smem, &occ));
+            TRY(proj_occupancy(p->bits, 1 << i, p == &L->pqkv ? kModeQKV : kModeO, p->group, smem,
+                               &occ));
             if (occ < 1)
                 occ = 1;
-            // at most one CTA per resident slot, and at least kProjMinSteps k units
-            // per CTA so that each row block has few partials to merge
-            const long long T = (long long)p->nrb * p->nku;
-            long long gsz = (long long)L->num_sms * occ;
-            const long long by_work = std::max<long long>(1, T / kProjMinSteps);
-            gsz = std::min(gsz, by_work);
-            p->grid[i] = (int)(T < gsz ? T : gsz);
+            // split K over as many CTAs as a cluster allows while every CTA of
+            // the grid stays resident (one wave)
+            const long long capacity = (long long)L->num_sms * occ;
+            const int nclusters = p->nrb / p->rbc;
+            int ks = 1;
+            while (ks * 2 * p->rbc <= kMaxCluster && ks * 2 <= p->nku &&
+                   (long long)nclusters * p->rbc * ks * 2 <= capacity)
+                ks *= 2;
+            p->ks[i] = ks;
+            p->grid[i] = nclusters * p->rbc * ks;
         }
     }
     L->attn_grid = L->num_sms;
@@ -299,15 +308,6 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaMemset(L->xsum_o, 0, nku_o * (kKU / L->po.group) * MP * sizeof(float)));
     TRY(cudaMalloc(&L->qn, (size_t)L->M_max * L->Ko * 2));
     TRY(cudaMalloc(&L->gate, (size_t)L->M_max * L->Ko * sizeof(float)));
-    int grid_max = 0;
-    for (int i = 0; i < 3; ++i)
-        grid_max = std::max(grid_max, std::max(L->pqkv.grid[i], L->po.grid[i]));
-    L->ws_proj_floats = (size_t)(std::max(L->pqkv.nrb, L->po.nrb) + grid_max + 1) * kRBR * MP;
-    TRY(cudaMalloc(&L->ws_proj, L->ws_proj_floats * sizeof(float)));
-    TRY(cudaMalloc(&L->cnt_qkv, (size_t)L->pqkv.nrb * sizeof(int)));
-    TRY(cudaMalloc(&L->cnt_o, (size_t)L->po.nrb * sizeof(int)));
-    TRY(cudaMemset(L->cnt_qkv, 0, (size_t)L->pqkv.nrb * sizeof(int)));
-    TRY(cudaMemset(L->cnt_o, 0, (size_t)L->po.nrb * sizeof(int)));
     // attention segments: batch x KV heads x row blocks (at most gqa row blocks)
     L->max_seg = c.max_batch * c.num_kv_heads * std::min(L->gqa, kMaxRowBlocks);
     L->ws_attn_floats = (size_t)(L->max_seg + L->attn_grid + 1) * attn_slot_floats(c.head_dim);
@@ -331,8 +331,8 @@ void gattn_layer_destroy(gattn_layer *L)
     if (!L)
         return;
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
-                    L->qn,     L->gate,      L->ws_proj, L->ws_attn, L->cnt_qkv, L->cnt_o,
-                    L->status,  L->inv_freq, L->q_norm, L->k_norm};
+                    L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq,
+                    L->q_norm, L->k_norm};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -495,10 +495,9 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     a.step_bytes = L->pqkv.step_bytes;
     a.stage_bytes = L->pqkv.stage_bytes[nia];
     a.stages = L->pqkv.stages[nia];
-    a.T = (long long)a.nrb * a.nku;
-    a.ws = L->ws_proj;
-    a.cnt = L->cnt_qkv;
-    a.eb_rows = std::max(kRBR, c.head_dim);
+    a.rbc = L->pqkv.rbc;
+    a.ks = L->pqkv.ks[nia];
+    a.eb_rows = a.rbc * kRBR;
     a.xsplit = c.x_dtype == GATTN_DTYPE_F32 ? M : 0;
     a.status = L->status;
     EpiQKV eq{};
@@ -590,8 +589,8 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     o.step_bytes = L->po.step_bytes;
     o.stage_bytes = L->po.stage_bytes[ni];
     o.stages = L->po.stages[ni];
-    o.T = (long long)o.nrb * o.nku;
-    o.cnt = L->cnt_o;
+    o.rbc = 1;
+    o.ks = L->po.ks[ni];
     o.eb_rows = kRBR;
     o.xsplit = 0;
     EpiO e2{};

@@ -245,14 +245,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 fence_proxy_async_smem();
             }
 
-            // ---- S = q K^T for this warp's 8 tokens
+            // ---- S = q K^T for this warp's 8 tokens; the head_dim contraction is
+            //      spread over SPLIT independent accumulator chains (MMA latency)
+            constexpr int SPLIT = MT >= 4 ? 1 : (MT >= 2 ? 2 : 4);
             float sc[MT][4];
+            float scs[SPLIT][MT][4];
             const bool has_tok = ok && (warp * 8 < ntok);
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int q = 0; q < SPLIT; ++q)
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    sc[mt][e] = 0.f;
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        scs[q][mt][e] = 0.f;
             if (has_tok) {
                 const int tok = warp * 8 + (lane & 7);
 #pragma unroll
@@ -270,11 +275,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             const int qch = 2 * ks + (lane >> 4);
                             uint32_t qa[4];
                             ldsm_x4(qa, smem_u32(qs + qrow * (D * 2) + ((qch ^ (qrow & 7)) << 4)));
-                            mma_bf16(sc[mt], qa, kb[2 * h], kb[2 * h + 1], sc[mt]);
+                            mma_bf16(scs[ks % SPLIT][mt], qa, kb[2 * h], kb[2 * h + 1],
+                                     scs[ks % SPLIT][mt]);
                         }
                     }
                 }
             }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float t = scs[0][mt][e];
+#pragma unroll
+                    for (int q = 1; q < SPLIT; ++q)
+                        t += scs[q][mt][e];
+                    sc[mt][e] = t;
+                }
             // ---- mask (causal per verify row), scale, warp row max
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {

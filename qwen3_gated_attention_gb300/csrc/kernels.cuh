@@ -51,6 +51,10 @@ __host__ __device__ inline long long x16_offset(int m, int k, int NT)
            (q & 1);
 }
 
+// One cluster computes one block of rows (whole heads for the q|k|v
+// projection) over all of K: its rbc row blocks times ks k-splits are the
+// cluster's CTAs (rank = row block * ks + split).  Partial sums are reduced
+// through distributed shared memory, so no global scratch is used.
 struct ProjArgs {
     const uint8_t *w;     // repacked weights
     const __half *x16;    // B-fragment-ordered x
@@ -60,10 +64,9 @@ struct ProjArgs {
     int M;                // valid x rows (columns of the product)
     int group;
     int unit_bytes, step_bytes, stage_bytes, stages;
-    long long T;          // nrb * nku stream-K units
-    float *ws;            // partial sums [slot][MP][kRBR]
-    int *cnt;             // arrival counters per epilogue block
-    int eb_rows;          // rows per epilogue block (multiple of kRBR)
+    int rbc;              // row blocks per cluster
+    int ks;               // k splits per row block (cluster size = rbc * ks)
+    int eb_rows;          // rows per cluster = rbc * kRBR
     int xsplit;           // > 0: column m + xsplit holds the low fp16 part of column m
     unsigned *status;
 };
@@ -99,7 +102,7 @@ cudaError_t launch_proj(int bits, int NT, int mode, const ProjArgs &a, const Epi
                         const EpiO &eo, int grid, bool pdl, cudaStream_t s);
 int proj_smem_bytes(const ProjArgs &a);
 cudaError_t proj_set_smem_limits(int bits, int NT, int mode, int bytes);
-cudaError_t proj_occupancy(int bits, int NT, int mode, int smem, int *blocks_per_sm);
+cudaError_t proj_occupancy(int bits, int NT, int mode, int group, int smem, int *blocks_per_sm);
 
 // fp32 x is split exactly into hi = fp16(x) (column m) and lo = fp16(x - hi)
 // (column M + m); bf16 x converts to fp16 exactly (finite, |x| < 65504).

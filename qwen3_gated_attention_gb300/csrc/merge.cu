@@ -73,28 +73,38 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a)
 #pragma unroll
     for (int cidx = 0; cidx < 32; ++cidx)
         acc[cidx] = 0.f;
-#pragma unroll 2
-    for (int j = lane; j < n; j += 32) {
-        const float *pj = base + (long long)j * slot_floats;
-        const float mj = __ldcg(pj + i);
-        const float lj = __ldcg(pj + kAttnMaxRows + i);
-        const float4 *src = reinterpret_cast<const float4 *>(pj + 2 * kAttnMaxRows +
-                                                             (long long)i * D + c0);
-        float4 v[8];
+    // contributors j and j + 32 are loaded together (one memory round trip for
+    // up to 64 contributors), then folded
+    for (int j0 = lane; j0 < n; j0 += 64) {
+        float mj[2], lj[2];
+        float4 v[2][8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            v[q] = __ldcg(src + q);
-        const float mnew = fmaxf(mloc, mj);
-        const float sa = (mloc == -INFINITY) ? 0.f : exp2f(mloc - mnew);
-        const float sb = (mj == -INFINITY) ? 0.f : exp2f(mj - mnew);
-        mloc = mnew;
-        lloc = lloc * sa + lj * sb;
+        for (int u = 0; u < 2; ++u) {
+            const int j = j0 + 32 * u;
+            const bool live = j < n;
+            const float *pj = base + (long long)(live ? j : j0) * slot_floats;
+            mj[u] = live ? __ldcg(pj + i) : -INFINITY;
+            lj[u] = __ldcg(pj + kAttnMaxRows + i);
+            const float4 *src = reinterpret_cast<const float4 *>(pj + 2 * kAttnMaxRows +
+                                                                 (long long)i * D + c0);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            acc[4 * q] = acc[4 * q] * sa + v[q].x * sb;
-            acc[4 * q + 1] = acc[4 * q + 1] * sa + v[q].y * sb;
-            acc[4 * q + 2] = acc[4 * q + 2] * sa + v[q].z * sb;
-            acc[4 * q + 3] = acc[4 * q + 3] * sa + v[q].w * sb;
+            for (int q = 0; q < 8; ++q)
+                v[u][q] = __ldcg(src + q);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float mnew = fmaxf(mloc, mj[u]);
+            const float sa = (mloc == -INFINITY) ? 0.f : exp2f(mloc - mnew);
+            const float sb = (mj[u] == -INFINITY) ? 0.f : exp2f(mj[u] - mnew);
+            mloc = mnew;
+            lloc = lloc * sa + lj[u] * sb;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                acc[4 * q] = acc[4 * q] * sa + v[u][q].x * sb;
+                acc[4 * q + 1] = acc[4 * q + 1] * sa + v[u][q].y * sb;
+                acc[4 * q + 2] = acc[4 * q + 2] * sa + v[u][q].z * sb;
+                acc[4 * q + 3] = acc[4 * q + 3] * sa + v[u][q].w * sb;
+            }
         }
     }
     float M = mloc;

@@ -9,10 +9,11 @@
 // Per group, D = sum code*x is folded as y += scale*D + bias*sum(x) in fp32, so
 // no per-weight dequantization multiply is spent.
 //
-// Work is split stream-K: the nrb*nku (row block, k unit) units are cut into
-// gridDim.x contiguous ranges.  A CTA writes one partial per row block it
-// touches; the last CTA to arrive on an epilogue block (counter, no waiting)
-// sums the partials in a fixed order and runs the epilogue.
+// Split-K inside a thread-block cluster: the cluster's CTAs share a block of
+// rows (whole heads for the q|k|v projection) and split K; each CTA keeps its
+// partial sums in its own shared memory and, after a cluster barrier, the
+// epilogue reads the partials of the whole block through distributed shared
+// memory.  No global scratch, no atomics, no waiting on other grids' CTAs.
 #pragma once
 
 #include "common.cuh"
@@ -73,15 +74,15 @@ __device__ __forceinline__ void unpack_a(const uint32_t *cw, int mi, uint32_t (&
 }
 
 // One stage: all 8 k16-steps of this warp's unit, folded into Y.
-template <int BITS, int NT>
-__device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, int ubytes, int group,
-                                           int w, int lane, float (&Y)[2][NT][4])
+template <int BITS, int NT, int GROUP>
+__device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, int ubytes, int w,
+                                           int lane, float (&Y)[2][NT][4])
 {
     const uint8_t *unit = st + w * ubytes;
     const uint8_t *sb = unit + unit_code_bytes(BITS);
     const uint2 *xf = reinterpret_cast<const uint2 *>(st + step_bytes);
     const float *xs = reinterpret_cast<const float *>(st + step_bytes + 2048 * NT);
-    const int kpg = group >> 4;
+    constexpr int kpg = GROUP / 16;     // k16-steps per group (compile time: no branches)
     const int g = lane >> 2, c = lane & 3;
 
     uint32_t cw[4 * BITS];
@@ -93,25 +94,31 @@ __device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, in
         cw[4 * i + 2] = v.z;
         cw[4 * i + 3] = v.w;
     }
-    float D[2][NT][4];
+    // spread the k16-steps of a group over SPLIT independent accumulator sets
+    // (more independent MMA chains per warp) and add the sets at the group end
+    constexpr int SPLIT = (NT == 1 && kpg >= 2) ? 2 : 1;
+    float D[SPLIT][2][NT][4];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int sp = 0; sp < SPLIT; ++sp)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                D[mt][nt][i] = 0.f;
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    D[sp][mt][nt][i] = 0.f;
 
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
+        const int sp = ks % SPLIT;
         uint32_t A[2][4];
         unpack_a<BITS>(cw, 2 * ks, A[0]);
         unpack_a<BITS>(cw, 2 * ks + 1, A[1]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const uint2 b = xf[(nt * 8 + ks) * 32 + lane];
-            mma_f16(D[0][nt], A[0], b.x, b.y, D[0][nt]);
-            mma_f16(D[1][nt], A[1], b.x, b.y, D[1][nt]);
+            mma_f16(D[sp][0][nt], A[0], b.x, b.y, D[sp][0][nt]);
+            mma_f16(D[sp][1][nt], A[1], b.x, b.y, D[sp][1][nt]);
         }
         if ((ks % kpg) == kpg - 1) {
             const int gi = ks / kpg;
@@ -123,13 +130,22 @@ __device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, in
                 const float2 xv = *reinterpret_cast<const float2 *>(xs + gi * 8 * NT + nt * 8 + 2 * c);
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
+                    float dd[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        dd[i] = D[0][mt][nt][i];
+#pragma unroll
+                        for (int q = 1; q < SPLIT; ++q)
+                            dd[i] += D[q][mt][nt][i];
+#pragma unroll
+                        for (int q = 0; q < SPLIT; ++q)
+                            D[q][mt][nt][i] = 0.f;
+                    }
                     float *y = Y[mt][nt];
-                    float *dd = D[mt][nt];
                     y[0] = fmaf(s[2 * mt], dd[0], fmaf(bb[2 * mt], xv.x, y[0]));
                     y[1] = fmaf(s[2 * mt], dd[1], fmaf(bb[2 * mt], xv.y, y[1]));
                     y[2] = fmaf(s[2 * mt + 1], dd[2], fmaf(bb[2 * mt + 1], xv.x, y[2]));
                     y[3] = fmaf(s[2 * mt + 1], dd[3], fmaf(bb[2 * mt + 1], xv.y, y[3]));
-                    dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
                 }
             }
         }
@@ -137,73 +153,52 @@ __device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, in
 }
 
 // Statics an epilogue needs, staged in shared memory before the main loop so
-// the epilogue itself has no dependent global round trips besides the partials.
+// the epilogue itself has no dependent global round trips.
 struct EpiSmem {
-    float *vals;        // [8][eb_rows] final values of up to 8 columns
+    float *red;         // [MP][kRBR] this CTA's partial sums (aliases the stage ring)
+    float *vals;        // [eb_rows] final values of one column of the cluster's rows
     float *nq, *nk;     // q_norm / k_norm as fp32 [d]
     double *invf;       // inv_freq [rd/2]
     int *cpos;          // cache_pos [B]
 };
 
-// Phase 1 of an epilogue: the final value of every row of epilogue block eb
-// for columns m0 .. m0+mc-1, i.e. the sum of the partials of every CTA whose
-// range touched the row's block, into vals[mm][row].  One row per thread.
+// Final value of row `row` (0 .. eb_rows-1 of the cluster), column m: the sum of
+// the ks partials of the row's block, read from the cluster's shared memory.
 template <int MP>
-__device__ __forceinline__ void gather_block(const ProjArgs &a, int eb, int m0, int mc, int tid,
-                                             float *vals)
+__device__ __forceinline__ float cluster_row_sum(const ProjArgs &a, const EpiSmem &sm, int row, int m)
 {
-    const long long G = gridDim.x;
-    const int rb0 = eb * a.eb_rows / kRBR, nrbs = a.eb_rows / kRBR;
-    for (int q = 0; q < nrbs; ++q) {
-        const int rb = rb0 + q;
-        if (rb >= a.nrb)
-            break;
-        const long long s0 = (long long)rb * a.nku;
-        const long long cf = sk_owner(s0, a.T, G), cl = sk_owner(s0 + a.nku - 1, a.T, G);
-        const float *p0 = a.ws + ((long long)rb + cf) * MP * kRBR + tid;
-        float acc[8];
-#pragma unroll
-        for (int mm = 0; mm < 8; ++mm)
-            acc[mm] = 0.f;
-        const int n = (int)(cl - cf + 1);
-#pragma unroll 4
-        for (int j = 0; j < n; ++j) {
-            const float *p = p0 + (long long)j * MP * kRBR;
-#pragma unroll
-            for (int mm = 0; mm < 8; ++mm) {
-                if (mm < mc) {
-                    acc[mm] += __ldcg(p + (long long)(m0 + mm) * kRBR);
-                    if (a.xsplit)
-                        acc[mm] += __ldcg(p + (long long)(m0 + mm + a.xsplit) * kRBR);
-                }
-            }
-        }
-#pragma unroll
-        for (int mm = 0; mm < 8; ++mm)
-            if (mm < mc)
-                vals[mm * a.eb_rows + q * kRBR + tid] = acc[mm];
+    const int q = row / kRBR, rr = row % kRBR;
+    const float *local = sm.red + (long long)m * kRBR + rr;
+    float v = 0.f;
+    for (int k = 0; k < a.ks; ++k) {
+        const uint32_t rank = (uint32_t)(q * a.ks + k);
+        v += ld_dsmem(dsmem_addr(local, rank));
+        if (a.xsplit)
+            v += ld_dsmem(dsmem_addr(local + (long long)a.xsplit * kRBR, rank));
     }
+    return v;
 }
 
-// qkv epilogue for one epilogue block (whole heads): per (head, column) one
-// warp splits query / gate / k / v, applies RMSNorm + partial RoPE to query
-// and k, and writes q (bf16), the gate (fp32) and the new cache rows (bf16).
+// q|k|v epilogue of the cluster's rows (whole heads): this CTA takes the
+// columns m with m % cluster_size == rank.  Per column: the final values into
+// shared memory, then per head one warp splits query / gate / k / v, applies
+// RMSNorm + partial RoPE to query and k, and writes q (bf16), the gate (fp32)
+// and the new cache rows (bf16).
 template <int MP>
-static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const EpiSmem &sm, int eb,
-                                    int warp, int lane, int tid)
+static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const EpiSmem &sm, int row0,
+                                    int rank, int csize, int warp, int lane, int tid)
 {
     const int d = e.d, half = e.rd >> 1, heads = a.eb_rows / d, per = d >> 5;
     const int Ny = e.Nq + 2 * e.Nkv;
-    for (int m0 = 0; m0 < a.M; m0 += 8) {
-        const int mc = min(8, a.M - m0);
-        gather_block<MP>(a, eb, m0, mc, tid, sm.vals);
+    for (int m = rank; m < a.M; m += csize) {
+        for (int r = tid; r < a.eb_rows; r += kWR * 32)
+            sm.vals[r] = cluster_row_sum<MP>(a, sm, r, m);
         named_bar_sync(1, kWR * 32);
-        for (int job = warp; job < heads * mc; job += kWR) {
-            const int hb = job / mc, mm = job % mc, m = m0 + mm;
-            const int n0 = eb * a.eb_rows + hb * d;
+        for (int hb = warp; hb < heads; hb += kWR) {
+            const int n0 = row0 + hb * d;
             if (n0 >= a.N)
                 continue;
-            const float *hv = sm.vals + mm * a.eb_rows + hb * d;
+            const float *hv = sm.vals + hb * d;
             float v[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -252,7 +247,7 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int j = lane + 32 * i;
-                    o[i] = v[i] * inv * nw[j];
+                    o[i] = i < per ? v[i] * inv * nw[j] : 0.f;
                     if (i < per && j < e.rd) {
                         const int fi = j < half ? j : j - half;
                         const int jp = j < half ? j + half : j - half;
@@ -261,7 +256,7 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
                         const double turns = rint(ang * 0.15915494309189535);
                         const float red = (float)fma(-turns, 6.283185307179586, ang);
                         float sn, cs;
-                        sincosf(red, &sn, &cs);
+                        __sincosf(red, &sn, &cs);   // |red| <= pi: hardware path
                         o[i] = j < half ? o[i] * cs - partner * sn : o[i] * cs + partner * sn;
                     }
                 }
@@ -293,51 +288,35 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
     }
 }
 
-// o_proj epilogue: final bf16 outputs of one row block, one row per thread.
+// o_proj epilogue: the cluster's single row block, rows split across its CTAs;
+// thread t takes row rank * rpr + t % rpr and the columns t / rpr + j * (128 / rpr).
 template <int MP>
-static __device__ void epilogue_o(const ProjArgs &a, const EpiO &e, const EpiSmem &sm, int eb,
-                                  int tid)
+static __device__ void epilogue_o(const ProjArgs &a, const EpiO &e, const EpiSmem &sm, int row0,
+                                  int rank, int csize, int tid)
 {
-    const int n = eb * a.eb_rows + tid;     // eb_rows == kRBR, one row per thread
-    if (tid >= a.eb_rows || n >= a.N)
+    const int rpr = kRBR / csize;              // rows per rank
+    const int lanes_m = (kWR * 32) / rpr;      // column lanes per row
+    const int r = rank * rpr + tid % rpr;
+    const int n = row0 + r;
+    if (n >= a.N)
         return;
-    const long long G = gridDim.x;
-    const int rb = n / kRBR, rr = n % kRBR;
-    const long long s0 = (long long)rb * a.nku;
-    const long long cf = sk_owner(s0, a.T, G), cl = sk_owner(s0 + a.nku - 1, a.T, G);
-    const float *p0 = a.ws + ((long long)rb + cf) * MP * kRBR + rr;
-    float acc[MP];
-#pragma unroll
-    for (int m = 0; m < MP; ++m)
-        acc[m] = 0.f;
-    const int nc = (int)(cl - cf + 1);
-#pragma unroll 4
-    for (int j = 0; j < nc; ++j) {
-        const float *p = p0 + (long long)j * MP * kRBR;
-#pragma unroll
-        for (int m = 0; m < MP; ++m)
-            if (m < a.M)
-                acc[m] += __ldcg(p + (long long)m * kRBR);
-    }
-#pragma unroll
-    for (int m = 0; m < MP; ++m) {
-        if (m < a.M) {
-            const int b = m / e.R;
-            const int pb = sm.cpos[b];
-            const bool valid = pb >= 0 && pb + e.R <= e.cap;
-            e.out[(long long)m * a.N + n] = __float2bfloat16_rn(valid ? acc[m] : 0.f);
-        }
+    for (int m = tid / rpr; m < a.M; m += lanes_m) {
+        const int b = m / e.R;
+        const int pb = sm.cpos[b];
+        const bool valid = pb >= 0 && pb + e.R <= e.cap;
+        const float v = valid ? cluster_row_sum<MP>(a, sm, r, m) : 0.f;
+        e.out[(long long)m * a.N + n] = __float2bfloat16_rn(v);
     }
 }
 
 // shared memory past the stage ring: barriers, flags, epilogue statics
 __host__ __device__ inline int proj_tail_bytes(int eb_rows)
 {
-    return 256 + 8 * eb_rows * 4 + 2 * 256 * 4 + 128 * 8 + 32 * 4;
+    return 256 + eb_rows * 4 + 2 * 256 * 4 + 128 * 8 + 32 * 4;
 }
 
-template <int BITS, int NT, int MODE>
-__global__ void __launch_bounds__((kWR + 1) * 32)
+template <int BITS, int NT, int MODE, int GROUP>
+__global__ void __launch_bounds__((kWR + 1) * 32, 2)
     proj_kernel(const ProjArgs a, const EpiQKV eq, const EpiO eo)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -347,22 +326,29 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
     uint8_t *tail = smem + (size_t)S * a.stage_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(tail);             // [S <= 8]
     uint64_t *empty = full + 8;                                       // [8]
-    int *flags = reinterpret_cast<int *>(tail + 128);                 // [0] abort, [1] last arrival
+    int *flags = reinterpret_cast<int *>(tail + 128);                 // [0] abort
     EpiSmem sm;
+    sm.red = reinterpret_cast<float *>(smem);                         // after the main loop
     sm.vals = reinterpret_cast<float *>(tail + 256);
-    sm.nq = sm.vals + 8 * a.eb_rows;
+    sm.nq = sm.vals + a.eb_rows;
     sm.nk = sm.nq + 256;
     sm.invf = reinterpret_cast<double *>(sm.nk + 256);
     sm.cpos = reinterpret_cast<int *>(sm.invf + 128);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int csize = a.rbc * a.ks;
+    const int rank = (int)cluster_ctarank();
+    const int cluster = blockIdx.x / csize;
+    const int rb = cluster * a.rbc + rank / a.ks, kr = rank % a.ks;
+    const int ku0 = (int)((long long)kr * a.nku / a.ks), ku1 = (int)((long long)(kr + 1) * a.nku / a.ks);
+    const long long beg = (long long)rb * a.nku + ku0, end = (long long)rb * a.nku + ku1;
+
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kWR);
         }
         flags[0] = 0;
-        flags[1] = 0;
         fence_mbar_init();
     }
     // o_proj lets the next step's kernels launch at once: their pre-wait work
@@ -379,20 +365,25 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
             }
             for (int j = t; j < eq.rd / 2; j += kWR * 32)
                 sm.invf[j] = eq.inv_freq[j];
-            if (t < a.M / eq.R + (a.M % eq.R != 0))
+            if (t < (a.M + eq.R - 1) / eq.R)
                 sm.cpos[t] = eq.cache_pos[t];
         } else {
-            if (t < a.M / eo.R + (a.M % eo.R != 0))
+            if (t < (a.M + eo.R - 1) / eo.R)
                 sm.cpos[t] = eo.cache_pos[t];
         }
     }
     __syncthreads();
 
-    // every CTA of the grid owns at least one unit: the host launches at most T CTAs
-    const long long G = gridDim.x, c = blockIdx.x;
-    const long long beg = sk_start(c, a.T, G), end = sk_start(c + 1, a.T, G);
-    const int xbytes = 2048 * NT, sbytes = (kKU / a.group) * 4 * MP;
+    const int xbytes = 2048 * NT, sbytes = (kKU / GROUP) * 4 * MP;
     volatile int *abort = flags;
+    float Y[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                Y[mt][nt][i] = 0.f;
 
     if (warp == kWR) {
         // ------------------------------------------------------------ producer
@@ -410,12 +401,11 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
             }
             pdl_wait();
             for (long long i = 0; i < pre; ++i) {
-                const long long s = beg + i;
-                const int ku = (int)(s % a.nku);
+                const int ku = (int)((beg + i) % a.nku);
                 uint8_t *st = stages + (size_t)(i % S) * a.stage_bytes;
                 bulk_g2s(st + a.step_bytes, a.x16 + (long long)ku * NT * 1024, xbytes,
                          &full[i % S], pol);
-                bulk_g2s(st + a.step_bytes + xbytes, a.xsum + (long long)ku * (kKU / a.group) * MP,
+                bulk_g2s(st + a.step_bytes + xbytes, a.xsum + (long long)ku * (kKU / GROUP) * MP,
                          sbytes, &full[i % S], pol);
             }
             for (; beg + it < end; ++it) {
@@ -430,10 +420,10 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
                 bulk_g2s(st, a.w + s * a.step_bytes, a.step_bytes, &full[slot], pol);
                 bulk_g2s(st + a.step_bytes, a.x16 + (long long)ku * NT * 1024, xbytes, &full[slot],
                          pol);
-                bulk_g2s(st + a.step_bytes + xbytes, a.xsum + (long long)ku * (kKU / a.group) * MP,
+                bulk_g2s(st + a.step_bytes + xbytes, a.xsum + (long long)ku * (kKU / GROUP) * MP,
                          sbytes, &full[slot], pol);
             }
-            // let every copy this CTA issued land before the CTA may exit
+            // let every copy this CTA issued land before the ring is reused
             const long long first = it > S ? it - S : 0;
             for (long long i = first; i < it; ++i) {
                 unsigned long long t0 = global_ns();
@@ -442,84 +432,53 @@ __global__ void __launch_bounds__((kWR + 1) * 32)
                 }
             }
         }
-        return;
-    }
-
-    // ------------------------------------------------------------- consumers
-    pdl_wait();
-    // q|k|v: dependents (attention) may launch only once the previous kernels
-    // have completed, so that attention can prefetch cache rows before waiting
-    if constexpr (MODE == kModeQKV)
-        pdl_launch_dependents();
-    const int tid = threadIdx.x;           // 0 .. kWR*32-1
-    const int g = lane >> 2, cq = lane & 3;
-    float Y[2][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                Y[mt][nt][i] = 0.f;
-
-    long long it = 0;
-    for (long long s = beg; s < end; ++s, ++it) {
-        const int slot = (int)(it % S);
-        const uint32_t ph = (uint32_t)((it / S) & 1);
-        const int rb = (int)(s / a.nku), ku = (int)(s % a.nku);
-        if (mbar_wait(&full[slot], ph, abort, a.status))
-            proj_stage<BITS, NT>(stages + (size_t)slot * a.stage_bytes, a.step_bytes, a.unit_bytes,
-                                 a.group, warp, lane, Y);
         __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[slot]);
-
-        if (ku == a.nku - 1 || s == end - 1) {
-            // partial of this row block: [MP][kRBR] floats in slot rb + c
-            float *p = a.ws + ((long long)rb + c) * MP * kRBR;
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int row = warp * 32 + mt * 16 + g, col = nt * 8 + 2 * cq;
-                    p[(long long)col * kRBR + row] = Y[mt][nt][0];
-                    p[(long long)(col + 1) * kRBR + row] = Y[mt][nt][1];
-                    p[(long long)col * kRBR + row + 8] = Y[mt][nt][2];
-                    p[(long long)(col + 1) * kRBR + row + 8] = Y[mt][nt][3];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        Y[mt][nt][i] = 0.f;
-                }
-            named_bar_sync(1, kWR * 32);
-            const int eb = rb * kRBR / a.eb_rows;
-            if (tid == 0) {
-                __threadfence();   // publishes the CTA's partial (ordered by the barrier)
-                int total = 0;
-                const int rb0 = eb * a.eb_rows / kRBR, rb1 = rb0 + a.eb_rows / kRBR;
-                for (int q = rb0; q < rb1 && q < a.nrb; ++q) {
-                    const long long q0 = (long long)q * a.nku;
-                    total += (int)(sk_owner(q0 + a.nku - 1, a.T, G) - sk_owner(q0, a.T, G) + 1);
-                }
-                const int old = atomicAdd(&a.cnt[eb], 1);
-                flags[1] = (old == total - 1);
-                if (flags[1])
-                    __threadfence();
-            }
-            named_bar_sync(1, kWR * 32);
-            if (flags[1]) {
-                if constexpr (MODE == kModeQKV)
-                    epilogue_qkv<MP>(a, eq, sm, eb, warp, lane, tid);
-                else
-                    epilogue_o<MP>(a, eo, sm, eb, tid);
-                named_bar_sync(1, kWR * 32);
-                if (tid == 0)
-                    a.cnt[eb] = 0;
-            }
+    } else {
+        // ------------------------------------------------------------ consumers
+        pdl_wait();
+        // q|k|v: dependents (attention) may launch only once the previous kernels
+        // have completed, so that attention can prefetch cache rows before waiting
+        if constexpr (MODE == kModeQKV)
+            pdl_launch_dependents();
+        long long it = 0;
+        for (long long s = beg; s < end; ++s, ++it) {
+            const int slot = (int)(it % S);
+            const uint32_t ph = (uint32_t)((it / S) & 1);
+            if (mbar_wait(&full[slot], ph, abort, a.status))
+                proj_stage<BITS, NT, GROUP>(stages + (size_t)slot * a.stage_bytes, a.step_bytes,
+                                            a.unit_bytes, warp, lane, Y);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[slot]);
         }
     }
+    // the ring is drained: it now holds this CTA's partial sums [MP][kRBR]
+    __syncthreads();
+    if (warp < kWR) {
+        const int g = lane >> 2, cq = lane & 3;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int row = warp * 32 + mt * 16 + g, col = nt * 8 + 2 * cq;
+                sm.red[col * kRBR + row] = Y[mt][nt][0];
+                sm.red[(col + 1) * kRBR + row] = Y[mt][nt][1];
+                sm.red[col * kRBR + row + 8] = Y[mt][nt][2];
+                sm.red[(col + 1) * kRBR + row + 8] = Y[mt][nt][3];
+            }
+    }
+    cluster_sync();     // every CTA's partial is visible to the cluster
+    if (warp < kWR) {
+        const int row0 = cluster * a.eb_rows;
+        if constexpr (MODE == kModeQKV)
+            epilogue_qkv<MP>(a, eq, sm, row0, rank, csize, warp, lane, threadIdx.x);
+        else
+            epilogue_o<MP>(a, eo, sm, row0, rank, csize, threadIdx.x);
+    }
+    cluster_sync();     // no CTA leaves while others may still read its partial
 }
 
-template <int BITS, int NT, int MODE>
+template <int BITS, int NT, int MODE, int GROUP>
 cudaError_t launch_proj_t(const ProjArgs &a, const EpiQKV &eq, const EpiO &eo, int grid, bool pdl,
                           cudaStream_t s)
 {
@@ -528,40 +487,31 @@ cudaError_t launch_proj_t(const ProjArgs &a, const EpiQKV &eq, const EpiO &eo, i
     cfg.blockDim = dim3((kWR + 1) * 32);
     cfg.dynamicSmemBytes = proj_smem_bytes(a);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = a.rbc * a.ks;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, proj_kernel<BITS, NT, MODE>, a, eq, eo);
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, proj_kernel<BITS, NT, MODE, GROUP>, a, eq, eo);
 }
 
-template <int BITS>
-cudaError_t launch_proj_bits(int NT, int mode, const ProjArgs &a, const EpiQKV &eq, const EpiO &eo,
-                             int grid, bool pdl, cudaStream_t s)
+// the kernel instantiation for runtime (NT, mode, group)
+template <int BITS, typename F>
+cudaError_t with_proj_kernel(int NT, int mode, int group, F &&f)
 {
-    if (mode == kModeQKV) {
-        if (NT == 1) return launch_proj_t<BITS, 1, kModeQKV>(a, eq, eo, grid, pdl, s);
-        if (NT == 2) return launch_proj_t<BITS, 2, kModeQKV>(a, eq, eo, grid, pdl, s);
-        return launch_proj_t<BITS, 4, kModeQKV>(a, eq, eo, grid, pdl, s);
-    }
-    if (NT == 1) return launch_proj_t<BITS, 1, kModeO>(a, eq, eo, grid, pdl, s);
-    if (NT == 2) return launch_proj_t<BITS, 2, kModeO>(a, eq, eo, grid, pdl, s);
-    return launch_proj_t<BITS, 4, kModeO>(a, eq, eo, grid, pdl, s);
-}
-
-template <int BITS>
-cudaError_t set_smem_bits(int bytes)
-{
-    cudaError_t e = cudaSuccess;
-#define GATTN_SET(NT, MODE)                                                                        \
-    if (e == cudaSuccess)                                                                          \
-        e = cudaFuncSetAttribute(proj_kernel<BITS, NT, MODE>,                                      \
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    GATTN_SET(1, kModeQKV) GATTN_SET(2, kModeQKV) GATTN_SET(4, kModeQKV)
-    GATTN_SET(1, kModeO) GATTN_SET(2, kModeO) GATTN_SET(4, kModeO)
-#undef GATTN_SET
-    return e;
+#define GATTN_K(nt, md, gr)                                                                        \
+    if (NT == nt && mode == md && group == gr)                                                     \
+        return f(proj_kernel<BITS, nt, md, gr>, launch_proj_t<BITS, nt, md, gr>);
+#define GATTN_G(nt, md) GATTN_K(nt, md, 32) GATTN_K(nt, md, 64) GATTN_K(nt, md, 128)
+    GATTN_G(1, kModeQKV) GATTN_G(2, kModeQKV) GATTN_G(4, kModeQKV)
+    GATTN_G(1, kModeO) GATTN_G(2, kModeO) GATTN_G(4, kModeO)
+#undef GATTN_G
+#undef GATTN_K
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gattn

@@ -7,14 +7,14 @@ namespace gattn {
     cudaError_t launch_proj_b##B(int, int, const ProjArgs &, const EpiQKV &, const EpiO &, int,    \
                                  bool, cudaStream_t);                                              \
     cudaError_t set_smem_b##B(int);                                                                \
-    cudaError_t occupancy_b##B(int, int, int, int *);
+    cudaError_t occupancy_b##B(int, int, int, int, int *);
 GATTN_DECL(2) GATTN_DECL(3) GATTN_DECL(4) GATTN_DECL(5) GATTN_DECL(6) GATTN_DECL(8)
 #undef GATTN_DECL
 
 int proj_smem_bytes(const ProjArgs &a)
 {
-    // stage ring + barriers/flags + epilogue statics (see proj_tail_bytes)
-    return a.stages * a.stage_bytes + 256 + 8 * a.eb_rows * 4 + 2 * 256 * 4 + 128 * 8 + 32 * 4;
+    // stage ring + barriers/flags + epilogue statics (see proj_tail_bytes in proj.cuh)
+    return a.stages * a.stage_bytes + 256 + a.eb_rows * 4 + 2 * 256 * 4 + 128 * 8 + 32 * 4;
 }
 
 cudaError_t launch_proj(int bits, int NT, int mode, const ProjArgs &a, const EpiQKV &eq,
@@ -46,15 +46,15 @@ cudaError_t proj_set_smem_limits(int bits, int NT, int mode, int bytes)
     }
 }
 
-cudaError_t proj_occupancy(int bits, int NT, int mode, int smem, int *occ)
+cudaError_t proj_occupancy(int bits, int NT, int mode, int group, int smem, int *occ)
 {
     switch (bits) {
-    case 2: return occupancy_b2(NT, mode, smem, occ);
-    case 3: return occupancy_b3(NT, mode, smem, occ);
-    case 4: return occupancy_b4(NT, mode, smem, occ);
-    case 5: return occupancy_b5(NT, mode, smem, occ);
-    case 6: return occupancy_b6(NT, mode, smem, occ);
-    case 8: return occupancy_b8(NT, mode, smem, occ);
+    case 2: return occupancy_b2(NT, mode, group, smem, occ);
+    case 3: return occupancy_b3(NT, mode, group, smem, occ);
+    case 4: return occupancy_b4(NT, mode, group, smem, occ);
+    case 5: return occupancy_b5(NT, mode, group, smem, occ);
+    case 6: return occupancy_b6(NT, mode, group, smem, occ);
+    case 8: return occupancy_b8(NT, mode, group, smem, occ);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -3,34 +3,35 @@
 #pragma once
 #include "proj.cuh"
 
-namespace gattn {
-
-template <int BITS>
-cudaError_t occupancy_bits(int NT, int mode, int smem, int *occ)
-{
-    const int threads = (kWR + 1) * 32;
-#define GATTN_OCC(nt, md)                                                                          \
-    if (NT == nt && mode == md)                                                                    \
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, proj_kernel<BITS, nt, md>,       \
-                                                             threads, smem);
-    GATTN_OCC(1, kModeQKV) GATTN_OCC(2, kModeQKV) GATTN_OCC(4, kModeQKV)
-    GATTN_OCC(1, kModeO) GATTN_OCC(2, kModeO) GATTN_OCC(4, kModeO)
-#undef GATTN_OCC
-    return cudaErrorInvalidValue;
-}
-
-}  // namespace gattn
-
 #define GATTN_PROJ_INSTANCE(B)                                                                     \
     namespace gattn {                                                                              \
     cudaError_t launch_proj_b##B(int NT, int mode, const ProjArgs &a, const EpiQKV &eq,            \
                                  const EpiO &eo, int grid, bool pdl, cudaStream_t s)               \
     {                                                                                              \
-        return launch_proj_bits<B>(NT, mode, a, eq, eo, grid, pdl, s);                             \
+        return with_proj_kernel<B>(NT, mode, a.group, [&](auto kern, auto launch) {                \
+            (void)kern;                                                                            \
+            return launch(a, eq, eo, grid, pdl, s);                                                \
+        });                                                                                        \
     }                                                                                              \
-    cudaError_t set_smem_b##B(int bytes) { return set_smem_bits<B>(bytes); }                       \
-    cudaError_t occupancy_b##B(int NT, int mode, int smem, int *occ)                               \
+    cudaError_t set_smem_b##B(int bytes)                                                           \
     {                                                                                              \
-        return occupancy_bits<B>(NT, mode, smem, occ);                                             \
+        cudaError_t e = cudaSuccess;                                                               \
+        for (int nt : {1, 2, 4})                                                                   \
+            for (int md : {kModeQKV, kModeO})                                                      \
+                for (int gr : {32, 64, 128})                                                       \
+                    if (e == cudaSuccess)                                                          \
+                        e = with_proj_kernel<B>(nt, md, gr, [&](auto kern, auto launch) {          \
+                            (void)launch;                                                          \
+                            return cudaFuncSetAttribute(                                           \
+                                kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);         \
+                        });                                                                        \
+        return e;                                                                                  \
+    }                                                                                              \
+    cudaError_t occupancy_b##B(int NT, int mode, int group, int smem, int *occ)                    \
+    {                                                                                              \
+        return with_proj_kernel<B>(NT, mode, group, [&](auto kern, auto launch) {                  \
+            (void)launch;                                                                          \
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, (kWR + 1) * 32, smem); \
+        });                                                                                        \
     }                                                                                              \
     }
