@@ -286,8 +286,14 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
             // the grid stays resident (one wave)
             const long long capacity = (long long)L->num_sms * occ;
             const int nclusters = p->nrb / p->rbc;
+            // 16-CTA clusters (non-portable) when this kernel can run them
+            int max_cluster = kMaxCluster, n16 = 0;
+            if (proj_max_clusters(p->bits, 1 << i, p == &L->pqkv ? kModeQKV : kModeO, p->group,
+                                  smem, 16, &n16) == cudaSuccess && n16 > 0)
+                max_cluster = 16;
+            cudaGetLastError();
             int ks = 1;
-            while (ks * 2 * p->rbc <= kMaxCluster && ks * 2 <= p->nku &&
+            while (ks * 2 * p->rbc <= max_cluster && ks * 2 <= p->nku &&
                    (long long)nclusters * p->rbc * ks * 2 <= capacity)
                 ks *= 2;
             p->ks[i] = ks;

@@ -20,9 +20,14 @@
 
 namespace gattn {
 
+// bytes of one 64-wide head_dim box of a tile (kAttnTile tokens x 128 bytes);
+// a multiple of 1024 so every box starts on a 128-byte-swizzle atom
+constexpr int kDBox = kAttnTile * 128;
+static_assert(kDBox % 1024 == 0, "tile boxes must stay swizzle-atom aligned");
+
 template <int MT, int DB>
 struct AttnSmem {
-    static constexpr int kTileBytes = DB * 64 * 128;          // 64 tokens x d bf16
+    static constexpr int kTileBytes = DB * kDBox;             // kAttnTile tokens x d bf16
     static constexpr int kStageBytes = 2 * kTileBytes;        // K + V
     static constexpr int kQBytes = MT * 16 * DB * 64 * 2;
     static constexpr int kPBytes = MT * 16 * 128;             // rows x 64 tokens bf16
@@ -160,9 +165,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const int t = (u + ui) * kAttnUnit;
 #pragma unroll
                         for (int db = 0; db < DB; ++db) {
-                            tensor4d_g2s(kst + db * 8192 + ui * 2048, &kmap, db * 64, t, p.kh, p.b,
+                            tensor4d_g2s(kst + db * kDBox + ui * 2048, &kmap, db * 64, t, p.kh, p.b,
                                          &full[slot], pol);
-                            tensor4d_g2s(vst + db * 8192 + ui * 2048, &vmap, db * 64, t, p.kh, p.b,
+                            tensor4d_g2s(vst + db * kDBox + ui * 2048, &vmap, db * 64, t, p.kh, p.b,
                                          &full[slot], pol);
                         }
                     }
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int idx = tid; idx < (ntok - first) * DB * 8; idx += kAttnWarps * 32) {
                     const int row = first + idx / (DB * 8), rest = idx % (DB * 8);
                     const int db = rest >> 3, cc = rest & 7;
-                    *reinterpret_cast<uint4 *>(vst + db * 8192 + row * 128 + cc * 16) =
+                    *reinterpret_cast<uint4 *>(vst + db * kDBox + row * 128 + cc * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int k2 = 0; k2 < 2 * DB; ++k2) {
                     const int chunk = k2 * 4 + (lane >> 3);
                     uint32_t kb[4];
-                    ldsm_x4(kb, smem_u32(kst + (chunk >> 3) * 8192 + tok * 128 +
+                    ldsm_x4(kb, smem_u32(kst + (chunk >> 3) * kDBox + tok * 128 +
                                          (((chunk & 7) ^ (tok & 7)) << 4)));
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt) {
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // ---- O += P V for this warp's head_dim slice
             if (ok) {
 #pragma unroll
-                for (int kt = 0; kt < 4; ++kt) {
+                for (int kt = 0; kt < kAttnTile / 16; ++kt) {
                     if (kt * 16 < ntok) {
                         const int tok = kt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
                         uint32_t vb[DB][2];
@@ -353,7 +358,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             if (j + 1 < DB) {
                                 const int chunk = nd + (lane >> 4);
                                 uint32_t r[4];
-                                ldsm_x4_trans(r, smem_u32(vst + (chunk >> 3) * 8192 + tok * 128 +
+                                ldsm_x4_trans(r, smem_u32(vst + (chunk >> 3) * kDBox + tok * 128 +
                                                           (((chunk & 7) ^ (tok & 7)) << 4)));
                                 vb[j][0] = r[0];
                                 vb[j][1] = r[1];
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             } else {
                                 const int chunk = nd;
                                 ldsm_x2_trans(vb[j][0], vb[j][1],
-                                              smem_u32(vst + (chunk >> 3) * 8192 + tok * 128 +
+                                              smem_u32(vst + (chunk >> 3) * kDBox + tok * 128 +
                                                        (((chunk & 7) ^ (tok & 7)) << 4)));
                             }
                         }

@@ -182,10 +182,12 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank)
     return r;
 }
 
+// Remote load without a memory clobber, so independent loads can be in flight
+// together; being volatile it stays after cluster_sync() (also volatile).
 __device__ __forceinline__ float ld_dsmem(uint32_t addr)
 {
     float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
 }
 

@@ -103,6 +103,8 @@ cudaError_t launch_proj(int bits, int NT, int mode, const ProjArgs &a, const Epi
 int proj_smem_bytes(const ProjArgs &a);
 cudaError_t proj_set_smem_limits(int bits, int NT, int mode, int bytes);
 cudaError_t proj_occupancy(int bits, int NT, int mode, int group, int smem, int *blocks_per_sm);
+// clusters of csize CTAs that can be resident at once (0: that size cannot launch)
+cudaError_t proj_max_clusters(int bits, int NT, int mode, int group, int smem, int csize, int *n);
 
 // fp32 x is split exactly into hi = fp16(x) (column m) and lo = fp16(x - hi)
 // (column M + m); bf16 x converts to fp16 exactly (finite, |x| < 65504).
@@ -128,7 +130,7 @@ cudaError_t launch_unpack_codes(const uint32_t *packed, long long N, long long K
 constexpr int kAttnWarps = 8;          // consumer warps
 constexpr int kAttnThreads = (kAttnWarps + 1) * 32;
 constexpr int kAttnUnit = 16;          // tokens per stream-K unit
-constexpr int kAttnTile = 64;          // tokens per pipeline stage
+constexpr int kAttnTile = 48;          // tokens per pipeline stage (<= 64: the P tile width)
 constexpr int kAttnStages = 2;
 constexpr int kMaxRowBlocks = 64;
 constexpr int kAttnMaxRows = 64;       // query rows per segment

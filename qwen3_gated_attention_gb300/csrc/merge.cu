@@ -1,12 +1,11 @@
 // merge.cu -- combine the attention partials of every segment, apply the
 // output gate, and write the o_proj operand.
 //
-// One CTA per (segment, query row), one warp per 32 head_dim columns.  The
-// lanes of a warp split the segment's contributors (the CTAs whose unit ranges
-// touched it), so a segment cut into many pieces merges in about one memory
-// round trip: each lane folds its contributors (m_j, l_j, O_j) with a running
-// log2-domain maximum, the lanes agree on M = max m, rescale by 2^(m - M), and
-// a shuffle reduce-scatter sums O and l across lanes (column c lands on lane c).
+// One CTA per (segment, query row), one thread per head_dim column.  Every
+// contributor (the CTAs whose unit ranges touched the segment) left m_j (the
+// log2-domain row maximum), l_j and O_j; with M = max m_j,
+//   attn = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
+// Threads own columns so each partial row is read as coalesced lines.
 //
 //   attn = O / l,   a = attn * sigmoid(gate)   (the layer's output gate)
 //
@@ -66,73 +65,59 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a)
     const long long Ktot = (long long)a.H * D;
 
     pdl_wait();                 // partials (attention) and the gate (q|k|v projection)
-    const float gt = a.gate[(long long)m * Ktot + (long long)h * D + c0 + lane];
-    // one pass per lane over its contributors with a running maximum
-    float mloc = -INFINITY, lloc = 0.f;
-    float acc[32];
+    const int jd = c0 + lane;   // this thread's head_dim column
+    const float gt = a.gate[(long long)m * Ktot + (long long)h * D + jd];
+    // lanes own columns, so every partial load is one coalesced 128-byte line
+    // per warp (m_j and l_j are warp-uniform broadcast loads).  Contributors are
+    // loaded 16 at a time into registers (independent loads in flight
+    // together), then folded with a running log2-domain maximum.
+    constexpr int kBatch = 16;
+    float M = -INFINITY, L = 0.f, acc = 0.f;
+    const float *pm = base + i;                                   // m_j of row i
+    const int off_l = kAttnMaxRows, off_o = 2 * kAttnMaxRows + i * D + jd - i;
+    auto fold = [&](const float (&mv)[kBatch], const float (&lv)[kBatch],
+                    const float (&ov)[kBatch]) {
+        float mb = M;
 #pragma unroll
-    for (int cidx = 0; cidx < 32; ++cidx)
-        acc[cidx] = 0.f;
-    // contributors j and j + 32 are loaded together (one memory round trip for
-    // up to 64 contributors), then folded
-    for (int j0 = lane; j0 < n; j0 += 64) {
-        float mj[2], lj[2];
-        float4 v[2][8];
+        for (int u = 0; u < kBatch; ++u)
+            mb = fmaxf(mb, mv[u]);
+        const float sc = (M == -INFINITY) ? 0.f : exp2f(M - mb);
+        L *= sc;
+        acc *= sc;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int j = j0 + 32 * u;
-            const bool live = j < n;
-            const float *pj = base + (long long)(live ? j : j0) * slot_floats;
-            mj[u] = live ? __ldcg(pj + i) : -INFINITY;
-            lj[u] = __ldcg(pj + kAttnMaxRows + i);
-            const float4 *src = reinterpret_cast<const float4 *>(pj + 2 * kAttnMaxRows +
-                                                                 (long long)i * D + c0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                v[u][q] = __ldcg(src + q);
+        for (int u = 0; u < kBatch; ++u) {
+            const float w = (mv[u] == -INFINITY) ? 0.f : exp2f(mv[u] - mb);
+            L = fmaf(w, lv[u], L);
+            acc = fmaf(w, ov[u], acc);
         }
+        M = mb;
+    };
+    int j0 = 0;
+    for (; j0 + kBatch <= n; j0 += kBatch) {
+        float mv[kBatch], lv[kBatch], ov[kBatch];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const float mnew = fmaxf(mloc, mj[u]);
-            const float sa = (mloc == -INFINITY) ? 0.f : exp2f(mloc - mnew);
-            const float sb = (mj[u] == -INFINITY) ? 0.f : exp2f(mj[u] - mnew);
-            mloc = mnew;
-            lloc = lloc * sa + lj[u] * sb;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                acc[4 * q] = acc[4 * q] * sa + v[u][q].x * sb;
-                acc[4 * q + 1] = acc[4 * q + 1] * sa + v[u][q].y * sb;
-                acc[4 * q + 2] = acc[4 * q + 2] * sa + v[u][q].z * sb;
-                acc[4 * q + 3] = acc[4 * q + 3] * sa + v[u][q].w * sb;
-            }
+        for (int u = 0; u < kBatch; ++u) {
+            const float *pj = pm + u * slot_floats;
+            mv[u] = pj[0];
+            lv[u] = pj[off_l];
+            ov[u] = __ldcg(pj + off_o);
         }
+        fold(mv, lv, ov);
+        pm += kBatch * slot_floats;
     }
-    float M = mloc;
+    if (j0 < n) {
+        float mv[kBatch], lv[kBatch], ov[kBatch];
 #pragma unroll
-    for (int o = 16; o; o >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float sc = (mloc == -INFINITY) ? 0.f : exp2f(mloc - M);
-    float L = lloc * sc;
-#pragma unroll
-    for (int cidx = 0; cidx < 32; ++cidx)
-        acc[cidx] *= sc;
-#pragma unroll
-    for (int o = 16; o; o >>= 1)
-        L += __shfl_xor_sync(0xffffffffu, L, o);
-    // reduce-scatter: after the step with offset `off`, the lane keeps the half
-    // of its columns selected by lane bit `off`; column c0 + lane ends on lane
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int cidx = 0; cidx < off; ++cidx) {
-            const float send = upper ? acc[cidx] : acc[cidx + off];
-            const float keep = upper ? acc[cidx + off] : acc[cidx];
-            acc[cidx] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        for (int u = 0; u < kBatch; ++u) {
+            const bool live = j0 + u < n;
+            const float *pj = pm + (live ? u : 0) * slot_floats;
+            mv[u] = live ? pj[0] : -INFINITY;
+            lv[u] = pj[off_l];
+            ov[u] = __ldcg(pj + off_o);
         }
+        fold(mv, lv, ov);
     }
-    const int jd = c0 + lane;
-    const float o = L > 0.f ? acc[0] / L : 0.f;
+    const float o = L > 0.f ? acc / L : 0.f;
     const float gated = o * (1.f / (1.f + __expf(-gt)));
     const __half hv = __float2half_rn(gated);
     const int k = h * D + jd;

@@ -7,7 +7,8 @@ namespace gattn {
     cudaError_t launch_proj_b##B(int, int, const ProjArgs &, const EpiQKV &, const EpiO &, int,    \
                                  bool, cudaStream_t);                                              \
     cudaError_t set_smem_b##B(int);                                                                \
-    cudaError_t occupancy_b##B(int, int, int, int, int *);
+    cudaError_t occupancy_b##B(int, int, int, int, int *);                                       \
+    cudaError_t clusters_b##B(int, int, int, int, int, int *);
 GATTN_DECL(2) GATTN_DECL(3) GATTN_DECL(4) GATTN_DECL(5) GATTN_DECL(6) GATTN_DECL(8)
 #undef GATTN_DECL
 
@@ -55,6 +56,19 @@ cudaError_t proj_occupancy(int bits, int NT, int mode, int group, int smem, int 
     case 5: return occupancy_b5(NT, mode, group, smem, occ);
     case 6: return occupancy_b6(NT, mode, group, smem, occ);
     case 8: return occupancy_b8(NT, mode, group, smem, occ);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t proj_max_clusters(int bits, int NT, int mode, int group, int smem, int csize, int *n)
+{
+    switch (bits) {
+    case 2: return clusters_b2(NT, mode, group, smem, csize, n);
+    case 3: return clusters_b3(NT, mode, group, smem, csize, n);
+    case 4: return clusters_b4(NT, mode, group, smem, csize, n);
+    case 5: return clusters_b5(NT, mode, group, smem, csize, n);
+    case 6: return clusters_b6(NT, mode, group, smem, csize, n);
+    case 8: return clusters_b8(NT, mode, group, smem, csize, n);
     default: return cudaErrorInvalidValue;
     }
 }

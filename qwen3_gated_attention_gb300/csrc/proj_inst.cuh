@@ -22,8 +22,12 @@
                     if (e == cudaSuccess)                                                          \
                         e = with_proj_kernel<B>(nt, md, gr, [&](auto kern, auto launch) {          \
                             (void)launch;                                                          \
-                            return cudaFuncSetAttribute(                                           \
+                            cudaError_t r = cudaFuncSetAttribute(                                  \
                                 kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);         \
+                            if (r == cudaSuccess)                                                  \
+                                r = cudaFuncSetAttribute(                                          \
+                                    kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);      \
+                            return r;                                                              \
                         });                                                                        \
         return e;                                                                                  \
     }                                                                                              \
@@ -32,6 +36,24 @@
         return with_proj_kernel<B>(NT, mode, group, [&](auto kern, auto launch) {                  \
             (void)launch;                                                                          \
             return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, (kWR + 1) * 32, smem); \
+        });                                                                                        \
+    }                                                                                              \
+    cudaError_t clusters_b##B(int NT, int mode, int group, int smem, int csize, int *n)            \
+    {                                                                                              \
+        return with_proj_kernel<B>(NT, mode, group, [&](auto kern, auto launch) {                  \
+            (void)launch;                                                                          \
+            cudaLaunchConfig_t cfg = {};                                                           \
+            cfg.gridDim = dim3(csize);                                                             \
+            cfg.blockDim = dim3((kWR + 1) * 32);                                                   \
+            cfg.dynamicSmemBytes = smem;                                                           \
+            cudaLaunchAttribute at[1];                                                             \
+            at[0].id = cudaLaunchAttributeClusterDimension;                                        \
+            at[0].val.clusterDim.x = csize;                                                        \
+            at[0].val.clusterDim.y = 1;                                                            \
+            at[0].val.clusterDim.z = 1;                                                            \
+            cfg.attrs = at;                                                                        \
+            cfg.numAttrs = 1;                                                                      \
+            return cudaOccupancyMaxActiveClusters(n, kern, &cfg);                                  \
         });                                                                                        \
     }                                                                                              \
     }
