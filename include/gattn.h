@@ -215,6 +215,26 @@ gattn_status gattn_layer_dequant_device(gattn_layer *layer, int32_t proj, float 
                                         gattn_stream stream);
 
 /*
+ * Same result as gattn_layer_dequant_device (bit for bit), for callers that
+ * cannot allocate device memory or synchronize at the point of the call: code
+ * recording a CUDA graph in global capture mode, code whose framework owns the
+ * whole device memory budget, latency-sensitive paths.  It allocates nothing:
+ * its staging buffer is a fixed 16 MiB device array inside the library (held
+ * on every GPU that loads it, until exit), and it returns without waiting for
+ * the GPU (w is ready once `stream` reaches that point).
+ *   - Limit: the 128-row blocks spanning the projection times K must fit in
+ *     4 Mi floats; larger projections fail with GATTN_E_UNSUPPORTED and a
+ *     message naming the sizes.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the one array: calls that can overlap on the GPU (on
+ *     different streams, or different layers at once) race on it.
+ * The pages have no counterpart of this entry point (it is a library utility).
+ */
+gattn_status gattn_layer_dequant_device_static(gattn_layer *layer, int32_t proj, float *w,
+                                               gattn_stream stream);
+
+/*
  * The verify head-chunk plan (DS4Server issue 113, "Reproduction and boundary"):
  * when enabled and q_len*gqa > 32 and q_len <= 32, the query heads of each KV
  * group are split into chunks of max(1, min(gqa, 32/q_len)) heads (the last

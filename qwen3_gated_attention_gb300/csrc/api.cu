@@ -186,6 +186,24 @@ struct gattn_kv {
     CUtensorMap vmap;
 };
 
+bool gattn::layer_proj_tiles(const gattn_layer *L, int proj, ProjTiles *out)
+{
+    if (!L || !out || proj < 0 || proj > 3 || !L->weights_set)
+        return false;
+    const ProjPlan &p = proj == 3 ? L->po : L->pqkv;
+    out->w = p.w;
+    out->nku = p.nku;
+    out->bits = p.bits;
+    out->group = p.group;
+    out->step_bytes = p.step_bytes;
+    out->K = p.K;
+    out->row0 = proj == 0 ? 0 : (proj == 1 ? L->Nq : (proj == 2 ? L->Nq + L->Nkv : 0));
+    out->rows = proj == 0 ? L->Nq : (proj == 3 ? L->po.N : L->Nkv);
+    return true;
+}
+
+void gattn_set_error(const char *msg) { g_err = msg; }
+
 extern "C" {
 
 const char *gattn_last_error(void) { return g_err.c_str(); }

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+struct gattn_layer;
+
 namespace gattn {
 
 // ----------------------------------------------------- projection layout
@@ -125,6 +127,16 @@ cudaError_t launch_dequant_tiles(const uint8_t *w, int N, int K, int bits, int g
 cudaError_t launch_unpack_codes(const uint32_t *packed, long long N, long long K, int bits,
                                 uint8_t *codes, cudaStream_t s);
 
+// Where one projection of a layer lives in its repacked tile layout (for
+// entry points outside api.cu): row blocks [rb0, rb1) of buffer w hold the
+// projection's rows row0 .. row0 + rows - 1 (counted from the buffer's row 0).
+struct ProjTiles {
+    const uint8_t *w;      // the buffer's first row block
+    int nku, bits, group, step_bytes;
+    int row0, rows, K;
+};
+bool layer_proj_tiles(const ::gattn_layer *layer, int proj, ProjTiles *out);
+
 // ------------------------------------------------------------- attention
 
 constexpr int kAttnWarps = 8;          // consumer warps
@@ -175,3 +187,6 @@ int attn_smem_bytes(int MT, int DB);
 cudaError_t attn_set_smem_limits();
 
 }  // namespace gattn
+
+// records the thread-local message returned by gattn_last_error()
+void gattn_set_error(const char *msg);

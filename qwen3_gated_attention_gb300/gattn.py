@@ -29,7 +29,7 @@ EXPORTS = (
     "gattn_kv_register", "gattn_layer_step", "gattn_layer_poll_status", "gattn_layer_set_taps",
     "gattn_layer_destroy", "gattn_kv_destroy", "gattn_last_error", "gattn_pack_affine_host",
     "gattn_unpack_codes_device", "gattn_layer_dequant_device", "gattn_head_chunk_plan",
-    "gattn_layer_launches_per_step", "gattn_layer_set_events",
+    "gattn_layer_launches_per_step", "gattn_layer_set_events", "gattn_layer_dequant_device_static",
 )
 
 
@@ -95,6 +95,7 @@ def lib():
         L.gattn_pack_affine_host.argtypes = [p, i64, i64, i32, i32, p, p, p]
         L.gattn_unpack_codes_device.argtypes = [p, i64, i64, i32, p, p]
         L.gattn_layer_dequant_device.argtypes = [p, i32, p, p]
+        L.gattn_layer_dequant_device_static.argtypes = [p, i32, p, p]
         L.gattn_head_chunk_plan.argtypes = [i32, i32, i32, i32, p, p, i32]
         L.gattn_head_chunk_plan.restype = i32
         L.gattn_layer_launches_per_step.argtypes = [p]
@@ -103,7 +104,8 @@ def lib():
         for name in ("gattn_cfg_validate", "gattn_layer_create", "gattn_layer_set_weights",
                      "gattn_kv_register", "gattn_layer_step", "gattn_layer_poll_status",
                      "gattn_layer_set_taps", "gattn_pack_affine_host", "gattn_unpack_codes_device",
-                     "gattn_layer_dequant_device", "gattn_layer_set_events"):
+                     "gattn_layer_dequant_device", "gattn_layer_set_events",
+                     "gattn_layer_dequant_device_static"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -228,6 +230,12 @@ def unpack_codes_device(packed: int, N: int, K: int, bits: int, codes: int, stre
 
 def layer_dequant_device(layer: int, proj: int, w: int, stream: int = 0):
     _check(lib().gattn_layer_dequant_device(layer, proj, w, stream))
+
+
+def layer_dequant_device_static(layer: int, proj: int, w: int, stream: int = 0):
+    """Like layer_dequant_device but allocation-free (fixed device staging array,
+    no synchronization); see include/gattn.h for the size limit."""
+    _check(lib().gattn_layer_dequant_device_static(layer, proj, w, stream))
 
 
 def head_chunk_plan(q_len: int, num_heads: int, num_kv_heads: int, enabled: bool = True):
