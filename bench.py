@@ -221,6 +221,25 @@ def config_dict(spec, args, extra=None):
 
 # ------------------------------------------------------------------ ours
 
+# ----------------------------------------------------- replicas across ranks
+
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (a time: the job ends with its slowest
+    replica); the value itself when there is one rank."""
+    import torch
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, elapsed_ms, world):
+    """Whole-job throughput: the units all replicas processed over the job's
+    (slowest rank's) time."""
+    return world * units_per_rank / (elapsed_ms / 1e3)
+
+
 def our_arm(args, spec):
     import torch
     import torch.distributed as dist
@@ -337,13 +356,10 @@ def our_arm(args, spec):
     stream.synchronize()
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
-    elapsed_ms = ev0.elapsed_time(ev1)
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dist if world > 1 else None, dev)
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
         dist.barrier()
-    steps_per_s = world * K / (elapsed_ms / 1e3)
+    steps_per_s = job_rate(K, elapsed_ms, world)
     for dl in layers:
         gattn.layer_poll_status(dl.h, sh)
 
@@ -402,12 +418,8 @@ def our_arm(args, spec):
             oh.copy_(outs[i % n_inst], non_blocking=True)
         e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_rate = world * n_e2e / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist if world > 1 else None, dev)
+    e2e_rate = job_rate(n_e2e, e2e_ms, world)
 
     tokens_per_step = spec.batch * spec.q_len
     line = {
