@@ -287,7 +287,8 @@ def our_arm(args, spec):
     layers = []
     for _ in range(n_inst):
         dl = DeviceLayer(spec, packed, qn, kn, cap, head_chunk=not args.no_head_chunk,
-                         device=dev)
+                         device=dev, path={"auto": gattn.PATH_AUTO, "fused": gattn.PATH_FUSED,
+                                           "split": gattn.PATH_SPLIT}[args.path])
         dl._w = None          # interchange copies are no longer needed after repacking
         dl.load_cache(ck, cv)
         layers.append(dl)
@@ -364,7 +365,11 @@ def our_arm(args, spec):
         gattn.layer_poll_status(dl.h, sh)
 
     # per-kernel pass: events between the step's kernels (programmatic overlap off)
-    names = ["xprep", "proj_qkv", "attn", "merge", "proj_o"]
+    if launches == 1:
+        names = ["layer_step"]
+        kernel_bytes = {"layer_step": step_bytes}
+    else:
+        names = ["xprep", "proj_qkv", "attn", "merge", "proj_o"]
     nper = min(K, max(n_inst, 4 * n_inst))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(nper)]
     per_kernel_ms = {n: [] for n in names}
@@ -429,7 +434,8 @@ def our_arm(args, spec):
         "config": config_dict(spec, args, {
             "l2": f"rotating {n_inst} layer instances, {n_inst * inst_bytes / 2**20:.0f} MiB "
                   f"> 4x L2 ({l2 / 2**20:.0f} MiB)",
-            "arith": "bf16/fp16 tensor-core operands, fp32 accumulate; 8/4/6/3-bit codes"}),
+            "arith": "bf16/fp16 tensor-core operands, fp32 accumulate; 8/4/6/3-bit codes",
+            "path": "one kernel per step" if launches == 1 else "five kernels per step"}),
         "tokens_per_s": steps_per_s * tokens_per_step,
         "hbm_gbs": steps_per_s / world * step_bytes / 1e9,
         "hbm_frac_of_peak": steps_per_s / world * step_bytes / 1e9 / peak,
@@ -462,6 +468,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-head-chunk", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "split"],
+                    help="one-kernel or five-kernel step (auto: one kernel when it fits)")
     args = ap.parse_args()
     spec = synth.WORKLOADS[args.workload]
     if args.impl == "reference":

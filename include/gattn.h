@@ -246,17 +246,39 @@ int32_t gattn_head_chunk_plan(int32_t q_len, int32_t num_heads, int32_t num_kv_h
                               int32_t enabled, int32_t *chunk_first_head, int32_t *chunk_len,
                               int32_t cap);
 
+/*
+ * Which kernels run a step (an execution choice; both compute the same layer,
+ * equal up to fp32 summation order):
+ *   GATTN_PATH_AUTO   (default) the faster path for the step; in this build
+ *                     that is the five-kernel path.
+ *   GATTN_PATH_FUSED  the one-kernel path; a step that does not fit it fails
+ *                     with GATTN_E_UNSUPPORTED (nothing is launched).
+ *   GATTN_PATH_SPLIT  always the five-kernel path.
+ * One-kernel path: one persistent CTA per SM, launched cooperatively, runs the
+ * q|k|v projection with its epilogue, attention, the merge with the gate and
+ * o_proj, handing data between CTAs through flags in library scratch.  A step
+ * fits it when batch*q_len <= 8 (<= 4 for fp32 x), batch <= 8, head_dim is 64,
+ * 128 or 256, num_kv_heads*head_dim is a multiple of lcm(head_dim, 128), the
+ * device supports cooperative launch and its shared memory holds the ring.
+ * Five-kernel path: x operand prep, fused q|k|v projection, attention,
+ * attention merge + gate, o_proj, chained with programmatic dependent launch.
+ * Errors: GATTN_E_INVALID_ARG for a NULL layer or an unknown path.
+ */
+enum { GATTN_PATH_AUTO = 0, GATTN_PATH_FUSED = 1, GATTN_PATH_SPLIT = 2 };
+gattn_status gattn_layer_set_path(gattn_layer *layer, int32_t path);
+
 /* Per-step launch report of the layer's last step: number of kernel launches
- * it enqueued (all of them this library's own kernels: x operand prep, fused
- * q|k|v projection, attention, attention merge + gate, o_proj). */
+ * it enqueued, all of them this library's own kernels (1 on the one-kernel
+ * path, 5 on the five-kernel path). */
 int32_t gattn_layer_launches_per_step(const gattn_layer *layer);
 
-/* Instrumentation: with n == launches_per_step + 1 cudaEvent_t handles, each
- * following step records events[i] on its stream right before its i-th kernel
- * launch and events[n-1] after the last one, so per-kernel durations can be
- * read with cudaEventElapsedTime.  n == 0 (or events == NULL) turns it off.
- * The events are borrowed.  Recording between kernels serializes them (no
- * programmatic overlap), so use it for per-kernel timing passes only. */
+/* Instrumentation: with n >= 2 cudaEvent_t handles, each following step
+ * records events[i] on its stream right before its i-th kernel launch (for
+ * i < n - 1) and events[n-1] after its last launch, so per-kernel durations
+ * can be read with cudaEventElapsedTime (use n = launches_per_step + 1).
+ * n == 0 (or events == NULL) turns it off.  The events are borrowed.
+ * Recording between kernels serializes them (no programmatic overlap), so use
+ * it for per-kernel timing passes only. */
 gattn_status gattn_layer_set_events(gattn_layer *layer, void *const *events, int32_t n);
 
 #ifdef __cplusplus

@@ -6,6 +6,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <numeric>
 #include <string>
 #include <vector>
 
@@ -118,7 +119,6 @@ struct ProjPlan {
 
 int nt_index(int NT) { return NT == 1 ? 0 : (NT == 2 ? 1 : 2); }
 
-constexpr int kLaunchesPerStep = 5;  // xprep, q|k|v projection, attention, merge, o_proj
 constexpr int kAttnMinUnits = 4;     // 16-token units per attention CTA, at least
 constexpr int kMaxCluster = 8;       // portable cluster size
 
@@ -172,6 +172,15 @@ struct gattn_layer {
     size_t ws_attn_floats = 0;
     int attn_grid = 0;
     int max_seg = 0;
+    // one-kernel path (steps with at most 8 operand columns)
+    bool fused_ok = false;                 // the configuration admits it
+    int path = GATTN_PATH_AUTO;
+    int fused_smem_max = 0;
+    int fused_occ_smem = -1, fused_occ = 0;   // occupancy at that shared-memory size
+    int GR = 0, ngrp = 0;                  // q|k|v epilogue group rows, groups
+    float *part_a = nullptr, *part_o = nullptr;
+    unsigned *sync = nullptr;
+    int s_cnt_a = 0, s_rdy_a = 0, s_seg = 0, s_xo = 0, s_cnt_o = 0, nsync = 0;
     gattn_taps taps{};
     bool weights_set = false;
     int launches = 0;
@@ -338,6 +347,37 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaMalloc(&L->ws_attn, L->ws_attn_floats * sizeof(float)));
     TRY(cudaMalloc(&L->status, sizeof(unsigned)));
     TRY(cudaMemset(L->status, 0, sizeof(unsigned)));
+
+    // the one-kernel path: whole heads per epilogue group (GR = lcm(d, 128)
+    // rows tiling the k and v rows), every CTA resident (cooperative launch)
+    {
+        const int d = c.head_dim;
+        L->GR = d * kRBR / std::gcd(d, kRBR);
+        int coop = 0, optin = 0;
+        TRY(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, L->device));
+        TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->device));
+        L->fused_smem_max = optin;
+        L->fused_ok = coop && (d == 64 || d == 128 || d == 256) && L->Nkv % L->GR == 0 &&
+                      L->num_sms + 1 <= kFMaxContrib;
+        if (L->fused_ok) {
+            static std::once_flag fonce;
+            static cudaError_t ferr = cudaSuccess;
+            std::call_once(fonce, [optin] { ferr = fused_set_smem_limits(optin); });
+            TRY(ferr);
+            L->ngrp = (L->Nq + 2 * L->Nkv) / L->GR;
+            const int nrb_a = (L->Nq + 2 * L->Nkv) / kRBR, nrb_o = c.hidden / kRBR;
+            L->s_cnt_a = 2;
+            L->s_rdy_a = L->s_cnt_a + L->ngrp;
+            L->s_seg = L->s_rdy_a + L->ngrp;
+            L->s_xo = L->s_seg + L->max_seg;
+            L->s_cnt_o = L->s_xo + (int)nku_o;
+            L->nsync = L->s_cnt_o + nrb_o;
+            TRY(cudaMalloc(&L->part_a, (size_t)(L->num_sms + nrb_a) * 1024 * sizeof(float)));
+            TRY(cudaMalloc(&L->part_o, (size_t)(L->num_sms + nrb_o) * 1024 * sizeof(float)));
+            TRY(cudaMalloc(&L->sync, (size_t)L->nsync * sizeof(unsigned)));
+            TRY(cudaMemset(L->sync, 0, (size_t)L->nsync * sizeof(unsigned)));
+        }
+    }
     std::vector<double> inv(L->rd / 2);
     for (int i = 0; i < L->rd / 2; ++i)
         inv[i] = std::pow((double)c.rope_theta, -2.0 * (double)i / (double)L->rd);
@@ -356,7 +396,7 @@ void gattn_layer_destroy(gattn_layer *L)
         return;
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq,
-                    L->q_norm, L->k_norm};
+                    L->q_norm, L->k_norm, L->part_a,  L->part_o,  L->sync};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -459,13 +499,22 @@ gattn_status gattn_layer_set_taps(gattn_layer *L, const gattn_taps *t)
 
 int32_t gattn_layer_launches_per_step(const gattn_layer *L) { return L ? L->launches : -1; }
 
+gattn_status gattn_layer_set_path(gattn_layer *L, int32_t path)
+{
+    if (!L)
+        return fail(GATTN_E_INVALID_ARG, "layer is NULL");
+    if (path != GATTN_PATH_AUTO && path != GATTN_PATH_FUSED && path != GATTN_PATH_SPLIT)
+        return fail(GATTN_E_INVALID_ARG, "unknown path %d", (int)path);
+    L->path = path;
+    return GATTN_OK;
+}
+
 gattn_status gattn_layer_set_events(gattn_layer *L, void *const *events, int32_t n)
 {
     if (!L || n < 0 || (n > 0 && !events))
         return fail(GATTN_E_INVALID_ARG, "bad event arguments");
-    if (n != 0 && n != kLaunchesPerStep + 1)
-        return fail(GATTN_E_INVALID_ARG, "need launches_per_step + 1 = %d events",
-                    kLaunchesPerStep + 1);
+    if (n == 1)
+        return fail(GATTN_E_INVALID_ARG, "need at least 2 events (before and after a step)");
     L->events.assign(reinterpret_cast<cudaEvent_t const *>(events),
                      reinterpret_cast<cudaEvent_t const *>(events) + n);
     return GATTN_OK;
@@ -495,10 +544,136 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     const int nia = nt_index(NTa), ni = nt_index(NT);
     const bool timing = !L->events.empty();
     const bool pdl = L->pdl && !timing;
+    const int nev = (int)L->events.size();
     int launches = 0;
+    // events[i] before the i-th launch (i < n - 1), events[n - 1] after the last
     auto mark = [&](int i) -> cudaError_t {
-        return timing ? cudaEventRecord(L->events[i], s) : cudaSuccess;
+        return timing && i < nev - 1 ? cudaEventRecord(L->events[i], s) : cudaSuccess;
     };
+    auto mark_end = [&]() -> cudaError_t {
+        return timing ? cudaEventRecord(L->events[nev - 1], s) : cudaSuccess;
+    };
+
+    // attention segments: per KV group the head chunks of the verify plan, a
+    // chunk of more than 64 rows cut into row blocks of whole heads
+    AttnArgs t{};
+    int32_t first[kMaxRowBlocks * 64], len[kMaxRowBlocks * 64];
+    const int nchunks = gattn_head_chunk_plan(q_len, c.num_heads, c.num_kv_heads, c.head_chunk,
+                                              first, len, kMaxRowBlocks * 64);
+    const int per_group = nchunks / c.num_kv_heads;
+    int nrb = 0, max_rows = 0;
+    for (int j = 0; j < per_group; ++j) {
+        const int hpb = std::max(1, 64 / q_len);
+        for (int h = 0; h < len[j]; h += hpb) {
+            if (nrb >= kMaxRowBlocks)
+                return fail(GATTN_E_UNSUPPORTED, "too many attention row blocks");
+            t.rb_h0[nrb] = first[j] + h;
+            t.rb_nh[nrb] = std::min(hpb, len[j] - h);
+            max_rows = std::max(max_rows, t.rb_nh[nrb] * q_len);
+            ++nrb;
+        }
+    }
+    if ((long long)batch * c.num_kv_heads * nrb > L->max_seg)
+        return fail(GATTN_E_UNSUPPORTED, "attention segments exceed the scratch sized at create");
+    const int MT = (max_rows + 15) / 16;
+    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+
+    // ---- one kernel for the whole step when the operand is one column tile
+    // the default stays on the five-kernel path until the one-kernel path is faster
+    if (L->path == GATTN_PATH_FUSED) {
+        // x arrives by bulk copy: 16-byte alignment
+        bool ok = L->fused_ok && Ma <= 8 && batch <= kFMaxB && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+        FusedArgs f{};
+        if (ok) {
+            f.wa = L->pqkv.w;
+            f.wo = L->po.w;
+            f.bits_a = L->pqkv.bits;
+            f.group_a = L->pqkv.group;
+            f.ubytes_a = L->pqkv.ubytes;
+            f.step_a = L->pqkv.step_bytes;
+            f.nrb_a = (L->Nq + 2 * L->Nkv) / kRBR;
+            f.nku_a = L->pqkv.nku;
+            f.Na = L->Nq + 2 * L->Nkv;
+            f.bits_o = L->po.bits;
+            f.group_o = L->po.group;
+            f.ubytes_o = L->po.ubytes;
+            f.step_o = L->po.step_bytes;
+            f.nrb_o = c.hidden / kRBR;
+            f.nku_o = L->po.nku;
+            f.No = c.hidden;
+            f.x = x;
+            f.x_f32 = c.x_dtype == GATTN_DTYPE_F32;
+            f.M = M;
+            f.Mx = Ma;
+            f.B = batch;
+            f.R = q_len;
+            f.cache_pos = cache_pos;
+            f.H = c.num_heads;
+            f.Hk = c.num_kv_heads;
+            f.d = c.head_dim;
+            f.rd = L->rd;
+            f.gqa = L->gqa;
+            f.Nq = L->Nq;
+            f.Nkv = L->Nkv;
+            f.GR = L->GR;
+            f.ngrp = L->ngrp;
+            f.eps = c.rms_eps;
+            f.scale_log2 = scale_log2;
+            f.q_norm = L->q_norm;
+            f.k_norm = L->k_norm;
+            f.inv_freq = L->inv_freq;
+            f.kc = static_cast<__nv_bfloat16 *>(kv->desc.k);
+            f.vc = static_cast<__nv_bfloat16 *>(kv->desc.v);
+            f.st_tok = kv->desc.stride_token;
+            f.st_head = kv->desc.stride_head;
+            f.st_batch = kv->desc.stride_batch;
+            f.cap = kv->desc.capacity;
+            f.nrb = nrb;
+            f.MT = MT;
+            f.min_units = kAttnMinUnits;
+            for (int i = 0; i < nrb; ++i) {
+                f.rb_h0[i] = t.rb_h0[i];
+                f.rb_nh[i] = t.rb_nh[i];
+            }
+            f.part_a = L->part_a;
+            f.part_o = L->part_o;
+            f.qn = L->qn;
+            f.gate = L->gate;
+            f.ws = L->ws_attn;
+            f.x16o = L->x16_o;
+            f.xsumo = L->xsum_o;
+            f.sync = L->sync;
+            f.s_cnt_a = L->s_cnt_a;
+            f.s_rdy_a = L->s_rdy_a;
+            f.s_seg = L->s_seg;
+            f.s_xo = L->s_xo;
+            f.s_cnt_o = L->s_cnt_o;
+            f.nsync = L->nsync;
+            f.out = static_cast<__nv_bfloat16 *>(out);
+            f.tap_y = L->taps.y;
+            f.tap_attn = L->taps.attn;
+            f.status = L->status;
+            ok = fused_plan(f, L->num_sms, L->fused_smem_max);
+        }
+        if (ok && f.smem_bytes != L->fused_occ_smem) {
+            int occ = 0;
+            CUDA_TRY(fused_occupancy(f.smem_bytes, &occ));
+            L->fused_occ_smem = f.smem_bytes;
+            L->fused_occ = occ;
+        }
+        ok = ok && L->fused_occ >= 1;
+        if (ok) {
+            CUDA_TRY(mark(0));
+            CUDA_TRY(launch_fused(f, kv->kmap, kv->vmap, L->num_sms, s));
+            CUDA_TRY(mark_end());
+            L->launches = 1;
+            return GATTN_OK;
+        }
+        if (L->path == GATTN_PATH_FUSED)
+            return fail(GATTN_E_UNSUPPORTED,
+                        "this step cannot run as one kernel (needs batch*q_len <= 8, or <= 4 "
+                        "for fp32 x, head_dim 64/128/256, whole heads per 128-row block)");
+    }
 
     // 1. x -> fp16 tensor-core operand + group sums
     CUDA_TRY(mark(0));
@@ -552,7 +727,6 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     ++launches;
 
     // 3. attention + merge + gate -> o_proj operand
-    AttnArgs t{};
     t.qn = L->qn;
     t.gate = L->gate;
     t.cache_pos = cache_pos;
@@ -562,27 +736,8 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     t.Hk = c.num_kv_heads;
     t.d = c.head_dim;
     t.cap = kv->desc.capacity;
-    int32_t first[kMaxRowBlocks * 64], len[kMaxRowBlocks * 64];
-    const int nchunks = gattn_head_chunk_plan(q_len, c.num_heads, c.num_kv_heads, c.head_chunk,
-                                              first, len, kMaxRowBlocks * 64);
-    const int per_group = nchunks / c.num_kv_heads;
-    int nrb = 0, max_rows = 0;
-    for (int j = 0; j < per_group; ++j) {
-        // a chunk of more than 64 rows is cut into row blocks of whole heads
-        const int hpb = std::max(1, 64 / q_len);
-        for (int h = 0; h < len[j]; h += hpb) {
-            if (nrb >= kMaxRowBlocks)
-                return fail(GATTN_E_UNSUPPORTED, "too many attention row blocks");
-            t.rb_h0[nrb] = first[j] + h;
-            t.rb_nh[nrb] = std::min(hpb, len[j] - h);
-            max_rows = std::max(max_rows, t.rb_nh[nrb] * q_len);
-            ++nrb;
-        }
-    }
-    if ((long long)batch * c.num_kv_heads * nrb > L->max_seg)
-        return fail(GATTN_E_UNSUPPORTED, "attention segments exceed the scratch sized at create");
     t.nrb = nrb;
-    t.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+    t.scale_log2 = scale_log2;
     t.ws = L->ws_attn;
     t.min_units = kAttnMinUnits;
     t.grid = L->attn_grid;
@@ -592,7 +747,6 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     t.group_o = L->po.group;
     t.tap_attn = L->taps.attn;
     t.status = L->status;
-    const int MT = (max_rows + 15) / 16;
     CUDA_TRY(mark(2));
     CUDA_TRY(launch_attn(MT, c.head_dim / 64, t, kv->kmap, kv->vmap, L->attn_grid, pdl, s));
     ++launches;
@@ -625,7 +779,7 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     CUDA_TRY(mark(4));
     CUDA_TRY(launch_proj(L->po.bits, NT, kModeO, o, eq, e2, L->po.grid[ni], pdl, s));
     ++launches;
-    CUDA_TRY(mark(5));
+    CUDA_TRY(mark_end());
     L->launches = launches;
     return GATTN_OK;
 }

@@ -42,36 +42,6 @@ struct AttnSmem {
     static constexpr int kTotal = kFlags + 256 + 1024;        // + alignment slack
 };
 
-struct Piece {
-    int b, kh, rb;
-    long long seg;          // global segment id (b, kh, rb order)
-    long long seg_start, seg_end;
-    int u0, u1;             // units [u0, u1) of the segment in this piece
-};
-
-// Locate the piece that starts at unit `pos`.
-__device__ __forceinline__ Piece find_piece(const long long *prefix, const int *ub, int B, int Hk,
-                                            int nrb, long long pos, long long end)
-{
-    Piece p;
-    int b = 0;
-    while (b + 1 < B && prefix[b + 1] <= pos)
-        ++b;
-    const long long U = ub[b];
-    const long long loc = pos - prefix[b];
-    const long long segl = loc / U;
-    p.b = b;
-    p.kh = (int)(segl / nrb);
-    p.rb = (int)(segl % nrb);
-    p.seg = ((long long)b * Hk + p.kh) * nrb + p.rb;
-    p.seg_start = prefix[b] + segl * U;
-    p.seg_end = p.seg_start + U;
-    p.u0 = (int)(loc - segl * U);
-    const long long pe = end < p.seg_end ? end : p.seg_end;
-    p.u1 = (int)(pe - p.seg_start);
-    return p;
-}
-
 template <int MT, int DB>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,

@@ -159,6 +159,39 @@ __host__ __device__ inline long long attn_ranges(long long T, long long grid, in
     return g > 0 ? g : 1;
 }
 
+// One CTA's share of one segment: segments are (sequence b, KV head kh, row
+// block rb) in that order, each cut into ub[b] 16-token units; prefix[b] is
+// the first unit of sequence b's segments.
+struct Piece {
+    int b, kh, rb;
+    long long seg;          // global segment id (b, kh, rb order)
+    long long seg_start, seg_end;
+    int u0, u1;             // units [u0, u1) of the segment in this piece
+};
+
+// Locate the piece that starts at unit `pos`.
+__device__ __forceinline__ Piece find_piece(const long long *prefix, const int *ub, int B, int Hk,
+                                            int nrb, long long pos, long long end)
+{
+    Piece p;
+    int b = 0;
+    while (b + 1 < B && prefix[b + 1] <= pos)
+        ++b;
+    const long long U = ub[b];
+    const long long loc = pos - prefix[b];
+    const long long segl = loc / U;
+    p.b = b;
+    p.kh = (int)(segl / nrb);
+    p.rb = (int)(segl % nrb);
+    p.seg = ((long long)b * Hk + p.kh) * nrb + p.rb;
+    p.seg_start = prefix[b] + segl * U;
+    p.seg_end = p.seg_start + U;
+    p.u0 = (int)(loc - segl * U);
+    const long long pe = end < p.seg_end ? end : p.seg_end;
+    p.u1 = (int)(pe - p.seg_start);
+    return p;
+}
+
 struct AttnArgs {
     const __nv_bfloat16 *qn;     // [B][R][H][d]
     const float *gate;           // [M][H*d]
@@ -185,6 +218,66 @@ cudaError_t launch_attn(int MT, int DB, const AttnArgs &a, const CUtensorMap &km
 cudaError_t launch_attn_merge(const AttnArgs &a, int max_rows, bool pdl, cudaStream_t s);
 int attn_smem_bytes(int MT, int DB);
 cudaError_t attn_set_smem_limits();
+
+// ------------------------------------------------- one-kernel layer step
+//
+// For steps whose operand has at most 8 columns (batch * q_len <= 8, <= 4 for
+// fp32 x) the whole step runs as one persistent kernel, one CTA per SM,
+// launched cooperatively (every CTA resident, so CTAs may wait on flags that
+// other CTAs set).  See fused.cu.
+
+constexpr int kFW = 8;                        // consumer warps
+constexpr int kFThreads = (kFW + 1) * 32;     // + one producer warp
+constexpr int kFEntries = 32;                 // ring entries in flight
+constexpr int kFMaxB = 8;                     // sequences per step
+constexpr int kFMaxContrib = 160;             // attention contributors per segment (>= SMs + 1)
+
+struct FusedArgs {
+    // projections in the device tile layout
+    const uint8_t *wa, *wo;
+    int bits_a, group_a, ubytes_a, step_a, nrb_a, nku_a, Na;
+    int bits_o, group_o, ubytes_o, step_o, nrb_o, nku_o, No;
+    // step inputs
+    const void *x;
+    int x_f32, M, Mx, B, R;          // Mx: operand columns (2M for fp32 x: hi and lo planes)
+    const int *cache_pos;
+    // layer
+    int H, Hk, d, rd, gqa, Nq, Nkv;
+    int GR, ngrp;                    // q|k|v rows per epilogue group (lcm(d, 128)), groups
+    float eps, scale_log2;
+    const uint16_t *q_norm, *k_norm;
+    const double *inv_freq;
+    // caller's bf16 cache (element strides)
+    __nv_bfloat16 *kc, *vc;
+    long long st_tok, st_head, st_batch;
+    int cap;
+    // attention segments: per KV head nrb row blocks of whole query heads
+    int nrb, MT, min_units;
+    int rb_h0[kMaxRowBlocks], rb_nh[kMaxRowBlocks];
+    // library scratch
+    float *part_a, *part_o;          // split-K partials, [slot][8 columns][128 rows]
+    __nv_bfloat16 *qn;               // [M][H][d]
+    float *gate;                     // [M][H*d]
+    float *ws;                       // attention partial slots
+    __half *x16o;                    // o_proj operand, one-column-tile fragment order
+    float *xsumo;                    // its group sums
+    unsigned *sync;                  // counters and flags, all zero between steps
+    int s_cnt_a, s_rdy_a, s_seg, s_xo, s_cnt_o, nsync;
+    __nv_bfloat16 *out;              // [M][No]
+    float *tap_y, *tap_attn;
+    unsigned *status;
+    // shared memory plan: byte offsets from the 1024-aligned base
+    int ring_bytes, xslots, xslot_bytes, off_x, off_u, off_red, off_misc, smem_bytes;
+};
+
+// Sizes the shared-memory plan of `a` (ring, x slots, scratch) for the given
+// attention tile rows; false when the step does not fit one CTA per SM.
+bool fused_plan(FusedArgs &a, int num_sms, int max_smem);
+cudaError_t fused_set_smem_limits(int bytes);
+// CTAs of the fused kernel that can be resident at once (cooperative limit)
+cudaError_t fused_occupancy(int smem, int *blocks_per_sm);
+cudaError_t launch_fused(const FusedArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                         int grid, cudaStream_t s);
 
 }  // namespace gattn
 

@@ -30,7 +30,8 @@ class DeviceLayer:
     """One layer handle with its weights set and one registered bf16 cache."""
 
     def __init__(self, spec, packed, q_norm, k_norm, capacity, *, batch=None, max_batch=None,
-                 max_q_len=None, head_chunk=True, layout="bhtd", device="cuda:0"):
+                 max_q_len=None, head_chunk=True, layout="bhtd", device="cuda:0",
+                 path=gattn.PATH_AUTO):
         self.spec = spec
         self.device = torch.device(device)
         self.batch = batch or spec.batch
@@ -44,6 +45,7 @@ class DeviceLayer:
         self.h = gattn.layer_create(self.cfg)
         self.kv = 0
         try:
+            gattn.layer_set_path(self.h, path)
             self._w = [(_dev_u32(p, self.device), _dev_u16(s, self.device), _dev_u16(b, self.device))
                        for p, s, b in packed]
             self._qn = _dev_u16(q_norm, self.device)

@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "GATTN_OK", 1: "GATTN_E_INVALID_ARG", 2: "GATTN_E_UNSUPPORTED
                 6: "GATTN_E_DEVICE_TIMEOUT"}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 PROJ_Q, PROJ_K, PROJ_V, PROJ_O = 0, 1, 2, 3
+PATH_AUTO, PATH_FUSED, PATH_SPLIT = 0, 1, 2
 
 # every symbol include/gattn.h declares
 EXPORTS = (
@@ -30,6 +31,7 @@ EXPORTS = (
     "gattn_layer_destroy", "gattn_kv_destroy", "gattn_last_error", "gattn_pack_affine_host",
     "gattn_unpack_codes_device", "gattn_layer_dequant_device", "gattn_head_chunk_plan",
     "gattn_layer_launches_per_step", "gattn_layer_set_events", "gattn_layer_dequant_device_static",
+    "gattn_layer_set_path",
 )
 
 
@@ -101,11 +103,12 @@ def lib():
         L.gattn_layer_launches_per_step.argtypes = [p]
         L.gattn_layer_launches_per_step.restype = i32
         L.gattn_layer_set_events.argtypes = [p, p, i32]
+        L.gattn_layer_set_path.argtypes = [p, i32]
         for name in ("gattn_cfg_validate", "gattn_layer_create", "gattn_layer_set_weights",
                      "gattn_kv_register", "gattn_layer_step", "gattn_layer_poll_status",
                      "gattn_layer_set_taps", "gattn_pack_affine_host", "gattn_unpack_codes_device",
                      "gattn_layer_dequant_device", "gattn_layer_set_events",
-                     "gattn_layer_dequant_device_static"):
+                     "gattn_layer_dequant_device_static", "gattn_layer_set_path"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -202,6 +205,11 @@ def kv_destroy(kv: int) -> None:
 
 def layer_launches_per_step(layer: int) -> int:
     return int(lib().gattn_layer_launches_per_step(layer))
+
+
+def layer_set_path(layer: int, path: int) -> None:
+    """Which kernels run the layer's steps: PATH_AUTO, PATH_FUSED or PATH_SPLIT."""
+    _check(lib().gattn_layer_set_path(layer, path))
 
 
 def layer_set_events(layer: int, events) -> None:

@@ -29,13 +29,16 @@ def gpu():
     torch.cuda.init()
 
 
+PATHS = {"fused": gattn.PATH_FUSED, "split": gattn.PATH_SPLIT}
+
+
 def gpu_run(case, head_chunk=True, layout="bhtd", taps=True, pos=None, x=None, q_len=None,
-            batch=None, dl=None, keep=False):
+            batch=None, dl=None, keep=False, path=gattn.PATH_AUTO):
     spec = case.spec
     own = dl is None
     if own:
         dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap,
-                         head_chunk=head_chunk, layout=layout)
+                         head_chunk=head_chunk, layout=layout, path=path)
         dl.load_cache(case.ck, case.cv)
     B = batch or spec.batch
     R = q_len or spec.q_len
@@ -49,10 +52,18 @@ def gpu_run(case, head_chunk=True, layout="bhtd", taps=True, pos=None, x=None, q
     out = torch.full((B, R, Hd), float("nan"), dtype=torch.bfloat16, device="cuda")
     xd = x_to_device(spec, xx)
     pd = torch.from_numpy(np.ascontiguousarray(pp, np.int32)).cuda()
-    dl.step(xd, pd, out, batch=B, q_len=R)
+    try:
+        dl.step(xd, pd, out, batch=B, q_len=R)
+    except gattn.GattnError as e:
+        if own:
+            dl.close()
+        if e.status == 2 and path == gattn.PATH_FUSED:
+            pytest.skip(f"the one-kernel path does not take this step: {e}")
+        raise
     dl.poll()
     k, v = dl.read_cache()
-    res = dict(out=out.float().cpu().numpy().astype(np.float64), k=k, v=v)
+    res = dict(out=out.float().cpu().numpy().astype(np.float64), k=k, v=v,
+               launches=gattn.layer_launches_per_step(dl.h))
     if taps:
         res["y"] = ty.cpu().numpy().astype(np.float64).reshape(B, R, Ny)
         res["attn"] = ta.cpu().numpy().astype(np.float64).reshape(B, R, H, d)
@@ -61,6 +72,23 @@ def gpu_run(case, head_chunk=True, layout="bhtd", taps=True, pos=None, x=None, q
     elif keep:
         res["dl"] = dl
     return res
+
+
+def assert_rows_close(rows_g, rows_r, what):
+    """Appended bf16 cache rows: within one bf16 ulp; near-zero elements, where
+    the fp32 dot product over K terms may move a tiny value by more than its own
+    ulp, within one ulp plus 1e-5 of the row's RMS (fp32 accumulation error)."""
+    ulp = bf16_ulp_distance(rows_g, rows_r)
+    if ulp.max() <= 1:
+        return
+    vg = bf16_bits_to_f32(rows_g).astype(np.float64)
+    vr = bf16_bits_to_f32(rows_r).astype(np.float64)
+    rms = np.sqrt(np.mean(vr ** 2, axis=-1, keepdims=True))
+    ulp_r = np.abs(vr) * 2.0 ** -7 + 1e-38
+    bad = np.abs(vg - vr) > ulp_r + 1e-5 * rms
+    worst = np.unravel_index(np.argmax(ulp), ulp.shape)
+    assert not bad.any(), (f"{what} rows differ by {ulp.max()} ulp at {worst}: "
+                           f"{vg[worst]} vs {vr[worst]}")
 
 
 def check_parity(case, got, ref, batches=None, what=""):
@@ -75,21 +103,7 @@ def check_parity(case, got, ref, batches=None, what=""):
     for name, gc, rc, before in (("k", gk, ref["k"], case.ck[idx]), ("v", gv, ref["v"], case.cv[idx])):
         for j in range(len(idx)):
             p = int(pos[j])
-            rows_g = gc[j, :, p:p + R]
-            rows_r = rc[j, :, p:p + R]
-            ulp = bf16_ulp_distance(rows_g, rows_r)
-            if ulp.max() > 1:
-                # near-zero elements: the fp32 dot product over K terms may move
-                # a tiny value by more than its own bf16 ulp; bound the error by
-                # one ulp plus 1e-5 of the row's RMS (fp32 accumulation error)
-                vg = bf16_bits_to_f32(rows_g).astype(np.float64)
-                vr = bf16_bits_to_f32(rows_r).astype(np.float64)
-                rms = np.sqrt(np.mean(vr ** 2, axis=-1, keepdims=True))
-                ulp_r = np.abs(vr) * 2.0 ** -7 + 1e-38
-                bad = np.abs(vg - vr) > ulp_r + 1e-5 * rms
-                worst = np.unravel_index(np.argmax(ulp), ulp.shape)
-                assert not bad.any(), (f"{what}: {name} rows differ by {ulp.max()} ulp at "
-                                       f"{worst}: gpu {vg[worst]} oracle {vr[worst]}")
+            assert_rows_close(gc[j, :, p:p + R], rc[j, :, p:p + R], f"{what}: {name}")
             mask = np.ones(gc.shape[1:3], bool)
             mask[:, p:p + R] = False
             assert np.array_equal(gc[j][mask], before[j][mask]), f"{what}: {name} cache bytes changed"
@@ -117,13 +131,39 @@ SMALL = {
 }
 
 
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("name", list(SMALL))
-def test_layer_parity(name):
+def test_layer_parity(name, path):
     case = make_case(SMALL[name])
-    got = gpu_run(case)
+    got = gpu_run(case, path=PATHS[path])
+    assert got["launches"] == (1 if path == "fused" else 5)
     ref = oracle_run(case)
-    rep = check_parity(case, got, ref, what=name)
-    print(name, rep)
+    rep = check_parity(case, got, ref, what=f"{name} {path}")
+    print(name, path, rep)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_4b", "verify_2k_p2048", "batched_mixed_small",
+                                  "batch8_decode"])
+def test_one_kernel_and_five_kernel_paths_agree(name):
+    """Same layer, two schedules: the projections' split-K sums are added in
+    different orders, so results agree to fp32 rounding (cache rows to one
+    bf16 ulp, outputs to bf16 level); every untouched cache byte is equal."""
+    case = make_case(SMALL[name])
+    f = gpu_run(case, path=gattn.PATH_FUSED)
+    s = gpu_run(case, path=gattn.PATH_SPLIT)
+    assert f["launches"] == 1 and s["launches"] == 5
+    R = case.spec.q_len
+    for key in ("k", "v"):
+        for b in range(case.spec.batch):
+            p = int(case.pos[b])
+            assert_rows_close(f[key][b, :, p:p + R], s[key][b, :, p:p + R], f"{name} {key}")
+            mask = np.ones(f[key].shape[1:3], bool)
+            mask[:, p:p + R] = False
+            assert np.array_equal(f[key][b][mask], s[key][b][mask])
+    ok, rep = refs.close(f["out"], s["out"], abs_tol=2e-3, rel_tol=1e-2, l2_tol=2e-3)
+    assert ok, rep
+    ok, rep = refs.close(f["attn"], s["attn"], abs_tol=2e-3, rel_tol=1e-2, l2_tol=2e-3)
+    assert ok, rep
 
 
 @pytest.mark.parametrize("name", ["verify_2k_p46", "verify_2k_p2048", "d128_b5_b2"])
