@@ -176,11 +176,14 @@ struct gattn_layer {
     bool fused_ok = false;                 // the configuration admits it
     int path = GATTN_PATH_AUTO;
     int fused_smem_max = 0;
-    int fused_occ_smem = -1, fused_occ = 0;   // occupancy at that shared-memory size
+    // residency of the last instance launched, at its shared-memory size
+    cudaError_t (*fused_occ_fn)(const gattn::FusedArgs &, const CUtensorMap &, const CUtensorMap &,
+                                int, cudaStream_t) = nullptr;
+    int fused_occ_smem = -1, fused_occ = 0;
     int GR = 0, ngrp = 0;                  // q|k|v epilogue group rows, groups
     float *part_a = nullptr, *part_o = nullptr;
     unsigned *sync = nullptr;
-    int s_cnt_a = 0, s_rdy_a = 0, s_seg = 0, s_xo = 0, s_cnt_o = 0, nsync = 0;
+    int s_cnt_a = 0, s_rdy_a = 0, s_seg = 0, s_cnt_o = 0, nsync = 0;
     gattn_taps taps{};
     bool weights_set = false;
     int launches = 0;
@@ -360,20 +363,15 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
         L->fused_ok = coop && (d == 64 || d == 128 || d == 256) && L->Nkv % L->GR == 0 &&
                       L->num_sms + 1 <= kFMaxContrib;
         if (L->fused_ok) {
-            static std::once_flag fonce;
-            static cudaError_t ferr = cudaSuccess;
-            std::call_once(fonce, [optin] { ferr = fused_set_smem_limits(optin); });
-            TRY(ferr);
             L->ngrp = (L->Nq + 2 * L->Nkv) / L->GR;
             const int nrb_a = (L->Nq + 2 * L->Nkv) / kRBR, nrb_o = c.hidden / kRBR;
             L->s_cnt_a = 2;
             L->s_rdy_a = L->s_cnt_a + L->ngrp;
             L->s_seg = L->s_rdy_a + L->ngrp;
-            L->s_xo = L->s_seg + L->max_seg;
-            L->s_cnt_o = L->s_xo + (int)nku_o;
+            L->s_cnt_o = L->s_seg + L->max_seg;
             L->nsync = L->s_cnt_o + nrb_o;
             TRY(cudaMalloc(&L->part_a, (size_t)(L->num_sms + nrb_a) * 1024 * sizeof(float)));
-            TRY(cudaMalloc(&L->part_o, (size_t)(L->num_sms + nrb_o) * 1024 * sizeof(float)));
+            TRY(cudaMalloc(&L->part_o, (size_t)nku_o * nrb_o * 1024 * sizeof(float)));
             TRY(cudaMalloc(&L->sync, (size_t)L->nsync * sizeof(unsigned)));
             TRY(cudaMemset(L->sync, 0, (size_t)L->nsync * sizeof(unsigned)));
         }
@@ -640,13 +638,10 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
             f.qn = L->qn;
             f.gate = L->gate;
             f.ws = L->ws_attn;
-            f.x16o = L->x16_o;
-            f.xsumo = L->xsum_o;
             f.sync = L->sync;
             f.s_cnt_a = L->s_cnt_a;
             f.s_rdy_a = L->s_rdy_a;
             f.s_seg = L->s_seg;
-            f.s_xo = L->s_xo;
             f.s_cnt_o = L->s_cnt_o;
             f.nsync = L->nsync;
             f.out = static_cast<__nv_bfloat16 *>(out);
@@ -655,16 +650,23 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
             f.status = L->status;
             ok = fused_plan(f, L->num_sms, L->fused_smem_max);
         }
-        if (ok && f.smem_bytes != L->fused_occ_smem) {
+        FusedOps ops{};
+        if (ok)
+            ok = fused_ops(FusedKey{f.bits_a, f.group_a, f.bits_o, f.group_o, f.MT, c.head_dim / 64},
+                           &ops);
+        if (ok && (ops.launch != L->fused_occ_fn || f.smem_bytes != L->fused_occ_smem)) {
+            // once per instance and size: raise its shared-memory limit, check residency
             int occ = 0;
-            CUDA_TRY(fused_occupancy(f.smem_bytes, &occ));
+            CUDA_TRY(ops.set_smem(L->fused_smem_max));
+            CUDA_TRY(ops.occupancy(f.smem_bytes, &occ));
+            L->fused_occ_fn = ops.launch;
             L->fused_occ_smem = f.smem_bytes;
             L->fused_occ = occ;
         }
         ok = ok && L->fused_occ >= 1;
         if (ok) {
             CUDA_TRY(mark(0));
-            CUDA_TRY(launch_fused(f, kv->kmap, kv->vmap, L->num_sms, s));
+            CUDA_TRY(ops.launch(f, kv->kmap, kv->vmap, L->num_sms, s));
             CUDA_TRY(mark_end());
             L->launches = 1;
             return GATTN_OK;
@@ -672,7 +674,8 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
         if (L->path == GATTN_PATH_FUSED)
             return fail(GATTN_E_UNSUPPORTED,
                         "this step cannot run as one kernel (needs batch*q_len <= 8, or <= 4 "
-                        "for fp32 x, head_dim 64/128/256, whole heads per 128-row block)");
+                        "for fp32 x, head_dim 64/128/256, whole heads per 128-row block, a "
+                        "16-byte aligned x and a compiled instance for its bit widths)");
     }
 
     // 1. x -> fp16 tensor-core operand + group sums

@@ -255,14 +255,13 @@ struct FusedArgs {
     int nrb, MT, min_units;
     int rb_h0[kMaxRowBlocks], rb_nh[kMaxRowBlocks];
     // library scratch
-    float *part_a, *part_o;          // split-K partials, [slot][8 columns][128 rows]
+    float *part_a;                   // q|k|v split-K partials, [slot][8 columns][128 rows]
+    float *part_o;                   // o_proj partial of every (k unit, row block) item
     __nv_bfloat16 *qn;               // [M][H][d]
     float *gate;                     // [M][H*d]
     float *ws;                       // attention partial slots
-    __half *x16o;                    // o_proj operand, one-column-tile fragment order
-    float *xsumo;                    // its group sums
     unsigned *sync;                  // counters and flags, all zero between steps
-    int s_cnt_a, s_rdy_a, s_seg, s_xo, s_cnt_o, nsync;
+    int s_cnt_a, s_rdy_a, s_seg, s_cnt_o, nsync;
     __nv_bfloat16 *out;              // [M][No]
     float *tap_y, *tap_attn;
     unsigned *status;
@@ -273,11 +272,19 @@ struct FusedArgs {
 // Sizes the shared-memory plan of `a` (ring, x slots, scratch) for the given
 // attention tile rows; false when the step does not fit one CTA per SM.
 bool fused_plan(FusedArgs &a, int num_sms, int max_smem);
-cudaError_t fused_set_smem_limits(int bytes);
-// CTAs of the fused kernel that can be resident at once (cooperative limit)
-cudaError_t fused_occupancy(int smem, int *blocks_per_sm);
-cudaError_t launch_fused(const FusedArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                         int grid, cudaStream_t s);
+
+// The compiled instances of the one-kernel step, by configuration.
+struct FusedKey {
+    int bits_a, group_a, bits_o, group_o, MT, DB;
+};
+struct FusedOps {
+    cudaError_t (*launch)(const FusedArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                          int grid, cudaStream_t s);   // cooperative launch
+    cudaError_t (*set_smem)(int bytes);
+    cudaError_t (*occupancy)(int smem, int *blocks_per_sm);
+};
+// false when no instance was compiled for this configuration
+bool fused_ops(const FusedKey &k, FusedOps *ops);
 
 }  // namespace gattn
 

@@ -202,18 +202,23 @@ def test_stale_nan_cache_slots_do_not_leak():
     assert np.array_equal(a["attn"], b["attn"])
 
 
-def test_verify_step_equals_row_by_row_steps():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_verify_step_equals_row_by_row_steps(path):
+    """Four one-row steps on one layer (each reads the rows the previous ones
+    appended) equal one four-row step; on the one-kernel path this also checks
+    that every step leaves its counters and flags cleared for the next."""
     spec = SMALL["verify_2k_p46"]
     case = make_case(spec)
-    full = gpu_run(case)
+    full = gpu_run(case, path=PATHS[path])
     s1 = spec.with_(q_len=1)
-    dl = DeviceLayer(s1, case.lib_packed, case.qn, case.kn, case.cap, max_q_len=1)
+    dl = DeviceLayer(s1, case.lib_packed, case.qn, case.kn, case.cap, max_q_len=1,
+                     path=PATHS[path])
     dl.load_cache(case.ck, case.cv)
     case1 = make_case(s1, capacity=case.cap)
     rows = []
     for r in range(spec.q_len):
         res = gpu_run(case1, x=np.ascontiguousarray(case.x[:, r:r + 1]), pos=case.pos + r, dl=dl,
-                      q_len=1)
+                      q_len=1, path=PATHS[path])
         rows.append(res)
     dl.close()
     assert np.array_equal(rows[-1]["k"], full["k"]) and np.array_equal(rows[-1]["v"], full["v"])
