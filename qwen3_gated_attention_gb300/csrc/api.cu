@@ -322,10 +322,25 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
                                   smem, 16, &n16) == cudaSuccess && n16 > 0)
                 max_cluster = 16;
             cudaGetLastError();
+            // the largest k split (any count up to the cluster limit) whose
+            // clusters all fit on the GPU at once: one wave (a second, partial
+            // wave of clusters costs more than the split saves)
             int ks = 1;
-            while (ks * 2 * p->rbc <= max_cluster && ks * 2 <= p->nku &&
-                   (long long)nclusters * p->rbc * ks * 2 <= capacity)
-                ks *= 2;
+            for (int cand = std::min(max_cluster / p->rbc, p->nku); cand > 1; --cand) {
+                const int csize = cand * p->rbc;
+                if ((long long)nclusters * csize > capacity)
+                    continue;
+                int nres = 0;
+                if (proj_max_clusters(p->bits, 1 << i, p == &L->pqkv ? kModeQKV : kModeO,
+                                      p->group, smem, csize, &nres) != cudaSuccess) {
+                    cudaGetLastError();
+                    continue;
+                }
+                if (nres >= nclusters) {
+                    ks = cand;
+                    break;
+                }
+            }
             p->ks[i] = ks;
             p->grid[i] = nclusters * p->rbc * ks;
         }

@@ -237,17 +237,20 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
     }
 }
 
-// o_proj epilogue: the cluster's single row block, rows split across its CTAs;
-// thread t takes row rank * rpr + t % rpr and the columns t / rpr + j * (128 / rpr).
+// o_proj epilogue: the cluster's single row block, rows split across its CTAs
+// (ceil(128 / cluster size) per rank); thread t takes row rank * rpr + t % rpr
+// and the columns t / rpr + j * (128 / rpr).
 template <int MP>
 static __device__ void epilogue_o(const ProjArgs &a, const EpiO &e, const EpiSmem &sm, int row0,
                                   int rank, int csize, int tid)
 {
-    const int rpr = kRBR / csize;              // rows per rank
-    const int lanes_m = (kWR * 32) / rpr;      // column lanes per row
+    const int rpr = (kRBR + csize - 1) / csize;   // rows per rank
+    const int lanes_m = (kWR * 32) / rpr;         // column lanes per row
+    if (tid >= lanes_m * rpr)
+        return;
     const int r = rank * rpr + tid % rpr;
     const int n = row0 + r;
-    if (n >= a.N)
+    if (r >= kRBR || n >= a.N)
         return;
     for (int m = tid / rpr; m < a.M; m += lanes_m) {
         const int b = m / e.R;
@@ -264,8 +267,10 @@ __host__ __device__ inline int proj_tail_bytes(int eb_rows)
     return 256 + eb_rows * 4 + 2 * 256 * 4 + 128 * 8 + 32 * 4;
 }
 
+// Two CTAs per SM at least; the four-column-tile instances, whose grids are
+// short of CTAs at two per SM, ask for three.
 template <int BITS, int NT, int MODE, int GROUP>
-__global__ void __launch_bounds__((kWR + 1) * 32, 2)
+__global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
     proj_kernel(const ProjArgs a, const EpiQKV eq, const EpiO eo)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
