@@ -31,14 +31,19 @@ struct AttnSmem {
     static constexpr int kStageBytes = 2 * kTileBytes;        // K + V
     static constexpr int kQBytes = MT * 16 * DB * 64 * 2;
     static constexpr int kPBytes = MT * 16 * 128;             // rows x 64 tokens bf16
-    static constexpr int kStages = kAttnStages * kStageBytes;
+    // as many K/V stages (2 .. kAttnStages) as fit beside the rest in 227 KB
+    static constexpr int kFixed = kQBytes + kPBytes + 2 * kAttnWarps * 64 * 4 + 40 * 8 +
+                                  2 * kAttnStages * 8 + 256 + 1024;
+    static constexpr int kFit = (227 * 1024 - kFixed) / kStageBytes;
+    static constexpr int kNStages = kFit < 2 ? 2 : (kFit > kAttnStages ? kAttnStages : kFit);
+    static constexpr int kStages = kNStages * kStageBytes;
     static constexpr int kQ = kStages;
     static constexpr int kP = kQ + kQBytes;
     static constexpr int kRedMax = kP + kPBytes;              // [8][64] floats
     static constexpr int kRedL = kRedMax + kAttnWarps * 64 * 4;
     static constexpr int kPrefix = kRedL + kAttnWarps * 64 * 4;   // [33] long long
     static constexpr int kBars = kPrefix + 40 * 8;
-    static constexpr int kFlags = kBars + 2 * kAttnStages * 8;
+    static constexpr int kFlags = kBars + 2 * kNStages * 8;
     static constexpr int kTotal = kFlags + 256 + 1024;        // + alignment slack
 };
 
@@ -58,7 +63,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     float *red_l = reinterpret_cast<float *>(smem + L::kRedL);
     long long *prefix = reinterpret_cast<long long *>(smem + L::kPrefix);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBars);
-    uint64_t *empty = full + kAttnStages;
+    uint64_t *empty = full + L::kNStages;
     int *flags = reinterpret_cast<int *>(smem + L::kFlags);   // [0] abort [1] last [2..] ub
     int *ub = flags + 4;                                        // units per segment of b [32]
 
@@ -72,7 +77,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     pdl_launch_dependents();
 
     if (tid == 0) {
-        for (int i = 0; i < kAttnStages; ++i) {
+        for (int i = 0; i < L::kNStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kAttnWarps);
         }
@@ -118,12 +123,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int u = p.u0; u < p.u1; u += kAttnTile / kAttnUnit, ++it) {
                     const int nun = min(kAttnTile / kAttnUnit, p.u1 - u);
                     // tiles that hold this step's new rows load after the projection
-                    if (!waited && (it >= kAttnStages || (u + nun) * kAttnUnit > p0)) {
+                    if (!waited && (it >= L::kNStages || (u + nun) * kAttnUnit > p0)) {
                         pdl_wait();
                         waited = true;
                     }
-                    const int slot = (int)(it % kAttnStages);
-                    const uint32_t ph = (uint32_t)((it / kAttnStages) & 1);
+                    const int slot = (int)(it % L::kNStages);
+                    const uint32_t ph = (uint32_t)((it / L::kNStages) & 1);
                     if (!mbar_wait(&empty[slot], ph ^ 1u, abort, a.status)) {
                         stop = true;
                         break;
@@ -146,10 +151,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             if (!waited)
                 pdl_wait();
-            const long long first = it > kAttnStages ? it - kAttnStages : 0;
+            const long long first = it > L::kNStages ? it - L::kNStages : 0;
             for (long long i = first; i < it; ++i) {
                 unsigned long long t0 = global_ns();
-                while (!mbar_try(&full[i % kAttnStages], (uint32_t)((i / kAttnStages) & 1)) &&
+                while (!mbar_try(&full[i % L::kNStages], (uint32_t)((i / L::kNStages) & 1)) &&
                        global_ns() - t0 < kWaitLimitNs) {
                 }
             }
@@ -202,8 +207,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int nun = min(kAttnTile / kAttnUnit, p.u1 - u);
             const int ntok = nun * kAttnUnit;
             const int t0 = u * kAttnUnit;
-            const int slot = (int)(it % kAttnStages);
-            const uint32_t ph = (uint32_t)((it / kAttnStages) & 1);
+            const int slot = (int)(it % L::kNStages);
+            const uint32_t ph = (uint32_t)((it / L::kNStages) & 1);
             const bool ok = mbar_wait(&full[slot], ph, abort, a.status);
             uint8_t *kst = smem + slot * L::kStageBytes;
             uint8_t *vst = kst + L::kTileBytes;

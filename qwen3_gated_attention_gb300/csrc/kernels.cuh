@@ -143,7 +143,7 @@ constexpr int kAttnWarps = 8;          // consumer warps
 constexpr int kAttnThreads = (kAttnWarps + 1) * 32;
 constexpr int kAttnUnit = 16;          // tokens per stream-K unit
 constexpr int kAttnTile = 48;          // tokens per pipeline stage (<= 64: the P tile width)
-constexpr int kAttnStages = 2;
+constexpr int kAttnStages = 4;        // pipeline stages, at most (fewer when shared memory is short)
 constexpr int kMaxRowBlocks = 64;
 constexpr int kAttnMaxRows = 64;       // query rows per segment
 
