@@ -142,7 +142,7 @@ bool layer_proj_tiles(const ::gattn_layer *layer, int proj, ProjTiles *out);
 constexpr int kAttnWarps = 8;          // consumer warps
 constexpr int kAttnThreads = (kAttnWarps + 1) * 32;
 constexpr int kAttnUnit = 16;          // tokens per stream-K unit
-constexpr int kAttnTile = 48;          // tokens per pipeline stage (<= 64: the P tile width)
+constexpr int kAttnTile = 64;         // tokens per pipeline stage (<= 64: the P tile width)
 constexpr int kAttnStages = 4;        // pipeline stages, at most (fewer when shared memory is short)
 constexpr int kMaxRowBlocks = 64;
 constexpr int kAttnMaxRows = 64;       // query rows per segment
