@@ -317,9 +317,13 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
             const long long capacity = (long long)L->num_sms * occ;
             const int nclusters = p->nrb / p->rbc;
             // 16-CTA clusters (non-portable) when this kernel can run them
+            // (the q|k|v projection, which attention waits on, keeps the portable
+            // size: a cluster larger than 8 can wait several microseconds for a GPC
+            // with room for all of its CTAs)
             int max_cluster = kMaxCluster, n16 = 0;
-            if (proj_max_clusters(p->bits, 1 << i, p == &L->pqkv ? kModeQKV : kModeO, p->group,
-                                  smem, 16, &n16) == cudaSuccess && n16 > 0)
+            if (p == &L->po &&
+                proj_max_clusters(p->bits, 1 << i, kModeO, p->group, smem, 16, &n16) == cudaSuccess &&
+                n16 > 0)
                 max_cluster = 16;
             cudaGetLastError();
             // the largest k split (any count up to the cluster limit) whose
