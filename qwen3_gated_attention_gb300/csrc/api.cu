@@ -349,7 +349,9 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
             p->grid[i] = nclusters * p->rbc * ks;
         }
     }
-    L->attn_grid = L->num_sms;
+    // one attention CTA per SM; a segment's contributors (at most the grid)
+    // fit the merge's factor table of 160
+    L->attn_grid = std::min(L->num_sms, 159);
 
     const int MP = 32;  // columns of the widest (NT = 4) operand layout
     const size_t nku_a = c.hidden / kKU, nku_o = L->Ko / kKU;

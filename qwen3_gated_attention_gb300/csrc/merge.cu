@@ -1,11 +1,15 @@
 // merge.cu -- combine the attention partials of every segment, apply the
 // output gate, and write the o_proj operand.
 //
-// One CTA per (segment, query row), one thread per head_dim column.  Every
-// contributor (the CTAs whose unit ranges touched the segment) left m_j (the
-// log2-domain row maximum), l_j and O_j; with M = max m_j,
+// One CTA per (segment, query row).  Every contributor (the CTAs whose unit
+// ranges touched the segment) left m_j (the log2-domain row maximum), l_j and
+// O_j; with M = max m_j,
 //   attn = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
-// Threads own columns so each partial row is read as coalesced lines.
+// Two dependent rounds of loads: one warp loads every (m_j, l_j) at once and
+// leaves the factors 2^(m_j - M) / L in shared memory; then two threads per
+// head_dim column each load half of the contributors' O_j values (all in
+// flight together; a warp's loads are one coalesced line per contributor) and
+// their sums are added.
 //
 //   attn = O / l,   a = attn * sigmoid(gate)   (the layer's output gate)
 //
@@ -16,11 +20,15 @@
 
 namespace gattn {
 
-__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a)
+constexpr int kMergeMaxContrib = 160;       // contributors per segment (>= attention grid)
+
+__global__ void __launch_bounds__(512) attn_merge_kernel(const AttnArgs a)
 {
     __shared__ long long prefix[33];
     __shared__ int ub[32];
     __shared__ float gsum_sm[8];
+    __shared__ float fct[kMergeMaxContrib];
+    __shared__ float comb[512];
     // the o_proj launches at once to stream its weights; this kernel's own
     // pre-wait work reads only cache_pos (a step input)
     pdl_launch_dependents();
@@ -61,63 +69,67 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a)
     const int hl = i / a.R, r = i % a.R;
     const int h = kh * (a.H / a.Hk) + a.rb_h0[rb] + hl;
     const int m = b * a.R + r;
-    const int c0 = warp * 32;
+    const int half = tid / D, jd = tid - half * D;    // column and contributor half
     const long long Ktot = (long long)a.H * D;
 
     pdl_wait();                 // partials (attention) and the gate (q|k|v projection)
-    const int jd = c0 + lane;   // this thread's head_dim column
     const float gt = a.gate[(long long)m * Ktot + (long long)h * D + jd];
-    // lanes own columns, so every partial load is one coalesced 128-byte line
-    // per warp (m_j and l_j are warp-uniform broadcast loads).  Contributors are
-    // loaded 16 at a time into registers (independent loads in flight
-    // together), then folded with a running log2-domain maximum.
-    constexpr int kBatch = 16;
-    float M = -INFINITY, L = 0.f, acc = 0.f;
-    const float *pm = base + i;                                   // m_j of row i
-    const int off_l = kAttnMaxRows, off_o = 2 * kAttnMaxRows + i * D + jd - i;
-    auto fold = [&](const float (&mv)[kBatch], const float (&lv)[kBatch],
-                    const float (&ov)[kBatch]) {
-        float mb = M;
+
+    // ---- factors 2^(m_j - M) / L (one warp, every contributor's loads at once)
+    if (warp == 0) {
+        constexpr int kPer = kMergeMaxContrib / 32;
+        float mv[kPer], lv[kPer];
+        float mx = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-            mb = fmaxf(mb, mv[u]);
-        const float sc = (M == -INFINITY) ? 0.f : exp2f(M - mb);
-        L *= sc;
-        acc *= sc;
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const float w = (mv[u] == -INFINITY) ? 0.f : exp2f(mv[u] - mb);
-            L = fmaf(w, lv[u], L);
-            acc = fmaf(w, ov[u], acc);
+        for (int u = 0; u < kPer; ++u) {
+            const int j = lane + 32 * u;
+            mv[u] = j < n ? base[(long long)j * slot_floats + i] : -INFINITY;
+            lv[u] = j < n ? base[(long long)j * slot_floats + kAttnMaxRows + i] : 0.f;
+            mx = fmaxf(mx, mv[u]);
         }
-        M = mb;
-    };
-    int j0 = 0;
-    for (; j0 + kBatch <= n; j0 += kBatch) {
-        float mv[kBatch], lv[kBatch], ov[kBatch];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const float *pj = pm + u * slot_floats;
-            mv[u] = pj[0];
-            lv[u] = pj[off_l];
-            ov[u] = __ldcg(pj + off_o);
+        for (int o = 16; o; o >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float L = 0.f;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            mv[u] = mv[u] == -INFINITY ? 0.f : exp2f(mv[u] - mx);
+            L = fmaf(mv[u], lv[u], L);
         }
-        fold(mv, lv, ov);
-        pm += kBatch * slot_floats;
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            L += __shfl_xor_sync(0xffffffffu, L, o);
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int j = lane + 32 * u;
+            if (j < n)
+                fct[j] = mv[u] * inv;
+        }
     }
-    if (j0 < n) {
-        float mv[kBatch], lv[kBatch], ov[kBatch];
+    __syncthreads();
+
+    // ---- weighted sum of the O_j of column jd over this thread's contributors
+    //      (j = half, half + 2, ...), sixteen loads in flight at a time
+    const float *po = base + 2 * kAttnMaxRows + (long long)i * D + jd;
+    float acc = 0.f;
+    int j = half;
+    for (; j + 30 < n; j += 32) {
+        float v[16];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const bool live = j0 + u < n;
-            const float *pj = pm + (live ? u : 0) * slot_floats;
-            mv[u] = live ? pj[0] : -INFINITY;
-            lv[u] = pj[off_l];
-            ov[u] = __ldcg(pj + off_o);
-        }
-        fold(mv, lv, ov);
+        for (int u = 0; u < 16; ++u)
+            v[u] = __ldcg(po + (long long)(j + 2 * u) * slot_floats);
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            acc = fmaf(fct[j + 2 * u], v[u], acc);
     }
-    const float o = L > 0.f ? acc / L : 0.f;
+    for (; j < n; j += 2)
+        acc = fmaf(fct[j], __ldcg(po + (long long)j * slot_floats), acc);
+    comb[tid] = acc;
+    __syncthreads();
+    if (half != 0)
+        return;
+    const float o = comb[jd] + comb[jd + D];
     const float gated = o * (1.f / (1.f + __expf(-gt)));
     const __half hv = __float2half_rn(gated);
     const int k = h * D + jd;
@@ -125,8 +137,9 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a)
     if (a.tap_attn)
         a.tap_attn[(long long)m * Ktot + k] = o;
 
-    // group sums of the fp16 operand values (groups of gs columns within the head)
-    const int gs = a.group_o, MP = 8 * a.NT;
+    // group sums of the fp16 operand values (groups of gs columns within the
+    // head); only the first D threads (warps 0 .. D/32 - 1) remain
+    const int gs = a.group_o, MP = 8 * a.NT, c0 = warp * 32;
     float gsum = __half2float(hv);
 #pragma unroll
     for (int o2 = 1; o2 < 32; o2 <<= 1)
@@ -140,7 +153,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a)
     } else {
         if (lane == 0)
             gsum_sm[warp] = gsum;
-        __syncthreads();
+        named_bar_sync(1, D);
         const int wpg = gs / 32;                 // warps per group
         if (lane == 0 && (warp % wpg) == 0) {
             float t = 0.f;
@@ -156,7 +169,7 @@ cudaError_t launch_attn_merge(const AttnArgs &a, int max_rows, bool pdl, cudaStr
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.B * a.Hk * a.nrb, max_rows);
-    cfg.blockDim = dim3(a.d);
+    cfg.blockDim = dim3(2 * a.d);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
