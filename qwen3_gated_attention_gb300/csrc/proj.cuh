@@ -112,18 +112,31 @@ struct EpiSmem {
 };
 
 // Final value of row `row` (0 .. eb_rows-1 of the cluster), column m: the sum of
-// the ks partials of the row's block, read from the cluster's shared memory.
-template <int MP>
+// the ks partials of the row's block, read from the cluster's shared memory, in
+// rank order.  With BATCH > 1 the remote loads are issued BATCH at a time
+// before their adds (the loads are ordered asm statements: interleaving them
+// with the adds serializes their latencies) -- worth its registers for the
+// o_proj's wide splits, not for the q|k|v epilogue.
+template <int MP, int BATCH>
 __device__ __forceinline__ float cluster_row_sum(const ProjArgs &a, const EpiSmem &sm, int row, int m)
 {
     const int q = row / kRBR, rr = row % kRBR;
     const float *local = sm.red + (long long)m * kRBR + rr;
+    const float *lo = local + (long long)a.xsplit * kRBR;
     float v = 0.f;
-    for (int k = 0; k < a.ks; ++k) {
-        const uint32_t rank = (uint32_t)(q * a.ks + k);
-        v += ld_dsmem(dsmem_addr(local, rank));
-        if (a.xsplit)
-            v += ld_dsmem(dsmem_addr(local + (long long)a.xsplit * kRBR, rank));
+    for (int k0 = 0; k0 < a.ks; k0 += BATCH) {
+        float t[BATCH], u[BATCH];
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+            const uint32_t rank = (uint32_t)(q * a.ks + k0 + k);
+            t[k] = k0 + k < a.ks ? ld_dsmem(dsmem_addr(local, rank)) : 0.f;
+            u[k] = (a.xsplit && k0 + k < a.ks) ? ld_dsmem(dsmem_addr(lo, rank)) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+            v += t[k];
+            v += u[k];
+        }
     }
     return v;
 }
@@ -141,7 +154,7 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
     const int Ny = e.Nq + 2 * e.Nkv;
     for (int m = rank; m < a.M; m += csize) {
         for (int r = tid; r < a.eb_rows; r += kWR * 32)
-            sm.vals[r] = cluster_row_sum<MP>(a, sm, r, m);
+            sm.vals[r] = cluster_row_sum<MP, 1>(a, sm, r, m);
         named_bar_sync(1, kWR * 32);
         for (int hb = warp; hb < heads; hb += kWR) {
             const int n0 = row0 + hb * d;
@@ -256,7 +269,7 @@ static __device__ void epilogue_o(const ProjArgs &a, const EpiO &e, const EpiSme
         const int b = m / e.R;
         const int pb = sm.cpos[b];
         const bool valid = pb >= 0 && pb + e.R <= e.cap;
-        const float v = valid ? cluster_row_sum<MP>(a, sm, r, m) : 0.f;
+        const float v = valid ? cluster_row_sum<MP, 8>(a, sm, r, m) : 0.f;
         e.out[(long long)m * a.N + n] = __float2bfloat16_rn(v);
     }
 }
