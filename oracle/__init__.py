@@ -94,6 +94,8 @@ def _declare(L):
     L.orc_sdpa.argtypes = [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p]
     L.orc_layer_step.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _p, _p, _i,
                                  _p, _i, _i, _p, _p, _p]
+    L.orc_block_step.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _p, _p, _p,
+                                 _p, _i, _p, _i, _i, _p, _p]
 
 
 def _ptr(a: np.ndarray | None):
@@ -214,16 +216,8 @@ class OracleWeights:
     group: list = field(default_factory=list)
 
 
-def layer_step(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.ndarray,
-               cache_v: np.ndarray, cache_pos: np.ndarray, head_chunk: bool = True,
-               mutate: str = "none", taps: bool = False):
-    """One gated full-attention layer step ([mlxd#99] Summary: doubled q_proj ->
-    split query/gate -> o_proj(attn * sigmoid(gate)); [atlas-mod] KV append at
-    cache_pos, attention over cache_pos + 1 per row).
-
-    x: [B][R][hidden] float64 values; cache_k/v: [B][Hk][cap][d] bf16 bits,
-    updated in place.  Returns out [B][R][hidden] (and the taps when asked)."""
-    B, R, Hd = x.shape
+def _layer_structs(spec, weights: OracleWeights, head_chunk: bool, mutate: str):
+    """The C structs of a layer; `keep` holds the arrays they point into."""
     L = _OrcLayer()
     L.hidden, L.num_heads, L.num_kv_heads, L.head_dim = (spec.hidden, spec.num_heads,
                                                          spec.num_kv_heads, spec.head_dim)
@@ -245,7 +239,22 @@ def layer_step(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.ndarray,
             slot[i] = _ptr(a)
     qn = np.ascontiguousarray(weights.q_norm, np.uint16)
     kn = np.ascontiguousarray(weights.k_norm, np.uint16)
+    keep += [qn, kn]
     Wt.q_norm, Wt.k_norm = _ptr(qn), _ptr(kn)
+    return L, Wt, keep
+
+
+def layer_step(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.ndarray,
+               cache_v: np.ndarray, cache_pos: np.ndarray, head_chunk: bool = True,
+               mutate: str = "none", taps: bool = False):
+    """One gated full-attention layer step ([mlxd#99] Summary: doubled q_proj ->
+    split query/gate -> o_proj(attn * sigmoid(gate)); [atlas-mod] KV append at
+    cache_pos, attention over cache_pos + 1 per row).
+
+    x: [B][R][hidden] float64 values; cache_k/v: [B][Hk][cap][d] bf16 bits,
+    updated in place.  Returns out [B][R][hidden] (and the taps when asked)."""
+    B, R, Hd = x.shape
+    L, Wt, keep = _layer_structs(spec, weights, head_chunk, mutate)
     x = np.ascontiguousarray(x, np.float64)
     assert cache_k.flags["C_CONTIGUOUS"] and cache_v.flags["C_CONTIGUOUS"]
     cap = cache_k.shape[2]
@@ -260,3 +269,26 @@ def layer_step(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.ndarray,
     if taps:
         return out, ty, ta
     return out
+
+
+def block_step(spec, weights: OracleWeights, x: np.ndarray, input_ln: np.ndarray,
+               post_ln, cache_k: np.ndarray, cache_v: np.ndarray, cache_pos: np.ndarray,
+               head_chunk: bool = True):
+    """The decoder block around the layer ([atlas-mod] forward_full_attention:
+    input RMSNorm -> layer -> residual add -> post-attention RMSNorm): returns
+    out = x + layer(RMSNorm(x) * input_ln) and, when post_ln is given,
+    RMSNorm(bf16(out)) * post_ln (else None).  input_ln / post_ln: bf16 bits
+    [hidden]; caches as in layer_step (updated in place)."""
+    B, R, Hd = x.shape
+    L, Wt, keep = _layer_structs(spec, weights, head_chunk, "none")
+    x = np.ascontiguousarray(x, np.float64)
+    iw = np.ascontiguousarray(input_ln, np.uint16)
+    pw = None if post_ln is None else np.ascontiguousarray(post_ln, np.uint16)
+    assert cache_k.flags["C_CONTIGUOUS"] and cache_v.flags["C_CONTIGUOUS"]
+    cp = np.ascontiguousarray(cache_pos, np.int32)
+    out = np.zeros((B, R, Hd), np.float64)
+    on = np.zeros((B, R, Hd), np.float64) if pw is not None else None
+    rc = lib().orc_block_step(C.byref(L), C.byref(Wt), _ptr(x), _ptr(iw), _ptr(pw), _ptr(cache_k),
+                              _ptr(cache_v), cache_k.shape[2], _ptr(cp), B, R, _ptr(out), _ptr(on))
+    _check(rc, "block_step")
+    return out, on

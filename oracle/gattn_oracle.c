@@ -555,3 +555,53 @@ done:
     free(scores); free(knew); free(vnew); free(cf); free(cl);
     return rc;
 }
+
+/* ------------------------------------------------------ decoder block */
+
+/* The steps on either side of the layer in a decoder block ([atlas-mod]
+ * forward_full_attention: norm -> projections -> attention -> residual +
+ * post-norm -> MLP): per row of x [B][R][hidden],
+ *   h          = RMSNorm(x) * input_ln
+ *   out        = x + layer(h)                       (the residual stream)
+ *   out_normed = RMSNorm(bf16(out)) * post_ln       (the MLP's input)
+ * The residual stream is stored as bf16, and the post-norm reads the stored
+ * row.  input_ln / post_ln are bf16 [hidden]; post_ln and out_normed may be
+ * NULL.  Cache behaviour is that of orc_layer_step. */
+int orc_block_step(const orc_layer *L, const orc_weights *W, const double *x,
+                   const uint16_t *input_ln, const uint16_t *post_ln,
+                   uint16_t *cache_k, uint16_t *cache_v, int capacity,
+                   const int32_t *cache_pos, int B, int R, double *out, double *out_normed)
+{
+    const int Hd = L->hidden;
+    const int64_t M = (int64_t)B * R;
+    double *w = malloc((size_t)Hd * sizeof(double));
+    double *h = malloc((size_t)(M * Hd) * sizeof(double));
+    double *y = malloc((size_t)(M * Hd) * sizeof(double));
+    double *rb = malloc((size_t)Hd * sizeof(double));
+    int rc = ORC_OK;
+    if (!w || !h || !y || !rb) {
+        rc = ORC_E_ARG;
+        goto done;
+    }
+    for (int i = 0; i < Hd; ++i)
+        w[i] = orc_bf16_to_double(input_ln[i]);
+    for (int64_t m = 0; m < M; ++m)
+        orc_rms_norm(x + m * Hd, Hd, w, L->rms_eps, h + m * Hd);
+    rc = orc_layer_step(L, W, h, cache_k, cache_v, capacity, cache_pos, B, R, y, NULL, NULL);
+    if (rc != ORC_OK)
+        goto done;
+    for (int64_t j = 0; j < M * Hd; ++j)
+        out[j] = x[j] + y[j];
+    if (post_ln && out_normed) {
+        for (int i = 0; i < Hd; ++i)
+            w[i] = orc_bf16_to_double(post_ln[i]);
+        for (int64_t m = 0; m < M; ++m) {
+            for (int i = 0; i < Hd; ++i)
+                rb[i] = orc_bf16_to_double(orc_bf16_from_double(out[m * Hd + i]));
+            orc_rms_norm(rb, Hd, w, L->rms_eps, out_normed + m * Hd);
+        }
+    }
+done:
+    free(w); free(h); free(y); free(rb);
+    return rc;
+}

@@ -25,7 +25,7 @@ from dataclasses import dataclass, replace
 import numpy as np
 
 # substream ids
-_X, _WQ, _WK, _WV, _WO, _QN, _KN, _CK, _CV, _LEN = range(1, 11)
+_X, _WQ, _WK, _WV, _WO, _QN, _KN, _CK, _CV, _LEN, _IN_LN, _POST_LN = range(1, 13)
 
 
 @dataclass(frozen=True)
@@ -145,6 +145,14 @@ def norm_weights_bf16(spec: LayerSpec):
     qn = f32_to_bf16_bits((1.0 + 0.1 * _normal(spec.seed, _QN, n=spec.head_dim)).astype(np.float32))
     kn = f32_to_bf16_bits((1.0 + 0.1 * _normal(spec.seed, _KN, n=spec.head_dim)).astype(np.float32))
     return qn, kn
+
+
+def block_norm_weights_bf16(spec: LayerSpec):
+    """input_ln and post_ln of the decoder block around the layer, bf16 bits
+    [hidden], 1 + 0.1 N(0, 1) like the QK norms (no values are given)."""
+    il = f32_to_bf16_bits((1.0 + 0.1 * _normal(spec.seed, _IN_LN, n=spec.hidden)).astype(np.float32))
+    pl = f32_to_bf16_bits((1.0 + 0.1 * _normal(spec.seed, _POST_LN, n=spec.hidden)).astype(np.float32))
+    return il, pl
 
 
 def layer_input(spec: LayerSpec, step: int = 0):

@@ -166,6 +166,28 @@ def test_one_kernel_and_five_kernel_paths_agree(name):
     assert ok, rep
 
 
+# Wider verify / short prefill rows: q_len 8, 16 and 32 on the verify layer
+# (gqa 12), where the head-chunk plan cuts each KV group into 4, 2 and 1 head(s)
+# per chunk; a 32-row step spans several 64-row attention row blocks unchunked.
+WIDE = {
+    "verify_r8": synth.WORKLOADS["verify_2k_p46"].with_(name="verify_r8", q_len=8, cache_pos=(300,)),
+    "verify_r16_b2": synth.WORKLOADS["verify_2k_p46"].with_(
+        name="verify_r16_b2", q_len=16, batch=2, cache_pos=None, length_range=(40, 700)),
+    "verify_r32": synth.WORKLOADS["verify_2k_p46"].with_(name="verify_r32", q_len=32,
+                                                        cache_pos=(1000,)),
+}
+
+
+@pytest.mark.parametrize("name", list(WIDE))
+def test_wide_verify_rows(name):
+    case = make_case(WIDE[name])
+    ref = oracle_run(case)
+    for chunk in (True, False):
+        got = gpu_run(case, head_chunk=chunk)
+        rep = check_parity(case, got, ref, what=f"{name} chunk={chunk}")
+        print(name, chunk, rep)
+
+
 @pytest.mark.parametrize("name", ["verify_2k_p46", "verify_2k_p2048", "d128_b5_b2"])
 def test_head_chunk_route_agrees_with_unchunked(name):
     case = make_case(SMALL[name])

@@ -414,3 +414,59 @@ def test_capacity_overflow_is_rejected_without_writes():
     with pytest.raises(ValueError):
         orc.layer_step(spec, W, x, ck2, cv2, bad)
     assert np.array_equal(ck2, ck) and np.array_equal(cv2, cv)
+
+
+# ------------------------------------------------ decoder block (norm + residual)
+
+def _block(spec, x, scale=1.0, input_ln=None, post_ln=None, with_post=True):
+    from tests.cases import make_case
+    case = make_case(spec)
+    il, pl = synth.block_norm_weights_bf16(spec)
+    il = il if input_ln is None else input_ln
+    pl = pl if post_ln is None else post_ln
+    k2, v2 = case.ck.copy(), case.cv.copy()
+    out, on = orc.block_step(spec, case.orc_weights, x * scale, il, pl if with_post else None,
+                             k2, v2, case.pos)
+    return case, out, on, k2, v2
+
+
+def test_block_layer_part_is_invariant_to_the_input_scale():
+    """h = RMSNorm(x) * input_ln does not depend on the scale of x (up to eps),
+    so out - x does not either; a block that skipped the input norm would
+    scale its layer part by c (the q/k norms undo it, v and o_proj do not)."""
+    spec = synth.WORKLOADS["tiny"]
+    x = synth.x_values(spec, synth.layer_input(spec))
+    _, o1, _, k1, v1 = _block(spec, x, 1.0)
+    _, o4, _, k4, v4 = _block(spec, x, 4.0)
+    ok, rep = refs.close(o4 - 4.0 * x, o1 - x, abs_tol=1e-5, rel_tol=1e-5, l2_tol=1e-5)
+    assert ok, rep
+    bad = np.abs((o4 - 4.0 * x) - 4.0 * (o1 - x)).max()
+    assert bad > 1e-3      # the check above has power: scaled layer parts differ
+
+
+def test_block_reduces_to_the_layer_on_unit_rms_rows():
+    """input_ln = 1 and rows of unit RMS: h = x up to eps, so out - x is the layer."""
+    spec = synth.WORKLOADS["batched_mixed_small"] if "batched_mixed_small" in synth.WORKLOADS else \
+        synth.WORKLOADS["tiny"].with_(batch=3, q_len=2, cache_pos=None, length_range=(20, 300))
+    x = synth.x_values(spec, synth.layer_input(spec))
+    x = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True))
+    ones = np.full(spec.hidden, 0x3F80, np.uint16)
+    case, out, _, k2, v2 = _block(spec, x, input_ln=ones)
+    k3, v3 = case.ck.copy(), case.cv.copy()
+    ref = orc.layer_step(spec, case.orc_weights, x, k3, v3, case.pos)
+    ok, rep = refs.close(out - x, ref, abs_tol=1e-6, rel_tol=1e-5, l2_tol=1e-5)
+    assert ok, rep
+
+
+def test_block_post_norm_rows_have_unit_rms():
+    """post_ln = 1: every row of RMSNorm(bf16(out)) has RMS 1 (up to eps)."""
+    spec = synth.WORKLOADS["tiny"]
+    x = synth.x_values(spec, synth.layer_input(spec))
+    ones = np.full(spec.hidden, 0x3F80, np.uint16)
+    _, out, on, _, _ = _block(spec, x, post_ln=ones)
+    rms = np.sqrt(np.mean(on * on, axis=-1))
+    assert np.allclose(rms, 1.0, atol=1e-5)
+    # it normalizes the stored bf16 row, not the exact sum
+    rb = np.vectorize(lambda v: orc.bf16_to_double(orc.bf16_from_double(v)))(out)
+    exp = rb / np.sqrt(np.mean(rb * rb, axis=-1, keepdims=True) + spec.rms_eps)
+    assert np.allclose(on, exp, rtol=0, atol=1e-12)
