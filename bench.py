@@ -39,10 +39,12 @@ METRIC = "gated-attn layer steps/s & tokens/s; achieved HBM GB/s vs GB300 peak"
 UNIT = "layer-steps/s"
 
 
-def algorithmic_bytes(spec):
+def algorithmic_bytes(spec, block=False):
     """Per-step and per-kernel algorithmic bytes (packed weights + bf16
     scales/biases, KV read over every attended position, KV rows written, x,
-    out and the small intermediates each kernel must move)."""
+    out and the small intermediates each kernel must move).  block: the
+    decoder-block step, which adds the two norm weight vectors and the
+    post-norm output to the step (x is still read once)."""
     H, Hk, d, Hd, B, R = (spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.hidden,
                           spec.batch, spec.q_len)
     M = B * R
@@ -71,6 +73,12 @@ def algorithmic_bytes(spec):
         "proj_o": wo + o16 + outb,
     }
     step = wq + wk + wv + wo + kv_read + kv_write + xb + outb
+    if block:
+        lnb = Hd * 2
+        per_kernel["xprep"] += lnb
+        per_kernel["proj_o"] += xb                   # the residual rows
+        per_kernel["postnorm"] = outb + lnb + outb
+        step += 2 * lnb + outb
     return step, per_kernel
 
 
@@ -161,9 +169,9 @@ class ClockSampler:
 
 # ----------------------------------------------------------- cpu baseline
 
-def oracle_sample(spec, budget_s=15.0, max_steps=64):
+def oracle_sample(spec, budget_s=15.0, max_steps=64, block=False):
     """Time the oracle as it stands on a bounded sample of the workload: whole
-    layer steps of the same shapes, one core."""
+    layer (or decoder-block) steps of the same shapes, one core."""
     import oracle as orc
     wf = synth.weights_f32(spec)
     op = [orc.quantize_affine(w.astype(np.float64), spec.bits[i], spec.group[i])
@@ -175,12 +183,16 @@ def oracle_sample(spec, budget_s=15.0, max_steps=64):
     ck, cv = synth.cache(spec, cap)
     x = synth.x_values(spec, synth.layer_input(spec))
     pos = spec.positions()
+    il, pl = synth.block_norm_weights_bf16(spec)
     steps = 0
     t0 = time.perf_counter()
     while steps < max_steps:
         k2, v2 = ck.copy(), cv.copy()
         ts = time.perf_counter()
-        orc.layer_step(spec, W, x, k2, v2, pos)
+        if block:
+            orc.block_step(spec, W, x, il, pl, k2, v2, pos)
+        else:
+            orc.layer_step(spec, W, x, k2, v2, pos)
         steps += 1
         if time.perf_counter() - t0 + (time.perf_counter() - ts) > budget_s:
             break
@@ -194,17 +206,22 @@ def reference_arm(args, spec):
         return
     K, W = args.steps, max(args.warmup, 0)
     budget = min(120.0, max(10.0, 2.0 * (K + W)))
-    rate, n, el = oracle_sample(spec, budget_s=budget, max_steps=max(1, K + W))
+    rate, n, el = oracle_sample(spec, budget_s=budget, max_steps=max(1, K + W), block=args.block)
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT,
         "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": 1000.0 / rate,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_dict(spec, args),
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{n} whole layer steps of {spec.name} in {el:.1f} s"},
+                         "sample": f"{n} whole {unit_name(args)} steps of {spec.name} in "
+                                   f"{el:.1f} s"},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def unit_name(args):
+    return "decoder-block" if args.block else "layer"
 
 
 def config_dict(spec, args, extra=None):
@@ -213,7 +230,9 @@ def config_dict(spec, args, extra=None):
          "rotary_dim": int(spec.head_dim * spec.partial_rotary_factor),
          "bits": list(spec.bits), "group": list(spec.group), "batch": spec.batch,
          "q_len": spec.q_len, "cache_len": int(spec.positions().max()) + spec.q_len,
-         "head_chunk": not args.no_head_chunk, "parallelism": f"replicas x{args.gpus}"}
+         "head_chunk": not args.no_head_chunk, "parallelism": f"replicas x{args.gpus}",
+         "step": "decoder block (input RMSNorm, layer, residual, post-norm)" if args.block
+         else "attention layer"}
     if extra:
         d.update(extra)
     return d
@@ -255,9 +274,9 @@ def our_arm(args, spec):
     # CPU baseline first (rank 0, N = 1): the oracle as it stands, before any GPU work
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, n, el = oracle_sample(spec, budget_s=args.cpu_budget)
+        rate, n, el = oracle_sample(spec, budget_s=args.cpu_budget, block=args.block)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} whole layer steps of {spec.name} ({el:.1f} s, one core)"}
+               "sample": f"{n} whole {unit_name(args)} steps of {spec.name} ({el:.1f} s, one core)"}
 
     if rank == 0:
         libbuild.build()
@@ -269,7 +288,7 @@ def our_arm(args, spec):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
 
-    step_bytes, kernel_bytes = algorithmic_bytes(spec)
+    step_bytes, kernel_bytes = algorithmic_bytes(spec, args.block)
     inst_bytes = step_bytes
     n_inst = max(2, math.ceil(4 * l2 / inst_bytes))
     if args.instances:
@@ -297,13 +316,22 @@ def our_arm(args, spec):
     pd = torch.from_numpy(pos).to(dev)
     outs = [torch.empty((spec.batch, spec.q_len, spec.hidden), dtype=torch.bfloat16, device=dev)
             for _ in range(n_inst)]
+    il, pl = synth.block_norm_weights_bf16(spec)
+    ild = torch.from_numpy(il.view(np.int16)).to(dev)
+    pld = torch.from_numpy(pl.view(np.int16)).to(dev)
+    normed = torch.empty_like(outs[0])
+
+    def step_call(dl, xp, pp, op):
+        if args.block:
+            gattn.layer_step_block(dl.h, xp, dl.kv, pp, spec.batch, spec.q_len, ild.data_ptr(),
+                                   pld.data_ptr(), op, normed.data_ptr(), sh)
+        else:
+            gattn.layer_step(dl.h, xp, dl.kv, pp, spec.batch, spec.q_len, op, sh)
     stream = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
 
     def enqueue(i):
-        dl = layers[i % n_inst]
-        gattn.layer_step(dl.h, xd.data_ptr(), dl.kv, pd.data_ptr(), spec.batch, spec.q_len,
-                         outs[i % n_inst].data_ptr(), sh)
+        step_call(layers[i % n_inst], xd.data_ptr(), pd.data_ptr(), outs[i % n_inst].data_ptr())
 
     # eager warm-up (also checks status), then graphs
     with torch.cuda.stream(stream):
@@ -369,7 +397,10 @@ def our_arm(args, spec):
         names = ["layer_step"]
         kernel_bytes = {"layer_step": step_bytes}
     else:
-        names = ["xprep", "proj_qkv", "attn", "merge", "proj_o"]
+        names = ["xprep", "proj_qkv", "attn", "merge", "proj_o"] + (["postnorm"] if launches == 6
+                                                                      else [])
+        if launches == 5 and "postnorm" in kernel_bytes:     # post-norm inside the o_proj
+            kernel_bytes["proj_o"] += kernel_bytes.pop("postnorm")
     nper = min(K, max(n_inst, 4 * n_inst))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(nper)]
     per_kernel_ms = {n: [] for n in names}
@@ -418,9 +449,8 @@ def our_arm(args, spec):
             xdev.view(torch.int16 if spec.x_dtype != "f32" else torch.float32).copy_(
                 xh, non_blocking=True)
             pdev.copy_(ph, non_blocking=True)
-            gattn.layer_step(dl.h, xdev.data_ptr(), dl.kv, pdev.data_ptr(), spec.batch, spec.q_len,
-                             outs[i % n_inst].data_ptr(), sh)
-            oh.copy_(outs[i % n_inst], non_blocking=True)
+            step_call(dl, xdev.data_ptr(), pdev.data_ptr(), outs[i % n_inst].data_ptr())
+            oh.copy_(normed if args.block else outs[i % n_inst], non_blocking=True)
         e1.record(stream)
     stream.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist if world > 1 else None, dev)
@@ -435,7 +465,7 @@ def our_arm(args, spec):
             "l2": f"rotating {n_inst} layer instances, {n_inst * inst_bytes / 2**20:.0f} MiB "
                   f"> 4x L2 ({l2 / 2**20:.0f} MiB)",
             "arith": "bf16/fp16 tensor-core operands, fp32 accumulate; 8/4/6/3-bit codes",
-            "path": "one kernel per step" if launches == 1 else "five kernels per step"}),
+            "path": "one kernel per step" if launches == 1 else f"{launches} kernels per step"}),
         "tokens_per_s": steps_per_s * tokens_per_step,
         "hbm_gbs": steps_per_s / world * step_bytes / 1e9,
         "hbm_frac_of_peak": steps_per_s / world * step_bytes / 1e9 / peak,
@@ -470,6 +500,9 @@ def main():
     ap.add_argument("--no-head-chunk", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "fused", "split"],
                     help="one-kernel or five-kernel step (auto: one kernel when it fits)")
+    ap.add_argument("--block", action="store_true",
+                    help="time the decoder-block step (input RMSNorm + layer + residual + "
+                         "post-attention RMSNorm) instead of the layer alone")
     args = ap.parse_args()
     spec = synth.WORKLOADS[args.workload]
     if args.impl == "reference":

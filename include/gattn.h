@@ -267,9 +267,37 @@ int32_t gattn_head_chunk_plan(int32_t q_len, int32_t num_heads, int32_t num_kv_h
 enum { GATTN_PATH_AUTO = 0, GATTN_PATH_FUSED = 1, GATTN_PATH_SPLIT = 2 };
 gattn_status gattn_layer_set_path(gattn_layer *layer, int32_t path);
 
+/*
+ * Decoder-block variant of gattn_layer_step: the steps on either side of the
+ * layer in forward_full_attention (Atlas spark_model/forward/qwen3_5/mod.rs,
+ * module doc and FullAttentionLayer: input_ln, post_ln, norm -> projections ->
+ * attention -> residual + post-norm -> MLP).  Per row of x:
+ *   h          = x / sqrt(mean(x^2) + rms_eps) * input_ln     (RMSNorm)
+ *   out        = bf16(x + layer(h))                           (residual stream)
+ *   out_normed = bf16(RMSNorm(out) * post_ln)                 (the MLP's input;
+ *                computed from the stored bf16 row of out)
+ * Arguments: x is the raw hidden state [batch][q_len][hidden] in the layer's x
+ * dtype (device); input_ln and post_ln are bf16 [hidden] device vectors,
+ * borrowed; out is bf16 [batch][q_len][hidden]; out_normed (may be NULL, then
+ * post_ln may be NULL too) is bf16 of the same shape and must not alias out.
+ * Cache, position, launch and error behaviour as gattn_layer_step.  The
+ * post-norm runs inside the o_proj launch (its last CTA to finish normalizes
+ * every row) when batch * q_len * hidden <= 16384 and out, out_normed and
+ * post_ln are 16-byte aligned, else in one more launch.  The norm of the
+ * input is rounded to bf16 for a bf16 layer (kept fp32 for an fp32 one)
+ * before the projections.  GATTN_E_INVALID_ARG for a NULL input_ln,
+ * out_normed without post_ln or aliasing out; GATTN_E_UNSUPPORTED on
+ * GATTN_PATH_FUSED (the one-kernel path runs the layer alone).
+ */
+gattn_status gattn_layer_step_block(gattn_layer *layer, const void *x, gattn_kv *kv,
+                                    const int32_t *cache_pos, int32_t batch, int32_t q_len,
+                                    const void *input_ln, const void *post_ln, void *out,
+                                    void *out_normed, gattn_stream stream);
+
 /* Per-step launch report of the layer's last step: number of kernel launches
  * it enqueued, all of them this library's own kernels (1 on the one-kernel
- * path, 5 on the five-kernel path). */
+ * path, 5 on the five-kernel path, 6 for a decoder-block step whose post-norm
+ * takes its own launch). */
 int32_t gattn_layer_launches_per_step(const gattn_layer *layer);
 
 /* Instrumentation: with n >= 2 cudaEvent_t handles, each following step

@@ -94,8 +94,8 @@ def _declare(L):
     L.orc_sdpa.argtypes = [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p]
     L.orc_layer_step.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _p, _p, _i,
                                  _p, _i, _i, _p, _p, _p]
-    L.orc_block_step.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _p, _p, _p,
-                                 _p, _i, _p, _i, _i, _p, _p]
+    L.orc_block_step.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _i, _p, _p,
+                                 _p, _p, _i, _p, _i, _i, _p, _p]
 
 
 def _ptr(a: np.ndarray | None):
@@ -277,8 +277,10 @@ def block_step(spec, weights: OracleWeights, x: np.ndarray, input_ln: np.ndarray
     """The decoder block around the layer ([atlas-mod] forward_full_attention:
     input RMSNorm -> layer -> residual add -> post-attention RMSNorm): returns
     out = x + layer(RMSNorm(x) * input_ln) and, when post_ln is given,
-    RMSNorm(bf16(out)) * post_ln (else None).  input_ln / post_ln: bf16 bits
-    [hidden]; caches as in layer_step (updated in place)."""
+    RMSNorm(bf16(out)) * post_ln (else None).  The normed input h is rounded
+    to bf16 for a bf16 layer (spec.x_dtype), kept exact for an fp32 one.
+    input_ln / post_ln: bf16 bits [hidden]; caches as in layer_step (updated
+    in place)."""
     B, R, Hd = x.shape
     L, Wt, keep = _layer_structs(spec, weights, head_chunk, "none")
     x = np.ascontiguousarray(x, np.float64)
@@ -288,7 +290,8 @@ def block_step(spec, weights: OracleWeights, x: np.ndarray, input_ln: np.ndarray
     cp = np.ascontiguousarray(cache_pos, np.int32)
     out = np.zeros((B, R, Hd), np.float64)
     on = np.zeros((B, R, Hd), np.float64) if pw is not None else None
-    rc = lib().orc_block_step(C.byref(L), C.byref(Wt), _ptr(x), _ptr(iw), _ptr(pw), _ptr(cache_k),
+    rc = lib().orc_block_step(C.byref(L), C.byref(Wt), _ptr(x),
+                              1 if spec.x_dtype == "bf16" else 0, _ptr(iw), _ptr(pw), _ptr(cache_k),
                               _ptr(cache_v), cache_k.shape[2], _ptr(cp), B, R, _ptr(out), _ptr(on))
     _check(rc, "block_step")
     return out, on

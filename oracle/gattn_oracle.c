@@ -565,9 +565,11 @@ done:
  *   out        = x + layer(h)                       (the residual stream)
  *   out_normed = RMSNorm(bf16(out)) * post_ln       (the MLP's input)
  * The residual stream is stored as bf16, and the post-norm reads the stored
- * row.  input_ln / post_ln are bf16 [hidden]; post_ln and out_normed may be
- * NULL.  Cache behaviour is that of orc_layer_step. */
-int orc_block_step(const orc_layer *L, const orc_weights *W, const double *x,
+ * row.  h is an activation of the residual stream's type: h_bf16 != 0 rounds
+ * it to bf16 (a bf16 stream, as the engine's x_norm buffer), 0 keeps it exact
+ * (an fp32 stream).  input_ln / post_ln are bf16 [hidden]; post_ln and
+ * out_normed may be NULL.  Cache behaviour is that of orc_layer_step. */
+int orc_block_step(const orc_layer *L, const orc_weights *W, const double *x, int h_bf16,
                    const uint16_t *input_ln, const uint16_t *post_ln,
                    uint16_t *cache_k, uint16_t *cache_v, int capacity,
                    const int32_t *cache_pos, int B, int R, double *out, double *out_normed)
@@ -587,6 +589,9 @@ int orc_block_step(const orc_layer *L, const orc_weights *W, const double *x,
         w[i] = orc_bf16_to_double(input_ln[i]);
     for (int64_t m = 0; m < M; ++m)
         orc_rms_norm(x + m * Hd, Hd, w, L->rms_eps, h + m * Hd);
+    if (h_bf16)
+        for (int64_t j = 0; j < M * Hd; ++j)
+            h[j] = orc_bf16_to_double(orc_bf16_from_double(h[j]));
     rc = orc_layer_step(L, W, h, cache_k, cache_v, capacity, cache_pos, B, R, y, NULL, NULL);
     if (rc != ORC_OK)
         goto done;

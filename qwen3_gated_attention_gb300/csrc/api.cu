@@ -183,6 +183,8 @@ struct gattn_layer {
     int GR = 0, ngrp = 0;                  // q|k|v epilogue group rows, groups
     float *part_a = nullptr, *part_o = nullptr;
     unsigned *sync = nullptr;
+    float *ss_part = nullptr;              // decoder-block post-norm: per-CTA sums of squares
+    unsigned *post_ticket = nullptr;
     int s_cnt_a = 0, s_rdy_a = 0, s_seg = 0, s_cnt_o = 0, nsync = 0;
     gattn_taps taps{};
     bool weights_set = false;
@@ -371,6 +373,12 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaMalloc(&L->ws_attn, L->ws_attn_floats * sizeof(float)));
     TRY(cudaMalloc(&L->status, sizeof(unsigned)));
     TRY(cudaMemset(L->status, 0, sizeof(unsigned)));
+    {
+        const int gmax = *std::max_element(L->po.grid, L->po.grid + 3);
+        TRY(cudaMalloc(&L->ss_part, (size_t)gmax * L->M_max * sizeof(float)));
+        TRY(cudaMalloc(&L->post_ticket, sizeof(unsigned)));
+        TRY(cudaMemset(L->post_ticket, 0, sizeof(unsigned)));
+    }
 
     // the one-kernel path: whole heads per epilogue group (GR = lcm(d, 128)
     // rows tiling the k and v rows), every CTA resident (cooperative launch)
@@ -415,7 +423,8 @@ void gattn_layer_destroy(gattn_layer *L)
         return;
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq,
-                    L->q_norm, L->k_norm, L->part_a,  L->part_o,  L->sync};
+                    L->q_norm, L->k_norm, L->part_a,  L->part_o,  L->sync,
+                    L->ss_part, L->post_ticket};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -539,8 +548,17 @@ gattn_status gattn_layer_set_events(gattn_layer *L, void *const *events, int32_t
     return GATTN_OK;
 }
 
-gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const int32_t *cache_pos,
-                              int32_t batch, int32_t q_len, void *out, gattn_stream stream)
+namespace {
+
+// The decoder block around the layer (gattn_layer_step_block); null: the layer alone.
+struct BlockArgs {
+    const uint16_t *input_ln, *post_ln;
+    __nv_bfloat16 *out_normed;
+};
+
+gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_t *cache_pos,
+                       int32_t batch, int32_t q_len, void *out, gattn_stream stream,
+                       const BlockArgs *blk)
 {
     if (!L || !x || !kv || !cache_pos || !out)
         return fail(GATTN_E_INVALID_ARG, "NULL argument");
@@ -598,7 +616,10 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
 
     // ---- one kernel for the whole step when the operand is one column tile
-    // the default stays on the five-kernel path until the one-kernel path is faster
+    // the default stays on the five-kernel path until the one-kernel path is faster;
+    // the one-kernel path runs the layer alone (no decoder-block steps)
+    if (L->path == GATTN_PATH_FUSED && blk)
+        return fail(GATTN_E_UNSUPPORTED, "the one-kernel path runs no decoder-block steps");
     if (L->path == GATTN_PATH_FUSED) {
         // x arrives by bulk copy: 16-byte alignment
         bool ok = L->fused_ok && Ma <= 8 && batch <= kFMaxB && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
@@ -701,7 +722,8 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
 
     // 1. x -> fp16 tensor-core operand + group sums
     CUDA_TRY(mark(0));
-    CUDA_TRY(launch_xprep(x, c.x_dtype, M, c.hidden, L->pqkv.group, NTa, L->x16_a, L->xsum_a, pdl, s));
+    CUDA_TRY(launch_xprep(x, c.x_dtype, M, c.hidden, L->pqkv.group, NTa, L->x16_a, L->xsum_a,
+                          blk ? blk->input_ln : nullptr, c.rms_eps, pdl, s));
     ++launches;
 
     // 2. fused q|k|v projection with the norm / rotary / append epilogue
@@ -800,12 +822,59 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
     e2.cache_pos = cache_pos;
     e2.cap = kv->desc.capacity;
     e2.out = static_cast<__nv_bfloat16 *>(out);
+    e2.resid = blk ? x : nullptr;
+    e2.resid_f32 = c.x_dtype == GATTN_DTYPE_F32;
+    // decoder block: the post-norm rides in this launch when one CTA can do
+    // it quickly and the rows allow 16-byte vectors
+    auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    const bool post_fused = blk && blk->out_normed && M * c.hidden <= kPostFuseMaxElems &&
+                            a16(out) && a16(blk->out_normed) && a16(blk->post_ln);
+    if (post_fused) {
+        e2.post_w = blk->post_ln;
+        e2.out_n = blk->out_normed;
+        e2.eps = c.rms_eps;
+        e2.ss_part = L->ss_part;
+        e2.ticket = L->post_ticket;
+    }
     CUDA_TRY(mark(4));
     CUDA_TRY(launch_proj(L->po.bits, NT, kModeO, o, eq, e2, L->po.grid[ni], pdl, s));
     ++launches;
+
+    // 5. decoder block: the post-attention RMSNorm of the residual stream,
+    //    in its own launch when the o_proj did not take it
+    if (blk && blk->out_normed && !post_fused) {
+        CUDA_TRY(mark(launches));
+        CUDA_TRY(launch_postnorm(static_cast<const __nv_bfloat16 *>(out), blk->post_ln, c.rms_eps, M,
+                                 c.hidden, blk->out_normed, pdl, s));
+        ++launches;
+    }
     CUDA_TRY(mark_end());
     L->launches = launches;
     return GATTN_OK;
+}
+
+}  // namespace
+
+gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const int32_t *cache_pos,
+                              int32_t batch, int32_t q_len, void *out, gattn_stream stream)
+{
+    return step_impl(L, x, kv, cache_pos, batch, q_len, out, stream, nullptr);
+}
+
+gattn_status gattn_layer_step_block(gattn_layer *L, const void *x, gattn_kv *kv,
+                                    const int32_t *cache_pos, int32_t batch, int32_t q_len,
+                                    const void *input_ln, const void *post_ln, void *out,
+                                    void *out_normed, gattn_stream stream)
+{
+    if (!input_ln)
+        return fail(GATTN_E_INVALID_ARG, "input_ln is NULL");
+    if (out_normed && !post_ln)
+        return fail(GATTN_E_INVALID_ARG, "out_normed needs post_ln");
+    if (out_normed && out_normed == out)
+        return fail(GATTN_E_INVALID_ARG, "out_normed must not alias out");
+    BlockArgs blk{static_cast<const uint16_t *>(input_ln), static_cast<const uint16_t *>(post_ln),
+                  static_cast<__nv_bfloat16 *>(out_normed)};
+    return step_impl(L, x, kv, cache_pos, batch, q_len, out, stream, &blk);
 }
 
 gattn_status gattn_layer_poll_status(gattn_layer *L, gattn_stream stream)

@@ -95,7 +95,20 @@ struct EpiO {
     const int *cache_pos;
     int cap;
     __nv_bfloat16 *out;            // [M][N]
+    const void *resid;             // decoder block: out = bf16(resid + o_proj), or null
+    int resid_f32;                 // resid dtype: fp32 (1) or bf16 (0)
+    // decoder block, post-attention RMSNorm in the o_proj launch (null: none):
+    // out_n = bf16(RMSNorm(out) * post_w), finished by the last CTA to arrive
+    const uint16_t *post_w;        // [N] bf16 bits
+    __nv_bfloat16 *out_n;          // [M][N]
+    float eps;
+    float *ss_part;                // [grid][M] each CTA's sums of squares of its stored rows
+    unsigned *ticket;              // CTAs arrived; zero between launches
 };
+
+// the post-norm rides in the o_proj launch up to this many output elements
+// (one CTA normalizes every row); larger steps launch postnorm_kernel
+constexpr int kPostFuseMaxElems = 16384;
 
 enum { kModeQKV = 0, kModeO = 1 };
 
@@ -110,8 +123,12 @@ cudaError_t proj_max_clusters(int bits, int NT, int mode, int group, int smem, i
 
 // fp32 x is split exactly into hi = fp16(x) (column m) and lo = fp16(x - hi)
 // (column M + m); bf16 x converts to fp16 exactly (finite, |x| < 65504).
+// in_w (bf16 [K], or null): decoder-block input, the operand is RMSNorm(x) * in_w.
 cudaError_t launch_xprep(const void *x, int x_dtype, int M, int K, int group, int NT, __half *x16,
-                         float *xsum, bool pdl, cudaStream_t s);
+                         float *xsum, const uint16_t *in_w, float eps, bool pdl, cudaStream_t s);
+// out_n[m] = bf16(RMSNorm(r[m]) * w) for the M bf16 rows of r (N columns each).
+cudaError_t launch_postnorm(const __nv_bfloat16 *r, const uint16_t *w, float eps, int M, int N,
+                            __nv_bfloat16 *out_n, bool pdl, cudaStream_t s);
 
 struct RepackSrc {
     const uint32_t *packed[3];

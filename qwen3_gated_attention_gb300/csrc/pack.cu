@@ -202,21 +202,67 @@ cudaError_t launch_unpack_codes(const uint32_t *packed, long long N, long long K
 
 // x [M][K] (fp32 or bf16) -> fp16 B fragments + fp32 group sums of the fp16
 // values.  One CTA per 128-wide k unit; thread (m, part) converts 16 elements.
-__global__ void __launch_bounds__(256) xprep_kernel(const void *x, int x_dtype, int M, int K,
-                                                    int group, int NT, __half *x16, float *xsum)
+// Row m's input RMSNorm factor 1 / sqrt(mean(x^2) + eps) over all K columns:
+// one warp per row, four vector loads in flight per lane.
+__device__ __forceinline__ float row_inv_rms(const void *x, int x_dtype, int m, int K, int lane,
+                                             float eps)
 {
+    float ss = 0.f;
+    if (x_dtype == 0) {
+        const float4 *row = reinterpret_cast<const float4 *>(static_cast<const float *>(x) +
+                                                             (long long)m * K);
+#pragma unroll 4
+        for (int i = lane; i < K / 4; i += 32) {
+            const float4 f = row[i];
+            ss = fmaf(f.x, f.x, fmaf(f.y, f.y, fmaf(f.z, f.z, fmaf(f.w, f.w, ss))));
+        }
+    } else {
+        const uint4 *row = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(x) +
+                                                           (long long)m * K);
+#pragma unroll 4
+        for (int i = lane; i < K / 8; i += 32) {
+            const uint4 u = row[i];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+                ss = fmaf(a, a, fmaf(b, b, ss));
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    return rsqrtf(ss / (float)K + eps);
+}
+
+__global__ void __launch_bounds__(256) xprep_kernel(const void *x, int x_dtype, int M, int K,
+                                                    int group, int NT, __half *x16, float *xsum,
+                                                    const uint16_t *in_w, float eps)
+{
+    __shared__ float s_inv[32];
     // the next kernel (the q|k|v projection) may start streaming weights at once
     pdl_launch_dependents();
     pdl_wait();
     const int ku = blockIdx.x;
     const int m = threadIdx.x >> 3, part = threadIdx.x & 7;
     const int MP = 8 * NT;
+    if (in_w) {                 // decoder-block input: per-row norm factors first
+        for (int rr = threadIdx.x >> 5; rr < M; rr += blockDim.x >> 5) {
+            const float inv = row_inv_rms(x, x_dtype, rr, K, threadIdx.x & 31, eps);
+            if ((threadIdx.x & 31) == 0)
+                s_inv[rr] = inv;
+        }
+        __syncthreads();
+    }
     if (m >= MP)
         return;
     const int k0 = ku * kKU + part * 16;
     // fp32 input: columns [M, 2M) carry the exact remainder x - fp16(x)
     const bool lo_part = x_dtype == 0 && m >= M && m < 2 * M;
     const int src_m = lo_part ? m - M : m;
+    // decoder-block input: the operand is RMSNorm(x) * input_ln
+    const float scale = in_w && (m < M || lo_part) ? s_inv[src_m] : 1.f;
     float v[16];
     if (m < M || lo_part) {
         if (x_dtype == 0) {
@@ -249,6 +295,16 @@ __global__ void __launch_bounds__(256) xprep_kernel(const void *x, int x_dtype, 
         for (int i = 0; i < 16; ++i)
             v[i] = 0.f;
     }
+    if (in_w && (m < M || lo_part)) {
+        // the normed row is an activation of the residual stream's type: bf16
+        // rows give a bf16 operand, fp32 rows keep fp32 (hi + lo columns)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            v[i] = v[i] * scale * __uint_as_float((uint32_t)in_w[k0 + i] << 16);
+            if (x_dtype != 0)
+                v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+        }
+    }
     __half h[16];
     float sum = 0.f;
 #pragma unroll
@@ -280,7 +336,7 @@ __global__ void __launch_bounds__(256) xprep_kernel(const void *x, int x_dtype, 
 }
 
 cudaError_t launch_xprep(const void *x, int x_dtype, int M, int K, int group, int NT, __half *x16,
-                         float *xsum, bool pdl, cudaStream_t s)
+                         float *xsum, const uint16_t *in_w, float eps, bool pdl, cudaStream_t s)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(K / kKU);
@@ -291,7 +347,57 @@ cudaError_t launch_xprep(const void *x, int x_dtype, int M, int K, int group, in
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, xprep_kernel, x, x_dtype, M, K, group, NT, x16, xsum);
+    return cudaLaunchKernelEx(&cfg, xprep_kernel, x, x_dtype, M, K, group, NT, x16, xsum, in_w, eps);
+}
+
+}  // namespace gattn
+
+namespace gattn {
+
+// Post-attention RMSNorm of the decoder block: one CTA per row of the stored
+// bf16 residual stream, out_n = bf16(r / sqrt(mean(r^2) + eps) * w).
+__global__ void __launch_bounds__(256) postnorm_kernel(const __nv_bfloat16 *r, const uint16_t *w,
+                                                       float eps, int N, __nv_bfloat16 *out_n)
+{
+    __shared__ float red[8];
+    pdl_launch_dependents();
+    pdl_wait();                 // r is the o_proj's output
+    const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const __nv_bfloat16 *row = r + (long long)m * N;
+    float ss = 0.f;
+    for (int i = tid; i < N; i += 256) {
+        const float v = __bfloat162float(row[i]);
+        ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0)
+        red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < 8; ++w2)
+        tot += red[w2];
+    const float inv = rsqrtf(tot / (float)N + eps);
+    for (int i = tid; i < N; i += 256)
+        out_n[(long long)m * N + i] = __float2bfloat16_rn(
+            __bfloat162float(row[i]) * inv * __uint_as_float((uint32_t)w[i] << 16));
+}
+
+cudaError_t launch_postnorm(const __nv_bfloat16 *r, const uint16_t *w, float eps, int M, int N,
+                            __nv_bfloat16 *out_n, bool pdl, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(M);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, postnorm_kernel, r, w, eps, N, out_n);
 }
 
 }  // namespace gattn

@@ -269,9 +269,84 @@ static __device__ void epilogue_o(const ProjArgs &a, const EpiO &e, const EpiSme
         const int b = m / e.R;
         const int pb = sm.cpos[b];
         const bool valid = pb >= 0 && pb + e.R <= e.cap;
-        const float v = valid ? cluster_row_sum<MP, 8>(a, sm, r, m) : 0.f;
+        float v = valid ? cluster_row_sum<MP, 8>(a, sm, r, m) : 0.f;
+        if (e.resid) {
+            const long long ri = (long long)m * a.N + n;
+            v += e.resid_f32 ? static_cast<const float *>(e.resid)[ri]
+                             : __uint_as_float((uint32_t)static_cast<const uint16_t *>(e.resid)[ri]
+                                               << 16);
+        }
         e.out[(long long)m * a.N + n] = __float2bfloat16_rn(v);
     }
+}
+
+// Decoder-block post-norm inside the o_proj launch, after the cluster's last
+// barrier (the stage ring is free again).  Each CTA adds up the squares of the
+// bf16 rows it stored (its own writes, in a fixed order) into its slot of
+// ss_part; the CTA that takes the last ticket sums the slots in CTA order and
+// writes out_n = bf16(out * rsqrt(mean(out^2) + eps) * post_w).  Nothing
+// waits: CTAs that are not last just leave.
+template <int MP>
+static __device__ void postnorm_tail(const ProjArgs &a, const EpiO &e, float *scratch, int row0,
+                                     int rank, int csize)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kWarps = kWR + 1;
+    const int rpr = (kRBR + csize - 1) / csize;
+    const int r0 = rank * rpr;
+    const int nr = max(0, min(min(rpr, kRBR - r0), a.N - (row0 + r0)));
+    __syncthreads();            // this CTA's out stores are visible to all its threads
+    for (int m = warp; m < a.M; m += kWarps) {
+        float ss = 0.f;
+        for (int j = lane; j < nr; j += 32) {
+            const float v = __bfloat162float(e.out[(long long)m * a.N + row0 + r0 + j]);
+            ss = fmaf(v, v, ss);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0)
+            e.ss_part[(long long)blockIdx.x * a.M + m] = ss;
+    }
+    __threadfence();
+    __syncthreads();
+    unsigned *last = reinterpret_cast<unsigned *>(scratch);
+    if (tid == 0)
+        *last = atomicAdd(e.ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!*last)
+        return;
+    __threadfence();
+    float *inv = scratch + 32;
+    for (int m = warp; m < a.M; m += kWarps) {
+        float ss = 0.f;
+        for (int c = lane; c < (int)gridDim.x; c += 32)
+            ss += __ldcg(e.ss_part + (long long)c * a.M + m);
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0)
+            inv[m] = rsqrtf(ss / (float)a.N + e.eps);
+    }
+    __syncthreads();
+    const int vpr = a.N / 8;    // 16-byte vectors per row
+    for (int i = tid; i < a.M * vpr; i += kWarps * 32) {
+        const int m = i / vpr, c8 = i - m * vpr;
+        const uint4 u = __ldcg(reinterpret_cast<const uint4 *>(e.out + (long long)m * a.N) + c8);
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(e.post_w) + c8);
+        const uint32_t uu[4] = {u.x, u.y, u.z, u.w}, ww[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o[4];
+        const float f = inv[m];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(bf16_lo(uu[j]) * f * bf16_lo(ww[j]),
+                                                          bf16_hi(uu[j]) * f * bf16_hi(ww[j]));
+            o[j] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        reinterpret_cast<uint4 *>(e.out_n + (long long)m * a.N)[c8] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (tid == 0)
+        *e.ticket = 0u;         // ready for the next launch
 }
 
 // shared memory past the stage ring: barriers, flags, epilogue statics
@@ -443,6 +518,11 @@ __global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
             epilogue_o<MP>(a, eo, sm, row0, rank, csize, threadIdx.x);
     }
     cluster_sync();     // no CTA leaves while others may still read its partial
+    if constexpr (MODE == kModeO) {
+        if (eo.out_n)
+            postnorm_tail<MP>(a, eo, reinterpret_cast<float *>(stages), cluster * a.eb_rows, rank,
+                              csize);
+    }
 }
 
 template <int BITS, int NT, int MODE, int GROUP>

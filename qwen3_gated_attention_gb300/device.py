@@ -92,6 +92,15 @@ class DeviceLayer:
         gattn.layer_step(self.h, x.data_ptr(), self.kv, cache_pos.data_ptr(), batch or self.batch,
                          q_len or self.spec.q_len, out.data_ptr(), s)
 
+    def step_block(self, x: torch.Tensor, cache_pos: torch.Tensor, input_ln: torch.Tensor,
+                   post_ln: torch.Tensor | None, out: torch.Tensor,
+                   out_normed: torch.Tensor | None = None, batch=None, q_len=None, stream=None):
+        s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        gattn.layer_step_block(self.h, x.data_ptr(), self.kv, cache_pos.data_ptr(),
+                               batch or self.batch, q_len or self.spec.q_len, input_ln.data_ptr(),
+                               post_ln.data_ptr() if post_ln is not None else None, out.data_ptr(),
+                               out_normed.data_ptr() if out_normed is not None else None, s)
+
     def set_taps(self, y: torch.Tensor | None, attn: torch.Tensor | None):
         gattn.layer_set_taps(self.h, y.data_ptr() if y is not None else None,
                              attn.data_ptr() if attn is not None else None)

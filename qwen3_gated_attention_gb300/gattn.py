@@ -31,7 +31,7 @@ EXPORTS = (
     "gattn_layer_destroy", "gattn_kv_destroy", "gattn_last_error", "gattn_pack_affine_host",
     "gattn_unpack_codes_device", "gattn_layer_dequant_device", "gattn_head_chunk_plan",
     "gattn_layer_launches_per_step", "gattn_layer_set_events", "gattn_layer_dequant_device_static",
-    "gattn_layer_set_path",
+    "gattn_layer_set_path", "gattn_layer_step_block",
 )
 
 
@@ -104,11 +104,13 @@ def lib():
         L.gattn_layer_launches_per_step.restype = i32
         L.gattn_layer_set_events.argtypes = [p, p, i32]
         L.gattn_layer_set_path.argtypes = [p, i32]
+        L.gattn_layer_step_block.argtypes = [p, p, p, p, i32, i32, p, p, p, p, p]
         for name in ("gattn_cfg_validate", "gattn_layer_create", "gattn_layer_set_weights",
                      "gattn_kv_register", "gattn_layer_step", "gattn_layer_poll_status",
                      "gattn_layer_set_taps", "gattn_pack_affine_host", "gattn_unpack_codes_device",
                      "gattn_layer_dequant_device", "gattn_layer_set_events",
-                     "gattn_layer_dequant_device_static", "gattn_layer_set_path"):
+                     "gattn_layer_dequant_device_static", "gattn_layer_set_path",
+                     "gattn_layer_step_block"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -205,6 +207,15 @@ def kv_destroy(kv: int) -> None:
 
 def layer_launches_per_step(layer: int) -> int:
     return int(lib().gattn_layer_launches_per_step(layer))
+
+
+def layer_step_block(layer: int, x: int, kv: int, cache_pos: int, batch: int, q_len: int,
+                     input_ln: int, post_ln: int | None, out: int, out_normed: int | None,
+                     stream: int | None = None) -> None:
+    """Decoder-block step: out = x + layer(RMSNorm(x) * input_ln); out_normed =
+    RMSNorm(out) * post_ln when given (device pointers)."""
+    _check(lib().gattn_layer_step_block(layer, x, kv, cache_pos, batch, q_len, input_ln, post_ln,
+                                        out, out_normed, stream))
 
 
 def layer_set_path(layer: int, path: int) -> None:

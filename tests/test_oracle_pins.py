@@ -444,12 +444,33 @@ def test_block_layer_part_is_invariant_to_the_input_scale():
     assert bad > 1e-3      # the check above has power: scaled layer parts differ
 
 
-def test_block_reduces_to_the_layer_on_unit_rms_rows():
-    """input_ln = 1 and rows of unit RMS: h = x up to eps, so out - x is the layer."""
-    spec = synth.WORKLOADS["batched_mixed_small"] if "batched_mixed_small" in synth.WORKLOADS else \
-        synth.WORKLOADS["tiny"].with_(batch=3, q_len=2, cache_pos=None, length_range=(20, 300))
-    x = synth.x_values(spec, synth.layer_input(spec))
-    x = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True))
+def _unit_rms_bf16_rows(B, R, hidden, seed):
+    """Rows whose every element is a bf16 number and whose mean square is
+    exactly 1: groups of five (+-2, +-0.5 x 4; squares summing to 5) with the
+    rest +-1, in random places and signs."""
+    rng = np.random.default_rng(seed)
+    x = np.empty((B, R, hidden))
+    for b in range(B):
+        for r in range(R):
+            g = rng.integers(0, hidden // 5 + 1)
+            row = np.array([2.0] * g + [0.5] * (4 * g) + [1.0] * (hidden - 5 * g))
+            x[b, r] = rng.permutation(row) * rng.choice([-1.0, 1.0], hidden)
+    assert np.all(np.mean(x * x, axis=-1) == 1.0)
+    return x
+
+
+@pytest.mark.parametrize("x_dtype", ["f32", "bf16"])
+def test_block_reduces_to_the_layer_on_unit_rms_rows(x_dtype):
+    """input_ln = 1 and rows of unit RMS: h = x up to eps, so out - x is the
+    layer.  For a bf16 layer the rows are bf16 numbers, where rounding h to
+    bf16 gives back x exactly (eps moves it by far less than half an ulp)."""
+    spec = synth.WORKLOADS["tiny"].with_(batch=3, q_len=2, cache_pos=None,
+                                         length_range=(20, 300), x_dtype=x_dtype)
+    if x_dtype == "f32":
+        x = synth.x_values(spec, synth.layer_input(spec))
+        x = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True))
+    else:
+        x = _unit_rms_bf16_rows(spec.batch, spec.q_len, spec.hidden, 7)
     ones = np.full(spec.hidden, 0x3F80, np.uint16)
     case, out, _, k2, v2 = _block(spec, x, input_ln=ones)
     k3, v3 = case.ck.copy(), case.cv.copy()
