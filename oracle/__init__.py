@@ -33,6 +33,7 @@ MUTATIONS = {
     "split_alternate": 7,
     "no_knorm": 8,
     "no_bf16_cache": 9,
+    "turbo_no_iwht": 10,
 }
 
 
@@ -96,6 +97,18 @@ def _declare(L):
                                  _p, _i, _i, _p, _p, _p]
     L.orc_block_step.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _i, _p, _p,
                                  _p, _p, _i, _p, _i, _i, _p, _p]
+    L.orc_e4m3_to_double.argtypes = [C.c_uint8]
+    L.orc_e4m3_to_double.restype = C.c_double
+    L.orc_e4m3_from_float.argtypes = [C.c_float]
+    L.orc_e4m3_from_float.restype = C.c_uint8
+    L.orc_turbo4_codebook.argtypes = [_p]
+    L.orc_turbo4_codebook.restype = None
+    L.orc_turbo4_tables_f32.argtypes = [_p, _p]
+    L.orc_turbo4_tables_f32.restype = None
+    L.orc_turbo4_quantize_rows.argtypes = [_p, _i64, _i, _p, _p]
+    L.orc_turbo4_dequant_rows.argtypes = [_p, _p, _i64, _i, _i, _p]
+    L.orc_layer_step_turbo4v.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _p, _p,
+                                         _p, _i, _p, _i, _i, _p, _p, _p]
 
 
 def _ptr(a: np.ndarray | None):
@@ -266,6 +279,88 @@ def layer_step(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.ndarray,
     rc = lib().orc_layer_step(C.byref(L), C.byref(Wt), _ptr(x), _ptr(cache_k), _ptr(cache_v), cap,
                               _ptr(cp), B, R, _ptr(out), _ptr(ty), _ptr(ta))
     _check(rc, "layer_step")
+    if taps:
+        return out, ty, ta
+    return out
+
+
+# ------------------------------------------------- Turbo4 V cache ([atlas-mod])
+
+def e4m3_to_double(b: int) -> float:
+    """Value of an FP8 E4M3 byte ([atlas-mod] MetalKvDtype: FP8 group scales)."""
+    return lib().orc_e4m3_to_double(int(b))
+
+
+def e4m3_from_float(x: float) -> int:
+    """Nearest E4M3 byte of an fp32 value (ties to even, saturating at 448)."""
+    return int(lib().orc_e4m3_from_float(float(np.float32(x))))
+
+
+def turbo4_codebook() -> np.ndarray:
+    """The 16 Lloyd-Max levels of N(0, 1), ascending, float64 ([atlas-mod]
+    MetalKvDtype::Turbo4: 4-bit Lloyd-Max codebook indices)."""
+    c = np.zeros(16, np.float64)
+    lib().orc_turbo4_codebook(_ptr(c))
+    return c
+
+
+def turbo4_tables_f32():
+    """(levels fp32 [16], decision thresholds fp32 [15]) the quantizer uses."""
+    lv = np.zeros(16, np.float32)
+    th = np.zeros(15, np.float32)
+    lib().orc_turbo4_tables_f32(_ptr(lv), _ptr(th))
+    return lv, th
+
+
+def turbo4_quantize_rows(v_bf16: np.ndarray):
+    """bf16 bits [..., d] -> (codes uint8 [..., d/2], scales uint8 [..., d/16]):
+    WHT rotation, per-16 RMS-normalized nearest Lloyd-Max level, matched-norm
+    E4M3 scale; decisions in fp32 in the order the C source states."""
+    v = np.ascontiguousarray(v_bf16, np.uint16)
+    d = v.shape[-1]
+    n = v.size // d
+    codes = np.zeros(v.shape[:-1] + (d // 2,), np.uint8)
+    scales = np.zeros(v.shape[:-1] + (d // 16,), np.uint8)
+    _check(lib().orc_turbo4_quantize_rows(_ptr(v), n, d, _ptr(codes), _ptr(scales)),
+           "turbo4_quantize_rows")
+    return codes, scales
+
+
+def turbo4_dequant_rows(codes: np.ndarray, scales: np.ndarray, mutate: str = "none") -> np.ndarray:
+    """(codes [..., d/2], scales [..., d/16]) -> float64 rows [..., d] in the
+    original basis (the inverse rotation applied)."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    d = codes.shape[-1] * 2
+    n = codes.size // (d // 2)
+    out = np.zeros(codes.shape[:-1] + (d,), np.float64)
+    _check(lib().orc_turbo4_dequant_rows(_ptr(codes), _ptr(scales), n, d, MUTATIONS[mutate],
+                                         _ptr(out)), "turbo4_dequant_rows")
+    return out
+
+
+def layer_step_turbo4v(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.ndarray,
+                       v_codes: np.ndarray, v_scales: np.ndarray, cache_pos: np.ndarray,
+                       head_chunk: bool = True, mutate: str = "none", taps: bool = False):
+    """layer_step over a Bf16KTurbo4V cache ([atlas-mod] MetalKvDtype,
+    LayerKvCache): K bf16 [B][Hk][cap][d]; V codes [B][Hk][cap][d/2] and
+    E4M3 scales [B][Hk][cap][d/16], all updated in place."""
+    B, R, Hd = x.shape
+    L, Wt, keep = _layer_structs(spec, weights, head_chunk, mutate)
+    x = np.ascontiguousarray(x, np.float64)
+    for a in (cache_k, v_codes, v_scales):
+        assert a.flags["C_CONTIGUOUS"]
+    cap = cache_k.shape[2]
+    assert v_codes.dtype == np.uint8 and v_scales.dtype == np.uint8
+    cp = np.ascontiguousarray(cache_pos, np.int32)
+    out = np.zeros((B, R, Hd), np.float64)
+    H, Hk, d = spec.num_heads, spec.num_kv_heads, spec.head_dim
+    ty = np.zeros((B, R, 2 * H * d + 2 * Hk * d), np.float64) if taps else None
+    ta = np.zeros((B, R, H, d), np.float64) if taps else None
+    rc = lib().orc_layer_step_turbo4v(C.byref(L), C.byref(Wt), _ptr(x), _ptr(cache_k),
+                                      _ptr(v_codes), _ptr(v_scales), cap, _ptr(cp), B, R,
+                                      _ptr(out), _ptr(ty), _ptr(ta))
+    _check(rc, "layer_step_turbo4v")
     if taps:
         return out, ty, ta
     return out

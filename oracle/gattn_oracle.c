@@ -246,6 +246,7 @@ enum {
     ORC_MUT_SPLIT_ALTERNATE = 7,/* query/gate taken element-wise alternating */
     ORC_MUT_NO_KNORM = 8,       /* skip the K RMSNorm */
     ORC_MUT_NO_BF16_CACHE = 9,  /* attend the new rows unrounded */
+    ORC_MUT_TURBO_NO_IWHT = 10, /* Turbo4 V: dequantize without rotating back */
 };
 
 /* x[0..d) rotated in place at position pos; only dims [0, rd) move. */
@@ -382,6 +383,249 @@ int orc_sdpa(const double *q, const uint16_t *cache_k, const uint16_t *cache_v,
     return ORC_OK;
 }
 
+/* ------------------------------------------------ Turbo4 V cache
+ *
+ * [atlas-mod] MetalKvDtype / LayerKvCache: the Bf16KTurbo4V format keeps K as
+ * raw bf16 and stores V in a Walsh-Hadamard-rotated basis as 4-bit Lloyd-Max
+ * codebook indices (two per byte) with one FP8 E4M3 scale per group of 16
+ * coordinates ("matched-norm L2"); the attention output is rotated back.  The
+ * pages name the parts, not the formulas; the readings taken:
+ *   - rotation: y = H v / sqrt(d), H the Sylvester Hadamard matrix of order d
+ *     (natural order), by the fast transform with stages h = 1, 2, 4, ...
+ *   - codebook: the 16-level Lloyd-Max quantizer of N(0, 1), levels ascending,
+ *     index j for level j; a group's coordinates are divided by the group's RMS
+ *     and each takes the nearest level (a tie goes to the lower level).
+ *   - scale: s = ||y_g|| / ||c(idx_g)||, so the dequantized group keeps the
+ *     group's L2 norm; stored as E4M3 (nearest, ties to even, saturating).
+ *   - input: the bf16 V row the cache would otherwise hold.  The quantizer's
+ *     decisions (codes, scale byte) are taken in fp32 in a fixed order: the
+ *     butterfly stages in order, the 1/sqrt(d) factor (rounded to fp32) after
+ *     them, pairwise sums over each group ((a0+a1)+(a2+a3))+..., correctly
+ *     rounded sqrt and division.  A kernel taking them the same way agrees
+ *     bit for bit.
+ *   - byte j/2 of a row holds code j in its low nibble (j even) or its high
+ *     nibble (j odd); row r of a (sequence, KV head) is d/2 code bytes and d/16
+ *     scale bytes, rows in token order.
+ *   - dequantized row: v = H (s * c(idx)) / sqrt(d), in float64.
+ */
+
+/* E4M3 (OCP FP8): sign, 4 exponent bits (bias 7), 3 mantissa bits; no
+ * infinities, S.1111.111 is NaN, largest finite 448, subnormals m * 2^-9. */
+double orc_e4m3_to_double(uint8_t b)
+{
+    const int e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return (b & 0x80) ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to the even mantissa, magnitudes past 448
+ * saturating to 448; NaN gives the NaN byte. */
+uint8_t orc_e4m3_from_float(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int e2;
+    frexp(a, &e2);
+    int be = e2 - 1;                    /* a in [2^be, 2^(be+1)) */
+    if (be < -6)
+        be = -6;                        /* subnormal quantum below 2^-6 */
+    const double q = ldexp(1.0, be - 3);
+    const double n = nearbyint(a / q);  /* a / q is exact; ties to even */
+    const double v = n * q;
+    if (v == 0.0)
+        return sign;
+    frexp(v, &e2);
+    const int bv = e2 - 1;
+    if (bv < -6)
+        return sign | (uint8_t)(v / ldexp(1.0, -9));
+    return sign | (uint8_t)((bv + 7) << 3) | (uint8_t)(v / ldexp(1.0, bv - 3) - 8.0);
+}
+
+static double gauss_pdf(double x)
+{
+    return isinf(x) ? 0.0 : exp(-0.5 * x * x) / sqrt(6.283185307179586476925);
+}
+
+/* P(a < X < b) for X ~ N(0, 1), from the tail on the side of the cell */
+static double gauss_mass(double a, double b)
+{
+    const double r2 = 1.4142135623730950488;
+    if (a >= 0.0)
+        return 0.5 * (erfc(a / r2) - erfc(b / r2));
+    return 0.5 * (erfc(-b / r2) - erfc(-a / r2));
+}
+
+/* The 16 levels of the Lloyd-Max quantizer of N(0, 1): Lloyd's iteration
+ * (thresholds at the midpoints of the levels, each level the mean of N(0, 1)
+ * over its cell) from 16 evenly spaced levels on [-3, 3], run to its fixed
+ * point (it settles to rounding noise in under a thousand rounds). */
+void orc_turbo4_codebook(double c[16])
+{
+    static double cached[16];
+    static int have = 0;            /* the oracle is single-threaded */
+    if (have) {
+        memcpy(c, cached, sizeof(cached));
+        return;
+    }
+    double lv[16], t[17];
+    for (int j = 0; j < 16; ++j)
+        lv[j] = -3.0 + 6.0 * (j + 0.5) / 16.0;
+    for (int it = 0; it < 4000; ++it) {
+        t[0] = -INFINITY;
+        t[16] = INFINITY;
+        for (int j = 1; j < 16; ++j)
+            t[j] = 0.5 * (lv[j - 1] + lv[j]);
+        for (int j = 0; j < 16; ++j)
+            lv[j] = (gauss_pdf(t[j]) - gauss_pdf(t[j + 1])) / gauss_mass(t[j], t[j + 1]);
+    }
+    memcpy(cached, lv, sizeof(lv));
+    have = 1;
+    memcpy(c, lv, sizeof(lv));
+}
+
+/* fp32 levels and the 15 decision thresholds between them (midpoints taken
+ * in double, then rounded) */
+void orc_turbo4_tables_f32(float levels[16], float thresholds[15])
+{
+    double c[16];
+    orc_turbo4_codebook(c);
+    for (int j = 0; j < 16; ++j)
+        levels[j] = (float)c[j];
+    for (int j = 0; j < 15; ++j)
+        thresholds[j] = (float)(0.5 * (c[j] + c[j + 1]));
+}
+
+static float pairwise16(const float *a)
+{
+    float t[16];
+    memcpy(t, a, sizeof(t));
+    for (int w = 1; w < 16; w <<= 1)
+        for (int i = 0; i < 16; i += 2 * w)
+            t[i] = t[i] + t[i + w];
+    return t[0];
+}
+
+/* n rows of d bf16 values -> codes [n][d/2] and scales [n][d/16] */
+int orc_turbo4_quantize_rows(const uint16_t *v, int64_t n, int d, uint8_t *codes, uint8_t *scales)
+{
+    if (d < 16 || d > 1024 || (d & (d - 1)) || n < 0)
+        return ORC_E_ARG;
+    float lv[16], th[15], y[1024], sq[16], cq[16];
+    orc_turbo4_tables_f32(lv, th);
+    const float sc = (float)(1.0 / sqrt((double)d));
+    for (int64_t row = 0; row < n; ++row) {
+        const uint16_t *vr = v + row * d;
+        uint8_t *cr = codes + row * (d / 2), *sr = scales + row * (d / 16);
+        for (int j = 0; j < d; ++j)
+            y[j] = (float)orc_bf16_to_double(vr[j]);
+        for (int h = 1; h < d; h <<= 1)
+            for (int i = 0; i < d; ++i)
+                if (!(i & h)) {
+                    const float a = y[i], b = y[i + h];
+                    y[i] = a + b;
+                    y[i + h] = a - b;
+                }
+        for (int j = 0; j < d; ++j)
+            y[j] = y[j] * sc;
+        for (int g = 0; g < d / 16; ++g) {
+            const float *yg = y + 16 * g;
+            uint8_t idx[16];
+            for (int i = 0; i < 16; ++i)
+                sq[i] = yg[i] * yg[i];
+            const float ss = pairwise16(sq);
+            if (ss == 0.0f) {
+                memset(idx, 0, sizeof(idx));
+                sr[g] = 0;
+            } else {
+                const float r = sqrtf(ss * 0.0625f);
+                for (int i = 0; i < 16; ++i) {
+                    const float u = yg[i] / r;
+                    int k = 0;
+                    while (k < 15 && u > th[k])
+                        ++k;
+                    idx[i] = (uint8_t)k;
+                    cq[i] = lv[k] * lv[k];
+                }
+                const float cs = pairwise16(cq);
+                sr[g] = orc_e4m3_from_float(sqrtf(ss / cs));
+            }
+            for (int i = 0; i < 16; i += 2)
+                cr[8 * g + i / 2] = (uint8_t)(idx[i] | (idx[i + 1] << 4));
+        }
+    }
+    return ORC_OK;
+}
+
+/* n code rows -> float64 rows [n][d] in the original basis */
+static void turbo4_dequant(const uint8_t *codes, const uint8_t *scales, int64_t n, int d,
+                           const double *c, int mutate, double *out)
+{
+    const double sc = 1.0 / sqrt((double)d);
+    for (int64_t row = 0; row < n; ++row) {
+        const uint8_t *cr = codes + row * (d / 2), *sr = scales + row * (d / 16);
+        double *y = out + row * d;
+        for (int j = 0; j < d; ++j)
+            y[j] = orc_e4m3_to_double(sr[j / 16]) * c[(cr[j / 2] >> (4 * (j & 1))) & 15];
+        if (mutate == ORC_MUT_TURBO_NO_IWHT)
+            continue;
+        for (int h = 1; h < d; h <<= 1)
+            for (int i = 0; i < d; ++i)
+                if (!(i & h)) {
+                    const double a = y[i], b = y[i + h];
+                    y[i] = a + b;
+                    y[i + h] = a - b;
+                }
+        for (int j = 0; j < d; ++j)
+            y[j] *= sc;
+    }
+}
+
+int orc_turbo4_dequant_rows(const uint8_t *codes, const uint8_t *scales, int64_t n, int d,
+                            int mutate, double *out)
+{
+    if (d < 16 || d > 1024 || (d & (d - 1)) || n < 0)
+        return ORC_E_ARG;
+    double c[16];
+    orc_turbo4_codebook(c);
+    turbo4_dequant(codes, scales, n, d, c, mutate, out);
+    return ORC_OK;
+}
+
+/* sdpa_row over V rows given in float64 (a dequantized cache) */
+static void sdpa_row_vd(const double *q, const uint16_t *kc, int64_t tstride, const double *vd,
+                        int d, int last, double *o, double *scores)
+{
+    double scale = 1.0 / sqrt((double)d);
+    double mx = -INFINITY;
+    for (int t = 0; t <= last; ++t) {
+        const uint16_t *kt = kc + (int64_t)t * tstride;
+        double s = 0.0;
+        for (int j = 0; j < d; ++j)
+            s += q[j] * orc_bf16_to_double(kt[j]);
+        s *= scale;
+        scores[t] = s;
+        if (s > mx) mx = s;
+    }
+    double z = 0.0;
+    for (int t = 0; t <= last; ++t) {
+        scores[t] = exp(scores[t] - mx);
+        z += scores[t];
+    }
+    for (int j = 0; j < d; ++j)
+        o[j] = 0.0;
+    for (int t = 0; t <= last; ++t) {
+        const double p = scores[t] / z;
+        for (int j = 0; j < d; ++j)
+            o[j] += p * vd[(int64_t)t * d + j];
+    }
+}
+
 /*
  * One layer step for B sequences of R new rows each.
  *   x        [B][R][hidden]                     layer input (exact values)
@@ -393,11 +637,12 @@ int orc_sdpa(const double *q, const uint16_t *cache_k, const uint16_t *cache_v,
  * Returns ORC_OK, ORC_E_ARG for an inadmissible layer, ORC_E_RANGE when a
  * sequence would write past the capacity (nothing is written for it).
  */
-int orc_layer_step(const orc_layer *L, const orc_weights *W, const double *x,
-                   uint16_t *cache_k, uint16_t *cache_v, int capacity,
-                   const int32_t *cache_pos, int B, int R,
-                   double *out, double *tap_y, double *tap_attn)
+static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
+                      uint16_t *cache_k, uint16_t *cache_v, uint8_t *v_codes, uint8_t *v_scales,
+                      int capacity, const int32_t *cache_pos, int B, int R,
+                      double *out, double *tap_y, double *tap_attn)
 {
+    const int turbo = v_codes != NULL;
     const int Hd = L->hidden, H = L->num_heads, Hk = L->num_kv_heads, d = L->head_dim;
     if (Hd <= 0 || H <= 0 || Hk <= 0 || d <= 0 || H % Hk || B <= 0 || R <= 0)
         return ORC_E_ARG;
@@ -430,7 +675,18 @@ int orc_layer_step(const orc_layer *L, const orc_weights *W, const double *x,
     double *vnew = (double *)malloc((size_t)((int64_t)R * Hk * d) * sizeof(double));
     int32_t *cf = (int32_t *)malloc((size_t)H * sizeof(int32_t));
     int32_t *cl = (int32_t *)malloc((size_t)H * sizeof(int32_t));
-    if (!wrow || !y || !qn || !attn || !ga || !tmp || !nq || !nk || !scores || !knew || !vnew || !cf || !cl) {
+    double *vdq = NULL, cbk[16];
+    uint16_t *vb16 = (uint16_t *)malloc((size_t)d * sizeof(uint16_t));
+    if (turbo) {
+        if (d < 16 || d > 1024 || (d & (d - 1))) {
+            rc = ORC_E_ARG;
+            goto done;
+        }
+        orc_turbo4_codebook(cbk);
+        vdq = (double *)malloc((size_t)capacity * d * sizeof(double) + 8);
+    }
+    if (!wrow || !y || !qn || !attn || !ga || !tmp || !nq || !nk || !scores || !knew || !vnew || !cf ||
+        !cl || !vb16 || (turbo && !vdq)) {
         rc = ORC_E_ARG;
         goto done;
     }
@@ -457,7 +713,7 @@ int orc_layer_step(const orc_layer *L, const orc_weights *W, const double *x,
             memcpy(tap_y + (int64_t)b * R * Ny, y, (size_t)(R * Ny) * sizeof(double));
 
         uint16_t *kcb = cache_k + (int64_t)b * Hk * capacity * d;
-        uint16_t *vcb = cache_v + (int64_t)b * Hk * capacity * d;
+        uint16_t *vcb = turbo ? NULL : cache_v + (int64_t)b * Hk * capacity * d;
         for (int r = 0; r < R; ++r) {
             const double *yr = y + (int64_t)r * Ny;
             double pos = (double)(p0 + r);
@@ -485,16 +741,42 @@ int orc_layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                 rope_partial(kr, d, rd, pos, L->rope_theta, L->mutate);
                 memcpy(vr, vsrc, (size_t)d * sizeof(double));
                 uint16_t *kdst = kcb + ((int64_t)kh * capacity + p0 + r) * d;
-                uint16_t *vdst = vcb + ((int64_t)kh * capacity + p0 + r) * d;
                 for (int j = 0; j < d; ++j) {
                     kdst[j] = orc_bf16_from_double(kr[j]);
-                    vdst[j] = orc_bf16_from_double(vr[j]);
+                    vb16[j] = orc_bf16_from_double(vr[j]);
+                }
+                if (turbo) {
+                    const int64_t row = ((int64_t)b * Hk + kh) * capacity + p0 + r;
+                    orc_turbo4_quantize_rows(vb16, 1, d, v_codes + row * (d / 2),
+                                             v_scales + row * (d / 16));
+                } else {
+                    memcpy(vcb + ((int64_t)kh * capacity + p0 + r) * d, vb16,
+                           (size_t)d * sizeof(uint16_t));
+                }
+            }
+        }
+        /* Turbo4 V: per KV head, dequantize its rows [0, p0 + R) back to the
+         * original basis, then attend them as float64 rows */
+        if (turbo) {
+            for (int kh = 0; kh < Hk; ++kh) {
+                const int64_t row0 = ((int64_t)b * Hk + kh) * capacity;
+                turbo4_dequant(v_codes + row0 * (d / 2), v_scales + row0 * (d / 16), p0 + R, d, cbk,
+                               L->mutate, vdq);
+                for (int h = 0; h < H; ++h) {
+                    const int khh = (L->mutate == ORC_MUT_GQA_MODULO) ? h % Hk : h / gqa;
+                    if (khh != kh)
+                        continue;
+                    for (int r = 0; r < R; ++r) {
+                        const int last = (L->mutate == ORC_MUT_NO_CAUSAL) ? p0 + R - 1 : p0 + r;
+                        sdpa_row_vd(qn + ((int64_t)r * H + h) * d, kcb + (int64_t)kh * capacity * d,
+                                    d, vdq, d, last, attn + ((int64_t)r * H + h) * d, scores);
+                    }
                 }
             }
         }
         /* attention, chunk by chunk along the head plan (one chunk per KV
          * group when the route is off or ineligible) */
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = 0; c < (turbo ? 0 : nchunks); ++c) {
             for (int h = cf[c]; h < cf[c] + cl[c]; ++h) {
                 int kh = (L->mutate == ORC_MUT_GQA_MODULO) ? h % Hk : h / gqa;
                 const uint16_t *kc = kcb + (int64_t)kh * capacity * d;
@@ -552,8 +834,32 @@ int orc_layer_step(const orc_layer *L, const orc_weights *W, const double *x,
     }
 done:
     free(wrow); free(y); free(qn); free(attn); free(ga); free(tmp); free(nq); free(nk);
-    free(scores); free(knew); free(vnew); free(cf); free(cl);
+    free(scores); free(knew); free(vnew); free(cf); free(cl); free(vdq); free(vb16);
     return rc;
+}
+
+int orc_layer_step(const orc_layer *L, const orc_weights *W, const double *x,
+                   uint16_t *cache_k, uint16_t *cache_v, int capacity,
+                   const int32_t *cache_pos, int B, int R,
+                   double *out, double *tap_y, double *tap_attn)
+{
+    return layer_step(L, W, x, cache_k, cache_v, NULL, NULL, capacity, cache_pos, B, R, out, tap_y,
+                      tap_attn);
+}
+
+/* The layer step over a Bf16KTurbo4V cache: K as in orc_layer_step, V as
+ * code rows [B][Hk][capacity][d/2] and scale rows [B][Hk][capacity][d/16]
+ * (Turbo4 V cache above); the new V rows are quantized from their bf16
+ * values, attention reads every V row dequantized. */
+int orc_layer_step_turbo4v(const orc_layer *L, const orc_weights *W, const double *x,
+                           uint16_t *cache_k, uint8_t *v_codes, uint8_t *v_scales, int capacity,
+                           const int32_t *cache_pos, int B, int R,
+                           double *out, double *tap_y, double *tap_attn)
+{
+    if (!v_codes || !v_scales)
+        return ORC_E_ARG;
+    return layer_step(L, W, x, cache_k, NULL, v_codes, v_scales, capacity, cache_pos, B, R, out,
+                      tap_y, tap_attn);
 }
 
 /* ------------------------------------------------------ decoder block */

@@ -25,7 +25,7 @@ from dataclasses import dataclass, replace
 import numpy as np
 
 # substream ids
-_X, _WQ, _WK, _WV, _WO, _QN, _KN, _CK, _CV, _LEN, _IN_LN, _POST_LN = range(1, 13)
+_X, _WQ, _WK, _WV, _WO, _QN, _KN, _CK, _CV, _LEN, _IN_LN, _POST_LN, _VQC, _VQS = range(1, 15)
 
 
 @dataclass(frozen=True)
@@ -196,3 +196,31 @@ def cache(spec: LayerSpec, capacity: int | None = None, fill: int = 0, batches=N
         ks.append(k)
         vs.append(v)
     return np.stack(ks), np.stack(vs)
+
+
+def turbo4v_cache(spec: LayerSpec, capacity: int | None = None, stale_code: int = 0xFF,
+                  stale_scale: int = 0x7F, batches=None):
+    """Prior Bf16KTurbo4V V planes for the sequences in ``batches``: codes
+    [B'][Hk][cap][d/2] uint8 (uniform random nibbles) and E4M3 scales
+    [B'][Hk][cap][d/16] uint8, uniform over the bytes 0x30..0x3F (0.5 to
+    1.875, the scale of a unit-variance group) for positions < cache_pos;
+    every later slot holds ``stale_code`` / ``stale_scale`` (0x7F is an E4M3
+    NaN, so a kernel that reads a stale slot shows it).  Random bytes only:
+    no quantizer arithmetic here."""
+    cap = capacity or spec.capacity()
+    pos = spec.positions()
+    Hk, d = spec.num_kv_heads, spec.head_dim
+    idx = range(spec.batch) if batches is None else list(batches)
+    cs, ss = [], []
+    for b in idx:
+        p = int(pos[b])
+        c = np.full((Hk, cap, d // 2), stale_code, np.uint8)
+        sc = np.full((Hk, cap, d // 16), stale_scale, np.uint8)
+        for kh in range(Hk):
+            rng = np.random.default_rng([spec.seed, _VQC, b, kh])
+            c[kh, :p] = rng.integers(0, 256, size=(p, d // 2), dtype=np.uint8)
+            rng = np.random.default_rng([spec.seed, _VQS, b, kh])
+            sc[kh, :p] = rng.integers(0x30, 0x40, size=(p, d // 16), dtype=np.uint8)
+        cs.append(c)
+        ss.append(sc)
+    return np.stack(cs), np.stack(ss)
