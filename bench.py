@@ -39,12 +39,13 @@ METRIC = "gated-attn layer steps/s & tokens/s; achieved HBM GB/s vs GB300 peak"
 UNIT = "layer-steps/s"
 
 
-def algorithmic_bytes(spec, block=False):
+def algorithmic_bytes(spec, block=False, kv="bf16"):
     """Per-step and per-kernel algorithmic bytes (packed weights + bf16
     scales/biases, KV read over every attended position, KV rows written, x,
     out and the small intermediates each kernel must move).  block: the
     decoder-block step, which adds the two norm weight vectors and the
-    post-norm output to the step (x is still read once)."""
+    post-norm output to the step (x is still read once).  kv="turbo4v": V rows
+    are d/2 code bytes + d/16 E4M3 scale bytes instead of 2d."""
     H, Hk, d, Hd, B, R = (spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.hidden,
                           spec.batch, spec.q_len)
     M = B * R
@@ -57,8 +58,9 @@ def algorithmic_bytes(spec, block=False):
     wv = wbytes(spec.n_kv, Hd, spec.bits[2], spec.group[2])
     wo = wbytes(Hd, H * d, spec.bits[3], spec.group[3])
     pos = spec.positions().astype(np.int64)
-    kv_read = int(((pos + R) * Hk * d * 2 * 2).sum())
-    kv_write = M * Hk * d * 2 * 2
+    row_kv = d * 2 + (d // 2 + d // 16 if kv == "turbo4v" else d * 2)   # K + V bytes per row
+    kv_read = int(((pos + R) * Hk * row_kv).sum())
+    kv_write = M * Hk * row_kv
     xb = M * Hd * (4 if spec.x_dtype == "f32" else 2)
     outb = M * Hd * 2
     x16 = M * Hd * 2
@@ -169,7 +171,7 @@ class ClockSampler:
 
 # ----------------------------------------------------------- cpu baseline
 
-def oracle_sample(spec, budget_s=15.0, max_steps=64, block=False):
+def oracle_sample(spec, budget_s=15.0, max_steps=64, block=False, kv="bf16"):
     """Time the oracle as it stands on a bounded sample of the workload: whole
     layer (or decoder-block) steps of the same shapes, one core."""
     import oracle as orc
@@ -181,6 +183,7 @@ def oracle_sample(spec, budget_s=15.0, max_steps=64, block=False):
                           qn, kn, list(spec.bits), list(spec.group))
     cap = spec.capacity()
     ck, cv = synth.cache(spec, cap)
+    vq = synth.turbo4v_cache(spec, cap) if kv == "turbo4v" else None
     x = synth.x_values(spec, synth.layer_input(spec))
     pos = spec.positions()
     il, pl = synth.block_norm_weights_bf16(spec)
@@ -189,7 +192,9 @@ def oracle_sample(spec, budget_s=15.0, max_steps=64, block=False):
     while steps < max_steps:
         k2, v2 = ck.copy(), cv.copy()
         ts = time.perf_counter()
-        if block:
+        if kv == "turbo4v":
+            orc.layer_step_turbo4v(spec, W, x, k2, vq[0].copy(), vq[1].copy(), pos)
+        elif block:
             orc.block_step(spec, W, x, il, pl, k2, v2, pos)
         else:
             orc.layer_step(spec, W, x, k2, v2, pos)
@@ -206,7 +211,8 @@ def reference_arm(args, spec):
         return
     K, W = args.steps, max(args.warmup, 0)
     budget = min(120.0, max(10.0, 2.0 * (K + W)))
-    rate, n, el = oracle_sample(spec, budget_s=budget, max_steps=max(1, K + W), block=args.block)
+    rate, n, el = oracle_sample(spec, budget_s=budget, max_steps=max(1, K + W), block=args.block,
+                                kv=args.kv)
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT,
         "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": 1000.0 / rate,
@@ -232,7 +238,9 @@ def config_dict(spec, args, extra=None):
          "q_len": spec.q_len, "cache_len": int(spec.positions().max()) + spec.q_len,
          "head_chunk": not args.no_head_chunk, "parallelism": f"replicas x{args.gpus}",
          "step": "decoder block (input RMSNorm, layer, residual, post-norm)" if args.block
-         else "attention layer"}
+         else "attention layer",
+         "kv_cache": "bf16 K, Turbo4 V (WHT basis, 4-bit Lloyd-Max codes, E4M3 group-16 scales)"
+         if args.kv == "turbo4v" else "bf16 K and V"}
     if extra:
         d.update(extra)
     return d
@@ -274,7 +282,7 @@ def our_arm(args, spec):
     # CPU baseline first (rank 0, N = 1): the oracle as it stands, before any GPU work
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, n, el = oracle_sample(spec, budget_s=args.cpu_budget, block=args.block)
+        rate, n, el = oracle_sample(spec, budget_s=args.cpu_budget, block=args.block, kv=args.kv)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n} whole {unit_name(args)} steps of {spec.name} ({el:.1f} s, one core)"}
 
@@ -288,7 +296,7 @@ def our_arm(args, spec):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
 
-    step_bytes, kernel_bytes = algorithmic_bytes(spec, args.block)
+    step_bytes, kernel_bytes = algorithmic_bytes(spec, args.block, args.kv)
     inst_bytes = step_bytes
     n_inst = max(2, math.ceil(4 * l2 / inst_bytes))
     if args.instances:
@@ -301,17 +309,19 @@ def our_arm(args, spec):
     qn, kn = synth.norm_weights_bf16(spec)
     cap = spec.capacity()
     ck, cv = synth.cache(spec, cap)
+    vq = synth.turbo4v_cache(spec, cap) if args.kv == "turbo4v" else None
     pos = spec.positions()
     x = synth.layer_input(spec)
     layers = []
     for _ in range(n_inst):
         dl = DeviceLayer(spec, packed, qn, kn, cap, head_chunk=not args.no_head_chunk,
                          device=dev, path={"auto": gattn.PATH_AUTO, "fused": gattn.PATH_FUSED,
-                                           "split": gattn.PATH_SPLIT}[args.path])
+                                           "split": gattn.PATH_SPLIT}[args.path],
+                         kv_format=args.kv)
         dl._w = None          # interchange copies are no longer needed after repacking
-        dl.load_cache(ck, cv)
+        dl.load_cache(ck, vq if args.kv == "turbo4v" else cv)
         layers.append(dl)
-    del ck, cv
+    del ck, cv, vq
     xd = x_to_device(spec, x, dev)
     pd = torch.from_numpy(pos).to(dev)
     outs = [torch.empty((spec.batch, spec.q_len, spec.hidden), dtype=torch.bfloat16, device=dev)
@@ -500,6 +510,8 @@ def main():
     ap.add_argument("--no-head-chunk", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "fused", "split"],
                     help="one-kernel or five-kernel step (auto: one kernel when it fits)")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "turbo4v"],
+                    help="KV cache format: bf16, or bf16 K with a Turbo4 V cache")
     ap.add_argument("--block", action="store_true",
                     help="time the decoder-block step (input RMSNorm + layer + residual + "
                          "post-attention RMSNorm) instead of the layer alone")

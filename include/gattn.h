@@ -162,6 +162,63 @@ gattn_status gattn_layer_set_weights(gattn_layer *layer, const gattn_weights *w,
 gattn_status gattn_kv_register(gattn_layer *layer, const gattn_kv_desc *desc, gattn_kv **out);
 
 /*
+ * A caller-owned Bf16KTurbo4V cache (device): the "safer-asym" format of the
+ * Atlas qwen3_5 forward page (MetalKvDtype::Bf16KTurbo4V, LayerKvCache with a
+ * V-side scale buffer): K raw bf16, V in a Walsh-Hadamard-rotated basis as
+ * 4-bit Lloyd-Max codebook indices plus one FP8 E4M3 scale per group of 16.
+ *   K       bf16, element (b, kv_head, token, j) at
+ *           k + b*k_stride_batch + kv_head*k_stride_head + token*k_stride_token + j
+ *           (strides in elements, multiples of 8)
+ *   v_codes uint8, the row of (b, kv_head, token) -- d/2 bytes, code j in the
+ *           low (j even) or high (j odd) nibble of byte j/2 -- at
+ *           v_codes + b*code_stride_batch + kv_head*code_stride_head + token*(d/2)
+ *   v_scales uint8 E4M3, d/16 bytes per row, at
+ *           v_scales + b*scale_stride_batch + kv_head*scale_stride_head + token*(d/16)
+ * Code and scale strides are in bytes, multiples of 16; rows of one
+ * (b, kv_head) are consecutive.  Pointers 16-byte aligned; capacity a
+ * multiple of 16; head_dim a power of two from 64 to 256.  A V row is
+ * dequantized as H (s * c(code)) / sqrt(d) (H the Sylvester Hadamard matrix,
+ * c the levels of gattn_turbo4_codebook); the step quantizes its new V rows
+ * from their bf16 values (gattn_turbo4_quantize_device states how) and
+ * applies the inverse rotation once to each attention output row.
+ */
+typedef struct gattn_kv_turbo4v_desc {
+    void *k;
+    void *v_codes;
+    void *v_scales;
+    int32_t batch;
+    int32_t capacity;
+    int64_t k_stride_token, k_stride_head, k_stride_batch;
+    int64_t code_stride_head, code_stride_batch;
+    int64_t scale_stride_head, scale_stride_batch;
+} gattn_kv_turbo4v_desc;
+
+/* Register a Bf16KTurbo4V cache (as gattn_kv_register).  GATTN_E_INVALID_ARG
+ * for a bad pointer, stride, capacity or head_dim.  Steps on such a cache run
+ * on the five-kernel path; GATTN_PATH_FUSED refuses them (GATTN_E_UNSUPPORTED). */
+gattn_status gattn_kv_register_turbo4v(gattn_layer *layer, const gattn_kv_turbo4v_desc *desc,
+                                       gattn_kv **out);
+
+/* The Turbo4 codebook as the kernels use it (host, no GPU): the 16 levels of
+ * the Lloyd-Max quantizer of N(0, 1), ascending, rounded to fp32, and the 15
+ * decision thresholds between them (midpoints taken in double, then rounded;
+ * the middle one is 0).  Computed once per process by Lloyd's iteration. */
+gattn_status gattn_turbo4_codebook(float levels[16], float thresholds[15]);
+
+/*
+ * Quantize `rows` bf16 rows of `d` values (device, [rows][d]) into Turbo4
+ * codes (device, [rows][d/2]) and E4M3 scales (device, [rows][d/16]), as the
+ * step does for its new V rows; enqueued on `stream`, no synchronization.
+ * Per row: y = H v * fp32(1/sqrt(d)) (butterfly stages h = 1, 2, 4, ... in
+ * fp32); per group of 16: ss = pairwise fp32 sum of y_i^2, u_i = y_i /
+ * sqrt(ss/16), code_i = number of thresholds below u_i, scale = E4M3 (nearest,
+ * ties to even, saturating at 448) of sqrt(ss / pairwise sum of level^2); a
+ * zero group gets codes 0 and scale 0.  d a power of two from 64 to 256.
+ */
+gattn_status gattn_turbo4_quantize_device(const void *v_bf16, int64_t rows, int32_t d,
+                                          void *codes, void *scales, gattn_stream stream);
+
+/*
  * One layer step, enqueued on `stream` with no host synchronization and no
  * allocation (capturable into a CUDA graph).
  *   x          (device) [batch][q_len][hidden], cfg.x_dtype

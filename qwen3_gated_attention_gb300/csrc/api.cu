@@ -185,6 +185,10 @@ struct gattn_layer {
     unsigned *sync = nullptr;
     float *ss_part = nullptr;              // decoder-block post-norm: per-CTA sums of squares
     unsigned *post_ticket = nullptr;
+    // Bf16KTurbo4V caches: decision tables (host copy, passed by value) and the
+    // byte -> fp16 level pair table the attention dequantizes with
+    TurboTables tq{};
+    uint32_t *tq_lut = nullptr;
     int s_cnt_a = 0, s_rdy_a = 0, s_seg = 0, s_cnt_o = 0, nsync = 0;
     gattn_taps taps{};
     bool weights_set = false;
@@ -195,7 +199,9 @@ struct gattn_layer {
 
 struct gattn_kv {
     gattn_layer *layer = nullptr;
-    gattn_kv_desc desc{};
+    gattn_kv_desc desc{};          // K (and V for a bf16 cache); v is NULL for Turbo4 V
+    bool turbo = false;            // Bf16KTurbo4V: V as codes + E4M3 scales
+    gattn_kv_turbo4v_desc tdesc{};
     CUtensorMap kmap;   // CUtensorMap is itself 64-byte aligned
     CUtensorMap vmap;
 };
@@ -374,6 +380,23 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaMalloc(&L->status, sizeof(unsigned)));
     TRY(cudaMemset(L->status, 0, sizeof(unsigned)));
     {
+        float lv[16], th[15];
+        gattn_turbo4_codebook(lv, th);
+        std::memcpy(L->tq.lv, lv, sizeof lv);
+        std::memcpy(L->tq.th, th, sizeof th);
+        L->tq.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.head_dim));
+        uint32_t lut[256];
+        for (int b = 0; b < 256; ++b) {
+            const __half lo = __float2half_rn(lv[b & 15]), hi = __float2half_rn(lv[b >> 4]);
+            uint16_t l16, h16;
+            std::memcpy(&l16, &lo, 2);
+            std::memcpy(&h16, &hi, 2);
+            lut[b] = (uint32_t)l16 | ((uint32_t)h16 << 16);
+        }
+        TRY(cudaMalloc(&L->tq_lut, sizeof lut));
+        TRY(cudaMemcpy(L->tq_lut, lut, sizeof lut, cudaMemcpyHostToDevice));
+    }
+    {
         const int gmax = *std::max_element(L->po.grid, L->po.grid + 3);
         TRY(cudaMalloc(&L->ss_part, (size_t)gmax * L->M_max * sizeof(float)));
         TRY(cudaMalloc(&L->post_ticket, sizeof(unsigned)));
@@ -424,7 +447,7 @@ void gattn_layer_destroy(gattn_layer *L)
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq,
                     L->q_norm, L->k_norm, L->part_a,  L->part_o,  L->sync,
-                    L->ss_part, L->post_ticket};
+                    L->ss_part, L->post_ticket, L->tq_lut};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -512,6 +535,68 @@ gattn_status gattn_kv_register(gattn_layer *L, const gattn_kv_desc *d, gattn_kv 
         }
     }
     *out = kv;
+    return GATTN_OK;
+}
+
+gattn_status gattn_kv_register_turbo4v(gattn_layer *L, const gattn_kv_turbo4v_desc *d,
+                                       gattn_kv **out)
+{
+    if (!L || !d || !out)
+        return fail(GATTN_E_INVALID_ARG, "NULL argument");
+    *out = nullptr;
+    const int hd = L->cfg.head_dim;
+    if (hd != 64 && hd != 128 && hd != 256)
+        return fail(GATTN_E_INVALID_ARG, "a Turbo4 V cache needs head_dim 64, 128 or 256 (got %d)",
+                    hd);
+    if (!d->v_codes || !d->v_scales)
+        return fail(GATTN_E_INVALID_ARG, "V code or scale pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(d->v_codes) | reinterpret_cast<uintptr_t>(d->v_scales)) & 15)
+        return fail(GATTN_E_INVALID_ARG, "V code and scale pointers must be 16-byte aligned");
+    if (d->capacity % 16)
+        return fail(GATTN_E_INVALID_ARG, "a Turbo4 V cache needs capacity %% 16 == 0 (got %d)",
+                    (int)d->capacity);
+    const long long cap = d->capacity;
+    if (d->code_stride_head <= 0 || d->code_stride_batch <= 0 || d->scale_stride_head <= 0 ||
+        d->scale_stride_batch <= 0 ||
+        (d->code_stride_head | d->code_stride_batch | d->scale_stride_head | d->scale_stride_batch) & 15)
+        return fail(GATTN_E_INVALID_ARG, "code and scale strides must be positive multiples of 16 bytes");
+    if (d->code_stride_head < cap * (hd / 2) || d->scale_stride_head < cap * (hd / 16))
+        return fail(GATTN_E_INVALID_ARG, "a head's code or scale rows overlap the next head's");
+    gattn_kv_desc kd{};
+    kd.k = d->k;
+    kd.v = d->k;                // checked like a bf16 V pointer, never read as V
+    kd.batch = d->batch;
+    kd.capacity = d->capacity;
+    kd.stride_token = d->k_stride_token;
+    kd.stride_head = d->k_stride_head;
+    kd.stride_batch = d->k_stride_batch;
+    gattn_kv *kv = nullptr;
+    const gattn_status st = gattn_kv_register(L, &kd, &kv);
+    if (st != GATTN_OK)
+        return st;
+    kv->desc.v = nullptr;
+    kv->turbo = true;
+    kv->tdesc = *d;
+    *out = kv;
+    return GATTN_OK;
+}
+
+gattn_status gattn_turbo4_quantize_device(const void *v, int64_t rows, int32_t d, void *codes,
+                                          void *scales, gattn_stream stream)
+{
+    if (rows < 0 || (rows > 0 && (!v || !codes || !scales)))
+        return fail(GATTN_E_INVALID_ARG, "bad rows or NULL pointer");
+    if (d != 64 && d != 128 && d != 256)
+        return fail(GATTN_E_INVALID_ARG, "d must be 64, 128 or 256 (got %d)", (int)d);
+    TurboTables t{};
+    float lv[16], th[15];
+    gattn_turbo4_codebook(lv, th);
+    std::memcpy(t.lv, lv, sizeof lv);
+    std::memcpy(t.th, th, sizeof th);
+    t.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
+    CUDA_TRY(launch_turbo4_quantize(static_cast<const uint16_t *>(v), rows, d,
+                                    static_cast<uint8_t *>(codes), static_cast<uint8_t *>(scales), t,
+                                    reinterpret_cast<cudaStream_t>(stream)));
     return GATTN_OK;
 }
 
@@ -620,6 +705,8 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     // the one-kernel path runs the layer alone (no decoder-block steps)
     if (L->path == GATTN_PATH_FUSED && blk)
         return fail(GATTN_E_UNSUPPORTED, "the one-kernel path runs no decoder-block steps");
+    if (L->path == GATTN_PATH_FUSED && kv->turbo)
+        return fail(GATTN_E_UNSUPPORTED, "the one-kernel path reads bf16 V caches only");
     if (L->path == GATTN_PATH_FUSED) {
         // x arrives by bulk copy: 16-byte alignment
         bool ok = L->fused_ok && Ma <= 8 && batch <= kFMaxB && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
@@ -767,6 +854,15 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     eq.qn = L->qn;
     eq.gate = L->gate;
     eq.tap_y = L->taps.y;
+    if (kv->turbo) {
+        eq.vq_codes = static_cast<uint8_t *>(kv->tdesc.v_codes);
+        eq.vq_scales = static_cast<uint8_t *>(kv->tdesc.v_scales);
+        eq.cq_head = kv->tdesc.code_stride_head;
+        eq.cq_batch = kv->tdesc.code_stride_batch;
+        eq.sq_head = kv->tdesc.scale_stride_head;
+        eq.sq_batch = kv->tdesc.scale_stride_batch;
+        eq.tq = L->tq;
+    }
     EpiO eo{};
     CUDA_TRY(mark(1));
     CUDA_TRY(launch_proj(L->pqkv.bits, NTa, kModeQKV, a, eq, eo, L->pqkv.grid[nia], pdl, s));
@@ -793,8 +889,22 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     t.group_o = L->po.group;
     t.tap_attn = L->taps.attn;
     t.status = L->status;
+    if (kv->turbo) {
+        t.vq = 1;
+        t.vq_codes = static_cast<const uint8_t *>(kv->tdesc.v_codes);
+        t.vq_scales = static_cast<const uint8_t *>(kv->tdesc.v_scales);
+        t.cq_head = kv->tdesc.code_stride_head;
+        t.cq_batch = kv->tdesc.code_stride_batch;
+        t.sq_head = kv->tdesc.scale_stride_head;
+        t.sq_batch = kv->tdesc.scale_stride_batch;
+        t.vq_lut = L->tq_lut;
+        t.inv_sqrt_d = L->tq.inv_sqrt_d;
+    }
     CUDA_TRY(mark(2));
-    CUDA_TRY(launch_attn(MT, c.head_dim / 64, t, kv->kmap, kv->vmap, L->attn_grid, pdl, s));
+    if (kv->turbo)
+        CUDA_TRY(launch_attn_vq(MT, c.head_dim / 64, t, kv->kmap, L->attn_grid, pdl, s));
+    else
+        CUDA_TRY(launch_attn(MT, c.head_dim / 64, t, kv->kmap, kv->vmap, L->attn_grid, pdl, s));
     ++launches;
     CUDA_TRY(mark(3));
     CUDA_TRY(launch_attn_merge(t, max_rows, pdl, s));

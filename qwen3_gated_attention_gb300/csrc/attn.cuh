@@ -1,0 +1,514 @@
+// attn.cuh -- the attention kernel template, instantiated for bf16 V caches
+// in attn.cu and for Bf16KTurbo4V caches in attn_vq.cu.
+#pragma once
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace gattn {
+
+// bytes of one 64-wide head_dim box of a tile (kAttnTile tokens x 128 bytes);
+// a multiple of 1024 so every box starts on a 128-byte-swizzle atom
+constexpr int kDBox = kAttnTile * 128;
+static_assert(kDBox % 1024 == 0, "tile boxes must stay swizzle-atom aligned");
+
+template <int MT, int DB, int VQ>
+struct AttnSmem {
+    static constexpr int kTileBytes = DB * kDBox;             // kAttnTile tokens x d bf16
+    // V of a stage: the bf16 tile, or (Turbo4) the tile's code rows (d/2 bytes
+    // per token) followed by its scale rows (d/16 bytes per token)
+    static constexpr int kVCodeBytes = kAttnTile * DB * 32;
+    static constexpr int kVBytes =
+        VQ ? ((kVCodeBytes + kAttnTile * DB * 4 + 1023) & ~1023) : kTileBytes;
+    static constexpr int kStageBytes = kTileBytes + kVBytes;  // K + V
+    static constexpr int kDqBytes = VQ ? kTileBytes : 0;      // Turbo4: dequantized fp16 V tile
+    static constexpr int kLutBytes = VQ ? 1024 : 0;           // Turbo4: byte -> level pair
+    static constexpr int kQBytes = MT * 16 * DB * 64 * 2;
+    static constexpr int kPBytes = MT * 16 * 128;             // rows x 64 tokens bf16
+    // as many K/V stages (2 .. kAttnStages) as fit beside the rest in 227 KB
+    static constexpr int kFixed = kDqBytes + kLutBytes + kQBytes + kPBytes +
+                                  2 * kAttnWarps * 64 * 4 + 40 * 8 + 2 * kAttnStages * 8 + 256 + 1024;
+    static constexpr int kFit = (227 * 1024 - kFixed) / kStageBytes;
+    static constexpr int kNStages = kFit < 2 ? 2 : (kFit > kAttnStages ? kAttnStages : kFit);
+    static constexpr int kStages = kNStages * kStageBytes;
+    static constexpr int kDq = kStages;
+    static constexpr int kLut = kDq + kDqBytes;
+    static constexpr int kQ = kLut + kLutBytes;
+    static constexpr int kP = kQ + kQBytes;
+    static constexpr int kRedMax = kP + kPBytes;              // [8][64] floats
+    static constexpr int kRedL = kRedMax + kAttnWarps * 64 * 4;
+    static constexpr int kPrefix = kRedL + kAttnWarps * 64 * 4;   // [33] long long
+    static constexpr int kBars = kPrefix + 40 * 8;
+    static constexpr int kFlags = kBars + 2 * kNStages * 8;
+    static constexpr int kTotal = kFlags + 256 + 1024;        // + alignment slack
+    static_assert(kTotal <= 227 * 1024, "attention shared memory exceeds 227 KB");
+};
+
+template <int MT, int DB, int VQ>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap vmap)
+{
+    using L = AttnSmem<MT, DB, VQ>;
+    constexpr int D = DB * 64;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *qs = smem + L::kQ;
+    uint8_t *dq = smem + L::kDq;                                // Turbo4 only
+    uint32_t *lut = reinterpret_cast<uint32_t *>(smem + L::kLut);
+    uint8_t *ps = smem + L::kP;
+    float *red_max = reinterpret_cast<float *>(smem + L::kRedMax);
+    float *red_l = reinterpret_cast<float *>(smem + L::kRedL);
+    long long *prefix = reinterpret_cast<long long *>(smem + L::kPrefix);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBars);
+    uint64_t *empty = full + L::kNStages;
+    int *flags = reinterpret_cast<int *>(smem + L::kFlags);   // [0] abort [1] last [2..] ub
+    int *ub = flags + 4;                                        // units per segment of b [32]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gqa = a.H / a.Hk;
+
+    // Dependents (the merge) may launch at once.  Before waiting for the q|k|v
+    // projection this kernel only reads cache_pos and cache rows older than the
+    // step: the projection starts its dependents after its own wait, so every
+    // earlier kernel (which wrote those rows) has completed by then.
+    pdl_launch_dependents();
+
+    if (tid == 0) {
+        for (int i = 0; i < L::kNStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kAttnWarps);
+        }
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    if (tid < a.B) {
+        const int p0 = a.cache_pos[tid];
+        const bool valid = p0 >= 0 && p0 + a.R <= a.cap;
+        ub[tid] = valid ? (p0 + a.R + kAttnUnit - 1) / kAttnUnit : 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        long long acc = 0;
+        for (int b = 0; b < a.B; ++b) {
+            prefix[b] = acc;
+            acc += (long long)ub[b] * a.Hk * a.nrb;
+        }
+        prefix[a.B] = acc;
+    }
+    __syncthreads();
+
+    // Ranges are cut over attn_ranges(T) CTAs, each owning at least min_units
+    // units (the merge kernel counts contributors by range); the remaining CTAs
+    // have nothing to do.
+    const long long T = prefix[a.B], c = blockIdx.x;
+    const long long G = attn_ranges(T, gridDim.x, a.min_units);
+    const long long beg = c < G ? sk_start(c, T, G) : T, end = c < G ? sk_start(c + 1, T, G) : T;
+    volatile int *abort = flags;
+
+    if (warp == kAttnWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && beg < end) {
+            prefetch_tensormap(&kmap);
+            if constexpr (!VQ)
+                prefetch_tensormap(&vmap);
+            const uint64_t pol = l2_evict_first_policy();
+            long long it = 0;
+            bool stop = false, waited = false;
+            for (long long pos = beg; pos < end && !stop;) {
+                const Piece p = find_piece(prefix, ub, a.B, a.Hk, a.nrb, pos, end);
+                const int p0 = a.cache_pos[p.b];
+                for (int u = p.u0; u < p.u1; u += kAttnTile / kAttnUnit, ++it) {
+                    const int nun = min(kAttnTile / kAttnUnit, p.u1 - u);
+                    // tiles that hold this step's new rows load after the projection
+                    if (!waited && (it >= L::kNStages || (u + nun) * kAttnUnit > p0)) {
+                        pdl_wait();
+                        waited = true;
+                    }
+                    const int slot = (int)(it % L::kNStages);
+                    const uint32_t ph = (uint32_t)((it / L::kNStages) & 1);
+                    if (!mbar_wait(&empty[slot], ph ^ 1u, abort, a.status)) {
+                        stop = true;
+                        break;
+                    }
+                    uint8_t *kst = smem + slot * L::kStageBytes;
+                    uint8_t *vst = kst + L::kTileBytes;
+                    // Turbo4 V: the tile's code and scale rows are contiguous (the
+                    // capacity is a multiple of the 16-token unit, so they end in range)
+                    const uint32_t vq_code = VQ ? (uint32_t)(nun * kAttnUnit * DB * 32) : 0u;
+                    const uint32_t vq_scale = VQ ? (uint32_t)(nun * kAttnUnit * DB * 4) : 0u;
+                    mbar_arrive_expect_tx(&full[slot], VQ ? (uint32_t)(nun * DB * 2048) + vq_code +
+                                                                vq_scale
+                                                          : (uint32_t)(nun * DB * 2048 * 2));
+                    for (int ui = 0; ui < nun; ++ui) {
+                        const int t = (u + ui) * kAttnUnit;
+#pragma unroll
+                        for (int db = 0; db < DB; ++db) {
+                            tensor4d_g2s(kst + db * kDBox + ui * 2048, &kmap, db * 64, t, p.kh, p.b,
+                                         &full[slot], pol);
+                            if constexpr (!VQ)
+                                tensor4d_g2s(vst + db * kDBox + ui * 2048, &vmap, db * 64, t, p.kh,
+                                             p.b, &full[slot], pol);
+                        }
+                    }
+                    if constexpr (VQ) {
+                        const long long t = (long long)u * kAttnUnit;
+                        bulk_g2s(vst, a.vq_codes + p.b * a.cq_batch + p.kh * a.cq_head + t * (DB * 32),
+                                 vq_code, &full[slot], pol);
+                        bulk_g2s(vst + L::kVCodeBytes,
+                                 a.vq_scales + p.b * a.sq_batch + p.kh * a.sq_head + t * (DB * 4),
+                                 vq_scale, &full[slot], pol);
+                    }
+                }
+                pos = p.seg_start + p.u1;
+            }
+            if (!waited)
+                pdl_wait();
+            const long long first = it > L::kNStages ? it - L::kNStages : 0;
+            for (long long i = first; i < it; ++i) {
+                unsigned long long t0 = global_ns();
+                while (!mbar_try(&full[i % L::kNStages], (uint32_t)((i / L::kNStages) & 1)) &&
+                       global_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+        return;
+    }
+
+    // --------------------------------------------------------------- consumers
+    if constexpr (VQ) {
+        for (int i = tid; i < 256; i += kAttnWarps * 32)
+            lut[i] = a.vq_lut[i];   // a layer constant; read by all after the first barrier
+    }
+    pdl_wait();                 // q rows come from the q|k|v projection
+    const int g = lane >> 2, cq = lane & 3;
+    long long it = 0;
+    for (long long pos = beg; pos < end;) {
+        const Piece p = find_piece(prefix, ub, a.B, a.Hk, a.nrb, pos, end);
+        const int nh = a.rb_nh[p.rb];
+        const int h0 = p.kh * gqa + a.rb_h0[p.rb];
+        const int nrows = nh * a.R;
+        const int p0 = a.cache_pos[p.b];
+        const int Lb = p0 + a.R;
+
+        // ---- q rows of this segment into shared memory (swizzled 16-byte chunks)
+        constexpr int CH = D / 8;   // chunks per row
+        for (int idx = tid; idx < MT * 16 * CH; idx += kAttnWarps * 32) {
+            const int i = idx / CH, cc = idx % CH;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (i < nrows) {
+                const int hl = i / a.R, r = i % a.R;
+                const __nv_bfloat16 *src =
+                    a.qn + (((long long)p.b * a.R + r) * a.H + h0 + hl) * D + cc * 8;
+                v = *reinterpret_cast<const uint4 *>(src);
+            }
+            *reinterpret_cast<uint4 *>(qs + i * (D * 2) + ((cc ^ (i & 7)) << 4)) = v;
+        }
+        named_bar_sync(1, kAttnWarps * 32);
+
+        float m_run[MT][2], l_run[MT][2], O[MT][DB][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            m_run[mt][0] = m_run[mt][1] = -INFINITY;
+            l_run[mt][0] = l_run[mt][1] = 0.f;
+#pragma unroll
+            for (int j = 0; j < DB; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    O[mt][j][e] = 0.f;
+        }
+
+        for (int u = p.u0; u < p.u1; u += kAttnTile / kAttnUnit, ++it) {
+            const int nun = min(kAttnTile / kAttnUnit, p.u1 - u);
+            const int ntok = nun * kAttnUnit;
+            const int t0 = u * kAttnUnit;
+            const int slot = (int)(it % L::kNStages);
+            const uint32_t ph = (uint32_t)((it / L::kNStages) & 1);
+            const bool ok = mbar_wait(&full[slot], ph, abort, a.status);
+            uint8_t *kst = smem + slot * L::kStageBytes;
+            uint8_t *vst = kst + L::kTileBytes;
+
+            // positions past the sequence end hold stale memory: zero those V rows
+            // (Turbo4: the dequantization writes zeros there instead)
+            if (!VQ && ok && t0 + ntok > Lb) {
+                const int first = Lb - t0 > 0 ? Lb - t0 : 0;
+                for (int idx = tid; idx < (ntok - first) * DB * 8; idx += kAttnWarps * 32) {
+                    const int row = first + idx / (DB * 8), rest = idx % (DB * 8);
+                    const int db = rest >> 3, cc = rest & 7;
+                    *reinterpret_cast<uint4 *>(vst + db * kDBox + row * 128 + cc * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+
+            // ---- S = q K^T for this warp's 8 tokens; the head_dim contraction is
+            //      spread over SPLIT independent accumulator chains (MMA latency)
+            constexpr int SPLIT = MT >= 4 ? 1 : (MT >= 2 ? 2 : 4);
+            float sc[MT][4];
+            float scs[SPLIT][MT][4];
+            const bool has_tok = ok && (warp * 8 < ntok);
+#pragma unroll
+            for (int q = 0; q < SPLIT; ++q)
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        scs[q][mt][e] = 0.f;
+            if (has_tok) {
+                const int tok = warp * 8 + (lane & 7);
+#pragma unroll
+                for (int k2 = 0; k2 < 2 * DB; ++k2) {
+                    const int chunk = k2 * 4 + (lane >> 3);
+                    uint32_t kb[4];
+                    ldsm_x4(kb, smem_u32(kst + (chunk >> 3) * kDBox + tok * 128 +
+                                         (((chunk & 7) ^ (tok & 7)) << 4)));
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int ks = 2 * k2 + h;
+                            const int qrow = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+                            const int qch = 2 * ks + (lane >> 4);
+                            uint32_t qa[4];
+                            ldsm_x4(qa, smem_u32(qs + qrow * (D * 2) + ((qch ^ (qrow & 7)) << 4)));
+                            mma_bf16(scs[ks % SPLIT][mt], qa, kb[2 * h], kb[2 * h + 1],
+                                     scs[ks % SPLIT][mt]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float t = scs[0][mt][e];
+#pragma unroll
+                    for (int q = 1; q < SPLIT; ++q)
+                        t += scs[q][mt][e];
+                    sc[mt][e] = t;
+                }
+            // ---- mask (causal per verify row), scale, warp row max
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = mt * 16 + g + ((e & 2) ? 8 : 0);
+                    const int t = t0 + warp * 8 + 2 * cq + (e & 1);
+                    const bool vis = has_tok && i < nrows && t <= p0 + (i % a.R);
+                    sc[mt][e] = vis ? sc[mt][e] * a.scale_log2 : -INFINITY;
+                }
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    float mx = fmaxf(sc[mt][2 * hr], sc[mt][2 * hr + 1]);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    if (cq == 0)
+                        red_max[warp * 64 + mt * 16 + g + 8 * hr] = mx;
+                }
+            }
+            named_bar_sync(1, kAttnWarps * 32);
+            // ---- Turbo4 V: dequantize the tile into the fp16 tile (same layout as the
+            //      bf16 V tile); every warp has finished the previous tile's P V
+            if constexpr (VQ) {
+                if (ok) {
+                    const uint8_t *cst = vst, *sst = vst + L::kVCodeBytes;
+                    // A 16-byte store is served eight lanes at a time; those lanes
+                    // share a token and take its eight 32-column pieces c, so each
+                    // lane writes its four 8-column chunks in an order rotated by c:
+                    // at every step the eight lanes hit eight different bank groups.
+                    constexpr int kRotShift = DB == 4 ? 1 : 0;
+                    for (int idx = tid; idx < kAttnTile * DB * 2; idx += kAttnWarps * 32) {
+                        const int tl = idx / (DB * 2), c = idx % (DB * 2);   // token, 32 columns
+                        const int rot = (c >> kRotShift) & 3;
+                        const bool live = tl < ntok && t0 + tl < Lb;
+                        uint4 cb = make_uint4(0, 0, 0, 0);
+                        __half2 s0 = __float2half2_rn(0.f), s1 = s0;
+                        if (live) {
+                            cb = *reinterpret_cast<const uint4 *>(cst + tl * (DB * 32) + c * 16);
+                            const uint32_t sb = *reinterpret_cast<const uint16_t *>(
+                                sst + tl * (DB * 4) + c * 2);
+                            s0 = __half2half2(e4m3_to_half((uint8_t)(sb & 0xFF)));
+                            s1 = __half2half2(e4m3_to_half((uint8_t)(sb >> 8)));
+                        }
+#pragma unroll
+                        for (int st = 0; st < 4; ++st) {
+                            const int q = (st + rot) & 3;            // bytes 4q .. 4q + 3
+                            const uint32_t wq = q == 0 ? cb.x : (q == 1 ? cb.y : (q == 2 ? cb.z : cb.w));
+                            const __half2 sc = q < 2 ? s0 : s1;      // groups 2c, 2c + 1
+                            uint32_t o[4];
+#pragma unroll
+                            for (int k2 = 0; k2 < 4; ++k2) {
+                                const uint32_t pr = live ? lut[(wq >> (8 * k2)) & 0xFF] : 0u;
+                                const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&pr), sc);
+                                o[k2] = *reinterpret_cast<const uint32_t *>(&v);
+                            }
+                            const int ch = 4 * c + q;                   // 8-column chunk of the row
+                            *reinterpret_cast<uint4 *>(dq + (ch >> 3) * kDBox + tl * 128 +
+                                                       (((ch & 7) ^ (tl & 7)) << 4)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+            }
+            // ---- online softmax update, P to shared memory
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int i = mt * 16 + g + 8 * hr;
+                    float tmax = -INFINITY;
+#pragma unroll
+                    for (int w2 = 0; w2 < kAttnWarps; ++w2)
+                        tmax = fmaxf(tmax, red_max[w2 * 64 + i]);
+                    const float m_new = fmaxf(m_run[mt][hr], tmax);
+                    const float base = (m_new == -INFINITY) ? 0.f : m_new;
+                    const float alpha = exp2f(m_run[mt][hr] - base);
+                    m_run[mt][hr] = m_new;
+                    const float p0f = exp2f(sc[mt][2 * hr] - base);
+                    const float p1f = exp2f(sc[mt][2 * hr + 1] - base);
+                    // P in the V tile's type (bf16, or fp16 for the Turbo4 tile); l sums the
+                    // rounded values the MMA multiplies
+                    float pr0, pr1;
+                    uint32_t pk;
+                    if constexpr (VQ) {
+                        const __half2 hp = __floats2half2_rn(p0f, p1f);
+                        pk = *reinterpret_cast<const uint32_t *>(&hp);
+                        pr0 = __low2float(hp);
+                        pr1 = __high2float(hp);
+                    } else {
+                        pk = pack_bf16x2(p0f, p1f);
+                        pr0 = bf16_lo(pk);
+                        pr1 = bf16_hi(pk);
+                    }
+                    l_run[mt][hr] = l_run[mt][hr] * alpha + (pr0 + pr1);
+#pragma unroll
+                    for (int j = 0; j < DB; ++j) {
+                        O[mt][j][2 * hr] *= alpha;
+                        O[mt][j][2 * hr + 1] *= alpha;
+                    }
+                    if (has_tok)
+                        *reinterpret_cast<uint32_t *>(ps + i * 128 + ((warp ^ (i & 7)) << 4) +
+                                                      cq * 4) = pk;
+                }
+            }
+            named_bar_sync(1, kAttnWarps * 32);
+            // ---- O += P V for this warp's head_dim slice
+            const uint8_t *vt = VQ ? dq : vst;
+            if (ok) {
+#pragma unroll
+                for (int kt = 0; kt < kAttnTile / 16; ++kt) {
+                    if (kt * 16 < ntok) {
+                        const int tok = kt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+                        uint32_t vb[DB][2];
+#pragma unroll
+                        for (int j = 0; j < DB; j += 2) {
+                            const int nd = warp * DB + j;
+                            if (j + 1 < DB) {
+                                const int chunk = nd + (lane >> 4);
+                                uint32_t r[4];
+                                ldsm_x4_trans(r, smem_u32(vt + (chunk >> 3) * kDBox + tok * 128 +
+                                                          (((chunk & 7) ^ (tok & 7)) << 4)));
+                                vb[j][0] = r[0];
+                                vb[j][1] = r[1];
+                                vb[j + 1][0] = r[2];
+                                vb[j + 1][1] = r[3];
+                            } else {
+                                const int chunk = nd;
+                                ldsm_x2_trans(vb[j][0], vb[j][1],
+                                              smem_u32(vt + (chunk >> 3) * kDBox + tok * 128 +
+                                                       (((chunk & 7) ^ (tok & 7)) << 4)));
+                            }
+                        }
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            const int prow = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+                            const int pch = 2 * kt + (lane >> 4);
+                            uint32_t pa[4];
+                            ldsm_x4(pa, smem_u32(ps + prow * 128 + ((pch ^ (prow & 7)) << 4)));
+#pragma unroll
+                            for (int j = 0; j < DB; ++j) {
+                                if constexpr (VQ)
+                                    mma_f16(O[mt][j], pa, vb[j][0], vb[j][1], O[mt][j]);
+                                else
+                                    mma_bf16(O[mt][j], pa, vb[j][0], vb[j][1], O[mt][j]);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[slot]);
+        }
+
+        // ---- partial (m, l, O) of this piece into slot seg + c (valid rows only);
+        //      a separate merge kernel combines the slots of each segment
+        float *part = a.ws + (p.seg + c) * (long long)attn_slot_floats(D);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                float l = l_run[mt][hr];
+                l += __shfl_xor_sync(0xffffffffu, l, 1);
+                l += __shfl_xor_sync(0xffffffffu, l, 2);
+                if (cq == 0)
+                    red_l[warp * 64 + mt * 16 + g + 8 * hr] = l;
+            }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int j = 0; j < DB; ++j) {
+                const int col = (warp * DB + j) * 8 + 2 * cq;
+                const int r0 = mt * 16 + g;
+                if (r0 < nrows)
+                    *reinterpret_cast<float2 *>(part + 2 * kAttnMaxRows + (long long)r0 * D + col) =
+                        make_float2(O[mt][j][0], O[mt][j][1]);
+                if (r0 + 8 < nrows)
+                    *reinterpret_cast<float2 *>(part + 2 * kAttnMaxRows + (long long)(r0 + 8) * D +
+                                                col) = make_float2(O[mt][j][2], O[mt][j][3]);
+            }
+        named_bar_sync(1, kAttnWarps * 32);
+        if (warp == 0 && cq == 0) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int i = mt * 16 + g + 8 * hr;
+                    float l = 0.f;
+#pragma unroll
+                    for (int w2 = 0; w2 < kAttnWarps; ++w2)
+                        l += red_l[w2 * 64 + i];
+                    part[i] = m_run[mt][hr];
+                    part[kAttnMaxRows + i] = l;
+                }
+        }
+        // red_l is reused by the next piece: keep warp 0's reads before new writes
+        named_bar_sync(1, kAttnWarps * 32);
+        pos = p.seg_start + p.u1;
+    }
+}
+
+
+template <int MT, int DB, int VQ>
+static cudaError_t launch_attn_t(const AttnArgs &a, const CUtensorMap &kmap,
+                                 const CUtensorMap &vmap, int grid, bool pdl, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = AttnSmem<MT, DB, VQ>::kTotal;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_kernel<MT, DB, VQ>, a, kmap, vmap);
+}
+
+// the (MT, DB) instances: MT = 16-row tiles of a segment's rows, DB = d / 64
+#define GATTN_ATTN_INSTANCES(X)                                                                    \
+    X(1, 1) X(2, 1) X(3, 1) X(4, 1) X(1, 2) X(2, 2) X(3, 2) X(4, 2) X(1, 4) X(2, 4) X(3, 4) X(4, 4)
+
+}  // namespace gattn

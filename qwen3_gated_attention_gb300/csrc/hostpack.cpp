@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "gattn.h"
 
@@ -91,5 +92,54 @@ extern "C" gattn_status gattn_pack_affine_host(const float *w, int64_t N, int64_
             }
         }
     }
+    return GATTN_OK;
+}
+
+// ------------------------------------------------------------- Turbo4 tables
+//
+// The 16-level Lloyd-Max quantizer of N(0, 1) (the codebook of the Turbo4
+// V-cache format): symmetric, so only the 8 positive levels are iterated.
+// Lloyd's iteration alternates the decision points (midpoints of adjacent
+// levels; 0 between the two innermost) and the levels (the mean of N(0, 1)
+// over each cell, phi(a) - phi(b) over its upper-tail mass Q(a) - Q(b)),
+// starting from evenly spaced levels and running to its fixed point.
+namespace {
+
+void lloyd_max16(double pos[8])
+{
+    const double inv_sqrt_2pi = 0.39894228040143267794, inv_sqrt2 = 0.70710678118654752440;
+    auto pdf = [&](double x) { return std::isinf(x) ? 0.0 : inv_sqrt_2pi * std::exp(-0.5 * x * x); };
+    auto upper = [&](double x) { return 0.5 * std::erfc(x * inv_sqrt2); };
+    for (int k = 0; k < 8; ++k)
+        pos[k] = 3.0 * (k + 0.5) / 8.0;
+    for (int round = 0; round < 4000; ++round) {
+        double edge[9];
+        edge[0] = 0.0;
+        for (int k = 1; k < 8; ++k)
+            edge[k] = 0.5 * (pos[k - 1] + pos[k]);
+        edge[8] = INFINITY;
+        for (int k = 0; k < 8; ++k)
+            pos[k] = (pdf(edge[k]) - pdf(edge[k + 1])) / (upper(edge[k]) - upper(edge[k + 1]));
+    }
+}
+
+}  // namespace
+
+extern "C" gattn_status gattn_turbo4_codebook(float levels[16], float thresholds[15])
+{
+    if (!levels || !thresholds)
+        return GATTN_E_INVALID_ARG;
+    static double pos[8];
+    static std::once_flag once;
+    std::call_once(once, [] { lloyd_max16(pos); });
+    double c[16];
+    for (int k = 0; k < 8; ++k) {
+        c[8 + k] = pos[k];
+        c[7 - k] = -pos[k];
+    }
+    for (int j = 0; j < 16; ++j)
+        levels[j] = (float)c[j];
+    for (int j = 0; j < 15; ++j)
+        thresholds[j] = (float)(0.5 * (c[j] + c[j + 1]));
     return GATTN_OK;
 }

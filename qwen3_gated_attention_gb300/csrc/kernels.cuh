@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "turbo.cuh"
+
 struct gattn_layer;
 
 namespace gattn {
@@ -88,6 +90,11 @@ struct EpiQKV {
     __nv_bfloat16 *qn;             // [B][R][H][d]
     float *gate;                   // [M][H*d]
     float *tap_y;                  // [M][Nq + 2 Nkv] or null
+    // Bf16KTurbo4V cache: the new V rows are quantized (turbo.cuh), not stored
+    // as bf16 (null: bf16 V)
+    uint8_t *vq_codes, *vq_scales;
+    long long cq_head, cq_batch, sq_head, sq_batch;   // byte strides
+    TurboTables tq;
 };
 
 struct EpiO {
@@ -116,6 +123,14 @@ enum { kModeQKV = 0, kModeO = 1 };
 cudaError_t launch_proj(int bits, int NT, int mode, const ProjArgs &a, const EpiQKV &eq,
                         const EpiO &eo, int grid, bool pdl, cudaStream_t s);
 int proj_smem_bytes(const ProjArgs &a);
+// shared memory past the projection's stage ring: barriers, flags, epilogue
+// statics; the q|k|v epilogue stages up to kWR head rows of d <= 256 values
+constexpr int kValsFloats = kWR * 256;
+__host__ __device__ inline int proj_tail_bytes(int eb_rows)
+{
+    (void)eb_rows;
+    return 256 + kValsFloats * 4 + 2 * 256 * 4 + 128 * 8 + 32 * 4;
+}
 cudaError_t proj_set_smem_limits(int bits, int NT, int mode, int bytes);
 cudaError_t proj_occupancy(int bits, int NT, int mode, int group, int smem, int *blocks_per_sm);
 // clusters of csize CTAs that can be resident at once (0: that size cannot launch)
@@ -227,10 +242,25 @@ struct AttnArgs {
     int NT, group_o;
     float *tap_attn;             // [M][H*d] or null
     unsigned *status;
+    // Bf16KTurbo4V cache (vq != 0): V code / scale rows, the byte -> fp16 level
+    // pair table, and the inverse rotation applied in the merge
+    int vq;
+    const uint8_t *vq_codes, *vq_scales;
+    long long cq_head, cq_batch, sq_head, sq_batch;   // byte strides
+    const uint32_t *vq_lut;      // [256] half2 (level of the low nibble, of the high nibble)
+    float inv_sqrt_d;
 };
 
 cudaError_t launch_attn(int MT, int DB, const AttnArgs &a, const CUtensorMap &kmap,
                         const CUtensorMap &vmap, int grid, bool pdl, cudaStream_t s);
+// the Bf16KTurbo4V instances (attn_vq.cu); vmap is unused there
+cudaError_t launch_attn_vq(int MT, int DB, const AttnArgs &a, const CUtensorMap &kmap, int grid,
+                           bool pdl, cudaStream_t s);
+int attn_vq_smem_bytes(int MT, int DB);
+cudaError_t attn_vq_set_smem_limits();
+// standalone Turbo4 quantizer: one warp per row of d bf16 values
+cudaError_t launch_turbo4_quantize(const uint16_t *v, long long rows, int d, uint8_t *codes,
+                                   uint8_t *scales, const TurboTables &t, cudaStream_t s);
 // merge of the attention partials + output gate -> o_proj operand
 cudaError_t launch_attn_merge(const AttnArgs &a, int max_rows, bool pdl, cudaStream_t s);
 int attn_smem_bytes(int MT, int DB);

@@ -13,6 +13,9 @@
 //
 //   attn = O / l,   a = attn * sigmoid(gate)   (the layer's output gate)
 //
+// Over a Bf16KTurbo4V cache the V rows were attended in their Walsh-Hadamard
+// basis, so attn is first rotated back: attn = H (O / l) / sqrt(d).
+//
 // `a` goes to the o_proj input in fp16 tensor-core fragment order, with the
 // group sums of those fp16 values that the projection's bias term needs.
 #include "common.cuh"
@@ -129,7 +132,25 @@ __global__ void __launch_bounds__(512) attn_merge_kernel(const AttnArgs a)
     __syncthreads();
     if (half != 0)
         return;
-    const float o = comb[jd] + comb[jd + D];
+    float o = comb[jd] + comb[jd + D];
+    if (a.vq) {
+        // Turbo4 V cache: the values were attended in the rotated basis; rotate
+        // the output row back, H o / sqrt(d) (butterflies over the d columns:
+        // within a warp by shuffles, across warps through shared memory)
+#pragma unroll
+        for (int h2 = 1; h2 < 32; h2 <<= 1) {
+            const float p = __shfl_xor_sync(0xffffffffu, o, h2);
+            o = (lane & h2) ? p - o : o + p;
+        }
+        for (int h2 = 32; h2 < D; h2 <<= 1) {
+            named_bar_sync(2, D);       // the partner has read this slot's last value
+            comb[jd] = o;
+            named_bar_sync(2, D);
+            const float p = comb[jd ^ h2];
+            o = (jd & h2) ? p - o : o + p;
+        }
+        o *= a.inv_sqrt_d;
+    }
     const float gated = o * (1.f / (1.f + __expf(-gt)));
     const __half hv = __float2half_rn(gated);
     const int k = h * D + jd;

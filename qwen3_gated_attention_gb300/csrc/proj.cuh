@@ -152,15 +152,24 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
 {
     const int d = e.d, half = e.rd >> 1, heads = a.eb_rows / d, per = d >> 5;
     const int Ny = e.Nq + 2 * e.Nkv;
-    for (int m = rank; m < a.M; m += csize) {
-        for (int r = tid; r < a.eb_rows; r += kWR * 32)
-            sm.vals[r] = cluster_row_sum<MP, 1>(a, sm, r, m);
+    // up to kWR / heads of this CTA's columns at a time, so that every warp has
+    // a (column, head) to finish even when the cluster spans a single head
+    const int mper = heads >= kWR ? 1 : kWR / heads;
+    for (int m0 = rank; m0 < a.M; m0 += csize * mper) {
+        for (int idx = tid; idx < mper * a.eb_rows; idx += kWR * 32) {
+            const int j = idx / a.eb_rows, r = idx - j * a.eb_rows;
+            const int m = m0 + j * csize;
+            if (m < a.M)
+                sm.vals[idx] = cluster_row_sum<MP, 1>(a, sm, r, m);
+        }
         named_bar_sync(1, kWR * 32);
-        for (int hb = warp; hb < heads; hb += kWR) {
+        for (int wi = warp; wi < mper * heads; wi += kWR) {
+            const int j = wi / heads, hb = wi - j * heads;
+            const int m = m0 + j * csize;
             const int n0 = row0 + hb * d;
-            if (n0 >= a.N)
+            if (m >= a.M || n0 >= a.N)
                 continue;
-            const float *hv = sm.vals + hb * d;
+            const float *hv = sm.vals + j * a.eb_rows + hb * d;
             float v[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -237,6 +246,18 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
             if (!valid) {
                 if (lane == 0)
                     atomicOr(a.status, kStatusRange);
+                continue;
+            }
+            if (kind == 3 && e.vq_codes) {
+                // Bf16KTurbo4V cache: quantize the bf16 V row (turbo.cuh)
+                float xq[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    xq[i] = i < per ? __bfloat162float(__float2bfloat16_rn(v[i])) : 0.f;
+                const long long row = p0 + r;
+                turbo4_quantize_warp(xq, per, lane, e.tq,
+                                     e.vq_codes + b * e.cq_batch + head * e.cq_head + row * (d / 2),
+                                     e.vq_scales + b * e.sq_batch + head * e.sq_head + row * (d / 16));
                 continue;
             }
             __nv_bfloat16 *dst = (kind == 2 ? e.kc : e.vc) + (long long)b * e.st_batch +
@@ -349,11 +370,6 @@ static __device__ void postnorm_tail(const ProjArgs &a, const EpiO &e, float *sc
         *e.ticket = 0u;         // ready for the next launch
 }
 
-// shared memory past the stage ring: barriers, flags, epilogue statics
-__host__ __device__ inline int proj_tail_bytes(int eb_rows)
-{
-    return 256 + eb_rows * 4 + 2 * 256 * 4 + 128 * 8 + 32 * 4;
-}
 
 // Two CTAs per SM at least; the four-column-tile instances, whose grids are
 // short of CTAs at two per SM, ask for three.
@@ -372,7 +388,7 @@ __global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
     EpiSmem sm;
     sm.red = reinterpret_cast<float *>(smem);                         // after the main loop
     sm.vals = reinterpret_cast<float *>(tail + 256);
-    sm.nq = sm.vals + a.eb_rows;
+    sm.nq = sm.vals + kValsFloats;
     sm.nk = sm.nq + 256;
     sm.invf = reinterpret_cast<double *>(sm.nk + 256);
     sm.cpos = reinterpret_cast<int *>(sm.invf + 128);

@@ -14,8 +14,8 @@ GATTN_DECL(2) GATTN_DECL(3) GATTN_DECL(4) GATTN_DECL(5) GATTN_DECL(6) GATTN_DECL
 
 int proj_smem_bytes(const ProjArgs &a)
 {
-    // stage ring + barriers/flags + epilogue statics (see proj_tail_bytes in proj.cuh)
-    return a.stages * a.stage_bytes + 256 + a.eb_rows * 4 + 2 * 256 * 4 + 128 * 8 + 32 * 4;
+    // stage ring + barriers/flags + epilogue statics (proj_tail_bytes in kernels.cuh)
+    return a.stages * a.stage_bytes + proj_tail_bytes(a.eb_rows);
 }
 
 cudaError_t launch_proj(int bits, int NT, int mode, const ProjArgs &a, const EpiQKV &eq,

@@ -27,16 +27,19 @@ def cache_strides(layout: str, batch: int, Hk: int, cap: int, d: int):
 
 
 class DeviceLayer:
-    """One layer handle with its weights set and one registered bf16 cache."""
+    """One layer handle with its weights set and one registered cache: bf16 K/V,
+    or (kv_format="turbo4v") bf16 K with Turbo4 V code and E4M3 scale planes
+    [B][Hk][cap][d/2] and [B][Hk][cap][d/16] uint8."""
 
     def __init__(self, spec, packed, q_norm, k_norm, capacity, *, batch=None, max_batch=None,
                  max_q_len=None, head_chunk=True, layout="bhtd", device="cuda:0",
-                 path=gattn.PATH_AUTO):
+                 path=gattn.PATH_AUTO, kv_format="bf16"):
         self.spec = spec
         self.device = torch.device(device)
         self.batch = batch or spec.batch
         self.layout = layout
         self.capacity = capacity
+        self.kv_format = kv_format
         self.cfg = gattn.make_cfg(spec.hidden, spec.num_heads, spec.num_kv_heads, spec.head_dim,
                                   spec.partial_rotary_factor, spec.rope_theta, spec.rms_eps,
                                   tuple(spec.bits), tuple(spec.group), x_dtype=spec.x_dtype,
@@ -57,17 +60,37 @@ class DeviceLayer:
             Hk, d = spec.num_kv_heads, spec.head_dim
             shape, st, sh, sb = cache_strides(layout, self.batch, Hk, capacity, d)
             self.k = torch.zeros(shape, dtype=torch.bfloat16, device=self.device)
-            self.v = torch.zeros(shape, dtype=torch.bfloat16, device=self.device)
-            self.kv = gattn.kv_register(self.h, self.k.data_ptr(), self.v.data_ptr(), self.batch,
-                                        capacity, st, sh, sb)
+            if kv_format == "turbo4v":
+                assert layout == "bhtd"
+                B = self.batch
+                self.vc = torch.zeros((B, Hk, capacity, d // 2), dtype=torch.uint8, device=self.device)
+                self.vs = torch.zeros((B, Hk, capacity, d // 16), dtype=torch.uint8,
+                                      device=self.device)
+                self.kv = gattn.kv_register_turbo4v(
+                    self.h, self.k.data_ptr(), self.vc.data_ptr(), self.vs.data_ptr(), B, capacity,
+                    (st, sh, sb), (capacity * d // 2, Hk * capacity * d // 2),
+                    (capacity * d // 16, Hk * capacity * d // 16))
+            else:
+                self.v = torch.zeros(shape, dtype=torch.bfloat16, device=self.device)
+                self.kv = gattn.kv_register(self.h, self.k.data_ptr(), self.v.data_ptr(),
+                                            self.batch, capacity, st, sh, sb)
         except Exception:
             self.close()
             raise
 
     # caches are exchanged with the host as [B][Hk][cap][d] bf16 bit patterns
-    def load_cache(self, k_bits: np.ndarray, v_bits: np.ndarray, batches=None):
+    def load_cache(self, k_bits: np.ndarray, v_bits, batches=None):
+        """v_bits: bf16 bits [B][Hk][cap][d], or (codes, scales) for a turbo4v cache."""
         idx = list(range(self.batch)) if batches is None else list(batches)
-        for dst, src in ((self.k, k_bits), (self.v, v_bits)):
+        if self.kv_format == "turbo4v":
+            codes, scales = v_bits
+            for j, b in enumerate(idx):
+                self.vc[b].copy_(torch.from_numpy(np.ascontiguousarray(codes[j], np.uint8)))
+                self.vs[b].copy_(torch.from_numpy(np.ascontiguousarray(scales[j], np.uint8)))
+            pairs = ((self.k, k_bits),)
+        else:
+            pairs = ((self.k, k_bits), (self.v, v_bits))
+        for dst, src in pairs:
             for j, b in enumerate(idx):
                 t = _dev_u16(src[j], self.device).view(torch.bfloat16)      # [Hk][cap][d]
                 if self.layout == "bhtd":
@@ -76,7 +99,13 @@ class DeviceLayer:
                     dst[b].copy_(t.transpose(0, 1))
 
     def read_cache(self, batches=None):
+        """(K bits, V bits), or (K bits, (codes, scales)) for a turbo4v cache."""
         idx = list(range(self.batch)) if batches is None else list(batches)
+        if self.kv_format == "turbo4v":
+            k = np.stack([self.k[b].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+                          for b in idx])
+            return k, (np.stack([self.vc[b].cpu().numpy() for b in idx]),
+                       np.stack([self.vs[b].cpu().numpy() for b in idx]))
         outs = []
         for src in (self.k, self.v):
             parts = []

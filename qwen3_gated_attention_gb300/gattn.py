@@ -31,7 +31,8 @@ EXPORTS = (
     "gattn_layer_destroy", "gattn_kv_destroy", "gattn_last_error", "gattn_pack_affine_host",
     "gattn_unpack_codes_device", "gattn_layer_dequant_device", "gattn_head_chunk_plan",
     "gattn_layer_launches_per_step", "gattn_layer_set_events", "gattn_layer_dequant_device_static",
-    "gattn_layer_set_path", "gattn_layer_step_block",
+    "gattn_layer_set_path", "gattn_layer_step_block", "gattn_kv_register_turbo4v",
+    "gattn_turbo4_codebook", "gattn_turbo4_quantize_device",
 )
 
 
@@ -62,6 +63,15 @@ class gattn_kv_desc(C.Structure):
     _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("batch", C.c_int32),
                 ("capacity", C.c_int32), ("stride_token", C.c_int64), ("stride_head", C.c_int64),
                 ("stride_batch", C.c_int64)]
+
+
+class gattn_kv_turbo4v_desc(C.Structure):
+    _fields_ = [("k", C.c_void_p), ("v_codes", C.c_void_p), ("v_scales", C.c_void_p),
+                ("batch", C.c_int32), ("capacity", C.c_int32),
+                ("k_stride_token", C.c_int64), ("k_stride_head", C.c_int64),
+                ("k_stride_batch", C.c_int64), ("code_stride_head", C.c_int64),
+                ("code_stride_batch", C.c_int64), ("scale_stride_head", C.c_int64),
+                ("scale_stride_batch", C.c_int64)]
 
 
 class gattn_taps(C.Structure):
@@ -105,12 +115,16 @@ def lib():
         L.gattn_layer_set_events.argtypes = [p, p, i32]
         L.gattn_layer_set_path.argtypes = [p, i32]
         L.gattn_layer_step_block.argtypes = [p, p, p, p, i32, i32, p, p, p, p, p]
+        L.gattn_kv_register_turbo4v.argtypes = [p, C.POINTER(gattn_kv_turbo4v_desc), C.POINTER(p)]
+        L.gattn_turbo4_codebook.argtypes = [p, p]
+        L.gattn_turbo4_quantize_device.argtypes = [p, i64, i32, p, p, p]
         for name in ("gattn_cfg_validate", "gattn_layer_create", "gattn_layer_set_weights",
                      "gattn_kv_register", "gattn_layer_step", "gattn_layer_poll_status",
                      "gattn_layer_set_taps", "gattn_pack_affine_host", "gattn_unpack_codes_device",
                      "gattn_layer_dequant_device", "gattn_layer_set_events",
                      "gattn_layer_dequant_device_static", "gattn_layer_set_path",
-                     "gattn_layer_step_block"):
+                     "gattn_layer_step_block", "gattn_kv_register_turbo4v",
+                     "gattn_turbo4_codebook", "gattn_turbo4_quantize_device"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -175,6 +189,32 @@ def kv_register(layer: int, k: int, v: int, batch: int, capacity: int, stride_to
     h = C.c_void_p()
     _check(lib().gattn_kv_register(layer, C.byref(d), C.byref(h)))
     return h.value
+
+
+def kv_register_turbo4v(layer: int, k: int, v_codes: int, v_scales: int, batch: int,
+                        capacity: int, k_strides, code_strides, scale_strides) -> int:
+    """Register a Bf16KTurbo4V cache.  k_strides: (token, head, batch) in
+    elements; code_strides / scale_strides: (head, batch) in bytes."""
+    d = gattn_kv_turbo4v_desc(k, v_codes, v_scales, batch, capacity, *k_strides, *code_strides,
+                              *scale_strides)
+    h = C.c_void_p()
+    _check(lib().gattn_kv_register_turbo4v(layer, C.byref(d), C.byref(h)))
+    return h.value
+
+
+def turbo4_codebook():
+    """(levels fp32 [16], thresholds fp32 [15]) as the kernels use them (host call)."""
+    import numpy as np
+    lv = np.zeros(16, np.float32)
+    th = np.zeros(15, np.float32)
+    _check(lib().gattn_turbo4_codebook(lv.ctypes.data, th.ctypes.data))
+    return lv, th
+
+
+def turbo4_quantize_device(v: int, rows: int, d: int, codes: int, scales: int,
+                           stream: int = 0) -> None:
+    """Quantize bf16 rows (device) into Turbo4 codes and E4M3 scales (device)."""
+    _check(lib().gattn_turbo4_quantize_device(v, rows, d, codes, scales, stream))
 
 
 def layer_step(layer: int, x: int, kv: int, cache_pos: int, batch: int, q_len: int, out: int,

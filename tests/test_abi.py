@@ -116,3 +116,23 @@ def test_step_rejects_null_arguments_without_a_gpu():
     with pytest.raises(gattn.GattnError) as ei:
         gattn.layer_step(0, 0, 0, 0, 1, 1, 0, 0)
     assert ei.value.status == 1
+
+
+def test_turbo4_codebook_matches_oracle_bit_exactly():
+    """The library derives its Turbo4 tables (Lloyd-Max levels of N(0, 1) and
+    the thresholds between them) by its own iteration; the fp32 values the
+    kernels decide with equal the oracle's bit for bit, so both sides take the
+    same quantization decisions."""
+    lv, th = gattn.turbo4_codebook()
+    olv, oth = orc.turbo4_tables_f32()
+    assert np.array_equal(lv.view(np.uint32), olv.view(np.uint32))
+    assert np.array_equal(th.view(np.uint32), oth.view(np.uint32))
+    assert th[7] == 0.0 and np.array_equal(lv, -lv[::-1])
+
+
+def test_turbo4_quantize_rejects_bad_arguments_without_a_gpu():
+    with pytest.raises(gattn.GattnError) as e:
+        gattn.turbo4_quantize_device(0, 4, 96, 0, 0)
+    assert e.value.status == 1                                  # GATTN_E_INVALID_ARG
+    with pytest.raises(gattn.GattnError):
+        gattn.turbo4_quantize_device(0, 4, 128, 0, 0)          # NULL pointers
