@@ -107,6 +107,8 @@ def _declare(L):
     L.orc_turbo4_tables_f32.restype = None
     L.orc_turbo4_quantize_rows.argtypes = [_p, _i64, _i, _p, _p]
     L.orc_turbo4_dequant_rows.argtypes = [_p, _p, _i64, _i, _i, _p]
+    L.orc_layer_step_masked.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _p, _p,
+                                        _i, _p, _i, _i, _p, _i, _i64, _i64, _i64, _p, _p, _p]
     L.orc_layer_step_turbo4v.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _p, _p,
                                          _p, _i, _p, _i, _i, _p, _p, _p]
 
@@ -118,7 +120,15 @@ def _ptr(a: np.ndarray | None):
     return a.ctypes.data
 
 
+class MaskRouteError(ValueError):
+    """A head-specific mask met the head-chunked attention route ([DS4#113]:
+    the route hands the mask unchanged to every head chunk, so only a
+    broadcast mask fits)."""
+
+
 def _check(rc, what):
+    if rc == 3:
+        raise MaskRouteError(f"oracle {what}: a head-specific mask cannot take the head-chunk route")
     if rc != 0:
         raise ValueError(f"oracle {what} rejected its arguments (code {rc})")
 
@@ -259,13 +269,16 @@ def _layer_structs(spec, weights: OracleWeights, head_chunk: bool, mutate: str):
 
 def layer_step(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.ndarray,
                cache_v: np.ndarray, cache_pos: np.ndarray, head_chunk: bool = True,
-               mutate: str = "none", taps: bool = False):
+               mutate: str = "none", taps: bool = False, mask: np.ndarray | None = None):
     """One gated full-attention layer step ([mlxd#99] Summary: doubled q_proj ->
     split query/gate -> o_proj(attn * sigmoid(gate)); [atlas-mod] KV append at
     cache_pos, attention over cache_pos + 1 per row).
 
     x: [B][R][hidden] float64 values; cache_k/v: [B][Hk][cap][d] bf16 bits,
-    updated in place.  Returns out [B][R][hidden] (and the taps when asked)."""
+    updated in place.  mask (optional, [DS4#113] broadcast / head-specific
+    masks): uint8 [B][1 or H][R][T >= max(cache_pos) + R], nonzero = attend;
+    it replaces the causal rule.  Returns out [B][R][hidden] (and the taps
+    when asked)."""
     B, R, Hd = x.shape
     L, Wt, keep = _layer_structs(spec, weights, head_chunk, mutate)
     x = np.ascontiguousarray(x, np.float64)
@@ -276,8 +289,17 @@ def layer_step(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.ndarray,
     H, Hk, d = spec.num_heads, spec.num_kv_heads, spec.head_dim
     ty = np.zeros((B, R, 2 * H * d + 2 * Hk * d), np.float64) if taps else None
     ta = np.zeros((B, R, H, d), np.float64) if taps else None
-    rc = lib().orc_layer_step(C.byref(L), C.byref(Wt), _ptr(x), _ptr(cache_k), _ptr(cache_v), cap,
-                              _ptr(cp), B, R, _ptr(out), _ptr(ty), _ptr(ta))
+    if mask is None:
+        rc = lib().orc_layer_step(C.byref(L), C.byref(Wt), _ptr(x), _ptr(cache_k), _ptr(cache_v),
+                                  cap, _ptr(cp), B, R, _ptr(out), _ptr(ty), _ptr(ta))
+    else:
+        mk = np.ascontiguousarray(mask, np.uint8)
+        assert mk.ndim == 4 and mk.shape[0] == B and mk.shape[2] == R
+        assert int(np.max(cp)) + R <= mk.shape[3]
+        rc = lib().orc_layer_step_masked(C.byref(L), C.byref(Wt), _ptr(x), _ptr(cache_k),
+                                         _ptr(cache_v), cap, _ptr(cp), B, R, _ptr(mk), mk.shape[1],
+                                         mk.strides[2], mk.strides[1], mk.strides[0], _ptr(out),
+                                         _ptr(ty), _ptr(ta))
     _check(rc, "layer_step")
     if taps:
         return out, ty, ta

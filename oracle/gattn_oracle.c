@@ -330,11 +330,15 @@ typedef struct orc_weights {
  * against the cache of its KV head: scores q.k/sqrt(d) over t in [0, last],
  * softmax exp(s - max)/sum, output sum p_t v_t. */
 static void sdpa_row(const double *q, const uint16_t *kc, const uint16_t *vc, int64_t tstride,
-                     int d, int last, double *o, double *scores)
+                     int d, int last, const uint8_t *keep, double *o, double *scores)
 {
     double scale = 1.0 / sqrt((double)d);
     double mx = -INFINITY;
     for (int t = 0; t <= last; ++t) {
+        if (keep && !keep[t]) {
+            scores[t] = -INFINITY;
+            continue;
+        }
         const uint16_t *kt = kc + (int64_t)t * tstride;
         double s = 0.0;
         for (int j = 0; j < d; ++j)
@@ -343,13 +347,15 @@ static void sdpa_row(const double *q, const uint16_t *kc, const uint16_t *vc, in
         scores[t] = s;
         if (s > mx) mx = s;
     }
+    for (int j = 0; j < d; ++j)
+        o[j] = 0.0;
+    if (mx == -INFINITY)            /* every position masked out: a zero row */
+        return;
     double z = 0.0;
     for (int t = 0; t <= last; ++t) {
         scores[t] = exp(scores[t] - mx);
         z += scores[t];
     }
-    for (int j = 0; j < d; ++j)
-        o[j] = 0.0;
     for (int t = 0; t <= last; ++t) {
         const uint16_t *vt = vc + (int64_t)t * tstride;
         double p = scores[t] / z;
@@ -377,7 +383,7 @@ int orc_sdpa(const double *q, const uint16_t *cache_k, const uint16_t *cache_v,
         const uint16_t *vc = cache_v + (int64_t)kh * capacity * head_dim;
         for (int r = 0; r < R; ++r)
             sdpa_row(q + ((int64_t)i * R + r) * head_dim, kc, vc, head_dim, head_dim,
-                     pos0 + r, out + ((int64_t)i * R + r) * head_dim, scores);
+                     pos0 + r, NULL, out + ((int64_t)i * R + r) * head_dim, scores);
     }
     free(scores);
     return ORC_OK;
@@ -599,11 +605,15 @@ int orc_turbo4_dequant_rows(const uint8_t *codes, const uint8_t *scales, int64_t
 
 /* sdpa_row over V rows given in float64 (a dequantized cache) */
 static void sdpa_row_vd(const double *q, const uint16_t *kc, int64_t tstride, const double *vd,
-                        int d, int last, double *o, double *scores)
+                        int d, int last, const uint8_t *keep, double *o, double *scores)
 {
     double scale = 1.0 / sqrt((double)d);
     double mx = -INFINITY;
     for (int t = 0; t <= last; ++t) {
+        if (keep && !keep[t]) {
+            scores[t] = -INFINITY;
+            continue;
+        }
         const uint16_t *kt = kc + (int64_t)t * tstride;
         double s = 0.0;
         for (int j = 0; j < d; ++j)
@@ -612,13 +622,15 @@ static void sdpa_row_vd(const double *q, const uint16_t *kc, int64_t tstride, co
         scores[t] = s;
         if (s > mx) mx = s;
     }
+    for (int j = 0; j < d; ++j)
+        o[j] = 0.0;
+    if (mx == -INFINITY)
+        return;
     double z = 0.0;
     for (int t = 0; t <= last; ++t) {
         scores[t] = exp(scores[t] - mx);
         z += scores[t];
     }
-    for (int j = 0; j < d; ++j)
-        o[j] = 0.0;
     for (int t = 0; t <= last; ++t) {
         const double p = scores[t] / z;
         for (int j = 0; j < d; ++j)
@@ -637,9 +649,23 @@ static void sdpa_row_vd(const double *q, const uint16_t *kc, int64_t tstride, co
  * Returns ORC_OK, ORC_E_ARG for an inadmissible layer, ORC_E_RANGE when a
  * sequence would write past the capacity (nothing is written for it).
  */
+/* An attention mask ([DS4#113] "broadcast/head-specific masks"): byte
+ * m[b*stride_batch + hm*stride_head + r*stride_row + t], nonzero = row r may
+ * attend position t; hm = 0 for a broadcast mask (heads == 1), the query head
+ * for a head-specific one (heads == num_heads).  Reading: a mask replaces the
+ * causal rule (it carries it), positions run over [0, cache_pos + R), and a
+ * row with no position left is a zero row. */
+typedef struct orc_mask {
+    const uint8_t *m;
+    int32_t heads;
+    int64_t stride_row, stride_head, stride_batch;
+} orc_mask;
+
+#define ORC_E_MASK 3
+
 static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                       uint16_t *cache_k, uint16_t *cache_v, uint8_t *v_codes, uint8_t *v_scales,
-                      int capacity, const int32_t *cache_pos, int B, int R,
+                      int capacity, const int32_t *cache_pos, int B, int R, const orc_mask *M,
                       double *out, double *tap_y, double *tap_attn)
 {
     const int turbo = v_codes != NULL;
@@ -695,6 +721,16 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
         nk[j] = orc_bf16_to_double(W->k_norm[j]);
     }
     int nchunks = orc_head_chunk_plan(R, H, Hk, L->head_chunk, cf, cl, H);
+    if (M && M->heads != 1 && M->heads != H) {
+        rc = ORC_E_ARG;
+        goto done;
+    }
+    /* [DS4#113] the head-chunked route hands the mask unchanged to every head
+     * chunk: a broadcast mask fits each chunk, a mask over all H heads does not */
+    if (M && M->heads > 1 && nchunks > Hk) {
+        rc = ORC_E_MASK;
+        goto done;
+    }
 
     for (int b = 0; b < B; ++b) {
         const int p0 = cache_pos[b];
@@ -767,9 +803,15 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                     if (khh != kh)
                         continue;
                     for (int r = 0; r < R; ++r) {
-                        const int last = (L->mutate == ORC_MUT_NO_CAUSAL) ? p0 + R - 1 : p0 + r;
+                        int last = (L->mutate == ORC_MUT_NO_CAUSAL) ? p0 + R - 1 : p0 + r;
+                        const uint8_t *keep = NULL;
+                        if (M) {
+                            last = p0 + R - 1;
+                            keep = M->m + b * M->stride_batch + (M->heads > 1 ? h : 0) * M->stride_head +
+                                   r * M->stride_row;
+                        }
                         sdpa_row_vd(qn + ((int64_t)r * H + h) * d, kcb + (int64_t)kh * capacity * d,
-                                    d, vdq, d, last, attn + ((int64_t)r * H + h) * d, scores);
+                                    d, vdq, d, last, keep, attn + ((int64_t)r * H + h) * d, scores);
                     }
                 }
             }
@@ -809,8 +851,12 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                                                       : orc_bf16_to_double(vc[(int64_t)t * d + j]);
                                 o[j] += scores[t] / z * vv;
                             }
+                    } else if (M) {
+                        sdpa_row(qv, kc, vc, d, d, p0 + R - 1,
+                                 M->m + b * M->stride_batch + (M->heads > 1 ? h : 0) * M->stride_head +
+                                     r * M->stride_row, o, scores);
                     } else {
-                        sdpa_row(qv, kc, vc, d, d, last, o, scores);
+                        sdpa_row(qv, kc, vc, d, d, last, NULL, o, scores);
                     }
                 }
             }
@@ -843,8 +889,24 @@ int orc_layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                    const int32_t *cache_pos, int B, int R,
                    double *out, double *tap_y, double *tap_attn)
 {
-    return layer_step(L, W, x, cache_k, cache_v, NULL, NULL, capacity, cache_pos, B, R, out, tap_y,
-                      tap_attn);
+    return layer_step(L, W, x, cache_k, cache_v, NULL, NULL, capacity, cache_pos, B, R, NULL, out,
+                      tap_y, tap_attn);
+}
+
+/* orc_layer_step with an attention mask (orc_mask above): mask bytes, heads
+ * (1 or num_heads) and strides in bytes.  ORC_E_MASK when a head-specific
+ * mask meets the head-chunked route. */
+int orc_layer_step_masked(const orc_layer *L, const orc_weights *W, const double *x,
+                          uint16_t *cache_k, uint16_t *cache_v, int capacity,
+                          const int32_t *cache_pos, int B, int R, const uint8_t *mask,
+                          int32_t mask_heads, int64_t stride_row, int64_t stride_head,
+                          int64_t stride_batch, double *out, double *tap_y, double *tap_attn)
+{
+    if (!mask)
+        return ORC_E_ARG;
+    const orc_mask M = {mask, mask_heads, stride_row, stride_head, stride_batch};
+    return layer_step(L, W, x, cache_k, cache_v, NULL, NULL, capacity, cache_pos, B, R, &M, out,
+                      tap_y, tap_attn);
 }
 
 /* The layer step over a Bf16KTurbo4V cache: K as in orc_layer_step, V as
@@ -858,8 +920,8 @@ int orc_layer_step_turbo4v(const orc_layer *L, const orc_weights *W, const doubl
 {
     if (!v_codes || !v_scales)
         return ORC_E_ARG;
-    return layer_step(L, W, x, cache_k, NULL, v_codes, v_scales, capacity, cache_pos, B, R, out,
-                      tap_y, tap_attn);
+    return layer_step(L, W, x, cache_k, NULL, v_codes, v_scales, capacity, cache_pos, B, R, NULL,
+                      out, tap_y, tap_attn);
 }
 
 /* ------------------------------------------------------ decoder block */
