@@ -243,6 +243,31 @@ gattn_status gattn_layer_poll_status(gattn_layer *layer, gattn_stream stream);
 /* Ask the next steps to also write the taps (NULL or all-NULL turns them off). */
 gattn_status gattn_layer_set_taps(gattn_layer *layer, const gattn_taps *taps);
 
+/*
+ * An attention mask for the following steps (DS4Server issue 113: the verify
+ * route's broadcast and head-specific masks), device bytes, borrowed:
+ *   byte mask[b*stride_batch + hm*stride_head + r*stride_row + t]
+ * nonzero = row r of sequence b may attend cache position t; hm = 0 for a
+ * broadcast mask (heads == 1), the query head for a head-specific one
+ * (heads == num_heads).  A mask replaces the causal rule: row r attends the
+ * marked positions t < cache_pos[b] + q_len (positions >= `positions` are not
+ * attended and never read); a row with no position left gives a zero attention
+ * row.  Strides in bytes; stride_row >= positions.  The step refuses
+ * (GATTN_E_UNSUPPORTED) a head-specific mask when the head-chunked verify route
+ * applies (it hands the mask unchanged to every head chunk, where only a
+ * broadcast mask fits) and any mask on GATTN_PATH_FUSED.  The contents may
+ * change between steps (read at run time, graph-capturable).
+ */
+typedef struct gattn_mask {
+    const uint8_t *mask;
+    int32_t heads;
+    int32_t positions;
+    int64_t stride_row, stride_head, stride_batch;
+} gattn_mask;
+
+/* Set (or with NULL / mask->mask == NULL clear) the attention mask. */
+gattn_status gattn_layer_set_mask(gattn_layer *layer, const gattn_mask *mask);
+
 void gattn_layer_destroy(gattn_layer *layer);
 void gattn_kv_destroy(gattn_kv *kv);
 

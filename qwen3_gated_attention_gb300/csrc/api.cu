@@ -185,12 +185,13 @@ struct gattn_layer {
     unsigned *sync = nullptr;
     float *ss_part = nullptr;              // decoder-block post-norm: per-CTA sums of squares
     unsigned *post_ticket = nullptr;
-    // Bf16KTurbo4V caches: decision tables (host copy, passed by value) and the
-    // byte -> fp16 level pair table the attention dequantizes with
+    // Bf16KTurbo4V caches: decision tables (passed by value) and the bytes of
+    // the 8 positive fp16 levels the attention dequantizes with
     TurboTables tq{};
-    uint32_t *tq_lut = nullptr;
+    uint32_t tq_tl[2] = {0, 0}, tq_th[2] = {0, 0};
     int s_cnt_a = 0, s_rdy_a = 0, s_seg = 0, s_cnt_o = 0, nsync = 0;
     gattn_taps taps{};
+    gattn_mask mask{};                     // attention mask of the following steps (mask.mask null: causal)
     bool weights_set = false;
     int launches = 0;
     bool pdl = true;
@@ -385,16 +386,13 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
         std::memcpy(L->tq.lv, lv, sizeof lv);
         std::memcpy(L->tq.th, th, sizeof th);
         L->tq.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.head_dim));
-        uint32_t lut[256];
-        for (int b = 0; b < 256; ++b) {
-            const __half lo = __float2half_rn(lv[b & 15]), hi = __float2half_rn(lv[b >> 4]);
-            uint16_t l16, h16;
-            std::memcpy(&l16, &lo, 2);
-            std::memcpy(&h16, &hi, 2);
-            lut[b] = (uint32_t)l16 | ((uint32_t)h16 << 16);
+        for (int m = 0; m < 8; ++m) {
+            const __half h = __float2half_rn(lv[8 + m]);
+            uint16_t h16;
+            std::memcpy(&h16, &h, 2);
+            L->tq_tl[m >> 2] |= (uint32_t)(h16 & 0xFF) << (8 * (m & 3));
+            L->tq_th[m >> 2] |= (uint32_t)(h16 >> 8) << (8 * (m & 3));
         }
-        TRY(cudaMalloc(&L->tq_lut, sizeof lut));
-        TRY(cudaMemcpy(L->tq_lut, lut, sizeof lut, cudaMemcpyHostToDevice));
     }
     {
         const int gmax = *std::max_element(L->po.grid, L->po.grid + 3);
@@ -447,7 +445,7 @@ void gattn_layer_destroy(gattn_layer *L)
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq,
                     L->q_norm, L->k_norm, L->part_a,  L->part_o,  L->sync,
-                    L->ss_part, L->post_ticket, L->tq_lut};
+                    L->ss_part, L->post_ticket};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -610,6 +608,24 @@ gattn_status gattn_layer_set_taps(gattn_layer *L, const gattn_taps *t)
     return GATTN_OK;
 }
 
+gattn_status gattn_layer_set_mask(gattn_layer *L, const gattn_mask *m)
+{
+    if (!L)
+        return fail(GATTN_E_INVALID_ARG, "layer is NULL");
+    if (!m || !m->mask) {
+        L->mask = gattn_mask{};
+        return GATTN_OK;
+    }
+    if (m->heads != 1 && m->heads != L->cfg.num_heads)
+        return fail(GATTN_E_INVALID_ARG, "mask heads must be 1 or num_heads (%d), got %d",
+                    (int)L->cfg.num_heads, (int)m->heads);
+    if (m->positions <= 0 || m->stride_row < m->positions || m->stride_head < 0 ||
+        m->stride_batch < 0)
+        return fail(GATTN_E_INVALID_ARG, "bad mask row length or strides");
+    L->mask = *m;
+    return GATTN_OK;
+}
+
 int32_t gattn_layer_launches_per_step(const gattn_layer *L) { return L ? L->launches : -1; }
 
 gattn_status gattn_layer_set_path(gattn_layer *L, int32_t path)
@@ -707,6 +723,14 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
         return fail(GATTN_E_UNSUPPORTED, "the one-kernel path runs no decoder-block steps");
     if (L->path == GATTN_PATH_FUSED && kv->turbo)
         return fail(GATTN_E_UNSUPPORTED, "the one-kernel path reads bf16 V caches only");
+    if (L->path == GATTN_PATH_FUSED && L->mask.mask)
+        return fail(GATTN_E_UNSUPPORTED, "the one-kernel path runs causal steps only");
+    // the head-chunked verify route hands the mask unchanged to each head chunk:
+    // a broadcast mask fits every chunk, a mask over all heads does not
+    if (L->mask.mask && L->mask.heads > 1 && nchunks > c.num_kv_heads)
+        return fail(GATTN_E_UNSUPPORTED,
+                    "a head-specific mask cannot take the head-chunked verify route "
+                    "(q_len %d, %d query heads per KV head)", (int)q_len, (int)L->gqa);
     if (L->path == GATTN_PATH_FUSED) {
         // x arrives by bulk copy: 16-byte alignment
         bool ok = L->fused_ok && Ma <= 8 && batch <= kFMaxB && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
@@ -889,6 +913,14 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     t.group_o = L->po.group;
     t.tap_attn = L->taps.attn;
     t.status = L->status;
+    if (L->mask.mask) {
+        t.mask = L->mask.mask;
+        t.mask_heads = L->mask.heads;
+        t.mask_len = L->mask.positions;
+        t.mask_row = L->mask.stride_row;
+        t.mask_head = L->mask.stride_head;
+        t.mask_batch = L->mask.stride_batch;
+    }
     if (kv->turbo) {
         t.vq = 1;
         t.vq_codes = static_cast<const uint8_t *>(kv->tdesc.v_codes);
@@ -897,7 +929,10 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
         t.cq_batch = kv->tdesc.code_stride_batch;
         t.sq_head = kv->tdesc.scale_stride_head;
         t.sq_batch = kv->tdesc.scale_stride_batch;
-        t.vq_lut = L->tq_lut;
+        t.vq_tl[0] = L->tq_tl[0];
+        t.vq_tl[1] = L->tq_tl[1];
+        t.vq_th[0] = L->tq_th[0];
+        t.vq_th[1] = L->tq_th[1];
         t.inv_sqrt_d = L->tq.inv_sqrt_d;
     }
     CUDA_TRY(mark(2));

@@ -21,7 +21,7 @@ struct AttnSmem {
         VQ ? ((kVCodeBytes + kAttnTile * DB * 4 + 1023) & ~1023) : kTileBytes;
     static constexpr int kStageBytes = kTileBytes + kVBytes;  // K + V
     static constexpr int kDqBytes = VQ ? kTileBytes : 0;      // Turbo4: dequantized fp16 V tile
-    static constexpr int kLutBytes = VQ ? 1024 : 0;           // Turbo4: byte -> level pair
+    static constexpr int kLutBytes = 0;
     static constexpr int kQBytes = MT * 16 * DB * 64 * 2;
     static constexpr int kPBytes = MT * 16 * 128;             // rows x 64 tokens bf16
     // as many K/V stages (2 .. kAttnStages) as fit beside the rest in 227 KB
@@ -55,7 +55,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *qs = smem + L::kQ;
     uint8_t *dq = smem + L::kDq;                                // Turbo4 only
-    uint32_t *lut = reinterpret_cast<uint32_t *>(smem + L::kLut);
     uint8_t *ps = smem + L::kP;
     float *red_max = reinterpret_cast<float *>(smem + L::kRedMax);
     float *red_l = reinterpret_cast<float *>(smem + L::kRedL);
@@ -177,10 +176,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
 
     // --------------------------------------------------------------- consumers
-    if constexpr (VQ) {
-        for (int i = tid; i < 256; i += kAttnWarps * 32)
-            lut[i] = a.vq_lut[i];   // a layer constant; read by all after the first barrier
-    }
     pdl_wait();                 // q rows come from the q|k|v projection
     const int g = lane >> 2, cq = lane & 3;
     long long it = 0;
@@ -248,6 +243,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             float sc[MT][4];
             float scs[SPLIT][MT][4];
             const bool has_tok = ok && (warp * 8 < ntok);
+            // attention mask: this lane's score bytes (bit mt * 4 + e), loaded before
+            // the q K^T loop so that their latency hides behind it
+            uint32_t mkeep = 0;
+            if (a.mask && has_tok) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = mt * 16 + g + ((e & 2) ? 8 : 0);
+                        const int t = t0 + warp * 8 + 2 * cq + (e & 1);
+                        if (i < nrows && t < Lb && t < a.mask_len) {
+                            const int hh = h0 + i / a.R, rr = i % a.R;
+                            const uint8_t *mp = a.mask + p.b * a.mask_batch +
+                                                (a.mask_heads > 1 ? hh : 0) * a.mask_head +
+                                                rr * a.mask_row + t;
+                            if (__ldg(mp))
+                                mkeep |= 1u << (mt * 4 + e);
+                        }
+                    }
+            }
 #pragma unroll
             for (int q = 0; q < SPLIT; ++q)
 #pragma unroll
@@ -295,7 +310,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int e = 0; e < 4; ++e) {
                     const int i = mt * 16 + g + ((e & 2) ? 8 : 0);
                     const int t = t0 + warp * 8 + 2 * cq + (e & 1);
-                    const bool vis = has_tok && i < nrows && t <= p0 + (i % a.R);
+                    const bool vis = has_tok && i < nrows &&
+                                     (a.mask ? ((mkeep >> (mt * 4 + e)) & 1u) != 0u
+                                             : t <= p0 + (i % a.R));
                     sc[mt][e] = vis ? sc[mt][e] * a.scale_log2 : -INFINITY;
                 }
 #pragma unroll
@@ -312,7 +329,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             //      bf16 V tile); every warp has finished the previous tile's P V
             if constexpr (VQ) {
                 if (ok) {
-                    const uint8_t *cst = vst, *sst = vst + L::kVCodeBytes;
+                    const uint32_t cst = smem_u32(vst), sst = cst + L::kVCodeBytes;
+                    const uint32_t dq_a = smem_u32(dq);
+                    const uint32_t lvl_lo[2] = {a.vq_tl[0], a.vq_tl[1]}, lvl_hi[2] = {a.vq_th[0], a.vq_th[1]};
                     // A 16-byte store is served eight lanes at a time; those lanes
                     // share a token and take its eight 32-column pieces c, so each
                     // lane writes its four 8-column chunks in an order rotated by c:
@@ -325,9 +344,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         uint4 cb = make_uint4(0, 0, 0, 0);
                         __half2 s0 = __float2half2_rn(0.f), s1 = s0;
                         if (live) {
-                            cb = *reinterpret_cast<const uint4 *>(cst + tl * (DB * 32) + c * 16);
-                            const uint32_t sb = *reinterpret_cast<const uint16_t *>(
-                                sst + tl * (DB * 4) + c * 2);
+                            cb = lds_v4(cst + tl * (DB * 32) + c * 16);
+                            const uint32_t sb = lds_u16(sst + tl * (DB * 4) + c * 2);
                             s0 = __half2half2(e4m3_to_half((uint8_t)(sb & 0xFF)));
                             s1 = __half2half2(e4m3_to_half((uint8_t)(sb >> 8)));
                         }
@@ -337,16 +355,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             const uint32_t wq = q == 0 ? cb.x : (q == 1 ? cb.y : (q == 2 ? cb.z : cb.w));
                             const __half2 sc = q < 2 ? s0 : s1;      // groups 2c, 2c + 1
                             uint32_t o[4];
+                            turbo4_levels8(wq, lvl_lo, lvl_hi, o);
 #pragma unroll
                             for (int k2 = 0; k2 < 4; ++k2) {
-                                const uint32_t pr = live ? lut[(wq >> (8 * k2)) & 0xFF] : 0u;
-                                const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&pr), sc);
+                                const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&o[k2]), sc);
                                 o[k2] = *reinterpret_cast<const uint32_t *>(&v);
                             }
                             const int ch = 4 * c + q;                   // 8-column chunk of the row
-                            *reinterpret_cast<uint4 *>(dq + (ch >> 3) * kDBox + tl * 128 +
-                                                       (((ch & 7) ^ (tl & 7)) << 4)) =
-                                make_uint4(o[0], o[1], o[2], o[3]);
+                            sts_v4(dq_a + (ch >> 3) * kDBox + tl * 128 + (((ch & 7) ^ (tl & 7)) << 4),
+                                   o[0], o[1], o[2], o[3]);
                         }
                     }
                 }

@@ -247,8 +247,13 @@ struct AttnArgs {
     int vq;
     const uint8_t *vq_codes, *vq_scales;
     long long cq_head, cq_batch, sq_head, sq_batch;   // byte strides
-    const uint32_t *vq_lut;      // [256] half2 (level of the low nibble, of the high nibble)
+    uint32_t vq_tl[2], vq_th[2]; // low / high bytes of the 8 positive fp16 levels (turbo.cuh)
     float inv_sqrt_d;
+    // attention mask (null: causal): byte (b, head or 0, row r, position t),
+    // nonzero = attend; replaces the causal rule; positions >= mask_len unread
+    const uint8_t *mask;
+    int mask_heads, mask_len;
+    long long mask_row, mask_head, mask_batch;
 };
 
 cudaError_t launch_attn(int MT, int DB, const AttnArgs &a, const CUtensorMap &kmap,

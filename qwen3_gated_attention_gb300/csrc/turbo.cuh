@@ -105,6 +105,25 @@ __device__ __forceinline__ void turbo4_quantize_warp(float (&x)[8], int per, int
     }
 }
 
+// Levels of 8 codes at once, in registers: w holds 8 nibbles (code j in
+// nibble j).  The codebook is symmetric (level n = -level 15 - n), so nibble n
+// names magnitude m = n - 8 (n >= 8) or 7 - n (n < 8) of the 8 positive fp16
+// levels, whose low bytes are tl[0..1] and high bytes th[0..1] (byte m of the
+// pair); byte permutes gather them and the sign bit comes from the nibble.
+// o[k] = the fp16 pair (level of nibble 2k, level of nibble 2k + 1).
+__device__ __forceinline__ void turbo4_levels8(uint32_t w, const uint32_t (&tl)[2],
+                                               const uint32_t (&th)[2], uint32_t (&o)[4])
+{
+    const uint32_t neg = ~w & 0x88888888u;                      // nibble < 8: negative
+    const uint32_t m = (w ^ ((neg >> 3) * 7u)) & 0x77777777u;   // magnitude index
+    const uint32_t lo0 = __byte_perm(tl[0], tl[1], m), hi0 = __byte_perm(th[0], th[1], m);
+    const uint32_t lo1 = __byte_perm(tl[0], tl[1], m >> 16), hi1 = __byte_perm(th[0], th[1], m >> 16);
+    o[0] = __byte_perm(lo0, hi0, 0x5140) ^ (((neg << 12) & 0x8000u) | ((neg << 24) & 0x80000000u));
+    o[1] = __byte_perm(lo0, hi0, 0x7362) ^ (((neg << 4) & 0x8000u) | ((neg << 16) & 0x80000000u));
+    o[2] = __byte_perm(lo1, hi1, 0x5140) ^ (((neg >> 4) & 0x8000u) | ((neg << 8) & 0x80000000u));
+    o[3] = __byte_perm(lo1, hi1, 0x7362) ^ (((neg >> 12) & 0x8000u) | (neg & 0x80000000u));
+}
+
 // fp16 value of an E4M3 byte (exact: every E4M3 value is an fp16 value)
 __device__ __forceinline__ __half e4m3_to_half(uint8_t b)
 {

@@ -134,6 +134,16 @@ class DeviceLayer:
         gattn.layer_set_taps(self.h, y.data_ptr() if y is not None else None,
                              attn.data_ptr() if attn is not None else None)
 
+    def set_mask(self, mask: torch.Tensor | None):
+        """mask: uint8 [B][1 or H][R][T] on the device (None clears it)."""
+        if mask is None:
+            gattn.layer_set_mask(self.h, None)
+            return
+        assert mask.dtype == torch.uint8 and mask.dim() == 4 and mask.is_contiguous()
+        self._mask = mask
+        gattn.layer_set_mask(self.h, mask.data_ptr(), mask.shape[1], mask.shape[3],
+                             (mask.stride(2), mask.stride(1), mask.stride(0)))
+
     def poll(self):
         gattn.layer_poll_status(self.h, torch.cuda.current_stream(self.device).cuda_stream)
 

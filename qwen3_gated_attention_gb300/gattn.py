@@ -32,7 +32,7 @@ EXPORTS = (
     "gattn_unpack_codes_device", "gattn_layer_dequant_device", "gattn_head_chunk_plan",
     "gattn_layer_launches_per_step", "gattn_layer_set_events", "gattn_layer_dequant_device_static",
     "gattn_layer_set_path", "gattn_layer_step_block", "gattn_kv_register_turbo4v",
-    "gattn_turbo4_codebook", "gattn_turbo4_quantize_device",
+    "gattn_turbo4_codebook", "gattn_turbo4_quantize_device", "gattn_layer_set_mask",
 )
 
 
@@ -72,6 +72,11 @@ class gattn_kv_turbo4v_desc(C.Structure):
                 ("k_stride_batch", C.c_int64), ("code_stride_head", C.c_int64),
                 ("code_stride_batch", C.c_int64), ("scale_stride_head", C.c_int64),
                 ("scale_stride_batch", C.c_int64)]
+
+
+class gattn_mask(C.Structure):
+    _fields_ = [("mask", C.c_void_p), ("heads", C.c_int32), ("positions", C.c_int32),
+                ("stride_row", C.c_int64), ("stride_head", C.c_int64), ("stride_batch", C.c_int64)]
 
 
 class gattn_taps(C.Structure):
@@ -118,13 +123,15 @@ def lib():
         L.gattn_kv_register_turbo4v.argtypes = [p, C.POINTER(gattn_kv_turbo4v_desc), C.POINTER(p)]
         L.gattn_turbo4_codebook.argtypes = [p, p]
         L.gattn_turbo4_quantize_device.argtypes = [p, i64, i32, p, p, p]
+        L.gattn_layer_set_mask.argtypes = [p, C.POINTER(gattn_mask)]
         for name in ("gattn_cfg_validate", "gattn_layer_create", "gattn_layer_set_weights",
                      "gattn_kv_register", "gattn_layer_step", "gattn_layer_poll_status",
                      "gattn_layer_set_taps", "gattn_pack_affine_host", "gattn_unpack_codes_device",
                      "gattn_layer_dequant_device", "gattn_layer_set_events",
                      "gattn_layer_dequant_device_static", "gattn_layer_set_path",
                      "gattn_layer_step_block", "gattn_kv_register_turbo4v",
-                     "gattn_turbo4_codebook", "gattn_turbo4_quantize_device"):
+                     "gattn_turbo4_codebook", "gattn_turbo4_quantize_device",
+                     "gattn_layer_set_mask"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -200,6 +207,17 @@ def kv_register_turbo4v(layer: int, k: int, v_codes: int, v_scales: int, batch: 
     h = C.c_void_p()
     _check(lib().gattn_kv_register_turbo4v(layer, C.byref(d), C.byref(h)))
     return h.value
+
+
+def layer_set_mask(layer: int, mask: int | None, heads: int = 1, positions: int = 0,
+                   strides=(0, 0, 0)) -> None:
+    """Attention mask of the following steps (device bytes; None clears it).
+    strides: (row, head, batch) in bytes."""
+    if not mask:
+        _check(lib().gattn_layer_set_mask(layer, None))
+        return
+    m = gattn_mask(mask, heads, positions, *strides)
+    _check(lib().gattn_layer_set_mask(layer, C.byref(m)))
 
 
 def turbo4_codebook():
