@@ -434,7 +434,9 @@ def our_arm(args, spec):
     peak, peak_kind = load_peaks()
     achieved = kernel_bytes[dominant] / (kernel_avg_ms[dominant] / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(dominant, spec.name),
+                "frac": achieved / peak,
+                "traffic": profiled_traffic(dominant, spec.name + ("_turbo4v" if args.kv == "turbo4v"
+                                                                   else "")),
                 "kernel": dominant, "peak_source": peak_kind,
                 "kernel_avg_us": {n: 1e3 * v for n, v in kernel_avg_ms.items()},
                 "kernel_bytes": kernel_bytes}
