@@ -72,6 +72,11 @@ class _OrcLayer(C.Structure):
                 ("head_chunk", C.c_int32), ("mutate", C.c_int32)]
 
 
+class _OrcStepExt(C.Structure):
+    _fields_ = [("v_codes", _p), ("v_scales", _p), ("mask", _p), ("mask_heads", C.c_int32),
+                ("mask_row", _i64), ("mask_head", _i64), ("mask_batch", _i64)]
+
+
 class _OrcWeights(C.Structure):
     _fields_ = [("packed", _p * 4), ("scales", _p * 4), ("biases", _p * 4),
                 ("q_norm", _p), ("k_norm", _p)]
@@ -109,6 +114,10 @@ def _declare(L):
     L.orc_turbo4_dequant_rows.argtypes = [_p, _p, _i64, _i, _i, _p]
     L.orc_layer_step_masked.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _p, _p,
                                         _i, _p, _i, _i, _p, _i, _i64, _i64, _i64, _p, _p, _p]
+    L.orc_layer_step_ext.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _p, _p, _i,
+                                     _p, _i, _i, C.POINTER(_OrcStepExt), _p, _p, _p]
+    L.orc_block_step_ext.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _i, _p, _p,
+                                     _p, _p, _i, _p, _i, _i, C.POINTER(_OrcStepExt), _p, _p]
     L.orc_layer_step_turbo4v.argtypes = [C.POINTER(_OrcLayer), C.POINTER(_OrcWeights), _p, _p, _p,
                                          _p, _i, _p, _i, _i, _p, _p, _p]
 
@@ -388,9 +397,46 @@ def layer_step_turbo4v(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.
     return out
 
 
+def _step_ext(turbo, mask, keep):
+    """orc_step_ext for a Turbo4 V cache (codes, scales) and/or a mask [B][1|H][R][T]."""
+    e = _OrcStepExt()
+    if turbo is not None:
+        codes, scales = turbo
+        assert codes.dtype == np.uint8 and scales.dtype == np.uint8
+        assert codes.flags["C_CONTIGUOUS"] and scales.flags["C_CONTIGUOUS"]
+        e.v_codes, e.v_scales = _ptr(codes), _ptr(scales)
+    if mask is not None:
+        mk = np.ascontiguousarray(mask, np.uint8)
+        keep.append(mk)
+        e.mask, e.mask_heads = _ptr(mk), mk.shape[1]
+        e.mask_row, e.mask_head, e.mask_batch = mk.strides[2], mk.strides[1], mk.strides[0]
+    return e
+
+
+def layer_step_ext(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.ndarray, cache_v,
+                   cache_pos: np.ndarray, turbo=None, mask=None, head_chunk: bool = True,
+                   taps: bool = False):
+    """layer_step with the optional parts together: turbo = (codes, scales) of a
+    Bf16KTurbo4V cache (cache_v unused, may be None), mask as in layer_step."""
+    B, R, Hd = x.shape
+    L, Wt, keep = _layer_structs(spec, weights, head_chunk, "none")
+    x = np.ascontiguousarray(x, np.float64)
+    cp = np.ascontiguousarray(cache_pos, np.int32)
+    e = _step_ext(turbo, mask, keep)
+    out = np.zeros((B, R, Hd), np.float64)
+    H, Hk, d = spec.num_heads, spec.num_kv_heads, spec.head_dim
+    ty = np.zeros((B, R, 2 * H * d + 2 * Hk * d), np.float64) if taps else None
+    ta = np.zeros((B, R, H, d), np.float64) if taps else None
+    rc = lib().orc_layer_step_ext(C.byref(L), C.byref(Wt), _ptr(x), _ptr(cache_k), _ptr(cache_v),
+                                  cache_k.shape[2], _ptr(cp), B, R, C.byref(e), _ptr(out), _ptr(ty),
+                                  _ptr(ta))
+    _check(rc, "layer_step_ext")
+    return (out, ty, ta) if taps else out
+
+
 def block_step(spec, weights: OracleWeights, x: np.ndarray, input_ln: np.ndarray,
-               post_ln, cache_k: np.ndarray, cache_v: np.ndarray, cache_pos: np.ndarray,
-               head_chunk: bool = True):
+               post_ln, cache_k: np.ndarray, cache_v, cache_pos: np.ndarray,
+               head_chunk: bool = True, turbo=None, mask=None):
     """The decoder block around the layer ([atlas-mod] forward_full_attention:
     input RMSNorm -> layer -> residual add -> post-attention RMSNorm): returns
     out = x + layer(RMSNorm(x) * input_ln) and, when post_ln is given,
@@ -403,12 +449,15 @@ def block_step(spec, weights: OracleWeights, x: np.ndarray, input_ln: np.ndarray
     x = np.ascontiguousarray(x, np.float64)
     iw = np.ascontiguousarray(input_ln, np.uint16)
     pw = None if post_ln is None else np.ascontiguousarray(post_ln, np.uint16)
-    assert cache_k.flags["C_CONTIGUOUS"] and cache_v.flags["C_CONTIGUOUS"]
+    assert cache_k.flags["C_CONTIGUOUS"]
+    assert turbo is not None or cache_v.flags["C_CONTIGUOUS"]
+    e = _step_ext(turbo, mask, keep)
     cp = np.ascontiguousarray(cache_pos, np.int32)
     out = np.zeros((B, R, Hd), np.float64)
     on = np.zeros((B, R, Hd), np.float64) if pw is not None else None
-    rc = lib().orc_block_step(C.byref(L), C.byref(Wt), _ptr(x),
-                              1 if spec.x_dtype == "bf16" else 0, _ptr(iw), _ptr(pw), _ptr(cache_k),
-                              _ptr(cache_v), cache_k.shape[2], _ptr(cp), B, R, _ptr(out), _ptr(on))
+    rc = lib().orc_block_step_ext(C.byref(L), C.byref(Wt), _ptr(x),
+                                  1 if spec.x_dtype == "bf16" else 0, _ptr(iw), _ptr(pw),
+                                  _ptr(cache_k), _ptr(cache_v), cache_k.shape[2], _ptr(cp), B, R,
+                                  C.byref(e), _ptr(out), _ptr(on))
     _check(rc, "block_step")
     return out, on

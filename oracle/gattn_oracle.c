@@ -937,10 +937,43 @@ int orc_layer_step_turbo4v(const orc_layer *L, const orc_weights *W, const doubl
  * it to bf16 (a bf16 stream, as the engine's x_norm buffer), 0 keeps it exact
  * (an fp32 stream).  input_ln / post_ln are bf16 [hidden]; post_ln and
  * out_normed may be NULL.  Cache behaviour is that of orc_layer_step. */
-int orc_block_step(const orc_layer *L, const orc_weights *W, const double *x, int h_bf16,
-                   const uint16_t *input_ln, const uint16_t *post_ln,
-                   uint16_t *cache_k, uint16_t *cache_v, int capacity,
-                   const int32_t *cache_pos, int B, int R, double *out, double *out_normed)
+/* The layer step's optional parts together: a Bf16KTurbo4V V cache (v_codes
+ * and v_scales, else cache_v is a bf16 V cache) and an attention mask (mask
+ * NULL: causal; orc_mask above). */
+typedef struct orc_step_ext {
+    uint8_t *v_codes, *v_scales;
+    const uint8_t *mask;
+    int32_t mask_heads;
+    int64_t mask_row, mask_head, mask_batch;
+} orc_step_ext;
+
+int orc_layer_step_ext(const orc_layer *L, const orc_weights *W, const double *x,
+                       uint16_t *cache_k, uint16_t *cache_v, int capacity,
+                       const int32_t *cache_pos, int B, int R, const orc_step_ext *e,
+                       double *out, double *tap_y, double *tap_attn)
+{
+    orc_mask M;
+    const orc_mask *mp = NULL;
+    if (e && e->mask) {
+        M.m = e->mask;
+        M.heads = e->mask_heads;
+        M.stride_row = e->mask_row;
+        M.stride_head = e->mask_head;
+        M.stride_batch = e->mask_batch;
+        mp = &M;
+    }
+    uint8_t *vc = e ? e->v_codes : NULL, *vs = e ? e->v_scales : NULL;
+    if ((vc == NULL) != (vs == NULL))
+        return ORC_E_ARG;
+    return layer_step(L, W, x, cache_k, vc ? NULL : cache_v, vc, vs, capacity, cache_pos, B, R, mp,
+                      out, tap_y, tap_attn);
+}
+
+static int block_step(const orc_layer *L, const orc_weights *W, const double *x, int h_bf16,
+                      const uint16_t *input_ln, const uint16_t *post_ln,
+                      uint16_t *cache_k, uint16_t *cache_v, int capacity,
+                      const int32_t *cache_pos, int B, int R, const orc_step_ext *e,
+                      double *out, double *out_normed)
 {
     const int Hd = L->hidden;
     const int64_t M = (int64_t)B * R;
@@ -960,7 +993,7 @@ int orc_block_step(const orc_layer *L, const orc_weights *W, const double *x, in
     if (h_bf16)
         for (int64_t j = 0; j < M * Hd; ++j)
             h[j] = orc_bf16_to_double(orc_bf16_from_double(h[j]));
-    rc = orc_layer_step(L, W, h, cache_k, cache_v, capacity, cache_pos, B, R, y, NULL, NULL);
+    rc = orc_layer_step_ext(L, W, h, cache_k, cache_v, capacity, cache_pos, B, R, e, y, NULL, NULL);
     if (rc != ORC_OK)
         goto done;
     for (int64_t j = 0; j < M * Hd; ++j)
@@ -977,4 +1010,24 @@ int orc_block_step(const orc_layer *L, const orc_weights *W, const double *x, in
 done:
     free(w); free(h); free(y); free(rb);
     return rc;
+}
+
+int orc_block_step(const orc_layer *L, const orc_weights *W, const double *x, int h_bf16,
+                   const uint16_t *input_ln, const uint16_t *post_ln,
+                   uint16_t *cache_k, uint16_t *cache_v, int capacity,
+                   const int32_t *cache_pos, int B, int R, double *out, double *out_normed)
+{
+    return block_step(L, W, x, h_bf16, input_ln, post_ln, cache_k, cache_v, capacity, cache_pos, B,
+                      R, NULL, out, out_normed);
+}
+
+/* orc_block_step with the optional parts of orc_step_ext */
+int orc_block_step_ext(const orc_layer *L, const orc_weights *W, const double *x, int h_bf16,
+                       const uint16_t *input_ln, const uint16_t *post_ln,
+                       uint16_t *cache_k, uint16_t *cache_v, int capacity,
+                       const int32_t *cache_pos, int B, int R, const orc_step_ext *e,
+                       double *out, double *out_normed)
+{
+    return block_step(L, W, x, h_bf16, input_ln, post_ln, cache_k, cache_v, capacity, cache_pos, B,
+                      R, e, out, out_normed);
 }

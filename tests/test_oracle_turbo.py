@@ -273,3 +273,56 @@ def test_turbo_layer_step_ignores_stale_slots():
     out = orc.layer_step_turbo4v(spec, case.orc_weights, synth.x_values(spec, case.x),
                                  case.ck.copy(), codes, scales, case.pos)
     assert np.all(np.isfinite(out))
+
+
+def test_turbo_layer_step_with_a_mask_matches_numpy():
+    """A Turbo4 V cache and a broadcast mask together: the attention tap is the
+    numpy attention over the dequantized rows with the mask's positions."""
+    spec = synth.WORKLOADS["tiny"].with_(batch=2, q_len=3, cache_pos=None, length_range=(20, 90),
+                                         x_dtype="bf16")
+    case, codes, scales = _turbo_case(spec)
+    rng = np.random.default_rng(21)
+    T = int(case.pos.max()) + spec.q_len
+    mask = (rng.random((spec.batch, 1, spec.q_len, T)) < 0.6).astype(np.uint8)
+    kc = case.ck.copy()
+    out, ty, ta = orc.layer_step_ext(spec, case.orc_weights, synth.x_values(spec, case.x), kc, None,
+                                     case.pos, turbo=(codes, scales), mask=mask, taps=True)
+    vd = orc.turbo4_dequant_rows(codes, scales)
+    B, R = spec.batch, spec.q_len
+    H, Hk, d = spec.num_heads, spec.num_kv_heads, spec.head_dim
+    rd = orc.rotary_dims(d, spec.partial_rotary_factor)
+    qn_w = bf16_bits_to_f32(synth.norm_weights_bf16(spec)[0]).astype(np.float64)
+    for b in range(B):
+        p0 = int(case.pos[b])
+        for h in range(H):
+            K = bf16_bits_to_f32(kc[b, h // (H // Hk), :p0 + R]).astype(np.float64)
+            for r in range(R):
+                q = orc.rope(orc.rms_norm(ty[b, r, h * 2 * d:h * 2 * d + d], qn_w,
+                                          float(np.float32(spec.rms_eps))), rd, p0 + r,
+                             float(np.float32(spec.rope_theta)))
+                keep = mask[b, 0, r, :p0 + R] != 0
+                if not keep.any():
+                    assert np.all(ta[b, r, h] == 0)
+                    continue
+                s = np.where(keep, K @ q / np.sqrt(d), -np.inf)
+                p = np.exp(s - s.max())
+                want = (p / p.sum()) @ vd[b, h // (H // Hk), :p0 + R]
+                assert np.allclose(ta[b, r, h], want, rtol=1e-10, atol=1e-12)
+
+
+def test_block_over_a_turbo_cache_reduces_to_the_turbo_layer():
+    """input_ln = 1 on bf16 rows of unit RMS: the block's layer part is the
+    Turbo4 layer step on x itself (rounding h to bf16 gives back x)."""
+    from tests.test_oracle_pins import _unit_rms_bf16_rows
+    spec = synth.WORKLOADS["tiny"].with_(batch=2, q_len=2, cache_pos=None, length_range=(20, 90),
+                                         x_dtype="bf16")
+    case, codes, scales = _turbo_case(spec)
+    x = _unit_rms_bf16_rows(spec.batch, spec.q_len, spec.hidden, 4)
+    ones = np.full(spec.hidden, 0x3F80, np.uint16)
+    k1, c1, s1 = case.ck.copy(), codes.copy(), scales.copy()
+    out, _ = orc.block_step(spec, case.orc_weights, x, ones, None, k1, None, case.pos,
+                            turbo=(c1, s1))
+    k2, c2, s2 = case.ck.copy(), codes.copy(), scales.copy()
+    ref = orc.layer_step_ext(spec, case.orc_weights, x, k2, None, case.pos, turbo=(c2, s2))
+    assert np.allclose(out - x, ref, rtol=1e-12, atol=1e-14)
+    assert np.array_equal(c1, c2) and np.array_equal(s1, s2) and np.array_equal(k1, k2)
