@@ -73,7 +73,8 @@ class _OrcLayer(C.Structure):
 
 
 class _OrcStepExt(C.Structure):
-    _fields_ = [("v_codes", _p), ("v_scales", _p), ("mask", _p), ("mask_heads", C.c_int32),
+    _fields_ = [("v_codes", _p), ("v_scales", _p), ("k_codes", _p), ("k_scales", _p),
+                ("mask", _p), ("mask_heads", C.c_int32),
                 ("mask_row", _i64), ("mask_head", _i64), ("mask_batch", _i64)]
 
 
@@ -397,14 +398,17 @@ def layer_step_turbo4v(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.
     return out
 
 
-def _step_ext(turbo, mask, keep):
-    """orc_step_ext for a Turbo4 V cache (codes, scales) and/or a mask [B][1|H][R][T]."""
+def _step_ext(turbo, mask, keep, turbo_k=None):
+    """orc_step_ext for a Turbo4 V cache (codes, scales), the K planes of a
+    symmetric Turbo4 cache, and/or a mask [B][1|H][R][T]."""
     e = _OrcStepExt()
-    if turbo is not None:
-        codes, scales = turbo
-        assert codes.dtype == np.uint8 and scales.dtype == np.uint8
-        assert codes.flags["C_CONTIGUOUS"] and scales.flags["C_CONTIGUOUS"]
-        e.v_codes, e.v_scales = _ptr(codes), _ptr(scales)
+    for planes, names in ((turbo, ("v_codes", "v_scales")), (turbo_k, ("k_codes", "k_scales"))):
+        if planes is not None:
+            codes, scales = planes
+            assert codes.dtype == np.uint8 and scales.dtype == np.uint8
+            assert codes.flags["C_CONTIGUOUS"] and scales.flags["C_CONTIGUOUS"]
+            setattr(e, names[0], _ptr(codes))
+            setattr(e, names[1], _ptr(scales))
     if mask is not None:
         mk = np.ascontiguousarray(mask, np.uint8)
         keep.append(mk)
@@ -413,23 +417,25 @@ def _step_ext(turbo, mask, keep):
     return e
 
 
-def layer_step_ext(spec, weights: OracleWeights, x: np.ndarray, cache_k: np.ndarray, cache_v,
+def layer_step_ext(spec, weights: OracleWeights, x: np.ndarray, cache_k, cache_v,
                    cache_pos: np.ndarray, turbo=None, mask=None, head_chunk: bool = True,
-                   taps: bool = False):
+                   taps: bool = False, turbo_k=None):
     """layer_step with the optional parts together: turbo = (codes, scales) of a
-    Bf16KTurbo4V cache (cache_v unused, may be None), mask as in layer_step."""
+    Bf16KTurbo4V cache (cache_v unused, may be None); turbo_k = the K planes of
+    the symmetric Turbo4 cache ([atlas-mod] MetalKvDtype::Turbo4; needs turbo,
+    cache_k unused); mask as in layer_step.  Planes are updated in place."""
     B, R, Hd = x.shape
     L, Wt, keep = _layer_structs(spec, weights, head_chunk, "none")
     x = np.ascontiguousarray(x, np.float64)
     cp = np.ascontiguousarray(cache_pos, np.int32)
-    e = _step_ext(turbo, mask, keep)
+    e = _step_ext(turbo, mask, keep, turbo_k)
+    cap = (turbo_k[0] if turbo_k is not None else cache_k).shape[2]
     out = np.zeros((B, R, Hd), np.float64)
     H, Hk, d = spec.num_heads, spec.num_kv_heads, spec.head_dim
     ty = np.zeros((B, R, 2 * H * d + 2 * Hk * d), np.float64) if taps else None
     ta = np.zeros((B, R, H, d), np.float64) if taps else None
     rc = lib().orc_layer_step_ext(C.byref(L), C.byref(Wt), _ptr(x), _ptr(cache_k), _ptr(cache_v),
-                                  cache_k.shape[2], _ptr(cp), B, R, C.byref(e), _ptr(out), _ptr(ty),
-                                  _ptr(ta))
+                                  cap, _ptr(cp), B, R, C.byref(e), _ptr(out), _ptr(ty), _ptr(ta))
     _check(rc, "layer_step_ext")
     return (out, ty, ta) if taps else out
 

@@ -603,9 +603,11 @@ int orc_turbo4_dequant_rows(const uint8_t *codes, const uint8_t *scales, int64_t
     return ORC_OK;
 }
 
-/* sdpa_row over V rows given in float64 (a dequantized cache) */
+/* sdpa_row over V rows given in float64 (a dequantized cache); K rows from
+ * the bf16 cache kc, or from float64 rows kd (a dequantized Turbo4 K cache) */
 static void sdpa_row_vd(const double *q, const uint16_t *kc, int64_t tstride, const double *vd,
-                        int d, int last, const uint8_t *keep, double *o, double *scores)
+                        int d, int last, const uint8_t *keep, double *o, double *scores,
+                        const double *kd)
 {
     double scale = 1.0 / sqrt((double)d);
     double mx = -INFINITY;
@@ -614,10 +616,15 @@ static void sdpa_row_vd(const double *q, const uint16_t *kc, int64_t tstride, co
             scores[t] = -INFINITY;
             continue;
         }
-        const uint16_t *kt = kc + (int64_t)t * tstride;
         double s = 0.0;
-        for (int j = 0; j < d; ++j)
-            s += q[j] * orc_bf16_to_double(kt[j]);
+        if (kd) {
+            for (int j = 0; j < d; ++j)
+                s += q[j] * kd[(int64_t)t * d + j];
+        } else {
+            const uint16_t *kt = kc + (int64_t)t * tstride;
+            for (int j = 0; j < d; ++j)
+                s += q[j] * orc_bf16_to_double(kt[j]);
+        }
         s *= scale;
         scores[t] = s;
         if (s > mx) mx = s;
@@ -663,12 +670,20 @@ typedef struct orc_mask {
 
 #define ORC_E_MASK 3
 
+/* k_codes / k_scales (with v_codes / v_scales): the symmetric Turbo4 cache of
+ * [atlas-mod] MetalKvDtype::Turbo4, K quantized like V (same rotation, codebook
+ * and scales) from the bf16 row of the normed, rotated key; scores then use
+ * the dequantized K rows.  cache_k is unused then. */
 static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                       uint16_t *cache_k, uint16_t *cache_v, uint8_t *v_codes, uint8_t *v_scales,
+                      uint8_t *k_codes, uint8_t *k_scales,
                       int capacity, const int32_t *cache_pos, int B, int R, const orc_mask *M,
                       double *out, double *tap_y, double *tap_attn)
 {
     const int turbo = v_codes != NULL;
+    const int kturbo = k_codes != NULL;
+    if (kturbo && (!turbo || !k_scales))
+        return ORC_E_ARG;
     const int Hd = L->hidden, H = L->num_heads, Hk = L->num_kv_heads, d = L->head_dim;
     if (Hd <= 0 || H <= 0 || Hk <= 0 || d <= 0 || H % Hk || B <= 0 || R <= 0)
         return ORC_E_ARG;
@@ -701,7 +716,7 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
     double *vnew = (double *)malloc((size_t)((int64_t)R * Hk * d) * sizeof(double));
     int32_t *cf = (int32_t *)malloc((size_t)H * sizeof(int32_t));
     int32_t *cl = (int32_t *)malloc((size_t)H * sizeof(int32_t));
-    double *vdq = NULL, cbk[16];
+    double *vdq = NULL, *kdq = NULL, cbk[16];
     uint16_t *vb16 = (uint16_t *)malloc((size_t)d * sizeof(uint16_t));
     if (turbo) {
         if (d < 16 || d > 1024 || (d & (d - 1))) {
@@ -710,9 +725,11 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
         }
         orc_turbo4_codebook(cbk);
         vdq = (double *)malloc((size_t)capacity * d * sizeof(double) + 8);
+        if (kturbo)
+            kdq = (double *)malloc((size_t)capacity * d * sizeof(double) + 8);
     }
     if (!wrow || !y || !qn || !attn || !ga || !tmp || !nq || !nk || !scores || !knew || !vnew || !cf ||
-        !cl || !vb16 || (turbo && !vdq)) {
+        !cl || !vb16 || (turbo && !vdq) || (kturbo && !kdq)) {
         rc = ORC_E_ARG;
         goto done;
     }
@@ -748,7 +765,7 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
         if (tap_y)
             memcpy(tap_y + (int64_t)b * R * Ny, y, (size_t)(R * Ny) * sizeof(double));
 
-        uint16_t *kcb = cache_k + (int64_t)b * Hk * capacity * d;
+        uint16_t *kcb = kturbo ? NULL : cache_k + (int64_t)b * Hk * capacity * d;
         uint16_t *vcb = turbo ? NULL : cache_v + (int64_t)b * Hk * capacity * d;
         for (int r = 0; r < R; ++r) {
             const double *yr = y + (int64_t)r * Ny;
@@ -776,11 +793,19 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                     orc_rms_norm(ksrc, d, nk, L->rms_eps, kr);
                 rope_partial(kr, d, rd, pos, L->rope_theta, L->mutate);
                 memcpy(vr, vsrc, (size_t)d * sizeof(double));
-                uint16_t *kdst = kcb + ((int64_t)kh * capacity + p0 + r) * d;
-                for (int j = 0; j < d; ++j) {
-                    kdst[j] = orc_bf16_from_double(kr[j]);
-                    vb16[j] = orc_bf16_from_double(vr[j]);
+                if (kturbo) {
+                    for (int j = 0; j < d; ++j)
+                        vb16[j] = orc_bf16_from_double(kr[j]);
+                    const int64_t row = ((int64_t)b * Hk + kh) * capacity + p0 + r;
+                    orc_turbo4_quantize_rows(vb16, 1, d, k_codes + row * (d / 2),
+                                             k_scales + row * (d / 16));
+                } else {
+                    uint16_t *kdst = kcb + ((int64_t)kh * capacity + p0 + r) * d;
+                    for (int j = 0; j < d; ++j)
+                        kdst[j] = orc_bf16_from_double(kr[j]);
                 }
+                for (int j = 0; j < d; ++j)
+                    vb16[j] = orc_bf16_from_double(vr[j]);
                 if (turbo) {
                     const int64_t row = ((int64_t)b * Hk + kh) * capacity + p0 + r;
                     orc_turbo4_quantize_rows(vb16, 1, d, v_codes + row * (d / 2),
@@ -798,6 +823,9 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                 const int64_t row0 = ((int64_t)b * Hk + kh) * capacity;
                 turbo4_dequant(v_codes + row0 * (d / 2), v_scales + row0 * (d / 16), p0 + R, d, cbk,
                                L->mutate, vdq);
+                if (kturbo)
+                    turbo4_dequant(k_codes + row0 * (d / 2), k_scales + row0 * (d / 16), p0 + R, d,
+                                   cbk, L->mutate, kdq);
                 for (int h = 0; h < H; ++h) {
                     const int khh = (L->mutate == ORC_MUT_GQA_MODULO) ? h % Hk : h / gqa;
                     if (khh != kh)
@@ -810,8 +838,10 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                             keep = M->m + b * M->stride_batch + (M->heads > 1 ? h : 0) * M->stride_head +
                                    r * M->stride_row;
                         }
-                        sdpa_row_vd(qn + ((int64_t)r * H + h) * d, kcb + (int64_t)kh * capacity * d,
-                                    d, vdq, d, last, keep, attn + ((int64_t)r * H + h) * d, scores);
+                        sdpa_row_vd(qn + ((int64_t)r * H + h) * d,
+                                    kturbo ? NULL : kcb + (int64_t)kh * capacity * d, d, vdq, d, last,
+                                    keep, attn + ((int64_t)r * H + h) * d, scores,
+                                    kturbo ? kdq : NULL);
                     }
                 }
             }
@@ -880,7 +910,7 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
     }
 done:
     free(wrow); free(y); free(qn); free(attn); free(ga); free(tmp); free(nq); free(nk);
-    free(scores); free(knew); free(vnew); free(cf); free(cl); free(vdq); free(vb16);
+    free(scores); free(knew); free(vnew); free(cf); free(cl); free(vdq); free(kdq); free(vb16);
     return rc;
 }
 
@@ -889,8 +919,8 @@ int orc_layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                    const int32_t *cache_pos, int B, int R,
                    double *out, double *tap_y, double *tap_attn)
 {
-    return layer_step(L, W, x, cache_k, cache_v, NULL, NULL, capacity, cache_pos, B, R, NULL, out,
-                      tap_y, tap_attn);
+    return layer_step(L, W, x, cache_k, cache_v, NULL, NULL, NULL, NULL, capacity, cache_pos, B, R,
+                      NULL, out, tap_y, tap_attn);
 }
 
 /* orc_layer_step with an attention mask (orc_mask above): mask bytes, heads
@@ -905,8 +935,8 @@ int orc_layer_step_masked(const orc_layer *L, const orc_weights *W, const double
     if (!mask)
         return ORC_E_ARG;
     const orc_mask M = {mask, mask_heads, stride_row, stride_head, stride_batch};
-    return layer_step(L, W, x, cache_k, cache_v, NULL, NULL, capacity, cache_pos, B, R, &M, out,
-                      tap_y, tap_attn);
+    return layer_step(L, W, x, cache_k, cache_v, NULL, NULL, NULL, NULL, capacity, cache_pos, B, R,
+                      &M, out, tap_y, tap_attn);
 }
 
 /* The layer step over a Bf16KTurbo4V cache: K as in orc_layer_step, V as
@@ -920,8 +950,8 @@ int orc_layer_step_turbo4v(const orc_layer *L, const orc_weights *W, const doubl
 {
     if (!v_codes || !v_scales)
         return ORC_E_ARG;
-    return layer_step(L, W, x, cache_k, NULL, v_codes, v_scales, capacity, cache_pos, B, R, NULL,
-                      out, tap_y, tap_attn);
+    return layer_step(L, W, x, cache_k, NULL, v_codes, v_scales, NULL, NULL, capacity, cache_pos, B,
+                      R, NULL, out, tap_y, tap_attn);
 }
 
 /* ------------------------------------------------------ decoder block */
@@ -942,6 +972,7 @@ int orc_layer_step_turbo4v(const orc_layer *L, const orc_weights *W, const doubl
  * NULL: causal; orc_mask above). */
 typedef struct orc_step_ext {
     uint8_t *v_codes, *v_scales;
+    uint8_t *k_codes, *k_scales;       /* with v_*: the symmetric Turbo4 cache */
     const uint8_t *mask;
     int32_t mask_heads;
     int64_t mask_row, mask_head, mask_batch;
@@ -963,10 +994,11 @@ int orc_layer_step_ext(const orc_layer *L, const orc_weights *W, const double *x
         mp = &M;
     }
     uint8_t *vc = e ? e->v_codes : NULL, *vs = e ? e->v_scales : NULL;
-    if ((vc == NULL) != (vs == NULL))
+    uint8_t *kc = e ? e->k_codes : NULL, *ks = e ? e->k_scales : NULL;
+    if ((vc == NULL) != (vs == NULL) || (kc == NULL) != (ks == NULL))
         return ORC_E_ARG;
-    return layer_step(L, W, x, cache_k, vc ? NULL : cache_v, vc, vs, capacity, cache_pos, B, R, mp,
-                      out, tap_y, tap_attn);
+    return layer_step(L, W, x, kc ? NULL : cache_k, vc ? NULL : cache_v, vc, vs, kc, ks, capacity,
+                      cache_pos, B, R, mp, out, tap_y, tap_attn);
 }
 
 static int block_step(const orc_layer *L, const orc_weights *W, const double *x, int h_bf16,

@@ -25,7 +25,8 @@ from dataclasses import dataclass, replace
 import numpy as np
 
 # substream ids
-_X, _WQ, _WK, _WV, _WO, _QN, _KN, _CK, _CV, _LEN, _IN_LN, _POST_LN, _VQC, _VQS = range(1, 15)
+(_X, _WQ, _WK, _WV, _WO, _QN, _KN, _CK, _CV, _LEN, _IN_LN, _POST_LN, _VQC, _VQS, _KQC,
+ _KQS) = range(1, 17)
 
 
 @dataclass(frozen=True)
@@ -199,14 +200,16 @@ def cache(spec: LayerSpec, capacity: int | None = None, fill: int = 0, batches=N
 
 
 def turbo4v_cache(spec: LayerSpec, capacity: int | None = None, stale_code: int = 0xFF,
-                  stale_scale: int = 0x7F, batches=None):
+                  stale_scale: int = 0x7F, batches=None, plane: str = "v"):
     """Prior Bf16KTurbo4V V planes for the sequences in ``batches``: codes
     [B'][Hk][cap][d/2] uint8 (uniform random nibbles) and E4M3 scales
     [B'][Hk][cap][d/16] uint8, uniform over the bytes 0x30..0x3F (0.5 to
     1.875, the scale of a unit-variance group) for positions < cache_pos;
     every later slot holds ``stale_code`` / ``stale_scale`` (0x7F is an E4M3
     NaN, so a kernel that reads a stale slot shows it).  Random bytes only:
-    no quantizer arithmetic here."""
+    no quantizer arithmetic here.  plane="k" draws the K planes of a symmetric
+    Turbo4 cache from their own substreams."""
+    ic, isc = (_VQC, _VQS) if plane == "v" else (_KQC, _KQS)
     cap = capacity or spec.capacity()
     pos = spec.positions()
     Hk, d = spec.num_kv_heads, spec.head_dim
@@ -217,9 +220,9 @@ def turbo4v_cache(spec: LayerSpec, capacity: int | None = None, stale_code: int 
         c = np.full((Hk, cap, d // 2), stale_code, np.uint8)
         sc = np.full((Hk, cap, d // 16), stale_scale, np.uint8)
         for kh in range(Hk):
-            rng = np.random.default_rng([spec.seed, _VQC, b, kh])
+            rng = np.random.default_rng([spec.seed, ic, b, kh])
             c[kh, :p] = rng.integers(0, 256, size=(p, d // 2), dtype=np.uint8)
-            rng = np.random.default_rng([spec.seed, _VQS, b, kh])
+            rng = np.random.default_rng([spec.seed, isc, b, kh])
             sc[kh, :p] = rng.integers(0x30, 0x40, size=(p, d // 16), dtype=np.uint8)
         cs.append(c)
         ss.append(sc)

@@ -326,3 +326,45 @@ def test_block_over_a_turbo_cache_reduces_to_the_turbo_layer():
     ref = orc.layer_step_ext(spec, case.orc_weights, x, k2, None, case.pos, turbo=(c2, s2))
     assert np.allclose(out - x, ref, rtol=1e-12, atol=1e-14)
     assert np.array_equal(c1, c2) and np.array_equal(s1, s2) and np.array_equal(k1, k2)
+
+
+def test_symmetric_turbo_layer_step_wiring():
+    """The symmetric Turbo4 cache ([atlas-mod] MetalKvDtype::Turbo4): the new K
+    rows are the quantizer's output on the bf16 normed, rotated key, the new V
+    rows on the bf16 value, and the attention tap is a numpy attention over
+    the dequantized K and V rows."""
+    spec = synth.WORKLOADS["tiny"].with_(batch=2, q_len=2, cache_pos=None, length_range=(20, 90),
+                                         x_dtype="bf16")
+    case, vcodes, vscales = _turbo_case(spec)
+    kcodes, kscales = synth.turbo4v_cache(spec, case.cap, plane="k")
+    out, ty, ta = orc.layer_step_ext(spec, case.orc_weights, synth.x_values(spec, case.x), None,
+                                     None, case.pos, turbo=(vcodes, vscales),
+                                     turbo_k=(kcodes, kscales), taps=True)
+    B, R = spec.batch, spec.q_len
+    H, Hk, d = spec.num_heads, spec.num_kv_heads, spec.head_dim
+    rd = orc.rotary_dims(d, spec.partial_rotary_factor)
+    qn_w, kn_w = (bf16_bits_to_f32(w).astype(np.float64) for w in synth.norm_weights_bf16(spec))
+    eps, theta = float(np.float32(spec.rms_eps)), float(np.float32(spec.rope_theta))
+    for b in range(B):
+        p0 = int(case.pos[b])
+        for r in range(R):
+            for kh in range(Hk):
+                k = orc.rope(orc.rms_norm(ty[b, r, 2 * H * d + kh * d:2 * H * d + (kh + 1) * d], kn_w,
+                                          eps), rd, p0 + r, theta)
+                kb = np.array([[orc.bf16_from_double(float(t)) for t in k]], np.uint16)
+                cq, sq = orc.turbo4_quantize_rows(kb)
+                assert np.array_equal(kcodes[b, kh, p0 + r], cq[0])
+                assert np.array_equal(kscales[b, kh, p0 + r], sq[0])
+    kd = orc.turbo4_dequant_rows(kcodes, kscales)
+    vd = orc.turbo4_dequant_rows(vcodes, vscales)
+    gqa = H // Hk
+    for b in range(B):
+        p0 = int(case.pos[b])
+        for h in range(H):
+            for r in range(R):
+                q = orc.rope(orc.rms_norm(ty[b, r, h * 2 * d:h * 2 * d + d], qn_w, eps), rd, p0 + r,
+                             theta)
+                s = kd[b, h // gqa, :p0 + r + 1] @ q / np.sqrt(d)
+                p = np.exp(s - s.max())
+                want = (p / p.sum()) @ vd[b, h // gqa, :p0 + r + 1]
+                assert np.allclose(ta[b, r, h], want, rtol=1e-10, atol=1e-12)
