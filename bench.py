@@ -58,7 +58,8 @@ def algorithmic_bytes(spec, block=False, kv="bf16"):
     wv = wbytes(spec.n_kv, Hd, spec.bits[2], spec.group[2])
     wo = wbytes(Hd, H * d, spec.bits[3], spec.group[3])
     pos = spec.positions().astype(np.int64)
-    row_kv = d * 2 + (d // 2 + d // 16 if kv == "turbo4v" else d * 2)   # K + V bytes per row
+    quant = d // 2 + d // 16                  # a Turbo4 row: codes + E4M3 scales
+    row_kv = (quant if kv == "turbo4" else d * 2) + (quant if kv in ("turbo4v", "turbo4") else d * 2)
     kv_read = int(((pos + R) * Hk * row_kv).sum())
     kv_write = M * Hk * row_kv
     xb = M * Hd * (4 if spec.x_dtype == "f32" else 2)
@@ -183,7 +184,8 @@ def oracle_sample(spec, budget_s=15.0, max_steps=64, block=False, kv="bf16"):
                           qn, kn, list(spec.bits), list(spec.group))
     cap = spec.capacity()
     ck, cv = synth.cache(spec, cap)
-    vq = synth.turbo4v_cache(spec, cap) if kv == "turbo4v" else None
+    vq = synth.turbo4v_cache(spec, cap) if kv in ("turbo4v", "turbo4") else None
+    kq = synth.turbo4v_cache(spec, cap, plane="k") if kv == "turbo4" else None
     x = synth.x_values(spec, synth.layer_input(spec))
     pos = spec.positions()
     il, pl = synth.block_norm_weights_bf16(spec)
@@ -192,7 +194,10 @@ def oracle_sample(spec, budget_s=15.0, max_steps=64, block=False, kv="bf16"):
     while steps < max_steps:
         k2, v2 = ck.copy(), cv.copy()
         ts = time.perf_counter()
-        if kv == "turbo4v":
+        if kv == "turbo4":
+            orc.layer_step_ext(spec, W, x, None, None, pos, turbo=(vq[0].copy(), vq[1].copy()),
+                               turbo_k=(kq[0].copy(), kq[1].copy()))
+        elif kv == "turbo4v":
             orc.layer_step_turbo4v(spec, W, x, k2, vq[0].copy(), vq[1].copy(), pos)
         elif block:
             orc.block_step(spec, W, x, il, pl, k2, v2, pos)
@@ -239,8 +244,10 @@ def config_dict(spec, args, extra=None):
          "head_chunk": not args.no_head_chunk, "parallelism": f"replicas x{args.gpus}",
          "step": "decoder block (input RMSNorm, layer, residual, post-norm)" if args.block
          else "attention layer",
-         "kv_cache": "bf16 K, Turbo4 V (WHT basis, 4-bit Lloyd-Max codes, E4M3 group-16 scales)"
-         if args.kv == "turbo4v" else "bf16 K and V"}
+         "kv_cache": {"turbo4v": "bf16 K, Turbo4 V (WHT basis, 4-bit Lloyd-Max codes, E4M3 "
+                                 "group-16 scales)",
+                      "turbo4": "Turbo4 K and V (WHT basis, 4-bit Lloyd-Max codes, E4M3 group-16 "
+                                "scales)"}.get(args.kv, "bf16 K and V")}
     if extra:
         d.update(extra)
     return d
@@ -309,7 +316,8 @@ def our_arm(args, spec):
     qn, kn = synth.norm_weights_bf16(spec)
     cap = spec.capacity()
     ck, cv = synth.cache(spec, cap)
-    vq = synth.turbo4v_cache(spec, cap) if args.kv == "turbo4v" else None
+    vq = synth.turbo4v_cache(spec, cap) if args.kv in ("turbo4v", "turbo4") else None
+    kq = synth.turbo4v_cache(spec, cap, plane="k") if args.kv == "turbo4" else None
     pos = spec.positions()
     x = synth.layer_input(spec)
     layers = []
@@ -319,9 +327,10 @@ def our_arm(args, spec):
                                            "split": gattn.PATH_SPLIT}[args.path],
                          kv_format=args.kv)
         dl._w = None          # interchange copies are no longer needed after repacking
-        dl.load_cache(ck, vq if args.kv == "turbo4v" else cv)
+        dl.load_cache(kq if args.kv == "turbo4" else ck,
+                      vq if args.kv in ("turbo4v", "turbo4") else cv)
         layers.append(dl)
-    del ck, cv, vq
+    del ck, cv, vq, kq
     xd = x_to_device(spec, x, dev)
     pd = torch.from_numpy(pos).to(dev)
     outs = [torch.empty((spec.batch, spec.q_len, spec.hidden), dtype=torch.bfloat16, device=dev)
@@ -435,8 +444,8 @@ def our_arm(args, spec):
     achieved = kernel_bytes[dominant] / (kernel_avg_ms[dominant] / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak,
-                "traffic": profiled_traffic(dominant, spec.name + ("_turbo4v" if args.kv == "turbo4v"
-                                                                   else "")),
+                "traffic": profiled_traffic(dominant, spec.name + ("" if args.kv == "bf16"
+                                                                   else "_" + args.kv)),
                 "kernel": dominant, "peak_source": peak_kind,
                 "kernel_avg_us": {n: 1e3 * v for n, v in kernel_avg_ms.items()},
                 "kernel_bytes": kernel_bytes}
@@ -512,8 +521,8 @@ def main():
     ap.add_argument("--no-head-chunk", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "fused", "split"],
                     help="one-kernel or five-kernel step (auto: one kernel when it fits)")
-    ap.add_argument("--kv", default="bf16", choices=["bf16", "turbo4v"],
-                    help="KV cache format: bf16, or bf16 K with a Turbo4 V cache")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "turbo4v", "turbo4"],
+                    help="KV cache format: bf16, bf16 K with a Turbo4 V cache, or Turbo4 K and V")
     ap.add_argument("--block", action="store_true",
                     help="time the decoder-block step (input RMSNorm + layer + residual + "
                          "post-attention RMSNorm) instead of the layer alone")

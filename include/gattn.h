@@ -199,6 +199,31 @@ typedef struct gattn_kv_turbo4v_desc {
 gattn_status gattn_kv_register_turbo4v(gattn_layer *layer, const gattn_kv_turbo4v_desc *desc,
                                        gattn_kv **out);
 
+/*
+ * A caller-owned symmetric Turbo4 cache (device; MetalKvDtype::Turbo4 of the
+ * Atlas qwen3_5 forward page: K and V both WHT-rotated 4-bit Lloyd-Max codes
+ * with E4M3 group-of-16 scales).  K and V planes have the layout of the V
+ * planes of gattn_kv_turbo4v_desc (one set of code and scale strides for
+ * both).  The step quantizes its new K rows from the bf16 values of the
+ * normed, rotary-embedded keys, and its new V rows as for Bf16KTurbo4V; the
+ * attention rotates each q row once (q' = H q / sqrt(d)) so the scores are
+ * q' . dequantized key rows in the rotated basis.  Same rules as
+ * gattn_kv_register_turbo4v (no bf16 K).
+ */
+typedef struct gattn_kv_turbo4_desc {
+    void *k_codes;
+    void *k_scales;
+    void *v_codes;
+    void *v_scales;
+    int32_t batch;
+    int32_t capacity;
+    int64_t code_stride_head, code_stride_batch;
+    int64_t scale_stride_head, scale_stride_batch;
+} gattn_kv_turbo4_desc;
+
+gattn_status gattn_kv_register_turbo4(gattn_layer *layer, const gattn_kv_turbo4_desc *desc,
+                                      gattn_kv **out);
+
 /* The Turbo4 codebook as the kernels use it (host, no GPU): the 16 levels of
  * the Lloyd-Max quantizer of N(0, 1), ascending, rounded to fp32, and the 15
  * decision thresholds between them (midpoints taken in double, then rounded;

@@ -203,6 +203,8 @@ struct gattn_kv {
     gattn_kv_desc desc{};          // K (and V for a bf16 cache); v is NULL for Turbo4 V
     bool turbo = false;            // Bf16KTurbo4V: V as codes + E4M3 scales
     gattn_kv_turbo4v_desc tdesc{};
+    bool kturbo = false;           // symmetric Turbo4: K as codes + E4M3 scales too
+    void *kq_codes = nullptr, *kq_scales = nullptr;
     CUtensorMap kmap;   // CUtensorMap is itself 64-byte aligned
     CUtensorMap vmap;
 };
@@ -536,30 +538,42 @@ gattn_status gattn_kv_register(gattn_layer *L, const gattn_kv_desc *d, gattn_kv 
     return GATTN_OK;
 }
 
+// Rules for the Turbo4 code / scale planes of a cache (V, and K for the
+// symmetric format): pointers, capacity, strides.
+static gattn_status check_turbo_planes(const gattn_layer *L, const char *which, const void *codes,
+                                       const void *scales, int32_t capacity, int64_t cs_head,
+                                       int64_t cs_batch, int64_t ss_head, int64_t ss_batch)
+{
+    const int hd = L->cfg.head_dim;
+    if (hd != 64 && hd != 128 && hd != 256)
+        return fail(GATTN_E_INVALID_ARG, "a Turbo4 cache needs head_dim 64, 128 or 256 (got %d)", hd);
+    if (!codes || !scales)
+        return fail(GATTN_E_INVALID_ARG, "%s code or scale pointer is NULL", which);
+    if ((reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(scales)) & 15)
+        return fail(GATTN_E_INVALID_ARG, "%s code and scale pointers must be 16-byte aligned", which);
+    if (capacity < 16 || capacity % 16)
+        return fail(GATTN_E_INVALID_ARG, "a Turbo4 cache needs capacity %% 16 == 0 (got %d)",
+                    (int)capacity);
+    const long long cap = capacity;
+    if (cs_head <= 0 || cs_batch <= 0 || ss_head <= 0 || ss_batch <= 0 ||
+        (cs_head | cs_batch | ss_head | ss_batch) & 15)
+        return fail(GATTN_E_INVALID_ARG, "code and scale strides must be positive multiples of 16 bytes");
+    if (cs_head < cap * (hd / 2) || ss_head < cap * (hd / 16))
+        return fail(GATTN_E_INVALID_ARG, "a head's code or scale rows overlap the next head's");
+    return GATTN_OK;
+}
+
 gattn_status gattn_kv_register_turbo4v(gattn_layer *L, const gattn_kv_turbo4v_desc *d,
                                        gattn_kv **out)
 {
     if (!L || !d || !out)
         return fail(GATTN_E_INVALID_ARG, "NULL argument");
     *out = nullptr;
-    const int hd = L->cfg.head_dim;
-    if (hd != 64 && hd != 128 && hd != 256)
-        return fail(GATTN_E_INVALID_ARG, "a Turbo4 V cache needs head_dim 64, 128 or 256 (got %d)",
-                    hd);
-    if (!d->v_codes || !d->v_scales)
-        return fail(GATTN_E_INVALID_ARG, "V code or scale pointer is NULL");
-    if ((reinterpret_cast<uintptr_t>(d->v_codes) | reinterpret_cast<uintptr_t>(d->v_scales)) & 15)
-        return fail(GATTN_E_INVALID_ARG, "V code and scale pointers must be 16-byte aligned");
-    if (d->capacity % 16)
-        return fail(GATTN_E_INVALID_ARG, "a Turbo4 V cache needs capacity %% 16 == 0 (got %d)",
-                    (int)d->capacity);
-    const long long cap = d->capacity;
-    if (d->code_stride_head <= 0 || d->code_stride_batch <= 0 || d->scale_stride_head <= 0 ||
-        d->scale_stride_batch <= 0 ||
-        (d->code_stride_head | d->code_stride_batch | d->scale_stride_head | d->scale_stride_batch) & 15)
-        return fail(GATTN_E_INVALID_ARG, "code and scale strides must be positive multiples of 16 bytes");
-    if (d->code_stride_head < cap * (hd / 2) || d->scale_stride_head < cap * (hd / 16))
-        return fail(GATTN_E_INVALID_ARG, "a head's code or scale rows overlap the next head's");
+    const gattn_status pst = check_turbo_planes(L, "V", d->v_codes, d->v_scales, d->capacity,
+                                                d->code_stride_head, d->code_stride_batch,
+                                                d->scale_stride_head, d->scale_stride_batch);
+    if (pst != GATTN_OK)
+        return pst;
     gattn_kv_desc kd{};
     kd.k = d->k;
     kd.v = d->k;                // checked like a bf16 V pointer, never read as V
@@ -575,6 +589,46 @@ gattn_status gattn_kv_register_turbo4v(gattn_layer *L, const gattn_kv_turbo4v_de
     kv->desc.v = nullptr;
     kv->turbo = true;
     kv->tdesc = *d;
+    *out = kv;
+    return GATTN_OK;
+}
+
+gattn_status gattn_kv_register_turbo4(gattn_layer *L, const gattn_kv_turbo4_desc *d,
+                                      gattn_kv **out)
+{
+    if (!L || !d || !out)
+        return fail(GATTN_E_INVALID_ARG, "NULL argument");
+    *out = nullptr;
+    if (d->batch <= 0)
+        return fail(GATTN_E_INVALID_ARG, "batch must be > 0");
+    for (int side = 0; side < 2; ++side) {
+        const gattn_status st = check_turbo_planes(
+            L, side ? "V" : "K", side ? d->v_codes : d->k_codes, side ? d->v_scales : d->k_scales,
+            d->capacity, d->code_stride_head, d->code_stride_batch, d->scale_stride_head,
+            d->scale_stride_batch);
+        if (st != GATTN_OK)
+            return st;
+    }
+    gattn_kv *kv = new (std::nothrow) gattn_kv();
+    if (!kv)
+        return fail(GATTN_E_CUDA, "out of host memory");
+    kv->layer = L;
+    kv->desc.batch = d->batch;           // no bf16 planes: no tensor maps either
+    kv->desc.capacity = d->capacity;
+    std::memset(&kv->kmap, 0, sizeof(kv->kmap));
+    std::memset(&kv->vmap, 0, sizeof(kv->vmap));
+    kv->turbo = true;
+    kv->tdesc.v_codes = d->v_codes;
+    kv->tdesc.v_scales = d->v_scales;
+    kv->tdesc.batch = d->batch;
+    kv->tdesc.capacity = d->capacity;
+    kv->tdesc.code_stride_head = d->code_stride_head;
+    kv->tdesc.code_stride_batch = d->code_stride_batch;
+    kv->tdesc.scale_stride_head = d->scale_stride_head;
+    kv->tdesc.scale_stride_batch = d->scale_stride_batch;
+    kv->kturbo = true;
+    kv->kq_codes = d->k_codes;
+    kv->kq_scales = d->k_scales;
     *out = kv;
     return GATTN_OK;
 }
@@ -886,6 +940,14 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
         eq.sq_head = kv->tdesc.scale_stride_head;
         eq.sq_batch = kv->tdesc.scale_stride_batch;
         eq.tq = L->tq;
+        if (kv->kturbo) {
+            eq.kq_codes = static_cast<uint8_t *>(kv->kq_codes);
+            eq.kq_scales = static_cast<uint8_t *>(kv->kq_scales);
+            eq.kcq_head = kv->tdesc.code_stride_head;
+            eq.kcq_batch = kv->tdesc.code_stride_batch;
+            eq.ksq_head = kv->tdesc.scale_stride_head;
+            eq.ksq_batch = kv->tdesc.scale_stride_batch;
+        }
     }
     EpiO eo{};
     CUDA_TRY(mark(1));
@@ -934,9 +996,20 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
         t.vq_th[0] = L->tq_th[0];
         t.vq_th[1] = L->tq_th[1];
         t.inv_sqrt_d = L->tq.inv_sqrt_d;
+        if (kv->kturbo) {
+            t.vq = 2;
+            t.kq_codes = static_cast<const uint8_t *>(kv->kq_codes);
+            t.kq_scales = static_cast<const uint8_t *>(kv->kq_scales);
+            t.kcq_head = kv->tdesc.code_stride_head;
+            t.kcq_batch = kv->tdesc.code_stride_batch;
+            t.ksq_head = kv->tdesc.scale_stride_head;
+            t.ksq_batch = kv->tdesc.scale_stride_batch;
+        }
     }
     CUDA_TRY(mark(2));
-    if (kv->turbo)
+    if (kv->kturbo)
+        CUDA_TRY(launch_attn_vqk(MT, c.head_dim / 64, t, kv->kmap, L->attn_grid, pdl, s));
+    else if (kv->turbo)
         CUDA_TRY(launch_attn_vq(MT, c.head_dim / 64, t, kv->kmap, L->attn_grid, pdl, s));
     else
         CUDA_TRY(launch_attn(MT, c.head_dim / 64, t, kv->kmap, kv->vmap, L->attn_grid, pdl, s));

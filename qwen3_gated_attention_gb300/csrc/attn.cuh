@@ -14,24 +14,28 @@ static_assert(kDBox % 1024 == 0, "tile boxes must stay swizzle-atom aligned");
 template <int MT, int DB, int VQ>
 struct AttnSmem {
     static constexpr int kTileBytes = DB * kDBox;             // kAttnTile tokens x d bf16
-    // V of a stage: the bf16 tile, or (Turbo4) the tile's code rows (d/2 bytes
-    // per token) followed by its scale rows (d/16 bytes per token)
+    // K and V of a stage: the bf16 tile, or (Turbo4) the tile's code rows (d/2
+    // bytes per token) followed by its scale rows (d/16 bytes per token); V is
+    // Turbo4 for VQ >= 1, K too for VQ == 2 (the symmetric format)
     static constexpr int kVCodeBytes = kAttnTile * DB * 32;
-    static constexpr int kVBytes =
-        VQ ? ((kVCodeBytes + kAttnTile * DB * 4 + 1023) & ~1023) : kTileBytes;
-    static constexpr int kStageBytes = kTileBytes + kVBytes;  // K + V
+    static constexpr int kQuantBytes = (kVCodeBytes + kAttnTile * DB * 4 + 1023) & ~1023;
+    static constexpr int kKBytes = VQ == 2 ? kQuantBytes : kTileBytes;
+    static constexpr int kVBytes = VQ ? kQuantBytes : kTileBytes;
+    static constexpr int kStageBytes = kKBytes + kVBytes;     // K + V
     static constexpr int kDqBytes = VQ ? kTileBytes : 0;      // Turbo4: dequantized fp16 V tile
+    static constexpr int kDqKBytes = VQ == 2 ? kTileBytes : 0;    // and K tile
     static constexpr int kLutBytes = 0;
     static constexpr int kQBytes = MT * 16 * DB * 64 * 2;
     static constexpr int kPBytes = MT * 16 * 128;             // rows x 64 tokens bf16
     // as many K/V stages (2 .. kAttnStages) as fit beside the rest in 227 KB
-    static constexpr int kFixed = kDqBytes + kLutBytes + kQBytes + kPBytes +
+    static constexpr int kFixed = kDqBytes + kDqKBytes + kLutBytes + kQBytes + kPBytes +
                                   2 * kAttnWarps * 64 * 4 + 40 * 8 + 2 * kAttnStages * 8 + 256 + 1024;
     static constexpr int kFit = (227 * 1024 - kFixed) / kStageBytes;
     static constexpr int kNStages = kFit < 2 ? 2 : (kFit > kAttnStages ? kAttnStages : kFit);
     static constexpr int kStages = kNStages * kStageBytes;
     static constexpr int kDq = kStages;
-    static constexpr int kLut = kDq + kDqBytes;
+    static constexpr int kDqK = kDq + kDqBytes;
+    static constexpr int kLut = kDqK + kDqKBytes;
     static constexpr int kQ = kLut + kLutBytes;
     static constexpr int kP = kQ + kQBytes;
     static constexpr int kRedMax = kP + kPBytes;              // [8][64] floats
@@ -42,6 +46,46 @@ struct AttnSmem {
     static constexpr int kTotal = kFlags + 256 + 1024;        // + alignment slack
     static_assert(kTotal <= 227 * 1024, "attention shared memory exceeds 227 KB");
 };
+
+// One Turbo4 dequantization item: 32 columns (c) of token tl of a tile, from
+// its 16 code bytes and 2 E4M3 scales into the fp16 tile (the bf16 tile's
+// swizzled layout).  A 16-byte store is served eight lanes at a time; those
+// lanes share a token and take its 32-column pieces c, so each lane writes its
+// four 8-column chunks in an order rotated by c: at every step the eight lanes
+// hit eight different bank groups.  live == false writes zeros.
+// Shared-memory addresses: dst the fp16 tile, cst / sst the code / scale rows.
+template <int DB>
+__device__ __forceinline__ void turbo_dequant_item(uint32_t dst, uint32_t cst, uint32_t sst, int tl,
+                                                   int c, bool live, const uint32_t (&lvl_lo)[2],
+                                                   const uint32_t (&lvl_hi)[2])
+{
+    constexpr int kRotShift = DB == 4 ? 1 : 0;
+    const int rot = (c >> kRotShift) & 3;
+    uint4 cb = make_uint4(0, 0, 0, 0);
+    __half2 s0 = __float2half2_rn(0.f), s1 = s0;
+    if (live) {
+        cb = lds_v4(cst + tl * (DB * 32) + c * 16);
+        const uint32_t sb = lds_u16(sst + tl * (DB * 4) + c * 2);
+        s0 = __half2half2(e4m3_to_half((uint8_t)(sb & 0xFF)));
+        s1 = __half2half2(e4m3_to_half((uint8_t)(sb >> 8)));
+    }
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+        const int q = (st + rot) & 3;            // bytes 4q .. 4q + 3
+        const uint32_t wq = q == 0 ? cb.x : (q == 1 ? cb.y : (q == 2 ? cb.z : cb.w));
+        const __half2 sc = q < 2 ? s0 : s1;      // groups 2c, 2c + 1
+        uint32_t o[4];
+        turbo4_levels8(wq, lvl_lo, lvl_hi, o);
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+            const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&o[k2]), sc);
+            o[k2] = *reinterpret_cast<const uint32_t *>(&v);
+        }
+        const int ch = 4 * c + q;                // 8-column chunk of the row
+        sts_v4(dst + (ch >> 3) * kDBox + tl * 128 + (((ch & 7) ^ (tl & 7)) << 4), o[0], o[1], o[2],
+               o[3]);
+    }
+}
 
 template <int MT, int DB, int VQ>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -55,6 +99,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *qs = smem + L::kQ;
     uint8_t *dq = smem + L::kDq;                                // Turbo4 only
+    uint8_t *dqk = smem + L::kDqK;                              // symmetric Turbo4 only
     uint8_t *ps = smem + L::kP;
     float *red_max = reinterpret_cast<float *>(smem + L::kRedMax);
     float *red_l = reinterpret_cast<float *>(smem + L::kRedL);
@@ -109,7 +154,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == kAttnWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && beg < end) {
-            prefetch_tensormap(&kmap);
+            if constexpr (VQ != 2)
+                prefetch_tensormap(&kmap);
             if constexpr (!VQ)
                 prefetch_tensormap(&vmap);
             const uint64_t pol = l2_evict_first_policy();
@@ -132,24 +178,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         break;
                     }
                     uint8_t *kst = smem + slot * L::kStageBytes;
-                    uint8_t *vst = kst + L::kTileBytes;
-                    // Turbo4 V: the tile's code and scale rows are contiguous (the
+                    uint8_t *vst = kst + L::kKBytes;
+                    // Turbo4 planes: the tile's code and scale rows are contiguous (the
                     // capacity is a multiple of the 16-token unit, so they end in range)
                     const uint32_t vq_code = VQ ? (uint32_t)(nun * kAttnUnit * DB * 32) : 0u;
                     const uint32_t vq_scale = VQ ? (uint32_t)(nun * kAttnUnit * DB * 4) : 0u;
-                    mbar_arrive_expect_tx(&full[slot], VQ ? (uint32_t)(nun * DB * 2048) + vq_code +
-                                                                vq_scale
-                                                          : (uint32_t)(nun * DB * 2048 * 2));
-                    for (int ui = 0; ui < nun; ++ui) {
-                        const int t = (u + ui) * kAttnUnit;
+                    const uint32_t tile_bytes = (uint32_t)(nun * DB * 2048);
+                    mbar_arrive_expect_tx(&full[slot], (VQ == 2 ? vq_code + vq_scale : tile_bytes) +
+                                                           (VQ ? vq_code + vq_scale : tile_bytes));
+                    if constexpr (VQ != 2) {
+                        for (int ui = 0; ui < nun; ++ui) {
+                            const int t = (u + ui) * kAttnUnit;
 #pragma unroll
-                        for (int db = 0; db < DB; ++db) {
-                            tensor4d_g2s(kst + db * kDBox + ui * 2048, &kmap, db * 64, t, p.kh, p.b,
-                                         &full[slot], pol);
-                            if constexpr (!VQ)
-                                tensor4d_g2s(vst + db * kDBox + ui * 2048, &vmap, db * 64, t, p.kh,
+                            for (int db = 0; db < DB; ++db) {
+                                tensor4d_g2s(kst + db * kDBox + ui * 2048, &kmap, db * 64, t, p.kh,
                                              p.b, &full[slot], pol);
+                                if constexpr (!VQ)
+                                    tensor4d_g2s(vst + db * kDBox + ui * 2048, &vmap, db * 64, t,
+                                                 p.kh, p.b, &full[slot], pol);
+                            }
                         }
+                    } else {
+                        const long long t = (long long)u * kAttnUnit;
+                        bulk_g2s(kst, a.kq_codes + p.b * a.kcq_batch + p.kh * a.kcq_head + t * (DB * 32),
+                                 vq_code, &full[slot], pol);
+                        bulk_g2s(kst + L::kVCodeBytes,
+                                 a.kq_scales + p.b * a.ksq_batch + p.kh * a.ksq_head + t * (DB * 4),
+                                 vq_scale, &full[slot], pol);
                     }
                     if constexpr (VQ) {
                         const long long t = (long long)u * kAttnUnit;
@@ -189,16 +244,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
         // ---- q rows of this segment into shared memory (swizzled 16-byte chunks)
         constexpr int CH = D / 8;   // chunks per row
-        for (int idx = tid; idx < MT * 16 * CH; idx += kAttnWarps * 32) {
-            const int i = idx / CH, cc = idx % CH;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (i < nrows) {
+        if constexpr (VQ == 2) {
+            // symmetric Turbo4: the keys live in the rotated basis, so the rows
+            // are rotated once (q' = H q / sqrt(d): q . k = q' . H k / sqrt(d))
+            // and kept in fp16 for the fp16 products with the dequantized keys
+            for (int i = warp; i < MT * 16; i += kAttnWarps) {
+                float xr[8];
                 const int hl = i / a.R, r = i % a.R;
                 const __nv_bfloat16 *src =
-                    a.qn + (((long long)p.b * a.R + r) * a.H + h0 + hl) * D + cc * 8;
-                v = *reinterpret_cast<const uint4 *>(src);
+                    a.qn + (((long long)p.b * a.R + r) * a.H + h0 + hl) * D;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    xr[k] = (i < nrows && k < D / 32) ? __bfloat162float(src[lane + 32 * k]) : 0.f;
+                wht_warp(xr, D / 32, lane);
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k) {
+                    const int j = lane + 32 * k;
+                    *reinterpret_cast<__half *>(qs + i * (D * 2) + (((j >> 3) ^ (i & 7)) << 4) +
+                                                (j & 7) * 2) = __float2half_rn(xr[k] * a.inv_sqrt_d);
+                }
             }
-            *reinterpret_cast<uint4 *>(qs + i * (D * 2) + ((cc ^ (i & 7)) << 4)) = v;
+        } else {
+            for (int idx = tid; idx < MT * 16 * CH; idx += kAttnWarps * 32) {
+                const int i = idx / CH, cc = idx % CH;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (i < nrows) {
+                    const int hl = i / a.R, r = i % a.R;
+                    const __nv_bfloat16 *src =
+                        a.qn + (((long long)p.b * a.R + r) * a.H + h0 + hl) * D + cc * 8;
+                    v = *reinterpret_cast<const uint4 *>(src);
+                }
+                *reinterpret_cast<uint4 *>(qs + i * (D * 2) + ((cc ^ (i & 7)) << 4)) = v;
+            }
         }
         named_bar_sync(1, kAttnWarps * 32);
 
@@ -222,7 +299,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint32_t ph = (uint32_t)((it / L::kNStages) & 1);
             const bool ok = mbar_wait(&full[slot], ph, abort, a.status);
             uint8_t *kst = smem + slot * L::kStageBytes;
-            uint8_t *vst = kst + L::kTileBytes;
+            uint8_t *vst = kst + L::kKBytes;
+
+            // symmetric Turbo4: each warp dequantizes the key rows of its own 8
+            // tokens (the only ones its q K^T reads) into the fp16 key tile
+            if constexpr (VQ == 2) {
+                if (ok && warp * 8 < ntok) {
+                    const uint32_t lvl_lo[2] = {a.vq_tl[0], a.vq_tl[1]};
+                    const uint32_t lvl_hi[2] = {a.vq_th[0], a.vq_th[1]};
+                    for (int it2 = lane; it2 < 8 * DB * 2; it2 += 32) {
+                        const int tl = warp * 8 + it2 / (DB * 2), c = it2 % (DB * 2);
+                        turbo_dequant_item<DB>(smem_u32(dqk), smem_u32(kst),
+                                               smem_u32(kst) + L::kVCodeBytes, tl, c,
+                                               tl < ntok && t0 + tl < Lb, lvl_lo, lvl_hi);
+                    }
+                    __syncwarp();
+                }
+            }
 
             // positions past the sequence end hold stale memory: zero those V rows
             // (Turbo4: the dequantization writes zeros there instead)
@@ -276,7 +369,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int k2 = 0; k2 < 2 * DB; ++k2) {
                     const int chunk = k2 * 4 + (lane >> 3);
                     uint32_t kb[4];
-                    ldsm_x4(kb, smem_u32(kst + (chunk >> 3) * kDBox + tok * 128 +
+                    ldsm_x4(kb, smem_u32((VQ == 2 ? dqk : kst) + (chunk >> 3) * kDBox + tok * 128 +
                                          (((chunk & 7) ^ (tok & 7)) << 4)));
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt) {
@@ -287,8 +380,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             const int qch = 2 * ks + (lane >> 4);
                             uint32_t qa[4];
                             ldsm_x4(qa, smem_u32(qs + qrow * (D * 2) + ((qch ^ (qrow & 7)) << 4)));
-                            mma_bf16(scs[ks % SPLIT][mt], qa, kb[2 * h], kb[2 * h + 1],
-                                     scs[ks % SPLIT][mt]);
+                            if constexpr (VQ == 2)
+                                mma_f16(scs[ks % SPLIT][mt], qa, kb[2 * h], kb[2 * h + 1],
+                                        scs[ks % SPLIT][mt]);
+                            else
+                                mma_bf16(scs[ks % SPLIT][mt], qa, kb[2 * h], kb[2 * h + 1],
+                                         scs[ks % SPLIT][mt]);
                         }
                     }
                 }
@@ -332,39 +429,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t cst = smem_u32(vst), sst = cst + L::kVCodeBytes;
                     const uint32_t dq_a = smem_u32(dq);
                     const uint32_t lvl_lo[2] = {a.vq_tl[0], a.vq_tl[1]}, lvl_hi[2] = {a.vq_th[0], a.vq_th[1]};
-                    // A 16-byte store is served eight lanes at a time; those lanes
-                    // share a token and take its eight 32-column pieces c, so each
-                    // lane writes its four 8-column chunks in an order rotated by c:
-                    // at every step the eight lanes hit eight different bank groups.
-                    constexpr int kRotShift = DB == 4 ? 1 : 0;
                     for (int idx = tid; idx < kAttnTile * DB * 2; idx += kAttnWarps * 32) {
                         const int tl = idx / (DB * 2), c = idx % (DB * 2);   // token, 32 columns
-                        const int rot = (c >> kRotShift) & 3;
-                        const bool live = tl < ntok && t0 + tl < Lb;
-                        uint4 cb = make_uint4(0, 0, 0, 0);
-                        __half2 s0 = __float2half2_rn(0.f), s1 = s0;
-                        if (live) {
-                            cb = lds_v4(cst + tl * (DB * 32) + c * 16);
-                            const uint32_t sb = lds_u16(sst + tl * (DB * 4) + c * 2);
-                            s0 = __half2half2(e4m3_to_half((uint8_t)(sb & 0xFF)));
-                            s1 = __half2half2(e4m3_to_half((uint8_t)(sb >> 8)));
-                        }
-#pragma unroll
-                        for (int st = 0; st < 4; ++st) {
-                            const int q = (st + rot) & 3;            // bytes 4q .. 4q + 3
-                            const uint32_t wq = q == 0 ? cb.x : (q == 1 ? cb.y : (q == 2 ? cb.z : cb.w));
-                            const __half2 sc = q < 2 ? s0 : s1;      // groups 2c, 2c + 1
-                            uint32_t o[4];
-                            turbo4_levels8(wq, lvl_lo, lvl_hi, o);
-#pragma unroll
-                            for (int k2 = 0; k2 < 4; ++k2) {
-                                const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&o[k2]), sc);
-                                o[k2] = *reinterpret_cast<const uint32_t *>(&v);
-                            }
-                            const int ch = 4 * c + q;                   // 8-column chunk of the row
-                            sts_v4(dq_a + (ch >> 3) * kDBox + tl * 128 + (((ch & 7) ^ (tl & 7)) << 4),
-                                   o[0], o[1], o[2], o[3]);
-                        }
+                        turbo_dequant_item<DB>(dq_a, cst, sst, tl, c, tl < ntok && t0 + tl < Lb,
+                                               lvl_lo, lvl_hi);
                     }
                 }
             }

@@ -38,7 +38,7 @@ cudaError_t attn_vq_set_smem_limits()
                                  AttnSmem<mt, db, 1>::kTotal);
     GATTN_ATTN_INSTANCES(GATTN_SET)
 #undef GATTN_SET
-    return e;
+    return e == cudaSuccess ? attn_vqk_set_smem_limits() : e;
 }
 
 }  // namespace gattn

@@ -94,6 +94,9 @@ struct EpiQKV {
     // as bf16 (null: bf16 V)
     uint8_t *vq_codes, *vq_scales;
     long long cq_head, cq_batch, sq_head, sq_batch;   // byte strides
+    // symmetric Turbo4 cache: the new K rows quantized the same way (null: bf16 K)
+    uint8_t *kq_codes, *kq_scales;
+    long long kcq_head, kcq_batch, ksq_head, ksq_batch;
     TurboTables tq;
 };
 
@@ -244,9 +247,11 @@ struct AttnArgs {
     unsigned *status;
     // Bf16KTurbo4V cache (vq != 0): V code / scale rows, the byte -> fp16 level
     // pair table, and the inverse rotation applied in the merge
-    int vq;
+    int vq;                      // 1: Turbo4 V, 2: Turbo4 K and V
     const uint8_t *vq_codes, *vq_scales;
     long long cq_head, cq_batch, sq_head, sq_batch;   // byte strides
+    const uint8_t *kq_codes, *kq_scales;               // vq == 2
+    long long kcq_head, kcq_batch, ksq_head, ksq_batch;
     uint32_t vq_tl[2], vq_th[2]; // low / high bytes of the 8 positive fp16 levels (turbo.cuh)
     float inv_sqrt_d;
     // attention mask (null: causal): byte (b, head or 0, row r, position t),
@@ -263,6 +268,10 @@ cudaError_t launch_attn_vq(int MT, int DB, const AttnArgs &a, const CUtensorMap 
                            bool pdl, cudaStream_t s);
 int attn_vq_smem_bytes(int MT, int DB);
 cudaError_t attn_vq_set_smem_limits();
+// the symmetric Turbo4 instances (attn_vqk.cu); no tensor map is read there
+cudaError_t launch_attn_vqk(int MT, int DB, const AttnArgs &a, const CUtensorMap &kmap, int grid,
+                            bool pdl, cudaStream_t s);
+cudaError_t attn_vqk_set_smem_limits();
 // standalone Turbo4 quantizer: one warp per row of d bf16 values
 cudaError_t launch_turbo4_quantize(const uint16_t *v, long long rows, int d, uint8_t *codes,
                                    uint8_t *scales, const TurboTables &t, cudaStream_t s);

@@ -248,16 +248,19 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
                     atomicOr(a.status, kStatusRange);
                 continue;
             }
-            if (kind == 3 && e.vq_codes) {
-                // Bf16KTurbo4V cache: quantize the bf16 V row (turbo.cuh)
+            if ((kind == 3 && e.vq_codes) || (kind == 2 && e.kq_codes)) {
+                // Turbo4 cache: quantize the bf16 row (turbo.cuh); V always, K for
+                // the symmetric format (after its norm and rotary embedding)
                 float xq[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     xq[i] = i < per ? __bfloat162float(__float2bfloat16_rn(v[i])) : 0.f;
                 const long long row = p0 + r;
-                turbo4_quantize_warp(xq, per, lane, e.tq,
-                                     e.vq_codes + b * e.cq_batch + head * e.cq_head + row * (d / 2),
-                                     e.vq_scales + b * e.sq_batch + head * e.sq_head + row * (d / 16));
+                uint8_t *qc = kind == 3 ? e.vq_codes + b * e.cq_batch + head * e.cq_head
+                                        : e.kq_codes + b * e.kcq_batch + head * e.kcq_head;
+                uint8_t *qs = kind == 3 ? e.vq_scales + b * e.sq_batch + head * e.sq_head
+                                        : e.kq_scales + b * e.ksq_batch + head * e.ksq_head;
+                turbo4_quantize_warp(xq, per, lane, e.tq, qc + row * (d / 2), qs + row * (d / 16));
                 continue;
             }
             __nv_bfloat16 *dst = (kind == 2 ? e.kc : e.vc) + (long long)b * e.st_batch +

@@ -29,12 +29,10 @@ struct TurboTables {
     float inv_sqrt_d;              // fp32(1 / sqrt(d))
 };
 
-// One warp quantizes one row of d = 32 * per values: lane l holds elements
-// l + 32 i (i < per) in x (bf16-exact fp32 values).  Writes d/2 code bytes
-// and d/16 scale bytes.
-__device__ __forceinline__ void turbo4_quantize_warp(float (&x)[8], int per, int lane,
-                                                     const TurboTables &t, uint8_t *codes,
-                                                     uint8_t *scales)
+// The unnormalized Walsh-Hadamard butterflies of one row of d = 32 * per
+// values held by a warp (lane l holds elements l + 32 i, i < per), stages
+// h = 1, 2, 4, ... in that order, each output one rounded fp32 add or subtract.
+__device__ __forceinline__ void wht_warp(float (&x)[8], int per, int lane)
 {
     // butterfly stages h < 32: partner lane l ^ h holds element e ^ h
 #pragma unroll
@@ -59,6 +57,16 @@ __device__ __forceinline__ void turbo4_quantize_warp(float (&x)[8], int per, int
                 }
         }
     }
+}
+
+// One warp quantizes one row of d = 32 * per values: lane l holds elements
+// l + 32 i (i < per) in x (bf16-exact fp32 values).  Writes d/2 code bytes
+// and d/16 scale bytes.
+__device__ __forceinline__ void turbo4_quantize_warp(float (&x)[8], int per, int lane,
+                                                     const TurboTables &t, uint8_t *codes,
+                                                     uint8_t *scales)
+{
+    wht_warp(x, per, lane);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         if (i >= per)

@@ -29,7 +29,8 @@ def cache_strides(layout: str, batch: int, Hk: int, cap: int, d: int):
 class DeviceLayer:
     """One layer handle with its weights set and one registered cache: bf16 K/V,
     or (kv_format="turbo4v") bf16 K with Turbo4 V code and E4M3 scale planes
-    [B][Hk][cap][d/2] and [B][Hk][cap][d/16] uint8."""
+    [B][Hk][cap][d/2] and [B][Hk][cap][d/16] uint8, or (kv_format="turbo4")
+    such planes for K and V both."""
 
     def __init__(self, spec, packed, q_norm, k_norm, capacity, *, batch=None, max_batch=None,
                  max_q_len=None, head_chunk=True, layout="bhtd", device="cuda:0",
@@ -60,7 +61,17 @@ class DeviceLayer:
             Hk, d = spec.num_kv_heads, spec.head_dim
             shape, st, sh, sb = cache_strides(layout, self.batch, Hk, capacity, d)
             self.k = torch.zeros(shape, dtype=torch.bfloat16, device=self.device)
-            if kv_format == "turbo4v":
+            if kv_format == "turbo4":
+                assert layout == "bhtd"
+                B = self.batch
+                pl = lambda w: torch.zeros((B, Hk, capacity, w), dtype=torch.uint8, device=self.device)
+                self.kc, self.ks = pl(d // 2), pl(d // 16)
+                self.vc, self.vs = pl(d // 2), pl(d // 16)
+                self.kv = gattn.kv_register_turbo4(
+                    self.h, self.kc.data_ptr(), self.ks.data_ptr(), self.vc.data_ptr(),
+                    self.vs.data_ptr(), B, capacity, (capacity * d // 2, Hk * capacity * d // 2),
+                    (capacity * d // 16, Hk * capacity * d // 16))
+            elif kv_format == "turbo4v":
                 assert layout == "bhtd"
                 B = self.batch
                 self.vc = torch.zeros((B, Hk, capacity, d // 2), dtype=torch.uint8, device=self.device)
@@ -82,6 +93,12 @@ class DeviceLayer:
     def load_cache(self, k_bits: np.ndarray, v_bits, batches=None):
         """v_bits: bf16 bits [B][Hk][cap][d], or (codes, scales) for a turbo4v cache."""
         idx = list(range(self.batch)) if batches is None else list(batches)
+        if self.kv_format == "turbo4":
+            (kc, ks), (vc, vs) = k_bits, v_bits
+            for j, b in enumerate(idx):
+                for dst, src in ((self.kc, kc), (self.ks, ks), (self.vc, vc), (self.vs, vs)):
+                    dst[b].copy_(torch.from_numpy(np.ascontiguousarray(src[j], np.uint8)))
+            return
         if self.kv_format == "turbo4v":
             codes, scales = v_bits
             for j, b in enumerate(idx):
@@ -101,6 +118,9 @@ class DeviceLayer:
     def read_cache(self, batches=None):
         """(K bits, V bits), or (K bits, (codes, scales)) for a turbo4v cache."""
         idx = list(range(self.batch)) if batches is None else list(batches)
+        if self.kv_format == "turbo4":
+            g = lambda t: np.stack([t[b].cpu().numpy() for b in idx])
+            return (g(self.kc), g(self.ks)), (g(self.vc), g(self.vs))
         if self.kv_format == "turbo4v":
             k = np.stack([self.k[b].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
                           for b in idx])

@@ -33,6 +33,7 @@ EXPORTS = (
     "gattn_layer_launches_per_step", "gattn_layer_set_events", "gattn_layer_dequant_device_static",
     "gattn_layer_set_path", "gattn_layer_step_block", "gattn_kv_register_turbo4v",
     "gattn_turbo4_codebook", "gattn_turbo4_quantize_device", "gattn_layer_set_mask",
+    "gattn_kv_register_turbo4",
 )
 
 
@@ -72,6 +73,13 @@ class gattn_kv_turbo4v_desc(C.Structure):
                 ("k_stride_batch", C.c_int64), ("code_stride_head", C.c_int64),
                 ("code_stride_batch", C.c_int64), ("scale_stride_head", C.c_int64),
                 ("scale_stride_batch", C.c_int64)]
+
+
+class gattn_kv_turbo4_desc(C.Structure):
+    _fields_ = [("k_codes", C.c_void_p), ("k_scales", C.c_void_p), ("v_codes", C.c_void_p),
+                ("v_scales", C.c_void_p), ("batch", C.c_int32), ("capacity", C.c_int32),
+                ("code_stride_head", C.c_int64), ("code_stride_batch", C.c_int64),
+                ("scale_stride_head", C.c_int64), ("scale_stride_batch", C.c_int64)]
 
 
 class gattn_mask(C.Structure):
@@ -124,6 +132,7 @@ def lib():
         L.gattn_turbo4_codebook.argtypes = [p, p]
         L.gattn_turbo4_quantize_device.argtypes = [p, i64, i32, p, p, p]
         L.gattn_layer_set_mask.argtypes = [p, C.POINTER(gattn_mask)]
+        L.gattn_kv_register_turbo4.argtypes = [p, C.POINTER(gattn_kv_turbo4_desc), C.POINTER(p)]
         for name in ("gattn_cfg_validate", "gattn_layer_create", "gattn_layer_set_weights",
                      "gattn_kv_register", "gattn_layer_step", "gattn_layer_poll_status",
                      "gattn_layer_set_taps", "gattn_pack_affine_host", "gattn_unpack_codes_device",
@@ -131,7 +140,7 @@ def lib():
                      "gattn_layer_dequant_device_static", "gattn_layer_set_path",
                      "gattn_layer_step_block", "gattn_kv_register_turbo4v",
                      "gattn_turbo4_codebook", "gattn_turbo4_quantize_device",
-                     "gattn_layer_set_mask"):
+                     "gattn_layer_set_mask", "gattn_kv_register_turbo4"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -218,6 +227,16 @@ def layer_set_mask(layer: int, mask: int | None, heads: int = 1, positions: int 
         return
     m = gattn_mask(mask, heads, positions, *strides)
     _check(lib().gattn_layer_set_mask(layer, C.byref(m)))
+
+
+def kv_register_turbo4(layer: int, k_codes: int, k_scales: int, v_codes: int, v_scales: int,
+                       batch: int, capacity: int, code_strides, scale_strides) -> int:
+    """Register a symmetric Turbo4 cache; strides (head, batch) in bytes, shared by K and V."""
+    d = gattn_kv_turbo4_desc(k_codes, k_scales, v_codes, v_scales, batch, capacity,
+                             *code_strides, *scale_strides)
+    h = C.c_void_p()
+    _check(lib().gattn_kv_register_turbo4(layer, C.byref(d), C.byref(h)))
+    return h.value
 
 
 def turbo4_codebook():

@@ -153,3 +153,73 @@ def test_turbo_is_refused_on_the_one_kernel_path():
     with pytest.raises(gattn.GattnError) as ei:
         _run_turbo(spec, case, codes, scales, path=gattn.PATH_FUSED)
     assert ei.value.status == 2
+
+
+# ------------------------------------------------- symmetric Turbo4 cache
+
+def _run_sym(spec, case, kplanes, vplanes, head_chunk=True):
+    dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap, kv_format="turbo4",
+                     head_chunk=head_chunk)
+    try:
+        dl.load_cache(kplanes, vplanes)
+        M, H, d = spec.batch * spec.q_len, spec.num_heads, spec.head_dim
+        out = torch.full((spec.batch, spec.q_len, spec.hidden), float("nan"), dtype=torch.bfloat16,
+                         device="cuda")
+        ta = torch.zeros((M, H * d), dtype=torch.float32, device="cuda")
+        dl.set_taps(None, ta)
+        pd = torch.from_numpy(np.ascontiguousarray(case.pos, np.int32)).cuda()
+        dl.step(x_to_device(spec, case.x), pd, out)
+        dl.poll()
+        (kc, ks), (vc, vs) = dl.read_cache()
+        return dict(out=out.float().cpu().numpy().astype(np.float64),
+                    attn=ta.cpu().numpy().astype(np.float64).reshape(spec.batch, spec.q_len, H, d),
+                    kc=kc, ks=ks, vc=vc, vs=vs)
+    finally:
+        dl.close()
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_symmetric_turbo_layer_parity(name):
+    spec = CASES[name]
+    case = make_case(spec)
+    vcodes, vscales = synth.turbo4v_cache(spec, case.cap)
+    kcodes, kscales = synth.turbo4v_cache(spec, case.cap, plane="k")
+    got = _run_sym(spec, case, (kcodes.copy(), kscales.copy()), (vcodes.copy(), vscales.copy()))
+    okc, oks, ovc, ovs = kcodes.copy(), kscales.copy(), vcodes.copy(), vscales.copy()
+    out, ty, ta = orc.layer_step_ext(spec, case.orc_weights, synth.x_values(spec, case.x), None,
+                                     None, case.pos, turbo=(ovc, ovs), turbo_k=(okc, oks),
+                                     taps=True)
+    ok, rep = refs.close(got["out"], out)
+    assert ok, f"out: {rep}"
+    ok, rep = refs.close(got["attn"], ta)
+    assert ok, f"attention: {rep}"
+    H, Hk, d, R = spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.q_len
+    rd = orc.rotary_dims(d, spec.partial_rotary_factor)
+    kn_w = synth.bf16_bits_to_f32(case.kn).astype(np.float64)
+    eps, theta = float(np.float32(spec.rms_eps)), float(np.float32(spec.rope_theta))
+    exact = rows = 0
+    for b in range(spec.batch):
+        p = int(case.pos[b])
+        for r in range(R):
+            for kh in range(Hk):
+                kraw = ty[b, r, 2 * H * d + kh * d:2 * H * d + (kh + 1) * d]
+                k64 = orc.rope(orc.rms_norm(kraw, kn_w, eps), rd, p + r, theta)
+                v64 = ty[b, r, 2 * H * d + Hk * d + kh * d:2 * H * d + Hk * d + (kh + 1) * d]
+                for g, w, val in (((got["kc"], got["ks"]), (okc, oks), k64),
+                                  ((got["vc"], got["vs"]), (ovc, ovs), v64)):
+                    rows += 1
+                    gc, gs = g[0][b, kh, p + r], g[1][b, kh, p + r]
+                    wc, ws = w[0][b, kh, p + r], w[1][b, kh, p + r]
+                    if _near_bf16_midpoint(val).any():
+                        gv = orc.turbo4_dequant_rows(gc[None], gs[None])[0]
+                        wv = orc.turbo4_dequant_rows(wc[None], ws[None])[0]
+                        assert np.linalg.norm(gv - wv) <= 0.2 * np.linalg.norm(wv)
+                        continue
+                    assert np.array_equal(gc, wc) and np.array_equal(gs, ws), (name, b, kh, r)
+                    exact += 1
+        for g, before in ((got["kc"], kcodes), (got["ks"], kscales), (got["vc"], vcodes),
+                          (got["vs"], vscales)):
+            mask = np.ones(g.shape[1:3], bool)
+            mask[:, p:p + R] = False
+            assert np.array_equal(g[b][mask], before[b][mask])
+    assert exact > 0, rows
