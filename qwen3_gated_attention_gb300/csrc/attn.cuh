@@ -49,30 +49,45 @@ struct AttnSmem {
 
 // One Turbo4 dequantization item: 32 columns (c) of token tl of a tile, from
 // its 16 code bytes and 2 E4M3 scales into the fp16 tile (the bf16 tile's
-// swizzled layout).  A 16-byte store is served eight lanes at a time; those
-// lanes share a token and take its 32-column pieces c, so each lane writes its
-// four 8-column chunks in an order rotated by c: at every step the eight lanes
-// hit eight different bank groups.  live == false writes zeros.
-// Shared-memory addresses: dst the fp16 tile, cst / sst the code / scale rows.
+// swizzled layout).  Split into its loads and its conversion so that a thread
+// issues the loads of all its items before converting any: the shared-memory
+// accesses are ordered asm statements, so only this order lets the items'
+// arithmetic overlap.
+struct TurboItem {
+    uint4 cb;
+    uint32_t sb;
+};
+
+// Shared-memory addresses: cst / sst the code / scale rows.
 template <int DB>
-__device__ __forceinline__ void turbo_dequant_item(uint32_t dst, uint32_t cst, uint32_t sst, int tl,
-                                                   int c, bool live, const uint32_t (&lvl_lo)[2],
-                                                   const uint32_t (&lvl_hi)[2])
+__device__ __forceinline__ TurboItem turbo_item_load(uint32_t cst, uint32_t sst, int tl, int c,
+                                                     bool live)
+{
+    TurboItem it{make_uint4(0, 0, 0, 0), 0u};
+    if (live) {
+        it.cb = lds_v4(cst + tl * (DB * 32) + c * 16);
+        it.sb = lds_u16(sst + tl * (DB * 4) + c * 2);
+    }
+    return it;
+}
+
+// A 16-byte store is served eight lanes at a time; those lanes share a token
+// and take its 32-column pieces c, so each lane writes its four 8-column
+// chunks in an order rotated by c: at every step the eight lanes hit eight
+// different bank groups.  A not-live item (zero scales) writes zeros.
+template <int DB>
+__device__ __forceinline__ void turbo_item_store(uint32_t dst, const TurboItem &it, int tl, int c,
+                                                 const uint32_t (&lvl_lo)[2],
+                                                 const uint32_t (&lvl_hi)[2])
 {
     constexpr int kRotShift = DB == 4 ? 1 : 0;
     const int rot = (c >> kRotShift) & 3;
-    uint4 cb = make_uint4(0, 0, 0, 0);
-    __half2 s0 = __float2half2_rn(0.f), s1 = s0;
-    if (live) {
-        cb = lds_v4(cst + tl * (DB * 32) + c * 16);
-        const uint32_t sb = lds_u16(sst + tl * (DB * 4) + c * 2);
-        s0 = __half2half2(e4m3_to_half((uint8_t)(sb & 0xFF)));
-        s1 = __half2half2(e4m3_to_half((uint8_t)(sb >> 8)));
-    }
+    const __half2 s0 = __half2half2(e4m3_to_half((uint8_t)(it.sb & 0xFF)));
+    const __half2 s1 = __half2half2(e4m3_to_half((uint8_t)(it.sb >> 8)));
 #pragma unroll
     for (int st = 0; st < 4; ++st) {
         const int q = (st + rot) & 3;            // bytes 4q .. 4q + 3
-        const uint32_t wq = q == 0 ? cb.x : (q == 1 ? cb.y : (q == 2 ? cb.z : cb.w));
+        const uint32_t wq = q == 0 ? it.cb.x : (q == 1 ? it.cb.y : (q == 2 ? it.cb.z : it.cb.w));
         const __half2 sc = q < 2 ? s0 : s1;      // groups 2c, 2c + 1
         uint32_t o[4];
         turbo4_levels8(wq, lvl_lo, lvl_hi, o);
@@ -307,11 +322,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (ok && warp * 8 < ntok) {
                     const uint32_t lvl_lo[2] = {a.vq_tl[0], a.vq_tl[1]};
                     const uint32_t lvl_hi[2] = {a.vq_th[0], a.vq_th[1]};
-                    for (int it2 = lane; it2 < 8 * DB * 2; it2 += 32) {
+                    constexpr int kKItems = (8 * DB * 2 + 31) / 32;
+                    TurboItem ki[kKItems];
+#pragma unroll
+                    for (int k = 0; k < kKItems; ++k) {
+                        const int it2 = lane + 32 * k;
                         const int tl = warp * 8 + it2 / (DB * 2), c = it2 % (DB * 2);
-                        turbo_dequant_item<DB>(smem_u32(dqk), smem_u32(kst),
-                                               smem_u32(kst) + L::kVCodeBytes, tl, c,
-                                               tl < ntok && t0 + tl < Lb, lvl_lo, lvl_hi);
+                        ki[k] = turbo_item_load<DB>(smem_u32(kst), smem_u32(kst) + L::kVCodeBytes,
+                                                    tl, c, it2 < 8 * DB * 2 && tl < ntok && t0 + tl < Lb);
+                    }
+#pragma unroll
+                    for (int k = 0; k < kKItems; ++k) {
+                        const int it2 = lane + 32 * k;
+                        const int tl = warp * 8 + it2 / (DB * 2), c = it2 % (DB * 2);
+                        if (it2 < 8 * DB * 2)
+                            turbo_item_store<DB>(smem_u32(dqk), ki[k], tl, c, lvl_lo, lvl_hi);
                     }
                     __syncwarp();
                 }
@@ -429,10 +454,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t cst = smem_u32(vst), sst = cst + L::kVCodeBytes;
                     const uint32_t dq_a = smem_u32(dq);
                     const uint32_t lvl_lo[2] = {a.vq_tl[0], a.vq_tl[1]}, lvl_hi[2] = {a.vq_th[0], a.vq_th[1]};
-                    for (int idx = tid; idx < kAttnTile * DB * 2; idx += kAttnWarps * 32) {
+                    // every item's loads first, then their conversions (see TurboItem)
+                    constexpr int kItems = (kAttnTile * DB * 2 + kAttnWarps * 32 - 1) /
+                                           (kAttnWarps * 32);
+                    TurboItem vi[kItems];
+#pragma unroll
+                    for (int k = 0; k < kItems; ++k) {
+                        const int idx = tid + k * kAttnWarps * 32;
                         const int tl = idx / (DB * 2), c = idx % (DB * 2);   // token, 32 columns
-                        turbo_dequant_item<DB>(dq_a, cst, sst, tl, c, tl < ntok && t0 + tl < Lb,
-                                               lvl_lo, lvl_hi);
+                        vi[k] = turbo_item_load<DB>(cst, sst, tl, c,
+                                                    idx < kAttnTile * DB * 2 && tl < ntok &&
+                                                        t0 + tl < Lb);
+                    }
+#pragma unroll
+                    for (int k = 0; k < kItems; ++k) {
+                        const int idx = tid + k * kAttnWarps * 32;
+                        const int tl = idx / (DB * 2), c = idx % (DB * 2);
+                        if (idx < kAttnTile * DB * 2)
+                            turbo_item_store<DB>(dq_a, vi[k], tl, c, lvl_lo, lvl_hi);
                     }
                 }
             }
