@@ -22,6 +22,14 @@
  * head-chunk plan); TensorFold issue 503 "Option C" (generic affine row decoder,
  * 2-8 bit, groups 32/64/128).
  *
+ * Optional parts, each on the same kernels: the decoder block around the layer
+ * (input RMSNorm, residual add, post-attention RMSNorm: gattn_layer_step_block;
+ * Atlas mod.rs module doc, FullAttentionLayer input_ln / post_ln), Turbo4
+ * quantized caches (Bf16KTurbo4V and symmetric Turbo4: gattn_kv_register_turbo4v,
+ * gattn_kv_register_turbo4; Atlas mod.rs MetalKvDtype, LayerKvCache) and
+ * attention masks (gattn_layer_set_mask; DS4Server issue 113, broadcast and
+ * head-specific masks of the verify route).
+ *
  * Conventions for every entry point:
  *   - Pointers marked (device) are CUDA device addresses, (host) host memory.
  *   - Weights, caches, x, out and cache_pos are BORROWED: the library never

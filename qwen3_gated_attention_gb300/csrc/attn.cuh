@@ -24,19 +24,17 @@ struct AttnSmem {
     static constexpr int kStageBytes = kKBytes + kVBytes;     // K + V
     static constexpr int kDqBytes = VQ ? kTileBytes : 0;      // Turbo4: dequantized fp16 V tile
     static constexpr int kDqKBytes = VQ == 2 ? kTileBytes : 0;    // and K tile
-    static constexpr int kLutBytes = 0;
     static constexpr int kQBytes = MT * 16 * DB * 64 * 2;
     static constexpr int kPBytes = MT * 16 * 128;             // rows x 64 tokens bf16
     // as many K/V stages (2 .. kAttnStages) as fit beside the rest in 227 KB
-    static constexpr int kFixed = kDqBytes + kDqKBytes + kLutBytes + kQBytes + kPBytes +
+    static constexpr int kFixed = kDqBytes + kDqKBytes + kQBytes + kPBytes +
                                   2 * kAttnWarps * 64 * 4 + 40 * 8 + 2 * kAttnStages * 8 + 256 + 1024;
     static constexpr int kFit = (227 * 1024 - kFixed) / kStageBytes;
     static constexpr int kNStages = kFit < 2 ? 2 : (kFit > kAttnStages ? kAttnStages : kFit);
     static constexpr int kStages = kNStages * kStageBytes;
     static constexpr int kDq = kStages;
     static constexpr int kDqK = kDq + kDqBytes;
-    static constexpr int kLut = kDqK + kDqKBytes;
-    static constexpr int kQ = kLut + kLutBytes;
+    static constexpr int kQ = kDqK + kDqKBytes;
     static constexpr int kP = kQ + kQBytes;
     static constexpr int kRedMax = kP + kPBytes;              // [8][64] floats
     static constexpr int kRedL = kRedMax + kAttnWarps * 64 * 4;

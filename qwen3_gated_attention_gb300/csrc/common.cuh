@@ -240,13 +240,6 @@ __device__ __forceinline__ void ldsm_x2_trans(uint32_t &r0, uint32_t &r1, uint32
 
 // explicit shared-memory accesses (a pointer that went through integer
 // alignment arithmetic no longer tells the compiler its address space)
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
-
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr)
 {
     uint16_t v;

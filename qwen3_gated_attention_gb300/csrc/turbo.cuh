@@ -1,9 +1,10 @@
-// turbo.cuh -- the Turbo4 V-cache format (the Bf16KTurbo4V cache of the
-// Atlas qwen3_5 forward page: MetalKvDtype / LayerKvCache): K stays bf16, V is
-// stored in a Walsh-Hadamard-rotated basis as 4-bit Lloyd-Max codebook indices
-// with one FP8 E4M3 scale per group of 16 coordinates ("matched-norm L2").
+// turbo.cuh -- the Turbo4 KV-cache format of the Atlas qwen3_5 forward page
+// (MetalKvDtype / LayerKvCache): a row is stored in a Walsh-Hadamard-rotated
+// basis as 4-bit Lloyd-Max codebook indices with one FP8 E4M3 scale per group
+// of 16 coordinates ("matched-norm L2").  Bf16KTurbo4V stores V this way and
+// keeps K in bf16; the symmetric Turbo4 format stores both.
 //
-// Per V row of d values (the bf16 row the cache would otherwise hold):
+// Per row of d values (the bf16 row the cache would otherwise hold):
 //   y   = H v / sqrt(d)            H: Sylvester Hadamard of order d, natural order
 //   per group g of 16 consecutive y:
 //   u_i = y_i / rms(y_g)           idx_i = number of decision thresholds below u_i
@@ -13,8 +14,9 @@
 // 2, 4, ..., the rounded 1/sqrt(d) factor after them, pairwise sums over a
 // group ((a0 + a1) + (a2 + a3)) + ..., correctly rounded sqrt and division --
 // written with explicit _rn intrinsics so nothing is contracted into an FMA.
-// Dequantized: v = H (s * c(idx)) / sqrt(d); the attention applies the
-// rotation once to its output instead of to every V row (it is linear).
+// Dequantized: v = H (s * c(idx)) / sqrt(d).  The attention never rotates a
+// cached row back: it rotates each output row once (values, by linearity) and
+// each q row once (keys: q . H k / sqrt(d) = (H q / sqrt(d)) . k).
 #pragma once
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>

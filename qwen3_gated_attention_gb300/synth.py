@@ -97,6 +97,10 @@ WORKLOADS = {
                            cache_pos=(46,)),
     "verify_2k_p2048": _spec("verify_2k_p2048", 2048, 24, 2, 256, (4,) * 4, (64,) * 4, 1, 4,
                              "bf16", cache_pos=(2048,)),
+    # the same verify at 32 new rows (a short prefill / wide speculative verify:
+    # the head-chunk route's upper bound on q_len)
+    "verify_2k_r32": _spec("verify_2k_r32", 2048, 24, 2, 256, (4,) * 4, (64,) * 4, 1, 32,
+                           "bf16", cache_pos=(2048,)),
     # 9B-class batched decode: 32 sequences, lengths U{512..8192}
     "batched_9b": _spec("batched_9b", 4096, 32, 8, 256, (4,) * 4, (64,) * 4, 32, 1, "bf16",
                         length_range=(512, 8192)),

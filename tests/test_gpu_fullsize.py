@@ -101,3 +101,9 @@ def test_batched_9b_turbo4v_full_size():
                 exact += 1
     assert exact > 0
     print("batched_9b turbo4v", idx, rep, "exact V rows", exact)
+
+
+def test_wide_verify_r32_full_size():
+    """The 2K-context verify at 32 new rows (the head-chunk route's widest
+    case: one head per chunk) at full size."""
+    _run("verify_2k_r32", lambda pos: [0])
