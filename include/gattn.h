@@ -70,7 +70,7 @@ enum { GATTN_PROJ_Q = 0, GATTN_PROJ_K = 1, GATTN_PROJ_V = 2, GATTN_PROJ_O = 3 };
  * Layer configuration (mirrors the config fields of Qwen35ForwardConfig).
  *   hidden                 Hd, width of x and out
  *   num_heads, num_kv_heads H, Hk (H % Hk == 0, gqa = H / Hk; query head h uses KV head h / gqa)
- *   head_dim               d; d % 64 == 0 and d <= 256 on this build
+ *   head_dim               d; d % 64 == 0 and d <= 256 in this library
  *   partial_rotary_factor  prf in (0, 1]; rotary dims rd = trunc(d * prf), even and >= 2
  *   rope_theta             base of inv_freq_i = theta^(-2i/rd)
  *   rms_eps                QK-RMSNorm epsilon (inside the square root)
@@ -364,7 +364,7 @@ int32_t gattn_head_chunk_plan(int32_t q_len, int32_t num_heads, int32_t num_kv_h
 /*
  * Which kernels run a step (an execution choice; both compute the same layer,
  * equal up to fp32 summation order):
- *   GATTN_PATH_AUTO   (default) the faster path for the step; in this build
+ *   GATTN_PATH_AUTO   (default) the faster path for the step; in this library
  *                     that is the five-kernel path.
  *   GATTN_PATH_FUSED  the one-kernel path; a step that does not fit it fails
  *                     with GATTN_E_UNSUPPORTED (nothing is launched).

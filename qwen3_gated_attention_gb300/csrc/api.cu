@@ -85,9 +85,9 @@ gattn_status validate(const gattn_cfg *c)
         return fail(GATTN_E_INVALID_ARG, "max_batch and max_q_len must be > 0");
     if (c->head_chunk != 0 && c->head_chunk != 1)
         return fail(GATTN_E_INVALID_ARG, "head_chunk must be 0 or 1");
-    // shapes this build implements
+    // shapes this library implements
     if (c->head_dim % 64 || c->head_dim > 256)
-        return fail(GATTN_E_UNSUPPORTED, "head_dim %d: this build needs a multiple of 64 <= 256",
+        return fail(GATTN_E_UNSUPPORTED, "head_dim %d: this library needs a multiple of 64 <= 256",
                     c->head_dim);
     if (c->hidden % 128)
         return fail(GATTN_E_UNSUPPORTED, "hidden %d must be a multiple of 128", c->hidden);

@@ -118,7 +118,7 @@ def test_block_over_a_turbo_cache():
         assert ok, f"{what}: {rep}"
     p = int(case.pos[0])
     assert_rows_close(k[0, :, p:p + 1], kc[0, :, p:p + 1], "block turbo k")
-    # the block's layer input is the normed row, so judge the V rows on their dequantized values
+    # the block's layer input is the normed row, so the V rows are checked on their dequantized values
     for kh in range(spec.num_kv_heads):
         gv = orc.turbo4_dequant_rows(gc[0, kh, p][None], gs[0, kh, p][None])[0]
         wv = orc.turbo4_dequant_rows(oc[0, kh, p][None], os_[0, kh, p][None])[0]
