@@ -68,8 +68,9 @@ enum { GATTN_PROJ_Q = 0, GATTN_PROJ_K = 1, GATTN_PROJ_V = 2, GATTN_PROJ_O = 3 };
 
 /*
  * Layer configuration (mirrors the config fields of Qwen35ForwardConfig).
- *   hidden                 Hd, width of x and out
- *   num_heads, num_kv_heads H, Hk (H % Hk == 0, gqa = H / Hk; query head h uses KV head h / gqa)
+ *   hidden                 Hd, width of x and out; Hd % 128 == 0 and Hd <= 16384
+ *   num_heads, num_kv_heads H, Hk (H % Hk == 0, gqa = H / Hk; query head h uses KV head h / gqa);
+ *                          H * d % 128 == 0 and H * d <= 16384
  *   head_dim               d; d % 64 == 0 and d <= 256 in this library
  *   partial_rotary_factor  prf in (0, 1]; rotary dims rd = trunc(d * prf), even and >= 2
  *   rope_theta             base of inv_freq_i = theta^(-2i/rd)
@@ -77,7 +78,8 @@ enum { GATTN_PROJ_Q = 0, GATTN_PROJ_K = 1, GATTN_PROJ_V = 2, GATTN_PROJ_O = 3 };
  *   bits, group_size       default code width {2,3,4,5,6,8} and group {32,64,128}
  *   proj_bits[4], proj_group[4]  per projection q,k,v,o; 0 = the default
  *   x_dtype                GATTN_DTYPE_F32 or GATTN_DTYPE_BF16 (out is always bf16)
- *   max_batch, max_q_len   upper bounds for step(); max_batch*max_q_len <= 32
+ *   max_batch, max_q_len   upper bounds for step(); max_batch*max_q_len <= 32 (<= 16 for
+ *                          fp32 x)
  *   head_chunk             1 = the verify head-chunk plan is on (the pages'
  *                          default), 0 = off; both routes give the same result
  */

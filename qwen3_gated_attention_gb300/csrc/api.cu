@@ -43,6 +43,8 @@ gattn_status fail(gattn_status st, const char *fmt, ...)
             return fail(GATTN_E_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));             \
     } while (0)
 
+constexpr int kMaxHidden = 16384;   // hidden and num_heads*head_dim
+
 bool bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
 bool group_ok(int g) { return g == 32 || g == 64 || g == 128; }
 
@@ -91,6 +93,11 @@ gattn_status validate(const gattn_cfg *c)
                     c->head_dim);
     if (c->hidden % 128)
         return fail(GATTN_E_UNSUPPORTED, "hidden %d must be a multiple of 128", c->hidden);
+    // sizes whose weight tiles, scratch and row counts stay within the kernels'
+    // 32-bit indexes (checked before any product of two fields is formed)
+    if (c->hidden > kMaxHidden || c->num_heads > kMaxHidden / 64 ||
+        c->num_heads * c->head_dim > kMaxHidden)
+        return fail(GATTN_E_UNSUPPORTED, "hidden and num_heads*head_dim must be <= %d", kMaxHidden);
     if ((c->num_heads * c->head_dim) % 128)
         return fail(GATTN_E_UNSUPPORTED, "num_heads*head_dim must be a multiple of 128");
     if (proj_bits(*c, 0) != proj_bits(*c, 1) || proj_bits(*c, 0) != proj_bits(*c, 2) ||
@@ -98,11 +105,11 @@ gattn_status validate(const gattn_cfg *c)
         return fail(GATTN_E_UNSUPPORTED, "q, k and v must share bits and group (one fused launch)");
     if (proj_group(*c, 3) > c->head_dim)
         return fail(GATTN_E_UNSUPPORTED, "o_proj group must not exceed head_dim");
-    if (c->max_batch * c->max_q_len > (c->x_dtype == GATTN_DTYPE_F32 ? 16 : 32))
+    if (c->max_batch > 32 || c->max_q_len > 32 ||
+        c->max_batch * c->max_q_len > (c->x_dtype == GATTN_DTYPE_F32 ? 16 : 32))
         return fail(GATTN_E_UNSUPPORTED,
-                    "max_batch*max_q_len must be <= 32 (<= 16 for fp32 x, which takes two fp16 planes)");
-    if (c->max_batch > 32)
-        return fail(GATTN_E_UNSUPPORTED, "max_batch must be <= 32");
+                    "max_batch, max_q_len and their product must be <= 32 (product <= 16 for fp32 x, "
+                    "which takes two fp16 planes)");
     const int gqa = c->num_heads / c->num_kv_heads;
     if (gqa > 64 * kMaxRowBlocks)
         return fail(GATTN_E_UNSUPPORTED, "gqa too large");

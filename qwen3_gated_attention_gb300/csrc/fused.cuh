@@ -49,11 +49,6 @@ __device__ __forceinline__ unsigned ld_relaxed(const unsigned *p)
     return v;
 }
 
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // gpu-scope release/acquire fence (cumulative: after a CTA barrier it covers
 // the other threads' writes that the barrier ordered before it)
 __device__ __forceinline__ void fence_acq_rel_gpu()
@@ -67,13 +62,6 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v)
     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
                  : "memory");
     return old;
-}
-
-// orders this thread's generic-proxy global accesses with its async-proxy
-// (bulk / tensor copy) accesses
-__device__ __forceinline__ void fence_proxy_async_global()
-{
-    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Next entry of `size` bytes in a ring of `rb` bytes, `h` being where the

@@ -62,6 +62,13 @@ def test_workload_configs_are_admitted(name):
     (dict(hidden=200), 2),
     (dict(max_batch=64), 2),
     (dict(bits=(4, 8, 4, 4)), 2),                # q/k/v widths must match
+    # sizes past the kernels' 32-bit indexes, and products of fields that would
+    # overflow a 32-bit int if they were formed before the bounds are checked
+    (dict(hidden=16384 + 128), 2),
+    (dict(num_heads=2 ** 23, num_kv_heads=2 ** 23, head_dim=256), 2),
+    (dict(max_batch=2, max_q_len=2 ** 31 - 1), 2),
+    (dict(max_batch=2 ** 30, max_q_len=2 ** 30), 2),
+    (dict(max_batch=1, max_q_len=33), 2),
 ])
 def test_inadmissible_configs_are_rejected(change, status):
     spec = synth.WORKLOADS["tiny"]
