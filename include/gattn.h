@@ -3,7 +3,8 @@
  *
  * One thing runs here: the Qwen3.5-family full-attention decoder layer at
  * decode and speculative-verify time, for B sequences of R new rows each
- * (R = q_len, 1..4 is the target range):
+ * (R = q_len: 1..4 for decode and the pages' verify rows, up to 32 for wider
+ * verify rows and short prefill chunks, with B*R <= 32):
  *
  *   q_full = Wq x  (doubled q_proj: per head h the rows [h*2d, h*2d+d) are the
  *                   query and [h*2d+d, (h+1)*2d) the output gate)
@@ -159,16 +160,27 @@ int32_t gattn_rotary_dims(const gattn_cfg *cfg);
 
 /* Create a layer on the current CUDA device: validates cfg, allocates scratch
  * (sized by max_batch/max_q_len) and the repacked-weight buffers.  *out owned
- * by the caller, release with gattn_layer_destroy. */
+ * by the caller, release with gattn_layer_destroy.  Errors: those of
+ * gattn_cfg_validate (GATTN_E_INVALID_ARG, GATTN_E_UNSUPPORTED; *out = NULL),
+ * GATTN_E_CUDA when an allocation or device query fails (nothing leaks). */
 gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out);
 
-/* Repack the interchange weights into the library's device tile layout (same
- * bytes per step).  Runs and synchronizes on `stream`; the caller may free the
- * interchange buffers after it returns. */
+/* Repack the interchange weights (TensorFold issue 503 "Option C" affine rows,
+ * layout of gattn_proj) into the library's device tile layout (same bytes per
+ * step); copies q_norm and k_norm.  Runs and synchronizes on `stream`; the
+ * caller may free the interchange buffers after it returns.  Errors:
+ * GATTN_E_INVALID_ARG for a NULL layer, weights or buffer; GATTN_E_CUDA when a
+ * launch or copy fails.  May be called again to replace the weights. */
 gattn_status gattn_layer_set_weights(gattn_layer *layer, const gattn_weights *w, gattn_stream stream);
 
-/* Register a cache for this layer: checks sizes/alignment and encodes the TMA
- * tensor maps once.  The cache memory must outlive the registration. */
+/* Register a cache for this layer (Atlas qwen3_5 forward page, LayerKvCache:
+ * the caller pre-allocates, the step appends at cache_pos): checks sizes and
+ * alignment and encodes the TMA tensor maps once.  *out is owned by the
+ * caller (gattn_kv_destroy); the cache memory is borrowed and must outlive the
+ * registration, and the registration must not outlive the layer.  Errors:
+ * GATTN_E_INVALID_ARG for a NULL or misaligned pointer, batch <= 0, capacity
+ * < 16, a stride that is not a positive multiple of 8, or a layout the TMA
+ * encoder rejects; GATTN_E_CUDA when the encoder cannot be found. */
 gattn_status gattn_kv_register(gattn_layer *layer, const gattn_kv_desc *desc, gattn_kv **out);
 
 /*
@@ -237,7 +249,9 @@ gattn_status gattn_kv_register_turbo4(gattn_layer *layer, const gattn_kv_turbo4_
 /* The Turbo4 codebook as the kernels use it (host, no GPU): the 16 levels of
  * the Lloyd-Max quantizer of N(0, 1), ascending, rounded to fp32, and the 15
  * decision thresholds between them (midpoints taken in double, then rounded;
- * the middle one is 0).  Computed once per process by Lloyd's iteration. */
+ * the middle one is 0).  Computed once per process by Lloyd's iteration (the
+ * pages name the codebook, Atlas MetalKvDtype::Turbo4, but print no values).
+ * GATTN_E_INVALID_ARG for a NULL array. */
 gattn_status gattn_turbo4_codebook(float levels[16], float thresholds[15]);
 
 /*
@@ -249,6 +263,8 @@ gattn_status gattn_turbo4_codebook(float levels[16], float thresholds[15]);
  * sqrt(ss/16), code_i = number of thresholds below u_i, scale = E4M3 (nearest,
  * ties to even, saturating at 448) of sqrt(ss / pairwise sum of level^2); a
  * zero group gets codes 0 and scale 0.  d a power of two from 64 to 256.
+ * GATTN_E_INVALID_ARG for rows < 0, a NULL pointer with rows > 0 or another
+ * d; GATTN_E_CUDA when the launch fails.  rows == 0 launches nothing.
  */
 gattn_status gattn_turbo4_quantize_device(const void *v_bf16, int64_t rows, int32_t d,
                                           void *codes, void *scales, gattn_stream stream);
@@ -266,16 +282,25 @@ gattn_status gattn_turbo4_quantize_device(const void *v_bf16, int64_t rows, int3
  * the device (its cache is untouched and its out rows are zero) and the next
  * gattn_layer_poll_status() returns GATTN_E_DEVICE_RANGE.  One step at a time
  * per layer handle: steps of one handle on different streams race on its scratch.
+ * Errors (nothing is launched): GATTN_E_INVALID_ARG for a NULL argument, a
+ * cache registered with another layer, batch outside [1, min(max_batch, cache
+ * batch)] or q_len outside [1, max_q_len]; GATTN_E_STATE before
+ * gattn_layer_set_weights; GATTN_E_UNSUPPORTED for a step the selected path or
+ * the set mask does not take (gattn_layer_set_path, gattn_layer_set_mask);
+ * GATTN_E_CUDA when a launch fails.
  */
 gattn_status gattn_layer_step(gattn_layer *layer, const void *x, gattn_kv *kv,
                               const int32_t *cache_pos, int32_t batch, int32_t q_len,
                               void *out, gattn_stream stream);
 
 /* Synchronize `stream`, then read and clear the layer's device status word:
- * GATTN_OK, GATTN_E_DEVICE_RANGE or GATTN_E_DEVICE_TIMEOUT. */
+ * GATTN_OK, GATTN_E_DEVICE_RANGE or GATTN_E_DEVICE_TIMEOUT (GATTN_E_INVALID_ARG
+ * for a NULL layer, GATTN_E_CUDA when the synchronization or read fails). */
 gattn_status gattn_layer_poll_status(gattn_layer *layer, gattn_stream stream);
 
-/* Ask the next steps to also write the taps (NULL or all-NULL turns them off). */
+/* Ask the next steps to also write the taps (layout of gattn_taps; borrowed
+ * device buffers; NULL or all-NULL turns them off).  GATTN_E_INVALID_ARG for a
+ * NULL layer.  Test instrumentation, not part of the layer's computation. */
 gattn_status gattn_layer_set_taps(gattn_layer *layer, const gattn_taps *taps);
 
 /*
@@ -300,10 +325,17 @@ typedef struct gattn_mask {
     int64_t stride_row, stride_head, stride_batch;
 } gattn_mask;
 
-/* Set (or with NULL / mask->mask == NULL clear) the attention mask. */
+/* Set (or with NULL / mask->mask == NULL clear) the attention mask of the
+ * following steps.  GATTN_E_INVALID_ARG for a NULL layer, heads other than 1
+ * or num_heads, positions <= 0, stride_row < positions or a negative stride. */
 gattn_status gattn_layer_set_mask(gattn_layer *layer, const gattn_mask *mask);
 
+/* Free a layer and everything it owns (NULL is a no-op).  Call it after the
+ * layer's last step has finished on the GPU and after destroying the caches
+ * registered with it; borrowed buffers are left alone. */
 void gattn_layer_destroy(gattn_layer *layer);
+/* Free a cache registration (NULL is a no-op); the cache memory is the
+ * caller's and is left alone. */
 void gattn_kv_destroy(gattn_kv *kv);
 
 /* Thread-local message of the last failed call on this thread ("" if none). */
@@ -321,13 +353,18 @@ gattn_status gattn_pack_affine_host(const float *w, int64_t N, int64_t K, int32_
                                     int32_t group, uint32_t *packed, uint16_t *scales,
                                     uint16_t *biases);
 
-/* Decode interchange codes on the GPU (device in/out): codes uint8 [N][K]. */
+/* Decode interchange codes on the GPU (device in/out): codes uint8 [N][K],
+ * enqueued on `stream`.  GATTN_E_INVALID_ARG for a NULL pointer, negative
+ * sizes, bits outside 1..8 or K*bits not a multiple of 32. */
 gattn_status gattn_unpack_codes_device(const uint32_t *packed, int64_t N, int64_t K, int32_t bits,
                                        uint8_t *codes, gattn_stream stream);
 
 /* Dequantize one projection of a layer FROM ITS REPACKED DEVICE LAYOUT with the
  * same register unpack the projection kernels use: w (device) float [N][K],
- * w = fp32(scale*code + bias) (exact: scale*code has <= 16 significant bits). */
+ * w = fp32(scale*code + bias) (exact: scale*code has <= 16 significant bits).
+ * Allocates a temporary device buffer and synchronizes `stream`.  Errors:
+ * GATTN_E_INVALID_ARG (NULL, proj outside 0..3), GATTN_E_STATE before
+ * gattn_layer_set_weights, GATTN_E_CUDA. */
 gattn_status gattn_layer_dequant_device(gattn_layer *layer, int32_t proj, float *w,
                                         gattn_stream stream);
 
