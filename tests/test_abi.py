@@ -143,3 +143,52 @@ def test_turbo4_quantize_rejects_bad_arguments_without_a_gpu():
     assert e.value.status == 1                                  # GATTN_E_INVALID_ARG
     with pytest.raises(gattn.GattnError):
         gattn.turbo4_quantize_device(0, 4, 128, 0, 0)          # NULL pointers
+
+
+def test_documented_errors_that_need_no_gpu():
+    """Every entry point's argument errors as the header states them, taken
+    before any CUDA call, so they hold on a machine without a GPU."""
+    import ctypes as C
+    L = gattn.lib()
+    null = None
+
+    def status(rc, want):
+        assert rc == want, (rc, want)
+        assert gattn.last_error()
+
+    # create refuses an inadmissible config with the validator's status and no handle
+    spec = synth.WORKLOADS["tiny"]
+    bad = gattn.make_cfg(spec.hidden, spec.num_heads, spec.num_kv_heads, 96,
+                         spec.partial_rotary_factor, spec.rope_theta, spec.rms_eps,
+                         tuple(spec.bits), tuple(spec.group))
+    h = C.c_void_p(1)
+    status(L.gattn_layer_create(C.byref(bad), C.byref(h)), 2)
+    assert h.value is None
+    status(L.gattn_layer_create(C.byref(_cfg(spec)), null), 1)
+    # NULL handles
+    status(L.gattn_layer_set_weights(null, null, null), 1)
+    status(L.gattn_kv_register(null, null, null), 1)
+    status(L.gattn_kv_register_turbo4v(null, null, null), 1)
+    status(L.gattn_kv_register_turbo4(null, null, null), 1)
+    status(L.gattn_layer_poll_status(null, null), 1)
+    status(L.gattn_layer_set_taps(null, null), 1)
+    status(L.gattn_layer_set_mask(null, null), 1)
+    status(L.gattn_layer_set_path(null, 0), 1)
+    status(L.gattn_layer_set_events(null, null, 0), 1)
+    status(L.gattn_layer_step_block(null, null, null, null, 1, 1, null, null, null, null, null), 1)
+    status(L.gattn_layer_dequant_device(null, 0, null, null), 1)
+    status(L.gattn_layer_dequant_device_static(null, 0, null, null), 1)
+    status(L.gattn_unpack_codes_device(null, 1, 32, 4, null, null), 1)
+    status(L.gattn_turbo4_codebook(null, null), 1)
+    status(L.gattn_pack_affine_host(null, 4, 64, 4, 64, null, null, null), 1)
+    # the plain-value queries
+    assert L.gattn_rotary_dims(null) == -1
+    assert L.gattn_layer_launches_per_step(null) == -1
+    first = (C.c_int32 * 4)()
+    assert L.gattn_head_chunk_plan(0, 4, 2, 1, first, first, 4) == -1
+    assert L.gattn_head_chunk_plan(4, 6, 4, 1, first, first, 4) == -1      # 6 % 4
+    assert L.gattn_head_chunk_plan(4, 4, 2, 1, null, null, 4) == -1
+    assert L.gattn_head_chunk_plan(4, 4, 2, 1, null, null, 0) == 2         # count only
+    # destroy(NULL) is a no-op
+    L.gattn_layer_destroy(null)
+    L.gattn_kv_destroy(null)
