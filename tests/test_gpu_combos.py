@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle as orc
-from qwen3_gated_attention_gb300 import gattn, synth
+from qwen3_gated_attention_gb300 import synth
 from qwen3_gated_attention_gb300.device import DeviceLayer, x_to_device
 from tests import refs
 from tests.cases import make_case

@@ -15,7 +15,7 @@ from qwen3_gated_attention_gb300 import gattn, synth
 from qwen3_gated_attention_gb300.device import DeviceLayer, x_to_device
 from qwen3_gated_attention_gb300.synth import bf16_bits_to_f32
 from tests import refs
-from tests.cases import bf16_ulp_distance, make_case, new_rows, oracle_run
+from tests.cases import bf16_ulp_distance, make_case, oracle_run
 
 pytestmark = pytest.mark.gpu
 

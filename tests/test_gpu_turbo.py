@@ -8,7 +8,7 @@ import torch
 import oracle as orc
 from qwen3_gated_attention_gb300 import gattn, synth
 from qwen3_gated_attention_gb300.device import DeviceLayer, x_to_device
-from qwen3_gated_attention_gb300.synth import bf16_bits_to_f32, f32_to_bf16_bits
+from qwen3_gated_attention_gb300.synth import f32_to_bf16_bits
 from tests import refs
 from tests.cases import make_case
 from tests.test_gpu_layer import SMALL, assert_rows_close

@@ -8,7 +8,6 @@ point bit for bit (the tolerance every dequant test here uses), on calls made
 back to back: the fixed staging array keeps the previous call's contents, so a
 second call must not depend on them.  Collected last on purpose, so that a run
 stopping at the first failure has already run every other test."""
-import numpy as np
 import pytest
 import torch
 
