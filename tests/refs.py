@@ -58,7 +58,18 @@ def rope_complex(x: torch.Tensor, rd: int, pos: torch.Tensor, theta: float) -> t
 
 
 def to_bf16_values(t: torch.Tensor) -> torch.Tensor:
-    return t.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    """float64 values rounded once to bf16 (nearest, ties to even).  torch takes
+    float64 to bfloat16 through float32, which can round twice; a float32
+    intermediate rounded to odd (truncated toward zero, last bit set when
+    inexact) keeps enough bits for the final float32 -> bfloat16 rounding to be
+    the correct single rounding (round-to-odd, Boldo and Melquiond)."""
+    x = t.detach().cpu().numpy().astype(np.float64)
+    f = x.astype(np.float32)
+    over = np.abs(f.astype(np.float64)) > np.abs(x)
+    f = np.where(over, np.nextafter(f, np.float32(0)), f).astype(np.float32)
+    inexact = f.astype(np.float64) != x
+    f = (f.view(np.uint32) | inexact.astype(np.uint32)).view(np.float32)
+    return torch.from_numpy(f).to(torch.bfloat16).to(torch.float64)
 
 
 def torch_layer(spec, Wdeq, qn_w, kn_w, x, cache_k, cache_v, cache_pos):
