@@ -553,3 +553,26 @@ def test_block_post_norm_rows_have_unit_rms():
     rb = np.vectorize(lambda v: orc.bf16_to_double(orc.bf16_from_double(v)))(out)
     exp = rb / np.sqrt(np.mean(rb * rb, axis=-1, keepdims=True) + spec.rms_eps)
     assert np.allclose(on, exp, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("spec", [SMALL["tiny"], SMALL["batched_small"],
+                                  SMALL["verify_small"]] + _random_geometries()[:4],
+                         ids=lambda s: s.name)
+def test_block_matches_torch_composition(spec):
+    """The decoder-block oracle against library routines: h = F.rms_norm(x,
+    input_ln) (rounded once to bf16 for a bf16 layer), the torch layer on h,
+    out = x + layer, out_normed = F.rms_norm(bf16(out), post_ln)."""
+    _, W, x, ck, cv, pos = _oracle_case(spec)
+    il, pl = synth.block_norm_weights_bf16(spec)
+    out, on = orc.block_step(spec, W, x, il, pl, ck.copy(), cv.copy(), pos)
+    eps = float(np.float32(spec.rms_eps))
+    ilw = torch.from_numpy(bf16_bits_to_f32(il).astype(np.float64))
+    plw = torch.from_numpy(bf16_bits_to_f32(pl).astype(np.float64))
+    h = F.rms_norm(torch.from_numpy(x), (spec.hidden,), ilw, eps)
+    if spec.x_dtype == "bf16":
+        h = refs.to_bf16_values(h)
+    ref = _torch_case(spec, W, h.numpy(), ck, cv, pos)
+    want = x + ref["out"]
+    np.testing.assert_allclose(out, want, rtol=1e-10, atol=1e-12)
+    want_n = F.rms_norm(refs.to_bf16_values(torch.from_numpy(want)), (spec.hidden,), plw, eps).numpy()
+    np.testing.assert_allclose(on, want_n, rtol=1e-9, atol=1e-11)
