@@ -75,7 +75,8 @@ class _OrcLayer(C.Structure):
 class _OrcStepExt(C.Structure):
     _fields_ = [("v_codes", _p), ("v_scales", _p), ("k_codes", _p), ("k_scales", _p),
                 ("mask", _p), ("mask_heads", C.c_int32),
-                ("mask_row", _i64), ("mask_head", _i64), ("mask_batch", _i64)]
+                ("mask_row", _i64), ("mask_head", _i64), ("mask_batch", _i64),
+                ("mask_len", C.c_int32)]
 
 
 class _OrcWeights(C.Structure):
@@ -414,6 +415,7 @@ def _step_ext(turbo, mask, keep, turbo_k=None):
         keep.append(mk)
         e.mask, e.mask_heads = _ptr(mk), mk.shape[1]
         e.mask_row, e.mask_head, e.mask_batch = mk.strides[2], mk.strides[1], mk.strides[0]
+        e.mask_len = mk.shape[3]           # positions from T on are not attended
     return e
 
 
@@ -423,7 +425,9 @@ def layer_step_ext(spec, weights: OracleWeights, x: np.ndarray, cache_k, cache_v
     """layer_step with the optional parts together: turbo = (codes, scales) of a
     Bf16KTurbo4V cache (cache_v unused, may be None); turbo_k = the K planes of
     the symmetric Turbo4 cache ([atlas-mod] MetalKvDtype::Turbo4; needs turbo,
-    cache_k unused); mask as in layer_step.  Planes are updated in place."""
+    cache_k unused); mask as in layer_step, except that its rows may be shorter
+    than cache_pos + R: positions from T on are not attended (the library's
+    mask rows of `positions` bytes).  Planes are updated in place."""
     B, R, Hd = x.shape
     L, Wt, keep = _layer_structs(spec, weights, head_chunk, "none")
     x = np.ascontiguousarray(x, np.float64)

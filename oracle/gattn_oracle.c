@@ -661,12 +661,24 @@ static void sdpa_row_vd(const double *q, const uint16_t *kc, int64_t tstride, co
  * attend position t; hm = 0 for a broadcast mask (heads == 1), the query head
  * for a head-specific one (heads == num_heads).  Reading: a mask replaces the
  * causal rule (it carries it), positions run over [0, cache_pos + R), and a
- * row with no position left is a zero row. */
+ * row with no position left is a zero row.  len > 0: a row holds len
+ * positions and the positions from len on are not attended (the library's
+ * mask rows, `positions` long); len <= 0: every row covers [0, cache_pos + R). */
 typedef struct orc_mask {
     const uint8_t *m;
     int32_t heads;
     int64_t stride_row, stride_head, stride_batch;
+    int32_t len;
 } orc_mask;
+
+/* the last position a masked row may attend: cache_pos + R - 1, cut at the row's length */
+static int mask_last(const orc_mask *M, int p0, int R)
+{
+    int last = p0 + R - 1;
+    if (M->len > 0 && last > M->len - 1)
+        last = M->len - 1;
+    return last;
+}
 
 #define ORC_E_MASK 3
 
@@ -834,7 +846,7 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                         int last = (L->mutate == ORC_MUT_NO_CAUSAL) ? p0 + R - 1 : p0 + r;
                         const uint8_t *keep = NULL;
                         if (M) {
-                            last = p0 + R - 1;
+                            last = mask_last(M, p0, R);
                             keep = M->m + b * M->stride_batch + (M->heads > 1 ? h : 0) * M->stride_head +
                                    r * M->stride_row;
                         }
@@ -882,7 +894,7 @@ static int layer_step(const orc_layer *L, const orc_weights *W, const double *x,
                                 o[j] += scores[t] / z * vv;
                             }
                     } else if (M) {
-                        sdpa_row(qv, kc, vc, d, d, p0 + R - 1,
+                        sdpa_row(qv, kc, vc, d, d, mask_last(M, p0, R),
                                  M->m + b * M->stride_batch + (M->heads > 1 ? h : 0) * M->stride_head +
                                      r * M->stride_row, o, scores);
                     } else {
@@ -934,7 +946,7 @@ int orc_layer_step_masked(const orc_layer *L, const orc_weights *W, const double
 {
     if (!mask)
         return ORC_E_ARG;
-    const orc_mask M = {mask, mask_heads, stride_row, stride_head, stride_batch};
+    const orc_mask M = {mask, mask_heads, stride_row, stride_head, stride_batch, 0};
     return layer_step(L, W, x, cache_k, cache_v, NULL, NULL, NULL, NULL, capacity, cache_pos, B, R,
                       &M, out, tap_y, tap_attn);
 }
@@ -976,6 +988,7 @@ typedef struct orc_step_ext {
     const uint8_t *mask;
     int32_t mask_heads;
     int64_t mask_row, mask_head, mask_batch;
+    int32_t mask_len;                  /* positions per mask row (orc_mask.len) */
 } orc_step_ext;
 
 int orc_layer_step_ext(const orc_layer *L, const orc_weights *W, const double *x,
@@ -991,6 +1004,7 @@ int orc_layer_step_ext(const orc_layer *L, const orc_weights *W, const double *x
         M.stride_row = e->mask_row;
         M.stride_head = e->mask_head;
         M.stride_batch = e->mask_batch;
+        M.len = e->mask_len;
         mp = &M;
     }
     uint8_t *vc = e ? e->v_codes : NULL, *vs = e ? e->v_scales : NULL;

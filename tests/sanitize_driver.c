@@ -158,14 +158,17 @@ static int layers(int H, int Hk, int R)
     CHECK(orc_layer_step_masked(&L, &W, x, ck, cv, cap, pos, B, R, mask, 1, cap, R * cap, R * cap,
                                 out, ty, ta) == 0);
     CHECK(orc_layer_step_turbo4v(&L, &W, x, ck, vc, vs, cap, pos, B, R, out, ty, ta) == 0);
-    orc_step_ext e = {vc, vs, kc, ks, mask, 1, cap, R * cap, R * cap};
+    orc_step_ext e = {vc, vs, kc, ks, mask, 1, cap, R * cap, R * cap, cap};
     CHECK(orc_layer_step_ext(&L, &W, x, NULL, NULL, cap, pos, B, R, &e, out, ty, ta) == 0);
     CHECK(orc_block_step_ext(&L, &W, x, 1, iln, pln, ck, cv, cap, pos, B, R, NULL, out, on) == 0);
-    orc_step_ext ev = {vc, vs, NULL, NULL, NULL, 0, 0, 0, 0};
+    orc_step_ext ev = {vc, vs, NULL, NULL, NULL, 0, 0, 0, 0, 0};
     CHECK(orc_block_step_ext(&L, &W, x, 0, iln, NULL, ck, NULL, cap, pos, B, R, &ev, out, NULL) == 0);
     L.head_chunk = 0;
-    orc_step_ext eh = {NULL, NULL, NULL, NULL, mask, H, cap, (int64_t)R * cap, (int64_t)H * R * cap};
+    orc_step_ext eh = {NULL, NULL, NULL, NULL, mask, H, cap, (int64_t)R * cap, (int64_t)H * R * cap, 0};
     CHECK(orc_layer_step_ext(&L, &W, x, ck, cv, cap, pos, B, R, &eh, out, ty, ta) == 0);
+    /* mask rows of 5 positions, shorter than every sequence's span */
+    orc_step_ext es = {vc, vs, NULL, NULL, mask, 1, 5, (int64_t)R * 5, (int64_t)R * 5, 5};
+    CHECK(orc_layer_step_ext(&L, &W, x, ck, NULL, cap, pos, B, R, &es, out, ty, ta) == 0);
     CHECK(orc_layer_step(&L, &W, x, ck, cv, cap, pos, B, R, out, NULL, NULL) == 0);
     int32_t cf[64], cl[64];
     for (int q = 1; q <= 33; ++q) {

@@ -136,3 +136,34 @@ def test_each_head_of_a_head_specific_mask_sees_its_own_positions():
     for h in range(spec.num_heads):
         v = bf16_bits_to_f32(vc[0, h // gqa, 2 * h + 1]).astype(np.float64)
         assert np.allclose(ta[0, 0, h], v, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "turbo4v"])
+def test_short_mask_rows_equal_zero_padded_rows(kv):
+    """Rows shorter than cache_pos + R (the library's mask of `positions`
+    bytes per row): the positions past a row are not attended, which is the
+    same as the full-length mask with those positions zeroed; a row that
+    keeps nothing within its length is a zero row."""
+    spec = _spec(R=3, B=2)
+    case = make_case(spec)
+    x = synth.x_values(spec, case.x)
+    full = _random_mask(spec, 1, 21, density=0.7)
+    T = int(case.pos.min()) + 1                     # shorter than every sequence's span
+    short = np.ascontiguousarray(full[..., :T])
+    padded = full.copy()
+    padded[..., T:] = 0
+    padded[0, 0, 1, :] = 0                          # a row with nothing left ...
+    short[0, 0, 1, :] = 0
+    turbo = synth.turbo4v_cache(spec, case.cap) if kv == "turbo4v" else None
+
+    def run(mask):
+        kc, vc = case.ck.copy(), case.cv.copy()
+        tv = None if turbo is None else (turbo[0].copy(), turbo[1].copy())
+        return orc.layer_step_ext(spec, case.orc_weights, x, kc, None if tv else vc, case.pos,
+                                  turbo=tv, mask=mask, taps=True)
+
+    a_out, _, a_attn = run(short)
+    b_out, _, b_attn = run(padded)
+    assert np.array_equal(a_out, b_out) and np.array_equal(a_attn, b_attn)
+    assert np.all(a_attn[0, 1] == 0.0)              # ... attends nothing
+    assert np.any(a_attn[1] != 0.0)
