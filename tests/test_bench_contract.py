@@ -67,3 +67,19 @@ def test_algorithmic_bytes_follow_the_cache_format():
     blk, per_blk = bench.algorithmic_bytes(spec, block=True)
     assert blk - bf16 == 2 * spec.hidden * 2 + M * spec.hidden * 2
     assert set(per_blk) == set(per_bf16) | {"postnorm"}
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """Launched the way a multi-GPU run launches it (torchrun, two ranks on
+    127.0.0.1): rank 0 alone prints, the other rank exits 0 without work."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0", "--workload", "tiny"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1 and lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
