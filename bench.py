@@ -39,13 +39,14 @@ METRIC = "gated-attn layer steps/s & tokens/s; achieved HBM GB/s vs GB300 peak"
 UNIT = "layer-steps/s"
 
 
-def algorithmic_bytes(spec, block=False, kv="bf16"):
+def algorithmic_bytes(spec, block=False, kv="bf16", x_folded=False):
     """Per-step and per-kernel algorithmic bytes (packed weights + bf16
     scales/biases, KV read over every attended position, KV rows written, x,
     out and the small intermediates each kernel must move).  block: the
     decoder-block step, which adds the two norm weight vectors and the
     post-norm output to the step (x is still read once).  kv="turbo4v": V rows
-    are d/2 code bytes + d/16 E4M3 scale bytes instead of 2d."""
+    are d/2 code bytes + d/16 E4M3 scale bytes instead of 2d.  x_folded: the
+    q|k|v kernel converts x itself (it reads x; no x prep kernel, no fp16 copy)."""
     H, Hk, d, Hd, B, R = (spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.hidden,
                           spec.batch, spec.q_len)
     M = B * R
@@ -75,6 +76,9 @@ def algorithmic_bytes(spec, block=False, kv="bf16"):
         "merge": gate + o16,
         "proj_o": wo + o16 + outb,
     }
+    if x_folded:
+        per_kernel["proj_qkv"] += xb - x16
+        del per_kernel["xprep"]
     step = wq + wk + wv + wo + kv_read + kv_write + xb + outb
     if block:
         lnb = Hd * 2
@@ -274,38 +278,35 @@ def job_rate(units_per_rank, elapsed_ms, world):
     return world * units_per_rank / (elapsed_ms / 1e3)
 
 
-def our_arm(args, spec):
-    import torch
-    import torch.distributed as dist
+# workloads whose numbers ride along in the default line, next to the headline
+PER_WORKLOAD = ("verify_2k_p46", "verify_2k_p2048", "batched_9b", "long_verify_mixed")
 
-    from qwen3_gated_attention_gb300 import build as libbuild
+
+def cpu_baseline_entry(spec, args, budget_s, max_steps):
+    rate, n, el = oracle_sample(spec, budget_s=budget_s, max_steps=max_steps, block=args.block,
+                                kv=args.kv)
+    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole {unit_name(args)} step{'s' if n != 1 else ''} of {spec.name} "
+                      f"({el:.1f} s, one core)"}
+
+
+def measure_workload(spec, args, dev, world, dist, l2, full=True):
+    """Device-timed throughput of one workload: a CUDA graph of `args.steps`
+    consecutive steps over rotating layer instances, replayed at least
+    `args.replays` times (each replay timed with CUDA events on the launching
+    stream; the median replay gives ms_per_step); then a per-kernel pass
+    (events between the step's kernels, programmatic overlap off) whose
+    per-kernel medians give the dominant kernel's roofline; with full=True also
+    the end-to-end rate through the C ABI from pinned host buffers and the
+    clocks sampled during the timed replays."""
+    import torch
+
     from qwen3_gated_attention_gb300 import gattn
     from qwen3_gated_attention_gb300.device import DeviceLayer, x_to_device
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-
-    # CPU baseline first (rank 0, N = 1): the oracle as it stands, before any GPU work
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, n, el = oracle_sample(spec, budget_s=args.cpu_budget, block=args.block, kv=args.kv)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} whole {unit_name(args)} steps of {spec.name} ({el:.1f} s, one core)"}
-
-    if rank == 0:
-        libbuild.build()
-    if world > 1:
-        dist.init_process_group("nccl")
-        dist.barrier()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
-
+    local = dev.index or 0
     step_bytes, kernel_bytes = algorithmic_bytes(spec, args.block, args.kv)
-    inst_bytes = step_bytes
-    n_inst = max(2, math.ceil(4 * l2 / inst_bytes))
+    n_inst = max(2, math.ceil(4 * l2 / step_bytes))
     if args.instances:
         n_inst = args.instances
 
@@ -339,6 +340,8 @@ def our_arm(args, spec):
     ild = torch.from_numpy(il.view(np.int16)).to(dev)
     pld = torch.from_numpy(pl.view(np.int16)).to(dev)
     normed = torch.empty_like(outs[0])
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
 
     def step_call(dl, xp, pp, op):
         if args.block:
@@ -346,13 +349,11 @@ def our_arm(args, spec):
                                    pld.data_ptr(), op, normed.data_ptr(), sh)
         else:
             gattn.layer_step(dl.h, xp, dl.kv, pp, spec.batch, spec.q_len, op, sh)
-    stream = torch.cuda.Stream(dev)
-    sh = stream.cuda_stream
 
     def enqueue(i):
         step_call(layers[i % n_inst], xd.data_ptr(), pd.data_ptr(), outs[i % n_inst].data_ptr())
 
-    # eager warm-up (also checks status), then graphs
+    # eager warm-up (also checks status), then the graph
     with torch.cuda.stream(stream):
         for i in range(n_inst):
             enqueue(i)
@@ -363,145 +364,209 @@ def our_arm(args, spec):
 
     K = args.steps
     W = max(args.warmup, 3)
-    gsize = min(K, args.graph_steps)
-    gsize = max(1, (gsize // n_inst) * n_inst) if gsize >= n_inst else gsize
-
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            g.capture_begin()
-            for i in range(n):
-                enqueue(i)
-            g.capture_end()
-        return g
-
-    graph = capture(gsize)
-    rem = K % gsize
-    graph_rem = capture(rem) if rem else None
-    reps = K // gsize
-
-    # warm-up: W steps
+    graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        for _ in range(max(1, math.ceil(W / gsize))):
+        graph.capture_begin()
+        for i in range(K):
+            enqueue(i)
+        graph.capture_end()
+
+    # warm-up: W steps (whole replays)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(W / K))):
             graph.replay()
     stream.synchronize()
 
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
+    # timed replays: at least args.replays, and at least args.min_timed_s of work
+    est_ms = None
+    with torch.cuda.stream(stream):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    est_ms = max(e0.elapsed_time(e1), 1e-3)
+    n_rep = max(args.replays, int(math.ceil(args.min_timed_s * 1e3 / est_ms)) if full else 0)
+    n_rep = min(n_rep, 100000)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+    clocks = ClockSampler(local) if full else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.3)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
     with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(reps):
+        evs[0].record(stream)
+        for r in range(n_rep):
             graph.replay()
-        if graph_rem is not None:
-            graph_rem.replay()
-        ev1.record(stream)
+            evs[r + 1].record(stream)
     stream.synchronize()
     torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dist if world > 1 else None, dev)
+    clk = clocks.stop() if clocks else None
+    rep_ms = sorted(evs[r].elapsed_time(evs[r + 1]) for r in range(n_rep))
+    med_ms = statistics.median(rep_ms)
+    med_ms = max_over_ranks(med_ms, dist if world > 1 else None, dev)
     if world > 1:
         dist.barrier()
-    steps_per_s = job_rate(K, elapsed_ms, world)
+    ms_per_step = med_ms / K
+    steps_per_s = job_rate(K, med_ms, world)
     for dl in layers:
         gattn.layer_poll_status(dl.h, sh)
 
     # per-kernel pass: events between the step's kernels (programmatic overlap off)
-    if launches == 1:
-        names = ["layer_step"]
+    names = gattn.layer_step_kernels(layers[0].h)
+    if names == ["layer_step"]:
         kernel_bytes = {"layer_step": step_bytes}
     else:
-        names = ["xprep", "proj_qkv", "attn", "merge", "proj_o"] + (["postnorm"] if launches == 6
-                                                                      else [])
-        if launches == 5 and "postnorm" in kernel_bytes:     # post-norm inside the o_proj
+        if "postnorm" not in names and "postnorm" in kernel_bytes:   # post-norm inside the o_proj
             kernel_bytes["proj_o"] += kernel_bytes.pop("postnorm")
-    nper = min(K, max(n_inst, 4 * n_inst))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(nper)]
+        if "xprep" not in names:           # x converted inside the q|k|v kernel
+            kernel_bytes = dict(algorithmic_bytes(spec, args.block, args.kv, x_folded=True)[1])
+            if "postnorm" not in names and "postnorm" in kernel_bytes:
+                kernel_bytes["proj_o"] += kernel_bytes.pop("postnorm")
+        kernel_bytes = {n: kernel_bytes[n] for n in names}
+    nper = max(args.replays, n_inst)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(nper)]
     per_kernel_ms = {n: [] for n in names}
     with torch.cuda.stream(stream):
-        for row in evs:
+        for row in kev:
             for e in row:
                 e.record(stream)          # creates the underlying cudaEvent_t
     stream.synchronize()
     with torch.cuda.stream(stream):
         for i in range(nper):
             dl = layers[i % n_inst]
-            gattn.layer_set_events(dl.h, [e.cuda_event for e in evs[i]])
+            gattn.layer_set_events(dl.h, [e.cuda_event for e in kev[i]])
             enqueue(i)
             gattn.layer_set_events(dl.h, [])
     stream.synchronize()
     for i in range(nper):
         for j, n in enumerate(names):
-            per_kernel_ms[n].append(evs[i][j].elapsed_time(evs[i][j + 1]))
-    kernel_avg_ms = {n: statistics.mean(v) for n, v in per_kernel_ms.items()}
+            per_kernel_ms[n].append(kev[i][j].elapsed_time(kev[i][j + 1]))
+    kernel_med_ms = {n: statistics.median(v) for n, v in per_kernel_ms.items()}
     dominant = max(kernel_bytes, key=lambda n: kernel_bytes[n])
     peak, peak_kind = load_peaks()
-    achieved = kernel_bytes[dominant] / (kernel_avg_ms[dominant] / 1e3) / 1e9
+    achieved = kernel_bytes[dominant] / (kernel_med_ms[dominant] / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak,
                 "traffic": profiled_traffic(dominant, spec.name + ("" if args.kv == "bf16"
                                                                    else "_" + args.kv)),
-                "kernel": dominant, "peak_source": peak_kind,
-                "kernel_avg_us": {n: 1e3 * v for n, v in kernel_avg_ms.items()},
+                "kernel": dominant, "peak_source": peak_kind, "kernel_launches_timed": nper,
+                "kernel_median_us": {n: 1e3 * v for n, v in kernel_med_ms.items()},
                 "kernel_bytes": kernel_bytes}
 
-    # e2e through the C ABI with pinned host buffers, copies inside the timed region
-    xh = torch.from_numpy(np.ascontiguousarray(xd.cpu().view(torch.int16).numpy())).pin_memory() \
-        if spec.x_dtype != "f32" else xd.cpu().pin_memory()
-    ph = torch.from_numpy(pos.copy()).pin_memory()
-    oh = torch.empty(outs[0].shape, dtype=torch.bfloat16).pin_memory()
-    xdev = torch.empty_like(xd)
-    pdev = torch.empty_like(pd)
-    n_e2e = min(K, args.e2e_steps)
-    h2d = xh.numel() * xh.element_size() + ph.numel() * ph.element_size()
-    d2h = oh.numel() * oh.element_size()
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(n_e2e):
-            dl = layers[i % n_inst]
-            xdev.view(torch.int16 if spec.x_dtype != "f32" else torch.float32).copy_(
-                xh, non_blocking=True)
-            pdev.copy_(ph, non_blocking=True)
-            step_call(dl, xdev.data_ptr(), pdev.data_ptr(), outs[i % n_inst].data_ptr())
-            oh.copy_(normed if args.block else outs[i % n_inst], non_blocking=True)
-        e1.record(stream)
-    stream.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist if world > 1 else None, dev)
-    e2e_rate = job_rate(n_e2e, e2e_ms, world)
+    res = {"value": steps_per_s, "ms_per_step": ms_per_step, "steps": K, "warmup": W,
+           "replays": n_rep, "replay_ms": {"median": med_ms, "min": rep_ms[0], "max": rep_ms[-1]},
+           "tokens_per_s": steps_per_s * spec.batch * spec.q_len,
+           "hbm_gbs": steps_per_s / world * step_bytes / 1e9,
+           "hbm_frac_of_peak": steps_per_s / world * step_bytes / 1e9 / peak,
+           "bytes_per_step": step_bytes, "roofline": roofline, "launches": launches,
+           "kernels": names,
+           "n_inst": n_inst, "inst_bytes": n_inst * step_bytes, "clocks": clk}
 
-    tokens_per_step = spec.batch * spec.q_len
-    line = {
-        "metric": METRIC, "value": steps_per_s, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(spec, args, {
-            "l2": f"rotating {n_inst} layer instances, {n_inst * inst_bytes / 2**20:.0f} MiB "
-                  f"> 4x L2 ({l2 / 2**20:.0f} MiB)",
-            "arith": "bf16/fp16 tensor-core operands, fp32 accumulate; 8/4/6/3-bit codes",
-            "path": "one kernel per step" if launches == 1 else f"{launches} kernels per step"}),
-        "tokens_per_s": steps_per_s * tokens_per_step,
-        "hbm_gbs": steps_per_s / world * step_bytes / 1e9,
-        "hbm_frac_of_peak": steps_per_s / world * step_bytes / 1e9 / peak,
-        "bytes_per_step": step_bytes,
-        "roofline": roofline,
-        "cpu_baseline": cpu,
-        "e2e": {"value": e2e_rate, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": n_e2e},
-        "gpu_launches": launches * K,
-        "clocks": clk,
-    }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    if full:
+        # e2e through the C ABI with pinned host buffers, copies inside the timed region
+        xh = torch.from_numpy(np.ascontiguousarray(xd.cpu().view(torch.int16).numpy())).pin_memory() \
+            if spec.x_dtype != "f32" else xd.cpu().pin_memory()
+        ph = torch.from_numpy(pos.copy()).pin_memory()
+        oh = torch.empty(outs[0].shape, dtype=torch.bfloat16).pin_memory()
+        xdev = torch.empty_like(xd)
+        pdev = torch.empty_like(pd)
+        n_e2e = min(K, args.e2e_steps)
+        h2d = xh.numel() * xh.element_size() + ph.numel() * ph.element_size()
+        d2h = oh.numel() * oh.element_size()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(n_e2e):
+                dl = layers[i % n_inst]
+                xdev.view(torch.int16 if spec.x_dtype != "f32" else torch.float32).copy_(
+                    xh, non_blocking=True)
+                pdev.copy_(ph, non_blocking=True)
+                step_call(dl, xdev.data_ptr(), pdev.data_ptr(), outs[i % n_inst].data_ptr())
+                oh.copy_(normed if args.block else outs[i % n_inst], non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist if world > 1 else None, dev)
+        res["e2e"] = {"value": job_rate(n_e2e, e2e_ms, world), "unit": UNIT,
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
+    del graph
     for dl in layers:
         dl.close()
+    del layers, outs, xd, pd
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return res
+
+
+def our_arm(args, spec):
+    import torch
+    import torch.distributed as dist
+
+    from qwen3_gated_attention_gb300 import build as libbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    others = [w for w in PER_WORKLOAD if w != spec.name] \
+        if (args.per_workload and not args.block and args.kv == "bf16" and args.path == "auto") \
+        else []
+
+    # CPU baselines first (rank 0, N = 1): the oracle as it stands, before any
+    # GPU work; one bounded oracle step for each ride-along workload
+    cpu, cpu_other = None, {}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_entry(spec, args, args.cpu_budget, 64)
+        for w in others:
+            cpu_other[w] = cpu_baseline_entry(synth.WORKLOADS[w], args, 1.0, 1)
+
+    if rank == 0:
+        libbuild.build()
+    if world > 1:
+        dist.init_process_group("nccl")
+        dist.barrier()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
+
+    r = measure_workload(spec, args, dev, world, dist, l2, full=True)
+    per = {}
+    for w in others:
+        o = measure_workload(synth.WORKLOADS[w], args, dev, world, dist, l2, full=False)
+        per[w] = {"value": o["value"], "unit": UNIT, "ms_per_step": o["ms_per_step"],
+                  "tokens_per_s": o["tokens_per_s"], "hbm_gbs": o["hbm_gbs"],
+                  "hbm_frac_of_peak": o["hbm_frac_of_peak"], "bytes_per_step": o["bytes_per_step"],
+                  "steps": o["steps"], "replays": o["replays"], "roofline": o["roofline"],
+                  "config": config_dict(synth.WORKLOADS[w], args),
+                  "cpu_baseline": cpu_other.get(w)}
+
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": r["steps"],
+        "warmup": r["warmup"], "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(spec, args, {
+            "l2": f"rotating {r['n_inst']} layer instances, {r['inst_bytes'] / 2**20:.0f} MiB "
+                  f"> 4x L2 ({l2 / 2**20:.0f} MiB)",
+            "arith": "bf16/fp16 tensor-core operands, fp32 accumulate; 8/4/6/3-bit codes",
+            "path": "one kernel per step" if r["launches"] == 1 else
+                    f"{r['launches']} kernels per step ({', '.join(r['kernels'])})",
+            "timing": f"median of {r['replays']} timed replays of a {r['steps']}-step graph"}),
+        "replays": r["replays"], "replay_ms": r["replay_ms"],
+        "tokens_per_s": r["tokens_per_s"], "hbm_gbs": r["hbm_gbs"],
+        "hbm_frac_of_peak": r["hbm_frac_of_peak"], "bytes_per_step": r["bytes_per_step"],
+        "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
+        "gpu_launches": r["launches"] * r["steps"] * r["replays"],
+        "clocks": r["clocks"],
+    }
+    if per:
+        line["per_workload"] = per
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
@@ -509,18 +574,23 @@ def our_arm(args, spec):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60000)
-    ap.add_argument("--warmup", type=int, default=600)
+    ap.add_argument("--steps", type=int, default=20, help="steps per timed graph replay")
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_4b", choices=list(synth.WORKLOADS))
     ap.add_argument("--instances", type=int, default=0)
-    ap.add_argument("--graph-steps", type=int, default=600)
+    ap.add_argument("--replays", type=int, default=20,
+                    help="timed replays of the step graph, at least (median reported)")
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="replay the graph for at least this long (seconds) in the timed region")
+    ap.add_argument("--no-per-workload", dest="per_workload", action="store_false",
+                    help="time only the selected workload (no per_workload entries)")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-head-chunk", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "fused", "split"],
-                    help="one-kernel or five-kernel step (auto: one kernel when it fits)")
+                    help="which kernels run a step: auto and split take the five-kernel chain, fused the one-kernel step")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "turbo4v", "turbo4"],
                     help="KV cache format: bf16, bf16 K with a Turbo4 V cache, or Turbo4 K and V")
     ap.add_argument("--block", action="store_true",

@@ -380,7 +380,12 @@ gattn_status gattn_layer_dequant_device(gattn_layer *layer, int32_t proj, float 
  *     4 Mi floats; larger projections fail with GATTN_E_UNSUPPORTED and a
  *     message naming the sizes.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress), and so does the first call after the device's
+ *     context was created anew (e.g. after cudaDeviceReset); make those
+ *     calls before any stream capture.
+ *   - A sticky CUDA error of the context is returned as GATTN_E_CUDA; an
+ *     error left by an earlier, unrelated launch is neither reported nor
+ *     cleared.
  *   - Every call shares the one array: calls that can overlap on the GPU (on
  *     different streams, or different layers at once) race on it.
  * The pages have no counterpart of this entry point (it is a library utility).
@@ -450,9 +455,24 @@ gattn_status gattn_layer_step_block(gattn_layer *layer, const void *x, gattn_kv 
 
 /* Per-step launch report of the layer's last step: number of kernel launches
  * it enqueued, all of them this library's own kernels (1 on the one-kernel
- * path, 5 on the five-kernel path, 6 for a decoder-block step whose post-norm
- * takes its own launch). */
+ * path; on the multi-kernel path 4 when the q|k|v kernel converts x itself,
+ * else 5 with the x prep launch, one more for a decoder-block step whose
+ * post-norm takes its own launch). */
 int32_t gattn_layer_launches_per_step(const gattn_layer *layer);
+
+/* The kernels of the layer's last step, in launch order. */
+enum {
+    GATTN_KERNEL_XPREP = 1,     /* x -> tensor-core operand (+ input RMSNorm of the block) */
+    GATTN_KERNEL_PROJ_QKV = 2,  /* q|k|v dequant projection + norm / rotary / KV append */
+    GATTN_KERNEL_ATTN = 3,      /* causal GQA attention partials */
+    GATTN_KERNEL_MERGE = 4,     /* attention merge + output gate -> o_proj operand */
+    GATTN_KERNEL_PROJ_O = 5,    /* o_proj (+ residual and fused post-norm of the block) */
+    GATTN_KERNEL_POSTNORM = 6,  /* post-attention RMSNorm of the block, own launch */
+    GATTN_KERNEL_FUSED = 7      /* the one-kernel step */
+};
+/* Writes up to `cap` GATTN_KERNEL_* values (host array) and returns the launch
+ * count of the last step (0 before any step), or -1 for bad arguments. */
+int32_t gattn_layer_step_kernels(const gattn_layer *layer, int32_t *kinds, int32_t cap);
 
 /* Instrumentation: with n >= 2 cudaEvent_t handles, each following step
  * records events[i] on its stream right before its i-th kernel launch (for

@@ -121,12 +121,16 @@ struct ProjPlan {
     int rbc = 1;                              // row blocks per cluster (whole heads for q|k|v)
     int stage_bytes[3] = {0, 0, 0}, stages[3] = {0, 0, 0};  // per NT index
     int ks[3] = {1, 1, 1}, grid[3] = {0, 0, 0};
+    int xtab[3] = {0, 0, 0};                  // q|k|v: bytes of the converted-x table (0: none)
     uint8_t *w = nullptr;
 };
 
 int nt_index(int NT) { return NT == 1 ? 0 : (NT == 2 ? 1 : 2); }
 
 constexpr int kAttnMinUnits = 4;     // 16-token units per attention CTA, at least
+// shared memory a q|k|v CTA may spend on converting x itself (the table of its
+// k units' fp16 fragments and group sums); a larger table keeps the x prep kernel
+constexpr int kXTabMax = 24 * 1024;
 constexpr int kMaxCluster = 8;       // portable cluster size
 
 void plan_proj(ProjPlan &p, int N, int K, int bits, int group, int rbc)
@@ -175,6 +179,7 @@ struct gattn_layer {
     float *ws_attn = nullptr;
     unsigned *status = nullptr;
     double *inv_freq = nullptr;
+    float2 *inv_freq2 = nullptr;           // the same frequencies as float (hi, lo) pairs
     uint16_t *q_norm = nullptr, *k_norm = nullptr;
     size_t ws_attn_floats = 0;
     int attn_grid = 0;
@@ -201,6 +206,7 @@ struct gattn_layer {
     gattn_mask mask{};                     // attention mask of the following steps (mask.mask null: causal)
     bool weights_set = false;
     int launches = 0;
+    int32_t kinds[8] = {0};                // GATTN_KERNEL_* of the last step's launches
     bool pdl = true;
     std::vector<cudaEvent_t> events;
 };
@@ -319,20 +325,15 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     });
     TRY(attr_err);
     for (ProjPlan *p : {&L->pqkv, &L->po}) {
+        const int mode = p == &L->pqkv ? kModeQKV : kModeO;
         for (int i = 0; i < 3; ++i) {
+            const int NT = 1 << i;
             ProjArgs a{};
             a.stages = p->stages[i];
             a.stage_bytes = p->stage_bytes[i];
             a.eb_rows = p->rbc * kRBR;
+            a.recv_cap = proj_recv_cap(mode, NT);
             const int smem = proj_smem_bytes(a);
-            int occ = 0;
-            TRY(proj_occupancy(p->bits, 1 << i, p == &L->pqkv ? kModeQKV : kModeO, p->group, smem,
-                               &occ));
-            if (occ < 1)
-                occ = 1;
-            // split K over as many CTAs as a cluster allows while every CTA of
-            // the grid stays resident (one wave)
-            const long long capacity = (long long)L->num_sms * occ;
             const int nclusters = p->nrb / p->rbc;
             // 16-CTA clusters (non-portable) when this kernel can run them
             // (the q|k|v projection, which attention waits on, keeps the portable
@@ -340,21 +341,35 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
             // with room for all of its CTAs)
             int max_cluster = kMaxCluster, n16 = 0;
             if (p == &L->po &&
-                proj_max_clusters(p->bits, 1 << i, kModeO, p->group, smem, 16, &n16) == cudaSuccess &&
+                proj_max_clusters(p->bits, NT, kModeO, p->group, smem, 16, &n16) == cudaSuccess &&
                 n16 > 0)
                 max_cluster = 16;
             cudaGetLastError();
+            // q|k|v with at most 16 operand columns: each CTA converts the x of its
+            // own k units when that table is small (no separate x prep launch)
+            auto xtab_for = [&](int ks) -> int {
+                if (mode != kModeQKV || NT > 2)
+                    return 0;
+                const int xe = 2048 * NT + (kKU / p->group) * 4 * 8 * NT;
+                const int xt = (p->nku + ks - 1) / ks * xe;
+                return xt <= kXTabMax ? xt : 0;
+            };
             // the largest k split (any count up to the cluster limit) whose
             // clusters all fit on the GPU at once: one wave (a second, partial
             // wave of clusters costs more than the split saves)
             int ks = 1;
             for (int cand = std::min(max_cluster / p->rbc, p->nku); cand > 1; --cand) {
                 const int csize = cand * p->rbc;
-                if ((long long)nclusters * csize > capacity)
+                const int sm_c = smem + xtab_for(cand);
+                int occ = 0;
+                TRY(proj_occupancy(p->bits, NT, mode, p->group, sm_c, &occ));
+                if (occ < 1)
+                    occ = 1;
+                if ((long long)nclusters * csize > (long long)L->num_sms * occ)
                     continue;
                 int nres = 0;
-                if (proj_max_clusters(p->bits, 1 << i, p == &L->pqkv ? kModeQKV : kModeO,
-                                      p->group, smem, csize, &nres) != cudaSuccess) {
+                if (proj_max_clusters(p->bits, NT, mode, p->group, sm_c, csize, &nres) !=
+                    cudaSuccess) {
                     cudaGetLastError();
                     continue;
                 }
@@ -364,6 +379,7 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
                 }
             }
             p->ks[i] = ks;
+            p->xtab[i] = xtab_for(ks);
             p->grid[i] = nclusters * p->rbc * ks;
         }
     }
@@ -440,6 +456,16 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
         inv[i] = std::pow((double)c.rope_theta, -2.0 * (double)i / (double)L->rd);
     TRY(cudaMalloc(&L->inv_freq, inv.size() * sizeof(double)));
     TRY(cudaMemcpy(L->inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice));
+    {
+        std::vector<float2> pairs(inv.size());
+        for (size_t i = 0; i < inv.size(); ++i) {
+            pairs[i].x = (float)inv[i];
+            pairs[i].y = (float)(inv[i] - (double)pairs[i].x);
+        }
+        TRY(cudaMalloc(&L->inv_freq2, pairs.size() * sizeof(float2)));
+        TRY(cudaMemcpy(L->inv_freq2, pairs.data(), pairs.size() * sizeof(float2),
+                       cudaMemcpyHostToDevice));
+    }
     TRY(cudaMalloc(&L->q_norm, c.head_dim * 2));
     TRY(cudaMalloc(&L->k_norm, c.head_dim * 2));
 #undef TRY
@@ -452,7 +478,7 @@ void gattn_layer_destroy(gattn_layer *L)
     if (!L)
         return;
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
-                    L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq,
+                    L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq, L->inv_freq2,
                     L->q_norm, L->k_norm, L->part_a,  L->part_o,  L->sync,
                     L->ss_part, L->post_ticket};
     for (void *p : ptrs)
@@ -689,6 +715,15 @@ gattn_status gattn_layer_set_mask(gattn_layer *L, const gattn_mask *m)
 
 int32_t gattn_layer_launches_per_step(const gattn_layer *L) { return L ? L->launches : -1; }
 
+int32_t gattn_layer_step_kernels(const gattn_layer *L, int32_t *kinds, int32_t cap)
+{
+    if (!L || cap < 0 || (cap > 0 && !kinds))
+        return -1;
+    for (int i = 0; i < L->launches && i < cap; ++i)
+        kinds[i] = L->kinds[i];
+    return L->launches;
+}
+
 gattn_status gattn_layer_set_path(gattn_layer *L, int32_t path)
 {
     if (!L)
@@ -883,6 +918,8 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
             CUDA_TRY(ops.launch(f, kv->kmap, kv->vmap, L->num_sms, s));
             CUDA_TRY(mark_end());
             L->launches = 1;
+            std::memset(L->kinds, 0, sizeof L->kinds);
+            L->kinds[0] = GATTN_KERNEL_FUSED;
             return GATTN_OK;
         }
         if (L->path == GATTN_PATH_FUSED)
@@ -892,11 +929,19 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
                         "16-byte aligned x and a compiled instance for its bit widths)");
     }
 
-    // 1. x -> fp16 tensor-core operand + group sums
-    CUDA_TRY(mark(0));
-    CUDA_TRY(launch_xprep(x, c.x_dtype, M, c.hidden, L->pqkv.group, NTa, L->x16_a, L->xsum_a,
-                          blk ? blk->input_ln : nullptr, c.rms_eps, pdl, s));
-    ++launches;
+    int32_t kinds[8] = {0};
+    auto launched = [&](int32_t kind) { kinds[launches++] = kind; };
+
+    // 1. x -> fp16 tensor-core operand + group sums: in the q|k|v kernel itself
+    //    when its CTAs' tables fit (layer steps; x 16-byte aligned), else its
+    //    own launch
+    const bool xfold = !blk && L->pqkv.xtab[nia] > 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    if (!xfold) {
+        CUDA_TRY(mark(launches));
+        CUDA_TRY(launch_xprep(x, c.x_dtype, M, c.hidden, L->pqkv.group, NTa, L->x16_a, L->xsum_a,
+                              blk ? blk->input_ln : nullptr, c.rms_eps, pdl, s));
+        launched(GATTN_KERNEL_XPREP);
+    }
 
     // 2. fused q|k|v projection with the norm / rotary / append epilogue
     ProjArgs a{};
@@ -915,6 +960,10 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     a.rbc = L->pqkv.rbc;
     a.ks = L->pqkv.ks[nia];
     a.eb_rows = a.rbc * kRBR;
+    a.recv_cap = proj_recv_cap(kModeQKV, NTa);
+    a.xtab_bytes = xfold ? L->pqkv.xtab[nia] : 0;
+    a.xraw = x;
+    a.x_f32 = c.x_dtype == GATTN_DTYPE_F32;
     a.xsplit = c.x_dtype == GATTN_DTYPE_F32 ? M : 0;
     a.status = L->status;
     EpiQKV eq{};
@@ -935,7 +984,7 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     eq.q_norm = L->q_norm;
     eq.k_norm = L->k_norm;
     eq.eps = c.rms_eps;
-    eq.inv_freq = L->inv_freq;
+    eq.inv_freq2 = L->inv_freq2;
     eq.qn = L->qn;
     eq.gate = L->gate;
     eq.tap_y = L->taps.y;
@@ -957,9 +1006,9 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
         }
     }
     EpiO eo{};
-    CUDA_TRY(mark(1));
+    CUDA_TRY(mark(launches));
     CUDA_TRY(launch_proj(L->pqkv.bits, NTa, kModeQKV, a, eq, eo, L->pqkv.grid[nia], pdl, s));
-    ++launches;
+    launched(GATTN_KERNEL_PROJ_QKV);
 
     // 3. attention + merge + gate -> o_proj operand
     t.qn = L->qn;
@@ -982,6 +1031,7 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     t.group_o = L->po.group;
     t.tap_attn = L->taps.attn;
     t.status = L->status;
+
     if (L->mask.mask) {
         t.mask = L->mask.mask;
         t.mask_heads = L->mask.heads;
@@ -1013,17 +1063,17 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
             t.ksq_batch = kv->tdesc.scale_stride_batch;
         }
     }
-    CUDA_TRY(mark(2));
+    CUDA_TRY(mark(launches));
     if (kv->kturbo)
         CUDA_TRY(launch_attn_vqk(MT, c.head_dim / 64, t, kv->kmap, L->attn_grid, pdl, s));
     else if (kv->turbo)
         CUDA_TRY(launch_attn_vq(MT, c.head_dim / 64, t, kv->kmap, L->attn_grid, pdl, s));
     else
         CUDA_TRY(launch_attn(MT, c.head_dim / 64, t, kv->kmap, kv->vmap, L->attn_grid, pdl, s));
-    ++launches;
-    CUDA_TRY(mark(3));
+    launched(GATTN_KERNEL_ATTN);
+    CUDA_TRY(mark(launches));
     CUDA_TRY(launch_attn_merge(t, max_rows, pdl, s));
-    ++launches;
+    launched(GATTN_KERNEL_MERGE);
 
     // 4. o_proj
     ProjArgs o = a;
@@ -1041,6 +1091,7 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     o.rbc = 1;
     o.ks = L->po.ks[ni];
     o.eb_rows = kRBR;
+    o.recv_cap = proj_recv_cap(kModeO, NT);
     o.xsplit = 0;
     EpiO e2{};
     e2.R = q_len;
@@ -1061,9 +1112,9 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
         e2.ss_part = L->ss_part;
         e2.ticket = L->post_ticket;
     }
-    CUDA_TRY(mark(4));
+    CUDA_TRY(mark(launches));
     CUDA_TRY(launch_proj(L->po.bits, NT, kModeO, o, eq, e2, L->po.grid[ni], pdl, s));
-    ++launches;
+    launched(GATTN_KERNEL_PROJ_O);
 
     // 5. decoder block: the post-attention RMSNorm of the residual stream,
     //    in its own launch when the o_proj did not take it
@@ -1071,10 +1122,11 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
         CUDA_TRY(mark(launches));
         CUDA_TRY(launch_postnorm(static_cast<const __nv_bfloat16 *>(out), blk->post_ln, c.rms_eps, M,
                                  c.hidden, blk->out_normed, pdl, s));
-        ++launches;
+        launched(GATTN_KERNEL_POSTNORM);
     }
     CUDA_TRY(mark_end());
     L->launches = launches;
+    std::memcpy(L->kinds, kinds, sizeof kinds);
     return GATTN_OK;
 }
 

@@ -182,6 +182,20 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank)
     return r;
 }
 
+// Stores into another CTA's shared memory (addresses from dsmem_addr); they are
+// visible to that CTA after the next cluster barrier.
+__device__ __forceinline__ void st_dsmem(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float4 v)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 // Remote load without a memory clobber, so independent loads can be in flight
 // together; being volatile it stays after cluster_sync() (also volatile).
 __device__ __forceinline__ float ld_dsmem(uint32_t addr)

@@ -14,6 +14,22 @@ struct gattn_layer;
 
 namespace gattn {
 
+// Launch kernel f and return the status of this launch alone.  (The
+// `<<<...>>>` form followed by cudaGetLastError() would also report, and
+// clear, an error left by an earlier unrelated asynchronous launch.)  A sticky
+// error of the context is reported as it is.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_plain(void (*f)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t s, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, f, static_cast<Args &&>(args)...);
+}
+
 // ----------------------------------------------------- projection layout
 //
 // A projection matrix W [N][K] (q|k|v concatenated for the fused launch) is
@@ -35,6 +51,9 @@ namespace gattn {
 constexpr int kWR = 4;            // consumer warps per CTA = 32-row tiles per row block
 constexpr int kRBR = 32 * kWR;    // rows per row block
 constexpr int kKU = 128;          // k per unit
+
+// Threads of a projection CTA: kWR consumer warps and one producer warp.
+__host__ __device__ constexpr int proj_threads(int NT) { return NT > 0 ? (kWR + 1) * 32 : 0; }
 
 __host__ __device__ inline int unit_code_bytes(int bits) { return 512 * bits; }
 __host__ __device__ inline int unit_sb_bytes(int group) { return 128 * (128 / group); }
@@ -72,6 +91,13 @@ struct ProjArgs {
     int ks;               // k splits per row block (cluster size = rbc * ks)
     int eb_rows;          // rows per cluster = rbc * kRBR
     int xsplit;           // > 0: column m + xsplit holds the low fp16 part of column m
+    int recv_cap;         // floats of the split-K receive area (proj_recv_cap)
+    // > 0 (q|k|v only): the CTA converts the layer input x itself into a table
+    // of this many bytes of shared memory (its k units' fp16 fragments and group
+    // sums), and the stages carry weights only; 0: x16 / xsum come prepared
+    int xtab_bytes;
+    const void *xraw;     // x [M][K] for the table
+    int x_f32;            // x dtype: fp32 (1) or bf16 (0)
     unsigned *status;
 };
 
@@ -86,7 +112,7 @@ struct EpiQKV {
     long long st_tok, st_head, st_batch;
     const uint16_t *q_norm, *k_norm;
     float eps;
-    const double *inv_freq;        // [rd/2]
+    const float2 *inv_freq2;       // [rd/2] inv_freq as float pairs: hi = fp32(f), lo = fp32(f - hi)
     __nv_bfloat16 *qn;             // [B][R][H][d]
     float *gate;                   // [M][H*d]
     float *tap_y;                  // [M][Nq + 2 Nkv] or null
@@ -121,6 +147,16 @@ struct EpiO {
 constexpr int kPostFuseMaxElems = 16384;
 
 enum { kModeQKV = 0, kModeO = 1 };
+
+// Floats of the receive area a projection CTA reserves for the partial sums
+// the cluster's CTAs push to it (proj.cuh): at most MP = 8 NT operand columns.
+// q|k|v: ceil(M / csize) columns (x2 with the fp32 low planes) of ks x eb_rows
+// values, at most (MP + 15) * 128 for clusters of <= 8 CTAs;
+// o_proj: ks * M * ceil(128 / csize) <= MP * 143 for clusters of <= 16 CTAs.
+__host__ __device__ inline int proj_recv_cap(int mode, int NT)
+{
+    return mode == kModeQKV ? (8 * NT + 15) * 128 : 8 * NT * 143;
+}
 
 // launchers (return cudaGetLastError() of the launch)
 cudaError_t launch_proj(int bits, int NT, int mode, const ProjArgs &a, const EpiQKV &eq,

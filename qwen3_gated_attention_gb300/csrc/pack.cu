@@ -3,6 +3,7 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "proj.cuh"
+#include "xconv.cuh"
 
 namespace gattn {
 
@@ -110,8 +111,8 @@ cudaError_t launch_repack(const RepackSrc &src, int K, int bits, int group, int 
     const long long total = (long long)nrb * (K / kKU) * kWR * 32;
     const int threads = 128;
     const long long blocks = (total + threads - 1) / threads;
-    repack_kernel<<<(unsigned)blocks, threads, 0, s>>>(src, K, bits, group, nrb, dst);
-    return cudaGetLastError();
+    return launch_plain(repack_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, src, K, bits,
+                        group, nrb, dst);
 }
 
 // Dequantize from the tile layout with the projection kernel's own unpack:
@@ -168,16 +169,18 @@ cudaError_t launch_dequant_tiles(const uint8_t *w, int N, int K, int bits, int g
 {
     const long long units = (long long)nrb * (K / kKU) * kWR;
     const unsigned blocks = (unsigned)((units * 32 + 127) / 128);
+    auto go = [&](auto kern) {
+        return launch_plain(kern, dim3(blocks), dim3(128), 0, s, w, N, K, group, nrb, out);
+    };
     switch (bits) {
-    case 2: dequant_tiles_kernel<2><<<blocks, 128, 0, s>>>(w, N, K, group, nrb, out); break;
-    case 3: dequant_tiles_kernel<3><<<blocks, 128, 0, s>>>(w, N, K, group, nrb, out); break;
-    case 4: dequant_tiles_kernel<4><<<blocks, 128, 0, s>>>(w, N, K, group, nrb, out); break;
-    case 5: dequant_tiles_kernel<5><<<blocks, 128, 0, s>>>(w, N, K, group, nrb, out); break;
-    case 6: dequant_tiles_kernel<6><<<blocks, 128, 0, s>>>(w, N, K, group, nrb, out); break;
-    case 8: dequant_tiles_kernel<8><<<blocks, 128, 0, s>>>(w, N, K, group, nrb, out); break;
+    case 2: return go(dequant_tiles_kernel<2>);
+    case 3: return go(dequant_tiles_kernel<3>);
+    case 4: return go(dequant_tiles_kernel<4>);
+    case 5: return go(dequant_tiles_kernel<5>);
+    case 6: return go(dequant_tiles_kernel<6>);
+    case 8: return go(dequant_tiles_kernel<8>);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 __global__ void unpack_codes_kernel(const uint32_t *packed, long long N, long long K, int bits,
@@ -196,8 +199,8 @@ cudaError_t launch_unpack_codes(const uint32_t *packed, long long N, long long K
     const long long total = N * K;
     if (total == 0)
         return cudaSuccess;
-    unpack_codes_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(packed, N, K, bits, codes);
-    return cudaGetLastError();
+    return launch_plain(unpack_codes_kernel, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, s,
+                        packed, N, K, bits, codes);
 }
 
 // x [M][K] (fp32 or bf16) -> fp16 B fragments + fp32 group sums of the fp16
@@ -257,82 +260,13 @@ __global__ void __launch_bounds__(256) xprep_kernel(const void *x, int x_dtype, 
     }
     if (m >= MP)
         return;
-    const int k0 = ku * kKU + part * 16;
     // fp32 input: columns [M, 2M) carry the exact remainder x - fp16(x)
     const bool lo_part = x_dtype == 0 && m >= M && m < 2 * M;
     const int src_m = lo_part ? m - M : m;
     // decoder-block input: the operand is RMSNorm(x) * input_ln
     const float scale = in_w && (m < M || lo_part) ? s_inv[src_m] : 1.f;
-    float v[16];
-    if (m < M || lo_part) {
-        if (x_dtype == 0) {
-            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(x) +
-                                                                 (long long)src_m * K + k0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 f = src[i];
-                v[4 * i] = f.x;
-                v[4 * i + 1] = f.y;
-                v[4 * i + 2] = f.z;
-                v[4 * i + 3] = f.w;
-            }
-        } else {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                static_cast<const __nv_bfloat16 *>(x) + (long long)m * K + k0);
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const uint4 u = src[i];
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    v[8 * i + 2 * j] = bf16_lo(w[j]);
-                    v[8 * i + 2 * j + 1] = bf16_hi(w[j]);
-                }
-            }
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            v[i] = 0.f;
-    }
-    if (in_w && (m < M || lo_part)) {
-        // the normed row is an activation of the residual stream's type: bf16
-        // rows give a bf16 operand, fp32 rows keep fp32 (hi + lo columns)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            v[i] = v[i] * scale * __uint_as_float((uint32_t)in_w[k0 + i] << 16);
-            if (x_dtype != 0)
-                v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
-        }
-    }
-    __half h[16];
-    float sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const __half hi = __float2half_rn(v[i]);
-        h[i] = lo_part ? __float2half_rn(v[i] - __half2float(hi)) : hi;
-        sum += __half2float(h[i]);
-    }
-    // element q of this k16 step goes to lane (m%8)*4 + (q%8)/2, half slot (q/8)*2 + q%2
-    const long long base = (((long long)ku * NT + (m >> 3)) * 8 + part) * 32;
-#pragma unroll
-    for (int cq = 0; cq < 4; ++cq) {
-        const int lane = ((m & 7) << 2) | cq;
-        __half2 lo = __halves2half2(h[2 * cq], h[2 * cq + 1]);
-        __half2 hi = __halves2half2(h[8 + 2 * cq], h[8 + 2 * cq + 1]);
-        uint2 u;
-        u.x = *reinterpret_cast<uint32_t *>(&lo);
-        u.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(x16 + (base + lane) * 4) = u;
-    }
-    // group sums: parts [gi*ppg, (gi+1)*ppg) of this column form group gi
-    const int ppg = group >> 4;
-    for (int o = 1; o < ppg; o <<= 1)
-        sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if ((part % ppg) == 0) {
-        const int gi = part / ppg;
-        xsum[((long long)ku * (kKU / group) + gi) * MP + m] = sum;
-    }
+    x_chunk_to_fragments(x, x_dtype, M, K, group, NT, ku * kKU, m, part, scale, in_w,
+                         x16 + (long long)ku * NT * 1024, xsum + (long long)ku * (kKU / group) * MP);
 }
 
 cudaError_t launch_xprep(const void *x, int x_dtype, int M, int K, int group, int NT, __half *x16,

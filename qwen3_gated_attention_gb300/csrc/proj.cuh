@@ -4,8 +4,9 @@
 // Weights stream once from HBM: one producer warp issues 1-D TMA bulk copies
 // of contiguous stages (all warps' units of one 128-wide k unit, plus the x
 // fragments and group sums of that k unit) into a shared-memory ring; kWR
-// consumer warps unpack the codes in registers straight into exact fp16
-// tensor-core A fragments and run mma.sync m16n8k16 against x (B fragments).
+// consumer warps unpack the codes in registers straight into tensor-core A
+// fragments (each code as the exact fp16 subnormal q * 2^-24, one mask or byte
+// permute per register) and run mma.sync m16n8k16 against x (B fragments).
 // Per group, D = sum code*x is folded as y += scale*D + bias*sum(x) in fp32, so
 // no per-weight dequantization multiply is spent.
 //
@@ -19,18 +20,25 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "unpack.cuh"
+#include "xconv.cuh"
 
 namespace gattn {
 
 // One stage: all 8 k16-steps of this warp's unit, folded into Y.
+//
+// Codes enter the tensor cores as exact fp16 subnormals (unpack_a_sub), so each
+// group's MMA chain ends at 2^-24 * D, D = sum q * x (2^-20 * D on the 4-bit
+// rows whose codes stay in the high nibble); the group folds as
+// y += (scale * 2^24) * (2^-24 D) + bias * X, X the group sum of x.
+// st: the stage's weights; xp: the x fragments of its k unit, group sums after.
 template <int BITS, int NT, int GROUP>
-__device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, int ubytes, int w,
+__device__ __forceinline__ void proj_stage(const uint8_t *st, const uint8_t *xp, int ubytes, int w,
                                            int lane, float (&Y)[2][NT][4])
 {
     const uint8_t *unit = st + w * ubytes;
     const uint8_t *sb = unit + unit_code_bytes(BITS);
-    const uint2 *xf = reinterpret_cast<const uint2 *>(st + step_bytes);
-    const float *xs = reinterpret_cast<const float *>(st + step_bytes + 2048 * NT);
+    const uint2 *xf = reinterpret_cast<const uint2 *>(xp);
+    const float *xs = reinterpret_cast<const float *>(xp + 2048 * NT);
     constexpr int kpg = GROUP / 16;     // k16-steps per group (compile time: no branches)
     const int g = lane >> 2, c = lane & 3;
 
@@ -61,8 +69,8 @@ __device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, in
     for (int ks = 0; ks < 8; ++ks) {
         const int sp = ks % SPLIT;
         uint32_t A[2][4];
-        unpack_a<BITS>(cw, 2 * ks, A[0]);
-        unpack_a<BITS>(cw, 2 * ks + 1, A[1]);
+        unpack_a_sub<BITS>(cw, 2 * ks, A[0]);
+        unpack_a_sub<BITS>(cw, 2 * ks + 1, A[1]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const uint2 b = xf[(nt * 8 + ks) * 32 + lane];
@@ -72,7 +80,10 @@ __device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, in
         if ((ks % kpg) == kpg - 1) {
             const int gi = ks / kpg;
             const uint4 e = *reinterpret_cast<const uint4 *>(sb + (gi * 8 + g) * 16);
-            const float s[4] = {bf16_lo(e.x), bf16_lo(e.y), bf16_lo(e.z), bf16_lo(e.w)};
+            // scale * 2^24 (2^20 for the high-nibble rows), exact powers of two
+            constexpr float kLo = 16777216.f, kHi = BITS == 4 ? 1048576.f : 16777216.f;
+            const float s[4] = {bf16_lo(e.x) * kLo, bf16_lo(e.y) * kHi, bf16_lo(e.z) * kLo,
+                                bf16_lo(e.w) * kHi};
             const float bb[4] = {bf16_hi(e.x), bf16_hi(e.y), bf16_hi(e.z), bf16_hi(e.w)};
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -105,47 +116,60 @@ __device__ __forceinline__ void proj_stage(const uint8_t *st, int step_bytes, in
 // the epilogue itself has no dependent global round trips.
 struct EpiSmem {
     float *red;         // [MP][kRBR] this CTA's partial sums (aliases the stage ring)
+    float *recv;        // partial sums pushed here by the cluster's CTAs (see below)
     float *vals;        // [eb_rows] final values of one column of the cluster's rows
     float *nq, *nk;     // q_norm / k_norm as fp32 [d]
-    double *invf;       // inv_freq [rd/2]
+    float2 *invf;       // inv_freq [rd/2] as float (hi, lo) pairs
     int *cpos;          // cache_pos [B]
 };
 
-// Final value of row `row` (0 .. eb_rows-1 of the cluster), column m: the sum of
-// the ks partials of the row's block, read from the cluster's shared memory, in
-// rank order.  With BATCH > 1 the remote loads are issued BATCH at a time
-// before their adds (the loads are ordered asm statements: interleaving them
-// with the adds serializes their latencies) -- worth its registers for the
-// o_proj's wide splits, not for the q|k|v epilogue.
-template <int MP, int BATCH>
-__device__ __forceinline__ float cluster_row_sum(const ProjArgs &a, const EpiSmem &sm, int row, int m)
+// Split-K reduction by pushing: after its main loop every CTA stores its
+// partial sums straight into the shared memory of the CTA that finishes those
+// values (st.shared::cluster, no round trip), one cluster barrier makes them
+// visible, and each finishing CTA adds its received partials in k-split order
+// from its own shared memory.  Nothing reads another CTA's shared memory after
+// the barrier, so CTAs leave without a second one.
+//
+// q|k|v: column m of the cluster's rows is finished by CTA m % csize; its
+// receive area holds, per local column lc = m / csize and part (0; 1 for the
+// low fp16 plane of fp32 x), per k split, the cluster's eb_rows rows:
+// recv[((lc * P + part) * ks + kr) * eb_rows + row].
+__device__ __forceinline__ void push_qkv(const ProjArgs &a, const EpiSmem &sm, int rank, int csize,
+                                         int tid)
 {
-    const int q = row / kRBR, rr = row % kRBR;
-    const float *local = sm.red + (long long)m * kRBR + rr;
-    const float *lo = local + (long long)a.xsplit * kRBR;
-    float v = 0.f;
-    for (int k0 = 0; k0 < a.ks; k0 += BATCH) {
-        float t[BATCH], u[BATCH];
-#pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-            const uint32_t rank = (uint32_t)(q * a.ks + k0 + k);
-            t[k] = k0 + k < a.ks ? ld_dsmem(dsmem_addr(local, rank)) : 0.f;
-            u[k] = (a.xsplit && k0 + k < a.ks) ? ld_dsmem(dsmem_addr(lo, rank)) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-            v += t[k];
-            v += u[k];
-        }
+    const int P = a.xsplit ? 2 : 1;
+    const int rbl = rank / a.ks, kr = rank % a.ks;
+    for (int idx = tid; idx < a.M * P * (kRBR / 4); idx += kWR * 32) {
+        const int r4 = idx % (kRBR / 4), mp = idx / (kRBR / 4);
+        const int m = mp / P, part = mp % P;
+        const float4 v = *reinterpret_cast<const float4 *>(sm.red + (m + part * a.xsplit) * kRBR + r4 * 4);
+        const int lc = m / csize;
+        float *dst = sm.recv + ((long long)(lc * P + part) * a.ks + kr) * a.eb_rows + rbl * kRBR + r4 * 4;
+        st_dsmem_v4(dsmem_addr(dst, (uint32_t)(m % csize)), v);
     }
-    return v;
+}
+
+// o_proj: row r of the row block is finished by CTA r / rpr (rpr = ceil(128 /
+// csize) rows each): recv[(kr * M + m) * rpr + r % rpr].
+__device__ __forceinline__ void push_o(const ProjArgs &a, const EpiSmem &sm, int rank, int csize,
+                                       int tid)
+{
+    const int rpr = (kRBR + csize - 1) / csize;
+    const int kr = rank;
+    for (int idx = tid; idx < a.M * kRBR; idx += kWR * 32) {
+        const int r = idx % kRBR, m = idx / kRBR;
+        const int owner = r / rpr;
+        float *dst = sm.recv + ((long long)kr * a.M + m) * rpr + (r - owner * rpr);
+        st_dsmem(dsmem_addr(dst, (uint32_t)owner), sm.red[m * kRBR + r]);
+    }
 }
 
 // q|k|v epilogue of the cluster's rows (whole heads): this CTA takes the
-// columns m with m % cluster_size == rank.  Per column: the final values into
-// shared memory, then per head one warp splits query / gate / k / v, applies
-// RMSNorm + partial RoPE to query and k, and writes q (bf16), the gate (fp32)
-// and the new cache rows (bf16).
+// columns m with m % cluster_size == rank.  Per column: the final values (the
+// received partials added in k-split order) into shared memory, then per head
+// one warp splits query / gate / k / v, applies RMSNorm + partial RoPE to
+// query and k, and writes q (bf16), the gate (fp32) and the new cache rows
+// (bf16).
 template <int MP>
 static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const EpiSmem &sm, int row0,
                                     int rank, int csize, int warp, int lane, int tid)
@@ -159,8 +183,18 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
         for (int idx = tid; idx < mper * a.eb_rows; idx += kWR * 32) {
             const int j = idx / a.eb_rows, r = idx - j * a.eb_rows;
             const int m = m0 + j * csize;
-            if (m < a.M)
-                sm.vals[idx] = cluster_row_sum<MP, 1>(a, sm, r, m);
+            if (m < a.M) {
+                const int P = a.xsplit ? 2 : 1, lc = m / csize;
+                const float *hi = sm.recv + (long long)(lc * P) * a.ks * a.eb_rows + r;
+                const float *lo = hi + (long long)a.ks * a.eb_rows;
+                float v = 0.f;
+                for (int k = 0; k < a.ks; ++k) {
+                    v += hi[(long long)k * a.eb_rows];
+                    if (a.xsplit)
+                        v += lo[(long long)k * a.eb_rows];
+                }
+                sm.vals[idx] = v;
+            }
         }
         named_bar_sync(1, kWR * 32);
         for (int wi = warp; wi < mper * heads; wi += kWR) {
@@ -212,8 +246,13 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
                     ss += __shfl_xor_sync(0xffffffffu, ss, o);
                 const float inv = rsqrtf(ss / (float)d + e.eps);
                 const float *nw = kind == 0 ? sm.nq : sm.nk;
-                // partial rotary on dims [0, rd): pairs (j, j + rd/2) at position p0 + r
-                const double pos = (double)(p0 + r);
+                // partial rotary on dims [0, rd): pairs (j, j + rd/2) at position p0 + r.
+                // The angle pos * inv_freq is formed as an unevaluated float pair
+                // (inv_freq split in hi + lo on the host, the product's rounding
+                // error recovered with an fma) and reduced modulo 2 pi with a
+                // two-constant Cody-Waite step, so the reduced angle is good to a
+                // few 1e-7 rad for positions far past 1e5 with no double math
+                const float pos = (float)(p0 + r);      // exact below 2^24
                 float o[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -223,11 +262,15 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
                         const int fi = j < half ? j : j - half;
                         const int jp = j < half ? j + half : j - half;
                         const float partner = hv[jp] * inv * nw[jp];
-                        const double ang = pos * sm.invf[fi];
-                        const double turns = rint(ang * 0.15915494309189535);
-                        const float red = (float)fma(-turns, 6.283185307179586, ang);
+                        const float2 fq = sm.invf[fi];
+                        const float ph = pos * fq.x;
+                        const float pl = fmaf(pos, fq.x, -ph) + pos * fq.y;
+                        const float turns = rintf(ph * 0.15915494f);
+                        float red = fmaf(-turns, 6.2831855f, ph);     // 2 pi = 6.2831855f
+                        red = fmaf(-turns, -1.7484555e-07f, red);    //   + -1.7484555e-07f
+                        red += pl;
                         float sn, cs;
-                        __sincosf(red, &sn, &cs);   // |red| <= pi: hardware path
+                        __sincosf(red, &sn, &cs);   // |red| <= pi + 1e-6: hardware path
                         o[i] = j < half ? o[i] * cs - partner * sn : o[i] * cs + partner * sn;
                     }
                 }
@@ -276,7 +319,8 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
 
 // o_proj epilogue: the cluster's single row block, rows split across its CTAs
 // (ceil(128 / cluster size) per rank); thread t takes row rank * rpr + t % rpr
-// and the columns t / rpr + j * (128 / rpr).
+// and the columns t / rpr + j * (128 / rpr), adding the received partials in
+// k-split order.
 template <int MP>
 static __device__ void epilogue_o(const ProjArgs &a, const EpiO &e, const EpiSmem &sm, int row0,
                                   int rank, int csize, int tid)
@@ -293,7 +337,12 @@ static __device__ void epilogue_o(const ProjArgs &a, const EpiO &e, const EpiSme
         const int b = m / e.R;
         const int pb = sm.cpos[b];
         const bool valid = pb >= 0 && pb + e.R <= e.cap;
-        float v = valid ? cluster_row_sum<MP, 8>(a, sm, r, m) : 0.f;
+        float v = 0.f;
+        if (valid) {
+            const float *pr = sm.recv + (long long)m * rpr + (r - rank * rpr);
+            for (int k = 0; k < a.ks; ++k)
+                v += pr[(long long)k * a.M * rpr];
+        }
         if (e.resid) {
             const long long ri = (long long)m * a.N + n;
             v += e.resid_f32 ? static_cast<const float *>(e.resid)[ri]
@@ -315,7 +364,7 @@ static __device__ void postnorm_tail(const ProjArgs &a, const EpiO &e, float *sc
                                      int rank, int csize)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int kWarps = kWR + 1;
+    const int kWarps = (int)(blockDim.x >> 5);
     const int rpr = (kRBR + csize - 1) / csize;
     const int r0 = rank * rpr;
     const int nr = max(0, min(min(rpr, kRBR - r0), a.N - (row0 + r0)));
@@ -377,11 +426,12 @@ static __device__ void postnorm_tail(const ProjArgs &a, const EpiO &e, float *sc
 // Two CTAs per SM at least; the four-column-tile instances, whose grids are
 // short of CTAs at two per SM, ask for three.
 template <int BITS, int NT, int MODE, int GROUP>
-__global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
+__global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
     proj_kernel(const ProjArgs a, const EpiQKV eq, const EpiO eo)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int MP = 8 * NT;
+    constexpr int kProducer = kWR;            // the producer warp
     const int S = a.stages;
     uint8_t *stages = smem;
     uint8_t *tail = smem + (size_t)S * a.stage_bytes;
@@ -393,8 +443,11 @@ __global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
     sm.vals = reinterpret_cast<float *>(tail + 256);
     sm.nq = sm.vals + kValsFloats;
     sm.nk = sm.nq + 256;
-    sm.invf = reinterpret_cast<double *>(sm.nk + 256);
+    sm.invf = reinterpret_cast<float2 *>(sm.nk + 256);
     sm.cpos = reinterpret_cast<int *>(sm.invf + 128);
+    sm.recv = reinterpret_cast<float *>(tail + proj_tail_bytes(a.eb_rows));
+    uint8_t *xtab = reinterpret_cast<uint8_t *>(sm.recv + a.recv_cap);   // a.xtab_bytes
+    const bool xfold = MODE == kModeQKV && a.xtab_bytes > 0;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int csize = a.rbc * a.ks;
@@ -425,7 +478,7 @@ __global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
                 sm.nk[j] = __uint_as_float((uint32_t)eq.k_norm[j] << 16);
             }
             for (int j = t; j < eq.rd / 2; j += kWR * 32)
-                sm.invf[j] = eq.inv_freq[j];
+                sm.invf[j] = eq.inv_freq2[j];
             if (t < (a.M + eq.R - 1) / eq.R)
                 sm.cpos[t] = eq.cache_pos[t];
         } else {
@@ -446,7 +499,7 @@ __global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
             for (int i = 0; i < 4; ++i)
                 Y[mt][nt][i] = 0.f;
 
-    if (warp == kWR) {
+    if (warp == kProducer) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
@@ -454,14 +507,16 @@ __global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
             // weights do not depend on the previous kernel: start streaming them
             // before waiting for it, then fetch x once it is visible.
             const long long pre = (end - beg) < S ? (end - beg) : S;
+            // bytes a stage brings: weights, and x unless the CTA converts x itself
+            const uint32_t stage_tx = a.step_bytes + (xfold ? 0 : xbytes + sbytes);
             for (; it < pre; ++it) {
                 const long long s = beg + it;
                 uint8_t *st = stages + (size_t)(it % S) * a.stage_bytes;
-                mbar_arrive_expect_tx(&full[it % S], a.step_bytes + xbytes + sbytes);
+                mbar_arrive_expect_tx(&full[it % S], stage_tx);
                 bulk_g2s(st, a.w + s * a.step_bytes, a.step_bytes, &full[it % S], pol);
             }
             pdl_wait();
-            for (long long i = 0; i < pre; ++i) {
+            for (long long i = 0; i < pre && !xfold; ++i) {
                 const int ku = (int)((beg + i) % a.nku);
                 uint8_t *st = stages + (size_t)(i % S) * a.stage_bytes;
                 bulk_g2s(st + a.step_bytes, a.x16 + (long long)ku * NT * 1024, xbytes,
@@ -477,12 +532,14 @@ __global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
                     break;
                 const int ku = (int)(s % a.nku);
                 uint8_t *st = stages + (size_t)slot * a.stage_bytes;
-                mbar_arrive_expect_tx(&full[slot], a.step_bytes + xbytes + sbytes);
+                mbar_arrive_expect_tx(&full[slot], stage_tx);
                 bulk_g2s(st, a.w + s * a.step_bytes, a.step_bytes, &full[slot], pol);
-                bulk_g2s(st + a.step_bytes, a.x16 + (long long)ku * NT * 1024, xbytes, &full[slot],
-                         pol);
-                bulk_g2s(st + a.step_bytes + xbytes, a.xsum + (long long)ku * (kKU / GROUP) * MP,
-                         sbytes, &full[slot], pol);
+                if (!xfold) {
+                    bulk_g2s(st + a.step_bytes, a.x16 + (long long)ku * NT * 1024, xbytes,
+                             &full[slot], pol);
+                    bulk_g2s(st + a.step_bytes + xbytes,
+                             a.xsum + (long long)ku * (kKU / GROUP) * MP, sbytes, &full[slot], pol);
+                }
             }
             // let every copy this CTA issued land before the ring is reused
             const long long first = it > S ? it - S : 0;
@@ -501,12 +558,28 @@ __global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
         // have completed, so that attention can prefetch cache rows before waiting
         if constexpr (MODE == kModeQKV)
             pdl_launch_dependents();
-        long long it = 0;
-        for (long long s = beg; s < end; ++s, ++it) {
+        // the x table of this CTA's k units: 16 (k unit, column) chunks of 128 k
+        // per pass, eight lanes each
+        const int xe = xbytes + sbytes;
+        if (xfold) {
+            const int nk = ku1 - ku0;
+            for (int b0 = 0; b0 < nk * MP; b0 += kWR * 4) {
+                const int item = b0 + (threadIdx.x >> 3);
+                const bool live = item < nk * MP;
+                const int kl = live ? item / MP : 0, m = live ? item % MP : 0;
+                x_chunk_to_fragments(a.xraw, a.x_f32 ? 0 : 1, a.M, a.nku * kKU, GROUP, NT,
+                                     (ku0 + kl) * kKU, m, threadIdx.x & 7, 1.f, nullptr,
+                                     reinterpret_cast<__half *>(xtab + kl * xe),
+                                     reinterpret_cast<float *>(xtab + kl * xe + xbytes), live);
+            }
+            named_bar_sync(1, kWR * 32);
+        }
+        for (long long it = 0; beg + it < end; ++it) {
             const int slot = (int)(it % S);
             const uint32_t ph = (uint32_t)((it / S) & 1);
+            const uint8_t *st = stages + (size_t)slot * a.stage_bytes;
             if (mbar_wait(&full[slot], ph, abort, a.status))
-                proj_stage<BITS, NT, GROUP>(stages + (size_t)slot * a.stage_bytes, a.step_bytes,
+                proj_stage<BITS, NT, GROUP>(st, xfold ? xtab + it * xe : st + a.step_bytes,
                                             a.unit_bytes, warp, lane, Y);
             __syncwarp();
             if (lane == 0)
@@ -528,7 +601,14 @@ __global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
                 sm.red[(col + 1) * kRBR + row + 8] = Y[mt][nt][3];
             }
     }
-    cluster_sync();     // every CTA's partial is visible to the cluster
+    __syncthreads();
+    if (warp < kWR) {
+        if constexpr (MODE == kModeQKV)
+            push_qkv(a, sm, rank, csize, threadIdx.x);
+        else
+            push_o(a, sm, rank, csize, threadIdx.x);
+    }
+    cluster_sync();     // every pushed partial has landed in its finishing CTA
     if (warp < kWR) {
         const int row0 = cluster * a.eb_rows;
         if constexpr (MODE == kModeQKV)
@@ -536,7 +616,6 @@ __global__ void __launch_bounds__((kWR + 1) * 32, NT >= 4 ? 3 : 2)
         else
             epilogue_o<MP>(a, eo, sm, row0, rank, csize, threadIdx.x);
     }
-    cluster_sync();     // no CTA leaves while others may still read its partial
     if constexpr (MODE == kModeO) {
         if (eo.out_n)
             postnorm_tail<MP>(a, eo, reinterpret_cast<float *>(stages), cluster * a.eb_rows, rank,
@@ -550,7 +629,7 @@ cudaError_t launch_proj_t(const ProjArgs &a, const EpiQKV &eq, const EpiO &eo, i
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3((kWR + 1) * 32);
+    cfg.blockDim = dim3(proj_threads(NT));
     cfg.dynamicSmemBytes = proj_smem_bytes(a);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];

@@ -15,7 +15,8 @@ GATTN_DECL(2) GATTN_DECL(3) GATTN_DECL(4) GATTN_DECL(5) GATTN_DECL(6) GATTN_DECL
 int proj_smem_bytes(const ProjArgs &a)
 {
     // stage ring + barriers/flags + epilogue statics (proj_tail_bytes in kernels.cuh)
-    return a.stages * a.stage_bytes + proj_tail_bytes(a.eb_rows);
+    // + the split-K receive area + the converted-x table
+    return a.stages * a.stage_bytes + proj_tail_bytes(a.eb_rows) + a.recv_cap * 4 + a.xtab_bytes;
 }
 
 cudaError_t launch_proj(int bits, int NT, int mode, const ProjArgs &a, const EpiQKV &eq,

@@ -35,7 +35,7 @@
     {                                                                                              \
         return with_proj_kernel<B>(NT, mode, group, [&](auto kern, auto launch) {                  \
             (void)launch;                                                                          \
-            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, (kWR + 1) * 32, smem); \
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, proj_threads(NT), smem); \
         });                                                                                        \
     }                                                                                              \
     cudaError_t clusters_b##B(int NT, int mode, int group, int smem, int csize, int *n)            \
@@ -44,7 +44,7 @@
             (void)launch;                                                                          \
             cudaLaunchConfig_t cfg = {};                                                           \
             cfg.gridDim = dim3(csize);                                                             \
-            cfg.blockDim = dim3((kWR + 1) * 32);                                                   \
+            cfg.blockDim = dim3(proj_threads(NT));                                                 \
             cfg.dynamicSmemBytes = smem;                                                           \
             cudaLaunchAttribute at[1];                                                             \
             at[0].id = cudaLaunchAttributeClusterDimension;                                        \

@@ -12,6 +12,7 @@
 #include <cstdio>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "gattn.h"
@@ -25,12 +26,51 @@ namespace {
 constexpr size_t kStaticScratchFloats = size_t(4) << 20;
 static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
 
-// Device address of g_static_scratch per device.  In host code the symbol's
-// name is only a host-side stand-in, not a device address, so it is looked up
-// with cudaGetSymbolAddress once per device (with that device current).
+// Device address of g_static_scratch per device, remembered together with the
+// CUDA context it was resolved in.  In host code the symbol's name is only a
+// host-side stand-in, not a device address, so it is looked up with
+// cudaGetSymbolAddress with the device current.  A context that is destroyed
+// and created again (cudaDeviceReset, or the primary context released and
+// retained again) reloads the module, and the array may then sit elsewhere:
+// the cached address is used only while the current context's unique id is
+// the one it was resolved under, and is looked up again otherwise.
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 float *g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
+
+typedef CUresult (*PfnCtxGetCurrent)(CUcontext *);
+typedef CUresult (*PfnCtxGetId)(CUcontext, unsigned long long *);
+
+// Unique id of the calling thread's current context (driver entry points
+// resolved once through the runtime, so the library needs no libcuda link).
+cudaError_t current_context_id(unsigned long long *id)
+{
+    static PfnCtxGetCurrent get_current = nullptr;
+    static PfnCtxGetId get_id = nullptr;
+    static cudaError_t resolved = cudaErrorUnknown;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000,
+                                                         cudaEnableDefault, &q1);
+        if (e == cudaSuccess)
+            e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+        if (e == cudaSuccess && (q1 != cudaDriverEntryPointSuccess || !f1 ||
+                                 q2 != cudaDriverEntryPointSuccess || !f2))
+            e = cudaErrorSymbolNotFound;
+        get_current = reinterpret_cast<PfnCtxGetCurrent>(f1);
+        get_id = reinterpret_cast<PfnCtxGetId>(f2);
+        resolved = e;
+    });
+    if (resolved != cudaSuccess)
+        return resolved;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, id) != CUDA_SUCCESS)
+        return cudaErrorDeviceUninitialized;
+    return cudaSuccess;
+}
 
 gattn_status scratch_for_current_device(float **out)
 {
@@ -44,10 +84,17 @@ gattn_status scratch_for_current_device(float **out)
         gattn_set_error("device index beyond the static scratch table");
         return GATTN_E_UNSUPPORTED;
     }
+    // the thread's current context; before the runtime has bound one to this
+    // thread there is none (id 0), and the symbol lookup below binds it
+    unsigned long long ctx = 0;
+    if (current_context_id(&ctx) != cudaSuccess)
+        ctx = 0;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         float *p = nullptr;
         e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_static_scratch);
+        if (e == cudaSuccess && ctx == 0)
+            e = current_context_id(&ctx);
         if (e != cudaSuccess || !p) {
             char msg[256];
             snprintf(msg, sizeof msg, "cudaGetSymbolAddress of the static scratch failed: %s",
@@ -56,6 +103,7 @@ gattn_status scratch_for_current_device(float **out)
             return GATTN_E_CUDA;
         }
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return GATTN_OK;

@@ -28,8 +28,8 @@ cudaError_t launch_turbo4_quantize(const uint16_t *v, long long rows, int d, uin
     if (rows <= 0)
         return cudaSuccess;
     const unsigned grid = (unsigned)((rows + 7) / 8);
-    turbo4_quantize_kernel<<<grid, 256, 0, s>>>(v, rows, d, codes, scales, t);
-    return cudaGetLastError();
+    return launch_plain(turbo4_quantize_kernel, dim3(grid), dim3(256), 0, s, v, rows, d, codes,
+                        scales, t);
 }
 
 }  // namespace gattn

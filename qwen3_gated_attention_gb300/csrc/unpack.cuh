@@ -63,4 +63,36 @@ __device__ __forceinline__ void unpack_a(const uint32_t *cw, int mi, uint32_t (&
     }
 }
 
+// The A fragment of MMA mi with each code q as the fp16 bit pattern q itself:
+// the subnormal q * 2^-24, exact (q < 2^10).  Products with fp16 x are exact in
+// fp32, so the tensor cores return 2^-24 * sum q * x, which the projection
+// scales back when it folds a group (scale * 2^24).  4-bit codes in the high
+// nibble of a byte (A[1], A[3]: rows g + 8 of the fragment) stay in place,
+// 16 q * 2^-24, and their rows fold with scale * 2^20.  One mask or one byte
+// permute per register.
+template <int BITS>
+__device__ __forceinline__ void unpack_a_sub(const uint32_t *cw, int mi, uint32_t (&A)[4])
+{
+    if constexpr (BITS == 8) {
+        const uint32_t w0 = cw[2 * mi], w1 = cw[2 * mi + 1];
+        A[0] = __byte_perm(w0, 0u, 0x4140);
+        A[1] = __byte_perm(w0, 0u, 0x4342);
+        A[2] = __byte_perm(w1, 0u, 0x4140);
+        A[3] = __byte_perm(w1, 0u, 0x4342);
+    } else if constexpr (BITS == 4) {
+        const uint32_t w = cw[mi], w8 = w >> 8;
+        A[0] = w & 0x000F000Fu;
+        A[1] = w & 0x00F000F0u;
+        A[2] = w8 & 0x000F000Fu;
+        A[3] = w8 & 0x00F000F0u;
+    } else {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int off = (mi * 8 + 2 * p) * BITS;
+            const uint32_t c0 = code_at<BITS>(cw, off), c1 = code_at<BITS>(cw, off + BITS);
+            A[p] = c0 | (c1 << 16);
+        }
+    }
+}
+
 }  // namespace gattn

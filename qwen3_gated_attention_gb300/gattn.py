@@ -23,6 +23,9 @@ STATUS_NAMES = {0: "GATTN_OK", 1: "GATTN_E_INVALID_ARG", 2: "GATTN_E_UNSUPPORTED
 DTYPE_F32, DTYPE_BF16 = 0, 1
 PROJ_Q, PROJ_K, PROJ_V, PROJ_O = 0, 1, 2, 3
 PATH_AUTO, PATH_FUSED, PATH_SPLIT = 0, 1, 2
+# kernels of a step (gattn_layer_step_kernels)
+KERNEL_NAMES = {1: "xprep", 2: "proj_qkv", 3: "attn", 4: "merge", 5: "proj_o", 6: "postnorm",
+                7: "layer_step"}
 
 # every symbol include/gattn.h declares
 EXPORTS = (
@@ -33,7 +36,7 @@ EXPORTS = (
     "gattn_layer_launches_per_step", "gattn_layer_set_events", "gattn_layer_dequant_device_static",
     "gattn_layer_set_path", "gattn_layer_step_block", "gattn_kv_register_turbo4v",
     "gattn_turbo4_codebook", "gattn_turbo4_quantize_device", "gattn_layer_set_mask",
-    "gattn_kv_register_turbo4",
+    "gattn_kv_register_turbo4", "gattn_layer_step_kernels",
 )
 
 
@@ -125,6 +128,8 @@ def lib():
         L.gattn_head_chunk_plan.restype = i32
         L.gattn_layer_launches_per_step.argtypes = [p]
         L.gattn_layer_launches_per_step.restype = i32
+        L.gattn_layer_step_kernels.argtypes = [p, p, i32]
+        L.gattn_layer_step_kernels.restype = i32
         L.gattn_layer_set_events.argtypes = [p, p, i32]
         L.gattn_layer_set_path.argtypes = [p, i32]
         L.gattn_layer_step_block.argtypes = [p, p, p, p, i32, i32, p, p, p, p, p]
@@ -284,6 +289,15 @@ def kv_destroy(kv: int) -> None:
 
 def layer_launches_per_step(layer: int) -> int:
     return int(lib().gattn_layer_launches_per_step(layer))
+
+
+def layer_step_kernels(layer: int) -> list:
+    """Names of the kernels the layer's last step launched, in order."""
+    arr = (C.c_int32 * 8)()
+    n = int(lib().gattn_layer_step_kernels(layer, C.addressof(arr), 8))
+    if n < 0:
+        raise GattnError(1, "bad arguments")
+    return [KERNEL_NAMES.get(int(arr[i]), "?") for i in range(min(n, 8))]
 
 
 def layer_step_block(layer: int, x: int, kv: int, cache_pos: int, batch: int, q_len: int,

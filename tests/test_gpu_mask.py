@@ -150,3 +150,27 @@ def test_mask_is_refused_on_the_one_kernel_path():
     with pytest.raises(gattn.GattnError) as ei:
         _run(spec, case, _mask(spec, 1, 14), path=gattn.PATH_FUSED)
     assert ei.value.status == 2
+
+
+@pytest.mark.parametrize("name", ["batched_mixed_small", "tiny_r8"])
+def test_mask_rows_shorter_than_the_attended_span(name):
+    """Mask rows of fewer positions than cache_pos + R (DS4Server issue 113,
+    masks sliced per head chunk): positions past a row are not attended.  The
+    row length here sits inside the shortest sequence's span, so every
+    sequence loses its tail.  Against the oracle's short-row entry, and
+    bitwise equal to the same mask padded with zeros."""
+    spec = CASES[name]
+    case = make_case(spec)
+    pos = spec.positions()
+    T = int(pos.min()) + 1
+    mask = _mask(spec, 1, 15, "tree")[..., :T].copy()
+    mask[..., 0] = 1                      # every row keeps one visible position
+    got = _run(spec, case, mask)
+    kc, vc = case.ck.copy(), case.cv.copy()
+    out, _, ta = orc.layer_step_ext(spec, case.orc_weights, synth.x_values(spec, case.x), kc, vc,
+                                    case.pos, mask=mask, taps=True)
+    _check(name, spec, case, got, out, ta, kc)
+    padded = np.zeros(mask.shape[:3] + (int(pos.max()) + spec.q_len,), np.uint8)
+    padded[..., :T] = mask
+    full = _run(spec, case, padded)
+    assert np.array_equal(got["out"], full["out"]) and np.array_equal(got["attn"], full["attn"])

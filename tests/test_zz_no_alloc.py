@@ -8,11 +8,14 @@ point bit for bit (the tolerance every dequant test here uses), on calls made
 back to back: the fixed staging array keeps the previous call's contents, so a
 second call must not depend on them.  Collected last on purpose, so that a run
 stopping at the first failure has already run every other test."""
+import numpy as np
 import pytest
 import torch
 
+import oracle as orc
 from qwen3_gated_attention_gb300 import gattn, synth
 from qwen3_gated_attention_gb300.device import DeviceLayer
+from tests.cases import make_case
 
 pytestmark = pytest.mark.gpu
 
@@ -23,6 +26,12 @@ SPECS = {
         name="d128_b5_b2", hidden=512, num_heads=12, num_kv_heads=2, head_dim=128,
         partial_rotary_factor=0.5, rope_theta=1e6, rms_eps=1e-6, bits=(5, 5, 5, 2),
         group=(32, 32, 32, 64), batch=2, q_len=4, x_dtype="f32", length_range=(70, 200)),
+    # one KV head of head_dim 64: the q rows fill two 128-row blocks, k takes the
+    # first half of the third and v starts 64 rows into it, so the copy out of
+    # the staging array begins inside a row block
+    "h2_hk1_d64": synth.WORKLOADS["tiny"].with_(
+        name="h2_hk1_d64", hidden=256, num_heads=2, num_kv_heads=1, bits=(8,) * 4,
+        group=(32,) * 4, x_dtype="bf16"),
 }
 
 
@@ -51,6 +60,7 @@ def _shape(spec, p):
 def test_static_dequant_matches_allocating_entry_point(name):
     spec = SPECS[name]
     dl = _layer(spec)
+    orc_w = make_case(spec, with_cache=False).orc_weights if name == "h2_hk1_d64" else None
     stream = torch.cuda.current_stream().cuda_stream
     try:
         # two passes over all projections, back to back on one stream: every
@@ -64,6 +74,11 @@ def test_static_dequant_matches_allocating_entry_point(name):
                 gattn.layer_dequant_device_static(dl.h, p, got.data_ptr(), stream)
                 torch.cuda.synchronize()
                 assert torch.equal(got, ref), f"projection {p}"
+                if name == "h2_hk1_d64":
+                    W = orc_w
+                    want = orc.dequantize(W.packed[p], W.scales[p], W.biases[p], N, K,
+                                          spec.bits[p], spec.group[p]).astype(np.float32)
+                    assert np.array_equal(got.cpu().numpy(), want), f"projection {p} vs oracle"
     finally:
         dl.close()
 
