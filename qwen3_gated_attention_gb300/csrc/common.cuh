@@ -182,6 +182,42 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank)
     return r;
 }
 
+// Split cluster barrier: arrive (relaxed) early, wait later.  With
+// fence_mbar_init() before the arrive, mbarriers initialized before it may be
+// signalled by other CTAs of the cluster after the wait.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Asynchronous stores into another CTA's shared memory (addresses from
+// dsmem_addr): each counts its bytes on the mbarrier `bar` of the destination
+// CTA (a shared::cluster address from dsmem_addr too), which completes its phase
+// once the bytes it expects have all landed.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+                 ::"r"(addr), "f"(v), "r"(bar)
+                 : "memory");
+}
+
 // Stores into another CTA's shared memory (addresses from dsmem_addr); they are
 // visible to that CTA after the next cluster barrier.
 __device__ __forceinline__ void st_dsmem(uint32_t addr, float v)

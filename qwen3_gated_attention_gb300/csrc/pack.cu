@@ -265,8 +265,9 @@ __global__ void __launch_bounds__(256) xprep_kernel(const void *x, int x_dtype, 
     const int src_m = lo_part ? m - M : m;
     // decoder-block input: the operand is RMSNorm(x) * input_ln
     const float scale = in_w && (m < M || lo_part) ? s_inv[src_m] : 1.f;
-    x_chunk_to_fragments(x, x_dtype, M, K, group, NT, ku * kKU, m, part, scale, in_w,
-                         x16 + (long long)ku * NT * 1024, xsum + (long long)ku * (kKU / group) * MP);
+    const XRaw raw = x_chunk_load(x, x_dtype, M, K, ku * kKU, m, part);
+    x_chunk_convert(raw, x_dtype, M, group, NT, ku * kKU, m, part, scale, in_w,
+                    x16 + (long long)ku * NT * 1024, xsum + (long long)ku * (kKU / group) * MP);
 }
 
 cudaError_t launch_xprep(const void *x, int x_dtype, int M, int K, int group, int NT, __half *x16,

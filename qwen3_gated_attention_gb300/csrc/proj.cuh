@@ -125,17 +125,19 @@ struct EpiSmem {
 
 // Split-K reduction by pushing: after its main loop every CTA stores its
 // partial sums straight into the shared memory of the CTA that finishes those
-// values (st.shared::cluster, no round trip), one cluster barrier makes them
-// visible, and each finishing CTA adds its received partials in k-split order
-// from its own shared memory.  Nothing reads another CTA's shared memory after
-// the barrier, so CTAs leave without a second one.
+// values (st.async, no round trip), each store counting its bytes on the
+// receiver's mbarrier `rbar`; a finishing CTA waits on its own rbar for the
+// bytes it expects and adds the received partials in k-split order from its own
+// shared memory.  No cluster-wide barrier between the main loop and the
+// epilogue; one at the very end keeps every CTA resident until all receivers
+// have their bytes.
 //
 // q|k|v: column m of the cluster's rows is finished by CTA m % csize; its
 // receive area holds, per local column lc = m / csize and part (0; 1 for the
 // low fp16 plane of fp32 x), per k split, the cluster's eb_rows rows:
 // recv[((lc * P + part) * ks + kr) * eb_rows + row].
-__device__ __forceinline__ void push_qkv(const ProjArgs &a, const EpiSmem &sm, int rank, int csize,
-                                         int tid)
+__device__ __forceinline__ void push_qkv(const ProjArgs &a, const EpiSmem &sm, const uint64_t *rbar,
+                                         int rank, int csize, int tid)
 {
     const int P = a.xsplit ? 2 : 1;
     const int rbl = rank / a.ks, kr = rank % a.ks;
@@ -145,14 +147,23 @@ __device__ __forceinline__ void push_qkv(const ProjArgs &a, const EpiSmem &sm, i
         const float4 v = *reinterpret_cast<const float4 *>(sm.red + (m + part * a.xsplit) * kRBR + r4 * 4);
         const int lc = m / csize;
         float *dst = sm.recv + ((long long)(lc * P + part) * a.ks + kr) * a.eb_rows + rbl * kRBR + r4 * 4;
-        st_dsmem_v4(dsmem_addr(dst, (uint32_t)(m % csize)), v);
+        const uint32_t owner = (uint32_t)(m % csize);
+        st_async_v4(dsmem_addr(dst, owner), v, dsmem_addr(rbar, owner));
     }
+}
+
+// Bytes the q|k|v receive area of CTA `rank` expects: every CTA of the cluster
+// sends its kRBR rows of each column the rank finishes (x2 with low planes).
+__device__ __forceinline__ uint32_t recv_bytes_qkv(const ProjArgs &a, int rank, int csize)
+{
+    const int cols = rank < a.M ? (a.M - rank + csize - 1) / csize : 0;
+    return (uint32_t)cols * (a.xsplit ? 2u : 1u) * (uint32_t)csize * kRBR * 4u;
 }
 
 // o_proj: row r of the row block is finished by CTA r / rpr (rpr = ceil(128 /
 // csize) rows each): recv[(kr * M + m) * rpr + r % rpr].
-__device__ __forceinline__ void push_o(const ProjArgs &a, const EpiSmem &sm, int rank, int csize,
-                                       int tid)
+__device__ __forceinline__ void push_o(const ProjArgs &a, const EpiSmem &sm, const uint64_t *rbar,
+                                       int rank, int csize, int tid)
 {
     const int rpr = (kRBR + csize - 1) / csize;
     const int kr = rank;
@@ -160,8 +171,18 @@ __device__ __forceinline__ void push_o(const ProjArgs &a, const EpiSmem &sm, int
         const int r = idx % kRBR, m = idx / kRBR;
         const int owner = r / rpr;
         float *dst = sm.recv + ((long long)kr * a.M + m) * rpr + (r - owner * rpr);
-        st_dsmem(dsmem_addr(dst, (uint32_t)owner), sm.red[m * kRBR + r]);
+        st_async_f32(dsmem_addr(dst, (uint32_t)owner), sm.red[m * kRBR + r],
+                     dsmem_addr(rbar, (uint32_t)owner));
     }
+}
+
+// Bytes the o_proj receive area of CTA `rank` expects: its rows from every
+// k split, all columns.
+__device__ __forceinline__ uint32_t recv_bytes_o(const ProjArgs &a, int rank, int csize)
+{
+    const int rpr = (kRBR + csize - 1) / csize;
+    const int rows = max(0, min(rpr, kRBR - rank * rpr));
+    return (uint32_t)csize * (uint32_t)a.M * (uint32_t)rows * 4u;
 }
 
 // q|k|v epilogue of the cluster's rows (whole heads): this CTA takes the
@@ -438,6 +459,7 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
     uint64_t *full = reinterpret_cast<uint64_t *>(tail);             // [S <= 8]
     uint64_t *empty = full + 8;                                       // [8]
     int *flags = reinterpret_cast<int *>(tail + 128);                 // [0] abort
+    uint64_t *rbar = reinterpret_cast<uint64_t *>(tail + 192);        // split-K receive
     EpiSmem sm;
     sm.red = reinterpret_cast<float *>(smem);                         // after the main loop
     sm.vals = reinterpret_cast<float *>(tail + 256);
@@ -457,14 +479,21 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
     const int ku0 = (int)((long long)kr * a.nku / a.ks), ku1 = (int)((long long)(kr + 1) * a.nku / a.ks);
     const long long beg = (long long)rb * a.nku + ku0, end = (long long)rb * a.nku + ku1;
 
+    const uint32_t rbytes = MODE == kModeQKV ? recv_bytes_qkv(a, rank, csize)
+                                             : recv_bytes_o(a, rank, csize);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kWR);
         }
+        mbar_init(rbar, 1);
+        if (rbytes)
+            mbar_arrive_expect_tx(rbar, rbytes);
         flags[0] = 0;
         fence_mbar_init();
     }
+    // the cluster's CTAs may signal rbar once everyone is past this point
+    cluster_arrive_relaxed();
     // o_proj lets the next step's kernels launch at once: their pre-wait work
     // (weight streaming) reads nothing this kernel writes
     if constexpr (MODE == kModeO)
@@ -558,19 +587,45 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
         // have completed, so that attention can prefetch cache rows before waiting
         if constexpr (MODE == kModeQKV)
             pdl_launch_dependents();
-        // the x table of this CTA's k units: 16 (k unit, column) chunks of 128 k
-        // per pass, eight lanes each
+        // the x table of this CTA's k units: items (k unit, column) of 128 k, eight
+        // lanes each, sixteen per pass; the columns that carry input come first
+        // and the loads of the first two passes are issued together (one round
+        // trip for the decode and verify shapes), the padding columns are zeros
         const int xe = xbytes + sbytes;
         if (xfold) {
             const int nk = ku1 - ku0;
-            for (int b0 = 0; b0 < nk * MP; b0 += kWR * 4) {
-                const int item = b0 + (threadIdx.x >> 3);
-                const bool live = item < nk * MP;
-                const int kl = live ? item / MP : 0, m = live ? item % MP : 0;
-                x_chunk_to_fragments(a.xraw, a.x_f32 ? 0 : 1, a.M, a.nku * kKU, GROUP, NT,
-                                     (ku0 + kl) * kKU, m, threadIdx.x & 7, 1.f, nullptr,
-                                     reinterpret_cast<__half *>(xtab + kl * xe),
-                                     reinterpret_cast<float *>(xtab + kl * xe + xbytes), live);
+            const int mx = a.xsplit ? 2 * a.M : a.M;            // columns with input
+            const int xd = a.x_f32 ? 0 : 1, K = a.nku * kKU, part = threadIdx.x & 7;
+            auto item_of = [&](int item, int &kl, int &m) {
+                if (item < nk * mx) {
+                    kl = item / mx;
+                    m = item % mx;
+                } else {
+                    const int j = item - nk * mx;
+                    kl = j / (MP - mx);
+                    m = mx + j % (MP - mx);
+                }
+            };
+            for (int b0 = 0; b0 < nk * MP; b0 += 2 * kWR * 4) {
+                int kl[2], m[2];
+                bool live[2];
+                XRaw raw[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int item = b0 + q * kWR * 4 + (threadIdx.x >> 3);
+                    live[q] = item < nk * MP;
+                    kl[q] = 0;
+                    m[q] = 0;
+                    if (live[q])
+                        item_of(item, kl[q], m[q]);
+                    raw[q] = x_chunk_load(a.xraw, xd, a.M, K, (ku0 + kl[q]) * kKU, m[q], part,
+                                          live[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    x_chunk_convert(raw[q], xd, a.M, GROUP, NT, (ku0 + kl[q]) * kKU, m[q], part,
+                                    1.f, nullptr, reinterpret_cast<__half *>(xtab + kl[q] * xe),
+                                    reinterpret_cast<float *>(xtab + kl[q] * xe + xbytes), live[q]);
             }
             named_bar_sync(1, kWR * 32);
         }
@@ -602,14 +657,20 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
             }
     }
     __syncthreads();
+    cluster_wait();     // every receive barrier of the cluster is initialized
     if (warp < kWR) {
         if constexpr (MODE == kModeQKV)
-            push_qkv(a, sm, rank, csize, threadIdx.x);
+            push_qkv(a, sm, rbar, rank, csize, threadIdx.x);
         else
-            push_o(a, sm, rank, csize, threadIdx.x);
+            push_o(a, sm, rbar, rank, csize, threadIdx.x);
     }
-    cluster_sync();     // every pushed partial has landed in its finishing CTA
-    if (warp < kWR) {
+    // every partial this CTA finishes has landed; then the cluster barrier that
+    // keeps each CTA resident until every receiver has its bytes (a CTA's shared
+    // memory must outlive the stores sent to it), waited on only at the end
+    if (warp < kWR && rbytes)
+        mbar_wait(rbar, 0, abort, a.status);
+    cluster_arrive();
+    if (warp < kWR && rbytes) {
         const int row0 = cluster * a.eb_rows;
         if constexpr (MODE == kModeQKV)
             epilogue_qkv<MP>(a, eq, sm, row0, rank, csize, warp, lane, threadIdx.x);
@@ -621,6 +682,7 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
             postnorm_tail<MP>(a, eo, reinterpret_cast<float *>(stages), cluster * a.eb_rows, rank,
                               csize);
     }
+    cluster_wait();
 }
 
 template <int BITS, int NT, int MODE, int GROUP>

@@ -5,46 +5,74 @@
 
 namespace gattn {
 
-// One 16-element chunk of operand column m at one 128-wide k unit: x (fp32 or
-// bf16, row-major [M][K]) to fp16 B-fragment halves, written into `frag` (that
-// k unit's NT x 1024 halves in the order of x16_offset), and the group sums of
-// the same fp16 values into `sums` (that k unit's (128 / group) x MP floats).
-// fp32 x: column m < M holds the nearest fp16, column M + m the exact
-// remainder x - fp16(x).  in_w (bf16 [K], or null): decoder-block input, the
-// operand is x * scale * in_w (scale the row's RMSNorm factor), rounded to bf16
-// for a bf16 stream.  Columns past the operand are zeros.  The eight lanes
-// part = 0..7 of an aligned lane octet call this together (the group sums are
-// shuffles among them); k0unit is the unit's first k in x.  A lane with live
-// false only takes part in the shuffles (it reads and writes nothing).
-__device__ __forceinline__ void x_chunk_to_fragments(const void *x, int x_dtype, int M, int K,
-                                                     int group, int NT, int k0unit, int m, int part,
-                                                     float scale, const uint16_t *in_w,
-                                                     __half *frag, float *sums, bool live = true)
+// The raw input of one 16-element chunk: 16 bf16 (two 16-byte words) or 16
+// fp32 (four), loaded ahead of the conversion so that a thread's loads for
+// several chunks are in flight together.
+struct XRaw {
+    uint4 w[4];
+};
+
+// Loads chunk `part` (16 elements from k0unit + 16 part) of operand column m
+// (fp32: m >= M is the low plane of row m - M) for x_chunk_convert; columns
+// with no input (and lanes with live false) load nothing.
+__device__ __forceinline__ XRaw x_chunk_load(const void *x, int x_dtype, int M, int K, int k0unit,
+                                            int m, int part, bool live = true)
+{
+    XRaw r;
+    const int k0 = k0unit + part * 16;
+    const bool lo_part = x_dtype == 0 && m >= M && m < 2 * M;
+    if (live && (m < M || lo_part)) {
+        const int src_m = lo_part ? m - M : m;
+        if (x_dtype == 0) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const float *>(x) +
+                                                               (long long)src_m * K + k0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                r.w[i] = src[i];
+        } else {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const __nv_bfloat16 *>(x) + (long long)m * K + k0);
+            r.w[0] = src[0];
+            r.w[1] = src[1];
+        }
+    }
+    return r;
+}
+
+// One 16-element chunk of operand column m at one 128-wide k unit (loaded by
+// x_chunk_load): x (fp32 or bf16, row-major [M][K]) to fp16 B-fragment halves,
+// written into `frag` (that k unit's NT x 1024 halves in the order of
+// x16_offset), and the group sums of the same fp16 values into `sums` (that k
+// unit's (128 / group) x MP floats).  fp32 x: column m < M holds the nearest
+// fp16, column M + m the exact remainder x - fp16(x).  in_w (bf16 [K], or
+// null): decoder-block input, the operand is x * scale * in_w (scale the row's
+// RMSNorm factor), rounded to bf16 for a bf16 stream.  Columns past the operand
+// are zeros.  The eight lanes part = 0..7 of an aligned lane octet call this
+// together (the group sums are shuffles among them); k0unit is the unit's first
+// k in x.  A lane with live false only takes part in the shuffles (it writes
+// nothing).
+__device__ __forceinline__ void x_chunk_convert(const XRaw &r, int x_dtype, int M, int group,
+                                                int NT, int k0unit, int m, int part, float scale,
+                                                const uint16_t *in_w, __half *frag, float *sums,
+                                                bool live = true)
 {
     const int MP = 8 * NT;
     const int k0 = k0unit + part * 16;
     const bool lo_part = live && x_dtype == 0 && m >= M && m < 2 * M;
-    const int src_m = lo_part ? m - M : m;
     float v[16];
     if (live && (m < M || lo_part)) {
         if (x_dtype == 0) {
-            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(x) +
-                                                                 (long long)src_m * K + k0);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float4 f = src[i];
-                v[4 * i] = f.x;
-                v[4 * i + 1] = f.y;
-                v[4 * i + 2] = f.z;
-                v[4 * i + 3] = f.w;
+                v[4 * i] = __uint_as_float(r.w[i].x);
+                v[4 * i + 1] = __uint_as_float(r.w[i].y);
+                v[4 * i + 2] = __uint_as_float(r.w[i].z);
+                v[4 * i + 3] = __uint_as_float(r.w[i].w);
             }
         } else {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                static_cast<const __nv_bfloat16 *>(x) + (long long)m * K + k0);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const uint4 u = src[i];
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                const uint32_t w[4] = {r.w[i].x, r.w[i].y, r.w[i].z, r.w[i].w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     v[8 * i + 2 * j] = bf16_lo(w[j]);
