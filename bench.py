@@ -324,9 +324,7 @@ def measure_workload(spec, args, dev, world, dist, l2, full=True):
     layers = []
     for _ in range(n_inst):
         dl = DeviceLayer(spec, packed, qn, kn, cap, head_chunk=not args.no_head_chunk,
-                         device=dev, path={"auto": gattn.PATH_AUTO, "fused": gattn.PATH_FUSED,
-                                           "split": gattn.PATH_SPLIT}[args.path],
-                         kv_format=args.kv)
+                         device=dev, kv_format=args.kv)
         dl._w = None          # interchange copies are no longer needed after repacking
         dl.load_cache(kq if args.kv == "turbo4" else ck,
                       vq if args.kv in ("turbo4v", "turbo4") else cv)
@@ -417,16 +415,11 @@ def measure_workload(spec, args, dev, world, dist, l2, full=True):
 
     # per-kernel pass: events between the step's kernels (programmatic overlap off)
     names = gattn.layer_step_kernels(layers[0].h)
-    if names == ["layer_step"]:
-        kernel_bytes = {"layer_step": step_bytes}
-    else:
-        if "postnorm" not in names and "postnorm" in kernel_bytes:   # post-norm inside the o_proj
-            kernel_bytes["proj_o"] += kernel_bytes.pop("postnorm")
-        if "xprep" not in names:           # x converted inside the q|k|v kernel
-            kernel_bytes = dict(algorithmic_bytes(spec, args.block, args.kv, x_folded=True)[1])
-            if "postnorm" not in names and "postnorm" in kernel_bytes:
-                kernel_bytes["proj_o"] += kernel_bytes.pop("postnorm")
-        kernel_bytes = {n: kernel_bytes[n] for n in names}
+    if "xprep" not in names:               # x converted inside the q|k|v kernel
+        kernel_bytes = dict(algorithmic_bytes(spec, args.block, args.kv, x_folded=True)[1])
+    if "postnorm" not in names and "postnorm" in kernel_bytes:       # post-norm inside the o_proj
+        kernel_bytes["proj_o"] += kernel_bytes.pop("postnorm")
+    kernel_bytes = {n: kernel_bytes[n] for n in names}
     nper = max(args.replays, n_inst)
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(nper)]
     per_kernel_ms = {n: [] for n in names}
@@ -513,7 +506,7 @@ def our_arm(args, spec):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     others = [w for w in PER_WORKLOAD if w != spec.name] \
-        if (args.per_workload and not args.block and args.kv == "bf16" and args.path == "auto") \
+        if (args.per_workload and not args.block and args.kv == "bf16") \
         else []
 
     # CPU baselines first (rank 0, N = 1): the oracle as it stands, before any
@@ -553,8 +546,7 @@ def our_arm(args, spec):
             "l2": f"rotating {r['n_inst']} layer instances, {r['inst_bytes'] / 2**20:.0f} MiB "
                   f"> 4x L2 ({l2 / 2**20:.0f} MiB)",
             "arith": "bf16/fp16 tensor-core operands, fp32 accumulate; 8/4/6/3-bit codes",
-            "path": "one kernel per step" if r["launches"] == 1 else
-                    f"{r['launches']} kernels per step ({', '.join(r['kernels'])})",
+            "path": f"{r['launches']} kernels per step ({', '.join(r['kernels'])})",
             "timing": f"median of {r['replays']} timed replays of a {r['steps']}-step graph"}),
         "replays": r["replays"], "replay_ms": r["replay_ms"],
         "tokens_per_s": r["tokens_per_s"], "hbm_gbs": r["hbm_gbs"],
@@ -589,8 +581,6 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-head-chunk", action="store_true")
-    ap.add_argument("--path", default="auto", choices=["auto", "fused", "split"],
-                    help="which kernels run a step: auto and split take the five-kernel chain, fused the one-kernel step")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "turbo4v", "turbo4"],
                     help="KV cache format: bf16, bf16 K with a Turbo4 V cache, or Turbo4 K and V")
     ap.add_argument("--block", action="store_true",

@@ -216,8 +216,7 @@ typedef struct gattn_kv_turbo4v_desc {
 } gattn_kv_turbo4v_desc;
 
 /* Register a Bf16KTurbo4V cache (as gattn_kv_register).  GATTN_E_INVALID_ARG
- * for a bad pointer, stride, capacity or head_dim.  Steps on such a cache run
- * on the five-kernel path; GATTN_PATH_FUSED refuses them (GATTN_E_UNSUPPORTED). */
+ * for a bad pointer, stride, capacity or head_dim. */
 gattn_status gattn_kv_register_turbo4v(gattn_layer *layer, const gattn_kv_turbo4v_desc *desc,
                                        gattn_kv **out);
 
@@ -285,8 +284,8 @@ gattn_status gattn_turbo4_quantize_device(const void *v_bf16, int64_t rows, int3
  * Errors (nothing is launched): GATTN_E_INVALID_ARG for a NULL argument, a
  * cache registered with another layer, batch outside [1, min(max_batch, cache
  * batch)] or q_len outside [1, max_q_len]; GATTN_E_STATE before
- * gattn_layer_set_weights; GATTN_E_UNSUPPORTED for a step the selected path or
- * the set mask does not take (gattn_layer_set_path, gattn_layer_set_mask);
+ * gattn_layer_set_weights; GATTN_E_UNSUPPORTED for a step the set mask does not
+ * take (gattn_layer_set_mask);
  * GATTN_E_CUDA when a launch fails.
  */
 gattn_status gattn_layer_step(gattn_layer *layer, const void *x, gattn_kv *kv,
@@ -315,7 +314,7 @@ gattn_status gattn_layer_set_taps(gattn_layer *layer, const gattn_taps *taps);
  * row.  Strides in bytes; stride_row >= positions.  The step refuses
  * (GATTN_E_UNSUPPORTED) a head-specific mask when the head-chunked verify route
  * applies (it hands the mask unchanged to every head chunk, where only a
- * broadcast mask fits) and any mask on GATTN_PATH_FUSED.  The contents may
+ * broadcast mask fits).  The contents may
  * change between steps (read at run time, graph-capturable).
  */
 typedef struct gattn_mask {
@@ -405,26 +404,6 @@ int32_t gattn_head_chunk_plan(int32_t q_len, int32_t num_heads, int32_t num_kv_h
                               int32_t enabled, int32_t *chunk_first_head, int32_t *chunk_len,
                               int32_t cap);
 
-/*
- * Which kernels run a step (an execution choice; both compute the same layer,
- * equal up to fp32 summation order):
- *   GATTN_PATH_AUTO   (default) the faster path for the step; in this library
- *                     that is the five-kernel path.
- *   GATTN_PATH_FUSED  the one-kernel path; a step that does not fit it fails
- *                     with GATTN_E_UNSUPPORTED (nothing is launched).
- *   GATTN_PATH_SPLIT  always the five-kernel path.
- * One-kernel path: one persistent CTA per SM, launched cooperatively, runs the
- * q|k|v projection with its epilogue, attention, the merge with the gate and
- * o_proj, handing data between CTAs through flags in library scratch.  A step
- * fits it when batch*q_len <= 8 (<= 4 for fp32 x), batch <= 8, head_dim is 64,
- * 128 or 256, num_kv_heads*head_dim is a multiple of lcm(head_dim, 128), the
- * device supports cooperative launch and its shared memory holds the ring.
- * Five-kernel path: x operand prep, fused q|k|v projection, attention,
- * attention merge + gate, o_proj, chained with programmatic dependent launch.
- * Errors: GATTN_E_INVALID_ARG for a NULL layer or an unknown path.
- */
-enum { GATTN_PATH_AUTO = 0, GATTN_PATH_FUSED = 1, GATTN_PATH_SPLIT = 2 };
-gattn_status gattn_layer_set_path(gattn_layer *layer, int32_t path);
 
 /*
  * Decoder-block variant of gattn_layer_step: the steps on either side of the
@@ -445,8 +424,7 @@ gattn_status gattn_layer_set_path(gattn_layer *layer, int32_t path);
  * post_ln are 16-byte aligned, else in one more launch.  The norm of the
  * input is rounded to bf16 for a bf16 layer (kept fp32 for an fp32 one)
  * before the projections.  GATTN_E_INVALID_ARG for a NULL input_ln,
- * out_normed without post_ln or aliasing out; GATTN_E_UNSUPPORTED on
- * GATTN_PATH_FUSED (the one-kernel path runs the layer alone).
+ * out_normed without post_ln or aliasing out.
  */
 gattn_status gattn_layer_step_block(gattn_layer *layer, const void *x, gattn_kv *kv,
                                     const int32_t *cache_pos, int32_t batch, int32_t q_len,
@@ -454,10 +432,9 @@ gattn_status gattn_layer_step_block(gattn_layer *layer, const void *x, gattn_kv 
                                     void *out_normed, gattn_stream stream);
 
 /* Per-step launch report of the layer's last step: number of kernel launches
- * it enqueued, all of them this library's own kernels (1 on the one-kernel
- * path; on the multi-kernel path 4 when the q|k|v kernel converts x itself,
- * else 5 with the x prep launch, one more for a decoder-block step whose
- * post-norm takes its own launch). */
+ * it enqueued, all of them this library's own kernels: 4 when the q|k|v kernel
+ * converts x itself, else 5 with the x prep launch, one more for a
+ * decoder-block step whose post-norm takes its own launch. */
 int32_t gattn_layer_launches_per_step(const gattn_layer *layer);
 
 /* The kernels of the layer's last step, in launch order. */
@@ -467,8 +444,7 @@ enum {
     GATTN_KERNEL_ATTN = 3,      /* causal GQA attention partials */
     GATTN_KERNEL_MERGE = 4,     /* attention merge + output gate -> o_proj operand */
     GATTN_KERNEL_PROJ_O = 5,    /* o_proj (+ residual and fused post-norm of the block) */
-    GATTN_KERNEL_POSTNORM = 6,  /* post-attention RMSNorm of the block, own launch */
-    GATTN_KERNEL_FUSED = 7      /* the one-kernel step */
+    GATTN_KERNEL_POSTNORM = 6   /* post-attention RMSNorm of the block, own launch */
 };
 /* Writes up to `cap` GATTN_KERNEL_* values (host array) and returns the launch
  * count of the last step (0 before any step), or -1 for bad arguments. */

@@ -184,24 +184,12 @@ struct gattn_layer {
     size_t ws_attn_floats = 0;
     int attn_grid = 0;
     int max_seg = 0;
-    // one-kernel path (steps with at most 8 operand columns)
-    bool fused_ok = false;                 // the configuration admits it
-    int path = GATTN_PATH_AUTO;
-    int fused_smem_max = 0;
-    // residency of the last instance launched, at its shared-memory size
-    cudaError_t (*fused_occ_fn)(const gattn::FusedArgs &, const CUtensorMap &, const CUtensorMap &,
-                                int, cudaStream_t) = nullptr;
-    int fused_occ_smem = -1, fused_occ = 0;
-    int GR = 0, ngrp = 0;                  // q|k|v epilogue group rows, groups
-    float *part_a = nullptr, *part_o = nullptr;
-    unsigned *sync = nullptr;
     float *ss_part = nullptr;              // decoder-block post-norm: per-CTA sums of squares
     unsigned *post_ticket = nullptr;
     // Bf16KTurbo4V caches: decision tables (passed by value) and the bytes of
     // the 8 positive fp16 levels the attention dequantizes with
     TurboTables tq{};
     uint32_t tq_tl[2] = {0, 0}, tq_th[2] = {0, 0};
-    int s_cnt_a = 0, s_rdy_a = 0, s_seg = 0, s_cnt_o = 0, nsync = 0;
     gattn_taps taps{};
     gattn_mask mask{};                     // attention mask of the following steps (mask.mask null: causal)
     bool weights_set = false;
@@ -426,31 +414,6 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
         TRY(cudaMemset(L->post_ticket, 0, sizeof(unsigned)));
     }
 
-    // the one-kernel path: whole heads per epilogue group (GR = lcm(d, 128)
-    // rows tiling the k and v rows), every CTA resident (cooperative launch)
-    {
-        const int d = c.head_dim;
-        L->GR = d * kRBR / std::gcd(d, kRBR);
-        int coop = 0, optin = 0;
-        TRY(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, L->device));
-        TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->device));
-        L->fused_smem_max = optin;
-        L->fused_ok = coop && (d == 64 || d == 128 || d == 256) && L->Nkv % L->GR == 0 &&
-                      L->num_sms + 1 <= kFMaxContrib;
-        if (L->fused_ok) {
-            L->ngrp = (L->Nq + 2 * L->Nkv) / L->GR;
-            const int nrb_a = (L->Nq + 2 * L->Nkv) / kRBR, nrb_o = c.hidden / kRBR;
-            L->s_cnt_a = 2;
-            L->s_rdy_a = L->s_cnt_a + L->ngrp;
-            L->s_seg = L->s_rdy_a + L->ngrp;
-            L->s_cnt_o = L->s_seg + L->max_seg;
-            L->nsync = L->s_cnt_o + nrb_o;
-            TRY(cudaMalloc(&L->part_a, (size_t)(L->num_sms + nrb_a) * 1024 * sizeof(float)));
-            TRY(cudaMalloc(&L->part_o, (size_t)nku_o * nrb_o * 1024 * sizeof(float)));
-            TRY(cudaMalloc(&L->sync, (size_t)L->nsync * sizeof(unsigned)));
-            TRY(cudaMemset(L->sync, 0, (size_t)L->nsync * sizeof(unsigned)));
-        }
-    }
     std::vector<double> inv(L->rd / 2);
     for (int i = 0; i < L->rd / 2; ++i)
         inv[i] = std::pow((double)c.rope_theta, -2.0 * (double)i / (double)L->rd);
@@ -479,7 +442,7 @@ void gattn_layer_destroy(gattn_layer *L)
         return;
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq, L->inv_freq2,
-                    L->q_norm, L->k_norm, L->part_a,  L->part_o,  L->sync,
+                    L->q_norm, L->k_norm,
                     L->ss_part, L->post_ticket};
     for (void *p : ptrs)
         if (p)
@@ -724,15 +687,6 @@ int32_t gattn_layer_step_kernels(const gattn_layer *L, int32_t *kinds, int32_t c
     return L->launches;
 }
 
-gattn_status gattn_layer_set_path(gattn_layer *L, int32_t path)
-{
-    if (!L)
-        return fail(GATTN_E_INVALID_ARG, "layer is NULL");
-    if (path != GATTN_PATH_AUTO && path != GATTN_PATH_FUSED && path != GATTN_PATH_SPLIT)
-        return fail(GATTN_E_INVALID_ARG, "unknown path %d", (int)path);
-    L->path = path;
-    return GATTN_OK;
-}
 
 gattn_status gattn_layer_set_events(gattn_layer *L, void *const *events, int32_t n)
 {
@@ -812,122 +766,12 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     const int MT = (max_rows + 15) / 16;
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
 
-    // ---- one kernel for the whole step when the operand is one column tile
-    // the default stays on the five-kernel path until the one-kernel path is faster;
-    // the one-kernel path runs the layer alone (no decoder-block steps)
-    if (L->path == GATTN_PATH_FUSED && blk)
-        return fail(GATTN_E_UNSUPPORTED, "the one-kernel path runs no decoder-block steps");
-    if (L->path == GATTN_PATH_FUSED && kv->turbo)
-        return fail(GATTN_E_UNSUPPORTED, "the one-kernel path reads bf16 V caches only");
-    if (L->path == GATTN_PATH_FUSED && L->mask.mask)
-        return fail(GATTN_E_UNSUPPORTED, "the one-kernel path runs causal steps only");
     // the head-chunked verify route hands the mask unchanged to each head chunk:
     // a broadcast mask fits every chunk, a mask over all heads does not
     if (L->mask.mask && L->mask.heads > 1 && nchunks > c.num_kv_heads)
         return fail(GATTN_E_UNSUPPORTED,
                     "a head-specific mask cannot take the head-chunked verify route "
                     "(q_len %d, %d query heads per KV head)", (int)q_len, (int)L->gqa);
-    if (L->path == GATTN_PATH_FUSED) {
-        // x arrives by bulk copy: 16-byte alignment
-        bool ok = L->fused_ok && Ma <= 8 && batch <= kFMaxB && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-        FusedArgs f{};
-        if (ok) {
-            f.wa = L->pqkv.w;
-            f.wo = L->po.w;
-            f.bits_a = L->pqkv.bits;
-            f.group_a = L->pqkv.group;
-            f.ubytes_a = L->pqkv.ubytes;
-            f.step_a = L->pqkv.step_bytes;
-            f.nrb_a = (L->Nq + 2 * L->Nkv) / kRBR;
-            f.nku_a = L->pqkv.nku;
-            f.Na = L->Nq + 2 * L->Nkv;
-            f.bits_o = L->po.bits;
-            f.group_o = L->po.group;
-            f.ubytes_o = L->po.ubytes;
-            f.step_o = L->po.step_bytes;
-            f.nrb_o = c.hidden / kRBR;
-            f.nku_o = L->po.nku;
-            f.No = c.hidden;
-            f.x = x;
-            f.x_f32 = c.x_dtype == GATTN_DTYPE_F32;
-            f.M = M;
-            f.Mx = Ma;
-            f.B = batch;
-            f.R = q_len;
-            f.cache_pos = cache_pos;
-            f.H = c.num_heads;
-            f.Hk = c.num_kv_heads;
-            f.d = c.head_dim;
-            f.rd = L->rd;
-            f.gqa = L->gqa;
-            f.Nq = L->Nq;
-            f.Nkv = L->Nkv;
-            f.GR = L->GR;
-            f.ngrp = L->ngrp;
-            f.eps = c.rms_eps;
-            f.scale_log2 = scale_log2;
-            f.q_norm = L->q_norm;
-            f.k_norm = L->k_norm;
-            f.inv_freq = L->inv_freq;
-            f.kc = static_cast<__nv_bfloat16 *>(kv->desc.k);
-            f.vc = static_cast<__nv_bfloat16 *>(kv->desc.v);
-            f.st_tok = kv->desc.stride_token;
-            f.st_head = kv->desc.stride_head;
-            f.st_batch = kv->desc.stride_batch;
-            f.cap = kv->desc.capacity;
-            f.nrb = nrb;
-            f.MT = MT;
-            f.min_units = kAttnMinUnits;
-            for (int i = 0; i < nrb; ++i) {
-                f.rb_h0[i] = t.rb_h0[i];
-                f.rb_nh[i] = t.rb_nh[i];
-            }
-            f.part_a = L->part_a;
-            f.part_o = L->part_o;
-            f.qn = L->qn;
-            f.gate = L->gate;
-            f.ws = L->ws_attn;
-            f.sync = L->sync;
-            f.s_cnt_a = L->s_cnt_a;
-            f.s_rdy_a = L->s_rdy_a;
-            f.s_seg = L->s_seg;
-            f.s_cnt_o = L->s_cnt_o;
-            f.nsync = L->nsync;
-            f.out = static_cast<__nv_bfloat16 *>(out);
-            f.tap_y = L->taps.y;
-            f.tap_attn = L->taps.attn;
-            f.status = L->status;
-            ok = fused_plan(f, L->num_sms, L->fused_smem_max);
-        }
-        FusedOps ops{};
-        if (ok)
-            ok = fused_ops(FusedKey{f.bits_a, f.group_a, f.bits_o, f.group_o, f.MT, c.head_dim / 64},
-                           &ops);
-        if (ok && (ops.launch != L->fused_occ_fn || f.smem_bytes != L->fused_occ_smem)) {
-            // once per instance and size: raise its shared-memory limit, check residency
-            int occ = 0;
-            CUDA_TRY(ops.set_smem(L->fused_smem_max));
-            CUDA_TRY(ops.occupancy(f.smem_bytes, &occ));
-            L->fused_occ_fn = ops.launch;
-            L->fused_occ_smem = f.smem_bytes;
-            L->fused_occ = occ;
-        }
-        ok = ok && L->fused_occ >= 1;
-        if (ok) {
-            CUDA_TRY(mark(0));
-            CUDA_TRY(ops.launch(f, kv->kmap, kv->vmap, L->num_sms, s));
-            CUDA_TRY(mark_end());
-            L->launches = 1;
-            std::memset(L->kinds, 0, sizeof L->kinds);
-            L->kinds[0] = GATTN_KERNEL_FUSED;
-            return GATTN_OK;
-        }
-        if (L->path == GATTN_PATH_FUSED)
-            return fail(GATTN_E_UNSUPPORTED,
-                        "this step cannot run as one kernel (needs batch*q_len <= 8, or <= 4 "
-                        "for fp32 x, head_dim 64/128/256, whole heads per 128-row block, a "
-                        "16-byte aligned x and a compiled instance for its bit widths)");
-    }
 
     int32_t kinds[8] = {0};
     auto launched = [&](int32_t kind) { kinds[launches++] = kind; };

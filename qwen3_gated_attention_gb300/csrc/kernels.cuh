@@ -316,73 +316,6 @@ cudaError_t launch_attn_merge(const AttnArgs &a, int max_rows, bool pdl, cudaStr
 int attn_smem_bytes(int MT, int DB);
 cudaError_t attn_set_smem_limits();
 
-// ------------------------------------------------- one-kernel layer step
-//
-// For steps whose operand has at most 8 columns (batch * q_len <= 8, <= 4 for
-// fp32 x) the whole step runs as one persistent kernel, one CTA per SM,
-// launched cooperatively (every CTA resident, so CTAs may wait on flags that
-// other CTAs set).  See fused.cu.
-
-constexpr int kFW = 8;                        // consumer warps
-constexpr int kFThreads = (kFW + 1) * 32;     // + one producer warp
-constexpr int kFEntries = 32;                 // ring entries in flight
-constexpr int kFMaxB = 8;                     // sequences per step
-constexpr int kFMaxContrib = 160;             // attention contributors per segment (>= SMs + 1)
-
-struct FusedArgs {
-    // projections in the device tile layout
-    const uint8_t *wa, *wo;
-    int bits_a, group_a, ubytes_a, step_a, nrb_a, nku_a, Na;
-    int bits_o, group_o, ubytes_o, step_o, nrb_o, nku_o, No;
-    // step inputs
-    const void *x;
-    int x_f32, M, Mx, B, R;          // Mx: operand columns (2M for fp32 x: hi and lo planes)
-    const int *cache_pos;
-    // layer
-    int H, Hk, d, rd, gqa, Nq, Nkv;
-    int GR, ngrp;                    // q|k|v rows per epilogue group (lcm(d, 128)), groups
-    float eps, scale_log2;
-    const uint16_t *q_norm, *k_norm;
-    const double *inv_freq;
-    // caller's bf16 cache (element strides)
-    __nv_bfloat16 *kc, *vc;
-    long long st_tok, st_head, st_batch;
-    int cap;
-    // attention segments: per KV head nrb row blocks of whole query heads
-    int nrb, MT, min_units;
-    int rb_h0[kMaxRowBlocks], rb_nh[kMaxRowBlocks];
-    // library scratch
-    float *part_a;                   // q|k|v split-K partials, [slot][8 columns][128 rows]
-    float *part_o;                   // o_proj partial of every (k unit, row block) item
-    __nv_bfloat16 *qn;               // [M][H][d]
-    float *gate;                     // [M][H*d]
-    float *ws;                       // attention partial slots
-    unsigned *sync;                  // counters and flags, all zero between steps
-    int s_cnt_a, s_rdy_a, s_seg, s_cnt_o, nsync;
-    __nv_bfloat16 *out;              // [M][No]
-    float *tap_y, *tap_attn;
-    unsigned *status;
-    // shared memory plan: byte offsets from the 1024-aligned base
-    int ring_bytes, xslots, xslot_bytes, off_x, off_u, off_red, off_misc, smem_bytes;
-};
-
-// Sizes the shared-memory plan of `a` (ring, x slots, scratch) for the given
-// attention tile rows; false when the step does not fit one CTA per SM.
-bool fused_plan(FusedArgs &a, int num_sms, int max_smem);
-
-// The compiled instances of the one-kernel step, by configuration.
-struct FusedKey {
-    int bits_a, group_a, bits_o, group_o, MT, DB;
-};
-struct FusedOps {
-    cudaError_t (*launch)(const FusedArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          int grid, cudaStream_t s);   // cooperative launch
-    cudaError_t (*set_smem)(int bytes);
-    cudaError_t (*occupancy)(int smem, int *blocks_per_sm);
-};
-// false when no instance was compiled for this configuration
-bool fused_ops(const FusedKey &k, FusedOps *ops);
-
 }  // namespace gattn
 
 // records the thread-local message returned by gattn_last_error()

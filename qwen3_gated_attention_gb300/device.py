@@ -34,7 +34,7 @@ class DeviceLayer:
 
     def __init__(self, spec, packed, q_norm, k_norm, capacity, *, batch=None, max_batch=None,
                  max_q_len=None, head_chunk=True, layout="bhtd", device="cuda:0",
-                 path=gattn.PATH_AUTO, kv_format="bf16"):
+                 kv_format="bf16"):
         self.spec = spec
         self.device = torch.device(device)
         self.batch = batch or spec.batch
@@ -49,7 +49,6 @@ class DeviceLayer:
         self.h = gattn.layer_create(self.cfg)
         self.kv = 0
         try:
-            gattn.layer_set_path(self.h, path)
             self._w = [(_dev_u32(p, self.device), _dev_u16(s, self.device), _dev_u16(b, self.device))
                        for p, s, b in packed]
             self._qn = _dev_u16(q_norm, self.device)

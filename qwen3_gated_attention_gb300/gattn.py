@@ -22,10 +22,8 @@ STATUS_NAMES = {0: "GATTN_OK", 1: "GATTN_E_INVALID_ARG", 2: "GATTN_E_UNSUPPORTED
                 6: "GATTN_E_DEVICE_TIMEOUT"}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 PROJ_Q, PROJ_K, PROJ_V, PROJ_O = 0, 1, 2, 3
-PATH_AUTO, PATH_FUSED, PATH_SPLIT = 0, 1, 2
 # kernels of a step (gattn_layer_step_kernels)
-KERNEL_NAMES = {1: "xprep", 2: "proj_qkv", 3: "attn", 4: "merge", 5: "proj_o", 6: "postnorm",
-                7: "layer_step"}
+KERNEL_NAMES = {1: "xprep", 2: "proj_qkv", 3: "attn", 4: "merge", 5: "proj_o", 6: "postnorm"}
 
 # every symbol include/gattn.h declares
 EXPORTS = (
@@ -34,7 +32,7 @@ EXPORTS = (
     "gattn_layer_destroy", "gattn_kv_destroy", "gattn_last_error", "gattn_pack_affine_host",
     "gattn_unpack_codes_device", "gattn_layer_dequant_device", "gattn_head_chunk_plan",
     "gattn_layer_launches_per_step", "gattn_layer_set_events", "gattn_layer_dequant_device_static",
-    "gattn_layer_set_path", "gattn_layer_step_block", "gattn_kv_register_turbo4v",
+    "gattn_layer_step_block", "gattn_kv_register_turbo4v",
     "gattn_turbo4_codebook", "gattn_turbo4_quantize_device", "gattn_layer_set_mask",
     "gattn_kv_register_turbo4", "gattn_layer_step_kernels",
 )
@@ -131,7 +129,6 @@ def lib():
         L.gattn_layer_step_kernels.argtypes = [p, p, i32]
         L.gattn_layer_step_kernels.restype = i32
         L.gattn_layer_set_events.argtypes = [p, p, i32]
-        L.gattn_layer_set_path.argtypes = [p, i32]
         L.gattn_layer_step_block.argtypes = [p, p, p, p, i32, i32, p, p, p, p, p]
         L.gattn_kv_register_turbo4v.argtypes = [p, C.POINTER(gattn_kv_turbo4v_desc), C.POINTER(p)]
         L.gattn_turbo4_codebook.argtypes = [p, p]
@@ -142,7 +139,7 @@ def lib():
                      "gattn_kv_register", "gattn_layer_step", "gattn_layer_poll_status",
                      "gattn_layer_set_taps", "gattn_pack_affine_host", "gattn_unpack_codes_device",
                      "gattn_layer_dequant_device", "gattn_layer_set_events",
-                     "gattn_layer_dequant_device_static", "gattn_layer_set_path",
+                     "gattn_layer_dequant_device_static",
                      "gattn_layer_step_block", "gattn_kv_register_turbo4v",
                      "gattn_turbo4_codebook", "gattn_turbo4_quantize_device",
                      "gattn_layer_set_mask", "gattn_kv_register_turbo4"):
@@ -307,11 +304,6 @@ def layer_step_block(layer: int, x: int, kv: int, cache_pos: int, batch: int, q_
     RMSNorm(out) * post_ln when given (device pointers)."""
     _check(lib().gattn_layer_step_block(layer, x, kv, cache_pos, batch, q_len, input_ln, post_ln,
                                         out, out_normed, stream))
-
-
-def layer_set_path(layer: int, path: int) -> None:
-    """Which kernels run the layer's steps: PATH_AUTO, PATH_FUSED or PATH_SPLIT."""
-    _check(lib().gattn_layer_set_path(layer, path))
 
 
 def layer_set_events(layer: int, events) -> None:

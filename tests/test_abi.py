@@ -173,7 +173,6 @@ def test_documented_errors_that_need_no_gpu():
     status(L.gattn_layer_poll_status(null, null), 1)
     status(L.gattn_layer_set_taps(null, null), 1)
     status(L.gattn_layer_set_mask(null, null), 1)
-    status(L.gattn_layer_set_path(null, 0), 1)
     status(L.gattn_layer_set_events(null, null, 0), 1)
     status(L.gattn_layer_step_block(null, null, null, null, 1, 1, null, null, null, null, null), 1)
     status(L.gattn_layer_dequant_device(null, 0, null, null), 1)

@@ -36,9 +36,9 @@ def _u16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
 
 
-def _run(case, x, il, pl, with_post=True, path=gattn.PATH_AUTO):
+def _run(case, x, il, pl, with_post=True):
     spec = case.spec
-    dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap, path=path)
+    dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap)
     try:
         dl.load_cache(case.ck, case.cv)
         out = torch.full((spec.batch, spec.q_len, spec.hidden), float("nan"), dtype=torch.bfloat16,
@@ -133,12 +133,3 @@ def test_block_without_post_norm_matches_block_with_it():
     b = _run(case, case.x, il, pl, with_post=False)
     assert a["launches"] == 5 and b["launches"] == 5
     assert np.array_equal(a["out"], b["out"])
-
-
-def test_block_is_refused_on_the_one_kernel_path():
-    spec = SMALL["decode_4b"]
-    case = make_case(spec)
-    il, pl = synth.block_norm_weights_bf16(spec)
-    with pytest.raises(gattn.GattnError) as ei:
-        _run(case, case.x, il, pl, path=gattn.PATH_FUSED)
-    assert ei.value.status == 2

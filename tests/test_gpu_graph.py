@@ -1,6 +1,6 @@
 """Steps captured in a CUDA graph and replayed equal the same steps run eagerly,
 bit for bit: three consecutive steps (each reading the rows the previous ones
-appended) on both paths and over a Bf16KTurbo4V cache, and the decoder-block
+appended) over bf16 and Bf16KTurbo4V caches, and the decoder-block
 step.  The step makes no allocation, host synchronization or host-side
 decision from device data, so its capture replays the same work."""
 import numpy as np
@@ -26,9 +26,9 @@ def gpu():
     build.build()
 
 
-def _run(spec, case, turbo, path, block, graph):
+def _run(spec, case, turbo, block, graph):
     B, R, Hd = spec.batch, spec.q_len, spec.hidden
-    dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap, path=path,
+    dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap,
                      kv_format="turbo4v" if turbo is not None else "bf16")
     try:
         dl.load_cache(case.ck, turbo if turbo is not None else case.cv)
@@ -75,20 +75,20 @@ def _run(spec, case, turbo, path, block, graph):
         dl.close()
 
 
-CASES = [("batched_mixed_small", gattn.PATH_AUTO, False, False),
-         ("verify_2k_p46", gattn.PATH_FUSED, False, False),
-         ("verify_2k_p46", gattn.PATH_AUTO, True, False),
-         ("decode_4b", gattn.PATH_AUTO, False, True)]
+CASES = [("batched_mixed_small", False, False),
+         ("verify_2k_p46", False, False),
+         ("verify_2k_p46", True, False),
+         ("decode_4b", False, True)]
 
 
-@pytest.mark.parametrize("name,path,turbo,block", CASES,
+@pytest.mark.parametrize("name,turbo,block", CASES,
                          ids=["-".join(map(str, c)) for c in CASES])
-def test_graph_replay_equals_eager_steps(name, path, turbo, block):
+def test_graph_replay_equals_eager_steps(name, turbo, block):
     spec = SMALL[name]
     case = make_case(spec, capacity=spec.capacity() + 64)
     tv = synth.turbo4v_cache(spec, case.cap) if turbo else None
-    eager, ec = _run(spec, case, tv, path, block, graph=False)
-    replay, gc = _run(spec, case, tv, path, block, graph=True)
+    eager, ec = _run(spec, case, tv, block, graph=False)
+    replay, gc = _run(spec, case, tv, block, graph=True)
     for i, (a, b) in enumerate(zip(eager, replay)):
         assert np.array_equal(a, b), f"output {i}"
     ek, ev = ec

@@ -88,11 +88,10 @@ def _register(h, spec, cap, kv_format, bufs):
     return gattn.kv_register_turbo4(h, p["kc"], p["ks"], p["vc"], p["vs"], B, cap, cst, sst)
 
 
-def _exact_run(case, host, kv_format, path, block):
+def _exact_run(case, host, kv_format, block):
     """The same step on a DeviceLayer's exactly sized buffers."""
     spec = case.spec
-    dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap, path=path,
-                     kv_format=kv_format)
+    dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap, kv_format=kv_format)
     try:
         if kv_format == "bf16":
             dl.load_cache(host["k"], host["v"])
@@ -159,19 +158,19 @@ class _Plain:
             self.view = torch.full((n,), S8, dtype=torch.uint8, device="cuda").view(shape)
 
 
-GUARD_CASES = [("batched_mixed_small", "bf16", gattn.PATH_AUTO, False),
-               ("verify_2k_p46", "bf16", gattn.PATH_FUSED, False),
-               ("verify_2k_p46", "turbo4v", gattn.PATH_AUTO, False),
-               ("batched_mixed_small", "turbo4", gattn.PATH_AUTO, False),
-               ("decode_4b", "bf16", gattn.PATH_AUTO, True)]
+GUARD_CASES = [("batched_mixed_small", "bf16", False),
+               ("verify_2k_p46", "bf16", False),
+               ("verify_2k_p46", "turbo4v", False),
+               ("batched_mixed_small", "turbo4", False),
+               ("decode_4b", "bf16", True)]
 
 
-@pytest.mark.parametrize("name,kv_format,path,block", GUARD_CASES,
+@pytest.mark.parametrize("name,kv_format,block", GUARD_CASES,
                          ids=["-".join(map(str, c)) for c in GUARD_CASES])
-def test_writes_stay_inside_their_buffers(name, kv_format, path, block):
+def test_writes_stay_inside_their_buffers(name, kv_format, block):
     spec = SMALL[name]
     case, host = _planes(spec, SMALL[name].capacity(), kv_format)
-    want, want_cache = _exact_run(case, host, kv_format, path, block)
+    want, want_cache = _exact_run(case, host, kv_format, block)
     Hk, d, B, cap = spec.num_kv_heads, spec.head_dim, spec.batch, case.cap
     bufs = {}
     for k, a in host.items():
@@ -186,7 +185,6 @@ def test_writes_stay_inside_their_buffers(name, kv_format, path, block):
     kv = 0
     try:
         dl_w = _weights(h, case)
-        gattn.layer_set_path(h, path)
         kv = _register(h, spec, cap, kv_format, bufs)
         got = _step(h, kv, case, block, guarded=True)
     finally:
@@ -223,9 +221,8 @@ def _weights(h, case):
     return w, qn, kn
 
 
-@pytest.mark.parametrize("kv_format,path", [("bf16", gattn.PATH_AUTO), ("bf16", gattn.PATH_FUSED),
-                                            ("turbo4v", gattn.PATH_AUTO)])
-def test_a_fresh_handle_resumes_from_the_cache(kv_format, path):
+@pytest.mark.parametrize("kv_format", ["bf16", "turbo4v"])
+def test_a_fresh_handle_resumes_from_the_cache(kv_format):
     """Two verify steps on one handle; the second again on a new handle over
     the cache the first step left: same output, same cache, bit for bit."""
     spec = SMALL["verify_2k_p46"]
@@ -235,8 +232,7 @@ def test_a_fresh_handle_resumes_from_the_cache(kv_format, path):
     step2 = types.SimpleNamespace(spec=spec, x=x2, pos=case.pos + R)
 
     def fresh():
-        dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap, path=path,
-                         kv_format=kv_format)
+        dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap, kv_format=kv_format)
         return dl
 
     def load(dl, cache):

@@ -29,16 +29,13 @@ def gpu():
     torch.cuda.init()
 
 
-PATHS = {"fused": gattn.PATH_FUSED, "split": gattn.PATH_SPLIT}
-
-
 def gpu_run(case, head_chunk=True, layout="bhtd", taps=True, pos=None, x=None, q_len=None,
-            batch=None, dl=None, keep=False, path=gattn.PATH_AUTO):
+            batch=None, dl=None, keep=False):
     spec = case.spec
     own = dl is None
     if own:
         dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap,
-                         head_chunk=head_chunk, layout=layout, path=path)
+                         head_chunk=head_chunk, layout=layout)
         dl.load_cache(case.ck, case.cv)
     B = batch or spec.batch
     R = q_len or spec.q_len
@@ -52,14 +49,7 @@ def gpu_run(case, head_chunk=True, layout="bhtd", taps=True, pos=None, x=None, q
     out = torch.full((B, R, Hd), float("nan"), dtype=torch.bfloat16, device="cuda")
     xd = x_to_device(spec, xx)
     pd = torch.from_numpy(np.ascontiguousarray(pp, np.int32)).cuda()
-    try:
-        dl.step(xd, pd, out, batch=B, q_len=R)
-    except gattn.GattnError as e:
-        if own:
-            dl.close()
-        if e.status == 2 and path == gattn.PATH_FUSED:
-            pytest.skip(f"the one-kernel path does not take this step: {e}")
-        raise
+    dl.step(xd, pd, out, batch=B, q_len=R)
     dl.poll()
     k, v = dl.read_cache()
     res = dict(out=out.float().cpu().numpy().astype(np.float64), k=k, v=v,
@@ -166,44 +156,17 @@ def test_admitted_head_layouts_parity(name):
         print(name, chunk, rep)
 
 
-@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("name", list(SMALL))
-def test_layer_parity(name, path):
+def test_layer_parity(name):
     case = make_case(SMALL[name])
-    got = gpu_run(case, path=PATHS[path])
-    if path == "fused":
-        assert got["launches"] == 1 and got["kernels"] == ["layer_step"]
-    else:
-        # the q|k|v kernel converts x itself when its tables fit, else x prep runs first
-        assert got["kernels"][-4:] == ["proj_qkv", "attn", "merge", "proj_o"]
-        assert got["launches"] == len(got["kernels"]) and got["launches"] in (4, 5)
+    got = gpu_run(case)
+    # the q|k|v kernel converts x itself when its tables fit, else x prep runs first
+    assert got["kernels"][-3:] == ["proj_qkv", "attn", "proj_o"] or \
+        got["kernels"][-4:] == ["proj_qkv", "attn", "merge", "proj_o"]
+    assert got["launches"] == len(got["kernels"])
     ref = oracle_run(case)
-    rep = check_parity(case, got, ref, what=f"{name} {path}")
-    print(name, path, rep)
-
-
-@pytest.mark.parametrize("name", ["tiny", "decode_4b", "verify_2k_p2048", "batched_mixed_small",
-                                  "batch8_decode"])
-def test_one_kernel_and_five_kernel_paths_agree(name):
-    """Same layer, two schedules: the projections' split-K sums are added in
-    different orders, so results agree to fp32 rounding (cache rows to one
-    bf16 ulp, outputs to bf16 level); every untouched cache byte is equal."""
-    case = make_case(SMALL[name])
-    f = gpu_run(case, path=gattn.PATH_FUSED)
-    s = gpu_run(case, path=gattn.PATH_SPLIT)
-    assert f["launches"] == 1 and s["launches"] in (4, 5)
-    R = case.spec.q_len
-    for key in ("k", "v"):
-        for b in range(case.spec.batch):
-            p = int(case.pos[b])
-            assert_rows_close(f[key][b, :, p:p + R], s[key][b, :, p:p + R], f"{name} {key}")
-            mask = np.ones(f[key].shape[1:3], bool)
-            mask[:, p:p + R] = False
-            assert np.array_equal(f[key][b][mask], s[key][b][mask])
-    ok, rep = refs.close(f["out"], s["out"], abs_tol=2e-3, rel_tol=1e-2, l2_tol=2e-3)
-    assert ok, rep
-    ok, rep = refs.close(f["attn"], s["attn"], abs_tol=2e-3, rel_tol=1e-2, l2_tol=2e-3)
-    assert ok, rep
+    rep = check_parity(case, got, ref, what=name)
+    print(name, rep)
 
 
 # Wider verify / short prefill rows: q_len 8, 16 and 32 on the verify layer
@@ -264,23 +227,21 @@ def test_stale_nan_cache_slots_do_not_leak():
     assert np.array_equal(a["attn"], b["attn"])
 
 
-@pytest.mark.parametrize("path", list(PATHS))
-def test_verify_step_equals_row_by_row_steps(path):
+def test_verify_step_equals_row_by_row_steps():
     """Four one-row steps on one layer (each reads the rows the previous ones
-    appended) equal one four-row step; on the one-kernel path this also checks
-    that every step leaves its counters and flags cleared for the next."""
+    appended) equal one four-row step, and every step leaves the layer's
+    counters ready for the next."""
     spec = SMALL["verify_2k_p46"]
     case = make_case(spec)
-    full = gpu_run(case, path=PATHS[path])
+    full = gpu_run(case)
     s1 = spec.with_(q_len=1)
-    dl = DeviceLayer(s1, case.lib_packed, case.qn, case.kn, case.cap, max_q_len=1,
-                     path=PATHS[path])
+    dl = DeviceLayer(s1, case.lib_packed, case.qn, case.kn, case.cap, max_q_len=1)
     dl.load_cache(case.ck, case.cv)
     case1 = make_case(s1, capacity=case.cap)
     rows = []
     for r in range(spec.q_len):
         res = gpu_run(case1, x=np.ascontiguousarray(case.x[:, r:r + 1]), pos=case.pos + r, dl=dl,
-                      q_len=1, path=PATHS[path])
+                      q_len=1)
         rows.append(res)
     dl.close()
     assert np.array_equal(rows[-1]["k"], full["k"]) and np.array_equal(rows[-1]["v"], full["v"])

@@ -22,9 +22,8 @@ def gpu():
     build.build()
 
 
-def _run(spec, case, mask, head_chunk=True, path=gattn.PATH_AUTO):
-    dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap, head_chunk=head_chunk,
-                     path=path)
+def _run(spec, case, mask, head_chunk=True):
+    dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap, head_chunk=head_chunk)
     try:
         dl.load_cache(case.ck, case.cv)
         M, H, d = spec.batch * spec.q_len, spec.num_heads, spec.head_dim
@@ -143,13 +142,6 @@ def test_fully_masked_rows_are_zero():
     out, ta, kc, vc = _oracle(spec, case, mask)
     _check("tiny_r8", spec, case, got, out, ta, kc)
 
-
-def test_mask_is_refused_on_the_one_kernel_path():
-    spec = CASES["decode_4b"]
-    case = make_case(spec)
-    with pytest.raises(gattn.GattnError) as ei:
-        _run(spec, case, _mask(spec, 1, 14), path=gattn.PATH_FUSED)
-    assert ei.value.status == 2
 
 
 @pytest.mark.parametrize("name", ["batched_mixed_small", "tiny_r8"])

@@ -67,9 +67,9 @@ def _near_bf16_midpoint(v, rel=4e-6):
     return (np.abs(t - np.floor(t) - 0.5) < rel * t) & (a > 0)
 
 
-def _run_turbo(spec, case, codes, scales, path=gattn.PATH_AUTO, head_chunk=True):
+def _run_turbo(spec, case, codes, scales, head_chunk=True):
     dl = DeviceLayer(spec, case.lib_packed, case.qn, case.kn, case.cap, kv_format="turbo4v",
-                     path=path, head_chunk=head_chunk)
+                     head_chunk=head_chunk)
     try:
         dl.load_cache(case.ck, (codes, scales))
         M, H, d = spec.batch * spec.q_len, spec.num_heads, spec.head_dim
@@ -145,14 +145,6 @@ def test_turbo_head_chunk_on_and_off_agree_bitwise():
     assert np.array_equal(a["out"], b["out"])
     assert np.array_equal(a["codes"], b["codes"]) and np.array_equal(a["scales"], b["scales"])
 
-
-def test_turbo_is_refused_on_the_one_kernel_path():
-    spec = CASES["decode_4b"]
-    case = make_case(spec)
-    codes, scales = synth.turbo4v_cache(spec, case.cap)
-    with pytest.raises(gattn.GattnError) as ei:
-        _run_turbo(spec, case, codes, scales, path=gattn.PATH_FUSED)
-    assert ei.value.status == 2
 
 
 # ------------------------------------------------- symmetric Turbo4 cache
