@@ -72,8 +72,7 @@ def algorithmic_bytes(spec, block=False, kv="bf16", x_folded=False):
     per_kernel = {
         "xprep": xb + x16,
         "proj_qkv": wq + wk + wv + x16 + qn + gate + kv_write,
-        "attn": kv_read + qn,
-        "merge": gate + o16,
+        "attn": kv_read + qn + gate + o16,          # with its merge and the output gate
         "proj_o": wo + o16 + outb,
     }
     if x_folded:

@@ -432,17 +432,17 @@ gattn_status gattn_layer_step_block(gattn_layer *layer, const void *x, gattn_kv 
                                     void *out_normed, gattn_stream stream);
 
 /* Per-step launch report of the layer's last step: number of kernel launches
- * it enqueued, all of them this library's own kernels: 4 when the q|k|v kernel
- * converts x itself, else 5 with the x prep launch, one more for a
- * decoder-block step whose post-norm takes its own launch. */
+ * it enqueued, all of them this library's own kernels: 3 (q|k|v projection,
+ * attention with its merge, o_proj) when the q|k|v kernel converts x itself,
+ * else 4 with the x prep launch, one more for a decoder-block step whose
+ * post-norm takes its own launch. */
 int32_t gattn_layer_launches_per_step(const gattn_layer *layer);
 
 /* The kernels of the layer's last step, in launch order. */
 enum {
     GATTN_KERNEL_XPREP = 1,     /* x -> tensor-core operand (+ input RMSNorm of the block) */
     GATTN_KERNEL_PROJ_QKV = 2,  /* q|k|v dequant projection + norm / rotary / KV append */
-    GATTN_KERNEL_ATTN = 3,      /* causal GQA attention partials */
-    GATTN_KERNEL_MERGE = 4,     /* attention merge + output gate -> o_proj operand */
+    GATTN_KERNEL_ATTN = 3,      /* causal GQA attention, merge and output gate -> o_proj operand */
     GATTN_KERNEL_PROJ_O = 5,    /* o_proj (+ residual and fused post-norm of the block) */
     GATTN_KERNEL_POSTNORM = 6   /* post-attention RMSNorm of the block, own launch */
 };
@@ -458,6 +458,28 @@ int32_t gattn_layer_step_kernels(const gattn_layer *layer, int32_t *kinds, int32
  * Recording between kernels serializes them (no programmatic overlap), so use
  * it for per-kernel timing passes only. */
 gattn_status gattn_layer_set_events(gattn_layer *layer, void *const *events, int32_t n);
+
+/* Failure-detection test hook for the bounded device waits.
+ *
+ * Every wait of the projection kernels (a weight stage landing in shared
+ * memory, a stage slot being released, partial sums arriving from the other
+ * CTAs of a cluster) gives up after a time limit; the kernel then skips the
+ * remaining work of that CTA, still reaches every barrier, and returns; the
+ * layer's status word gets the timeout bit, so the next
+ * gattn_layer_poll_status() returns GATTN_E_DEVICE_TIMEOUT and the context
+ * stays usable.
+ *
+ * wait_limit_ns: the limit of those waits for the following steps, in ns;
+ *   0 restores the default (2 s).  Negative: GATTN_E_INVALID_ARG.
+ * withhold_stage: nonzero makes CTA 0 of every following q|k|v projection
+ *   launch skip the copy of its last weight stage, so that the wait for it
+ *   runs out after wait_limit_ns (the outputs of such a step are garbage);
+ *   0 turns that off.
+ *
+ * Meant for tests of the timeout path; a layer that never calls it keeps the
+ * default limit and withholds nothing. */
+gattn_status gattn_layer_set_test_wait(gattn_layer *layer, int64_t wait_limit_ns,
+                                       int32_t withhold_stage);
 
 #ifdef __cplusplus
 }

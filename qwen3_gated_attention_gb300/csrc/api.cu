@@ -127,7 +127,45 @@ struct ProjPlan {
 
 int nt_index(int NT) { return NT == 1 ? 0 : (NT == 2 ? 1 : 2); }
 
-constexpr int kAttnMinUnits = 4;     // 16-token units per attention CTA, at least
+// Attention row blocks of a KV group for q_len rows: the head chunks of the
+// verify plan (enabled or not), a chunk of more than 64 rows cut into blocks of
+// whole heads.  Writes up to kMaxRowBlocks (first head, heads) pairs when the
+// arrays are given; returns the block count (-1 past kMaxRowBlocks) and the
+// largest block's rows.
+int attn_row_blocks(int q_len, int H, int Hk, int enabled, int *rb_h0, int *rb_nh, int *max_rows)
+{
+    int32_t first[kMaxRowBlocks * 64], len[kMaxRowBlocks * 64];
+    const int nchunks = gattn_head_chunk_plan(q_len, H, Hk, enabled, first, len, kMaxRowBlocks * 64);
+    const int per_group = nchunks / Hk;
+    int nrb = 0, mr = 0;
+    for (int j = 0; j < per_group; ++j) {
+        const int hpb = std::max(1, 64 / q_len);
+        for (int h = 0; h < len[j]; h += hpb) {
+            if (nrb >= kMaxRowBlocks)
+                return -1;
+            if (rb_h0) {
+                rb_h0[nrb] = first[j] + h;
+                rb_nh[nrb] = std::min(hpb, len[j] - h);
+            }
+            mr = std::max(mr, std::min(hpb, len[j] - h) * q_len);
+            ++nrb;
+        }
+    }
+    if (max_rows)
+        *max_rows = mr;
+    return nrb;
+}
+
+// Upper bound of the attention items (segment chunks) of a step: the chunk
+// length is at least the unchunked partition's units over the grid, so the
+// items are at most grid * nrb / nrb_u plus one partial chunk per segment.
+long long attn_items_bound(int grid, int nrb, int nrb_u, int batch, int Hk)
+{
+    return ((long long)grid * nrb + nrb_u - 1) / nrb_u + (long long)batch * Hk * nrb;
+}
+
+constexpr int kAttnMinUnits = 4;     // 16-token units per attention chunk, at least
+constexpr int kMergeGroupHost = 8;   // chunks per level-1 merge group (attn.cuh kMergeGroup)
 // shared memory a q|k|v CTA may spend on converting x itself (the table of its
 // k units' fp16 fragments and group sums); a larger table keeps the x prep kernel
 constexpr int kXTabMax = 24 * 1024;
@@ -176,7 +214,10 @@ struct gattn_layer {
     float *xsum_a = nullptr, *xsum_o = nullptr;
     __nv_bfloat16 *qn = nullptr;
     float *gate = nullptr;
-    float *ws_attn = nullptr;
+    float *ws_attn = nullptr;              // attention chunk partials
+    float *ws_attn1 = nullptr;             // attention level-1 merge slots
+    unsigned *cnt_seg = nullptr, *cnt_grp = nullptr;   // attention completion counters
+    long long items_cap = 0, l1_cap = 0;
     unsigned *status = nullptr;
     double *inv_freq = nullptr;
     float2 *inv_freq2 = nullptr;           // the same frequencies as float (hi, lo) pairs
@@ -197,6 +238,8 @@ struct gattn_layer {
     int32_t kinds[8] = {0};                // GATTN_KERNEL_* of the last step's launches
     bool pdl = true;
     std::vector<cudaEvent_t> events;
+    unsigned long long wait_ns = kWaitLimitNs;   // bound of the projection kernels' waits
+    int withhold = 0;                             // failure test hook (see gattn_layer_set_test_wait)
 };
 
 struct gattn_kv {
@@ -388,9 +431,31 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaMalloc(&L->qn, (size_t)L->M_max * L->Ko * 2));
     TRY(cudaMalloc(&L->gate, (size_t)L->M_max * L->Ko * sizeof(float)));
     // attention segments: batch x KV heads x row blocks (at most gqa row blocks)
-    L->max_seg = c.max_batch * c.num_kv_heads * std::min(L->gqa, kMaxRowBlocks);
-    L->ws_attn_floats = (size_t)(L->max_seg + L->attn_grid + 1) * attn_slot_floats(c.head_dim);
+    // attention scratch: chunk partials, level-1 merge slots and counters for the
+    // largest step the configuration admits (every q_len, both head partitions)
+    {
+        int nrb_max = 1;
+        for (int R = 1; R <= c.max_q_len; ++R) {
+            const int nrb = attn_row_blocks(R, c.num_heads, c.num_kv_heads, c.head_chunk, nullptr,
+                                            nullptr, nullptr);
+            const int nrb_u = attn_row_blocks(R, c.num_heads, c.num_kv_heads, 0, nullptr, nullptr,
+                                              nullptr);
+            if (nrb < 0 || nrb_u < 0)
+                return cleanup(fail(GATTN_E_UNSUPPORTED, "too many attention row blocks"));
+            nrb_max = std::max(nrb_max, std::max(nrb, nrb_u));
+            L->items_cap = std::max(L->items_cap, attn_items_bound(L->attn_grid, nrb, nrb_u,
+                                                                   c.max_batch, c.num_kv_heads));
+        }
+        L->max_seg = c.max_batch * c.num_kv_heads * nrb_max;
+        L->l1_cap = L->items_cap / kMergeGroupHost + L->max_seg + 1;
+    }
+    L->ws_attn_floats = (size_t)L->items_cap * attn_slot_floats(c.head_dim);
     TRY(cudaMalloc(&L->ws_attn, L->ws_attn_floats * sizeof(float)));
+    TRY(cudaMalloc(&L->ws_attn1, (size_t)L->l1_cap * attn_slot_floats(c.head_dim) * sizeof(float)));
+    TRY(cudaMalloc(&L->cnt_seg, (size_t)L->max_seg * sizeof(unsigned)));
+    TRY(cudaMemset(L->cnt_seg, 0, (size_t)L->max_seg * sizeof(unsigned)));
+    TRY(cudaMalloc(&L->cnt_grp, (size_t)L->l1_cap * sizeof(unsigned)));
+    TRY(cudaMemset(L->cnt_grp, 0, (size_t)L->l1_cap * sizeof(unsigned)));
     TRY(cudaMalloc(&L->status, sizeof(unsigned)));
     TRY(cudaMemset(L->status, 0, sizeof(unsigned)));
     {
@@ -442,6 +507,7 @@ void gattn_layer_destroy(gattn_layer *L)
         return;
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq, L->inv_freq2,
+                    L->ws_attn1, L->cnt_seg, L->cnt_grp,
                     L->q_norm, L->k_norm,
                     L->ss_part, L->post_ticket};
     for (void *p : ptrs)
@@ -699,6 +765,16 @@ gattn_status gattn_layer_set_events(gattn_layer *L, void *const *events, int32_t
     return GATTN_OK;
 }
 
+gattn_status gattn_layer_set_test_wait(gattn_layer *L, int64_t wait_limit_ns,
+                                       int32_t withhold_stage)
+{
+    if (!L || wait_limit_ns < 0)
+        return fail(GATTN_E_INVALID_ARG, "bad wait limit arguments");
+    L->wait_ns = wait_limit_ns ? (unsigned long long)wait_limit_ns : kWaitLimitNs;
+    L->withhold = withhold_stage ? 1 : 0;
+    return GATTN_OK;
+}
+
 namespace {
 
 // The decoder block around the layer (gattn_layer_step_block); null: the layer alone.
@@ -745,24 +821,18 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     // attention segments: per KV group the head chunks of the verify plan, a
     // chunk of more than 64 rows cut into row blocks of whole heads
     AttnArgs t{};
-    int32_t first[kMaxRowBlocks * 64], len[kMaxRowBlocks * 64];
+    int max_rows = 0;
+    const int nrb = attn_row_blocks(q_len, c.num_heads, c.num_kv_heads, c.head_chunk, t.rb_h0,
+                                    t.rb_nh, &max_rows);
+    const int nrb_u = attn_row_blocks(q_len, c.num_heads, c.num_kv_heads, 0, nullptr, nullptr,
+                                      nullptr);
+    if (nrb < 0 || nrb_u < 0)
+        return fail(GATTN_E_UNSUPPORTED, "too many attention row blocks");
+    if ((long long)batch * c.num_kv_heads * nrb > L->max_seg ||
+        attn_items_bound(L->attn_grid, nrb, nrb_u, batch, c.num_kv_heads) > L->items_cap)
+        return fail(GATTN_E_UNSUPPORTED, "attention items exceed the scratch sized at create");
     const int nchunks = gattn_head_chunk_plan(q_len, c.num_heads, c.num_kv_heads, c.head_chunk,
-                                              first, len, kMaxRowBlocks * 64);
-    const int per_group = nchunks / c.num_kv_heads;
-    int nrb = 0, max_rows = 0;
-    for (int j = 0; j < per_group; ++j) {
-        const int hpb = std::max(1, 64 / q_len);
-        for (int h = 0; h < len[j]; h += hpb) {
-            if (nrb >= kMaxRowBlocks)
-                return fail(GATTN_E_UNSUPPORTED, "too many attention row blocks");
-            t.rb_h0[nrb] = first[j] + h;
-            t.rb_nh[nrb] = std::min(hpb, len[j] - h);
-            max_rows = std::max(max_rows, t.rb_nh[nrb] * q_len);
-            ++nrb;
-        }
-    }
-    if ((long long)batch * c.num_kv_heads * nrb > L->max_seg)
-        return fail(GATTN_E_UNSUPPORTED, "attention segments exceed the scratch sized at create");
+                                              nullptr, nullptr, 0);
     const int MT = (max_rows + 15) / 16;
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
 
@@ -810,6 +880,8 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     a.x_f32 = c.x_dtype == GATTN_DTYPE_F32;
     a.xsplit = c.x_dtype == GATTN_DTYPE_F32 ? M : 0;
     a.status = L->status;
+    a.wait_ns = L->wait_ns;
+    a.withhold = L->withhold;
     EpiQKV eq{};
     eq.R = q_len;
     eq.H = c.num_heads;
@@ -866,9 +938,12 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     t.cap = kv->desc.capacity;
     t.nrb = nrb;
     t.scale_log2 = scale_log2;
+    t.nrb_u = nrb_u;
     t.ws = L->ws_attn;
+    t.ws1 = L->ws_attn1;
+    t.cnt_seg = L->cnt_seg;
+    t.cnt_grp = L->cnt_grp;
     t.min_units = kAttnMinUnits;
-    t.grid = L->attn_grid;
     t.x16 = L->x16_o;
     t.xsum = L->xsum_o;
     t.NT = NT;
@@ -916,8 +991,6 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
         CUDA_TRY(launch_attn(MT, c.head_dim / 64, t, kv->kmap, kv->vmap, L->attn_grid, pdl, s));
     launched(GATTN_KERNEL_ATTN);
     CUDA_TRY(mark(launches));
-    CUDA_TRY(launch_attn_merge(t, max_rows, pdl, s));
-    launched(GATTN_KERNEL_MERGE);
 
     // 4. o_proj
     ProjArgs o = a;
@@ -937,6 +1010,7 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     o.eb_rows = kRBR;
     o.recv_cap = proj_recv_cap(kModeO, NT);
     o.xsplit = 0;
+    o.withhold = 0;
     EpiO e2{};
     e2.R = q_len;
     e2.cache_pos = cache_pos;

@@ -1,20 +1,23 @@
 // attn.cu -- causal GQA decode / verify attention over a bf16 KV cache (the
-// kernel template is in attn.cuh; attn_vq.cu holds the Bf16KTurbo4V instances).
+// kernel template is in attn.cuh; attn_vq.cu and attn_vqk.cu hold the Turbo4
+// instances).
 //
 // For every (sequence b, KV head kh, row block rb) segment the rows are the
 // R new rows of the row block's query heads (one KV group, or one chunk of it
 // when the verify head-chunk plan is on), and the keys are cache positions
-// [0, cache_pos[b] + R).  Segments are cut into 16-token units and all units
-// of all segments are split stream-K over the grid, so variable lengths
-// balance across SMs.  One producer warp streams 64-token K/V tiles with 4-D
-// TMA tensor copies (128-byte swizzle) into a ring of up to four stages; one
-// tile read serves every query row of the segment.  Eight consumer warps
-// compute S = q K^T and O += P V with bf16 mma.sync (fp32 accumulate) and an
-// online softmax in the log2 domain.
+// [0, cache_pos[b] + R).  Segments are cut into chunks of whole 16-token units,
+// of one length for all segments of the step (from the unchunked partition,
+// so both head partitions cut every segment alike), and the chunks are spread
+// over the grid in contiguous ranges.  One producer warp streams 64-token K/V
+// tiles with 4-D TMA tensor copies (128-byte swizzle) into a ring of up to four
+// stages; one tile read serves every query row of the segment.  Eight consumer
+// warps compute S = q K^T and O += P V with bf16 mma.sync (fp32 accumulate) and
+// an online softmax in the log2 domain.
 //
-// Each CTA writes a partial (m, l, O) per segment piece; attn_merge_kernel
-// (merge.cu) combines them, applies the output gate attn * sigmoid(gate) and
-// writes the o_proj operand in tensor-core fragment order (fp16).
+// Each chunk leaves a partial (m, l, O).  The CTA that finishes the last chunk
+// of a segment merges the segment (in two levels when it has many chunks),
+// applies the output gate attn * sigmoid(gate) and writes the o_proj operand in
+// tensor-core fragment order (fp16), so no separate merge launch is needed.
 #include "attn.cuh"
 
 namespace gattn {

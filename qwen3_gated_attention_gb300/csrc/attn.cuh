@@ -28,7 +28,7 @@ struct AttnSmem {
     static constexpr int kPBytes = MT * 16 * 128;             // rows x 64 tokens bf16
     // as many K/V stages (2 .. kAttnStages) as fit beside the rest in 227 KB
     static constexpr int kFixed = kDqBytes + kDqKBytes + kQBytes + kPBytes +
-                                  2 * kAttnWarps * 64 * 4 + 40 * 8 + 2 * kAttnStages * 8 + 256 + 1024;
+                                  2 * kAttnWarps * 64 * 4 + 80 * 8 + 2 * kAttnStages * 8 + 512 + 1024;
     static constexpr int kFit = (227 * 1024 - kFixed) / kStageBytes;
     static constexpr int kNStages = kFit < 2 ? 2 : (kFit > kAttnStages ? kAttnStages : kFit);
     static constexpr int kStages = kNStages * kStageBytes;
@@ -38,10 +38,10 @@ struct AttnSmem {
     static constexpr int kP = kQ + kQBytes;
     static constexpr int kRedMax = kP + kPBytes;              // [8][64] floats
     static constexpr int kRedL = kRedMax + kAttnWarps * 64 * 4;
-    static constexpr int kPrefix = kRedL + kAttnWarps * 64 * 4;   // [33] long long
-    static constexpr int kBars = kPrefix + 40 * 8;
+    static constexpr int kPrefix = kRedL + kAttnWarps * 64 * 4;   // 2 x [33] long long
+    static constexpr int kBars = kPrefix + 80 * 8;
     static constexpr int kFlags = kBars + 2 * kNStages * 8;
-    static constexpr int kTotal = kFlags + 256 + 1024;        // + alignment slack
+    static constexpr int kTotal = kFlags + 512 + 1024;        // + alignment slack
     static_assert(kTotal <= 227 * 1024, "attention shared memory exceeds 227 KB");
 };
 
@@ -100,6 +100,159 @@ __device__ __forceinline__ void turbo_item_store(uint32_t dst, const TurboItem &
     }
 }
 
+// The chunk plan of a step, the same in every CTA: sequence b's segments (one
+// per KV head and row block) are cut into nc[b] chunks of cu 16-token units.
+// cu depends only on the lengths and on the row-block count of the unchunked
+// head partition (nrb_u), so the head-chunk route and the plain route cut every
+// segment at the same tokens, and each row sees the same chunks in both.
+struct ChunkPlan {
+    int cu;                        // units per chunk
+    const int *ub, *nc;            // units / chunks of each sequence's segments
+    const long long *pi, *pg;      // first item / first level-1 group of each sequence [B + 1]
+};
+
+struct Item {
+    int b, kh, rb, chunk;
+    long long seg, first;          // segment id, the segment's first item
+    int u0, u1;                    // units [u0, u1) of the segment
+};
+
+__device__ __forceinline__ Item item_of(const ChunkPlan &cp, int B, int Hk, int nrb, long long i)
+{
+    Item it;
+    int b = 0;
+    while (b + 1 < B && cp.pi[b + 1] <= i)
+        ++b;
+    const int n = cp.nc[b];
+    const long long loc = i - cp.pi[b];
+    const long long sl = loc / n;
+    it.b = b;
+    it.chunk = (int)(loc - sl * n);
+    it.kh = (int)(sl / nrb);
+    it.rb = (int)(sl % nrb);
+    it.seg = ((long long)b * Hk + it.kh) * nrb + it.rb;
+    it.first = cp.pi[b] + sl * n;
+    it.u0 = it.chunk * cp.cu;
+    it.u1 = min(cp.ub[b], (it.chunk + 1) * cp.cu);
+    return it;
+}
+
+// More chunk partials than this per segment merge in two levels: groups of
+// kMergeGroup chunks into level-1 slots first.
+constexpr int kMaxFinal = 32;
+constexpr int kMergeGroup = 8;
+
+// Merge n (<= 32) partial slots (m[64] l[64] O[64][D] each, sf floats apart)
+// of the rows [0, nrows); one warp per row, lane j holds slot j's (m, l) and the
+// lanes share the D columns (column lane + 32 k).  Every slot is added in slot
+// order.  FINAL false: writes the combined unnormalized slot to `out`.  FINAL:
+// normalizes, rotates back the Turbo4 V basis, writes the attention tap and the
+// gated o_proj operand (fp16 fragments and their group sums).
+template <int DB, bool FINAL>
+__device__ __forceinline__ void merge_slots(const AttnArgs &a, const float *slots, long long sf, int n,
+                                            int nrows, float *out, const Item &it, int warp,
+                                            int lane)
+{
+    constexpr int D = DB * 64, PER = D / 32;
+    for (int i = warp; i < nrows; i += kAttnWarps) {
+        const float mj = lane < n ? __ldcg(slots + lane * sf + i) : -INFINITY;
+        const float lj = lane < n ? __ldcg(slots + lane * sf + kAttnMaxRows + i) : 0.f;
+        float acc[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k)
+            acc[k] = 0.f;
+        float M = mj;
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float f = mj == -INFINITY ? 0.f : exp2f(mj - M);
+        float L = f * lj;
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            L += __shfl_xor_sync(0xffffffffu, L, o);
+        constexpr int JB = PER >= 8 ? 2 : 4;     // slots whose loads are in flight together
+        for (int j0 = 0; j0 < n; j0 += JB) {
+            float v[JB][PER];
+#pragma unroll
+            for (int jj = 0; jj < JB; ++jj)
+#pragma unroll
+                for (int k = 0; k < PER; ++k)
+                    v[jj][k] = j0 + jj < n
+                                   ? __ldcg(slots + (j0 + jj) * sf + 2 * kAttnMaxRows + (long long)i * D +
+                                            lane + 32 * k)
+                                   : 0.f;
+#pragma unroll
+            for (int jj = 0; jj < JB; ++jj) {
+                const float fj = __shfl_sync(0xffffffffu, f, (j0 + jj) & 31);
+                if (j0 + jj < n)
+#pragma unroll
+                    for (int k = 0; k < PER; ++k)
+                        acc[k] = fmaf(fj, v[jj][k], acc[k]);
+            }
+        }
+        if constexpr (!FINAL) {
+#pragma unroll
+            for (int k = 0; k < PER; ++k)
+                out[2 * kAttnMaxRows + (long long)i * D + lane + 32 * k] = acc[k];
+            if (lane == 0) {
+                out[i] = M;
+                out[kAttnMaxRows + i] = L;
+            }
+        } else {
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+            for (int k = 0; k < PER; ++k)
+                acc[k] *= inv;
+            if (a.vq) {
+                // the values were attended in their Walsh-Hadamard basis: H o / sqrt(d)
+                float x[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    x[k] = k < PER ? acc[k] : 0.f;
+                wht_warp(x, PER, lane);
+#pragma unroll
+                for (int k = 0; k < PER; ++k)
+                    acc[k] = x[k] * a.inv_sqrt_d;
+            }
+            const int gqa = a.H / a.Hk;
+            const int h = it.kh * gqa + a.rb_h0[it.rb] + i / a.R, r = i % a.R;
+            const int m = it.b * a.R + r;
+            const long long Ktot = (long long)a.H * D;
+            const int gs = a.group_o, MP = 8 * a.NT;
+            float hv[PER];
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int c = lane + 32 * k;
+                const long long kk = (long long)h * D + c;
+                const float gt = a.gate[(long long)m * Ktot + kk];
+                const __half q = __float2half_rn(acc[k] * (1.f / (1.f + __expf(-gt))));
+                a.x16[x16_offset(m, (int)kk, a.NT)] = q;
+                hv[k] = __half2float(q);
+                if (a.tap_attn)
+                    a.tap_attn[(long long)m * Ktot + kk] = acc[k];
+            }
+            // group sums of the fp16 operand: groups of gs (32, 64 or 128 <= d)
+            // consecutive columns of the head, i.e. gs / 32 registers of the warp
+            const int rpg = gs / 32;
+            float t = 0.f;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                t += hv[k];
+                if ((k + 1) % rpg == 0) {
+#pragma unroll
+                    for (int o = 16; o; o >>= 1)
+                        t += __shfl_xor_sync(0xffffffffu, t, o);
+                    if (lane == 0) {
+                        const int c0 = h * D + 32 * (k + 1 - rpg);
+                        a.xsum[((long long)(c0 >> 7) * (kKU / gs) + ((c0 & 127) / gs)) * MP + m] = t;
+                    }
+                    t = 0.f;
+                }
+            }
+        }
+    }
+}
+
 template <int MT, int DB, int VQ>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
@@ -116,16 +269,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t *ps = smem + L::kP;
     float *red_max = reinterpret_cast<float *>(smem + L::kRedMax);
     float *red_l = reinterpret_cast<float *>(smem + L::kRedL);
-    long long *prefix = reinterpret_cast<long long *>(smem + L::kPrefix);
+    long long *pi = reinterpret_cast<long long *>(smem + L::kPrefix);     // [33] first item
+    long long *pg = pi + 40;                                                // [33] first group
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBars);
     uint64_t *empty = full + L::kNStages;
-    int *flags = reinterpret_cast<int *>(smem + L::kFlags);   // [0] abort [1] last [2..] ub
-    int *ub = flags + 4;                                        // units per segment of b [32]
+    int *flags = reinterpret_cast<int *>(smem + L::kFlags);   // [0] abort [1..3] merge flags
+    int *ub = flags + 8;                                        // units per segment of b [32]
+    int *nc = ub + 32;                                          // chunks per segment of b [32]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gqa = a.H / a.Hk;
 
-    // Dependents (the merge) may launch at once.  Before waiting for the q|k|v
+    // Dependents (the o_proj) may launch at once.  Before waiting for the q|k|v
     // projection this kernel only reads cache_pos and cache rows older than the
     // step: the projection starts its dependents after its own wait, so every
     // earlier kernel (which wrote those rows) has completed by then.
@@ -146,22 +301,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ub[tid] = valid ? (p0 + a.R + kAttnUnit - 1) / kAttnUnit : 0;
     }
     __syncthreads();
+    // the chunk plan: cu units per chunk from the unchunked partition's unit
+    // count over the grid (at least min_units), then per sequence the chunks of
+    // each segment, the items (segment, chunk) and the level-1 merge groups
     if (tid == 0) {
-        long long acc = 0;
+        long long uu = 0;
+        for (int b = 0; b < a.B; ++b)
+            uu += (long long)ub[b] * a.Hk * a.nrb_u;
+        const long long per = (uu + gridDim.x - 1) / gridDim.x;
+        const int cu = (int)(per > a.min_units ? per : a.min_units);
+        long long ai = 0, ag = 0;
         for (int b = 0; b < a.B; ++b) {
-            prefix[b] = acc;
-            acc += (long long)ub[b] * a.Hk * a.nrb;
+            const int n = (ub[b] + cu - 1) / cu;
+            nc[b] = n;
+            pi[b] = ai;
+            pg[b] = ag;
+            ai += (long long)n * a.Hk * a.nrb;
+            ag += (long long)(n > kMaxFinal ? (n + kMergeGroup - 1) / kMergeGroup : 0) * a.Hk * a.nrb;
         }
-        prefix[a.B] = acc;
+        pi[a.B] = ai;
+        pg[a.B] = ag;
+        flags[4] = cu;
     }
     __syncthreads();
+    const ChunkPlan cp{flags[4], ub, nc, pi, pg};
 
-    // Ranges are cut over attn_ranges(T) CTAs, each owning at least min_units
-    // units (the merge kernel counts contributors by range); the remaining CTAs
-    // have nothing to do.
-    const long long T = prefix[a.B], c = blockIdx.x;
-    const long long G = attn_ranges(T, gridDim.x, a.min_units);
-    const long long beg = c < G ? sk_start(c, T, G) : T, end = c < G ? sk_start(c + 1, T, G) : T;
+    // contiguous item ranges over the grid (consecutive chunks of a segment in
+    // one CTA share its q rows)
+    const long long T = pi[a.B], c = blockIdx.x;
+    const long long beg = T * c / gridDim.x, end = T * (c + 1) / gridDim.x;
     volatile int *abort = flags;
 
     if (warp == kAttnWarps) {
@@ -174,8 +342,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint64_t pol = l2_evict_first_policy();
             long long it = 0;
             bool stop = false, waited = false;
-            for (long long pos = beg; pos < end && !stop;) {
-                const Piece p = find_piece(prefix, ub, a.B, a.Hk, a.nrb, pos, end);
+            for (long long item = beg; item < end && !stop; ++item) {
+                const Item p = item_of(cp, a.B, a.Hk, a.nrb, item);
                 const int p0 = a.cache_pos[p.b];
                 for (int u = p.u0; u < p.u1; u += kAttnTile / kAttnUnit, ++it) {
                     const int nun = min(kAttnTile / kAttnUnit, p.u1 - u);
@@ -228,7 +396,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                  vq_scale, &full[slot], pol);
                     }
                 }
-                pos = p.seg_start + p.u1;
             }
             if (!waited)
                 pdl_wait();
@@ -246,18 +413,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // --------------------------------------------------------------- consumers
     pdl_wait();                 // q rows come from the q|k|v projection
     const int g = lane >> 2, cq = lane & 3;
-    long long it = 0;
-    for (long long pos = beg; pos < end;) {
-        const Piece p = find_piece(prefix, ub, a.B, a.Hk, a.nrb, pos, end);
+    long long it = 0, qseg = -1;
+    for (long long item = beg; item < end; ++item) {
+        const Item p = item_of(cp, a.B, a.Hk, a.nrb, item);
         const int nh = a.rb_nh[p.rb];
         const int h0 = p.kh * gqa + a.rb_h0[p.rb];
         const int nrows = nh * a.R;
         const int p0 = a.cache_pos[p.b];
         const int Lb = p0 + a.R;
 
-        // ---- q rows of this segment into shared memory (swizzled 16-byte chunks)
+        // ---- q rows of this segment into shared memory (swizzled 16-byte chunks),
+        //      once per run of items of one segment
         constexpr int CH = D / 8;   // chunks per row
-        if constexpr (VQ == 2) {
+        const bool load_q = p.seg != qseg;
+        qseg = p.seg;
+        if (!load_q) {
+        } else if constexpr (VQ == 2) {
             // symmetric Turbo4: the keys live in the rotated basis, so the rows
             // are rotated once (q' = H q / sqrt(d): q . k = q' . H k / sqrt(d))
             // and kept in fp16 for the fp16 products with the dequantized keys
@@ -355,7 +526,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
             // ---- S = q K^T for this warp's 8 tokens; the head_dim contraction is
             //      spread over SPLIT independent accumulator chains (MMA latency)
-            constexpr int SPLIT = MT >= 4 ? 1 : (MT >= 2 ? 2 : 4);
+            // (two chains whatever the row count, so a row's sums do not depend on
+            // how many rows its segment has: the head-chunk route and the plain
+            // route add every score in the same order)
+            constexpr int SPLIT = 2;
             float sc[MT][4];
             float scs[SPLIT][MT][4];
             const bool has_tok = ok && (warp * 8 < ntok);
@@ -564,9 +738,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mbar_arrive(&empty[slot]);
         }
 
-        // ---- partial (m, l, O) of this piece into slot seg + c (valid rows only);
-        //      a separate merge kernel combines the slots of each segment
-        float *part = a.ws + (p.seg + c) * (long long)attn_slot_floats(D);
+        // ---- partial (m, l, O) of this chunk into its slot (valid rows only)
+        const long long sf = attn_slot_floats(D);
+        float *part = a.ws + item * sf;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -605,9 +779,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     part[kAttnMaxRows + i] = l;
                 }
         }
-        // red_l is reused by the next piece: keep warp 0's reads before new writes
+        // red_l is reused by the next item: keep warp 0's reads before new writes
+        __threadfence();
         named_bar_sync(1, kAttnWarps * 32);
-        pos = p.seg_start + p.u1;
+
+        // ---- merge: the CTA whose chunk completes a group of kMergeGroup chunks
+        //      (segments of more than kMaxFinal chunks) combines the group into
+        //      its level-1 slot; the CTA that completes the segment combines its
+        //      chunk (or level-1) slots, applies the gate and writes the o_proj
+        //      operand.  Completion is counted with atomics after a fence; the
+        //      last user of a counter resets it for the next step.
+        const int n = cp.nc[p.b];
+        const int ng = n > kMaxFinal ? (n + kMergeGroup - 1) / kMergeGroup : 0;
+        const long long sl = (long long)p.kh * a.nrb + p.rb;   // segment within the sequence
+        const int grp = p.chunk / kMergeGroup;
+        const long long gidx = cp.pg[p.b] + sl * ng + grp;
+        if (tid == 0) {
+            int lg = 0, ls = 0;
+            if (ng == 0) {
+                ls = atomicAdd(&a.cnt_seg[p.seg], 1u) == (unsigned)(n - 1);
+            } else {
+                const int gs = min(kMergeGroup, n - grp * kMergeGroup);
+                lg = atomicAdd(&a.cnt_grp[gidx], 1u) == (unsigned)(gs - 1);
+            }
+            flags[1] = lg;
+            flags[2] = ls;
+        }
+        named_bar_sync(1, kAttnWarps * 32);
+        if (flags[1]) {
+            __threadfence();
+            const int gs = min(kMergeGroup, n - grp * kMergeGroup);
+            merge_slots<DB, false>(a, a.ws + (p.first + (long long)grp * kMergeGroup) * sf, sf, gs,
+                                   nrows, a.ws1 + gidx * sf, p, warp, lane);
+            __threadfence();
+            named_bar_sync(1, kAttnWarps * 32);
+            if (tid == 0) {
+                a.cnt_grp[gidx] = 0u;
+                flags[2] = atomicAdd(&a.cnt_seg[p.seg], 1u) == (unsigned)(ng - 1);
+            }
+            named_bar_sync(1, kAttnWarps * 32);
+        }
+        if (flags[2]) {
+            __threadfence();
+            if (ng == 0)
+                merge_slots<DB, true>(a, a.ws + p.first * sf, sf, n, nrows, nullptr, p, warp, lane);
+            else
+                merge_slots<DB, true>(a, a.ws1 + (cp.pg[p.b] + sl * ng) * sf, sf, ng, nrows,
+                                      nullptr, p, warp, lane);
+            if (tid == 0)
+                a.cnt_seg[p.seg] = 0u;
+        }
+        // flags[1..2] are rewritten by the next item
+        named_bar_sync(1, kAttnWarps * 32);
     }
 }
 

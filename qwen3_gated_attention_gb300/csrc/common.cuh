@@ -76,12 +76,13 @@ __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase with the given parity.  Gives up after kWaitLimitNs, or at
+// Wait for the phase with the given parity.  Gives up after limit_ns, or at
 // once when *abort is already set; on giving up it sets *abort and the status
 // word's timeout bit and returns false.  Callers keep their control flow (every
 // named barrier is still reached) and skip the work of an aborted stage.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          unsigned *status)
+                                          unsigned *status,
+                                          unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try(bar, parity))
         return true;
@@ -93,12 +94,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
             return true;
         if (*abort)
             return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort = 1;
             atomicOr(status, kStatusTimeout);
             return false;
         }
     }
+}
+
+// Wait for the phase with the given parity, bounded by `limit_ns` but not cut
+// short by an abort flag: for barriers whose completion must be observed
+// before the thread goes on (bytes other CTAs are still sending here).  Sets
+// the status word's timeout bit and returns false if the limit passes.
+__device__ __forceinline__ bool mbar_wait_all(uint64_t *bar, uint32_t parity, unsigned *status,
+                                              unsigned long long limit_ns)
+{
+    if (mbar_try(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try(bar, parity)) {
+        if (global_ns() - t0 > limit_ns) {
+            atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+    return true;
 }
 
 // ------------------------------------------------------------- TMA copies
@@ -319,19 +339,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// Stream-K ownership: units [0, T) are cut into G contiguous ranges,
-// range c = [floor(c*T/G), floor((c+1)*T/G)).
-__host__ __device__ __forceinline__ long long sk_start(long long c, long long T, long long G)
-{
-    return (c * T) / G;
-}
-
-// The range that holds unit idx.
-__host__ __device__ __forceinline__ long long sk_owner(long long idx, long long T, long long G)
-{
-    return ((idx + 1) * G - 1) / T;
 }
 
 }  // namespace gattn

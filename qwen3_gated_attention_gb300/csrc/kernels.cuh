@@ -98,6 +98,10 @@ struct ProjArgs {
     int xtab_bytes;
     const void *xraw;     // x [M][K] for the table
     int x_f32;            // x dtype: fp32 (1) or bf16 (0)
+    unsigned long long wait_ns;   // bound of every wait on a stage
+    // failure test hook (q|k|v): nonzero makes CTA 0 withhold its last weight
+    // stage, so that stage's wait runs out
+    int withhold;
     unsigned *status;
 };
 
@@ -221,60 +225,20 @@ constexpr int kAttnMaxRows = 64;       // query rows per segment
 // floats per attention partial slot: m[64], l[64], O[64][d]
 __host__ __device__ inline int attn_slot_floats(int d) { return 2 * kAttnMaxRows + kAttnMaxRows * d; }
 
-// CTAs the attention units are cut over: at most the grid, at least min_units
-// units per CTA, at least one CTA.
-__host__ __device__ inline long long attn_ranges(long long T, long long grid, int min_units)
-{
-    long long g = (T + min_units - 1) / min_units;
-    g = g < grid ? g : grid;
-    return g > 0 ? g : 1;
-}
-
-// One CTA's share of one segment: segments are (sequence b, KV head kh, row
-// block rb) in that order, each cut into ub[b] 16-token units; prefix[b] is
-// the first unit of sequence b's segments.
-struct Piece {
-    int b, kh, rb;
-    long long seg;          // global segment id (b, kh, rb order)
-    long long seg_start, seg_end;
-    int u0, u1;             // units [u0, u1) of the segment in this piece
-};
-
-// Locate the piece that starts at unit `pos`.
-__device__ __forceinline__ Piece find_piece(const long long *prefix, const int *ub, int B, int Hk,
-                                            int nrb, long long pos, long long end)
-{
-    Piece p;
-    int b = 0;
-    while (b + 1 < B && prefix[b + 1] <= pos)
-        ++b;
-    const long long U = ub[b];
-    const long long loc = pos - prefix[b];
-    const long long segl = loc / U;
-    p.b = b;
-    p.kh = (int)(segl / nrb);
-    p.rb = (int)(segl % nrb);
-    p.seg = ((long long)b * Hk + p.kh) * nrb + p.rb;
-    p.seg_start = prefix[b] + segl * U;
-    p.seg_end = p.seg_start + U;
-    p.u0 = (int)(loc - segl * U);
-    const long long pe = end < p.seg_end ? end : p.seg_end;
-    p.u1 = (int)(pe - p.seg_start);
-    return p;
-}
-
 struct AttnArgs {
     const __nv_bfloat16 *qn;     // [B][R][H][d]
     const float *gate;           // [M][H*d]
     const int *cache_pos;
     int B, R, H, Hk, d, cap;
     int nrb;                     // row blocks per KV group
+    int nrb_u;                   // row blocks per KV group of the unchunked partition
     int rb_h0[kMaxRowBlocks];    // first head of each row block (relative to the group)
     int rb_nh[kMaxRowBlocks];    // heads of each row block
     float scale_log2;            // log2(e) / sqrt(d)
-    int min_units;               // minimum 16-token units per attention CTA
-    int grid;                    // attention grid size (the merge recomputes the ranges)
-    float *ws;                   // partials, attn_slot_floats(d) per slot
+    int min_units;               // minimum 16-token units per chunk
+    float *ws;                   // chunk partials, attn_slot_floats(d) per item
+    float *ws1;                  // level-1 merge slots
+    unsigned *cnt_seg, *cnt_grp; // completion counters per segment / level-1 group (zero between steps)
     // o_proj operand
     __half *x16;
     float *xsum;
@@ -311,8 +275,6 @@ cudaError_t attn_vqk_set_smem_limits();
 // standalone Turbo4 quantizer: one warp per row of d bf16 values
 cudaError_t launch_turbo4_quantize(const uint16_t *v, long long rows, int d, uint8_t *codes,
                                    uint8_t *scales, const TurboTables &t, cudaStream_t s);
-// merge of the attention partials + output gate -> o_proj operand
-cudaError_t launch_attn_merge(const AttnArgs &a, int max_rows, bool pdl, cudaStream_t s);
 int attn_smem_bytes(int MT, int DB);
 cudaError_t attn_set_smem_limits();
 

@@ -538,14 +538,23 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
             const long long pre = (end - beg) < S ? (end - beg) : S;
             // bytes a stage brings: weights, and x unless the CTA converts x itself
             const uint32_t stage_tx = a.step_bytes + (xfold ? 0 : xbytes + sbytes);
+            // failure test hook: CTA 0 never issues its last stage
+            const long long withhold_at = a.withhold && blockIdx.x == 0 ? end - 1 - beg : -1;
+            long long withheld = -1;
             for (; it < pre; ++it) {
                 const long long s = beg + it;
+                if (it == withhold_at) {
+                    withheld = it;
+                    continue;
+                }
                 uint8_t *st = stages + (size_t)(it % S) * a.stage_bytes;
                 mbar_arrive_expect_tx(&full[it % S], stage_tx);
                 bulk_g2s(st, a.w + s * a.step_bytes, a.step_bytes, &full[it % S], pol);
             }
             pdl_wait();
             for (long long i = 0; i < pre && !xfold; ++i) {
+                if (i == withheld)
+                    continue;
                 const int ku = (int)((beg + i) % a.nku);
                 uint8_t *st = stages + (size_t)(i % S) * a.stage_bytes;
                 bulk_g2s(st + a.step_bytes, a.x16 + (long long)ku * NT * 1024, xbytes,
@@ -557,8 +566,12 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
                 const long long s = beg + it;
                 const int slot = (int)(it % S);
                 const uint32_t ph = (uint32_t)((it / S) & 1);
-                if (!mbar_wait(&empty[slot], ph ^ 1u, abort, a.status))
+                if (!mbar_wait(&empty[slot], ph ^ 1u, abort, a.status, a.wait_ns))
                     break;
+                if (it == withhold_at) {
+                    withheld = it;          // never issued: its consumers' wait runs out
+                    continue;
+                }
                 const int ku = (int)(s % a.nku);
                 uint8_t *st = stages + (size_t)slot * a.stage_bytes;
                 mbar_arrive_expect_tx(&full[slot], stage_tx);
@@ -573,9 +586,11 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
             // let every copy this CTA issued land before the ring is reused
             const long long first = it > S ? it - S : 0;
             for (long long i = first; i < it; ++i) {
+                if (i == withheld)
+                    continue;
                 unsigned long long t0 = global_ns();
                 while (!mbar_try(&full[i % S], (uint32_t)((i / S) & 1)) &&
-                       global_ns() - t0 < kWaitLimitNs) {
+                       global_ns() - t0 < a.wait_ns) {
                 }
             }
         }
@@ -633,7 +648,7 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
             const int slot = (int)(it % S);
             const uint32_t ph = (uint32_t)((it / S) & 1);
             const uint8_t *st = stages + (size_t)slot * a.stage_bytes;
-            if (mbar_wait(&full[slot], ph, abort, a.status))
+            if (mbar_wait(&full[slot], ph, abort, a.status, a.wait_ns))
                 proj_stage<BITS, NT, GROUP>(st, xfold ? xtab + it * xe : st + a.step_bytes,
                                             a.unit_bytes, warp, lane, Y);
             __syncwarp();
@@ -667,8 +682,12 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
     // every partial this CTA finishes has landed; then the cluster barrier that
     // keeps each CTA resident until every receiver has its bytes (a CTA's shared
     // memory must outlive the stores sent to it), waited on only at the end
+    // (not cut short by an aborted main loop: every CTA pushes its bytes, and
+    // this CTA must see them all land before it may leave).  A sender whose own
+    // stage wait ran out pushes about one limit late, so this wait is bounded by
+    // four limits: it ends before the bytes land only if a copy never lands.
     if (warp < kWR && rbytes)
-        mbar_wait(rbar, 0, abort, a.status);
+        mbar_wait_all(rbar, 0, a.status, 4 * a.wait_ns);
     cluster_arrive();
     if (warp < kWR && rbytes) {
         const int row0 = cluster * a.eb_rows;

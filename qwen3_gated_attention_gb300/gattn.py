@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "GATTN_OK", 1: "GATTN_E_INVALID_ARG", 2: "GATTN_E_UNSUPPORTED
 DTYPE_F32, DTYPE_BF16 = 0, 1
 PROJ_Q, PROJ_K, PROJ_V, PROJ_O = 0, 1, 2, 3
 # kernels of a step (gattn_layer_step_kernels)
-KERNEL_NAMES = {1: "xprep", 2: "proj_qkv", 3: "attn", 4: "merge", 5: "proj_o", 6: "postnorm"}
+KERNEL_NAMES = {1: "xprep", 2: "proj_qkv", 3: "attn", 5: "proj_o", 6: "postnorm"}
 
 # every symbol include/gattn.h declares
 EXPORTS = (
@@ -34,7 +34,7 @@ EXPORTS = (
     "gattn_layer_launches_per_step", "gattn_layer_set_events", "gattn_layer_dequant_device_static",
     "gattn_layer_step_block", "gattn_kv_register_turbo4v",
     "gattn_turbo4_codebook", "gattn_turbo4_quantize_device", "gattn_layer_set_mask",
-    "gattn_kv_register_turbo4", "gattn_layer_step_kernels",
+    "gattn_kv_register_turbo4", "gattn_layer_step_kernels", "gattn_layer_set_test_wait",
 )
 
 
@@ -135,6 +135,7 @@ def lib():
         L.gattn_turbo4_quantize_device.argtypes = [p, i64, i32, p, p, p]
         L.gattn_layer_set_mask.argtypes = [p, C.POINTER(gattn_mask)]
         L.gattn_kv_register_turbo4.argtypes = [p, C.POINTER(gattn_kv_turbo4_desc), C.POINTER(p)]
+        L.gattn_layer_set_test_wait.argtypes = [p, i64, i32]
         for name in ("gattn_cfg_validate", "gattn_layer_create", "gattn_layer_set_weights",
                      "gattn_kv_register", "gattn_layer_step", "gattn_layer_poll_status",
                      "gattn_layer_set_taps", "gattn_pack_affine_host", "gattn_unpack_codes_device",
@@ -142,7 +143,8 @@ def lib():
                      "gattn_layer_dequant_device_static",
                      "gattn_layer_step_block", "gattn_kv_register_turbo4v",
                      "gattn_turbo4_codebook", "gattn_turbo4_quantize_device",
-                     "gattn_layer_set_mask", "gattn_kv_register_turbo4"):
+                     "gattn_layer_set_mask", "gattn_kv_register_turbo4",
+                     "gattn_layer_set_test_wait"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -310,6 +312,13 @@ def layer_set_events(layer: int, events) -> None:
     """events: sequence of cudaEvent_t handles (ints), or empty to turn off."""
     arr = (C.c_void_p * max(1, len(events)))(*events)
     _check(lib().gattn_layer_set_events(layer, C.addressof(arr) if events else None, len(events)))
+
+
+def layer_set_test_wait(layer: int, wait_limit_ns: int = 0, withhold_stage: bool = False) -> None:
+    """Failure-detection test hook: the bound of the projection kernels' device
+    waits (0 restores the default) and whether CTA 0 of the q|k|v projection
+    withholds its last weight stage so that one wait runs out."""
+    _check(lib().gattn_layer_set_test_wait(layer, int(wait_limit_ns), 1 if withhold_stage else 0))
 
 
 # ------------------------------------------------------------ host helpers

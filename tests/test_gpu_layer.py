@@ -161,8 +161,7 @@ def test_layer_parity(name):
     case = make_case(SMALL[name])
     got = gpu_run(case)
     # the q|k|v kernel converts x itself when its tables fit, else x prep runs first
-    assert got["kernels"][-3:] == ["proj_qkv", "attn", "proj_o"] or \
-        got["kernels"][-4:] == ["proj_qkv", "attn", "merge", "proj_o"]
+    assert got["kernels"][-3:] == ["proj_qkv", "attn", "proj_o"]
     assert got["launches"] == len(got["kernels"])
     ref = oracle_run(case)
     rep = check_parity(case, got, ref, what=name)
@@ -185,10 +184,14 @@ WIDE = {
 def test_wide_verify_rows(name):
     case = make_case(WIDE[name])
     ref = oracle_run(case)
+    runs = {}
     for chunk in (True, False):
-        got = gpu_run(case, head_chunk=chunk)
+        got = runs[chunk] = gpu_run(case, head_chunk=chunk)
         rep = check_parity(case, got, ref, what=f"{name} chunk={chunk}")
         print(name, chunk, rep)
+    # the head-chunk route changes only the head partition: bit for bit equal
+    assert np.array_equal(runs[True]["attn"], runs[False]["attn"])
+    assert np.array_equal(runs[True]["out"], runs[False]["out"])
 
 
 @pytest.mark.parametrize("name", ["verify_2k_p46", "verify_2k_p2048", "d128_b5_b2"])
@@ -201,11 +204,12 @@ def test_head_chunk_route_agrees_with_unchunked(name):
     ref = oracle_run(case)
     check_parity(case, on, ref, what="chunked")
     check_parity(case, off, ref, what="unchunked")
-    # the two routes differ only in how heads are grouped per CTA, hence in how
-    # the keys are cut into pieces: P is rounded to bf16 against different
-    # running maxima, so agreement is to bf16 level (~1e-3), not bitwise
-    ok, rep = refs.close(on["attn"], off["attn"], abs_tol=1e-3, rel_tol=1e-2, l2_tol=2e-3)
-    assert ok, rep
+    # the two routes differ only in how heads are grouped into segments: every
+    # segment is cut at the same tokens and a row's arithmetic does not depend
+    # on the other rows of its segment, so the results are equal bit for bit
+    # (DS4Server issue 113 closing comment: all results match the raw bits)
+    assert np.array_equal(on["attn"], off["attn"])
+    assert np.array_equal(on["out"], off["out"])
     assert np.array_equal(on["y"], off["y"])
     assert np.array_equal(on["k"], off["k"]) and np.array_equal(on["v"], off["v"])
 

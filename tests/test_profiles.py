@@ -18,7 +18,7 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
-SUMMARIES = sorted(f for f in os.listdir(PROFILES) if f.endswith(".md"))
+SUMMARIES = sorted(f for f in os.listdir(PROFILES) if f.endswith(".md")) if os.path.isdir(PROFILES) else []
 KERNEL_SUMMARIES = [f for f in SUMMARIES if not f.startswith("launches_")]
 LAUNCH_SUMMARIES = [f for f in SUMMARIES if f.startswith("launches_")]
 
