@@ -111,7 +111,7 @@ gattn_status validate(const gattn_cfg *c)
                     "max_batch, max_q_len and their product must be <= 32 (product <= 16 for fp32 x, "
                     "which takes two fp16 planes)");
     const int gqa = c->num_heads / c->num_kv_heads;
-    if (gqa > 64 * kMaxRowBlocks)
+    if (gqa > kRowBlockRows * kMaxRowBlocks)
         return fail(GATTN_E_UNSUPPORTED, "gqa too large");
     return GATTN_OK;
 }
@@ -128,8 +128,8 @@ struct ProjPlan {
 int nt_index(int NT) { return NT == 1 ? 0 : (NT == 2 ? 1 : 2); }
 
 // Attention row blocks of a KV group for q_len rows: the head chunks of the
-// verify plan (enabled or not), a chunk of more than 64 rows cut into blocks of
-// whole heads.  Writes up to kMaxRowBlocks (first head, heads) pairs when the
+// verify plan (enabled or not), each cut into blocks of whole heads of at most
+// kRowBlockRows rows (one head when q_len is larger).  Writes up to kMaxRowBlocks (first head, heads) pairs when the
 // arrays are given; returns the block count (-1 past kMaxRowBlocks) and the
 // largest block's rows.
 int attn_row_blocks(int q_len, int H, int Hk, int enabled, int *rb_h0, int *rb_nh, int *max_rows)
@@ -139,7 +139,7 @@ int attn_row_blocks(int q_len, int H, int Hk, int enabled, int *rb_h0, int *rb_n
     const int per_group = nchunks / Hk;
     int nrb = 0, mr = 0;
     for (int j = 0; j < per_group; ++j) {
-        const int hpb = std::max(1, 64 / q_len);
+        const int hpb = std::max(1, kRowBlockRows / q_len);
         for (int h = 0; h < len[j]; h += hpb) {
             if (nrb >= kMaxRowBlocks)
                 return -1;
@@ -156,16 +156,19 @@ int attn_row_blocks(int q_len, int H, int Hk, int enabled, int *rb_h0, int *rb_n
     return nrb;
 }
 
+constexpr int kAttnMinUnits = 4;     // 16-token units per attention chunk, at least
+constexpr int kAttnSplit = 8;        // attention chunks per CTA aimed at
+
 // Upper bound of the attention items (segment chunks) of a step: the chunk
-// length is at least the unchunked partition's units over the grid, so the
-// items are at most grid * nrb / nrb_u plus one partial chunk per segment.
-long long attn_items_bound(int grid, int nrb, int nrb_u, int batch, int Hk)
+// length is at least the unchunked partition's units over split x grid, so the
+// items are at most split * grid * nrb / nrb_u plus one partial chunk per
+// segment; and a segment has at most kMaxChunks (32) chunks.
+long long attn_items_bound(int grid, int split, int nrb, int nrb_u, int batch, int Hk)
 {
-    return ((long long)grid * nrb + nrb_u - 1) / nrb_u + (long long)batch * Hk * nrb;
+    const long long segs = (long long)batch * Hk * nrb;
+    return std::min(((long long)split * grid * nrb + nrb_u - 1) / nrb_u + segs, 32 * segs);
 }
 
-constexpr int kAttnMinUnits = 4;     // 16-token units per attention chunk, at least
-constexpr int kMergeGroupHost = 8;   // chunks per level-1 merge group (attn.cuh kMergeGroup)
 // shared memory a q|k|v CTA may spend on converting x itself (the table of its
 // k units' fp16 fragments and group sums); a larger table keeps the x prep kernel
 constexpr int kXTabMax = 24 * 1024;
@@ -215,9 +218,8 @@ struct gattn_layer {
     __nv_bfloat16 *qn = nullptr;
     float *gate = nullptr;
     float *ws_attn = nullptr;              // attention chunk partials
-    float *ws_attn1 = nullptr;             // attention level-1 merge slots
-    unsigned *cnt_seg = nullptr, *cnt_grp = nullptr;   // attention completion counters
-    long long items_cap = 0, l1_cap = 0;
+    unsigned *cnt_seg = nullptr;           // attention completion counters (per segment)
+    long long items_cap = 0;
     unsigned *status = nullptr;
     double *inv_freq = nullptr;
     float2 *inv_freq2 = nullptr;           // the same frequencies as float (hi, lo) pairs
@@ -431,8 +433,8 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaMalloc(&L->qn, (size_t)L->M_max * L->Ko * 2));
     TRY(cudaMalloc(&L->gate, (size_t)L->M_max * L->Ko * sizeof(float)));
     // attention segments: batch x KV heads x row blocks (at most gqa row blocks)
-    // attention scratch: chunk partials, level-1 merge slots and counters for the
-    // largest step the configuration admits (every q_len, both head partitions)
+    // attention scratch: chunk partials and completion counters for the largest
+    // step the configuration admits (every q_len, both head partitions)
     {
         int nrb_max = 1;
         for (int R = 1; R <= c.max_q_len; ++R) {
@@ -443,19 +445,15 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
             if (nrb < 0 || nrb_u < 0)
                 return cleanup(fail(GATTN_E_UNSUPPORTED, "too many attention row blocks"));
             nrb_max = std::max(nrb_max, std::max(nrb, nrb_u));
-            L->items_cap = std::max(L->items_cap, attn_items_bound(L->attn_grid, nrb, nrb_u,
+            L->items_cap = std::max(L->items_cap, attn_items_bound(L->attn_grid, kAttnSplit, nrb, nrb_u,
                                                                    c.max_batch, c.num_kv_heads));
         }
         L->max_seg = c.max_batch * c.num_kv_heads * nrb_max;
-        L->l1_cap = L->items_cap / kMergeGroupHost + L->max_seg + 1;
     }
     L->ws_attn_floats = (size_t)L->items_cap * attn_slot_floats(c.head_dim);
     TRY(cudaMalloc(&L->ws_attn, L->ws_attn_floats * sizeof(float)));
-    TRY(cudaMalloc(&L->ws_attn1, (size_t)L->l1_cap * attn_slot_floats(c.head_dim) * sizeof(float)));
     TRY(cudaMalloc(&L->cnt_seg, (size_t)L->max_seg * sizeof(unsigned)));
     TRY(cudaMemset(L->cnt_seg, 0, (size_t)L->max_seg * sizeof(unsigned)));
-    TRY(cudaMalloc(&L->cnt_grp, (size_t)L->l1_cap * sizeof(unsigned)));
-    TRY(cudaMemset(L->cnt_grp, 0, (size_t)L->l1_cap * sizeof(unsigned)));
     TRY(cudaMalloc(&L->status, sizeof(unsigned)));
     TRY(cudaMemset(L->status, 0, sizeof(unsigned)));
     {
@@ -507,7 +505,7 @@ void gattn_layer_destroy(gattn_layer *L)
         return;
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq, L->inv_freq2,
-                    L->ws_attn1, L->cnt_seg, L->cnt_grp,
+                    L->cnt_seg,
                     L->q_norm, L->k_norm,
                     L->ss_part, L->post_ticket};
     for (void *p : ptrs)
@@ -829,7 +827,7 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     if (nrb < 0 || nrb_u < 0)
         return fail(GATTN_E_UNSUPPORTED, "too many attention row blocks");
     if ((long long)batch * c.num_kv_heads * nrb > L->max_seg ||
-        attn_items_bound(L->attn_grid, nrb, nrb_u, batch, c.num_kv_heads) > L->items_cap)
+        attn_items_bound(L->attn_grid, kAttnSplit, nrb, nrb_u, batch, c.num_kv_heads) > L->items_cap)
         return fail(GATTN_E_UNSUPPORTED, "attention items exceed the scratch sized at create");
     const int nchunks = gattn_head_chunk_plan(q_len, c.num_heads, c.num_kv_heads, c.head_chunk,
                                               nullptr, nullptr, 0);
@@ -940,10 +938,9 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     t.scale_log2 = scale_log2;
     t.nrb_u = nrb_u;
     t.ws = L->ws_attn;
-    t.ws1 = L->ws_attn1;
     t.cnt_seg = L->cnt_seg;
-    t.cnt_grp = L->cnt_grp;
     t.min_units = kAttnMinUnits;
+    t.split = kAttnSplit;
     t.x16 = L->x16_o;
     t.xsum = L->xsum_o;
     t.NT = NT;

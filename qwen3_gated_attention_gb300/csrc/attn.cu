@@ -3,21 +3,23 @@
 // instances).
 //
 // For every (sequence b, KV head kh, row block rb) segment the rows are the
-// R new rows of the row block's query heads (one KV group, or one chunk of it
-// when the verify head-chunk plan is on), and the keys are cache positions
-// [0, cache_pos[b] + R).  Segments are cut into chunks of whole 16-token units,
-// of one length for all segments of the step (from the unchunked partition,
-// so both head partitions cut every segment alike), and the chunks are spread
-// over the grid in contiguous ranges.  One producer warp streams 64-token K/V
-// tiles with 4-D TMA tensor copies (128-byte swizzle) into a ring of up to four
-// stages; one tile read serves every query row of the segment.  Eight consumer
-// warps compute S = q K^T and O += P V with bf16 mma.sync (fp32 accumulate) and
-// an online softmax in the log2 domain.
+// R new rows of the row block's query heads (at most 16 rows of one KV group,
+// or of one chunk of it when the verify head-chunk plan is on), and the keys
+// are cache positions [0, cache_pos[b] + R).  Segments are cut into chunks of
+// whole 16-token units, of one length for all segments of the step (from the
+// unchunked partition, so both head partitions cut every segment alike; at
+// most 32 chunks a segment), and the chunks are spread over the grid in
+// contiguous ranges balanced by tokens.  One producer warp streams 64-token
+// K/V tiles with 4-D TMA tensor copies (128-byte swizzle) into a ring of up to
+// four stages; one tile read serves every query row of the segment.  Eight
+// consumer warps compute S = q K^T and O += P V with bf16 mma.sync (fp32
+// accumulate) and an online softmax in the log2 domain.
 //
-// Each chunk leaves a partial (m, l, O).  The CTA that finishes the last chunk
-// of a segment merges the segment (in two levels when it has many chunks),
-// applies the output gate attn * sigmoid(gate) and writes the o_proj operand in
-// tensor-core fragment order (fp16), so no separate merge launch is needed.
+// A segment of one chunk is finished from the accumulators.  Otherwise each
+// chunk leaves a partial (m, l, O) and the CTA that finishes the last chunk of
+// the segment merges them.  Either way the kernel applies the output gate
+// attn * sigmoid(gate) and writes the o_proj operand in tensor-core fragment
+// order (fp16) with its group sums, so no separate merge launch is needed.
 #include "attn.cuh"
 
 namespace gattn {

@@ -101,14 +101,15 @@ __device__ __forceinline__ void turbo_item_store(uint32_t dst, const TurboItem &
 }
 
 // The chunk plan of a step, the same in every CTA: sequence b's segments (one
-// per KV head and row block) are cut into nc[b] chunks of cu 16-token units.
-// cu depends only on the lengths and on the row-block count of the unchunked
-// head partition (nrb_u), so the head-chunk route and the plain route cut every
-// segment at the same tokens, and each row sees the same chunks in both.
+// per KV head and row block) are cut into nc[b] <= kMaxChunks chunks of cu
+// 16-token units.  cu depends only on the lengths and on the row-block count of
+// the unchunked head partition (nrb_u), so the head-chunk route and the plain
+// route cut every segment at the same tokens, and each row sees the same chunks
+// in both.
 struct ChunkPlan {
     int cu;                        // units per chunk
     const int *ub, *nc;            // units / chunks of each sequence's segments
-    const long long *pi, *pg;      // first item / first level-1 group of each sequence [B + 1]
+    const long long *pi;           // first item of each sequence [B + 1]
 };
 
 struct Item {
@@ -137,30 +138,70 @@ __device__ __forceinline__ Item item_of(const ChunkPlan &cp, int B, int Hk, int 
     return it;
 }
 
-// More chunk partials than this per segment merge in two levels: groups of
-// kMergeGroup chunks into level-1 slots first.
-constexpr int kMaxFinal = 32;
-constexpr int kMergeGroup = 8;
+// The first item (in item order) that starts at unit offset x or later; uo[b]
+// is the unit offset of sequence b's first item (uo[B]: all units).
+__device__ __forceinline__ long long first_item_at(const ChunkPlan &cp, const long long *uo, int B,
+                                                   long long x)
+{
+    if (x >= uo[B])
+        return cp.pi[B];
+    int b = 0;
+    while (b + 1 < B && uo[b + 1] <= x)
+        ++b;
+    const long long loc = x - uo[b];
+    const int ubb = cp.ub[b];              // > 0: an empty sequence spans no offsets
+    const long long sl = loc / ubb;
+    const long long r = loc - sl * ubb;
+    return cp.pi[b] + sl * cp.nc[b] + (r + cp.cu - 1) / cp.cu;
+}
 
-// Merge n (<= 32) partial slots (m[64] l[64] O[64][D] each, sf floats apart)
-// of the rows [0, nrows); one warp per row, lane j holds slot j's (m, l) and the
-// lanes share the D columns (column lane + 32 k).  Every slot is added in slot
-// order.  FINAL false: writes the combined unnormalized slot to `out`.  FINAL:
-// normalizes, rotates back the Turbo4 V basis, writes the attention tap and the
-// gated o_proj operand (fp16 fragments and their group sums).
-template <int DB, bool FINAL>
-__device__ __forceinline__ void merge_slots(const AttnArgs &a, const float *slots, long long sf, int n,
-                                            int nrows, float *out, const Item &it, int warp,
-                                            int lane)
+// Chunks per segment, at most: the chunk length grows for longer segments so
+// that one merge combines every partial of a segment (lane j holds chunk j).
+constexpr int kMaxChunks = 32;
+
+// Merge the n (<= kMaxChunks) chunk partials of a segment (slot j: m[64] l[64]
+// O[64][D], sf floats apart) into the gated o_proj operand of its nrows rows.
+// A work unit is one row's part of NP parts of D / NP columns (one part when
+// the values are rotated back, which needs the whole row in one warp); lane j
+// holds slot j's (m, l) and the lanes share the part's columns (column
+// part * D / NP + lane + 32 k).  The (m, l) pairs, the gate and the first JB
+// slots are requested together; the slots are added in slot order, so the
+// sums do not depend on the part split or on the head partition.  Writes the
+// attention tap, the fp16 o_proj operand and its group sums.
+template <int DB, int VQ>
+__device__ __forceinline__ void merge_final(const AttnArgs &a, const float *slots, long long sf,
+                                            int n, int nrows, const Item &it, int warp, int lane)
 {
     constexpr int D = DB * 64, PER = D / 32;
-    for (int i = warp; i < nrows; i += kAttnWarps) {
+    constexpr int NP = (VQ != 0 || PER < 4) ? 1 : 2;
+    constexpr int KP = PER / NP;           // columns per lane
+    constexpr int JB = 32 / KP;            // slots in flight together
+    const int gqa = a.H / a.Hk;
+    const long long Ktot = (long long)a.H * D;
+    const int gs = a.group_o, MP = 8 * a.NT, rpg = gs / 32;
+    for (int w = warp; w < nrows * NP; w += kAttnWarps) {
+        const int i = w / NP, cb = (w % NP) * (D / NP);
+        const int h = it.kh * gqa + a.rb_h0[it.rb] + i / a.R, r = i % a.R;
+        const int m = it.b * a.R + r;
+        const long long kb = (long long)m * Ktot + (long long)h * D + cb;
+        const float *col = slots + 2 * kAttnMaxRows + (long long)i * D + cb + lane;
         const float mj = lane < n ? __ldcg(slots + lane * sf + i) : -INFINITY;
         const float lj = lane < n ? __ldcg(slots + lane * sf + kAttnMaxRows + i) : 0.f;
-        float acc[PER];
+        float gt[KP], acc[KP], va[JB][KP], vb[JB][KP];
 #pragma unroll
-        for (int k = 0; k < PER; ++k)
+        for (int k = 0; k < KP; ++k) {
+            gt[k] = __ldcg(a.gate + kb + lane + 32 * k);
             acc[k] = 0.f;
+        }
+        // slots j0 .. j0 + JB - 1 into a register batch
+        auto load = [&](float (&v)[JB][KP], int j0) {
+#pragma unroll
+            for (int jj = 0; jj < JB; ++jj)
+#pragma unroll
+                for (int k = 0; k < KP; ++k)
+                    v[jj][k] = j0 + jj < n ? __ldcg(col + (long long)(j0 + jj) * sf + 32 * k) : 0.f;
+        };
+        load(va, 0);
         float M = mj;
 #pragma unroll
         for (int o = 16; o; o >>= 1)
@@ -170,84 +211,68 @@ __device__ __forceinline__ void merge_slots(const AttnArgs &a, const float *slot
 #pragma unroll
         for (int o = 16; o; o >>= 1)
             L += __shfl_xor_sync(0xffffffffu, L, o);
-        constexpr int JB = PER >= 8 ? 2 : 4;     // slots whose loads are in flight together
-        for (int j0 = 0; j0 < n; j0 += JB) {
-            float v[JB][PER];
-#pragma unroll
-            for (int jj = 0; jj < JB; ++jj)
-#pragma unroll
-                for (int k = 0; k < PER; ++k)
-                    v[jj][k] = j0 + jj < n
-                                   ? __ldcg(slots + (j0 + jj) * sf + 2 * kAttnMaxRows + (long long)i * D +
-                                            lane + 32 * k)
-                                   : 0.f;
+        auto add = [&](const float (&v)[JB][KP], int j0) {
 #pragma unroll
             for (int jj = 0; jj < JB; ++jj) {
                 const float fj = __shfl_sync(0xffffffffu, f, (j0 + jj) & 31);
                 if (j0 + jj < n)
 #pragma unroll
-                    for (int k = 0; k < PER; ++k)
+                    for (int k = 0; k < KP; ++k)
                         acc[k] = fmaf(fj, v[jj][k], acc[k]);
             }
+        };
+        // two batches in flight: the next batch is requested before this one
+        // is added
+        for (int j0 = 0; j0 < n; j0 += 2 * JB) {
+            if (j0 + JB < n)
+                load(vb, j0 + JB);
+            add(va, j0);
+            if (j0 + JB >= n)
+                break;
+            if (j0 + 2 * JB < n)
+                load(va, j0 + 2 * JB);
+            add(vb, j0 + JB);
         }
-        if constexpr (!FINAL) {
+        const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-            for (int k = 0; k < PER; ++k)
-                out[2 * kAttnMaxRows + (long long)i * D + lane + 32 * k] = acc[k];
-            if (lane == 0) {
-                out[i] = M;
-                out[kAttnMaxRows + i] = L;
-            }
-        } else {
-            const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int k = 0; k < KP; ++k)
+            acc[k] *= inv;
+        if constexpr (VQ != 0) {
+            // the values were attended in their Walsh-Hadamard basis: H o / sqrt(d)
+            float x[8];
 #pragma unroll
-            for (int k = 0; k < PER; ++k)
-                acc[k] *= inv;
-            if (a.vq) {
-                // the values were attended in their Walsh-Hadamard basis: H o / sqrt(d)
-                float x[8];
+            for (int k = 0; k < 8; ++k)
+                x[k] = k < KP ? acc[k] : 0.f;
+            wht_warp(x, KP, lane);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    x[k] = k < PER ? acc[k] : 0.f;
-                wht_warp(x, PER, lane);
+            for (int k = 0; k < KP; ++k)
+                acc[k] = x[k] * a.inv_sqrt_d;
+        }
+        float hv[KP];
 #pragma unroll
-                for (int k = 0; k < PER; ++k)
-                    acc[k] = x[k] * a.inv_sqrt_d;
-            }
-            const int gqa = a.H / a.Hk;
-            const int h = it.kh * gqa + a.rb_h0[it.rb] + i / a.R, r = i % a.R;
-            const int m = it.b * a.R + r;
-            const long long Ktot = (long long)a.H * D;
-            const int gs = a.group_o, MP = 8 * a.NT;
-            float hv[PER];
+        for (int k = 0; k < KP; ++k) {
+            const int c = h * D + cb + lane + 32 * k;
+            const __half q = __float2half_rn(acc[k] * (1.f / (1.f + __expf(-gt[k]))));
+            a.x16[x16_offset(m, c, a.NT)] = q;
+            hv[k] = __half2float(q);
+            if (a.tap_attn)
+                a.tap_attn[kb + lane + 32 * k] = acc[k];
+        }
+        // group sums of the fp16 operand: groups of gs (32, 64 or 128, at most
+        // the part's width) consecutive columns, i.e. gs / 32 registers
+        float t = 0.f;
 #pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int c = lane + 32 * k;
-                const long long kk = (long long)h * D + c;
-                const float gt = a.gate[(long long)m * Ktot + kk];
-                const __half q = __float2half_rn(acc[k] * (1.f / (1.f + __expf(-gt))));
-                a.x16[x16_offset(m, (int)kk, a.NT)] = q;
-                hv[k] = __half2float(q);
-                if (a.tap_attn)
-                    a.tap_attn[(long long)m * Ktot + kk] = acc[k];
-            }
-            // group sums of the fp16 operand: groups of gs (32, 64 or 128 <= d)
-            // consecutive columns of the head, i.e. gs / 32 registers of the warp
-            const int rpg = gs / 32;
-            float t = 0.f;
+        for (int k = 0; k < KP; ++k) {
+            t += hv[k];
+            if ((k + 1) % rpg == 0) {
 #pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                t += hv[k];
-                if ((k + 1) % rpg == 0) {
-#pragma unroll
-                    for (int o = 16; o; o >>= 1)
-                        t += __shfl_xor_sync(0xffffffffu, t, o);
-                    if (lane == 0) {
-                        const int c0 = h * D + 32 * (k + 1 - rpg);
-                        a.xsum[((long long)(c0 >> 7) * (kKU / gs) + ((c0 & 127) / gs)) * MP + m] = t;
-                    }
-                    t = 0.f;
+                for (int o = 16; o; o >>= 1)
+                    t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (lane == 0) {
+                    const int c0 = h * D + cb + 32 * (k + 1 - rpg);
+                    a.xsum[((long long)(c0 >> 7) * (kKU / gs) + ((c0 & 127) / gs)) * MP + m] = t;
                 }
+                t = 0.f;
             }
         }
     }
@@ -270,7 +295,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     float *red_max = reinterpret_cast<float *>(smem + L::kRedMax);
     float *red_l = reinterpret_cast<float *>(smem + L::kRedL);
     long long *pi = reinterpret_cast<long long *>(smem + L::kPrefix);     // [33] first item
-    long long *pg = pi + 40;                                                // [33] first group
+    long long *uo = pi + 40;                // [33] unit offset of each sequence's first item
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBars);
     uint64_t *empty = full + L::kNStages;
     int *flags = reinterpret_cast<int *>(smem + L::kFlags);   // [0] abort [1..3] merge flags
@@ -302,34 +327,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     __syncthreads();
     // the chunk plan: cu units per chunk from the unchunked partition's unit
-    // count over the grid (at least min_units), then per sequence the chunks of
-    // each segment, the items (segment, chunk) and the level-1 merge groups
+    // count over split x the grid, at least min_units and at least the longest
+    // segment's units over kMaxChunks; then per sequence the chunks of each
+    // segment, the items (segment, chunk) and their unit offsets
     if (tid == 0) {
         long long uu = 0;
-        for (int b = 0; b < a.B; ++b)
+        int umax = 0;
+        for (int b = 0; b < a.B; ++b) {
             uu += (long long)ub[b] * a.Hk * a.nrb_u;
-        const long long per = (uu + gridDim.x - 1) / gridDim.x;
-        const int cu = (int)(per > a.min_units ? per : a.min_units);
-        long long ai = 0, ag = 0;
+            umax = max(umax, ub[b]);
+        }
+        const long long parts = (long long)a.split * gridDim.x;
+        const long long per = (uu + parts - 1) / parts;
+        int cu = (int)(per > a.min_units ? per : a.min_units);
+        cu = max(cu, (umax + kMaxChunks - 1) / kMaxChunks);
+        long long ai = 0, au = 0;
         for (int b = 0; b < a.B; ++b) {
             const int n = (ub[b] + cu - 1) / cu;
             nc[b] = n;
             pi[b] = ai;
-            pg[b] = ag;
+            uo[b] = au;
             ai += (long long)n * a.Hk * a.nrb;
-            ag += (long long)(n > kMaxFinal ? (n + kMergeGroup - 1) / kMergeGroup : 0) * a.Hk * a.nrb;
+            au += (long long)ub[b] * a.Hk * a.nrb;
         }
         pi[a.B] = ai;
-        pg[a.B] = ag;
+        uo[a.B] = au;
         flags[4] = cu;
     }
     __syncthreads();
-    const ChunkPlan cp{flags[4], ub, nc, pi, pg};
+    const ChunkPlan cp{flags[4], ub, nc, pi};
 
-    // contiguous item ranges over the grid (consecutive chunks of a segment in
-    // one CTA share its q rows)
-    const long long T = pi[a.B], c = blockIdx.x;
-    const long long beg = T * c / gridDim.x, end = T * (c + 1) / gridDim.x;
+    // contiguous item ranges balanced by units: CTA c takes the items that
+    // start in its share of the units (consecutive chunks of a segment in one
+    // CTA share its q rows)
+    const long long U = uo[a.B], c = blockIdx.x;
+    const long long beg = first_item_at(cp, uo, a.B, U * c / gridDim.x);
+    const long long end = first_item_at(cp, uo, a.B, U * (c + 1) / gridDim.x);
     volatile int *abort = flags;
 
     if (warp == kAttnWarps) {
@@ -449,16 +482,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             }
         } else {
-            for (int idx = tid; idx < MT * 16 * CH; idx += kAttnWarps * 32) {
-                const int i = idx / CH, cc = idx % CH;
-                uint4 v = make_uint4(0, 0, 0, 0);
+            // every load first (one round trip), then the stores
+            constexpr int NQ = (MT * 16 * CH + kAttnWarps * 32 - 1) / (kAttnWarps * 32);
+            uint4 qv[NQ];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const int idx = tid + q * kAttnWarps * 32, i = idx / CH, cc = idx % CH;
+                qv[q] = make_uint4(0, 0, 0, 0);
                 if (i < nrows) {
                     const int hl = i / a.R, r = i % a.R;
-                    const __nv_bfloat16 *src =
-                        a.qn + (((long long)p.b * a.R + r) * a.H + h0 + hl) * D + cc * 8;
-                    v = *reinterpret_cast<const uint4 *>(src);
+                    qv[q] = *reinterpret_cast<const uint4 *>(
+                        a.qn + (((long long)p.b * a.R + r) * a.H + h0 + hl) * D + cc * 8);
                 }
-                *reinterpret_cast<uint4 *>(qs + i * (D * 2) + ((cc ^ (i & 7)) << 4)) = v;
+            }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const int idx = tid + q * kAttnWarps * 32, i = idx / CH, cc = idx % CH;
+                if (idx < MT * 16 * CH)
+                    *reinterpret_cast<uint4 *>(qs + i * (D * 2) + ((cc ^ (i & 7)) << 4)) = qv[q];
             }
         }
         named_bar_sync(1, kAttnWarps * 32);
@@ -738,9 +779,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mbar_arrive(&empty[slot]);
         }
 
-        // ---- partial (m, l, O) of this chunk into its slot (valid rows only)
-        const long long sf = attn_slot_floats(D);
-        float *part = a.ws + item * sf;
+        // the row sums of l: per warp (its tokens), then over the warps in order
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -751,85 +790,121 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (cq == 0)
                     red_l[warp * 64 + mt * 16 + g + 8 * hr] = l;
             }
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int j = 0; j < DB; ++j) {
-                const int col = (warp * DB + j) * 8 + 2 * cq;
-                const int r0 = mt * 16 + g;
-                if (r0 < nrows)
-                    *reinterpret_cast<float2 *>(part + 2 * kAttnMaxRows + (long long)r0 * D + col) =
-                        make_float2(O[mt][j][0], O[mt][j][1]);
-                if (r0 + 8 < nrows)
-                    *reinterpret_cast<float2 *>(part + 2 * kAttnMaxRows + (long long)(r0 + 8) * D +
-                                                col) = make_float2(O[mt][j][2], O[mt][j][3]);
-            }
-        named_bar_sync(1, kAttnWarps * 32);
-        if (warp == 0 && cq == 0) {
+        const int n = cp.nc[p.b];
+        if (VQ == 0 && n == 1) {
+            // ---- the segment's only chunk: normalize, gate and write the o_proj
+            //      operand from the accumulators (the same products as a one-slot
+            //      merge: o * (1 / l)); the gate is requested before the barrier
+            const long long Ktot = (long long)a.H * D;
+            float2 gv[MT][DB][2];
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
-                    const int i = mt * 16 + g + 8 * hr;
+                    const int r = mt * 16 + g + 8 * hr;
+                    const long long base = ((long long)p.b * a.R + r % a.R) * Ktot +
+                                           (long long)(h0 + r / a.R) * D;
+#pragma unroll
+                    for (int j = 0; j < DB; ++j)
+                        gv[mt][j][hr] = r < nrows ? __ldcg(reinterpret_cast<const float2 *>(
+                                                        a.gate + base + (warp * DB + j) * 8 + 2 * cq))
+                                                  : make_float2(0.f, 0.f);
+                }
+            named_bar_sync(1, kAttnWarps * 32);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int r = mt * 16 + g + 8 * hr;
                     float l = 0.f;
 #pragma unroll
                     for (int w2 = 0; w2 < kAttnWarps; ++w2)
-                        l += red_l[w2 * 64 + i];
-                    part[i] = m_run[mt][hr];
-                    part[kAttnMaxRows + i] = l;
+                        l += red_l[w2 * 64 + r];
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    const int m = p.b * a.R + r % a.R, h = h0 + r / a.R;
+                    float rs = 0.f;
+#pragma unroll
+                    for (int j = 0; j < DB; ++j) {
+                        const int c = h * D + (warp * DB + j) * 8 + 2 * cq;
+                        const float o0 = O[mt][j][2 * hr] * inv, o1 = O[mt][j][2 * hr + 1] * inv;
+                        const __half q0 = __float2half_rn(o0 * (1.f / (1.f + __expf(-gv[mt][j][hr].x))));
+                        const __half q1 = __float2half_rn(o1 * (1.f / (1.f + __expf(-gv[mt][j][hr].y))));
+                        if (r < nrows) {
+                            *reinterpret_cast<__half2 *>(a.x16 + x16_offset(m, c, a.NT)) =
+                                __halves2half2(q0, q1);
+                            if (a.tap_attn)
+                                *reinterpret_cast<float2 *>(a.tap_attn + (long long)m * Ktot + c) =
+                                    make_float2(o0, o1);
+                        }
+                        rs += __half2float(q0) + __half2float(q1);
+                    }
+                    rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+                    rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+                    if (cq == 0)
+                        red_max[warp * 64 + r] = rs;     // this warp's columns of row r
                 }
-        }
-        // red_l is reused by the next item: keep warp 0's reads before new writes
-        __threadfence();
-        named_bar_sync(1, kAttnWarps * 32);
+            named_bar_sync(1, kAttnWarps * 32);
+            // group sums of the fp16 operand: a group of gs columns is the column
+            // slices of gs / (8 DB) consecutive warps, added in warp order
+            const int gs = a.group_o, ng = D / gs, wpg = gs / (8 * DB), MP = 8 * a.NT;
+            for (int idx = tid; idx < nrows * ng; idx += kAttnWarps * 32) {
+                const int r = idx / ng, gi = idx % ng;
+                float t = 0.f;
+                for (int w2 = gi * wpg; w2 < (gi + 1) * wpg; ++w2)
+                    t += red_max[w2 * 64 + r];
+                const int m = p.b * a.R + r % a.R, c0 = (h0 + r / a.R) * D + gi * gs;
+                a.xsum[((long long)(c0 >> 7) * (kKU / gs) + ((c0 & 127) / gs)) * MP + m] = t;
+            }
+        } else {
+            // ---- partial (m, l, O) of this chunk into its slot (valid rows only)
+            const long long sf = attn_slot_floats(D);
+            float *part = a.ws + item * sf;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int j = 0; j < DB; ++j) {
+                    const int col = (warp * DB + j) * 8 + 2 * cq;
+                    const int r0 = mt * 16 + g;
+                    if (r0 < nrows)
+                        *reinterpret_cast<float2 *>(part + 2 * kAttnMaxRows + (long long)r0 * D + col) =
+                            make_float2(O[mt][j][0], O[mt][j][1]);
+                    if (r0 + 8 < nrows)
+                        *reinterpret_cast<float2 *>(part + 2 * kAttnMaxRows + (long long)(r0 + 8) * D +
+                                                    col) = make_float2(O[mt][j][2], O[mt][j][3]);
+                }
+            named_bar_sync(1, kAttnWarps * 32);
+            if (warp == 0 && cq == 0) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int i = mt * 16 + g + 8 * hr;
+                        float l = 0.f;
+#pragma unroll
+                        for (int w2 = 0; w2 < kAttnWarps; ++w2)
+                            l += red_l[w2 * 64 + i];
+                        part[i] = m_run[mt][hr];
+                        part[kAttnMaxRows + i] = l;
+                    }
+            }
+            named_bar_sync(1, kAttnWarps * 32);
 
-        // ---- merge: the CTA whose chunk completes a group of kMergeGroup chunks
-        //      (segments of more than kMaxFinal chunks) combines the group into
-        //      its level-1 slot; the CTA that completes the segment combines its
-        //      chunk (or level-1) slots, applies the gate and writes the o_proj
-        //      operand.  Completion is counted with atomics after a fence; the
-        //      last user of a counter resets it for the next step.
-        const int n = cp.nc[p.b];
-        const int ng = n > kMaxFinal ? (n + kMergeGroup - 1) / kMergeGroup : 0;
-        const long long sl = (long long)p.kh * a.nrb + p.rb;   // segment within the sequence
-        const int grp = p.chunk / kMergeGroup;
-        const long long gidx = cp.pg[p.b] + sl * ng + grp;
-        if (tid == 0) {
-            int lg = 0, ls = 0;
-            if (ng == 0) {
-                ls = atomicAdd(&a.cnt_seg[p.seg], 1u) == (unsigned)(n - 1);
-            } else {
-                const int gs = min(kMergeGroup, n - grp * kMergeGroup);
-                lg = atomicAdd(&a.cnt_grp[gidx], 1u) == (unsigned)(gs - 1);
-            }
-            flags[1] = lg;
-            flags[2] = ls;
-        }
-        named_bar_sync(1, kAttnWarps * 32);
-        if (flags[1]) {
-            __threadfence();
-            const int gs = min(kMergeGroup, n - grp * kMergeGroup);
-            merge_slots<DB, false>(a, a.ws + (p.first + (long long)grp * kMergeGroup) * sf, sf, gs,
-                                   nrows, a.ws1 + gidx * sf, p, warp, lane);
-            __threadfence();
-            named_bar_sync(1, kAttnWarps * 32);
-            if (tid == 0) {
-                a.cnt_grp[gidx] = 0u;
-                flags[2] = atomicAdd(&a.cnt_seg[p.seg], 1u) == (unsigned)(ng - 1);
-            }
-            named_bar_sync(1, kAttnWarps * 32);
-        }
-        if (flags[2]) {
-            __threadfence();
-            if (ng == 0)
-                merge_slots<DB, true>(a, a.ws + p.first * sf, sf, n, nrows, nullptr, p, warp, lane);
-            else
-                merge_slots<DB, true>(a, a.ws1 + (cp.pg[p.b] + sl * ng) * sf, sf, ng, nrows,
-                                      nullptr, p, warp, lane);
+            // ---- merge: the CTA whose chunk completes its segment combines the
+            //      segment's chunk partials, applies the gate and writes the o_proj
+            //      operand.  Completion is counted by one thread with an acq_rel
+            //      atomic after the barrier above (which orders every thread's
+            //      partial stores before it); the last user resets the counter for
+            //      the next step.
             if (tid == 0)
-                a.cnt_seg[p.seg] = 0u;
+                flags[2] = atom_add_acq_rel_gpu(&a.cnt_seg[p.seg], 1u) == (unsigned)(n - 1);
+            named_bar_sync(1, kAttnWarps * 32);
+            if (flags[2]) {
+                merge_final<DB, VQ>(a, a.ws + p.first * sf, sf, n, nrows, p, warp, lane);
+                if (tid == 0)
+                    a.cnt_seg[p.seg] = 0u;
+            }
         }
-        // flags[1..2] are rewritten by the next item
+        // flags[2] is rewritten by the next item
         named_bar_sync(1, kAttnWarps * 32);
     }
 }
@@ -854,6 +929,6 @@ static cudaError_t launch_attn_t(const AttnArgs &a, const CUtensorMap &kmap,
 
 // the (MT, DB) instances: MT = 16-row tiles of a segment's rows, DB = d / 64
 #define GATTN_ATTN_INSTANCES(X)                                                                    \
-    X(1, 1) X(2, 1) X(3, 1) X(4, 1) X(1, 2) X(2, 2) X(3, 2) X(4, 2) X(1, 4) X(2, 4) X(3, 4) X(4, 4)
+    X(1, 1) X(2, 1) X(1, 2) X(2, 2) X(1, 4) X(2, 4)
 
 }  // namespace gattn

@@ -121,6 +121,17 @@ __device__ __forceinline__ bool mbar_wait_all(uint64_t *bar, uint32_t parity, un
     return true;
 }
 
+// Atomic add at GPU scope with acquire-release semantics; returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
 // ------------------------------------------------------------- TMA copies
 
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
@@ -188,10 +199,12 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
 // Hardware barrier over every thread of the cluster (all CTAs of a cluster are
 // co-scheduled, so this cannot wait on a CTA that is not running).  Release /
 // acquire: shared-memory writes before it are visible to remote reads after it.
+// The cluster barriers here are the non-.aligned forms: a thread may reach them
+// from code its warp entered divergently.
 __device__ __forceinline__ void cluster_sync()
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.release;\n\t"
+                 "barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // Address of the same shared-memory offset in CTA `rank` of the cluster.
@@ -207,17 +220,17 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank)
 // signalled by other CTAs of the cluster after the wait.
 __device__ __forceinline__ void cluster_arrive_relaxed()
 {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_arrive()
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_wait()
 {
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // Asynchronous stores into another CTA's shared memory (addresses from

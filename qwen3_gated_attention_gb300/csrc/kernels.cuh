@@ -220,6 +220,10 @@ constexpr int kAttnUnit = 16;          // tokens per stream-K unit
 constexpr int kAttnTile = 64;         // tokens per pipeline stage (<= 64: the P tile width)
 constexpr int kAttnStages = 4;        // pipeline stages, at most (fewer when shared memory is short)
 constexpr int kMaxRowBlocks = 64;
+// query rows an attention row block holds, at most (more when one head has more
+// rows): one 16-row MMA tile, so a tile's products stay short and a KV group's
+// rows spread over more CTAs
+constexpr int kRowBlockRows = 16;
 constexpr int kAttnMaxRows = 64;       // query rows per segment
 
 // floats per attention partial slot: m[64], l[64], O[64][d]
@@ -236,9 +240,9 @@ struct AttnArgs {
     int rb_nh[kMaxRowBlocks];    // heads of each row block
     float scale_log2;            // log2(e) / sqrt(d)
     int min_units;               // minimum 16-token units per chunk
+    int split;                   // chunks per CTA aimed at (balance against per-chunk work)
     float *ws;                   // chunk partials, attn_slot_floats(d) per item
-    float *ws1;                  // level-1 merge slots
-    unsigned *cnt_seg, *cnt_grp; // completion counters per segment / level-1 group (zero between steps)
+    unsigned *cnt_seg;           // completion counter per segment (zero between steps)
     // o_proj operand
     __half *x16;
     float *xsum;
