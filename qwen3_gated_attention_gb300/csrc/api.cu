@@ -158,6 +158,7 @@ int attn_row_blocks(int q_len, int H, int Hk, int enabled, int *rb_h0, int *rb_n
 
 constexpr int kAttnMinUnits = 4;     // 16-token units per attention chunk, at least
 constexpr int kAttnSplit = 8;        // attention chunks per CTA aimed at
+constexpr int kInKernelMergeRows = 8; // attention segments up to this many rows merge in place
 
 // Upper bound of the attention items (segment chunks) of a step: the chunk
 // length is at least the unchunked partition's units over split x grid, so the
@@ -941,6 +942,11 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     t.cnt_seg = L->cnt_seg;
     t.min_units = kAttnMinUnits;
     t.split = kAttnSplit;
+    t.attn_grid = L->attn_grid;
+    // segments of more than kInKernelMergeRows rows: their merges run in a
+    // launch of their own, spread over many CTAs (one CTA merging a segment's
+    // rows times chunks would be the long pole); smaller ones merge in place
+    t.merge_sep = max_rows > kInKernelMergeRows ? (max_rows + 3) / 4 : 0;
     t.x16 = L->x16_o;
     t.xsum = L->xsum_o;
     t.NT = NT;
@@ -987,6 +993,12 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     else
         CUDA_TRY(launch_attn(MT, c.head_dim / 64, t, kv->kmap, kv->vmap, L->attn_grid, pdl, s));
     launched(GATTN_KERNEL_ATTN);
+    if (t.merge_sep) {
+        CUDA_TRY(mark(launches));
+        CUDA_TRY(launch_attn_merge(c.head_dim / 64, kv->kturbo ? 2 : kv->turbo ? 1 : 0, t,
+                                   batch * c.num_kv_heads * nrb, pdl, s));
+        launched(GATTN_KERNEL_MERGE);
+    }
     CUDA_TRY(mark(launches));
 
     // 4. o_proj

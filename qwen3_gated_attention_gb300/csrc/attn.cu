@@ -35,6 +35,19 @@ cudaError_t launch_attn(int MT, int DB, const AttnArgs &a, const CUtensorMap &km
     return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_attn_merge(int DB, int vq, const AttnArgs &a, int segments, bool pdl,
+                              cudaStream_t s)
+{
+#define GATTN_MERGE(db, v)                                                                         \
+    if (DB == db && vq == v)                                                                       \
+        return launch_attn_merge_t<db, v>(a, segments, pdl, s);
+    GATTN_MERGE(1, 0) GATTN_MERGE(2, 0) GATTN_MERGE(4, 0)
+    GATTN_MERGE(1, 1) GATTN_MERGE(2, 1) GATTN_MERGE(4, 1)
+    GATTN_MERGE(1, 2) GATTN_MERGE(2, 2) GATTN_MERGE(4, 2)
+#undef GATTN_MERGE
+    return cudaErrorInvalidValue;
+}
+
 int attn_smem_bytes(int MT, int DB)
 {
 #define GATTN_CASE(mt, db)                                                                         \

@@ -100,6 +100,10 @@ __device__ __forceinline__ void turbo_item_store(uint32_t dst, const TurboItem &
     }
 }
 
+// Chunks per segment, at most: the chunk length grows for longer segments so
+// that one merge combines every partial of a segment (lane j holds chunk j).
+constexpr int kMaxChunks = 32;
+
 // The chunk plan of a step, the same in every CTA: sequence b's segments (one
 // per KV head and row block) are cut into nc[b] <= kMaxChunks chunks of cu
 // 16-token units.  cu depends only on the lengths and on the row-block count of
@@ -138,6 +142,51 @@ __device__ __forceinline__ Item item_of(const ChunkPlan &cp, int B, int Hk, int 
     return it;
 }
 
+// The chunk plan of a step for an attention launch of `grid` CTAs (every CTA
+// of that launch and of the merge launch computes the same one): per sequence
+// the units ub, the chunks per segment nc, the first item pi and the first
+// item's unit offset uo (pi[B], uo[B]: totals), in shared memory; returns cu.
+// cu units per chunk: the unchunked partition's unit count over split x the
+// grid, at least min_units and at least the longest segment's units over
+// kMaxChunks.  Called by every thread of the block (two barriers).
+__device__ __forceinline__ int chunk_plan(const AttnArgs &a, int grid, int *ub, int *nc,
+                                          long long *pi, long long *uo, int *cu_slot)
+{
+    const int tid = threadIdx.x;
+    if (tid < a.B) {
+        const int p0 = a.cache_pos[tid];
+        const bool valid = p0 >= 0 && p0 + a.R <= a.cap;
+        ub[tid] = valid ? (p0 + a.R + kAttnUnit - 1) / kAttnUnit : 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        long long uu = 0;
+        int umax = 0;
+        for (int b = 0; b < a.B; ++b) {
+            uu += (long long)ub[b] * a.Hk * a.nrb_u;
+            umax = max(umax, ub[b]);
+        }
+        const long long parts = (long long)a.split * grid;
+        const long long per = (uu + parts - 1) / parts;
+        int cu = (int)(per > a.min_units ? per : a.min_units);
+        cu = max(cu, (umax + kMaxChunks - 1) / kMaxChunks);
+        long long ai = 0, au = 0;
+        for (int b = 0; b < a.B; ++b) {
+            const int n = (ub[b] + cu - 1) / cu;
+            nc[b] = n;
+            pi[b] = ai;
+            uo[b] = au;
+            ai += (long long)n * a.Hk * a.nrb;
+            au += (long long)ub[b] * a.Hk * a.nrb;
+        }
+        pi[a.B] = ai;
+        uo[a.B] = au;
+        *cu_slot = cu;
+    }
+    __syncthreads();
+    return *cu_slot;
+}
+
 // The first item (in item order) that starts at unit offset x or later; uo[b]
 // is the unit offset of sequence b's first item (uo[B]: all units).
 __device__ __forceinline__ long long first_item_at(const ChunkPlan &cp, const long long *uo, int B,
@@ -155,12 +204,9 @@ __device__ __forceinline__ long long first_item_at(const ChunkPlan &cp, const lo
     return cp.pi[b] + sl * cp.nc[b] + (r + cp.cu - 1) / cp.cu;
 }
 
-// Chunks per segment, at most: the chunk length grows for longer segments so
-// that one merge combines every partial of a segment (lane j holds chunk j).
-constexpr int kMaxChunks = 32;
-
 // Merge the n (<= kMaxChunks) chunk partials of a segment (slot j: m[64] l[64]
-// O[64][D], sf floats apart) into the gated o_proj operand of its nrows rows.
+// O[64][D], sf floats apart) into the gated o_proj operand of its rows
+// [row0, row0 + nrows).
 // A work unit is one row's part of NP parts of D / NP columns (one part when
 // the values are rotated back, which needs the whole row in one warp); lane j
 // holds slot j's (m, l) and the lanes share the part's columns (column
@@ -170,7 +216,8 @@ constexpr int kMaxChunks = 32;
 // attention tap, the fp16 o_proj operand and its group sums.
 template <int DB, int VQ>
 __device__ __forceinline__ void merge_final(const AttnArgs &a, const float *slots, long long sf,
-                                            int n, int nrows, const Item &it, int warp, int lane)
+                                            int n, int nrows, int row0, const Item &it, int warp,
+                                            int lane)
 {
     constexpr int D = DB * 64, PER = D / 32;
     constexpr int NP = (VQ != 0 || PER < 4) ? 1 : 2;
@@ -180,7 +227,7 @@ __device__ __forceinline__ void merge_final(const AttnArgs &a, const float *slot
     const long long Ktot = (long long)a.H * D;
     const int gs = a.group_o, MP = 8 * a.NT, rpg = gs / 32;
     for (int w = warp; w < nrows * NP; w += kAttnWarps) {
-        const int i = w / NP, cb = (w % NP) * (D / NP);
+        const int i = row0 + w / NP, cb = (w % NP) * (D / NP);
         const int h = it.kh * gqa + a.rb_h0[it.rb] + i / a.R, r = i % a.R;
         const int m = it.b * a.R + r;
         const long long kb = (long long)m * Ktot + (long long)h * D + cb;
@@ -320,42 +367,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         flags[1] = 0;
         fence_mbar_init();
     }
-    if (tid < a.B) {
-        const int p0 = a.cache_pos[tid];
-        const bool valid = p0 >= 0 && p0 + a.R <= a.cap;
-        ub[tid] = valid ? (p0 + a.R + kAttnUnit - 1) / kAttnUnit : 0;
-    }
-    __syncthreads();
-    // the chunk plan: cu units per chunk from the unchunked partition's unit
-    // count over split x the grid, at least min_units and at least the longest
-    // segment's units over kMaxChunks; then per sequence the chunks of each
-    // segment, the items (segment, chunk) and their unit offsets
-    if (tid == 0) {
-        long long uu = 0;
-        int umax = 0;
-        for (int b = 0; b < a.B; ++b) {
-            uu += (long long)ub[b] * a.Hk * a.nrb_u;
-            umax = max(umax, ub[b]);
-        }
-        const long long parts = (long long)a.split * gridDim.x;
-        const long long per = (uu + parts - 1) / parts;
-        int cu = (int)(per > a.min_units ? per : a.min_units);
-        cu = max(cu, (umax + kMaxChunks - 1) / kMaxChunks);
-        long long ai = 0, au = 0;
-        for (int b = 0; b < a.B; ++b) {
-            const int n = (ub[b] + cu - 1) / cu;
-            nc[b] = n;
-            pi[b] = ai;
-            uo[b] = au;
-            ai += (long long)n * a.Hk * a.nrb;
-            au += (long long)ub[b] * a.Hk * a.nrb;
-        }
-        pi[a.B] = ai;
-        uo[a.B] = au;
-        flags[4] = cu;
-    }
-    __syncthreads();
-    const ChunkPlan cp{flags[4], ub, nc, pi};
+    const int cu = chunk_plan(a, gridDim.x, ub, nc, pi, uo, &flags[4]);
+    const ChunkPlan cp{cu, ub, nc, pi};
 
     // contiguous item ranges balanced by units: CTA c takes the items that
     // start in its share of the units (consecutive chunks of a segment in one
@@ -444,6 +457,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
 
     // --------------------------------------------------------------- consumers
+    // the arguments read after the wait are brought into the constant cache
+    // while waiting
+    if (tid == 0)
+        reinterpret_cast<volatile unsigned *>(flags)[5] = arg_fold(a);
     pdl_wait();                 // q rows come from the q|k|v projection
     const int g = lane >> 2, cq = lane & 3;
     long long it = 0, qseg = -1;
@@ -887,25 +904,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         part[kAttnMaxRows + i] = l;
                     }
             }
-            named_bar_sync(1, kAttnWarps * 32);
-
-            // ---- merge: the CTA whose chunk completes its segment combines the
-            //      segment's chunk partials, applies the gate and writes the o_proj
-            //      operand.  Completion is counted by one thread with an acq_rel
-            //      atomic after the barrier above (which orders every thread's
-            //      partial stores before it); the last user resets the counter for
-            //      the next step.
-            if (tid == 0)
-                flags[2] = atom_add_acq_rel_gpu(&a.cnt_seg[p.seg], 1u) == (unsigned)(n - 1);
-            named_bar_sync(1, kAttnWarps * 32);
-            if (flags[2]) {
-                merge_final<DB, VQ>(a, a.ws + p.first * sf, sf, n, nrows, p, warp, lane);
-                if (tid == 0)
-                    a.cnt_seg[p.seg] = 0u;
-            }
         }
-        // flags[2] is rewritten by the next item
+        // red_l and red_max are rewritten by the next item
         named_bar_sync(1, kAttnWarps * 32);
+    }
+    if (a.merge_sep)
+        return;                 // the merge launch that follows combines the partials
+
+    // ---- completion, once every partial of this CTA is stored (the barrier
+    //      above orders them before the atomics, whose release covers them):
+    //      one acq_rel ticket per chunk item, all taken together so that their
+    //      round trips overlap and none stalls the tile stream; the CTA whose
+    //      ticket completes a segment merges its chunk partials, applies the
+    //      gate, writes the o_proj operand and resets the counter for the next
+    //      step.  Segments of one chunk were finished above.
+    int *mlist = reinterpret_cast<int *>(red_l);   // items whose segment this CTA merges
+    constexpr int kRound = kAttnWarps * 32;        // items per round (the list holds 512)
+    const long long sf = attn_slot_floats(D);
+    for (long long base = beg; base < end; base += kRound) {
+        if (tid == 0)
+            flags[6] = 0;
+        named_bar_sync(1, kAttnWarps * 32);
+        if (base + tid < end) {
+            const Item p = item_of(cp, a.B, a.Hk, a.nrb, base + tid);
+            const int n = cp.nc[p.b];
+            if (!(VQ == 0 && n == 1) &&
+                atom_add_acq_rel_gpu(&a.cnt_seg[p.seg], 1u) == (unsigned)(n - 1))
+                mlist[atomicAdd(&flags[6], 1)] = tid;
+        }
+        named_bar_sync(1, kAttnWarps * 32);
+        const int nmerge = flags[6];
+        for (int k = 0; k < nmerge; ++k) {
+            const Item p = item_of(cp, a.B, a.Hk, a.nrb, base + mlist[k]);
+            merge_final<DB, VQ>(a, a.ws + p.first * sf, sf, cp.nc[p.b], a.rb_nh[p.rb] * a.R, 0,
+                                p, warp, lane);
+            if (tid == 0)
+                a.cnt_seg[p.seg] = 0u;
+        }
+        named_bar_sync(1, kAttnWarps * 32);     // mlist and flags[6] are reused
     }
 }
 
@@ -928,6 +964,60 @@ static cudaError_t launch_attn_t(const AttnArgs &a, const CUtensorMap &kmap,
 }
 
 // the (MT, DB) instances: MT = 16-row tiles of a segment's rows, DB = d / 64
+// Rows of a segment one CTA of the merge launch finishes.
+constexpr int kMergeRows = 4;
+
+// The merge launch that follows the attention launch when segments have many
+// rows (merge_sep slices of 4 rows per segment): CTA (segment, slice) merges
+// rows [4 slice, 4 slice + 4) of
+// the segment's chunk partials (merge_final, the same code and order as the
+// merge inside the attention kernel), so the merges of large segments run on
+// many SMs instead of the one CTA that completes the segment.
+template <int DB, int VQ>
+__global__ void __launch_bounds__(kAttnWarps * 32) attn_merge_kernel(const AttnArgs a)
+{
+    __shared__ int ub[32], nc[32], cu_slot;
+    __shared__ long long pi[33], uo[33];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the o_proj launch may start streaming its weights at once
+    pdl_launch_dependents();
+    chunk_plan(a, a.attn_grid, ub, nc, pi, uo, &cu_slot);
+    pdl_wait();                 // the chunk partials come from the attention launch
+    const int slices = a.merge_sep;
+    const long long seg = blockIdx.x / slices;
+    const int sl = blockIdx.x % slices;
+    Item p;
+    p.rb = (int)(seg % a.nrb);
+    p.kh = (int)((seg / a.nrb) % a.Hk);
+    p.b = (int)(seg / ((long long)a.nrb * a.Hk));
+    p.seg = seg;
+    const int n = nc[p.b], nrows = a.rb_nh[p.rb] * a.R, row0 = sl * kMergeRows;
+    if (n == 0 || (VQ == 0 && n == 1) || row0 >= nrows)
+        return;
+    p.chunk = 0;
+    p.first = pi[p.b] + ((long long)p.kh * a.nrb + p.rb) * n;
+    p.u0 = p.u1 = 0;
+    const long long sf = attn_slot_floats(DB * 64);
+    merge_final<DB, VQ>(a, a.ws + p.first * sf, sf, n, min(kMergeRows, nrows - row0), row0, p,
+                        warp, lane);
+}
+
+template <int DB, int VQ>
+static cudaError_t launch_attn_merge_t(const AttnArgs &a, int segments, bool pdl, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(segments * a.merge_sep);
+    cfg.blockDim = dim3(kAttnWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_merge_kernel<DB, VQ>, a);
+}
+
 #define GATTN_ATTN_INSTANCES(X)                                                                    \
     X(1, 1) X(2, 1) X(1, 2) X(2, 2) X(1, 4) X(2, 4)
 

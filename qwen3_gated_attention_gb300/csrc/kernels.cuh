@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
 #include "turbo.cuh"
 
 struct gattn_layer;
@@ -105,6 +106,15 @@ struct ProjArgs {
     unsigned *status;
 };
 
+#ifdef __CUDACC__
+__device__ __forceinline__ unsigned arg_fold(const ProjArgs &a)
+{
+    return arg_fold(a.w, a.x16, a.xsum, a.nrb, a.nku, a.N, a.M, a.group, a.unit_bytes, a.step_bytes,
+                    a.stage_bytes, a.stages, a.rbc, a.ks, a.eb_rows, a.xsplit, a.recv_cap,
+                    a.xtab_bytes, a.xraw, a.x_f32, a.wait_ns, a.withhold, a.status);
+}
+#endif
+
 // qkv epilogue: per head block, RMSNorm + RoPE + bf16 append / q and gate outputs
 struct EpiQKV {
     int R;                         // q_len; column m is sequence m / R, row m % R
@@ -130,6 +140,21 @@ struct EpiQKV {
     TurboTables tq;
 };
 
+#ifdef __CUDACC__
+__device__ __forceinline__ unsigned arg_fold(const EpiQKV &e)
+{
+    unsigned h = arg_fold(e.R, e.H, e.Hk, e.d, e.rd, e.Nq, e.Nkv, e.cache_pos, e.cap, e.kc, e.vc,
+                          e.st_tok, e.st_head, e.st_batch, e.q_norm, e.k_norm, e.eps, e.inv_freq2,
+                          e.qn, e.gate, e.tap_y, e.vq_codes, e.vq_scales, e.cq_head, e.cq_batch,
+                          e.sq_head, e.sq_batch, e.kq_codes, e.kq_scales, e.kcq_head, e.kcq_batch,
+                          e.ksq_head, e.ksq_batch, e.tq.inv_sqrt_d);
+#pragma unroll
+    for (int i = 0; i < 16; i += 4)
+        h ^= arg_fold(e.tq.lv[i], e.tq.th[i < 15 ? i : 14]);
+    return h;
+}
+#endif
+
 struct EpiO {
     int R;
     const int *cache_pos;
@@ -145,6 +170,14 @@ struct EpiO {
     float *ss_part;                // [grid][M] each CTA's sums of squares of its stored rows
     unsigned *ticket;              // CTAs arrived; zero between launches
 };
+
+#ifdef __CUDACC__
+__device__ __forceinline__ unsigned arg_fold(const EpiO &e)
+{
+    return arg_fold(e.R, e.cache_pos, e.cap, e.out, e.resid, e.resid_f32, e.post_w, e.out_n, e.eps,
+                    e.ss_part, e.ticket);
+}
+#endif
 
 // the post-norm rides in the o_proj launch up to this many output elements
 // (one CTA normalizes every row); larger steps launch postnorm_kernel
@@ -241,6 +274,10 @@ struct AttnArgs {
     float scale_log2;            // log2(e) / sqrt(d)
     int min_units;               // minimum 16-token units per chunk
     int split;                   // chunks per CTA aimed at (balance against per-chunk work)
+    int attn_grid;               // CTAs of the attention launch (the chunk plan depends on it)
+    // 0: the attention launch merges each segment's chunk partials; > 0: a
+    // merge launch follows, with this many 4-row slices per segment
+    int merge_sep;
     float *ws;                   // chunk partials, attn_slot_floats(d) per item
     unsigned *cnt_seg;           // completion counter per segment (zero between steps)
     // o_proj operand
@@ -265,8 +302,30 @@ struct AttnArgs {
     long long mask_row, mask_head, mask_batch;
 };
 
+#ifdef __CUDACC__
+__device__ __forceinline__ unsigned arg_fold(const AttnArgs &a)
+{
+    unsigned h = arg_fold(a.qn, a.gate, a.cache_pos, a.B, a.R, a.H, a.Hk, a.d, a.cap, a.nrb, a.nrb_u,
+                          a.scale_log2, a.min_units, a.split, a.attn_grid, a.merge_sep, a.ws,
+                          a.cnt_seg, a.x16, a.xsum, a.NT,
+                          a.group_o, a.tap_attn, a.status, a.vq, a.vq_codes, a.vq_scales,
+                          a.cq_head, a.cq_batch, a.sq_head, a.sq_batch, a.kq_codes, a.kq_scales,
+                          a.kcq_head, a.kcq_batch, a.ksq_head, a.ksq_batch, a.vq_tl[0], a.vq_tl[1],
+                          a.vq_th[0], a.vq_th[1], a.inv_sqrt_d, a.mask, a.mask_heads, a.mask_len,
+                          a.mask_row, a.mask_head, a.mask_batch);
+#pragma unroll
+    for (int i = 0; i < kMaxRowBlocks; i += 4)
+        h ^= arg_fold(a.rb_h0[i], a.rb_nh[i]);
+    return h;
+}
+#endif
+
 cudaError_t launch_attn(int MT, int DB, const AttnArgs &a, const CUtensorMap &kmap,
                         const CUtensorMap &vmap, int grid, bool pdl, cudaStream_t s);
+// the merge launch after an attention launch with merge_sep > 0 (segments =
+// B * Hk * nrb); vq: the cache format of the attention instance (0, 1, 2)
+cudaError_t launch_attn_merge(int DB, int vq, const AttnArgs &a, int segments, bool pdl,
+                              cudaStream_t s);
 // the Bf16KTurbo4V instances (attn_vq.cu); vmap is unused there
 cudaError_t launch_attn_vq(int MT, int DB, const AttnArgs &a, const CUtensorMap &kmap, int grid,
                            bool pdl, cudaStream_t s);

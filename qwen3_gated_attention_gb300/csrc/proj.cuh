@@ -200,22 +200,25 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
     // up to kWR / heads of this CTA's columns at a time, so that every warp has
     // a (column, head) to finish even when the cluster spans a single head
     const int mper = heads >= kWR ? 1 : kWR / heads;
+    const int ebr = a.eb_rows, ks = a.ks, P = a.xsplit ? 2 : 1;
     for (int m0 = rank; m0 < a.M; m0 += csize * mper) {
-        for (int idx = tid; idx < mper * a.eb_rows; idx += kWR * 32) {
-            const int j = idx / a.eb_rows, r = idx - j * a.eb_rows;
-            const int m = m0 + j * csize;
-            if (m < a.M) {
-                const int P = a.xsplit ? 2 : 1, lc = m / csize;
-                const float *hi = sm.recv + (long long)(lc * P) * a.ks * a.eb_rows + r;
-                const float *lo = hi + (long long)a.ks * a.eb_rows;
-                float v = 0.f;
-                for (int k = 0; k < a.ks; ++k) {
-                    v += hi[(long long)k * a.eb_rows];
-                    if (a.xsplit)
-                        v += lo[(long long)k * a.eb_rows];
+        // the pass's columns m0 + j csize, j < nm (only those that exist)
+        const int nm = min(mper, (a.M - m0 + csize - 1) / csize);
+        for (int idx = tid; idx < nm * ebr; idx += kWR * 32) {
+            const int j = idx / ebr, r = idx - j * ebr;
+            const int lc = m0 / csize + j;              // (m0 + j csize) / csize
+            const float *hi = sm.recv + (lc * P * ks) * ebr + r;
+            float v = 0.f;
+            if (P == 1) {
+                for (int k = 0; k < ks; ++k)
+                    v += hi[k * ebr];
+            } else {
+                for (int k = 0; k < ks; ++k) {
+                    v += hi[k * ebr];
+                    v += hi[(ks + k) * ebr];
                 }
-                sm.vals[idx] = v;
             }
+            sm.vals[idx] = v;
         }
         named_bar_sync(1, kWR * 32);
         for (int wi = warp; wi < mper * heads; wi += kWR) {
@@ -597,6 +600,16 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ consumers
+        // the arguments read after the wait are brought into the constant cache
+        // while waiting
+        if (threadIdx.x == 0) {
+            unsigned h = arg_fold(a);
+            if constexpr (MODE == kModeQKV)
+                h ^= arg_fold(eq);
+            else
+                h ^= arg_fold(eo);
+            reinterpret_cast<volatile unsigned *>(flags)[4] = h;
+        }
         pdl_wait();
         // q|k|v: dependents (attention) may launch only once the previous kernels
         // have completed, so that attention can prefetch cache rows before waiting

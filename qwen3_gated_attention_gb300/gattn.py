@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "GATTN_OK", 1: "GATTN_E_INVALID_ARG", 2: "GATTN_E_UNSUPPORTED
 DTYPE_F32, DTYPE_BF16 = 0, 1
 PROJ_Q, PROJ_K, PROJ_V, PROJ_O = 0, 1, 2, 3
 # kernels of a step (gattn_layer_step_kernels)
-KERNEL_NAMES = {1: "xprep", 2: "proj_qkv", 3: "attn", 5: "proj_o", 6: "postnorm"}
+KERNEL_NAMES = {1: "xprep", 2: "proj_qkv", 3: "attn", 4: "merge", 5: "proj_o", 6: "postnorm"}
 
 # every symbol include/gattn.h declares
 EXPORTS = (
