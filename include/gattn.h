@@ -432,22 +432,20 @@ gattn_status gattn_layer_step_block(gattn_layer *layer, const void *x, gattn_kv 
                                     void *out_normed, gattn_stream stream);
 
 /* Per-step launch report of the layer's last step: number of kernel launches
- * it enqueued, all of them this library's own kernels: 3 (q|k|v projection,
- * attention with its merge, o_proj) when the q|k|v kernel converts x itself,
- * else 4 with the x prep launch; one more when an attention segment holds
- * more than 8 query rows, i.e. min(num_heads / num_kv_heads,
- * max(1, 16 / q_len)) * q_len > 8 in integer division (their merge takes a
- * launch of its own); and one more for a decoder-block step whose post-norm
- * takes its own launch. */
+ * it enqueued, all of them this library's own kernels: 4 (q|k|v projection,
+ * attention, the merge of its chunk partials with the output gate, o_proj)
+ * when the q|k|v kernel converts x itself, else 5 with the x prep launch, one
+ * more for a decoder-block step whose post-norm takes its own launch. */
 int32_t gattn_layer_launches_per_step(const gattn_layer *layer);
 
 /* The kernels of the layer's last step, in launch order. */
 enum {
     GATTN_KERNEL_XPREP = 1,     /* x -> tensor-core operand (+ input RMSNorm of the block) */
     GATTN_KERNEL_PROJ_QKV = 2,  /* q|k|v dequant projection + norm / rotary / KV append */
-    GATTN_KERNEL_ATTN = 3,      /* causal GQA attention, merge and output gate -> o_proj operand */
-    GATTN_KERNEL_MERGE = 4,     /* merge of the attention chunk partials of segments of more than
-                                   8 query rows, output gate -> o_proj operand */
+    GATTN_KERNEL_ATTN = 3,      /* causal GQA attention over key chunks (one-chunk segments:
+                                   output gate -> o_proj operand) */
+    GATTN_KERNEL_MERGE = 4,     /* merge of the attention chunk partials, output gate -> o_proj
+                                   operand */
     GATTN_KERNEL_PROJ_O = 5,    /* o_proj (+ residual and fused post-norm of the block) */
     GATTN_KERNEL_POSTNORM = 6   /* post-attention RMSNorm of the block, own launch */
 };

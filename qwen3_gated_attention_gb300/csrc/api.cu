@@ -158,7 +158,6 @@ int attn_row_blocks(int q_len, int H, int Hk, int enabled, int *rb_h0, int *rb_n
 
 constexpr int kAttnMinUnits = 4;     // 16-token units per attention chunk, at least
 constexpr int kAttnSplit = 8;        // attention chunks per CTA aimed at
-constexpr int kInKernelMergeRows = 8; // attention segments up to this many rows merge in place
 
 // Upper bound of the attention items (segment chunks) of a step: the chunk
 // length is at least the unchunked partition's units over split x grid, so the
@@ -219,7 +218,6 @@ struct gattn_layer {
     __nv_bfloat16 *qn = nullptr;
     float *gate = nullptr;
     float *ws_attn = nullptr;              // attention chunk partials
-    unsigned *cnt_seg = nullptr;           // attention completion counters (per segment)
     long long items_cap = 0;
     unsigned *status = nullptr;
     double *inv_freq = nullptr;
@@ -453,8 +451,6 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     }
     L->ws_attn_floats = (size_t)L->items_cap * attn_slot_floats(c.head_dim);
     TRY(cudaMalloc(&L->ws_attn, L->ws_attn_floats * sizeof(float)));
-    TRY(cudaMalloc(&L->cnt_seg, (size_t)L->max_seg * sizeof(unsigned)));
-    TRY(cudaMemset(L->cnt_seg, 0, (size_t)L->max_seg * sizeof(unsigned)));
     TRY(cudaMalloc(&L->status, sizeof(unsigned)));
     TRY(cudaMemset(L->status, 0, sizeof(unsigned)));
     {
@@ -506,7 +502,6 @@ void gattn_layer_destroy(gattn_layer *L)
         return;
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq, L->inv_freq2,
-                    L->cnt_seg,
                     L->q_norm, L->k_norm,
                     L->ss_part, L->post_ticket};
     for (void *p : ptrs)
@@ -939,14 +934,10 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     t.scale_log2 = scale_log2;
     t.nrb_u = nrb_u;
     t.ws = L->ws_attn;
-    t.cnt_seg = L->cnt_seg;
     t.min_units = kAttnMinUnits;
     t.split = kAttnSplit;
     t.attn_grid = L->attn_grid;
-    // segments of more than kInKernelMergeRows rows: their merges run in a
-    // launch of their own, spread over many CTAs (one CTA merging a segment's
-    // rows times chunks would be the long pole); smaller ones merge in place
-    t.merge_sep = max_rows > kInKernelMergeRows ? (max_rows + 3) / 4 : 0;
+    t.merge_rows = max_rows;
     t.x16 = L->x16_o;
     t.xsum = L->xsum_o;
     t.NT = NT;
@@ -993,12 +984,10 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     else
         CUDA_TRY(launch_attn(MT, c.head_dim / 64, t, kv->kmap, kv->vmap, L->attn_grid, pdl, s));
     launched(GATTN_KERNEL_ATTN);
-    if (t.merge_sep) {
-        CUDA_TRY(mark(launches));
-        CUDA_TRY(launch_attn_merge(c.head_dim / 64, kv->kturbo ? 2 : kv->turbo ? 1 : 0, t,
-                                   batch * c.num_kv_heads * nrb, pdl, s));
-        launched(GATTN_KERNEL_MERGE);
-    }
+    CUDA_TRY(mark(launches));
+    CUDA_TRY(launch_attn_merge(c.head_dim / 64, kv->kturbo ? 2 : kv->turbo ? 1 : 0, t,
+                               batch * c.num_kv_heads * nrb, pdl, s));
+    launched(GATTN_KERNEL_MERGE);
     CUDA_TRY(mark(launches));
 
     // 4. o_proj

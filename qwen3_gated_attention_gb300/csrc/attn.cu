@@ -15,11 +15,11 @@
 // consumer warps compute S = q K^T and O += P V with bf16 mma.sync (fp32
 // accumulate) and an online softmax in the log2 domain.
 //
-// A segment of one chunk is finished from the accumulators.  Otherwise each
-// chunk leaves a partial (m, l, O) and the CTA that finishes the last chunk of
-// the segment merges them.  Either way the kernel applies the output gate
-// attn * sigmoid(gate) and writes the o_proj operand in tensor-core fragment
-// order (fp16) with its group sums, so no separate merge launch is needed.
+// A segment of one chunk is finished from the accumulators (bf16 V).
+// Otherwise each chunk leaves a partial (m, l, O) and the merge launch that
+// follows (attn_merge_kernel, one CTA per segment row) combines them.  Either
+// way the output gate attn * sigmoid(gate) is applied and the o_proj operand
+// is written in tensor-core fragment order (fp16) with its group sums.
 #include "attn.cuh"
 
 namespace gattn {

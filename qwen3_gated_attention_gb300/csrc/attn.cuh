@@ -204,127 +204,6 @@ __device__ __forceinline__ long long first_item_at(const ChunkPlan &cp, const lo
     return cp.pi[b] + sl * cp.nc[b] + (r + cp.cu - 1) / cp.cu;
 }
 
-// Merge the n (<= kMaxChunks) chunk partials of a segment (slot j: m[64] l[64]
-// O[64][D], sf floats apart) into the gated o_proj operand of its rows
-// [row0, row0 + nrows).
-// A work unit is one row's part of NP parts of D / NP columns (one part when
-// the values are rotated back, which needs the whole row in one warp); lane j
-// holds slot j's (m, l) and the lanes share the part's columns (column
-// part * D / NP + lane + 32 k).  The (m, l) pairs, the gate and the first JB
-// slots are requested together; the slots are added in slot order, so the
-// sums do not depend on the part split or on the head partition.  Writes the
-// attention tap, the fp16 o_proj operand and its group sums.
-template <int DB, int VQ>
-__device__ __forceinline__ void merge_final(const AttnArgs &a, const float *slots, long long sf,
-                                            int n, int nrows, int row0, const Item &it, int warp,
-                                            int lane)
-{
-    constexpr int D = DB * 64, PER = D / 32;
-    constexpr int NP = (VQ != 0 || PER < 4) ? 1 : 2;
-    constexpr int KP = PER / NP;           // columns per lane
-    constexpr int JB = 32 / KP;            // slots in flight together
-    const int gqa = a.H / a.Hk;
-    const long long Ktot = (long long)a.H * D;
-    const int gs = a.group_o, MP = 8 * a.NT, rpg = gs / 32;
-    for (int w = warp; w < nrows * NP; w += kAttnWarps) {
-        const int i = row0 + w / NP, cb = (w % NP) * (D / NP);
-        const int h = it.kh * gqa + a.rb_h0[it.rb] + i / a.R, r = i % a.R;
-        const int m = it.b * a.R + r;
-        const long long kb = (long long)m * Ktot + (long long)h * D + cb;
-        const float *col = slots + 2 * kAttnMaxRows + (long long)i * D + cb + lane;
-        const float mj = lane < n ? __ldcg(slots + lane * sf + i) : -INFINITY;
-        const float lj = lane < n ? __ldcg(slots + lane * sf + kAttnMaxRows + i) : 0.f;
-        float gt[KP], acc[KP], va[JB][KP], vb[JB][KP];
-#pragma unroll
-        for (int k = 0; k < KP; ++k) {
-            gt[k] = __ldcg(a.gate + kb + lane + 32 * k);
-            acc[k] = 0.f;
-        }
-        // slots j0 .. j0 + JB - 1 into a register batch
-        auto load = [&](float (&v)[JB][KP], int j0) {
-#pragma unroll
-            for (int jj = 0; jj < JB; ++jj)
-#pragma unroll
-                for (int k = 0; k < KP; ++k)
-                    v[jj][k] = j0 + jj < n ? __ldcg(col + (long long)(j0 + jj) * sf + 32 * k) : 0.f;
-        };
-        load(va, 0);
-        float M = mj;
-#pragma unroll
-        for (int o = 16; o; o >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        const float f = mj == -INFINITY ? 0.f : exp2f(mj - M);
-        float L = f * lj;
-#pragma unroll
-        for (int o = 16; o; o >>= 1)
-            L += __shfl_xor_sync(0xffffffffu, L, o);
-        auto add = [&](const float (&v)[JB][KP], int j0) {
-#pragma unroll
-            for (int jj = 0; jj < JB; ++jj) {
-                const float fj = __shfl_sync(0xffffffffu, f, (j0 + jj) & 31);
-                if (j0 + jj < n)
-#pragma unroll
-                    for (int k = 0; k < KP; ++k)
-                        acc[k] = fmaf(fj, v[jj][k], acc[k]);
-            }
-        };
-        // two batches in flight: the next batch is requested before this one
-        // is added
-        for (int j0 = 0; j0 < n; j0 += 2 * JB) {
-            if (j0 + JB < n)
-                load(vb, j0 + JB);
-            add(va, j0);
-            if (j0 + JB >= n)
-                break;
-            if (j0 + 2 * JB < n)
-                load(va, j0 + 2 * JB);
-            add(vb, j0 + JB);
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-        for (int k = 0; k < KP; ++k)
-            acc[k] *= inv;
-        if constexpr (VQ != 0) {
-            // the values were attended in their Walsh-Hadamard basis: H o / sqrt(d)
-            float x[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                x[k] = k < KP ? acc[k] : 0.f;
-            wht_warp(x, KP, lane);
-#pragma unroll
-            for (int k = 0; k < KP; ++k)
-                acc[k] = x[k] * a.inv_sqrt_d;
-        }
-        float hv[KP];
-#pragma unroll
-        for (int k = 0; k < KP; ++k) {
-            const int c = h * D + cb + lane + 32 * k;
-            const __half q = __float2half_rn(acc[k] * (1.f / (1.f + __expf(-gt[k]))));
-            a.x16[x16_offset(m, c, a.NT)] = q;
-            hv[k] = __half2float(q);
-            if (a.tap_attn)
-                a.tap_attn[kb + lane + 32 * k] = acc[k];
-        }
-        // group sums of the fp16 operand: groups of gs (32, 64 or 128, at most
-        // the part's width) consecutive columns, i.e. gs / 32 registers
-        float t = 0.f;
-#pragma unroll
-        for (int k = 0; k < KP; ++k) {
-            t += hv[k];
-            if ((k + 1) % rpg == 0) {
-#pragma unroll
-                for (int o = 16; o; o >>= 1)
-                    t += __shfl_xor_sync(0xffffffffu, t, o);
-                if (lane == 0) {
-                    const int c0 = h * D + cb + 32 * (k + 1 - rpg);
-                    a.xsum[((long long)(c0 >> 7) * (kKU / gs) + ((c0 & 127) / gs)) * MP + m] = t;
-                }
-                t = 0.f;
-            }
-        }
-    }
-}
-
 template <int MT, int DB, int VQ>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
@@ -908,41 +787,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // red_l and red_max are rewritten by the next item
         named_bar_sync(1, kAttnWarps * 32);
     }
-    if (a.merge_sep)
-        return;                 // the merge launch that follows combines the partials
-
-    // ---- completion, once every partial of this CTA is stored (the barrier
-    //      above orders them before the atomics, whose release covers them):
-    //      one acq_rel ticket per chunk item, all taken together so that their
-    //      round trips overlap and none stalls the tile stream; the CTA whose
-    //      ticket completes a segment merges its chunk partials, applies the
-    //      gate, writes the o_proj operand and resets the counter for the next
-    //      step.  Segments of one chunk were finished above.
-    int *mlist = reinterpret_cast<int *>(red_l);   // items whose segment this CTA merges
-    constexpr int kRound = kAttnWarps * 32;        // items per round (the list holds 512)
-    const long long sf = attn_slot_floats(D);
-    for (long long base = beg; base < end; base += kRound) {
-        if (tid == 0)
-            flags[6] = 0;
-        named_bar_sync(1, kAttnWarps * 32);
-        if (base + tid < end) {
-            const Item p = item_of(cp, a.B, a.Hk, a.nrb, base + tid);
-            const int n = cp.nc[p.b];
-            if (!(VQ == 0 && n == 1) &&
-                atom_add_acq_rel_gpu(&a.cnt_seg[p.seg], 1u) == (unsigned)(n - 1))
-                mlist[atomicAdd(&flags[6], 1)] = tid;
-        }
-        named_bar_sync(1, kAttnWarps * 32);
-        const int nmerge = flags[6];
-        for (int k = 0; k < nmerge; ++k) {
-            const Item p = item_of(cp, a.B, a.Hk, a.nrb, base + mlist[k]);
-            merge_final<DB, VQ>(a, a.ws + p.first * sf, sf, cp.nc[p.b], a.rb_nh[p.rb] * a.R, 0,
-                                p, warp, lane);
-            if (tid == 0)
-                a.cnt_seg[p.seg] = 0u;
-        }
-        named_bar_sync(1, kAttnWarps * 32);     // mlist and flags[6] are reused
-    }
 }
 
 
@@ -964,50 +808,112 @@ static cudaError_t launch_attn_t(const AttnArgs &a, const CUtensorMap &kmap,
 }
 
 // the (MT, DB) instances: MT = 16-row tiles of a segment's rows, DB = d / 64
-// Rows of a segment one CTA of the merge launch finishes.
-constexpr int kMergeRows = 4;
-
-// The merge launch that follows the attention launch when segments have many
-// rows (merge_sep slices of 4 rows per segment): CTA (segment, slice) merges
-// rows [4 slice, 4 slice + 4) of
-// the segment's chunk partials (merge_final, the same code and order as the
-// merge inside the attention kernel), so the merges of large segments run on
-// many SMs instead of the one CTA that completes the segment.
+// The merge launch that follows every attention launch: CTA (segment, row i)
+// merges row i of the segment's n chunk partials (segments of one chunk were
+// finished by the attention kernel, except for the Turbo4 V formats, whose
+// rows are rotated back here).  Warp w
+// owns the row's columns 32 w .. 32 w + 31 (lane = column); every lane loads
+// its column of all n <= 32 slots at once together with the chunks' (m, l)
+// and its gate value, so the merge costs one round of loads.  The slots are
+// added in slot order.  Turbo4 V rows are rotated back through shared memory
+// by one warp.  Writes the attention tap, the fp16 o_proj operand and its
+// group sums (warp sums added in warp order).
 template <int DB, int VQ>
-__global__ void __launch_bounds__(kAttnWarps * 32) attn_merge_kernel(const AttnArgs a)
+__global__ void __launch_bounds__(DB * 64) attn_merge_kernel(const AttnArgs a)
 {
+    constexpr int D = DB * 64, NW = D / 32;
     __shared__ int ub[32], nc[32], cu_slot;
     __shared__ long long pi[33], uo[33];
+    __shared__ float row[D], wsum[NW];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the o_proj launch may start streaming its weights at once
     pdl_launch_dependents();
     chunk_plan(a, a.attn_grid, ub, nc, pi, uo, &cu_slot);
-    pdl_wait();                 // the chunk partials come from the attention launch
-    const int slices = a.merge_sep;
-    const long long seg = blockIdx.x / slices;
-    const int sl = blockIdx.x % slices;
-    Item p;
-    p.rb = (int)(seg % a.nrb);
-    p.kh = (int)((seg / a.nrb) % a.Hk);
-    p.b = (int)(seg / ((long long)a.nrb * a.Hk));
-    p.seg = seg;
-    const int n = nc[p.b], nrows = a.rb_nh[p.rb] * a.R, row0 = sl * kMergeRows;
-    if (n == 0 || (VQ == 0 && n == 1) || row0 >= nrows)
+    const long long seg = blockIdx.x / a.merge_rows;
+    const int i = blockIdx.x % a.merge_rows;
+    const int rb = (int)(seg % a.nrb), kh = (int)((seg / a.nrb) % a.Hk);
+    const int b = (int)(seg / ((long long)a.nrb * a.Hk));
+    const int n = nc[b], nrows = a.rb_nh[rb] * a.R;
+    if (n == 0 || (VQ == 0 && n == 1) || i >= nrows)
         return;
-    p.chunk = 0;
-    p.first = pi[p.b] + ((long long)p.kh * a.nrb + p.rb) * n;
-    p.u0 = p.u1 = 0;
-    const long long sf = attn_slot_floats(DB * 64);
-    merge_final<DB, VQ>(a, a.ws + p.first * sf, sf, n, min(kMergeRows, nrows - row0), row0, p,
-                        warp, lane);
+    const int gqa = a.H / a.Hk;
+    const int h = kh * gqa + a.rb_h0[rb] + i / a.R, m = b * a.R + i % a.R;
+    const long long Ktot = (long long)a.H * D, sf = attn_slot_floats(D);
+    const long long kb = (long long)m * Ktot + (long long)h * D + warp * 32 + lane;
+    const float *slots = a.ws + (pi[b] + ((long long)kh * a.nrb + rb) * n) * sf;
+    const float *col = slots + 2 * kAttnMaxRows + (long long)i * D + warp * 32 + lane;
+    pdl_wait();                 // the chunk partials come from the attention launch
+    const float mj = lane < n ? __ldcg(slots + lane * sf + i) : -INFINITY;
+    const float lj = lane < n ? __ldcg(slots + lane * sf + kAttnMaxRows + i) : 0.f;
+    const float gt = __ldcg(a.gate + kb);
+    float v[kMaxChunks];
+#pragma unroll
+    for (int j = 0; j < kMaxChunks; ++j)
+        v[j] = j < n ? __ldcg(col + j * sf) : 0.f;
+    float M = mj;
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float f = mj == -INFINITY ? 0.f : exp2f(mj - M);
+    float L = f * lj;
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        L += __shfl_xor_sync(0xffffffffu, L, o);
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxChunks; ++j) {
+        const float fj = __shfl_sync(0xffffffffu, f, j);
+        if (j < n)
+            acc = fmaf(fj, v[j], acc);
+    }
+    float o = acc * (L > 0.f ? 1.f / L : 0.f);
+    if constexpr (VQ != 0) {
+        // the values were attended in their Walsh-Hadamard basis: H o / sqrt(d)
+        row[warp * 32 + lane] = o;
+        __syncthreads();
+        if (warp == 0) {
+            float x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                x[k] = k < NW ? row[lane + 32 * k] : 0.f;
+            wht_warp(x, NW, lane);
+#pragma unroll
+            for (int k = 0; k < NW; ++k)
+                row[lane + 32 * k] = x[k] * a.inv_sqrt_d;
+        }
+        __syncthreads();
+        o = row[warp * 32 + lane];
+    }
+    const int c = h * D + warp * 32 + lane;
+    const __half q = __float2half_rn(o * (1.f / (1.f + __expf(-gt))));
+    a.x16[x16_offset(m, c, a.NT)] = q;
+    if (a.tap_attn)
+        a.tap_attn[kb] = o;
+    // group sums of the fp16 operand: groups of gs (32, 64 or 128) columns,
+    // gs / 32 consecutive warps
+    float t = __half2float(q);
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+        t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (lane == 0)
+        wsum[warp] = t;
+    __syncthreads();
+    const int gs = a.group_o, wpg = gs / 32, MP = 8 * a.NT;
+    if (threadIdx.x < D / gs) {
+        float g = 0.f;
+        for (int w = 0; w < wpg; ++w)
+            g += wsum[threadIdx.x * wpg + w];
+        const int c0 = h * D + threadIdx.x * gs;
+        a.xsum[((long long)(c0 >> 7) * (kKU / gs) + ((c0 & 127) / gs)) * MP + m] = g;
+    }
 }
 
 template <int DB, int VQ>
 static cudaError_t launch_attn_merge_t(const AttnArgs &a, int segments, bool pdl, cudaStream_t s)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(segments * a.merge_sep);
-    cfg.blockDim = dim3(kAttnWarps * 32);
+    cfg.gridDim = dim3(segments * a.merge_rows);
+    cfg.blockDim = dim3(DB * 64);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

@@ -144,17 +144,6 @@ __device__ __forceinline__ bool mbar_wait_all(uint64_t *bar, uint32_t parity, un
     return true;
 }
 
-// Atomic add at GPU scope with acquire-release semantics; returns the old value.
-__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v)
-{
-    unsigned old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
-                 : "=r"(old)
-                 : "l"(p), "r"(v)
-                 : "memory");
-    return old;
-}
-
 // ------------------------------------------------------------- TMA copies
 
 __device__ __forceinline__ uint64_t l2_evict_first_policy()

@@ -275,11 +275,8 @@ struct AttnArgs {
     int min_units;               // minimum 16-token units per chunk
     int split;                   // chunks per CTA aimed at (balance against per-chunk work)
     int attn_grid;               // CTAs of the attention launch (the chunk plan depends on it)
-    // 0: the attention launch merges each segment's chunk partials; > 0: a
-    // merge launch follows, with this many 4-row slices per segment
-    int merge_sep;
+    int merge_rows;              // rows a segment, at most: the merge launch's CTAs per segment
     float *ws;                   // chunk partials, attn_slot_floats(d) per item
-    unsigned *cnt_seg;           // completion counter per segment (zero between steps)
     // o_proj operand
     __half *x16;
     float *xsum;
@@ -306,8 +303,8 @@ struct AttnArgs {
 __device__ __forceinline__ unsigned arg_fold(const AttnArgs &a)
 {
     unsigned h = arg_fold(a.qn, a.gate, a.cache_pos, a.B, a.R, a.H, a.Hk, a.d, a.cap, a.nrb, a.nrb_u,
-                          a.scale_log2, a.min_units, a.split, a.attn_grid, a.merge_sep, a.ws,
-                          a.cnt_seg, a.x16, a.xsum, a.NT,
+                          a.scale_log2, a.min_units, a.split, a.attn_grid, a.merge_rows, a.ws,
+                          a.x16, a.xsum, a.NT,
                           a.group_o, a.tap_attn, a.status, a.vq, a.vq_codes, a.vq_scales,
                           a.cq_head, a.cq_batch, a.sq_head, a.sq_batch, a.kq_codes, a.kq_scales,
                           a.kcq_head, a.kcq_batch, a.ksq_head, a.ksq_batch, a.vq_tl[0], a.vq_tl[1],
@@ -322,8 +319,8 @@ __device__ __forceinline__ unsigned arg_fold(const AttnArgs &a)
 
 cudaError_t launch_attn(int MT, int DB, const AttnArgs &a, const CUtensorMap &kmap,
                         const CUtensorMap &vmap, int grid, bool pdl, cudaStream_t s);
-// the merge launch after an attention launch with merge_sep > 0 (segments =
-// B * Hk * nrb); vq: the cache format of the attention instance (0, 1, 2)
+// the merge launch after every attention launch (segments = B * Hk * nrb);
+// vq: the cache format of the attention instance (0, 1, 2)
 cudaError_t launch_attn_merge(int DB, int vq, const AttnArgs &a, int segments, bool pdl,
                               cudaStream_t s);
 // the Bf16KTurbo4V instances (attn_vq.cu); vmap is unused there

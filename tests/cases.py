@@ -76,11 +76,3 @@ def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
         return np.where(h & 0x8000, 0x8000 - (h & 0x7FFF), 0x8000 + h)
     return np.abs(key(a_bits) - key(b_bits))
 
-
-def merge_launch(spec, q_len=None) -> bool:
-    """Whether a step of this layer merges its attention partials in a launch of
-    its own: its attention segments (row blocks of whole heads, at most 16 rows
-    or one head) hold more than 8 query rows."""
-    R = q_len or spec.q_len
-    gqa = spec.num_heads // spec.num_kv_heads
-    return min(gqa, max(1, 16 // R)) * R > 8
