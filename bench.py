@@ -72,7 +72,8 @@ def algorithmic_bytes(spec, block=False, kv="bf16", x_folded=False):
     per_kernel = {
         "xprep": xb + x16,
         "proj_qkv": wq + wk + wv + x16 + qn + gate + kv_write,
-        "attn": kv_read + qn + gate + o16,          # with its merge and the output gate
+        "attn": kv_read + qn,
+        "merge": gate + o16,                        # the chunk merge and the output gate
         "proj_o": wo + o16 + outb,
     }
     if x_folded:
@@ -418,10 +419,6 @@ def measure_workload(spec, args, dev, world, dist, l2, full=True):
         kernel_bytes = dict(algorithmic_bytes(spec, args.block, args.kv, x_folded=True)[1])
     if "postnorm" not in names and "postnorm" in kernel_bytes:       # post-norm inside the o_proj
         kernel_bytes["proj_o"] += kernel_bytes.pop("postnorm")
-    if "merge" in names:                   # a merge launch reads the gate, writes the operand
-        hd = spec.batch * spec.q_len * spec.num_heads * spec.head_dim
-        kernel_bytes["attn"] -= hd * (4 + 2)
-        kernel_bytes["merge"] = hd * (4 + 2)
     kernel_bytes = {n: kernel_bytes[n] for n in names}
     nper = max(args.replays, n_inst)
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(nper)]

@@ -140,11 +140,12 @@ def test_turbo4_ratio_is_the_printed_one():
 @pytest.mark.parametrize("fmt", ["bf16", "turbo4v", "turbo4"])
 def test_bench_accounting_reads_the_whole_printed_cache(fmt):
     """A decode step at the last position reads every cache row once: the
-    attention's algorithmic bytes minus its q rows, its gate rows (fp32) and the
-    gated operand it writes (fp16) equal the printed cache size."""
+    attention's algorithmic bytes minus its q rows equal the printed cache size,
+    and the merge moves the gate rows (fp32) and the gated operand (fp16)."""
     kv = _kv_sizes()
     s = _cache_spec(kv)
     assert int(s.positions()[0]) + s.q_len == int(kv["max_seq"]) and s.batch == 1
     _, per = bench.algorithmic_bytes(s, kv=fmt)
     rows = s.batch * s.q_len * s.num_heads * s.head_dim
-    assert per["attn"] - rows * (2 + 4 + 2) == sum(kv[fmt])
+    assert per["attn"] - rows * 2 == sum(kv[fmt])
+    assert per["merge"] == rows * (4 + 2)
