@@ -174,7 +174,7 @@ long long attn_items_bound(int grid, int split, int nrb, int nrb_u, int batch, i
 constexpr int kXTabMax = 24 * 1024;
 constexpr int kMaxCluster = 8;       // portable cluster size
 
-void plan_proj(ProjPlan &p, int N, int K, int bits, int group, int rbc)
+void plan_proj(ProjPlan &p, int N, int K, int bits, int group, int rbc, int mode)
 {
     p.N = N;
     p.K = K;
@@ -193,8 +193,10 @@ void plan_proj(ProjPlan &p, int N, int K, int bits, int group, int rbc)
         sbytes = (sbytes + 127) & ~127;
         p.stage_bytes[i] = sbytes;
         // a small ring per CTA so that three or four CTAs (12-16 consumer warps)
-        // share an SM: the stage loop is latency bound, not bandwidth bound
-        int st = (48 * 1024) / sbytes;
+        // share an SM: the stage loop is latency bound, not bandwidth bound.
+        // o_proj at 32 operand columns takes a ring twice as deep (its CTAs
+        // stream only a few stages each, measured faster at batched_9b)
+        int st = ((mode == kModeO && NT >= 4 ? 96 : 48) * 1024) / sbytes;
         if (st < 2) st = 2;
         if (st > 8) st = 8;
         // the drained ring holds the CTA's partial sums [8*NT][kRBR] floats
@@ -341,8 +343,8 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
 
     // a q|k|v cluster covers whole heads (RMSNorm needs every row of a head)
     plan_proj(L->pqkv, L->Nq + 2 * L->Nkv, c.hidden, proj_bits(c, 0), proj_group(c, 0),
-              std::max(1, c.head_dim / kRBR));
-    plan_proj(L->po, c.hidden, L->Ko, proj_bits(c, 3), proj_group(c, 3), 1);
+              std::max(1, c.head_dim / kRBR), kModeQKV);
+    plan_proj(L->po, c.hidden, L->Ko, proj_bits(c, 3), proj_group(c, 3), 1, kModeO);
 
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
