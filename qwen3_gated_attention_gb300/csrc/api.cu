@@ -158,6 +158,7 @@ int attn_row_blocks(int q_len, int H, int Hk, int enabled, int *rb_h0, int *rb_n
 
 constexpr int kAttnMinUnits = 4;     // 16-token units per attention chunk, at least
 constexpr int kAttnSplit = 8;        // attention chunks per CTA aimed at
+constexpr int kChunkRowsBudget = 512; // attention chunks x segment rows, at most
 
 // Upper bound of the attention items (segment chunks) of a step: the chunk
 // length is at least the unchunked partition's units over split x grid, so the
@@ -940,6 +941,10 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     t.split = kAttnSplit;
     t.attn_grid = L->attn_grid;
     t.merge_rows = max_rows;
+    // the partials a step stores and merges grow with rows x chunks: segments
+    // of many rows are cut into fewer chunks (a route-independent bound: the
+    // largest row block has the same rows in both head partitions)
+    t.max_chunks = std::max(4, std::min(32, kChunkRowsBudget / std::max(1, max_rows)));
     t.x16 = L->x16_o;
     t.xsum = L->xsum_o;
     t.NT = NT;

@@ -148,7 +148,7 @@ __device__ __forceinline__ Item item_of(const ChunkPlan &cp, int B, int Hk, int 
 // item's unit offset uo (pi[B], uo[B]: totals), in shared memory; returns cu.
 // cu units per chunk: the unchunked partition's unit count over split x the
 // grid, at least min_units and at least the longest segment's units over
-// kMaxChunks.  Called by every thread of the block (two barriers).
+// max_chunks (<= kMaxChunks).  Called by every thread of the block (two barriers).
 __device__ __forceinline__ int chunk_plan(const AttnArgs &a, int grid, int *ub, int *nc,
                                           long long *pi, long long *uo, int *cu_slot)
 {
@@ -169,7 +169,7 @@ __device__ __forceinline__ int chunk_plan(const AttnArgs &a, int grid, int *ub, 
         const long long parts = (long long)a.split * grid;
         const long long per = (uu + parts - 1) / parts;
         int cu = (int)(per > a.min_units ? per : a.min_units);
-        cu = max(cu, (umax + kMaxChunks - 1) / kMaxChunks);
+        cu = max(cu, (umax + a.max_chunks - 1) / a.max_chunks);
         long long ai = 0, au = 0;
         for (int b = 0; b < a.B; ++b) {
             const int n = (ub[b] + cu - 1) / cu;

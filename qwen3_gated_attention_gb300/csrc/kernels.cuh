@@ -274,6 +274,7 @@ struct AttnArgs {
     float scale_log2;            // log2(e) / sqrt(d)
     int min_units;               // minimum 16-token units per chunk
     int split;                   // chunks per CTA aimed at (balance against per-chunk work)
+    int max_chunks;              // chunks per segment, at most (<= 32)
     int attn_grid;               // CTAs of the attention launch (the chunk plan depends on it)
     int merge_rows;              // rows a segment, at most: the merge launch's CTAs per segment
     float *ws;                   // chunk partials, attn_slot_floats(d) per item
@@ -303,7 +304,7 @@ struct AttnArgs {
 __device__ __forceinline__ unsigned arg_fold(const AttnArgs &a)
 {
     unsigned h = arg_fold(a.qn, a.gate, a.cache_pos, a.B, a.R, a.H, a.Hk, a.d, a.cap, a.nrb, a.nrb_u,
-                          a.scale_log2, a.min_units, a.split, a.attn_grid, a.merge_rows, a.ws,
+                          a.scale_log2, a.min_units, a.split, a.max_chunks, a.attn_grid, a.merge_rows, a.ws,
                           a.x16, a.xsum, a.NT,
                           a.group_o, a.tap_attn, a.status, a.vq, a.vq_codes, a.vq_scales,
                           a.cq_head, a.cq_batch, a.sq_head, a.sq_batch, a.kq_codes, a.kq_scales,
