@@ -610,50 +610,50 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
                 h ^= arg_fold(eo);
             reinterpret_cast<volatile unsigned *>(flags)[4] = h;
         }
+        // the x table of this CTA's k units (fp16 fragments and group sums of
+        // every operand column): zeroed while waiting, so that only the columns
+        // that carry input are converted after the wait
+        const int xe = xbytes + sbytes;
+        const int nk = ku1 - ku0;
+        if (xfold) {
+            uint4 *t4 = reinterpret_cast<uint4 *>(xtab);
+            for (int i = threadIdx.x; i < nk * xe / 16; i += kWR * 32)
+                t4[i] = make_uint4(0u, 0u, 0u, 0u);
+            named_bar_sync(1, kWR * 32);
+        }
         pdl_wait();
         // q|k|v: dependents (attention) may launch only once the previous kernels
         // have completed, so that attention can prefetch cache rows before waiting
         if constexpr (MODE == kModeQKV)
             pdl_launch_dependents();
-        // the x table of this CTA's k units: items (k unit, column) of 128 k, eight
-        // lanes each, sixteen per pass; the columns that carry input come first
-        // and the loads of the first two passes are issued together (one round
-        // trip for the decode and verify shapes), the padding columns are zeros
-        const int xe = xbytes + sbytes;
+        // items (k unit, column with input) of 128 k, eight lanes each, sixteen
+        // per pass; the loads of two passes are issued together (one round trip
+        // for up to 32 items: the decode and verify shapes)
         if (xfold) {
-            const int nk = ku1 - ku0;
             const int mx = a.xsplit ? 2 * a.M : a.M;            // columns with input
             const int xd = a.x_f32 ? 0 : 1, K = a.nku * kKU, part = threadIdx.x & 7;
-            auto item_of = [&](int item, int &kl, int &m) {
-                if (item < nk * mx) {
-                    kl = item / mx;
-                    m = item % mx;
-                } else {
-                    const int j = item - nk * mx;
-                    kl = j / (MP - mx);
-                    m = mx + j % (MP - mx);
-                }
-            };
-            for (int b0 = 0; b0 < nk * MP; b0 += 2 * kWR * 4) {
+            for (int b0 = 0; b0 < nk * mx; b0 += 2 * kWR * 4) {
                 int kl[2], m[2];
                 bool live[2];
                 XRaw raw[2];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int item = b0 + q * kWR * 4 + (threadIdx.x >> 3);
-                    live[q] = item < nk * MP;
-                    kl[q] = 0;
-                    m[q] = 0;
-                    if (live[q])
-                        item_of(item, kl[q], m[q]);
+                    live[q] = item < nk * mx;
+                    kl[q] = live[q] ? item / mx : 0;
+                    m[q] = live[q] ? item % mx : 0;
                     raw[q] = x_chunk_load(a.xraw, xd, a.M, K, (ku0 + kl[q]) * kKU, m[q], part,
                                           live[q]);
                 }
+                // a warp none of whose items carry input skips the conversion
+                // as a whole (its shuffles name every lane of the warp)
 #pragma unroll
                 for (int q = 0; q < 2; ++q)
-                    x_chunk_convert(raw[q], xd, a.M, GROUP, NT, (ku0 + kl[q]) * kKU, m[q], part,
-                                    1.f, nullptr, reinterpret_cast<__half *>(xtab + kl[q] * xe),
-                                    reinterpret_cast<float *>(xtab + kl[q] * xe + xbytes), live[q]);
+                    if (__any_sync(0xffffffffu, live[q]))
+                        x_chunk_convert(raw[q], xd, a.M, GROUP, NT, (ku0 + kl[q]) * kKU, m[q], part,
+                                        1.f, nullptr, reinterpret_cast<__half *>(xtab + kl[q] * xe),
+                                        reinterpret_cast<float *>(xtab + kl[q] * xe + xbytes),
+                                        live[q]);
             }
             named_bar_sync(1, kWR * 32);
         }
