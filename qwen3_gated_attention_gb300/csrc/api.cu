@@ -231,6 +231,7 @@ struct gattn_layer {
     int max_seg = 0;
     float *ss_part = nullptr;              // decoder-block post-norm: per-CTA sums of squares
     unsigned *post_ticket = nullptr;
+    unsigned long long *slot_ctr = nullptr;   // attention CTAs started (work slots, attn.cuh)
     // Bf16KTurbo4V caches: decision tables (passed by value) and the bytes of
     // the 8 positive fp16 levels the attention dequantizes with
     TurboTables tq{};
@@ -475,6 +476,8 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
         TRY(cudaMalloc(&L->ss_part, (size_t)gmax * L->M_max * sizeof(float)));
         TRY(cudaMalloc(&L->post_ticket, sizeof(unsigned)));
         TRY(cudaMemset(L->post_ticket, 0, sizeof(unsigned)));
+        TRY(cudaMalloc(&L->slot_ctr, sizeof(unsigned long long)));
+        TRY(cudaMemset(L->slot_ctr, 0, sizeof(unsigned long long)));
     }
 
     std::vector<double> inv(L->rd / 2);
@@ -506,7 +509,7 @@ void gattn_layer_destroy(gattn_layer *L)
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq, L->inv_freq2,
                     L->q_norm, L->k_norm,
-                    L->ss_part, L->post_ticket};
+                    L->ss_part, L->post_ticket, L->slot_ctr};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -937,6 +940,7 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
     t.scale_log2 = scale_log2;
     t.nrb_u = nrb_u;
     t.ws = L->ws_attn;
+    t.slot_ctr = L->slot_ctr;
     t.min_units = kAttnMinUnits;
     t.split = kAttnSplit;
     t.attn_grid = L->attn_grid;

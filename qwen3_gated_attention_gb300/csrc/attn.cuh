@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     long long *uo = pi + 40;                // [33] unit offset of each sequence's first item
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBars);
     uint64_t *empty = full + L::kNStages;
-    int *flags = reinterpret_cast<int *>(smem + L::kFlags);   // [0] abort [1..3] merge flags
+    int *flags = reinterpret_cast<int *>(smem + L::kFlags);   // [0] abort [2] work slot [4] cu
     int *ub = flags + 8;                                        // units per segment of b [32]
     int *nc = ub + 32;                                          // chunks per segment of b [32]
 
@@ -243,18 +243,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(&empty[i], kAttnWarps);
         }
         flags[0] = 0;
-        flags[1] = 0;
+        // this CTA's work slot, in the order the CTAs start: every launch adds
+        // exactly gridDim.x to the layer's counter, so the slots of a launch
+        // are 0 .. gridDim.x - 1 whatever the counter held before
+        flags[2] = (int)(atomicAdd(a.slot_ctr, 1ull) % gridDim.x);
         fence_mbar_init();
     }
     const int cu = chunk_plan(a, gridDim.x, ub, nc, pi, uo, &flags[4]);
     const ChunkPlan cp{cu, ub, nc, pi};
 
-    // contiguous item ranges balanced by units: CTA c takes the items that
-    // start in its share of the units (consecutive chunks of a segment in one
-    // CTA share its q rows)
-    const long long U = uo[a.B], c = blockIdx.x;
-    const long long beg = first_item_at(cp, uo, a.B, U * c / gridDim.x);
-    const long long end = first_item_at(cp, uo, a.B, U * (c + 1) / gridDim.x);
+    // the items of slot c: with no more items than CTAs, item c (the CTAs that
+    // start last, while the previous kernel still holds their SMs, are left
+    // without work); else contiguous item ranges balanced by units: slot c
+    // takes the items that start in its share of the units (consecutive
+    // chunks of a segment in one CTA share its q rows)
+    const long long U = uo[a.B], c = flags[2], items = pi[a.B];
+    const bool one_each = items <= (long long)gridDim.x;
+    const long long beg = one_each ? min(c, items) : first_item_at(cp, uo, a.B, U * c / gridDim.x);
+    const long long end = one_each ? min(c + 1, items)
+                                   : first_item_at(cp, uo, a.B, U * (c + 1) / gridDim.x);
     volatile int *abort = flags;
 
     if (warp == kAttnWarps) {

@@ -164,6 +164,22 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
+// Copies N (4, 8 or 16) bytes global -> shared without making the issuing
+// thread wait (cp.async); cp_async_wait_all() waits for every copy the thread
+// issued before it.  Both addresses aligned to N.
+template <int N>
+__device__ __forceinline__ void cp_async(void *dst, const void *src)
+{
+    static_assert(N == 4 || N == 8 || N == 16, "cp.async copies 4, 8 or 16 bytes");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src), "n"(N)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // 4-D tiled tensor copy global -> shared (coordinate x is innermost).
 __device__ __forceinline__ void tensor4d_g2s(void *dst, const CUtensorMap *map, int x, int y, int z,
                                              int w, uint64_t *bar, uint64_t policy)
@@ -358,6 +374,10 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, ui
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t v)
+{
+    return __uint_as_float((uint32_t)v << 16);
+}
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)

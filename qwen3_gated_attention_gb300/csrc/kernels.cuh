@@ -298,6 +298,8 @@ struct AttnArgs {
     const uint8_t *mask;
     int mask_heads, mask_len;
     long long mask_row, mask_head, mask_batch;
+    // the layer's count of attention CTAs started (each takes the next work slot)
+    unsigned long long *slot_ctr;
 };
 
 #ifdef __CUDACC__
@@ -310,7 +312,7 @@ __device__ __forceinline__ unsigned arg_fold(const AttnArgs &a)
                           a.cq_head, a.cq_batch, a.sq_head, a.sq_batch, a.kq_codes, a.kq_scales,
                           a.kcq_head, a.kcq_batch, a.ksq_head, a.ksq_batch, a.vq_tl[0], a.vq_tl[1],
                           a.vq_th[0], a.vq_th[1], a.inv_sqrt_d, a.mask, a.mask_heads, a.mask_len,
-                          a.mask_row, a.mask_head, a.mask_batch);
+                          a.mask_row, a.mask_head, a.mask_batch, a.slot_ctr);
 #pragma unroll
     for (int i = 0; i < kMaxRowBlocks; i += 4)
         h ^= arg_fold(a.rb_h0[i], a.rb_nh[i]);

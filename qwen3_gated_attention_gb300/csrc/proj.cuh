@@ -118,7 +118,7 @@ struct EpiSmem {
     float *red;         // [MP][kRBR] this CTA's partial sums (aliases the stage ring)
     float *recv;        // partial sums pushed here by the cluster's CTAs (see below)
     float *vals;        // [eb_rows] final values of one column of the cluster's rows
-    float *nq, *nk;     // q_norm / k_norm as fp32 [d]
+    uint16_t *nq, *nk;  // q_norm / k_norm [d] (bf16 bits)
     float2 *invf;       // inv_freq [rd/2] as float (hi, lo) pairs
     int *cpos;          // cache_pos [B]
 };
@@ -269,7 +269,7 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
                 for (int o = 16; o; o >>= 1)
                     ss += __shfl_xor_sync(0xffffffffu, ss, o);
                 const float inv = rsqrtf(ss / (float)d + e.eps);
-                const float *nw = kind == 0 ? sm.nq : sm.nk;
+                const uint16_t *nw = kind == 0 ? sm.nq : sm.nk;
                 // partial rotary on dims [0, rd): pairs (j, j + rd/2) at position p0 + r.
                 // The angle pos * inv_freq is formed as an unevaluated float pair
                 // (inv_freq split in hi + lo on the host, the product's rounding
@@ -281,11 +281,11 @@ static __device__ void epilogue_qkv(const ProjArgs &a, const EpiQKV &e, const Ep
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int j = lane + 32 * i;
-                    o[i] = i < per ? v[i] * inv * nw[j] : 0.f;
+                    o[i] = i < per ? v[i] * inv * bf16_bits_to_float(nw[j]) : 0.f;
                     if (i < per && j < e.rd) {
                         const int fi = j < half ? j : j - half;
                         const int jp = j < half ? j + half : j - half;
-                        const float partner = hv[jp] * inv * nw[jp];
+                        const float partner = hv[jp] * inv * bf16_bits_to_float(nw[jp]);
                         const float2 fq = sm.invf[fi];
                         const float ph = pos * fq.x;
                         const float pl = fmaf(pos, fq.x, -ph) + pos * fq.y;
@@ -466,9 +466,9 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
     EpiSmem sm;
     sm.red = reinterpret_cast<float *>(smem);                         // after the main loop
     sm.vals = reinterpret_cast<float *>(tail + 256);
-    sm.nq = sm.vals + kValsFloats;
+    sm.nq = reinterpret_cast<uint16_t *>(sm.vals + kValsFloats);
     sm.nk = sm.nq + 256;
-    sm.invf = reinterpret_cast<float2 *>(sm.nk + 256);
+    sm.invf = reinterpret_cast<float2 *>(sm.vals + kValsFloats + 256);
     sm.cpos = reinterpret_cast<int *>(sm.invf + 128);
     sm.recv = reinterpret_cast<float *>(tail + proj_tail_bytes(a.eb_rows));
     uint8_t *xtab = reinterpret_cast<uint8_t *>(sm.recv + a.recv_cap);   // a.xtab_bytes
@@ -501,21 +501,22 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
     // (weight streaming) reads nothing this kernel writes
     if constexpr (MODE == kModeO)
         pdl_launch_dependents();
-    // epilogue statics: layer weights and the step's cache_pos (a step input)
+    // epilogue statics: layer weights and the step's cache_pos (a step input),
+    // copied asynchronously: nothing waits for them before the epilogue
     if (threadIdx.x < kWR * 32) {
         const int t = threadIdx.x;
         if constexpr (MODE == kModeQKV) {
-            for (int j = t; j < eq.d; j += kWR * 32) {
-                sm.nq[j] = __uint_as_float((uint32_t)eq.q_norm[j] << 16);
-                sm.nk[j] = __uint_as_float((uint32_t)eq.k_norm[j] << 16);
+            for (int j = t; j < eq.d / 8; j += kWR * 32) {
+                cp_async<16>(sm.nq + 8 * j, eq.q_norm + 8 * j);
+                cp_async<16>(sm.nk + 8 * j, eq.k_norm + 8 * j);
             }
             for (int j = t; j < eq.rd / 2; j += kWR * 32)
-                sm.invf[j] = eq.inv_freq2[j];
+                cp_async<8>(sm.invf + j, eq.inv_freq2 + j);
             if (t < (a.M + eq.R - 1) / eq.R)
-                sm.cpos[t] = eq.cache_pos[t];
+                cp_async<4>(sm.cpos + t, eq.cache_pos + t);
         } else {
             if (t < (a.M + eo.R - 1) / eo.R)
-                sm.cpos[t] = eo.cache_pos[t];
+                cp_async<4>(sm.cpos + t, eo.cache_pos + t);
         }
     }
     __syncthreads();
@@ -601,14 +602,16 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
     } else {
         // ------------------------------------------------------------ consumers
         // the arguments read after the wait are brought into the constant cache
-        // while waiting
-        if (threadIdx.x == 0) {
-            unsigned h = arg_fold(a);
-            if constexpr (MODE == kModeQKV)
-                h ^= arg_fold(eq);
+        // while waiting, each block of them by another warp
+        if (lane == 0 && warp < 2) {
+            unsigned h;
+            if (warp == 0)
+                h = arg_fold(a);
+            else if constexpr (MODE == kModeQKV)
+                h = arg_fold(eq);
             else
-                h ^= arg_fold(eo);
-            reinterpret_cast<volatile unsigned *>(flags)[4] = h;
+                h = arg_fold(eo);
+            reinterpret_cast<volatile unsigned *>(flags)[4 + warp] = h;
         }
         // the x table of this CTA's k units (fp16 fragments and group sums of
         // every operand column): zeroed while waiting, so that only the columns
@@ -669,7 +672,9 @@ __global__ void __launch_bounds__(proj_threads(NT), NT >= 4 ? 3 : 2)
                 mbar_arrive(&empty[slot]);
         }
     }
-    // the ring is drained: it now holds this CTA's partial sums [MP][kRBR]
+    // the ring is drained: it now holds this CTA's partial sums [MP][kRBR]; the
+    // epilogue statics have landed
+    cp_async_wait_all();
     __syncthreads();
     if (warp < kWR) {
         const int g = lane >> 2, cq = lane & 3;
