@@ -10,8 +10,9 @@ Device timing: a CUDA graph of consecutive steps cycling over enough distinct
 layer instances (weights + caches) that their bytes exceed 4x the L2 cache, so
 every step streams from HBM; CUDA events on the launching stream.  A second
 pass records per-kernel events (no programmatic overlap) for the roofline of
-the dominant kernel.  e2e: the same steps through the C ABI with the input
-copied from pinned host memory and the output read back every step.
+the dominant kernel.  e2e: the same steps through the C ABI from pinned host
+buffers (gattn_layer_step_host: x and cache_pos copied in, the step, out read
+back, every step; the decoder block copies around gattn_layer_step_block).
 
 --impl reference times the float64 CPU oracle (the reference arm) on a bounded
 sample of the same workload.
@@ -477,11 +478,16 @@ def measure_workload(spec, args, dev, world, dist, l2, full=True):
             e0.record(stream)
             for i in range(n_e2e):
                 dl = layers[i % n_inst]
+                if not args.block:
+                    # one C call: x and cache_pos in, the step, out back
+                    gattn.layer_step_host(dl.h, xh.data_ptr(), dl.kv, ph.data_ptr(), spec.batch,
+                                          spec.q_len, oh.data_ptr(), sh)
+                    continue
                 xdev.view(torch.int16 if spec.x_dtype != "f32" else torch.float32).copy_(
                     xh, non_blocking=True)
                 pdev.copy_(ph, non_blocking=True)
                 step_call(dl, xdev.data_ptr(), pdev.data_ptr(), outs[i % n_inst].data_ptr())
-                oh.copy_(normed if args.block else outs[i % n_inst], non_blocking=True)
+                oh.copy_(normed, non_blocking=True)
             e1.record(stream)
         stream.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist if world > 1 else None, dev)

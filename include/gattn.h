@@ -292,6 +292,25 @@ gattn_status gattn_layer_step(gattn_layer *layer, const void *x, gattn_kv *kv,
                               const int32_t *cache_pos, int32_t batch, int32_t q_len,
                               void *out, gattn_stream stream);
 
+/*
+ * gattn_layer_step from host buffers: enqueues on `stream` the copy of x and
+ * cache_pos into the layer's own device staging buffers, the step, and the
+ * copy of its output rows into out_host, then returns (no host
+ * synchronization: out_host holds the result once the stream has reached it).
+ *   x_host          (host) [batch][q_len][hidden], cfg.x_dtype
+ *   cache_pos_host  (host) int32 [batch], as cache_pos of gattn_layer_step
+ *   out_host        (host) bf16 [batch][q_len][hidden]
+ * The host buffers are borrowed until the stream has passed the copies; pinned
+ * (page-locked) memory makes the copies asynchronous.  The staging buffers
+ * (allocated with the layer, for the largest step it admits) are shared by the
+ * calls on one handle, like its scratch.  Errors: those of gattn_layer_step,
+ * checked before anything is enqueued; GATTN_E_CUDA when a copy or a launch
+ * fails.
+ */
+gattn_status gattn_layer_step_host(gattn_layer *layer, const void *x_host, gattn_kv *kv,
+                                   const int32_t *cache_pos_host, int32_t batch, int32_t q_len,
+                                   void *out_host, gattn_stream stream);
+
 /* Synchronize `stream`, then read and clear the layer's device status word:
  * GATTN_OK, GATTN_E_DEVICE_RANGE or GATTN_E_DEVICE_TIMEOUT (GATTN_E_INVALID_ARG
  * for a NULL layer, GATTN_E_CUDA when the synchronization or read fails). */

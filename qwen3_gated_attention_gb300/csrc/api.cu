@@ -232,6 +232,9 @@ struct gattn_layer {
     float *ss_part = nullptr;              // decoder-block post-norm: per-CTA sums of squares
     unsigned *post_ticket = nullptr;
     unsigned long long *slot_ctr = nullptr;   // attention CTAs started (work slots, attn.cuh)
+    // gattn_layer_step_host: device copies of the step's x, cache_pos and out
+    void *x_stage = nullptr, *out_stage = nullptr;
+    int32_t *pos_stage = nullptr;
     // Bf16KTurbo4V caches: decision tables (passed by value) and the bytes of
     // the 8 positive fp16 levels the attention dequantizes with
     TurboTables tq{};
@@ -434,6 +437,10 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaMalloc(&L->xsum_o, nku_o * (kKU / L->po.group) * MP * sizeof(float)));
     TRY(cudaMemset(L->xsum_o, 0, nku_o * (kKU / L->po.group) * MP * sizeof(float)));
     TRY(cudaMalloc(&L->qn, (size_t)L->M_max * L->Ko * 2));
+    TRY(cudaMalloc(&L->x_stage, (size_t)L->M_max * c.hidden *
+                                    (c.x_dtype == GATTN_DTYPE_F32 ? 4 : 2)));
+    TRY(cudaMalloc(&L->out_stage, (size_t)L->M_max * c.hidden * 2));
+    TRY(cudaMalloc(&L->pos_stage, (size_t)c.max_batch * sizeof(int32_t)));
     TRY(cudaMalloc(&L->gate, (size_t)L->M_max * L->Ko * sizeof(float)));
     // attention segments: batch x KV heads x row blocks (at most gqa row blocks)
     // attention scratch: chunk partials and completion counters for the largest
@@ -509,7 +516,8 @@ void gattn_layer_destroy(gattn_layer *L)
     void *ptrs[] = {L->pqkv.w, L->po.w,      L->x16_a,  L->x16_o,   L->xsum_a,  L->xsum_o,
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq, L->inv_freq2,
                     L->q_norm, L->k_norm,
-                    L->ss_part, L->post_ticket, L->slot_ctr};
+                    L->ss_part, L->post_ticket, L->slot_ctr,
+                    L->x_stage, L->out_stage, L->pos_stage};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -783,12 +791,9 @@ struct BlockArgs {
     __nv_bfloat16 *out_normed;
 };
 
-gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_t *cache_pos,
-                       int32_t batch, int32_t q_len, void *out, gattn_stream stream,
-                       const BlockArgs *blk)
+// The argument checks of a step (everything but the data pointers).
+gattn_status check_step(const gattn_layer *L, const gattn_kv *kv, int32_t batch, int32_t q_len)
 {
-    if (!L || !x || !kv || !cache_pos || !out)
-        return fail(GATTN_E_INVALID_ARG, "NULL argument");
     if (!L->weights_set)
         return fail(GATTN_E_STATE, "set_weights has not been called");
     if (kv->layer != L)
@@ -799,6 +804,19 @@ gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_
                     batch, c.max_batch, kv->desc.batch);
     if (q_len <= 0 || q_len > c.max_q_len)
         return fail(GATTN_E_INVALID_ARG, "q_len %d outside [1, %d]", q_len, c.max_q_len);
+    return GATTN_OK;
+}
+
+gattn_status step_impl(gattn_layer *L, const void *x, gattn_kv *kv, const int32_t *cache_pos,
+                       int32_t batch, int32_t q_len, void *out, gattn_stream stream,
+                       const BlockArgs *blk)
+{
+    if (!L || !x || !kv || !cache_pos || !out)
+        return fail(GATTN_E_INVALID_ARG, "NULL argument");
+    const gattn_status chk = check_step(L, kv, batch, q_len);
+    if (chk != GATTN_OK)
+        return chk;
+    const gattn_cfg &c = L->cfg;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int M = batch * q_len;
     // the q|k|v operand has 2M columns for fp32 x (exact hi + lo fp16 planes)
@@ -1063,6 +1081,30 @@ gattn_status gattn_layer_step(gattn_layer *L, const void *x, gattn_kv *kv, const
                               int32_t batch, int32_t q_len, void *out, gattn_stream stream)
 {
     return step_impl(L, x, kv, cache_pos, batch, q_len, out, stream, nullptr);
+}
+
+gattn_status gattn_layer_step_host(gattn_layer *L, const void *x_host, gattn_kv *kv,
+                                   const int32_t *cache_pos_host, int32_t batch, int32_t q_len,
+                                   void *out_host, gattn_stream stream)
+{
+    if (!L || !x_host || !kv || !cache_pos_host || !out_host)
+        return fail(GATTN_E_INVALID_ARG, "NULL argument");
+    const gattn_status chk = check_step(L, kv, batch, q_len);
+    if (chk != GATTN_OK)
+        return chk;
+    const gattn_cfg &c = L->cfg;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t elems = (size_t)batch * q_len * c.hidden;
+    CUDA_TRY(cudaMemcpyAsync(L->x_stage, x_host, elems * (c.x_dtype == GATTN_DTYPE_F32 ? 4 : 2),
+                             cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(L->pos_stage, cache_pos_host, (size_t)batch * sizeof(int32_t),
+                             cudaMemcpyHostToDevice, s));
+    const gattn_status st =
+        step_impl(L, L->x_stage, kv, L->pos_stage, batch, q_len, L->out_stage, stream, nullptr);
+    if (st != GATTN_OK)
+        return st;
+    CUDA_TRY(cudaMemcpyAsync(out_host, L->out_stage, elems * 2, cudaMemcpyDeviceToHost, s));
+    return GATTN_OK;
 }
 
 gattn_status gattn_layer_step_block(gattn_layer *L, const void *x, gattn_kv *kv,

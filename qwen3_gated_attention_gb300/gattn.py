@@ -35,6 +35,7 @@ EXPORTS = (
     "gattn_layer_step_block", "gattn_kv_register_turbo4v",
     "gattn_turbo4_codebook", "gattn_turbo4_quantize_device", "gattn_layer_set_mask",
     "gattn_kv_register_turbo4", "gattn_layer_step_kernels", "gattn_layer_set_test_wait",
+    "gattn_layer_step_host",
 )
 
 
@@ -136,6 +137,7 @@ def lib():
         L.gattn_layer_set_mask.argtypes = [p, C.POINTER(gattn_mask)]
         L.gattn_kv_register_turbo4.argtypes = [p, C.POINTER(gattn_kv_turbo4_desc), C.POINTER(p)]
         L.gattn_layer_set_test_wait.argtypes = [p, i64, i32]
+        L.gattn_layer_step_host.argtypes = [p, p, p, p, i32, i32, p, p]
         for name in ("gattn_cfg_validate", "gattn_layer_create", "gattn_layer_set_weights",
                      "gattn_kv_register", "gattn_layer_step", "gattn_layer_poll_status",
                      "gattn_layer_set_taps", "gattn_pack_affine_host", "gattn_unpack_codes_device",
@@ -144,7 +146,7 @@ def lib():
                      "gattn_layer_step_block", "gattn_kv_register_turbo4v",
                      "gattn_turbo4_codebook", "gattn_turbo4_quantize_device",
                      "gattn_layer_set_mask", "gattn_kv_register_turbo4",
-                     "gattn_layer_set_test_wait"):
+                     "gattn_layer_set_test_wait", "gattn_layer_step_host"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -261,6 +263,14 @@ def turbo4_quantize_device(v: int, rows: int, d: int, codes: int, scales: int,
 def layer_step(layer: int, x: int, kv: int, cache_pos: int, batch: int, q_len: int, out: int,
                stream: int = 0) -> None:
     _check(lib().gattn_layer_step(layer, x, kv, cache_pos, batch, q_len, out, stream))
+
+
+def layer_step_host(layer: int, x_host: int, kv: int, cache_pos_host: int, batch: int,
+                    q_len: int, out_host: int, stream: int = 0) -> None:
+    """gattn_layer_step from host buffers (x, cache_pos in; out back), enqueued
+    on the stream; out_host holds the result once the stream has reached it."""
+    _check(lib().gattn_layer_step_host(layer, x_host, kv, cache_pos_host, batch, q_len, out_host,
+                                       stream))
 
 
 def layer_poll_status(layer: int, stream: int = 0) -> None:
