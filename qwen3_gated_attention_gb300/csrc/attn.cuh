@@ -915,6 +915,104 @@ __global__ void __launch_bounds__(DB * 64) attn_merge_kernel(const AttnArgs a)
     }
 }
 
+// The merge for a bf16 V cache when the o_proj groups are at most 64 columns:
+// CTA (segment, row i, slice sl) merges columns 64 sl .. 64 sl + 63 of row i,
+// whole groups, so its group sums need no other CTA.  Column by column the
+// arithmetic of attn_merge_kernel (the same results bit for bit), on d / 64
+// times as many CTAs, each loading that fraction of the row's partials.
+template <int DB>
+__global__ void __launch_bounds__(64) attn_merge_slice_kernel(const AttnArgs a)
+{
+    constexpr int D = DB * 64;
+    __shared__ int ub[32], nc[32], cu_slot;
+    __shared__ long long pi[33], uo[33];
+    __shared__ float wsum[2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the o_proj launch may start streaming its weights at once
+    pdl_launch_dependents();
+    chunk_plan(a, a.attn_grid, ub, nc, pi, uo, &cu_slot);
+    const int sl = (int)(blockIdx.x % DB);
+    const long long rowid = blockIdx.x / DB;
+    const long long seg = rowid / a.merge_rows;
+    const int i = (int)(rowid % a.merge_rows);
+    const int rb = (int)(seg % a.nrb), kh = (int)((seg / a.nrb) % a.Hk);
+    const int b = (int)(seg / ((long long)a.nrb * a.Hk));
+    const int n = nc[b], nrows = a.rb_nh[rb] * a.R;
+    if (n <= 1 || i >= nrows)
+        return;
+    const int gqa = a.H / a.Hk;
+    const int h = kh * gqa + a.rb_h0[rb] + i / a.R, m = b * a.R + i % a.R;
+    const int col0 = sl * 64 + warp * 32 + lane;           // column within the head
+    const long long Ktot = (long long)a.H * D, sf = attn_slot_floats(D);
+    const long long kb = (long long)m * Ktot + (long long)h * D + col0;
+    const float *slots = a.ws + (pi[b] + ((long long)kh * a.nrb + rb) * n) * sf;
+    const float *col = slots + 2 * kAttnMaxRows + (long long)i * D + col0;
+    pdl_wait();                 // the chunk partials come from the attention launch
+    const float mj = lane < n ? __ldcg(slots + lane * sf + i) : -INFINITY;
+    const float lj = lane < n ? __ldcg(slots + lane * sf + kAttnMaxRows + i) : 0.f;
+    const float gt = __ldcg(a.gate + kb);
+    float v[kMaxChunks];
+#pragma unroll
+    for (int j = 0; j < kMaxChunks; ++j)
+        v[j] = j < n ? __ldcg(col + j * sf) : 0.f;
+    float M = mj;
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float f = mj == -INFINITY ? 0.f : exp2f(mj - M);
+    float L = f * lj;
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        L += __shfl_xor_sync(0xffffffffu, L, o);
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxChunks; ++j) {
+        const float fj = __shfl_sync(0xffffffffu, f, j);
+        if (j < n)
+            acc = fmaf(fj, v[j], acc);
+    }
+    const float o = acc * (L > 0.f ? 1.f / L : 0.f);
+    const int c = h * D + col0;
+    const __half q = __float2half_rn(o * (1.f / (1.f + __expf(-gt))));
+    a.x16[x16_offset(m, c, a.NT)] = q;
+    if (a.tap_attn)
+        a.tap_attn[kb] = o;
+    // group sums of the fp16 operand: groups of gs (32 or 64) columns, the
+    // slice's warps added in warp order
+    float t = __half2float(q);
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+        t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (lane == 0)
+        wsum[warp] = t;
+    __syncthreads();
+    const int gs = a.group_o, wpg = gs / 32, MP = 8 * a.NT;
+    if (threadIdx.x < 64 / gs) {
+        float g = 0.f;
+        for (int w = 0; w < wpg; ++w)
+            g += wsum[threadIdx.x * wpg + w];
+        const int c0 = h * D + sl * 64 + threadIdx.x * gs;
+        a.xsum[((long long)(c0 >> 7) * (kKU / gs) + ((c0 & 127) / gs)) * MP + m] = g;
+    }
+}
+
+template <int DB>
+static cudaError_t launch_attn_merge_slice_t(const AttnArgs &a, int segments, bool pdl,
+                                             cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(segments * a.merge_rows * DB);
+    cfg.blockDim = dim3(64);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_merge_slice_kernel<DB>, a);
+}
+
 template <int DB, int VQ>
 static cudaError_t launch_attn_merge_t(const AttnArgs &a, int segments, bool pdl, cudaStream_t s)
 {
