@@ -293,19 +293,24 @@ gattn_status gattn_layer_step(gattn_layer *layer, const void *x, gattn_kv *kv,
                               void *out, gattn_stream stream);
 
 /*
- * gattn_layer_step from host buffers: enqueues on `stream` the copy of x and
- * cache_pos into the layer's own device staging buffers, the step, and the
- * copy of its output rows into out_host, then returns (no host
- * synchronization: out_host holds the result once the stream has reached it).
+ * gattn_layer_step from host buffers: copies x and cache_pos into the layer's
+ * own device staging buffers, enqueues the step on `stream` after those
+ * copies, and the copy of its output rows into out_host after the step, then
+ * returns (no host synchronization: out_host holds the result once `stream`
+ * has reached it).
  *   x_host          (host) [batch][q_len][hidden], cfg.x_dtype
  *   cache_pos_host  (host) int32 [batch], as cache_pos of gattn_layer_step
  *   out_host        (host) bf16 [batch][q_len][hidden]
- * The host buffers are borrowed until the stream has passed the copies; pinned
+ * The input copies run on a stream of the layer's own, ordered before the
+ * step but not after earlier work on `stream`: x_host and cache_pos_host must
+ * hold the step's inputs when the call is made (not be written by work still
+ * pending on `stream`), and stay unchanged until the stream has passed the
+ * step.  out_host is written by a copy on `stream` after the step.  Pinned
  * (page-locked) memory makes the copies asynchronous.  The staging buffers
- * (allocated with the layer, for the largest step it admits) are shared by the
- * calls on one handle, like its scratch.  Errors: those of gattn_layer_step,
- * checked before anything is enqueued; GATTN_E_CUDA when a copy or a launch
- * fails.
+ * (two input slots used in turn, allocated with the layer for the largest
+ * step it admits) belong to the handle, like its scratch.  Errors: those of
+ * gattn_layer_step, checked before anything is enqueued; GATTN_E_CUDA when a
+ * copy or a launch fails.
  */
 gattn_status gattn_layer_step_host(gattn_layer *layer, const void *x_host, gattn_kv *kv,
                                    const int32_t *cache_pos_host, int32_t batch, int32_t q_len,

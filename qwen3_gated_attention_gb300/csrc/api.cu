@@ -232,9 +232,14 @@ struct gattn_layer {
     float *ss_part = nullptr;              // decoder-block post-norm: per-CTA sums of squares
     unsigned *post_ticket = nullptr;
     unsigned long long *slot_ctr = nullptr;   // attention CTAs started (work slots, attn.cuh)
-    // gattn_layer_step_host: device copies of the step's x, cache_pos and out
-    void *x_stage = nullptr, *out_stage = nullptr;
-    int32_t *pos_stage = nullptr;
+    // gattn_layer_step_host: device copies of the step's x and cache_pos (two
+    // slots, filled on copy_stream while the previous step runs) and of out
+    void *x_stage[2] = {nullptr, nullptr}, *out_stage = nullptr;
+    int32_t *pos_stage[2] = {nullptr, nullptr};
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t stage_in[2] = {nullptr, nullptr};     // a slot's copies have landed
+    cudaEvent_t stage_free[2] = {nullptr, nullptr};   // the step that read a slot is done
+    int stage_slot = 0;
     // Bf16KTurbo4V caches: decision tables (passed by value) and the bytes of
     // the 8 positive fp16 levels the attention dequantizes with
     TurboTables tq{};
@@ -437,10 +442,15 @@ gattn_status gattn_layer_create(const gattn_cfg *cfg, gattn_layer **out)
     TRY(cudaMalloc(&L->xsum_o, nku_o * (kKU / L->po.group) * MP * sizeof(float)));
     TRY(cudaMemset(L->xsum_o, 0, nku_o * (kKU / L->po.group) * MP * sizeof(float)));
     TRY(cudaMalloc(&L->qn, (size_t)L->M_max * L->Ko * 2));
-    TRY(cudaMalloc(&L->x_stage, (size_t)L->M_max * c.hidden *
-                                    (c.x_dtype == GATTN_DTYPE_F32 ? 4 : 2)));
+    for (int i = 0; i < 2; ++i) {
+        TRY(cudaMalloc(&L->x_stage[i], (size_t)L->M_max * c.hidden *
+                                           (c.x_dtype == GATTN_DTYPE_F32 ? 4 : 2)));
+        TRY(cudaMalloc(&L->pos_stage[i], (size_t)c.max_batch * sizeof(int32_t)));
+        TRY(cudaEventCreateWithFlags(&L->stage_in[i], cudaEventDisableTiming));
+        TRY(cudaEventCreateWithFlags(&L->stage_free[i], cudaEventDisableTiming));
+    }
     TRY(cudaMalloc(&L->out_stage, (size_t)L->M_max * c.hidden * 2));
-    TRY(cudaMalloc(&L->pos_stage, (size_t)c.max_batch * sizeof(int32_t)));
+    TRY(cudaStreamCreateWithFlags(&L->copy_stream, cudaStreamNonBlocking));
     TRY(cudaMalloc(&L->gate, (size_t)L->M_max * L->Ko * sizeof(float)));
     // attention segments: batch x KV heads x row blocks (at most gqa row blocks)
     // attention scratch: chunk partials and completion counters for the largest
@@ -517,10 +527,19 @@ void gattn_layer_destroy(gattn_layer *L)
                     L->qn,     L->gate,      L->ws_attn, L->status,  L->inv_freq, L->inv_freq2,
                     L->q_norm, L->k_norm,
                     L->ss_part, L->post_ticket, L->slot_ctr,
-                    L->x_stage, L->out_stage, L->pos_stage};
+                    L->x_stage[0], L->x_stage[1], L->out_stage, L->pos_stage[0],
+                    L->pos_stage[1]};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
+    for (int i = 0; i < 2; ++i) {
+        if (L->stage_in[i])
+            cudaEventDestroy(L->stage_in[i]);
+        if (L->stage_free[i])
+            cudaEventDestroy(L->stage_free[i]);
+    }
+    if (L->copy_stream)
+        cudaStreamDestroy(L->copy_stream);
     delete L;
 }
 
@@ -1095,15 +1114,25 @@ gattn_status gattn_layer_step_host(gattn_layer *L, const void *x_host, gattn_kv 
     const gattn_cfg &c = L->cfg;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t elems = (size_t)batch * q_len * c.hidden;
-    CUDA_TRY(cudaMemcpyAsync(L->x_stage, x_host, elems * (c.x_dtype == GATTN_DTYPE_F32 ? 4 : 2),
-                             cudaMemcpyHostToDevice, s));
-    CUDA_TRY(cudaMemcpyAsync(L->pos_stage, cache_pos_host, (size_t)batch * sizeof(int32_t),
-                             cudaMemcpyHostToDevice, s));
-    const gattn_status st =
-        step_impl(L, L->x_stage, kv, L->pos_stage, batch, q_len, L->out_stage, stream, nullptr);
+    // the inputs go to the slot the step before last read, on the layer's copy
+    // stream once that step is done with it, so they land while the previous
+    // step still runs; the step waits for them, out comes back on `stream`
+    const int sl = L->stage_slot;
+    CUDA_TRY(cudaStreamWaitEvent(L->copy_stream, L->stage_free[sl], 0));
+    CUDA_TRY(cudaMemcpyAsync(L->x_stage[sl], x_host,
+                             elems * (c.x_dtype == GATTN_DTYPE_F32 ? 4 : 2),
+                             cudaMemcpyHostToDevice, L->copy_stream));
+    CUDA_TRY(cudaMemcpyAsync(L->pos_stage[sl], cache_pos_host, (size_t)batch * sizeof(int32_t),
+                             cudaMemcpyHostToDevice, L->copy_stream));
+    CUDA_TRY(cudaEventRecord(L->stage_in[sl], L->copy_stream));
+    CUDA_TRY(cudaStreamWaitEvent(s, L->stage_in[sl], 0));
+    const gattn_status st = step_impl(L, L->x_stage[sl], kv, L->pos_stage[sl], batch, q_len,
+                                      L->out_stage, stream, nullptr);
     if (st != GATTN_OK)
         return st;
+    CUDA_TRY(cudaEventRecord(L->stage_free[sl], s));
     CUDA_TRY(cudaMemcpyAsync(out_host, L->out_stage, elems * 2, cudaMemcpyDeviceToHost, s));
+    L->stage_slot = sl ^ 1;
     return GATTN_OK;
 }
 
