@@ -468,7 +468,7 @@ def measure_workload(spec, args, dev, world, dist, l2, full=True):
         oh = torch.empty(outs[0].shape, dtype=torch.bfloat16).pin_memory()
         xdev = torch.empty_like(xd)
         pdev = torch.empty_like(pd)
-        n_e2e = min(K, args.e2e_steps)
+        n_e2e = max(1, args.e2e_steps)     # consecutive steps, independent of K
         h2d = xh.numel() * xh.element_size() + ph.numel() * ph.element_size()
         d2h = oh.numel() * oh.element_size()
         torch.cuda.synchronize(dev)
@@ -583,7 +583,8 @@ def main():
                     help="replay the graph for at least this long (seconds) in the timed region")
     ap.add_argument("--no-per-workload", dest="per_workload", action="store_false",
                     help="time only the selected workload (no per_workload entries)")
-    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--e2e-steps", type=int, default=200,
+                    help="consecutive steps of the end-to-end leg")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-head-chunk", action="store_true")
